@@ -1,0 +1,445 @@
+"""Pins of the fp64 CPU oracle to facts fixed by the pages and by mathematics.
+
+Each test checks the oracle against something other than itself: a closed form,
+an invariant, a hand-worked case, a brute-force scalar loop on a tiny input, or a
+number printed on one of the pages (tests/golden/page_figures.json).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_figures.json")
+rng = np.random.default_rng(12345)
+
+
+def bf16_round(x):
+    """Round float64 values to bf16 (RNE) so test inputs are representable."""
+    f = np.asarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return O.bf16_bits_to_f64(u.astype(np.uint16))
+
+
+# ----------------------------------------------------------------------------- bf16
+
+def test_bf16_widening_known_patterns():
+    bits = np.array([0x3F80, 0xC000, 0x0000, 0x8000, 0x7F80, 0x0001, 0x3FC0, 0x4049], np.uint16)
+    v = O.bf16_bits_to_f64(bits)
+    assert v[0] == 1.0 and v[1] == -2.0 and v[2] == 0.0
+    assert math.copysign(1.0, v[3]) == -1.0 and v[3] == 0.0
+    assert math.isinf(v[4]) and v[4] > 0
+    assert v[5] == 2.0 ** -133          # smallest bf16 subnormal
+    assert v[6] == 1.5
+    assert v[7] == 3.140625
+
+
+# ----------------------------------------------------------------------------- LSE
+
+def test_lse_two_key_closed_form():
+    # x = [q.k0, q.k1] / sqrt(4) = [1, 0]  ->  LSE = ln(e + 1); a 1/d scale would give 0.5.
+    q = np.zeros((1, 1, 1, 4)); q[0, 0, 0, 0] = 2.0
+    k = np.zeros((1, 1, 2, 4)); k[0, 0, 0, 0] = 1.0
+    out = O.lse(q, k, None)
+    assert abs(out[0, 0, 0] - math.log(math.e + 1.0)) < 1e-15
+
+
+def test_lse_zero_queries_count_visible_keys():
+    # q = 0: every visible logit is 0, so LSE_j = ln(#visible) = ln(off + j + 1).
+    L, Hq, Hkv, d, T, nt, nq = 2, 4, 2, 8, 7, 5, 4
+    q = np.zeros((L, Hq, nq, d))
+    kc = rng.normal(size=(L, Hkv, T, d)); kt = rng.normal(size=(L, Hkv, nt, d))
+    out = O.lse(q, kc, kt)
+    off = T + nt - nq
+    want = np.log(off + np.arange(nq) + 1.0)
+    assert np.allclose(out, np.broadcast_to(want, out.shape), atol=1e-14, rtol=0)
+
+
+def test_lse_first_query_sees_one_key():
+    # Self-attention (n_q == n_k): query 0 sees key 0 only, so LSE_0 = q_0.k_0/sqrt(d).
+    d = 16
+    q = rng.normal(size=(1, 1, 3, d)); k = rng.normal(size=(1, 1, 3, d))
+    out = O.lse(q, k, None)
+    assert abs(out[0, 0, 0] - float(q[0, 0, 0] @ k[0, 0, 0]) / 4.0) < 1e-13
+
+
+def test_lse_rows_sum_to_one_bruteforce():
+    # Sum over visible keys of exp(x_ji - LSE_j) with scalar loops equals 1.
+    L, Hq, Hkv, d, T, nt, nq = 1, 2, 1, 8, 6, 4, 5
+    q = rng.normal(size=(L, Hq, nq, d)) * 2
+    kc = rng.normal(size=(L, Hkv, T, d)); kt = rng.normal(size=(L, Hkv, nt, d))
+    out = O.lse(q, kc, kt)
+    keys = np.concatenate([kc, kt], 2)[0, 0]
+    off = T + nt - nq
+    for h in range(Hq):
+        for j in range(nq):
+            s = 0.0
+            for i in range(off + j + 1):
+                dot = sum(q[0, h, j, c] * keys[i, c] for c in range(d))
+                s += math.exp(dot / math.sqrt(d) - out[0, h, j])
+            assert abs(s - 1.0) < 1e-12
+
+
+def test_lse_gqa_group_mapping():
+    # KV head 1 has all-zero keys: query heads 2 and 3 (group of KV head 1 under
+    # contiguous grouping) get ln(#visible); heads 0 and 1 do not.
+    L, Hq, Hkv, d, T, nq = 1, 4, 2, 8, 6, 6
+    q = rng.normal(size=(L, Hq, nq, d)) * 3
+    k = rng.normal(size=(L, Hkv, T, d)) * 3
+    k[:, 1] = 0.0
+    out = O.lse(q, k, None)
+    want = np.log(np.arange(nq) + 1.0)
+    assert np.allclose(out[0, 2], want) and np.allclose(out[0, 3], want)
+    assert not np.allclose(out[0, 0], want) and not np.allclose(out[0, 1], want)
+
+
+def test_lse_large_logits_stable():
+    # All keys equal: LSE = c + ln(#visible) even when c is huge.
+    d = 4
+    q = np.full((1, 1, 3, d), 40.0); k = np.full((1, 1, 5, d), 30.0)
+    out = O.lse(q, k, None)
+    c = 40.0 * 30.0 * d / 2.0
+    assert np.allclose(out[0, 0], c + np.log(np.arange(3) + 3.0), rtol=1e-15, atol=1e-9)
+
+
+# ----------------------------------------------------------------------------- KVzip / KVzip+
+
+def test_kvzip_zero_queries_closed_form():
+    # q = 0: a_ji = 1/(off+j+1) for every visible key; the max over j is at j = 0.
+    L, Hq, Hkv, d, T, nt, nq = 1, 4, 2, 8, 9, 6, 5
+    q = np.zeros((L, Hq, nq, d))
+    kc = rng.normal(size=(L, Hkv, T, d)); kt = rng.normal(size=(L, Hkv, nt, d))
+    s = O.kvzip_score(q, kc, kt)
+    off = T + nt - nq
+    assert np.allclose(s, -math.log(off + 1.0), atol=1e-14)
+
+
+def test_kvzip_plus_factors_closed_form():
+    # q = 0 with varying ||W_O v_i|| and ||h_j||:
+    # s+_i = vn_i * max_j 1 / ((off + j + 1) * ||h_j||)   (a product, not a ratio inverted).
+    L, Hq, Hkv, d, T, nt, nq, Dh = 1, 2, 1, 4, 5, 3, 3, 6
+    q = np.zeros((L, Hq, nq, d))
+    kc = rng.normal(size=(L, Hkv, T, d)); kt = rng.normal(size=(L, Hkv, nt, d))
+    vn = rng.uniform(0.5, 3.0, size=(L, Hq, T))
+    h = rng.normal(size=(L, nq, Dh)) * rng.uniform(0.2, 5.0, size=(1, nq, 1))
+    s = O.kvzip_score(q, kc, kt, vnorm=vn, h=h)
+    off = T + nt - nq
+    hn = [math.sqrt(sum(x * x for x in h[0, j])) for j in range(nq)]
+    best_j = max(1.0 / ((off + j + 1) * hn[j]) for j in range(nq))
+    for i in range(T):
+        want = math.log(max(vn[0, 0, i], vn[0, 1, i]) * best_j)
+        assert abs(s[0, 0, i] - want) < 1e-13
+
+
+def test_kvzip_one_hot_copy_orthogonal_keys():
+    # Orthonormal basis keys; query j of head h points at key pi_h(j) with logit c.
+    # Visible count n_j = off + j + 1; the pointed key gets e^c/(e^c + n_j - 1), the
+    # others 1/(e^c + n_j - 1).  Score = max over j and over the group's heads.
+    d = 16; T = 6; nt = 4; nq = 3; Hq = 2
+    keys = np.eye(d)[: T + nt]
+    kc = keys[:T][None, None]; kt = keys[T:][None, None]
+    beta = 8.0
+    c = beta / math.sqrt(d)
+    pis = [[0, 3, 3], [5, 1, 0]]
+    q = np.zeros((1, Hq, nq, d))
+    for h in range(Hq):
+        for j in range(nq):
+            q[0, h, j, pis[h][j]] = beta
+    s = O.kvzip_score(q, kc, kt, log=False)
+    off = T + nt - nq
+    for i in range(T):
+        best = 0.0
+        for h in range(Hq):
+            for j in range(nq):
+                n = off + j + 1
+                a = (math.exp(c) if pis[h][j] == i else 1.0) / (math.exp(c) + n - 1)
+                best = max(best, a)
+        assert abs(s[0, 0, i] - best) < 1e-14
+    assert s.max() < 1.0 and s.min() > 0.0
+
+
+def test_kvzip_score_in_unit_interval_and_attains_max():
+    L, Hq, Hkv, d, T, nt, nq = 2, 4, 2, 16, 20, 9, 7
+    q = rng.normal(size=(L, Hq, nq, d)) * 2
+    kc = rng.normal(size=(L, Hkv, T, d)) * 2; kt = rng.normal(size=(L, Hkv, nt, d))
+    s = O.kvzip_score(q, kc, kt, log=False)
+    assert (s > 0).all() and (s <= 1).all()
+    # brute force on one (layer, kv head): scalar-loop softmax rows, max over j and heads
+    keys = np.concatenate([kc, kt], 2)
+    off = T + nt - nq
+    l, hk = 1, 1
+    for i in range(0, T, 3):
+        best = 0.0
+        for hq in (2, 3):
+            for j in range(nq):
+                xs = [float(q[l, hq, j] @ keys[l, hk, t]) / 4.0 for t in range(off + j + 1)]
+                m = max(xs)
+                den = sum(math.exp(x - m) for x in xs)
+                best = max(best, math.exp(xs[i] - m) / den)
+        assert abs(s[l, hk, i] - best) < 1e-14
+
+
+def test_kvzip_chunked_is_max_over_chunks():
+    L, Hq, Hkv, d, T = 1, 2, 1, 8, 10
+    kc = rng.normal(size=(L, Hkv, T, d))
+    qs = [rng.normal(size=(L, Hq, 4, d)) for _ in range(3)]
+    tails = [rng.normal(size=(L, Hkv, n, d)) for n in (6, 9, 9)]
+    sc = O.kvzip_score_chunked(qs, kc, tails)
+    per = np.stack([O.kvzip_score(qs[c], kc, tails[c]) for c in range(3)])
+    assert np.array_equal(sc, per.max(axis=0))
+
+
+# ----------------------------------------------------------------------------- future mass
+
+def test_future_mass_zero_queries_harmonic():
+    # q = 0, causal: a_ji = 1/(j+1); f_i = g * sum_{j=i+w}^{n-1} 1/(j+1).
+    L, Hq, Hkv, d, n, w = 1, 4, 2, 8, 12, 3
+    q = np.zeros((L, Hq, n, d)); k = rng.normal(size=(L, Hkv, n, d))
+    f = O.future_attention_mass(q, k, w)
+    g = Hq // Hkv
+    for i in range(n):
+        want = g * sum(1.0 / (j + 1) for j in range(i + w, n))
+        assert abs(f[0, 0, i] - want) < 1e-13 and abs(f[0, 1, i] - want) < 1e-13
+
+
+def test_future_mass_w0_rows_sum_to_one():
+    L, Hq, Hkv, d, n = 2, 4, 2, 16, 17
+    q = rng.normal(size=(L, Hq, n, d)) * 2; k = rng.normal(size=(L, Hkv, n, d)) * 2
+    f = O.future_attention_mass(q, k, 0, row_block=5)
+    g = Hq // Hkv
+    assert np.allclose(f.sum(axis=-1), g * n, rtol=1e-13)
+
+
+def test_future_mass_window_limits():
+    L, Hq, Hkv, d, n = 1, 2, 1, 8, 9
+    q = rng.normal(size=(L, Hq, n, d)); k = rng.normal(size=(L, Hkv, n, d))
+    assert np.all(O.future_attention_mass(q, k, n) == 0.0)
+    assert np.all(O.future_attention_mass(q, k, n + 5) == 0.0)
+    f2 = O.future_attention_mass(q, k, 2)
+    assert np.all(f2[..., n - 2:] == 0.0) and np.all(f2[..., : n - 2] > 0.0)
+
+
+def test_future_mass_one_hot_orthogonal():
+    # Orthonormal keys, query j points at key p_j <= j with logit c: row j puts
+    # e^c/(e^c + j) on p_j and 1/(e^c + j) on every other key i <= j.
+    n, d, w = 7, 8, 2
+    k = np.eye(d)[:n][None, None]
+    beta = 6.0; c = beta / math.sqrt(d)
+    p = [0, 0, 1, 0, 2, 4, 4]
+    q = np.zeros((1, 1, n, d))
+    for j in range(n):
+        q[0, 0, j, p[j]] = beta
+    f = O.future_attention_mass(q, k, w)
+    for i in range(n):
+        want = 0.0
+        for j in range(i + w, n):
+            want += (math.exp(c) if p[j] == i else 1.0) / (math.exp(c) + j)
+        assert abs(f[0, 0, i] - want) < 1e-14
+
+
+# ----------------------------------------------------------------------------- norms
+
+def test_value_norm_orthonormal_columns_and_head_slices():
+    # W_O^{(h)} = c_h * (orthonormal columns)  =>  ||W_O^{(h)} v|| = c_h ||v||, with
+    # query head h reading KV head h // g.
+    L, Hkv, Hq, T, d, Dh = 1, 2, 4, 5, 4, 12
+    v = rng.normal(size=(L, Hkv, T, d)) * np.array([1.0, 3.0])[None, :, None, None]
+    w_o = np.zeros((L, Dh, Hq * d))
+    cs = [0.5, 1.0, 2.0, 4.0]
+    for h in range(Hq):
+        Qm, _ = np.linalg.qr(rng.normal(size=(Dh, d)))
+        w_o[0, :, h * d:(h + 1) * d] = cs[h] * Qm
+    vn = O.value_norm(v, w_o, Hq)
+    for h in range(Hq):
+        for i in range(T):
+            want = cs[h] * math.sqrt(sum(x * x for x in v[0, h // 2, i]))
+            assert abs(vn[0, h, i] - want) < 1e-12 * max(1.0, want)
+
+
+def test_value_norm_gram_identity():
+    # ||W v||^2 = v^T (W^T W) v  -- an independent route through the Gram matrix.
+    L, Hkv, Hq, T, d, Dh = 2, 1, 3, 6, 8, 20
+    v = rng.normal(size=(L, Hkv, T, d)); w_o = rng.normal(size=(L, Dh, Hq * d))
+    vn = O.value_norm(v, w_o, Hq)
+    for l in range(L):
+        for h in range(Hq):
+            Wh = w_o[l][:, h * d:(h + 1) * d]
+            G = Wh.T @ Wh
+            for i in range(T):
+                quad = float(v[l, 0, i] @ G @ v[l, 0, i])
+                assert abs(vn[l, h, i] ** 2 - quad) < 1e-10 * quad
+
+
+def test_hidden_norm_pythagoras():
+    h = np.array([[[3.0, 4.0, 0.0], [5.0, 12.0, 0.0], [0.0, 0.0, 0.0]]])
+    assert np.array_equal(O.hidden_norm(h), np.array([[5.0, 13.0, 0.0]]))
+
+
+# ----------------------------------------------------------------------------- surrogate
+
+def test_surrogate_zero_weight_gives_bias_head_major():
+    L, T, Dh, H = 2, 5, 6, 3
+    h = rng.normal(size=(L, T, Dh)); W = np.zeros((L, Dh, H)); b = rng.normal(size=(L, H))
+    z = O.linear_surrogate(h, W, b)
+    assert z.shape == (L, H, T)
+    assert np.array_equal(z, np.broadcast_to(b[:, :, None], (L, H, T)))
+
+
+def test_surrogate_one_hot_weight_selects_channel():
+    L, T, Dh, H = 1, 4, 7, 3
+    h = rng.normal(size=(L, T, Dh)); b = np.array([[1.0, -2.0, 0.5]])
+    W = np.zeros((L, Dh, H)); chan = [6, 0, 3]
+    for hh in range(H):
+        W[0, chan[hh], hh] = 1.0
+    z = O.linear_surrogate(h, W, b)
+    for hh in range(H):
+        for t in range(T):
+            assert z[0, hh, t] == h[0, t, chan[hh]] + b[0, hh]
+
+
+def test_surrogate_small_integers_exact():
+    L, T, Dh, H = 1, 6, 9, 4
+    hi = rng.integers(-8, 9, size=(L, T, Dh)); Wi = rng.integers(-8, 9, size=(L, Dh, H))
+    bi = rng.integers(-50, 50, size=(L, H))
+    z = O.linear_surrogate(hi.astype(float), Wi.astype(float), bi.astype(float))
+    for hh in range(H):
+        for t in range(T):
+            want = sum(int(hi[0, t, c]) * int(Wi[0, c, hh]) for c in range(Dh)) + int(bi[0, hh])
+            assert z[0, hh, t] == want
+
+
+# ----------------------------------------------------------------------------- pruning
+
+def test_threshold_hand_example():
+    s = np.array([-1.0, 0.5, np.nan, 0.49, -10.0, np.nan])
+    mask, keep = O.prune_threshold(s, 0.5, 2)
+    assert mask.tolist() == [0, 1, 0, 0, 1, 1] and int(keep) == 3
+
+
+def test_threshold_limits_and_monotone():
+    s = rng.normal(size=(3, 40)); w = 5
+    m_lo, _ = O.prune_threshold(s, -np.inf, w)
+    m_hi, k_hi = O.prune_threshold(s, np.inf, w)
+    assert m_lo.all()
+    assert (k_hi == w).all() and m_hi[:, -w:].all()
+    prev = None
+    for tau in np.linspace(-3, 3, 13):
+        _, k = O.prune_threshold(s, tau, w)
+        if prev is not None:
+            assert (k <= prev).all()
+        prev = k
+
+
+def test_topk_hand_example_ties_and_nan():
+    s = np.array([5.0, 1.0, 5.0, np.nan, 3.0, 5.0, 0.0, 0.0])
+    want = {3: [1, 0, 1, 0, 0, 1, 1, 1], 4: [1, 0, 1, 0, 1, 1, 1, 1],
+            5: [1, 1, 1, 0, 1, 1, 1, 1], 6: [1, 1, 1, 1, 1, 1, 1, 1],
+            2: [1, 0, 1, 0, 0, 0, 1, 1], 0: [0, 0, 0, 0, 0, 0, 1, 1]}
+    for k, m in want.items():
+        mask, keep = O.prune_topk(s, k, 2)
+        assert mask.tolist() == m, k
+        assert int(keep) == sum(m)
+
+
+def test_topk_budget_and_limits():
+    s = rng.normal(size=(2, 3, 50))
+    for k in (0, 1, 10, 44, 45, 46, 60):
+        for w in (0, 5, 50, 70):
+            mask, keep = O.prune_topk(s, k, w)
+            assert (keep == min(50, k + min(w, 50))).all()
+            assert mask[..., 50 - min(w, 50):].all()
+    # all-equal scores: the earliest positions win
+    mask, _ = O.prune_topk(np.zeros(10), 3, 2)
+    assert mask.tolist() == [1, 1, 1, 0, 0, 0, 0, 0, 1, 1]
+
+
+def test_topk_selects_largest():
+    s = rng.permutation(30).astype(float)
+    mask, _ = O.prune_topk(s, 7, 0)
+    assert sorted(np.nonzero(mask)[0].tolist()) == sorted(np.argsort(-s)[:7].tolist())
+
+
+# ----------------------------------------------------------------------------- compaction
+
+def test_compaction_hand_example():
+    k = np.zeros((1, 2, 5, 1), dtype=np.int64)
+    for h in range(2):
+        for t in range(5):
+            k[0, h, t, 0] = t + 10 * h + 1
+    v = -k
+    mask = np.array([[[1, 0, 1, 1, 0], [0, 1, 0, 0, 0]]], dtype=np.uint8)
+    kp, vp, bt, sl, tot = O.compact_paged(k, v, mask, page_size=2)
+    assert tot == 3
+    assert kp[:, :, 0].tolist() == [[1, 3], [4, 0], [12, 0]]
+    assert vp[:, :, 0].tolist() == [[-1, -3], [-4, 0], [-12, 0]]
+    assert bt.tolist() == [[[0, 1, -1], [2, -1, -1]]]
+    assert sl.tolist() == [[3, 1]]
+
+
+def test_compaction_all_kept_reproduces_input():
+    L, H, T, d, ps = 2, 3, 37, 4, 16
+    k = rng.normal(size=(L, H, T, d)); v = rng.normal(size=(L, H, T, d))
+    kp, vp, bt, sl, tot = O.compact_paged(k, v, np.ones((L, H, T), np.uint8), ps)
+    assert tot == L * H * 3 and (sl == T).all()
+    for l in range(L):
+        for h in range(H):
+            rows = np.concatenate([kp[p] for p in bt[l, h] if p >= 0])
+            assert np.array_equal(rows[:T], k[l, h]) and not rows[T:].any()
+
+
+def test_compaction_counts_match_mask():
+    L, H, T, d = 2, 2, 50, 2
+    k = rng.normal(size=(L, H, T, d)); v = rng.normal(size=(L, H, T, d))
+    mask = (rng.random((L, H, T)) < 0.4).astype(np.uint8)
+    kp, vp, bt, sl, tot = O.compact_paged(k, v, mask, 16)
+    assert int(sl.sum()) == int(mask.sum())
+    assert tot == int(sum(-(-int(n) // 16) for n in sl.ravel()))
+
+
+# ----------------------------------------------------------------------------- page numbers
+
+def _golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+def test_kv_memory_formula_reproduces_pages():
+    g = _golden()["kv_memory"]
+    a = g[0]
+    assert O.kv_cache_bytes(a["L"], a["T"], a["H_kv"], a["d"], a["bytes_per_elem"]) == a["bytes"]
+    b = g[1]
+    gb = O.kv_cache_bytes(b["L"], b["T"], b["H_kv"], b["d"], b["bytes_per_elem"]) / 1e9
+    assert math.floor(gb) == b["gigabytes_printed"]
+
+
+def test_overhead_formulas_reproduce_appendix_b():
+    for r in _golden()["overhead_percent"]:
+        C = O.layer_linear_flops(r["D_h"], r["H_q"], r["H_kv"], r["D"], r["D_int"])
+        mlp = 100 * O.kvzap_mlp_flops(r["D_h"], r["H_kv"]) / C
+        lin = 100 * O.kvzap_linear_flops(r["D_h"], r["H_kv"]) / C
+        assert round(mlp, 2) == r["mlp"], (r["cite"], mlp)
+        assert round(lin, 2) == r["linear"], (r["cite"], lin)
+
+
+def test_surrogate_param_counts_match_table():
+    for r in _golden()["surrogate_params_millions"]:
+        f = O.kvzap_mlp_params if r["kind"] == "mlp" else O.kvzap_linear_params
+        m = f(r["L"], r["D_h"], r["H_kv"]) / 1e6
+        tol = 0.5 if r["millions"] >= 10 else 0.06   # the table rounds to the shown digit
+        assert abs(m - r["millions"]) < tol, (r, m)
+
+
+def test_compression_factor_table2():
+    for r in _golden()["compression"]:
+        f = O.compression_factor(r["ratio"])
+        assert math.floor(f * 10) / 10 == r["factor_printed"]
+
+
+def test_quantile_lower_nearest_rank():
+    assert O.quantile_lower([3, 1, 2, 4], 0.25) == 1
+    assert O.quantile_lower([3, 1, 2, 4], 0.5) == 2
+    assert O.quantile_lower(np.arange(101), 0.25) == 25
