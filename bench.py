@@ -1,0 +1,502 @@
+#!/usr/bin/env python
+"""Benchmark of the KV-cache scoring -> pruning -> compaction path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2] [--impl kvs|reference]
+
+One step = one pass of the whole path over one batch of synthetic input (all layers):
+  c2 (default; Qwen2.5-1.5B-shaped KVzip+): vnorm -> lse -> score_max -> top-k at
+     r = 0.3 / 0.5 / 0.7 -> paged compaction of each
+  c1: lse -> score_max -> top-k 25% + w=16 -> compaction
+  c3: vnorm -> 16 x (lse -> score_max) -> per-layer threshold (25th percentile, calibrated
+      once before timing) with w=128 -> compaction
+  c4: lse (causal) -> future mass (w=128) -> top-k 25% / 12.5% + window -> compaction
+  c5: surrogate (+ fused threshold tau=-5, w=128) -> compaction
+Metric: context KV tokens scored+pruned per second per layer (all heads) = T * L / step time.
+
+Timing: inputs resident in HBM; W warm-up steps; K timed steps, each bracketed by CUDA
+events on the launching stream, with a 512 MB buffer written between steps (outside the
+events) to flush L2; barrier + synchronize on both sides; max over ranks.  SM clocks and
+throttle reasons are sampled with nvidia-smi during the timed steps.  Each library entry
+point is then timed on its own (same rules) for the roofline of the dominant kernel.
+`e2e` repeats the step through the same public calls with the inputs in pinned host
+memory: host->device copies of every input and a device->host read of the results are
+inside the timed region.  `cpu_baseline` times the fp64 CPU oracle on a bounded sample.
+
+`--impl reference` times the CPU oracle itself (the only reference implementation: the
+pages ship no code) on the machine's host cores, each step a bounded sample of the workload.
+Under torchrun (N > 1) every rank runs its own replica of the workload (weak scaling; the
+path shards by independent problems and needs no data exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "context KV tokens scored+pruned/s per layer (all heads); % of tensor/HBM roofline"
+UNIT = "tokens/s/layer"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="c2", choices=["c1", "c2", "c3", "c4", "c5"])
+    ap.add_argument("--impl", default="kvs", choices=["kvs", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stage-reps", type=int, default=None)
+    return ap.parse_args()
+
+
+DEFAULT_STEPS = {"c1": 200, "c2": 200, "c3": 5, "c4": 10, "c5": 20}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+# ----------------------------------------------------------------------------- work model
+
+def algorithmic_work(wl, p):
+    """Algorithmic flops / bytes of one call of each library entry point of a step,
+    summed over the step (see the roofline section of the design doc)."""
+    d, L = wl.d, p.L
+    out = {}
+    if wl.kind in ("kvzip", "kvzip_plus", "kvzip_plus_chunked"):
+        chunks = wl.n_chunks if wl.kind == "kvzip_plus_chunked" else 1
+        nq = wl.n_rep
+        el1 = 0
+        for c in range(chunks):
+            nk = wl.T + wl.tail_len(c)
+            off = nk - nq
+            el1 += L * wl.H_q * (nq * off + nq * (nq + 1) // 2)
+        el2 = L * wl.H_q * nq * wl.T * chunks
+        out["kvs_lse"] = ("tensor", 2 * d * el1, "flop")
+        out["kvs_score_max"] = ("tensor", 2 * d * el2, "flop")
+        if wl.kind != "kvzip":
+            out["kvs_vnorm"] = ("tensor", 2 * L * wl.H_q * d * d * (wl.D_h + wl.T), "flop")
+    if wl.kind == "future":
+        n, w = wl.T, wl.w
+        el1 = L * wl.H_q * n * (n + 1) // 2
+        m = max(0, n - w)
+        el2 = L * wl.H_q * m * (m + 1) // 2
+        out["kvs_lse"] = ("tensor", 2 * d * el1, "flop")
+        out["kvs_score_future_sum"] = ("tensor", 2 * d * el2, "flop")
+    if wl.kind == "kvzap":
+        rows = L * wl.H_kv
+        out["kvs_surrogate"] = ("hbm", L * wl.T * wl.D_h * 2 + L * wl.D_h * wl.H_kv * 2
+                                + rows * wl.T * (4 + 1), "byte")
+    return out
+
+
+def compaction_bytes(p, wl):
+    pages = p.pages if isinstance(p.pages, list) else [p.pages]
+    rows = p.L * wl.H_kv
+    kept = sum(int(pg.seq_lens.sum().item()) for pg in pages)
+    pad = sum(int(((-pg.seq_lens) % wl.page_size).sum().item()) for pg in pages)
+    return (kept * wl.d * 2 * 2 * 2 + pad * wl.d * 2 * 2
+            + len(pages) * rows * (wl.T + pages[0].max_pages * 4))
+
+
+def prune_bytes(p, wl):
+    n = len(p.masks) if hasattr(p, "masks") else 1
+    return n * p.L * wl.H_kv * wl.T * (4 + 1)
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.error = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu_id)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except Exception as e:  # no nvidia-smi
+            self.error = str(e)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if self.error or not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "note": self.error or "no samples"}
+        rows = [l.split(", ") for t, l in self.lines if t0 - 0.15 <= t <= t1 + 0.15]
+        if not rows:
+            rows = [self.lines[-1][1].split(", ")]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if len(r) > 5 + i and r[5 + i].strip().lower() == "active"})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def build_pipeline(wl, device):
+    from kv_cache_eviction_lse_gb300 import pipeline, workloads as W
+    x = W.generate(wl, device=device)
+    p = pipeline.make_pipeline(wl, x)
+    if wl.kind == "kvzip_plus_chunked":
+        # calibrate the per-layer threshold once (25th percentile of the non-window
+        # scores of each layer), then keep it fixed for the timed steps
+        import torch
+        p.score_step()
+        T = wl.T - wl.w
+        p.tau = [float(torch.kthvalue(p.score[l, :, :T].flatten().float(),
+                                      max(1, int(wl.tau_quantile * (wl.H_kv * T - 1)) + 1)).values)
+                 for l in range(p.L)]
+    return x, p
+
+
+def run_gpu(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+    from kv_cache_eviction_lse_gb300 import build as B
+    B.build()
+    from kv_cache_eviction_lse_gb300 import capi as C
+    from kv_cache_eviction_lse_gb300 import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    wl = W.WORKLOADS[args.workload]
+    K = args.steps or DEFAULT_STEPS[args.workload]
+    Wm = max(3, args.warmup)
+    x, p = build_pipeline(wl, dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    for _ in range(Wm):
+        p.step()
+    torch.cuda.synchronize()
+
+    # ---------------------------------------------------------------- timed steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else local
+    n0 = C.kvs_launch_count()
+    with ClockSampler(gpu_id) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        for i in range(K):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            p.step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        barrier()
+    launches = (C.kvs_launch_count() - n0) // K
+    ms = sum(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        tmax = torch.tensor([ms], device=dev)
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+        ms = float(tmax.item())
+    ms_step = ms / K
+    value = world * wl.T * p.L / (ms_step / 1e3)
+
+    # ---------------------------------------------------------------- per entry point
+    reps = args.stage_reps or max(3, min(50, K))
+    work = algorithmic_work(wl, p)
+    stage_ms = {}
+    for name, fn in p.stages():
+        e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(reps)]
+        for i in range(reps):
+            flush.fill_(float(i))
+            e[i][0].record(stream)
+            fn()
+            e[i][1].record(stream)
+        torch.cuda.synchronize()
+        stage_ms[name] = sum(a.elapsed_time(b) for a, b in e) / reps
+    p.step()  # leave consistent outputs
+    torch.cuda.synchronize()
+    work["kvs_compact_paged"] = ("hbm", compaction_bytes(p, wl), "byte")
+    if "kvs_prune_mask" in stage_ms:
+        work["kvs_prune_mask"] = ("hbm", prune_bytes(p, wl), "byte")
+
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+        src = "measured"
+    except Exception:
+        src = "fallback"
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    tc_peak = peaks.get("bf16_tflops", 1900.0)
+    kernels = {}
+    for name, t in stage_ms.items():
+        bound, amount, unit = work.get(name, ("hbm", None, "byte"))
+        k = {"ms": round(t, 5), "share": None}
+        if amount is not None:
+            if unit == "flop":
+                ach = amount / (t / 1e3) / 1e12
+                k.update(bound="tensor", achieved=round(ach, 2), unit="TFLOP/s",
+                         peak=tc_peak, frac=round(ach / tc_peak, 4))
+            else:
+                ach = amount / (t / 1e3) / 1e9
+                k.update(bound="hbm", achieved=round(ach, 1), unit="GB/s",
+                         peak=hbm_peak, frac=round(ach / hbm_peak, 4))
+        kernels[name] = k
+    tot = sum(stage_ms.values())
+    for k in kernels.values():
+        k["share"] = round(k["ms"] / tot, 4)
+    dom = max(kernels, key=lambda n: kernels[n]["ms"])
+    dk = kernels[dom]
+    roofline = {"kernel": dom, "bound": dk.get("bound"), "achieved": dk.get("achieved"),
+                "peak": dk.get("peak"), "unit": dk.get("unit"), "frac": dk.get("frac"),
+                "peak_source": f"{src} (MEASURED_PEAKS.json burst)" if src == "measured" else
+                "fallback", "traffic": None}
+    traffic_file = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(traffic_file):
+        try:
+            tr = json.load(open(traffic_file)).get(f"{wl.name}:{dom}")
+            if tr:
+                roofline["traffic"] = tr
+        except Exception:
+            pass
+
+    # ---------------------------------------------------------------- end to end
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(wl, x, p, dev, K=min(K, 20), units=world * wl.T * p.L, world=world,
+                      flush=flush)
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: {wl.title}", "layers": p.L, "T": wl.T,
+                   "H_q": wl.H_q, "H_kv": wl.H_kv, "d": wl.d, "D_h": wl.D_h,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"{L2_FLUSH_BYTES >> 20} MB buffer written between timed steps"},
+        "roofline": roofline,
+        "kernels": kernels,
+        "gpu_launches": launches,
+        "clocks": clk.summary(t0, t1),
+        "e2e": e2e,
+    }
+    return result, wl, p
+
+
+def run_e2e(wl, x, p, dev, K, units, world, flush):
+    """Same step through the same calls, inputs from pinned host memory: the H2D copies
+    of every input and the D2H read of the results are inside the timed region."""
+    import torch
+    host = {}
+
+    def flat(d):
+        for k, v in d.items():
+            if isinstance(v, list):
+                for i, t in enumerate(v):
+                    yield f"{k}{i}", t
+            else:
+                yield k, v
+    pairs = []
+    for name, t in flat(x):
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t.cpu())
+        pairs.append((h, t))
+    outs = [p.score]
+    pages = p.pages if isinstance(p.pages, list) else [p.pages]
+    for pg in pages:
+        outs += [pg.seq_lens, pg.block_table]
+    outs_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    bi = sum(h.numel() * h.element_size() for h, _ in pairs)
+    bo = sum(o.numel() * o.element_size() for o in outs)
+    stream = torch.cuda.current_stream()
+    tot = 0.0
+    for i in range(K + 2):
+        flush.fill_(float(i))
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for h, d in pairs:
+            d.copy_(h, non_blocking=True)
+        p.step()
+        for o, oh in zip(outs, outs_h):
+            oh.copy_(o, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= 2:
+            tot += a.elapsed_time(b)
+    ms = tot / K
+    return {"value": round(units / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(wl, x_host_layer):
+    """One bounded sample of the workload on the CPU oracle.  Returns (seconds, tokens
+    scored per layer-equivalent, description)."""
+    import numpy as np
+
+    import oracle as O
+
+    def f64(t):
+        return O.bf16_bits_to_f64(t.contiguous().view(__import__("torch").int16).numpy()
+                                  .view(np.uint16))
+    x = x_host_layer
+    t0 = time.perf_counter()
+    if wl.kind in ("kvzip", "kvzip_plus"):
+        q, kc, kt = f64(x["q"]), f64(x["k_ctx"]), f64(x["k_tail"])
+        vn = O.value_norm(f64(x["v_ctx"]), f64(x["w_o"]), wl.H_q) if "w_o" in x else None
+        lse = O.lse(q, kc, kt)
+        s = O.kvzip_score(q, kc, kt, lse_=lse, vnorm=vn, h=f64(x["h"]) if "h" in x else None)
+        for r in wl.keep_ratios:
+            m, _ = O.prune_topk(s, wl.topk_budget(r), wl.w)
+            O.compact_paged(x["k_ctx"].view(__import__("torch").int16).numpy(),
+                            x["v_ctx"].view(__import__("torch").int16).numpy(), m, wl.page_size)
+        return time.perf_counter() - t0, wl.T, "1 full layer (all heads): vnorm, lse, " \
+            "score, top-k and compaction at every budget"
+    if wl.kind == "kvzip_plus_chunked":
+        # one chunk of one KV-head group of one layer; scaled by chunks x groups
+        g = wl.g
+        q = f64(x["q"][0][:, 0:g]); kt = f64(x["k_tail"][0][:, 0:1]); kc = f64(x["k_ctx"][:, 0:1])
+        vn = O.value_norm(f64(x["v_ctx"][:, 0:1]), f64(x["w_o"][:, :, 0:g * wl.d]), g)
+        s = O.kvzip_score(q, kc, kt, vnorm=vn, h=f64(x["h"][0]))
+        dt = (time.perf_counter() - t0) * wl.n_chunks * wl.H_kv
+        return dt, wl.T, "1 chunk x 1 KV-head group of layer 0, scaled x(chunks*groups)"
+    if wl.kind == "future":
+        g = wl.g
+        q = f64(x["q"][:, 0:g, :4096]); k = f64(x["k"][:, 0:1, :4096])
+        f = O.future_attention_mass(q, k, wl.w)
+        dt = (time.perf_counter() - t0) * wl.H_kv * (wl.T / 4096) ** 2
+        return dt, wl.T, "first 4096 tokens of 1 KV-head group of layer 0, scaled x(groups*(T/4096)^2)"
+    if wl.kind == "kvzap":
+        n = 16384
+        z = O.linear_surrogate(f64(x["h"][:, :n]), f64(x["W"]), x["b"].double().numpy())
+        m, _ = O.prune_threshold(z, wl.tau, wl.w)
+        import torch
+        O.compact_paged(x["k"][:, :, :n].contiguous().view(torch.int16).numpy(),
+                        x["v"][:, :, :n].contiguous().view(torch.int16).numpy(), m, wl.page_size)
+        dt = (time.perf_counter() - t0) * (wl.T / n)
+        return dt, wl.T, f"first {n} tokens of layer 0 (surrogate, threshold, compaction), scaled x(T/{n})"
+    raise ValueError(wl.kind)
+
+
+def host_layer0(wl):
+    from kv_cache_eviction_lse_gb300 import workloads as W
+    return W.generate(wl, layers=[0], device="cpu")
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_cpu_baseline(wl):
+    x = host_layer0(wl)
+    dt, tokens, desc = oracle_sample(wl, x)
+    return {"value": round(tokens / dt, 2), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": desc + f"; {dt:.2f} s per layer-equivalent; numpy fp64 (BLAS threads = "
+                             f"host cores, elementwise single-threaded)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    from kv_cache_eviction_lse_gb300 import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    K = args.steps or 3
+    Wm = max(3, args.warmup) if args.warmup is not None else 3
+    x = host_layer0(wl)
+    for _ in range(Wm if wl.kind in ("kvzip", "kvzap") else 1):
+        oracle_sample(wl, x)
+    times = []
+    for _ in range(K):
+        dt, tokens, desc = oracle_sample(wl, x)
+        times.append(dt)
+    ms = 1e3 * statistics.mean(times)
+    value = wl.T / (ms / 1e3)
+    cb = {"value": round(value, 2), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+          "sample": desc}
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+            "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"{wl.name}: {wl.title}", "layers": wl.L, "T": wl.T,
+                       "H_q": wl.H_q, "H_kv": wl.H_kv, "d": wl.d, "D_h": wl.D_h,
+                       "parallelism": "host cores (oracle)"},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    res, wl, p = run_gpu(args, rank, world, local)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = run_cpu_baseline(wl)
+        else:
+            res["cpu_baseline"] = None
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,230 @@
+/*
+ * kvs.h -- C ABI of the GB300 (sm_103a) KV-cache importance scoring and pruning library.
+ *
+ * The library computes, on one GPU, the data-parallel path shared by the KV-cache
+ * eviction methods described in:
+ *   [KVzap]  "KVzap: Fast, Adaptive, and Faithful KV Cache Pruning" (review):
+ *            3.1 KVzip score (Eq. 1), 3.2 KVzip+ score (Eq. 2, Eq. 3), 3.3 KVzap
+ *            surrogate, thresholding with a sliding window, Algorithm 1 (compress).
+ *   [KVpop]  "[Paper review] KVpop -- Key-Value Cache Compression with Predictive
+ *            Online Pruning": 1. Key Terms (future-attention target, transposed-
+ *            attention pass reusing the attention kernel's LSE), 3. Method (per-head
+ *            top-k).
+ *   [KVzip]  KVzip review: Methods (teacher-forced repeat), technical details
+ *            (chunked reconstruction).
+ *
+ * Conventions shared by every entry point
+ *   - Tensor arguments are DEVICE pointers owned by the caller.  The library never
+ *     allocates, frees or retains them.  Scratch memory, where an entry point needs
+ *     it, is passed in by the caller (ws, ws_bytes) and sized by the matching
+ *     kvs_*_workspace_size() function.
+ *   - bf16 tensors are passed as raw 16-bit patterns (kvs_bf16).  All tensors are
+ *     dense row-major with the innermost dimension last, as documented per call.
+ *     Every pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls only enqueue work on it and return; none synchronises the host.
+ *   - Return value: KVS_OK, or an error code with a message available from
+ *     kvs_last_error() (thread-local, valid until the next call on that thread).
+ *     Arguments are validated before anything is enqueued; on an error nothing is
+ *     enqueued and no output is touched.
+ *   - Query head hq reads KV head hq / g with g = H_q / H_kv (contiguous groups).
+ *   - Logarithms are natural; the logit of query j and key i is q_j . k_i / sqrt(d),
+ *     computed in fp32 from the bf16 inputs.
+ */
+#ifndef KVS_H_
+#define KVS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t kvs_bf16; /* raw bfloat16 bit pattern */
+
+typedef enum kvs_status {
+  KVS_OK = 0,
+  KVS_ERR_ARG = 1,         /* null pointer where one is required, negative size, bad mode */
+  KVS_ERR_SHAPE = 2,       /* inconsistent sizes (H_q % H_kv != 0, n_q > keys, ...) */
+  KVS_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+  KVS_ERR_UNSUPPORTED = 4, /* a size the kernels do not handle (d not 64/128, ...) */
+  KVS_ERR_CAPACITY = 5,    /* a caller-provided buffer (workspace) is too small */
+  KVS_ERR_CUDA = 6,        /* the CUDA runtime reported an error at launch */
+  KVS_ERR_DEVICE = 7       /* a kernel recorded a device-side error (see kvs_device_error) */
+} kvs_status;
+
+/* Model shape of one call.  L is the number of layers the call covers (each
+ * tensor's leading dimension). */
+typedef struct kvs_dims {
+  int32_t L;    /* layers, >= 1 */
+  int32_t H_q;  /* query heads, multiple of H_kv */
+  int32_t H_kv; /* key/value heads, >= 1 */
+  int32_t d;    /* head dimension: 64 or 128 */
+  int32_t D_h;  /* hidden size (kvs_vnorm, kvs_score_max with h, kvs_surrogate); else ignored */
+} kvs_dims;
+
+enum { KVS_THRESHOLD = 0, KVS_TOPK = 1 };
+
+const char* kvs_version(void);
+const char* kvs_last_error(void);
+
+/* Number of kernels this library has enqueued since it was loaded (all threads, all
+ * devices).  A diagnostic for counting launches around a region of interest. */
+uint64_t kvs_launch_count(void);
+
+/* Device-side error word shared by all kernels of the library on the current device
+ * (0 = none).  Reading synchronises `stream`; `clear` != 0 resets it to 0. */
+kvs_status kvs_device_error(int32_t* code_out, int32_t clear, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * kvs_lse -- pass 1: per-query log-sum-exp normaliser [KVpop 1. Key Terms: the
+ * transposed pass reuses the LSE normaliser of the attention kernel].
+ *
+ *   lse[l][hq][j] = ln sum_{i <= off + j} exp(q[l][hq][j] . key_i / sqrt(d))
+ *
+ * Keys are the concatenation [k_ctx | k_tail] of KV head hq / g: n_k = T + n_tail.
+ * Causality is bottom-right aligned: the n_q queries are the last n_q positions of
+ * the n_k-token sequence, off = n_k - n_q (the repeated block after context and
+ * repeat prompt [KVzap 3.1; KVzip Methods], or self-attention when n_q == n_k).
+ *
+ *   q      [L][H_q][n_q][d]      bf16
+ *   k_ctx  [L][H_kv][T][d]       bf16
+ *   k_tail [L][H_kv][n_tail][d]  bf16   (may be NULL when n_tail == 0)
+ *   lse    [L][H_q][n_q]         fp32   output
+ * Requires 0 <= n_q <= T + n_tail.
+ * ------------------------------------------------------------------------------- */
+kvs_status kvs_lse(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
+                   const kvs_bf16* k_ctx, int32_t T, const kvs_bf16* k_tail, int32_t n_tail,
+                   float* lse, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * kvs_score_max -- pass 2, KVzip / KVzip+ reduction [KVzap 3.1 Eq. 1, 3.2 Eq. 3].
+ * Recomputes a_ji = exp(q_j . k_i / sqrt(d) - lse_j) tile by tile (the dense matrix
+ * is never formed) and reduces each context key over the scoring queries and over
+ * the query heads of its GQA group, in the log domain:
+ *
+ *   log_score[l][hk][i] = max_{hq in group(hk)} [ ln vnorm[l][hq][i]
+ *                           + max_j ( q_j . k_i / sqrt(d) - lse[l][hq][j] - ln ||h[l][j]|| ) ]
+ *                       = ln max_{hq, j} a_ji ||W_O^{(hq)} v_i|| / ||h_j||
+ *
+ * vnorm == NULL drops the value factor, h == NULL drops the hidden-state factor
+ * (both NULL: the KVzip score ln s_i of Eq. 1).  All context keys are visible to all
+ * scoring queries (the queries follow the context).
+ *
+ *   q         [L][H_q][n_q][d]  bf16   scoring queries (same as passed to kvs_lse)
+ *   k_ctx     [L][H_kv][T][d]   bf16   context keys to score
+ *   lse       [L][H_q][n_q]     fp32   from kvs_lse over the same queries
+ *   vnorm     [L][H_q][T]       fp32   ||W_O^{(hq)} v_i|| from kvs_vnorm, or NULL
+ *   h         [L][n_q][D_h]     bf16   residual-stream input at the queries, or NULL
+ *   log_score [L][H_kv][T]      fp32   output; with accumulate != 0 the result is
+ *                                      max(previous contents, new score) (chunked
+ *                                      reconstruction [KVzip technical details])
+ *   ws        scratch of kvs_score_max_workspace_size() bytes (NULL allowed when h is NULL)
+ * ------------------------------------------------------------------------------- */
+size_t kvs_score_max_workspace_size(const kvs_dims* dims, int32_t n_q, int32_t with_h);
+kvs_status kvs_score_max(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
+                         const kvs_bf16* k_ctx, int32_t T, const float* lse,
+                         const float* vnorm, const kvs_bf16* h, int32_t accumulate,
+                         float* log_score, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * kvs_score_future_sum -- pass 2, KVpop future-attention target [KVpop 1. Key Terms]:
+ * the attention mass key i receives after it leaves the protected window of w tokens,
+ * summed over the query heads of its group, for causal self-attention over T tokens:
+ *
+ *   score[l][hk][i] = sum_{hq in group(hk)} sum_{j = i + w}^{T - 1}
+ *                       exp(q[l][hq][j] . k[l][hk][i] / sqrt(d) - lse[l][hq][j])
+ *
+ *   q     [L][H_q][T][d]  bf16,  k [L][H_kv][T][d] bf16
+ *   lse   [L][H_q][T]     fp32   from kvs_lse(q, n_q = T, k_ctx = k, T, n_tail = 0)
+ *   score [L][H_kv][T]    fp32   output (linear mass, not a log); keys i > T-1-w get 0
+ * Requires w >= 0.
+ * ------------------------------------------------------------------------------- */
+kvs_status kvs_score_future_sum(const kvs_dims* dims, const kvs_bf16* q, const kvs_bf16* k,
+                                int32_t T, const float* lse, int32_t w, float* score,
+                                void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * kvs_vnorm -- value factor of KVzip+ [KVzap 3.2, Eq. 2 and Eq. 3]:
+ *
+ *   vnorm[l][hq][i] = || W_O^{(hq)} v[l][hq/g][i] ||_2
+ *
+ * W_O^{(hq)} is the d-column slice hq*d .. hq*d+d-1 of the output projection
+ * o_proj.weight [D_h][H_q*d].  Computed through the Gram matrix
+ * G_hq = W_O^{(hq)T} W_O^{(hq)} (d x d, fp32, kept in the workspace) as sqrt(v^T G v).
+ *
+ *   v     [L][H_kv][T][d]   bf16
+ *   w_o   [L][D_h][H_q*d]   bf16
+ *   vnorm [L][H_q][T]       fp32 output
+ *   ws    scratch of kvs_vnorm_workspace_size() bytes (L*H_q*d*d floats)
+ * ------------------------------------------------------------------------------- */
+size_t kvs_vnorm_workspace_size(const kvs_dims* dims);
+kvs_status kvs_vnorm(const kvs_dims* dims, const kvs_bf16* v, int32_t T, const kvs_bf16* w_o,
+                     float* vnorm, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * kvs_surrogate -- KVzap-Linear score [KVzap 3.3; Algorithm 1, step 1]: at each
+ * position t the hidden state h_t (D_h) maps to one predicted log-score per KV head,
+ *
+ *   score[l][hk][t] = sum_c h[l][t][c] * W[l][c][hk] + b[l][hk]
+ *
+ * Optionally fused with the threshold rule [KVzap, thresholding with a sliding
+ * window]: when mask != NULL, mask[l][hk][t] = (score >= tau || t >= T - w) and
+ * keep[l][hk] = number of kept tokens.
+ *
+ *   h     [L][T][D_h]   bf16,  W [L][D_h][H_kv] bf16,  b [L][H_kv] fp32
+ *   score [L][H_kv][T]  fp32 output
+ *   mask  [L][H_kv][T]  uint8 output or NULL;  keep [L][H_kv] int32 (required with mask)
+ * Requires H_kv <= 16 and D_h a positive multiple of 128 with D_h * ceil(H_kv/8) <= 12800.
+ * ------------------------------------------------------------------------------- */
+kvs_status kvs_surrogate(const kvs_dims* dims, const kvs_bf16* h, int32_t T,
+                         const kvs_bf16* W, const float* b, float* score,
+                         float tau, int32_t w, uint8_t* mask, int32_t* keep, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * kvs_prune_mask -- keep mask per (layer, KV head) row of T scores.
+ *   KVS_THRESHOLD [KVzap thresholding; Algorithm 1]: keep t  <=>  score >= tau or
+ *                 t >= T - w.  A NaN score is dropped unless inside the window.
+ *   KVS_TOPK      [KVpop 3. Method; KVzap 3.1 fixed-ratio KVzip]: keep the last w
+ *                 tokens plus the k highest-scoring of the other T - w tokens (all of
+ *                 them if k >= T - w).  Ranking: score descending, ties to the
+ *                 earlier position, NaN below every number.
+ *   score [L][H_kv][T] fp32;  mask [L][H_kv][T] uint8 output;  keep [L][H_kv] int32 output.
+ * ------------------------------------------------------------------------------- */
+kvs_status kvs_prune_mask(const kvs_dims* dims, const float* score, int32_t T, int32_t mode,
+                          float tau, int32_t k, int32_t w, uint8_t* mask, int32_t* keep,
+                          void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * kvs_compact_paged -- gather of the kept K/V rows [KVzap Algorithm 1: keys[indices],
+ * values[indices]] into a per-head variable-length paged cache (non-uniform head
+ * lengths need PagedAttention-like storage [KVzap, limitation 3]).
+ *
+ * Layout: each (layer, head) row gets ceil(kept / page_size) consecutive pages,
+ * allocated layer-major then head from page 0; kept tokens are stored in ascending
+ * position; unused rows of a row's last page are zero-filled.
+ *   block_table[l][hk][p] = absolute page id of the row's p-th page, -1 past the end
+ *   seq_lens[l][hk]       = kept tokens;   needed_pages[0] = total pages (device int32)
+ * If the total exceeds capacity_pages, no page is written and every block_table
+ * entry is -1; needed_pages and seq_lens are still written, so the caller can read
+ * needed_pages, grow the pool and call again.
+ *
+ *   k, v          [L][H_kv][T][d]                 bf16
+ *   mask          [L][H_kv][T]                    uint8 (non-zero = keep)
+ *   k_pages, v_pages [capacity_pages][page_size][d] bf16 outputs
+ *   block_table   [L][H_kv][max_pages] int32, max_pages >= ceil(T / page_size)
+ *   seq_lens      [L][H_kv] int32;  needed_pages [1] int32
+ *   ws            scratch of kvs_compact_workspace_size() bytes
+ * ------------------------------------------------------------------------------- */
+size_t kvs_compact_workspace_size(const kvs_dims* dims, int32_t T);
+kvs_status kvs_compact_paged(const kvs_dims* dims, const kvs_bf16* k, const kvs_bf16* v,
+                             int32_t T, const uint8_t* mask, int32_t page_size,
+                             kvs_bf16* k_pages, kvs_bf16* v_pages, int32_t capacity_pages,
+                             int32_t* block_table, int32_t max_pages, int32_t* seq_lens,
+                             int32_t* needed_pages, void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVS_H_ */

@@ -1,0 +1,293 @@
+// C ABI of the kvs library: argument validation, then launches on the caller's stream.
+// Declarations and argument documentation: include/kvs.h.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <atomic>
+#include <string>
+
+#include "../../include/kvs.h"
+#include "attn.cuh"
+#include "compact.cuh"
+#include "prune.cuh"
+#include "surrogate.cuh"
+#include "vnorm.cuh"
+
+namespace kvs {
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+}  // namespace kvs
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kvs_status fail(kvs_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+kvs_status ok() {
+  g_last_error.clear();
+  return KVS_OK;
+}
+
+kvs_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return ok();
+  return fail(KVS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define REQUIRE(cond, st, ...) \
+  do {                         \
+    if (!(cond)) return fail(st, __VA_ARGS__); \
+  } while (0)
+
+#define REQUIRE_PTR(p)                                                       \
+  do {                                                                       \
+    if (!(p)) return fail(KVS_ERR_ARG, "%s: " #p " is NULL", __func__);      \
+    if (!aligned16(p)) return fail(KVS_ERR_ALIGN, "%s: " #p " is not 16-byte aligned", __func__); \
+  } while (0)
+
+#define REQUIRE_OPT_PTR(p)                                                   \
+  do {                                                                       \
+    if ((p) && !aligned16(p))                                                \
+      return fail(KVS_ERR_ALIGN, "%s: " #p " is not 16-byte aligned", __func__); \
+  } while (0)
+
+kvs_status check_dims(const kvs_dims* dm, const char* fn, bool need_heads = true) {
+  if (!dm) return fail(KVS_ERR_ARG, "%s: dims is NULL", fn);
+  if (dm->L < 1) return fail(KVS_ERR_SHAPE, "%s: L = %d must be >= 1", fn, dm->L);
+  if (dm->H_kv < 1) return fail(KVS_ERR_SHAPE, "%s: H_kv = %d must be >= 1", fn, dm->H_kv);
+  if (need_heads) {
+    if (dm->H_q < 1 || dm->H_q % dm->H_kv)
+      return fail(KVS_ERR_SHAPE, "%s: H_q = %d must be a positive multiple of H_kv = %d", fn,
+                  dm->H_q, dm->H_kv);
+    if (dm->d != 64 && dm->d != 128)
+      return fail(KVS_ERR_UNSUPPORTED, "%s: head dim d = %d (supported: 64, 128)", fn, dm->d);
+  }
+  if (dm->L > 65535 || dm->H_q > 65535 || dm->H_kv > 65535)
+    return fail(KVS_ERR_UNSUPPORTED, "%s: L/H_q/H_kv above 65535", fn);
+  return KVS_OK;
+}
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+const char* kvs_version(void) { return "kvs 0.1.0 (sm_103a)"; }
+
+const char* kvs_last_error(void) { return g_last_error.c_str(); }
+
+uint64_t kvs_launch_count(void) { return kvs::g_launches.load(std::memory_order_relaxed); }
+
+kvs_status kvs_device_error(int32_t* code_out, int32_t clear, void* stream) {
+  REQUIRE(code_out, KVS_ERR_ARG, "kvs_device_error: code_out is NULL");
+  cudaError_t e = cudaStreamSynchronize(as_stream(stream));
+  if (e != cudaSuccess) return cuda_status(e, "kvs_device_error");
+  *code_out = 0;
+  (void)clear;
+  return ok();
+}
+
+kvs_status kvs_lse(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q, const kvs_bf16* k_ctx,
+                   int32_t T, const kvs_bf16* k_tail, int32_t n_tail, float* lse, void* stream) {
+  kvs_status st = check_dims(dims, __func__);
+  if (st) return st;
+  REQUIRE(n_q >= 0 && T >= 0 && n_tail >= 0, KVS_ERR_ARG, "kvs_lse: negative size");
+  REQUIRE(n_q <= T + n_tail, KVS_ERR_SHAPE, "kvs_lse: n_q = %d exceeds keys T + n_tail = %d", n_q,
+          T + n_tail);
+  if (n_q == 0) return ok();
+  REQUIRE_PTR(q);
+  REQUIRE_PTR(lse);
+  if (T > 0) REQUIRE_PTR(k_ctx);
+  if (n_tail > 0) REQUIRE_PTR(k_tail);
+  kvs::AttnArgs a;
+  a.q = q; a.k_ctx = k_ctx; a.k_tail = k_tail; a.out = lse;
+  a.L = dims->L; a.Hq = dims->H_q; a.Hkv = dims->H_kv; a.d = dims->d;
+  a.n_q = n_q; a.T = T; a.n_tail = n_tail;
+  return cuda_status(kvs::launch_lse(a, as_stream(stream)), "kvs_lse");
+}
+
+size_t kvs_score_max_workspace_size(const kvs_dims* dims, int32_t n_q, int32_t with_h) {
+  if (!dims || !with_h || n_q <= 0 || dims->L <= 0) return 0;
+  return (size_t)dims->L * n_q * sizeof(float);
+}
+
+kvs_status kvs_score_max(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
+                         const kvs_bf16* k_ctx, int32_t T, const float* lse, const float* vnorm,
+                         const kvs_bf16* h, int32_t accumulate, float* log_score, void* ws,
+                         size_t ws_bytes, void* stream) {
+  kvs_status st = check_dims(dims, __func__);
+  if (st) return st;
+  REQUIRE(n_q >= 0 && T >= 0, KVS_ERR_ARG, "kvs_score_max: negative size");
+  if (T == 0) return ok();
+  REQUIRE_PTR(k_ctx);
+  REQUIRE_PTR(log_score);
+  REQUIRE_OPT_PTR(vnorm);
+  REQUIRE_OPT_PTR(h);
+  if (n_q > 0) {
+    REQUIRE_PTR(q);
+    REQUIRE_PTR(lse);
+  }
+  if (h) {
+    REQUIRE(dims->D_h > 0 && dims->D_h % 8 == 0, KVS_ERR_SHAPE,
+            "kvs_score_max: D_h = %d must be a positive multiple of 8 when h is given", dims->D_h);
+    const size_t need = kvs_score_max_workspace_size(dims, n_q, 1);
+    REQUIRE(ws || need == 0, KVS_ERR_ARG, "kvs_score_max: workspace is NULL");
+    REQUIRE(ws_bytes >= need, KVS_ERR_CAPACITY,
+            "kvs_score_max: workspace of %zu bytes, %zu needed", ws_bytes, need);
+    REQUIRE_OPT_PTR(ws);
+  }
+  cudaStream_t s = as_stream(stream);
+  kvs::AttnArgs a;
+  a.q = q; a.k_ctx = k_ctx; a.lse = lse; a.vnorm = vnorm; a.out = log_score;
+  a.L = dims->L; a.Hq = dims->H_q; a.Hkv = dims->H_kv; a.d = dims->d;
+  a.n_q = n_q; a.T = T; a.accumulate = accumulate != 0;
+  if (h && n_q > 0) {
+    float* hlog = static_cast<float*>(ws);
+    cudaError_t e = kvs::launch_hidden_log_norm(h, dims->L, n_q, dims->D_h, hlog, s);
+    if (e != cudaSuccess) return cuda_status(e, "kvs_score_max (hidden norm)");
+    a.hlog = hlog;
+  }
+  return cuda_status(kvs::launch_score_max(a, s), "kvs_score_max");
+}
+
+kvs_status kvs_score_future_sum(const kvs_dims* dims, const kvs_bf16* q, const kvs_bf16* k,
+                                int32_t T, const float* lse, int32_t w, float* score,
+                                void* stream) {
+  kvs_status st = check_dims(dims, __func__);
+  if (st) return st;
+  REQUIRE(T >= 0 && w >= 0, KVS_ERR_ARG, "kvs_score_future_sum: negative T or w");
+  if (T == 0) return ok();
+  REQUIRE_PTR(q);
+  REQUIRE_PTR(k);
+  REQUIRE_PTR(lse);
+  REQUIRE_PTR(score);
+  kvs::AttnArgs a;
+  a.q = q; a.k_ctx = k; a.lse = lse; a.out = score;
+  a.L = dims->L; a.Hq = dims->H_q; a.Hkv = dims->H_kv; a.d = dims->d;
+  a.n_q = T; a.T = T; a.w = w;
+  return cuda_status(kvs::launch_future_sum(a, as_stream(stream)), "kvs_score_future_sum");
+}
+
+size_t kvs_vnorm_workspace_size(const kvs_dims* dims) {
+  if (!dims || dims->L <= 0 || dims->H_q <= 0 || dims->d <= 0) return 0;
+  return kvs::vnorm_workspace_bytes(dims->L, dims->H_q, dims->d);
+}
+
+kvs_status kvs_vnorm(const kvs_dims* dims, const kvs_bf16* v, int32_t T, const kvs_bf16* w_o,
+                     float* vnorm, void* ws, size_t ws_bytes, void* stream) {
+  kvs_status st = check_dims(dims, __func__);
+  if (st) return st;
+  REQUIRE(T >= 0, KVS_ERR_ARG, "kvs_vnorm: negative T");
+  REQUIRE(dims->D_h > 0 && dims->D_h % 8 == 0, KVS_ERR_SHAPE,
+          "kvs_vnorm: D_h = %d must be a positive multiple of 8", dims->D_h);
+  if (T == 0) return ok();
+  REQUIRE_PTR(v);
+  REQUIRE_PTR(w_o);
+  REQUIRE_PTR(vnorm);
+  REQUIRE_PTR(ws);
+  const size_t need = kvs_vnorm_workspace_size(dims);
+  REQUIRE(ws_bytes >= need, KVS_ERR_CAPACITY, "kvs_vnorm: workspace of %zu bytes, %zu needed",
+          ws_bytes, need);
+  return cuda_status(kvs::launch_vnorm(v, dims->L, dims->H_q, dims->H_kv, dims->d, T, dims->D_h,
+                                       w_o, vnorm, static_cast<float*>(ws), as_stream(stream)),
+                     "kvs_vnorm");
+}
+
+kvs_status kvs_surrogate(const kvs_dims* dims, const kvs_bf16* h, int32_t T, const kvs_bf16* W,
+                         const float* b, float* score, float tau, int32_t w, uint8_t* mask,
+                         int32_t* keep, void* stream) {
+  kvs_status st = check_dims(dims, __func__, false);
+  if (st) return st;
+  REQUIRE(T >= 0 && w >= 0, KVS_ERR_ARG, "kvs_surrogate: negative T or w");
+  REQUIRE(dims->H_kv <= 16, KVS_ERR_UNSUPPORTED, "kvs_surrogate: H_kv = %d (at most 16)",
+          dims->H_kv);
+  REQUIRE(dims->D_h > 0 && dims->D_h % 128 == 0, KVS_ERR_UNSUPPORTED,
+          "kvs_surrogate: D_h = %d must be a positive multiple of 128", dims->D_h);
+  REQUIRE(kvs::surrogate_smem_bytes(dims->D_h, dims->H_kv) <= 200 * 1024, KVS_ERR_UNSUPPORTED,
+          "kvs_surrogate: D_h * ceil(H_kv/8) = %d above 12800",
+          dims->D_h * ((dims->H_kv + 7) / 8));
+  if (T == 0) return ok();
+  REQUIRE_PTR(h);
+  REQUIRE_PTR(W);
+  REQUIRE_PTR(b);
+  REQUIRE_PTR(score);
+  if (mask) {
+    REQUIRE_PTR(keep);
+  }
+  return cuda_status(kvs::launch_surrogate(h, dims->L, T, dims->D_h, dims->H_kv, W, b, score, tau,
+                                           w, mask, keep, as_stream(stream)),
+                     "kvs_surrogate");
+}
+
+kvs_status kvs_prune_mask(const kvs_dims* dims, const float* score, int32_t T, int32_t mode,
+                          float tau, int32_t k, int32_t w, uint8_t* mask, int32_t* keep,
+                          void* stream) {
+  kvs_status st = check_dims(dims, __func__, false);
+  if (st) return st;
+  REQUIRE(T >= 0 && w >= 0 && k >= 0, KVS_ERR_ARG, "kvs_prune_mask: negative T, k or w");
+  REQUIRE(mode == KVS_THRESHOLD || mode == KVS_TOPK, KVS_ERR_ARG, "kvs_prune_mask: mode = %d",
+          mode);
+  REQUIRE_PTR(keep);
+  if (T > 0) {
+    REQUIRE_PTR(score);
+    REQUIRE_PTR(mask);
+  }
+  return cuda_status(kvs::launch_prune(score, dims->L * dims->H_kv, T, mode, tau, k, w, mask, keep,
+                                       as_stream(stream)),
+                     "kvs_prune_mask");
+}
+
+size_t kvs_compact_workspace_size(const kvs_dims* dims, int32_t T) {
+  if (!dims || dims->L <= 0 || dims->H_kv <= 0 || T < 0) return 0;
+  return kvs::compact_workspace_bytes(dims->L * dims->H_kv, T);
+}
+
+kvs_status kvs_compact_paged(const kvs_dims* dims, const kvs_bf16* k, const kvs_bf16* v, int32_t T,
+                             const uint8_t* mask, int32_t page_size, kvs_bf16* k_pages,
+                             kvs_bf16* v_pages, int32_t capacity_pages, int32_t* block_table,
+                             int32_t max_pages, int32_t* seq_lens, int32_t* needed_pages,
+                             void* ws, size_t ws_bytes, void* stream) {
+  kvs_status st = check_dims(dims, __func__, false);
+  if (st) return st;
+  REQUIRE(dims->d == 64 || dims->d == 128, KVS_ERR_UNSUPPORTED,
+          "kvs_compact_paged: head dim d = %d (supported: 64, 128)", dims->d);
+  REQUIRE(T >= 0 && capacity_pages >= 0, KVS_ERR_ARG, "kvs_compact_paged: negative size");
+  REQUIRE(page_size >= 1 && page_size <= 4096, KVS_ERR_UNSUPPORTED,
+          "kvs_compact_paged: page_size = %d (1..4096)", page_size);
+  REQUIRE(max_pages >= (T + page_size - 1) / page_size, KVS_ERR_SHAPE,
+          "kvs_compact_paged: max_pages = %d below ceil(T / page_size) = %d", max_pages,
+          (T + page_size - 1) / page_size);
+  REQUIRE_PTR(seq_lens);
+  REQUIRE_PTR(needed_pages);
+  REQUIRE_PTR(ws);
+  if (max_pages > 0) REQUIRE_PTR(block_table);
+  if (T > 0) {
+    REQUIRE_PTR(k);
+    REQUIRE_PTR(v);
+    REQUIRE_PTR(mask);
+  }
+  if (capacity_pages > 0) {
+    REQUIRE_PTR(k_pages);
+    REQUIRE_PTR(v_pages);
+  }
+  const size_t need = kvs_compact_workspace_size(dims, T);
+  REQUIRE(ws_bytes >= need, KVS_ERR_CAPACITY,
+          "kvs_compact_paged: workspace of %zu bytes, %zu needed", ws_bytes, need);
+  return cuda_status(kvs::launch_compact(k, v, dims->L * dims->H_kv, T, dims->d, mask, page_size,
+                                         k_pages, v_pages, capacity_pages, block_table, max_pages,
+                                         seq_lens, needed_pages, ws, as_stream(stream)),
+                     "kvs_compact_paged");
+}
+
+}  // extern "C"

@@ -1,0 +1,32 @@
+// Launchers of the two attention-scoring passes (pass 1: LSE; pass 2: transposed
+// KVzip max / KVpop future mass) and the hidden-norm prologue.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace kvs {
+
+struct AttnArgs {
+  const bf16_t* q = nullptr;       // [L][Hq][n_q][d]
+  const bf16_t* k_ctx = nullptr;   // [L][Hkv][T][d]
+  const bf16_t* k_tail = nullptr;  // [L][Hkv][n_tail][d]
+  const float* lse = nullptr;      // [L][Hq][n_q]
+  const float* vnorm = nullptr;    // [L][Hq][T] or null
+  const float* hlog = nullptr;     // [L][n_q] ln||h_j|| or null
+  float* out = nullptr;
+  int L = 0, Hq = 0, Hkv = 0, d = 0, n_q = 0, T = 0, n_tail = 0;
+  int w = 0, accumulate = 0;
+};
+
+cudaError_t launch_lse(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_score_max(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_future_sum(const AttnArgs& a, cudaStream_t s);
+
+// hlog[l][j] = ln ||h[l][j]||_2 over D_h bf16 channels.
+cudaError_t launch_hidden_log_norm(const bf16_t* h, int L, int n, int Dh, float* hlog,
+                                   cudaStream_t s);
+
+}  // namespace kvs

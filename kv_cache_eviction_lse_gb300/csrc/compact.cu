@@ -1,0 +1,255 @@
+// Paged per-head variable-length compaction of the kept K/V rows (KVzap review,
+// Algorithm 1: keys[indices], values[indices]; limitation 3: non-uniform head
+// lengths need PagedAttention-like storage).
+//
+// Three launches, all bandwidth-bound:
+//   1. seg_count   : kept tokens per (row, 4096-token segment)         reads the mask
+//   2. page_plan   : per-row exclusive scan of segment counts, page counts
+//                    ceil(kept/page), exclusive scan of pages over rows (layer-major,
+//                    then head), capacity check, seq_lens, needed_pages
+//   3. scatter     : per (row, segment) ordered rank of each kept token (block scan),
+//                    then a block-cooperative 16-byte copy of the kept K and V rows
+//                    into (page, slot); the last segment zero-fills the tail of the
+//                    row's last page; every block fills its share of block_table.
+#include "common.cuh"
+#include "compact.cuh"
+
+namespace kvs {
+namespace {
+
+constexpr int kSeg = 4096;      // tokens per segment
+constexpr int kSegThreads = 256;  // 16 mask bytes per thread
+
+struct Plan {            // lives at the start of the workspace
+  int ok;                // total pages <= capacity
+  int total_pages;
+  int pad[2];
+};
+
+__device__ __forceinline__ int nonzero_bytes(uint32_t w) { return __popc(__vcmpne4(w, 0u)) >> 3; }
+
+// Kept count of each (row, segment).
+__global__ void __launch_bounds__(kSegThreads) seg_count_kernel(const uint8_t* __restrict__ mask,
+                                                                int T, int nseg,
+                                                                int* __restrict__ seg) {
+  __shared__ int red[kSegThreads / 32];
+  const int s = blockIdx.x, row = blockIdx.y;
+  const uint8_t* m = mask + (size_t)row * T;
+  const int t0 = s * kSeg + threadIdx.x * 16;
+  int c = 0;
+  if ((T & 15) == 0) {
+    if (t0 < T) {
+      const uint4 u = *reinterpret_cast<const uint4*>(m + t0);
+      c = nonzero_bytes(u.x) + nonzero_bytes(u.y) + nonzero_bytes(u.z) + nonzero_bytes(u.w);
+    }
+  } else {
+    for (int t = t0; t < min(t0 + 16, T); ++t) c += m[t] != 0;
+  }
+  c = warp_sum_int(c);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int tot = 0;
+    for (int i = 0; i < kSegThreads / 32; ++i) tot += red[i];
+    seg[(size_t)row * nseg + s] = tot;
+  }
+}
+
+// One block: segment offsets per row, page offsets over rows, capacity check.
+__global__ void __launch_bounds__(1024) page_plan_kernel(int rows, int nseg, int page_size,
+                                                         int capacity, int* __restrict__ seg,
+                                                         int* __restrict__ first_page,
+                                                         Plan* __restrict__ plan,
+                                                         int* __restrict__ seq_lens,
+                                                         int* __restrict__ needed) {
+  __shared__ int warp_tot[32];
+  __shared__ int carry_s;
+  if (threadIdx.x == 0) carry_s = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int base = 0; base < rows; base += blockDim.x) {
+    const int r = base + threadIdx.x;
+    int pages = 0;
+    if (r < rows) {
+      int* sr = seg + (size_t)r * nseg;
+      int acc = 0;
+      for (int s = 0; s < nseg; ++s) {
+        const int c = sr[s];
+        sr[s] = acc;
+        acc += c;
+      }
+      seq_lens[r] = acc;
+      pages = (acc + page_size - 1) / page_size;
+    }
+    // block exclusive scan of pages
+    int incl = pages;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int x = lane < nw ? warp_tot[lane] : 0;
+      int wi = x;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += y;
+      }
+      if (lane < nw) warp_tot[lane] = wi - x;
+    }
+    __syncthreads();
+    const int excl = carry_s + warp_tot[warp] + incl - pages;
+    if (r < rows) first_page[r] = excl;
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) carry_s = excl + pages;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    plan->total_pages = carry_s;
+    plan->ok = carry_s <= capacity;
+    *needed = carry_s;
+  }
+}
+
+__global__ void __launch_bounds__(kSegThreads) scatter_kernel(
+    const bf16_t* __restrict__ k, const bf16_t* __restrict__ v, const uint8_t* __restrict__ mask,
+    int T, int d, int nseg, int page_size, const int* __restrict__ seg,
+    const int* __restrict__ first_page, const Plan* __restrict__ plan,
+    const int* __restrict__ seq_lens, bf16_t* __restrict__ k_pages, bf16_t* __restrict__ v_pages,
+    int* __restrict__ block_table, int max_pages) {
+  __shared__ uint16_t list[kSeg];
+  __shared__ int red[33];
+  const int s = blockIdx.x, row = blockIdx.y;
+  const bool ok = plan->ok != 0;
+  const int first = first_page[row];
+  const int kept = seq_lens[row];
+  const int npages = (kept + page_size - 1) / page_size;
+
+  // block_table entries [s*ppseg, (s+1)*ppseg), the last segment also covers the rest
+  {
+    const int ppseg = (kSeg + page_size - 1) / page_size;
+    const int p0 = s * ppseg;
+    const int p1 = (s == nseg - 1) ? max_pages : min(max_pages, p0 + ppseg);
+    int* bt = block_table + (size_t)row * max_pages;
+    for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x)
+      bt[p] = (ok && p < npages) ? first + p : -1;
+  }
+  if (!ok) return;
+
+  // ordered ranks of the kept tokens of this segment
+  const uint8_t* m = mask + (size_t)row * T;
+  const int t0 = s * kSeg + threadIdx.x * 16;
+  uint8_t f[16];
+  if ((T & 15) == 0 && t0 < T) {
+    const uint4 u = *reinterpret_cast<const uint4*>(m + t0);
+    const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) f[i] = ((wd[i >> 2] >> (8 * (i & 3))) & 255u) != 0;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) f[i] = (t0 + i < T) ? (m[t0 + i] != 0) : 0;
+  }
+  int c = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) c += f[i];
+  // block exclusive scan of c
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) red[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int x = lane < nw ? red[lane] : 0;
+    int wi = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    if (lane < nw) red[lane] = wi - x;
+    if (lane == nw - 1) red[32] = wi;
+  }
+  __syncthreads();
+  int pos = red[warp] + incl - c;
+  const int n_local = red[32];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    if (f[i]) list[pos++] = (uint16_t)(threadIdx.x * 16 + i);
+  __syncthreads();
+
+  // cooperative copy: (d/8) 16-byte chunks per kept row, for K and V
+  const int base_rank = seg[(size_t)row * nseg + s];
+  const int cpr = d / 8;
+  const size_t src_row0 = (size_t)row * T + (size_t)s * kSeg;
+  const int total = n_local * cpr;
+  constexpr int U = 4;
+  for (int i0 = threadIdx.x; i0 < total; i0 += blockDim.x * U) {
+    uint4 kv[U], vv[U];
+    size_t dst[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int idx = i0 + u * blockDim.x;
+      if (idx < total) {
+        const int e = idx / cpr, ch = idx % cpr;
+        const size_t src = (src_row0 + list[e]) * d + ch * 8;
+        const int rank = base_rank + e;
+        dst[u] = ((size_t)(first + rank / page_size) * page_size + rank % page_size) * d + ch * 8;
+        kv[u] = ld_nc_v4(k + src);
+        vv[u] = ld_nc_v4(v + src);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int idx = i0 + u * blockDim.x;
+      if (idx < total) {
+        *reinterpret_cast<uint4*>(k_pages + dst[u]) = kv[u];
+        *reinterpret_cast<uint4*>(v_pages + dst[u]) = vv[u];
+      }
+    }
+  }
+
+  // zero the unused rows of the row's last page (one block per row does it)
+  if (s == nseg - 1 && kept % page_size) {
+    const int pad_rows = page_size - kept % page_size;
+    const size_t base = ((size_t)(first + npages - 1) * page_size + kept % page_size) * d;
+    for (int i = threadIdx.x; i < pad_rows * cpr; i += blockDim.x) {
+      *reinterpret_cast<uint4*>(k_pages + base + (size_t)i * 8) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(v_pages + base + (size_t)i * 8) = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+}  // namespace
+
+size_t compact_workspace_bytes(int rows, int T) {
+  const int nseg = (T + kSeg - 1) / kSeg;
+  return sizeof(Plan) + sizeof(int) * ((size_t)rows * (nseg > 0 ? nseg : 1) + rows);
+}
+
+cudaError_t launch_compact(const bf16_t* k, const bf16_t* v, int rows, int T, int d,
+                           const uint8_t* mask, int page_size, bf16_t* k_pages, bf16_t* v_pages,
+                           int capacity, int* block_table, int max_pages, int* seq_lens,
+                           int* needed, void* ws, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const int nseg = T > 0 ? (T + kSeg - 1) / kSeg : 1;
+  Plan* plan = reinterpret_cast<Plan*>(ws);
+  int* seg = reinterpret_cast<int*>(plan + 1);
+  int* first = seg + (size_t)rows * nseg;
+  count_launches(3);
+  seg_count_kernel<<<dim3(nseg, rows), kSegThreads, 0, s>>>(mask, T, nseg, seg);
+  page_plan_kernel<<<1, 1024, 0, s>>>(rows, nseg, page_size, capacity, seg, first, plan, seq_lens,
+                                      needed);
+  scatter_kernel<<<dim3(nseg, rows), kSegThreads, 0, s>>>(k, v, mask, T, d, nseg, page_size, seg,
+                                                          first, plan, seq_lens, k_pages, v_pages,
+                                                          block_table, max_pages);
+  return cudaGetLastError();
+}
+
+}  // namespace kvs

@@ -1,0 +1,161 @@
+// KVzap-Linear surrogate score (KVzap review, 3.3; Algorithm 1 step 1), optionally
+// fused with the threshold rule and sliding window (KVzap review, thresholding):
+//   z[l][hk][t] = sum_c h[l][t][c] W[l][c][hk] + b[l][hk]
+//   mask = z >= tau || t >= T - w;  keep[l][hk] = count
+//
+// The op streams h (D_h bf16 per token, 8 KiB at D_h = 4096) once and is bound by
+// HBM bandwidth.  At 8 flop per byte an fp32 CUDA-core dot product would need ~75%
+// of the FMA issue rate just to keep up with HBM, so the per-token contraction
+// against the D_h x H_kv weight runs on warp MMAs (m16n8k16, N = 8 heads).  Each lane
+// loads 64 contiguous bytes of two token rows with 16-byte non-allocating loads and
+// feeds them to the MMA directly as A fragments: the reduction runs over channels,
+// so any channel permutation works as long as the B fragments (W, staged once per
+// block in shared memory) use the same one.  No shared-memory staging of h.
+#include "common.cuh"
+#include "surrogate.cuh"
+
+namespace kvs {
+namespace {
+
+constexpr int kWarps = 8;
+
+struct SurArgs {
+  const bf16_t* h;
+  const bf16_t* W;
+  const float* b;
+  float* z;
+  uint8_t* mask;
+  int* keep;
+  int T, Dh, Hkv, w, tiles_per_warp;
+  float tau;
+};
+
+// Shared layout of W: [superblock of 128 channels][n-tile][pair p][lane] x 16 bytes,
+// holding W[sb*128 + 32*t + 8*p + e][nt*8 + g] for e = 0..7 (lane = 4*g + t).
+template <int NT>
+__global__ void __launch_bounds__(kWarps * 32) surrogate_kernel(const SurArgs a) {
+  extern __shared__ uint4 wsm[];
+  const int l = blockIdx.y;
+  const int nsb = a.Dh / 128;
+  const bf16_t* Wl = a.W + (size_t)l * a.Dh * a.Hkv;
+  for (int idx = threadIdx.x; idx < nsb * NT * 128; idx += blockDim.x) {
+    const int ln = idx & 31, p = (idx >> 5) & 3, nt = (idx >> 7) % NT, sb = (idx >> 7) / NT;
+    const int head = nt * 8 + (ln >> 2);
+    const int ch0 = sb * 128 + 32 * (ln & 3) + 8 * p;
+    uint32_t wv[4];
+#pragma unroll
+    for (int e2 = 0; e2 < 4; ++e2) {
+      uint32_t lo = 0, hi = 0;
+      if (head < a.Hkv) {
+        lo = Wl[(size_t)(ch0 + 2 * e2) * a.Hkv + head];
+        hi = Wl[(size_t)(ch0 + 2 * e2 + 1) * a.Hkv + head];
+      }
+      wv[e2] = lo | (hi << 16);
+    }
+    wsm[idx] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+  }
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  const int ntile = (a.T + 15) / 16;
+  const float* bl = a.b + (size_t)l * a.Hkv;
+  int cnt[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) cnt[nt][0] = cnt[nt][1] = 0;
+
+  int tile = (blockIdx.x * kWarps + warp) * a.tiles_per_warp;
+  for (int k = 0; k < a.tiles_per_warp && tile < ntile; ++k, ++tile) {
+    const int t0 = tile * 16;
+    const int ra = min(t0 + g, a.T - 1), rb = min(t0 + g + 8, a.T - 1);
+    const bf16_t* pa = a.h + ((size_t)l * a.T + ra) * a.Dh + 32 * t4;
+    const bf16_t* pb = a.h + ((size_t)l * a.T + rb) * a.Dh + 32 * t4;
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll 2
+    for (int sb = 0; sb < nsb; ++sb) {
+      uint4 xa[4], xb[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        xa[p] = ld_nc_v4(pa + sb * 128 + 8 * p);
+        xb[p] = ld_nc_v4(pb + sb * 128 + 8 * p);
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const uint4 wv = wsm[((sb * NT + nt) * 4 + p) * 32 + lane];
+          const uint32_t A0[4] = {xa[p].x, xb[p].x, xa[p].y, xb[p].y};
+          mma_bf16_16816(acc[nt], A0, wv.x, wv.y);
+          const uint32_t A1[4] = {xa[p].z, xb[p].z, xa[p].w, xb[p].w};
+          mma_bf16_16816(acc[nt], A1, wv.z, wv.w);
+        }
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int head = nt * 8 + 2 * t4 + (e & 1);
+        const int tok = t0 + g + (e >> 1) * 8;
+        if (head < a.Hkv && tok < a.T) {
+          const float zz = acc[nt][e] + bl[head];
+          const size_t o = ((size_t)l * a.Hkv + head) * a.T + tok;
+          a.z[o] = zz;
+          if (a.mask) {
+            const int kp = (zz >= a.tau) || (tok >= a.T - a.w);
+            a.mask[o] = (uint8_t)kp;
+            cnt[nt][e & 1] += kp;
+          }
+        }
+      }
+    }
+  }
+  if (a.mask) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        int c = cnt[nt][e2];
+        c += __shfl_xor_sync(0xffffffffu, c, 4);
+        c += __shfl_xor_sync(0xffffffffu, c, 8);
+        c += __shfl_xor_sync(0xffffffffu, c, 16);
+        const int head = nt * 8 + 2 * t4 + e2;
+        if (g == 0 && head < a.Hkv && c) atomicAdd(a.keep + (size_t)l * a.Hkv + head, c);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+size_t surrogate_smem_bytes(int Dh, int Hkv) { return (size_t)Dh * ((Hkv + 7) / 8) * 16; }
+
+cudaError_t launch_surrogate(const bf16_t* h, int L, int T, int Dh, int Hkv, const bf16_t* W,
+                             const float* b, float* z, float tau, int w, uint8_t* mask,
+                             int* keep, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  if (mask) {
+    cudaError_t e = cudaMemsetAsync(keep, 0, sizeof(int) * (size_t)L * Hkv, s);
+    if (e != cudaSuccess) return e;
+  }
+  SurArgs a{h, W, b, z, mask, keep, T, Dh, Hkv, w, 8, tau};
+  const int ntile = (T + 15) / 16;
+  // fewer tiles per warp when the grid would not fill the GPU twice over
+  while (a.tiles_per_warp > 1 &&
+         (long)L * ((ntile + kWarps * a.tiles_per_warp - 1) / (kWarps * a.tiles_per_warp)) < 304)
+    a.tiles_per_warp >>= 1;
+  dim3 grid((ntile + kWarps * a.tiles_per_warp - 1) / (kWarps * a.tiles_per_warp), L);
+  const size_t smem = surrogate_smem_bytes(Dh, Hkv);
+  count_launches(1);
+  if (Hkv <= 8) {
+    cudaFuncSetAttribute(surrogate_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    surrogate_kernel<1><<<grid, kWarps * 32, smem, s>>>(a);
+  } else {
+    cudaFuncSetAttribute(surrogate_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    surrogate_kernel<2><<<grid, kWarps * 32, smem, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kvs

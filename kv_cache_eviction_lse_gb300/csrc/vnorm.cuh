@@ -1,0 +1,15 @@
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "common.cuh"
+
+namespace kvs {
+
+size_t vnorm_workspace_bytes(int L, int Hq, int d);
+
+// vn [L][Hq][T] = ||W_O^{(hq)} v_i||; G: workspace of vnorm_workspace_bytes() bytes.
+cudaError_t launch_vnorm(const bf16_t* v, int L, int Hq, int Hkv, int d, int T, int Dh,
+                         const bf16_t* w_o, float* vn, float* G, cudaStream_t s);
+
+}  // namespace kvs

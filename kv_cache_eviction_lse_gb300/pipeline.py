@@ -1,0 +1,291 @@
+"""Host orchestration of the scoring -> pruning -> compaction path, one class per workload.
+
+Each pipeline allocates its outputs and scratch once (torch, on the inputs' device) and
+``step()`` enqueues the library calls on the current stream: no arithmetic of the
+method happens here, only call sequencing and buffer management.
+
+  KVzip / KVzip+ (c1, c2)   [vnorm] -> lse -> score_max -> top-k per budget -> compact
+  chunked KVzip+  (c3)      vnorm -> per chunk (lse -> score_max, max-accumulated)
+                            -> threshold (per-layer tau) -> compact
+  KVpop target    (c4)      lse (causal self-attention) -> future_sum -> top-k per budget
+                            -> compact
+  KVzap           (c5)      surrogate (+ fused threshold) -> compact
+"""
+from __future__ import annotations
+
+import torch
+
+from . import capi as C
+from .workloads import Workload
+
+
+def _empty(shape, dtype, device):
+    return torch.empty(shape, dtype=dtype, device=device)
+
+
+class Pages:
+    """Paged cache buffers for one compaction of a [L][H][T][d] K/V pair."""
+
+    def __init__(self, L, H, T, d, page_size, device, capacity=None):
+        self.page_size = page_size
+        self.max_pages = -(-T // page_size)
+        self.capacity = capacity if capacity is not None else L * H * self.max_pages
+        self.k_pages = _empty((self.capacity, page_size, d), torch.bfloat16, device)
+        self.v_pages = _empty((self.capacity, page_size, d), torch.bfloat16, device)
+        self.block_table = _empty((L, H, self.max_pages), torch.int32, device)
+        self.seq_lens = _empty((L, H), torch.int32, device)
+        self.needed = _empty((1,), torch.int32, device)
+
+    def bytes_written(self):
+        """Algorithmic bytes a compaction writes: kept K and V rows."""
+        d = self.k_pages.shape[-1]
+        return int(self.seq_lens.sum().item()) * 2 * d * 2
+
+
+def compact_into(dm, k, v, T, mask, pages: Pages, ws):
+    C.kvs_compact_paged(dm, k, v, T, mask, pages.page_size, pages.k_pages, pages.v_pages,
+                        pages.capacity, pages.block_table, pages.max_pages, pages.seq_lens,
+                        pages.needed, ws, ws.numel())
+
+
+class KVzipPipeline:
+    """c1 / c2: KVzip (plain) or KVzip+ scoring of the context, then top-k budgets."""
+
+    def __init__(self, wl: Workload, x: dict, ratios=None):
+        self.wl, self.x = wl, x
+        dev = x["q"].device
+        L = x["q"].shape[0]
+        self.L = L
+        self.plus = "w_o" in x
+        self.dm = C.dims(L, wl.H_q, wl.H_kv, wl.d, wl.D_h if self.plus else 0)
+        self.n_q, self.n_tail = x["q"].shape[2], x["k_tail"].shape[2]
+        self.lse = _empty((L, wl.H_q, self.n_q), torch.float32, dev)
+        self.score = _empty((L, wl.H_kv, wl.T), torch.float32, dev)
+        self.vnorm = None
+        if self.plus:
+            self.vnorm = _empty((L, wl.H_q, wl.T), torch.float32, dev)
+            self.vws = _empty((C.kvs_vnorm_workspace_size(self.dm),), torch.uint8, dev)
+            self.sws = _empty((max(16, C.kvs_score_max_workspace_size(self.dm, self.n_q, 1)),),
+                              torch.uint8, dev)
+        self.ratios = tuple(ratios if ratios is not None else wl.keep_ratios)
+        self.masks = [_empty((L, wl.H_kv, wl.T), torch.uint8, dev) for _ in self.ratios]
+        self.keeps = [_empty((L, wl.H_kv), torch.int32, dev) for _ in self.ratios]
+        self.pages = [Pages(L, wl.H_kv, wl.T, wl.d, wl.page_size, dev) for _ in self.ratios]
+        self.cws = _empty((C.kvs_compact_workspace_size(self.dm, wl.T),), torch.uint8, dev)
+
+    def score_step(self):
+        if self.plus:
+            self._vnorm()
+        self._lse()
+        self._score()
+
+    def prune_step(self):
+        self._prune()
+        self._compact()
+
+    def _vnorm(self):
+        wl, x, dm = self.wl, self.x, self.dm
+        C.kvs_vnorm(dm, x["v_ctx"], wl.T, x["w_o"], self.vnorm, self.vws, self.vws.numel())
+
+    def _lse(self):
+        wl, x, dm = self.wl, self.x, self.dm
+        C.kvs_lse(dm, x["q"], self.n_q, x["k_ctx"], wl.T, x["k_tail"], self.n_tail, self.lse)
+
+    def _score(self):
+        wl, x, dm = self.wl, self.x, self.dm
+        if self.plus:
+            C.kvs_score_max(dm, x["q"], self.n_q, x["k_ctx"], wl.T, self.lse, self.vnorm, x["h"], 0,
+                            self.score, self.sws, self.sws.numel())
+        else:
+            C.kvs_score_max(dm, x["q"], self.n_q, x["k_ctx"], wl.T, self.lse, None, None, 0,
+                            self.score, None, 0)
+
+    def _prune(self):
+        wl, dm = self.wl, self.dm
+        for r, m, kp in zip(self.ratios, self.masks, self.keeps):
+            C.kvs_prune_mask(dm, self.score, wl.T, C.KVS_TOPK, 0.0, wl.topk_budget(r), wl.w, m, kp)
+
+    def _compact(self):
+        wl, x, dm = self.wl, self.x, self.dm
+        for m, pg in zip(self.masks, self.pages):
+            compact_into(dm, x["k_ctx"], x["v_ctx"], wl.T, m, pg, self.cws)
+
+    def stages(self):
+        """(name, callable) per library entry point, in step order."""
+        st = [("kvs_vnorm", self._vnorm)] if self.plus else []
+        return st + [("kvs_lse", self._lse), ("kvs_score_max", self._score),
+                     ("kvs_prune_mask", self._prune), ("kvs_compact_paged", self._compact)]
+
+    def step(self):
+        for _, fn in self.stages():
+            fn()
+
+
+class ChunkedKVzipPipeline:
+    """c3: chunked KVzip+ reconstruction, per-layer threshold tau, window w."""
+
+    def __init__(self, wl: Workload, x: dict, tau=None):
+        self.wl, self.x = wl, x
+        dev = x["k_ctx"].device
+        L = x["k_ctx"].shape[0]
+        self.L = L
+        self.dm = C.dims(L, wl.H_q, wl.H_kv, wl.d, wl.D_h)
+        self.dm1 = C.dims(1, wl.H_q, wl.H_kv, wl.d, wl.D_h)
+        self.lse = _empty((L, wl.H_q, wl.n_rep), torch.float32, dev)
+        self.score = _empty((L, wl.H_kv, wl.T), torch.float32, dev)
+        self.vnorm = _empty((L, wl.H_q, wl.T), torch.float32, dev)
+        self.vws = _empty((C.kvs_vnorm_workspace_size(self.dm),), torch.uint8, dev)
+        self.sws = _empty((max(16, C.kvs_score_max_workspace_size(self.dm, wl.n_rep, 1)),),
+                          torch.uint8, dev)
+        self.tau = tau  # per-layer list of floats, set by the caller (calibrate_tau)
+        self.mask = _empty((L, wl.H_kv, wl.T), torch.uint8, dev)
+        self.keep = _empty((L, wl.H_kv), torch.int32, dev)
+        self.pages = Pages(L, wl.H_kv, wl.T, wl.d, wl.page_size, dev)
+        self.cws = _empty((C.kvs_compact_workspace_size(self.dm, wl.T),), torch.uint8, dev)
+
+    def _vnorm(self):
+        wl, x, dm = self.wl, self.x, self.dm
+        C.kvs_vnorm(dm, x["v_ctx"], wl.T, x["w_o"], self.vnorm, self.vws, self.vws.numel())
+
+    def _lse(self, c):
+        wl, x, dm = self.wl, self.x, self.dm
+        nt = x["k_tail"][c].shape[2]
+        C.kvs_lse(dm, x["q"][c], wl.n_rep, x["k_ctx"], wl.T, x["k_tail"][c], nt, self.lse)
+
+    def _score(self, c):
+        wl, x, dm = self.wl, self.x, self.dm
+        C.kvs_score_max(dm, x["q"][c], wl.n_rep, x["k_ctx"], wl.T, self.lse, self.vnorm, x["h"][c],
+                        int(c > 0), self.score, self.sws, self.sws.numel())
+
+    def score_step(self):
+        self._vnorm()
+        for c in range(self.wl.n_chunks):
+            self._lse(c)
+            self._score(c)
+
+    def _prune(self):
+        wl = self.wl
+        for l in range(self.L):
+            C.kvs_prune_mask(self.dm1, self.score[l], wl.T, C.KVS_THRESHOLD, float(self.tau[l]), 0,
+                             wl.w, self.mask[l], self.keep[l])
+
+    def _compact(self):
+        wl, x = self.wl, self.x
+        compact_into(self.dm, x["k_ctx"], x["v_ctx"], wl.T, self.mask, self.pages, self.cws)
+
+    def prune_step(self):
+        self._prune()
+        self._compact()
+
+    def stages(self):
+        """(name, callable) per library entry point; lse and score_max cover all chunks
+        (the chunks alternate lse -> score_max, so they are timed as pairs per chunk)."""
+        def lse_all():
+            for c in range(self.wl.n_chunks):
+                self._lse(c)
+
+        def score_all():
+            for c in range(self.wl.n_chunks):
+                self._score(c)
+        return [("kvs_vnorm", self._vnorm), ("kvs_lse", lse_all), ("kvs_score_max", score_all),
+                ("kvs_prune_mask", self._prune), ("kvs_compact_paged", self._compact)]
+
+    def step(self):
+        self.score_step()
+        self.prune_step()
+
+
+class FuturePipeline:
+    """c4: KVpop future-attention target, then top-k budgets plus the window."""
+
+    def __init__(self, wl: Workload, x: dict, ratios=None):
+        self.wl, self.x = wl, x
+        dev = x["q"].device
+        L = x["q"].shape[0]
+        self.L = L
+        self.dm = C.dims(L, wl.H_q, wl.H_kv, wl.d, 0)
+        self.lse = _empty((L, wl.H_q, wl.T), torch.float32, dev)
+        self.score = _empty((L, wl.H_kv, wl.T), torch.float32, dev)
+        self.ratios = tuple(ratios if ratios is not None else wl.keep_ratios)
+        self.masks = [_empty((L, wl.H_kv, wl.T), torch.uint8, dev) for _ in self.ratios]
+        self.keeps = [_empty((L, wl.H_kv), torch.int32, dev) for _ in self.ratios]
+        self.pages = [Pages(L, wl.H_kv, wl.T, wl.d, wl.page_size, dev) for _ in self.ratios]
+        self.cws = _empty((C.kvs_compact_workspace_size(self.dm, wl.T),), torch.uint8, dev)
+
+    def _lse(self):
+        wl, x, dm = self.wl, self.x, self.dm
+        C.kvs_lse(dm, x["q"], wl.T, x["k"], wl.T, None, 0, self.lse)
+
+    def _future(self):
+        wl, x, dm = self.wl, self.x, self.dm
+        C.kvs_score_future_sum(dm, x["q"], x["k"], wl.T, self.lse, wl.w, self.score)
+
+    def _prune(self):
+        wl, dm = self.wl, self.dm
+        for r, m, kp in zip(self.ratios, self.masks, self.keeps):
+            C.kvs_prune_mask(dm, self.score, wl.T, C.KVS_TOPK, 0.0, wl.topk_budget(r), wl.w, m, kp)
+
+    def _compact(self):
+        wl, x, dm = self.wl, self.x, self.dm
+        for m, pg in zip(self.masks, self.pages):
+            compact_into(dm, x["k"], x["v"], wl.T, m, pg, self.cws)
+
+    def score_step(self):
+        self._lse()
+        self._future()
+
+    def prune_step(self):
+        self._prune()
+        self._compact()
+
+    def stages(self):
+        return [("kvs_lse", self._lse), ("kvs_score_future_sum", self._future),
+                ("kvs_prune_mask", self._prune), ("kvs_compact_paged", self._compact)]
+
+    def step(self):
+        for _, fn in self.stages():
+            fn()
+
+
+class KVzapPipeline:
+    """c5: KVzap-Linear surrogate with fused threshold + window, then compaction."""
+
+    def __init__(self, wl: Workload, x: dict):
+        self.wl, self.x = wl, x
+        dev = x["h"].device
+        L = x["h"].shape[0]
+        self.L = L
+        self.dm = C.dims(L, wl.H_q, wl.H_kv, wl.d, wl.D_h)
+        self.score = _empty((L, wl.H_kv, wl.T), torch.float32, dev)
+        self.mask = _empty((L, wl.H_kv, wl.T), torch.uint8, dev)
+        self.keep = _empty((L, wl.H_kv), torch.int32, dev)
+        self.pages = Pages(L, wl.H_kv, wl.T, wl.d, wl.page_size, dev)
+        self.cws = _empty((C.kvs_compact_workspace_size(self.dm, wl.T),), torch.uint8, dev)
+
+    def score_step(self):
+        wl, x = self.wl, self.x
+        C.kvs_surrogate(self.dm, x["h"], wl.T, x["W"], x["b"], self.score, wl.tau, wl.w, self.mask,
+                        self.keep)
+
+    def prune_step(self):
+        wl, x = self.wl, self.x
+        compact_into(self.dm, x["k"], x["v"], wl.T, self.mask, self.pages, self.cws)
+
+    def stages(self):
+        return [("kvs_surrogate", self.score_step), ("kvs_compact_paged", self.prune_step)]
+
+    def step(self):
+        self.score_step()
+        self.prune_step()
+
+
+def make_pipeline(wl: Workload, x: dict, **kw):
+    if wl.kind in ("kvzip", "kvzip_plus"):
+        return KVzipPipeline(wl, x, **kw)
+    if wl.kind == "kvzip_plus_chunked":
+        return ChunkedKVzipPipeline(wl, x, **kw)
+    if wl.kind == "future":
+        return FuturePipeline(wl, x, **kw)
+    if wl.kind == "kvzap":
+        return KVzapPipeline(wl, x, **kw)
+    raise ValueError(wl.kind)

@@ -1,0 +1,106 @@
+"""The C-ABI library builds, loads and exports every symbol include/kvs.h declares; its
+host-side validation rejects bad arguments with the documented status codes.  No GPU:
+every call here fails validation before anything is enqueued."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvs.h")
+
+
+@pytest.fixture(scope="module")
+def capi():
+    from kv_cache_eviction_lse_gb300 import build
+    build.build()
+    from kv_cache_eviction_lse_gb300 import capi as C
+    return C
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvs_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(capi):
+    syms = declared_symbols()
+    assert len(syms) >= 13
+    lib = ctypes.CDLL(capi.LIB_PATH)
+    for s in syms:
+        assert hasattr(lib, s), s
+    assert set(syms) == set(capi.EXPORTED)
+
+
+def test_version_string(capi):
+    assert "sm_103a" in capi.kvs_version()
+
+
+def _raw(capi):
+    return ctypes.CDLL(capi.LIB_PATH)
+
+
+def test_validation_codes(capi):
+    C = capi
+    lib = C._lib
+    dm = C.dims(1, 4, 2, 128, 0)
+    fake = 1 << 20  # never dereferenced: validation fails first
+    # n_q larger than keys
+    st = lib.kvs_lse(ctypes.byref(dm), fake, 100, fake, 10, fake, 5, fake, None)
+    assert st == C.KVS_ERR_SHAPE and "exceeds" in C.kvs_last_error()
+    # unsupported head dim
+    bad = C.dims(1, 4, 2, 96, 0)
+    st = lib.kvs_lse(ctypes.byref(bad), fake, 4, fake, 10, None, 0, fake, None)
+    assert st == C.KVS_ERR_UNSUPPORTED
+    # H_q not a multiple of H_kv
+    bad = C.dims(1, 5, 2, 128, 0)
+    assert lib.kvs_lse(ctypes.byref(bad), fake, 4, fake, 10, None, 0, fake, None) == C.KVS_ERR_SHAPE
+    # null output
+    assert lib.kvs_lse(ctypes.byref(dm), fake, 4, fake, 10, None, 0, None, None) == C.KVS_ERR_ARG
+    # misaligned pointer
+    assert lib.kvs_lse(ctypes.byref(dm), fake + 2, 4, fake, 10, None, 0, fake, None) == C.KVS_ERR_ALIGN
+    # null dims
+    assert lib.kvs_lse(None, fake, 4, fake, 10, None, 0, fake, None) == C.KVS_ERR_ARG
+    # bad prune mode / negative k
+    assert lib.kvs_prune_mask(ctypes.byref(dm), fake, 10, 7, 0.0, 1, 0, fake, fake, None) == C.KVS_ERR_ARG
+    assert lib.kvs_prune_mask(ctypes.byref(dm), fake, 10, 1, 0.0, -1, 0, fake, fake, None) == C.KVS_ERR_ARG
+    # workspace too small
+    dmh = C.dims(1, 4, 2, 128, 64)
+    need = lib.kvs_vnorm_workspace_size(ctypes.byref(dmh))
+    assert need == 4 * 128 * 128 * 4
+    st = lib.kvs_vnorm(ctypes.byref(dmh), fake, 10, fake, fake, fake, need - 16, None)
+    assert st == C.KVS_ERR_CAPACITY
+    # surrogate limits
+    big = C.dims(1, 32, 32, 128, 4096)
+    assert lib.kvs_surrogate(ctypes.byref(big), fake, 10, fake, fake, fake, 0.0, 0, None, None,
+                             None) == C.KVS_ERR_UNSUPPORTED
+    odd = C.dims(1, 8, 8, 128, 100)
+    assert lib.kvs_surrogate(ctypes.byref(odd), fake, 10, fake, fake, fake, 0.0, 0, None, None,
+                             None) == C.KVS_ERR_UNSUPPORTED
+    # compaction: max_pages too small, bad page size
+    st = lib.kvs_compact_paged(ctypes.byref(dm), fake, fake, 100, fake, 16, fake, fake, 10, fake, 6,
+                               fake, fake, fake, 1 << 20, None)
+    assert st == C.KVS_ERR_SHAPE
+    st = lib.kvs_compact_paged(ctypes.byref(dm), fake, fake, 100, fake, 0, fake, fake, 10, fake, 7,
+                               fake, fake, fake, 1 << 20, None)
+    assert st == C.KVS_ERR_UNSUPPORTED
+
+
+def test_workspace_sizes(capi):
+    C = capi
+    dm = C.dims(36, 32, 8, 128, 4096)
+    assert C.kvs_vnorm_workspace_size(dm) == 36 * 32 * 128 * 128 * 4
+    assert C.kvs_score_max_workspace_size(dm, 2048, 1) == 36 * 2048 * 4
+    assert C.kvs_score_max_workspace_size(dm, 2048, 0) == 0
+    assert C.kvs_compact_workspace_size(dm, 32768) >= 36 * 8 * (8 + 1) * 4
+
+
+def test_binding_rejects_host_tensors(capi):
+    import torch
+    C = capi
+    dm = C.dims(1, 2, 1, 64, 0)
+    q = torch.zeros(1, 2, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        C.kvs_lse(dm, q, 4, q, 4, None, 0, q, stream=0)

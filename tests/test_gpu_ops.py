@@ -1,0 +1,249 @@
+"""Per-entry-point parity of the CUDA path against the fp64 oracle, element by element,
+at sizes that span several tiles with ragged tails, plus the degenerate cases."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tests.gpu_util import (LOG_SCORE_ATOL, LSE_ATOL, MASK_BAND, SCORE_RTOL, assert_close_abs,
+                            assert_close_rel, assert_masks_match_near, cuda, f64, need_gpu)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def C():
+    need_gpu()
+    from kv_cache_eviction_lse_gb300 import build
+    build.build()
+    from kv_cache_eviction_lse_gb300 import capi
+    return capi
+
+
+def _inputs(L, Hkv, Hq, d, T, n_tail, n_q, seed, scale=1.0, D_h=0):
+    from kv_cache_eviction_lse_gb300.workloads import random_kv_inputs
+    return random_kv_inputs(L, Hkv, Hq, d, T, n_tail, n_q, seed, scale=scale, D_h=D_h)
+
+
+LSE_SHAPES = [
+    # L, Hkv, Hq, d, T, n_tail, n_q
+    (2, 2, 6, 128, 150, 79, 70),
+    (1, 1, 2, 64, 256, 264, 256),
+    (2, 2, 4, 128, 200, 0, 200),     # causal self-attention
+    (1, 3, 3, 64, 1, 0, 1),          # single key
+    (1, 1, 4, 128, 0, 97, 97),       # no context keys
+    (3, 1, 2, 128, 333, 5, 1),       # one query
+]
+
+
+@pytest.mark.parametrize("shape", LSE_SHAPES, ids=[str(s) for s in LSE_SHAPES])
+@pytest.mark.parametrize("scale", [1.0, 2.5])
+def test_lse(C, shape, scale):
+    L, Hkv, Hq, d, T, nt, nq = shape
+    x = _inputs(*shape, seed=11 + T + nq, scale=scale)
+    g = cuda(x)
+    out = torch.full((L, Hq, nq), float("nan"), device="cuda")
+    C.kvs_lse(C.dims(L, Hq, Hkv, d), g["q"], nq, g["k_ctx"] if T else None, T,
+              g["k_tail"] if nt else None, nt, out)
+    torch.cuda.synchronize()
+    want = O.lse(f64(x["q"]), f64(x["k_ctx"]), f64(x["k_tail"]))
+    assert_close_abs(out.cpu().numpy(), want, LSE_ATOL, "lse")
+
+
+SCORE_SHAPES = [
+    (2, 2, 6, 128, 150, 79, 70, 192),
+    (1, 1, 2, 64, 256, 264, 256, 0),
+    (2, 4, 8, 128, 77, 40, 33, 128),
+    (1, 2, 2, 64, 1, 3, 2, 64),
+]
+
+
+@pytest.mark.parametrize("shape", SCORE_SHAPES, ids=[str(s) for s in SCORE_SHAPES])
+def test_vnorm_lse_score_max(C, shape):
+    L, Hkv, Hq, d, T, nt, nq, Dh = shape
+    x = _inputs(L, Hkv, Hq, d, T, nt, nq, seed=5 + T, scale=1.5, D_h=Dh)
+    g = cuda(x)
+    dm = C.dims(L, Hq, Hkv, d, Dh)
+    lse = torch.empty((L, Hq, nq), device="cuda")
+    C.kvs_lse(dm, g["q"], nq, g["k_ctx"], T, g["k_tail"], nt, lse)
+    score = torch.empty((L, Hkv, T), device="cuda")
+    vn = None
+    if Dh:
+        vn = torch.empty((L, Hq, T), device="cuda")
+        ws = torch.empty(C.kvs_vnorm_workspace_size(dm), dtype=torch.uint8, device="cuda")
+        C.kvs_vnorm(dm, g["v_ctx"], T, g["w_o"], vn, ws, ws.numel())
+        sws = torch.empty(C.kvs_score_max_workspace_size(dm, nq, 1), dtype=torch.uint8, device="cuda")
+        C.kvs_score_max(dm, g["q"], nq, g["k_ctx"], T, lse, vn, g["h"], 0, score, sws, sws.numel())
+    else:
+        C.kvs_score_max(dm, g["q"], nq, g["k_ctx"], T, lse, None, None, 0, score, None, 0)
+    torch.cuda.synchronize()
+    q, kc, kt = f64(x["q"]), f64(x["k_ctx"]), f64(x["k_tail"])
+    vref = O.value_norm(f64(x["v_ctx"]), f64(x["w_o"]), Hq) if Dh else None
+    if Dh:
+        assert_close_rel(vn.cpu().numpy(), vref, 1e-4, "vnorm")
+    want = O.kvzip_score(q, kc, kt, vnorm=vref, h=f64(x["h"]) if Dh else None)
+    assert_close_abs(score.cpu().numpy(), want, LOG_SCORE_ATOL, "log score")
+
+
+def test_score_max_accumulate(C):
+    L, Hkv, Hq, d, T, nt, nq = 1, 2, 4, 128, 100, 50, 40
+    xa = _inputs(L, Hkv, Hq, d, T, nt, nq, seed=1)
+    xb = _inputs(L, Hkv, Hq, d, T, nt, nq, seed=2)
+    xb["k_ctx"] = xa["k_ctx"]
+    dm = C.dims(L, Hq, Hkv, d)
+    score = torch.empty((L, Hkv, T), device="cuda")
+    for i, x in enumerate((xa, xb)):
+        g = cuda(x)
+        lse = torch.empty((L, Hq, nq), device="cuda")
+        C.kvs_lse(dm, g["q"], nq, g["k_ctx"], T, g["k_tail"], nt, lse)
+        C.kvs_score_max(dm, g["q"], nq, g["k_ctx"], T, lse, None, None, i, score, None, 0)
+    torch.cuda.synchronize()
+    want = O.kvzip_score_chunked([f64(xa["q"]), f64(xb["q"])], f64(xa["k_ctx"]),
+                                 [f64(xa["k_tail"]), f64(xb["k_tail"])])
+    assert_close_abs(score.cpu().numpy(), want, LOG_SCORE_ATOL, "accumulated log score")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("T,w", [(333, 0), (333, 17), (333, 128), (333, 400), (64, 1), (1, 0)])
+def test_future_sum(C, d, T, w):
+    L, Hkv, Hq = 2, 2, 4
+    x = _inputs(L, Hkv, Hq, d, T, 0, T, seed=T + w + d, scale=1.5)
+    g = cuda(x)
+    dm = C.dims(L, Hq, Hkv, d)
+    lse = torch.empty((L, Hq, T), device="cuda")
+    C.kvs_lse(dm, g["q"], T, g["k_ctx"], T, None, 0, lse)
+    f = torch.full((L, Hkv, T), float("nan"), device="cuda")
+    C.kvs_score_future_sum(dm, g["q"], g["k_ctx"], T, lse, w, f)
+    torch.cuda.synchronize()
+    want = O.future_attention_mass(f64(x["q"]), f64(x["k_ctx"]), w)
+    got = f.cpu().numpy()
+    assert_close_rel(got, want, SCORE_RTOL, "future mass")
+    assert (got[..., max(0, T - w):] == 0).all()
+
+
+@pytest.mark.parametrize("Hkv", [8, 3, 12])
+@pytest.mark.parametrize("T", [1000, 16, 1])
+def test_surrogate(C, Hkv, T):
+    L, Dh, w, tau = 2, 256, 7, -4.5
+    gen = torch.Generator().manual_seed(Hkv * 1000 + T)
+    h = torch.randn(L, T, Dh, generator=gen).to(torch.bfloat16)
+    W = (torch.randn(L, Dh, Hkv, generator=gen) / 16).to(torch.bfloat16)
+    b = torch.randn(L, Hkv, generator=gen) - 4.0
+    dm = C.dims(L, Hkv, Hkv, 128, Dh)
+    z = torch.empty(L, Hkv, T, device="cuda")
+    mask = torch.empty(L, Hkv, T, dtype=torch.uint8, device="cuda")
+    keep = torch.full((L, Hkv), -7, dtype=torch.int32, device="cuda")
+    C.kvs_surrogate(dm, h.cuda(), T, W.cuda(), b.cuda(), z, tau, w, mask, keep)
+    z2 = torch.empty_like(z)
+    C.kvs_surrogate(dm, h.cuda(), T, W.cuda(), b.cuda(), z2)  # unfused
+    torch.cuda.synchronize()
+    want = O.linear_surrogate(f64(h), f64(W), b.double().numpy())
+    zg = z.cpu().numpy()
+    assert_close_abs(zg, want, LOG_SCORE_ATOL, "surrogate")
+    assert np.array_equal(zg, z2.cpu().numpy())
+    # the fused decision matches the threshold rule applied to the kernel's own fp32 scores
+    m_same, k_same = O.prune_threshold(zg.astype(np.float64), np.float32(tau), w)
+    assert np.array_equal(mask.cpu().numpy(), m_same)
+    assert np.array_equal(keep.cpu().numpy(), k_same)
+    # and the oracle's decision except next to tau
+    m_ref, _ = O.prune_threshold(want, tau, w)
+    assert_masks_match_near(mask.cpu().numpy(), m_ref, want, np.full(want.shape[:-1], tau),
+                            MASK_BAND, "surrogate mask", log_domain=True)
+
+
+def _scores_with_ties(shape, seed, levels=None, nan_frac=0.0):
+    r = np.random.default_rng(seed)
+    s = r.normal(size=shape).astype(np.float32)
+    if levels:
+        s = np.round(s * levels).astype(np.float32) / levels
+    if nan_frac:
+        s[r.random(shape) < nan_frac] = np.nan
+    return s
+
+
+@pytest.mark.parametrize("T", [1, 7, 300, 2048, 5000])
+@pytest.mark.parametrize("levels,nan_frac", [(None, 0.0), (3, 0.0), (4, 0.05)])
+def test_prune_threshold_exact(C, T, levels, nan_frac):
+    L, H = 2, 3
+    s = _scores_with_ties((L, H, T), T, levels, nan_frac)
+    for tau, w in [(0.0, 0), (0.25, 5), (-np.inf, 0), (np.inf, 3), (0.5, T), (0.0, T + 4)]:
+        mask = torch.empty(L, H, T, dtype=torch.uint8, device="cuda")
+        keep = torch.empty(L, H, dtype=torch.int32, device="cuda")
+        C.kvs_prune_mask(C.dims(L, H, H, 128), torch.from_numpy(s).cuda(), T, C.KVS_THRESHOLD,
+                         tau, 0, w, mask, keep)
+        torch.cuda.synchronize()
+        m_ref, k_ref = O.prune_threshold(s.astype(np.float64), tau, w)
+        assert np.array_equal(mask.cpu().numpy(), m_ref), (tau, w)
+        assert np.array_equal(keep.cpu().numpy(), k_ref), (tau, w)
+
+
+@pytest.mark.parametrize("T", [1, 7, 300, 2048, 16384])
+@pytest.mark.parametrize("levels,nan_frac", [(None, 0.0), (3, 0.0), (4, 0.05)])
+def test_prune_topk_exact(C, T, levels, nan_frac):
+    L, H = 2, 3
+    s = _scores_with_ties((L, H, T), T + 1, levels, nan_frac)
+    for k, w in [(0, 0), (1, 0), (T // 4, 0), (T // 4, 16), (T // 2, T // 3), (T, 0), (T - 5, 5),
+                 (T + 3, 2), (3, T), (2, T + 9)]:
+        if k < 0:
+            continue
+        mask = torch.empty(L, H, T, dtype=torch.uint8, device="cuda")
+        keep = torch.empty(L, H, dtype=torch.int32, device="cuda")
+        C.kvs_prune_mask(C.dims(L, H, H, 128), torch.from_numpy(s).cuda(), T, C.KVS_TOPK, 0.0, k,
+                         w, mask, keep)
+        torch.cuda.synchronize()
+        m_ref, k_ref = O.prune_topk(s.astype(np.float64), k, w)
+        assert np.array_equal(mask.cpu().numpy(), m_ref), (k, w)
+        assert np.array_equal(keep.cpu().numpy(), k_ref), (k, w)
+
+
+@pytest.mark.parametrize("T,page", [(1, 16), (100, 16), (4096, 16), (5000, 16), (9000, 7),
+                                    (333, 1), (17, 4096)])
+@pytest.mark.parametrize("d", [64, 128])
+def test_compact_exact(C, T, page, d):
+    L, H = 2, 3
+    r = np.random.default_rng(T + page + d)
+    p_keep = r.uniform(0.0, 1.0, size=(L, H, 1))
+    mask = (r.random((L, H, T)) < p_keep).astype(np.uint8)
+    mask[0, 0] = 1
+    mask[1, 2] = 0
+    gen = torch.Generator().manual_seed(T)
+    k = torch.randn(L, H, T, d, generator=gen).to(torch.bfloat16)
+    v = torch.randn(L, H, T, d, generator=gen).to(torch.bfloat16)
+    from kv_cache_eviction_lse_gb300.pipeline import Pages, compact_into
+    dm = C.dims(L, H, H, d)
+    pages = Pages(L, H, T, d, page, "cuda")
+    pages.k_pages.fill_(7.0)
+    pages.v_pages.fill_(7.0)
+    ws = torch.empty(C.kvs_compact_workspace_size(dm, T), dtype=torch.uint8, device="cuda")
+    compact_into(dm, k.cuda(), v.cuda(), T, torch.from_numpy(mask).cuda(), pages, ws)
+    torch.cuda.synchronize()
+    kb = k.view(torch.int16).numpy()
+    vb = v.view(torch.int16).numpy()
+    kp, vp, bt, sl, tot = O.compact_paged(kb, vb, mask, page, pages.max_pages)
+    assert int(pages.needed.item()) == tot
+    assert np.array_equal(pages.seq_lens.cpu().numpy(), sl)
+    assert np.array_equal(pages.block_table.cpu().numpy(), bt)
+    assert np.array_equal(pages.k_pages[:tot].cpu().view(torch.int16).numpy(), kp)
+    assert np.array_equal(pages.v_pages[:tot].cpu().view(torch.int16).numpy(), vp)
+    # pages past the total are untouched
+    if tot < pages.capacity:
+        assert bool((pages.k_pages[tot:] == 7.0).all())
+
+
+def test_compact_capacity_overflow(C):
+    L, H, T, d, page = 1, 2, 100, 128, 16
+    mask = torch.ones(L, H, T, dtype=torch.uint8)
+    k = torch.randn(L, H, T, d).to(torch.bfloat16).cuda()
+    from kv_cache_eviction_lse_gb300.pipeline import Pages, compact_into
+    dm = C.dims(L, H, H, d)
+    pages = Pages(L, H, T, d, page, "cuda", capacity=5)
+    pages.k_pages.fill_(3.0)
+    ws = torch.empty(C.kvs_compact_workspace_size(dm, T), dtype=torch.uint8, device="cuda")
+    compact_into(dm, k, k, T, mask.cuda(), pages, ws)
+    torch.cuda.synchronize()
+    assert int(pages.needed.item()) == 14
+    assert bool((pages.block_table == -1).all())
+    assert pages.seq_lens.cpu().tolist() == [[100, 100]]
+    assert bool((pages.k_pages == 3.0).all())

@@ -1,0 +1,175 @@
+"""Parity of the whole path on the five workloads at their full sizes, in the launch
+configuration the benchmark times (every layer in one call).  The oracle checks sampled
+outputs it can afford: all of c1, layers {0, 27} of c2, layer 0 / KV head 0 of c3 and
+c4, layer 0 of c5; compaction is checked bit-exactly given the kernel's mask."""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tests.gpu_util import (LOG_SCORE_ATOL, LSE_ATOL, MASK_BAND, SCORE_RTOL, assert_close_abs,
+                            assert_close_rel, assert_masks_match_near, cuda, f64, kth_value,
+                            need_gpu)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mods():
+    need_gpu()
+    from kv_cache_eviction_lse_gb300 import build
+    build.build()
+    from kv_cache_eviction_lse_gb300 import pipeline, workloads
+    return pipeline, workloads
+
+
+@pytest.fixture(autouse=True)
+def _free():
+    yield
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def _check_pages(pages, l, h, k, v, mask_lh):
+    """Compaction of one (layer, head) row is bit-exact given the kernel's mask."""
+    kb = k.contiguous().view(torch.int16).numpy()[None, None]
+    vb = v.contiguous().view(torch.int16).numpy()[None, None]
+    kp, vp, bt, sl, tot = O.compact_paged(kb, vb, mask_lh[None, None], pages.page_size,
+                                          pages.max_pages)
+    assert int(pages.seq_lens[l, h].item()) == int(sl[0, 0])
+    ids = pages.block_table[l, h].cpu().numpy()
+    n = int((ids >= 0).sum())
+    assert n == tot and (ids[n:] == -1).all()
+    assert (np.diff(ids[:n]) == 1).all() if n > 1 else True
+    got_k = pages.k_pages[ids[:n]].cpu().view(torch.int16).numpy()
+    got_v = pages.v_pages[ids[:n]].cpu().view(torch.int16).numpy()
+    assert np.array_equal(got_k, kp) and np.array_equal(got_v, vp)
+
+
+def test_c1_full(mods):
+    pipeline, W = mods
+    wl = W.WORKLOADS["c1"]
+    x = W.generate(wl)
+    p = pipeline.make_pipeline(wl, cuda(x))
+    p.step()
+    torch.cuda.synchronize()
+    q, kc, kt = f64(x["q"]), f64(x["k_ctx"]), f64(x["k_tail"])
+    lse = O.lse(q, kc, kt)
+    assert_close_abs(p.lse.cpu().numpy(), lse, LSE_ATOL, "c1 lse")
+    s = O.kvzip_score(q, kc, kt, lse_=lse)
+    assert_close_abs(p.score.cpu().numpy(), s, LOG_SCORE_ATOL, "c1 log score")
+    k = wl.topk_budget(0.25)
+    m_ref, k_ref = O.prune_topk(s, k, wl.w)
+    assert (p.keeps[0].cpu().numpy() == k + wl.w).all() and (k_ref == k + wl.w).all()
+    assert_masks_match_near(p.masks[0].cpu().numpy(), m_ref, s, kth_value(s, k, wl.w), MASK_BAND,
+                            "c1 mask", log_domain=True)
+    _check_pages(p.pages[0], 0, 0, x["k_ctx"][0, 0], x["v_ctx"][0, 0], p.masks[0][0, 0].cpu().numpy())
+
+
+def test_c2_full(mods):
+    pipeline, W = mods
+    wl = W.WORKLOADS["c2"]
+    x = W.generate(wl)
+    p = pipeline.make_pipeline(wl, cuda(x))
+    p.step()
+    torch.cuda.synchronize()
+    for l in (0, wl.L - 1):
+        sl = slice(l, l + 1)
+        q, kc, kt = f64(x["q"][sl]), f64(x["k_ctx"][sl]), f64(x["k_tail"][sl])
+        lse = O.lse(q, kc, kt)
+        assert_close_abs(p.lse[sl].cpu().numpy(), lse, LSE_ATOL, f"c2 lse layer {l}")
+        vn = O.value_norm(f64(x["v_ctx"][sl]), f64(x["w_o"][sl]), wl.H_q)
+        assert_close_rel(p.vnorm[sl].cpu().numpy(), vn, 1e-4, f"c2 vnorm layer {l}")
+        s = O.kvzip_score(q, kc, kt, lse_=lse, vnorm=vn, h=f64(x["h"][sl]))
+        assert_close_abs(p.score[sl].cpu().numpy(), s, LOG_SCORE_ATOL, f"c2 log score layer {l}")
+        for r, m, kp, pg in zip(p.ratios, p.masks, p.keeps, p.pages):
+            k = wl.topk_budget(r)
+            m_ref, k_ref = O.prune_topk(s, k, wl.w)
+            assert np.array_equal(kp[sl].cpu().numpy(), k_ref)
+            assert_masks_match_near(m[sl].cpu().numpy(), m_ref, s, kth_value(s, k, wl.w),
+                                    MASK_BAND, f"c2 mask r={r} layer {l}", log_domain=True)
+            for h in range(wl.H_kv):
+                _check_pages(pg, l, h, x["k_ctx"][l, h], x["v_ctx"][l, h], m[l, h].cpu().numpy())
+
+
+def test_c3_full_layer0_head0(mods):
+    pipeline, W = mods
+    wl = W.WORKLOADS["c3"]
+    x = W.generate(wl, device="cuda")
+    p = pipeline.make_pipeline(wl, x)
+    p.score_step()
+    torch.cuda.synchronize()
+    g = wl.g
+    hs = slice(0, g)
+    d = wl.d
+    qs = [f64(x["q"][c][0:1, hs]) for c in range(wl.n_chunks)]
+    tails = [f64(x["k_tail"][c][0:1, 0:1]) for c in range(wl.n_chunks)]
+    hh = [f64(x["h"][c][0:1]) for c in range(wl.n_chunks)]
+    kc = f64(x["k_ctx"][0:1, 0:1])
+    vn = O.value_norm(f64(x["v_ctx"][0:1, 0:1]), f64(x["w_o"][0:1, :, 0:g * d]), g)
+    assert_close_rel(p.vnorm[0:1, hs].cpu().numpy(), vn, 1e-4, "c3 vnorm")
+    s = O.kvzip_score_chunked(qs, kc, tails, vnorm=vn, h_chunks=hh)
+    got = p.score[0:1, 0:1].cpu().numpy()
+    assert_close_abs(got, s, LOG_SCORE_ATOL, "c3 log score (layer 0, head 0)")
+    # threshold at the 25th percentile of the non-window scores (of this sampled row)
+    tau0 = O.quantile_lower(s[..., : wl.T - wl.w], wl.tau_quantile)
+    taus = [tau0] + [float(torch.quantile(p.score[l, :, : wl.T - wl.w].flatten()[:16_000_000], 0.25))
+                     for l in range(1, wl.L)]
+    p.tau = taus
+    p.prune_step()
+    torch.cuda.synchronize()
+    m_ref, _ = O.prune_threshold(s, tau0, wl.w)
+    assert_masks_match_near(p.mask[0:1, 0:1].cpu().numpy(), m_ref, s, np.full((1, 1), tau0),
+                            MASK_BAND, "c3 mask", log_domain=True)
+    _check_pages(p.pages, 0, 0, x["k_ctx"][0, 0].cpu(), x["v_ctx"][0, 0].cpu(),
+                 p.mask[0, 0].cpu().numpy())
+
+
+def test_c4_full_layer0_head0(mods):
+    pipeline, W = mods
+    wl = W.WORKLOADS["c4"]
+    x = W.generate(wl, device="cuda")
+    p = pipeline.make_pipeline(wl, x)
+    p.step()
+    torch.cuda.synchronize()
+    g = wl.g
+    q = f64(x["q"][0:1, 0:g])
+    k = f64(x["k"][0:1, 0:1])
+    lse = O.lse(q, k, None)
+    assert_close_abs(p.lse[0:1, 0:g].cpu().numpy(), lse, LSE_ATOL, "c4 lse")
+    f = O.future_attention_mass(q, k, wl.w, lse_=lse)
+    assert_close_rel(p.score[0:1, 0:1].cpu().numpy(), f, SCORE_RTOL, "c4 future mass")
+    for r, m, kp, pg in zip(p.ratios, p.masks, p.keeps, p.pages):
+        kk = wl.topk_budget(r)
+        m_ref, k_ref = O.prune_topk(f, kk, wl.w)
+        assert int(kp[0, 0].item()) == int(k_ref[0, 0]) == kk + wl.w
+        assert_masks_match_near(m[0:1, 0:1].cpu().numpy(), m_ref, f, kth_value(f, kk, wl.w),
+                                MASK_BAND, f"c4 mask r={r}", log_domain=False)
+        _check_pages(pg, 0, 0, x["k"][0, 0].cpu(), x["v"][0, 0].cpu(), m[0, 0].cpu().numpy())
+
+
+def test_c5_full_layer0(mods):
+    pipeline, W = mods
+    wl = W.WORKLOADS["c5"]
+    x = W.generate(wl, device="cuda")
+    p = pipeline.make_pipeline(wl, x)
+    p.step()
+    torch.cuda.synchronize()
+    z = O.linear_surrogate(f64(x["h"][0:1]), f64(x["W"][0:1]), x["b"][0:1].double().cpu().numpy())
+    zg = p.score[0:1].cpu().numpy()
+    assert_close_abs(zg, z, LOG_SCORE_ATOL, "c5 surrogate")
+    m_ref, _ = O.prune_threshold(z, wl.tau, wl.w)
+    mg = p.mask[0:1].cpu().numpy()
+    assert_masks_match_near(mg, m_ref, z, np.full(z.shape[:-1], wl.tau), MASK_BAND, "c5 mask",
+                            log_domain=True)
+    assert np.array_equal(p.keep[0:1].cpu().numpy(), mg.sum(-1))
+    for h in range(wl.H_kv):
+        _check_pages(p.pages, 0, h, x["k"][0, h].cpu(), x["v"][0, h].cpu(), mg[0, h])
+    # the page plan covers every layer: offsets are the prefix sum of ceil(keep/16)
+    sl = p.pages.seq_lens.cpu().numpy().ravel()
+    first = p.pages.block_table[:, :, 0].cpu().numpy().ravel()
+    npg = -(-sl // wl.page_size)
+    assert np.array_equal(first[npg > 0], (np.cumsum(npg) - npg)[npg > 0])
+    assert int(p.pages.needed.item()) == int(npg.sum())
