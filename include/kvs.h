@@ -152,12 +152,13 @@ kvs_status kvs_score_future_sum(const kvs_dims* dims, const kvs_bf16* q, const k
  *
  * W_O^{(hq)} is the d-column slice hq*d .. hq*d+d-1 of the output projection
  * o_proj.weight [D_h][H_q*d].  Computed through the Gram matrix
- * G_hq = W_O^{(hq)T} W_O^{(hq)} (d x d, fp32, kept in the workspace) as sqrt(v^T G v).
+ * G_hq = W_O^{(hq)T} W_O^{(hq)} (d x d, kept in the workspace as a pair of bf16
+ * matrices whose sum carries G to ~2^-17 relative) as sqrt(v^T G v).
  *
  *   v     [L][H_kv][T][d]   bf16
  *   w_o   [L][D_h][H_q*d]   bf16
  *   vnorm [L][H_q][T]       fp32 output
- *   ws    scratch of kvs_vnorm_workspace_size() bytes (L*H_q*d*d floats)
+ *   ws    scratch of kvs_vnorm_workspace_size() bytes (4*L*H_q*d*d)
  * ------------------------------------------------------------------------------- */
 size_t kvs_vnorm_workspace_size(const kvs_dims* dims);
 kvs_status kvs_vnorm(const kvs_dims* dims, const kvs_bf16* v, int32_t T, const kvs_bf16* w_o,

@@ -91,10 +91,10 @@ uint64_t kvs_launch_count(void) { return kvs::g_launches.load(std::memory_order_
 
 kvs_status kvs_device_error(int32_t* code_out, int32_t clear, void* stream) {
   REQUIRE(code_out, KVS_ERR_ARG, "kvs_device_error: code_out is NULL");
-  cudaError_t e = cudaStreamSynchronize(as_stream(stream));
+  int code = 0;
+  cudaError_t e = kvs::attn_device_error(&code, clear != 0, as_stream(stream));
   if (e != cudaSuccess) return cuda_status(e, "kvs_device_error");
-  *code_out = 0;
-  (void)clear;
+  *code_out = code;
   return ok();
 }
 
@@ -200,7 +200,7 @@ kvs_status kvs_vnorm(const kvs_dims* dims, const kvs_bf16* v, int32_t T, const k
   REQUIRE(ws_bytes >= need, KVS_ERR_CAPACITY, "kvs_vnorm: workspace of %zu bytes, %zu needed",
           ws_bytes, need);
   return cuda_status(kvs::launch_vnorm(v, dims->L, dims->H_q, dims->H_kv, dims->d, T, dims->D_h,
-                                       w_o, vnorm, static_cast<float*>(ws), as_stream(stream)),
+                                       w_o, vnorm, ws, as_stream(stream)),
                      "kvs_vnorm");
 }
 

@@ -25,6 +25,9 @@ cudaError_t launch_lse(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_score_max(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_future_sum(const AttnArgs& a, cudaStream_t s);
 
+// Reads (and with `clear` resets) the device error word of the scoring kernels.
+cudaError_t attn_device_error(int* code, bool clear, cudaStream_t s);
+
 // hlog[l][j] = ln ||h[l][j]||_2 over D_h bf16 channels.
 cudaError_t launch_hidden_log_norm(const bf16_t* h, int L, int n, int Dh, float* hlog,
                                    cudaStream_t s);

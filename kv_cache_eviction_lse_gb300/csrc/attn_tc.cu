@@ -1,0 +1,472 @@
+// Attention-scoring passes on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Pass 1 (LSE) and pass 2 (transposed scoring) share one warp-specialised CTA:
+//   warp 0      TMA producer: loads the CTA's 128-row A tile once, then streams 128-row
+//               B tiles through a STAGES-deep ring of 128-byte-swizzled smem buffers
+//   warp 1      allocates 256 TMEM columns and issues tcgen05.mma (M=128, N=128, K=16,
+//               bf16 x bf16 -> fp32) into one of two TMEM accumulators per B tile
+//   warps 2-5   epilogue: one thread per accumulator row (TMEM lane) reads the 128
+//               columns with tcgen05.ld and reduces them in registers; the other
+//               accumulator is being filled by the MMA meanwhile
+// Modes (x = q.k / sqrt(d), never written to memory):
+//   kLse     A = 128 queries,  B = key tiles (context, then tail): online max and
+//            sum of 2^(x log2 e) per query -> ln sum exp(x)
+//   kMax     A = 128 context keys, B = query tiles of every head of the group: per key
+//            max of x - lse_j - ln||h_j||, folded per head with ln ||W_O^{(h)} v_i||
+//   kFuture  A = 128 keys, B = query tiles j >= i0 + w: per key sum over the group of
+//            2^((x - lse_j) log2 e) for j >= i + w
+// Sources: KVpop review, 1. Key Terms (LSE reuse, transposed-attention pass);
+// KVzap review, 3.1 Eq. 1 and 3.2 Eq. 3.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math_constants.h>
+
+#include "attn.cuh"
+#include "tc.cuh"
+
+namespace kvs {
+
+__device__ int g_attn_error = 0;
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int kThreads = 192;
+constexpr int kEpi = 128;
+constexpr uint32_t kBoxBytes = 128 * 128;  // 128 rows x 64 bf16 (one 128-byte swizzle span)
+constexpr uint32_t kTmemCols = 2 * BN;
+constexpr int kErrWaitTimeout = 1;  // a bounded mbarrier wait ran out
+
+enum Mode { kLse = 0, kMax = 1, kFuture = 2 };
+
+template <int D>
+struct Cfg {
+  static constexpr int KH = D / 64;
+  static constexpr int STAGES = D == 128 ? 4 : 6;
+  static constexpr uint32_t A_BYTES = KH * kBoxBytes;
+  static constexpr uint32_t B_BYTES = KH * kBoxBytes;
+  static constexpr uint32_t OFF_B = A_BYTES;
+  static constexpr uint32_t OFF_C = OFF_B + STAGES * B_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_C + 2 * BN * 4;
+  static constexpr uint32_t NBAR = 1 + 2 * STAGES + 4;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
+  static constexpr uint32_t IDESC = tc::idesc_bf16(BM, BN);
+};
+
+__device__ __forceinline__ void fail(volatile uint32_t* abort_flag, int code) {
+  *abort_flag = 1u;
+  atomicCAS(&g_attn_error, 0, code);
+}
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                   const __grid_constant__ CUtensorMap tm_b2, const AttnArgs a) {
+  using C = Cfg<D>;
+  constexpr int S = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sb = raw + pad;
+  const uint32_t sA = sb, sB = sb + C::OFF_B;
+  float* cbuf = reinterpret_cast<float*>(smem + C::OFF_C);
+  const uint32_t bar_a = sb + C::OFF_BAR;
+  auto bar_full = [&](int s) { return bar_a + 8u * (1 + s); };
+  auto bar_empty = [&](int s) { return bar_a + 8u * (1 + S + s); };
+  auto bar_tfull = [&](int x) { return bar_a + 8u * (1 + 2 * S + x); };
+  auto bar_tempty = [&](int x) { return bar_a + 8u * (3 + 2 * S + x); };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile uint32_t* abort_flag = misc + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int l = blockIdx.z;
+  const int G = a.Hq / a.Hkv;
+  const int n_k = a.T + a.n_tail;
+  const int off = n_k - a.n_q;
+  const float scale = rsqrtf((float)D);
+  const float sc2 = scale * kLog2e;
+  const int row0 = blockIdx.x * BM;
+  const int hq_a = (MODE == kLse) ? (int)blockIdx.y : 0;
+  const int hk = (MODE == kLse) ? hq_a / G : (int)blockIdx.y;
+
+  // ---------------------------------------------------------------- tile space of B
+  int ntiles, n_ctx = 0, per_head = 1, qt_begin = 0;
+  if (MODE == kLse) {
+    const int j_last = min(row0 + BM, a.n_q) - 1;
+    const int kv_end = off + j_last + 1;  // keys [0, kv_end) are visible to some query
+    n_ctx = (min(a.T, kv_end) + BN - 1) / BN;
+    const int tail_need = min(a.n_tail, max(0, kv_end - a.T));
+    ntiles = n_ctx + (tail_need + BN - 1) / BN;
+  } else {
+    const int nqt = (a.n_q + BN - 1) / BN;
+    if (MODE == kFuture) qt_begin = (row0 + a.w) / BN;
+    per_head = max(0, nqt - qt_begin);
+    ntiles = G * per_head;
+  }
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(bar_a, 1);
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(bar_full(s), 1);
+      tc::mbar_init(bar_empty(s), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      tc::mbar_init(bar_tfull(x), 1);
+      tc::mbar_init(bar_tempty(x), kEpi);
+    }
+    misc[1] = 0u;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(sb + C::OFF_MISC, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch_desc(&tm_a);
+    tc::tma_prefetch_desc(&tm_b);
+    if (MODE == kLse) tc::tma_prefetch_desc(&tm_b2);
+  }
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = misc[0];
+
+  if (warp == 0) {
+    // ============================================================ TMA producer
+    if (lane == 0) {
+      const int a_head = (MODE == kLse) ? l * a.Hq + hq_a : l * a.Hkv + hk;
+      tc::mbar_expect_tx(bar_a, C::A_BYTES);
+#pragma unroll
+      for (int kh = 0; kh < C::KH; ++kh)
+        tc::tma_load_3d(sA + kh * kBoxBytes, &tm_a, bar_a, kh * 64, row0, a_head);
+      int it = 0;
+      bool ok = true;
+      for (; it < ntiles; ++it) {
+        const int s = it % S;
+        const uint32_t ph = (uint32_t)(it / S) & 1u;
+        if (!tc::mbar_wait(bar_empty(s), ph ^ 1u) || *abort_flag) {
+          ok = false;
+          break;
+        }
+        const CUtensorMap* map;
+        int row, head;
+        if (MODE == kLse) {
+          head = l * a.Hkv + hk;
+          if (it < n_ctx) {
+            map = &tm_b;
+            row = it * BN;
+          } else {
+            map = &tm_b2;
+            row = (it - n_ctx) * BN;
+          }
+        } else {
+          map = &tm_b;
+          head = l * a.Hq + hk * G + it / per_head;
+          row = (qt_begin + it % per_head) * BN;
+        }
+        tc::mbar_expect_tx(bar_full(s), C::B_BYTES);
+#pragma unroll
+        for (int kh = 0; kh < C::KH; ++kh)
+          tc::tma_load_3d(sB + s * C::B_BYTES + kh * kBoxBytes, map, bar_full(s), kh * 64, row,
+                          head);
+      }
+      if (!ok) {
+        fail(abort_flag, kErrWaitTimeout);
+        // let the copies already in flight land before the CTA exits
+        tc::mbar_wait(bar_a, 0);
+        for (int j = max(0, it - S); j < it; ++j) tc::mbar_wait(bar_full(j % S), (j / S) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      bool ok = tc::mbar_wait(bar_a, 0);
+      int it = 0;
+      if (ok) {
+        for (; it < ntiles; ++it) {
+          const int s = it % S;
+          const uint32_t ph = (uint32_t)(it / S) & 1u;
+          const int acc = it & 1;
+          const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+          if (!tc::mbar_wait(bar_tempty(acc), aph ^ 1u) || !tc::mbar_wait(bar_full(s), ph) ||
+              *abort_flag) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t d_t = tmem + (uint32_t)(acc * BN);
+          const uint32_t b_s = sB + s * C::B_BYTES;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t o = (uint32_t)(k >> 2) * kBoxBytes + (uint32_t)(k & 3) * 32u;
+            tc::mma_bf16(d_t, tc::sdesc_sw128(sA + o), tc::sdesc_sw128(b_s + o), C::IDESC,
+                         k > 0 ? 1u : 0u);
+          }
+          tc::commit(bar_empty(s));
+          tc::commit(bar_tfull(acc));
+        }
+      }
+      if (!ok) fail(abort_flag, kErrWaitTimeout);
+      if (it > 0) tc::mbar_wait(bar_empty((it - 1) % S), ((it - 1) / S) & 1);
+    }
+    __syncwarp();
+  } else {
+    // ============================================================ epilogue
+    const int eq = warp & 3;
+    const int row = eq * 32 + lane;
+    const int e = threadIdx.x - 64;
+    const uint32_t t_lane = tmem + ((uint32_t)(eq * 32) << 16);
+
+    auto col_const = [&](int it) -> float {
+      const int hq = hk * G + it / per_head;
+      const int j = (qt_begin + it % per_head) * BN + e;
+      if (j >= a.n_q) return -CUDART_INF_F;
+      const float lj = a.lse[(size_t)(l * a.Hq + hq) * a.n_q + j];
+      if (MODE == kMax) return -(lj + (a.hlog ? a.hlog[(size_t)l * a.n_q + j] : 0.f));
+      return -lj * kLog2e;
+    };
+
+    float m = -1e30f, ssum = 0.f;                       // kLse
+    float r = -CUDART_INF_F, tot = -CUDART_INF_F;       // kMax
+    float f = 0.f;                                      // kFuture
+    const int jq = row0 + row;                          // kLse: this row's query
+    const int ik = row0 + row;                          // pass 2: this row's key
+    float cnext = 0.f;
+    if (MODE != kLse && ntiles > 0) {
+      cbuf[e] = col_const(0);
+      if (ntiles > 1) cnext = col_const(1);
+    }
+    bool failed = false;
+    for (int it = 0; it < ntiles; ++it) {
+      const int acc = it & 1;
+      const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+      const bool ok = tc::mbar_wait(bar_tfull(acc), aph) && !*abort_flag;
+      if (tc::bar_or(1, kEpi, !ok)) {
+        failed = true;
+        break;
+      }
+      tc::fence_after_sync();
+      uint32_t v[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) tc::tmem_ld32(t_lane + (uint32_t)(acc * BN + c * 32), v + c * 32);
+      tc::tmem_ld_wait();
+      tc::fence_before_sync();
+      tc::mbar_arrive(bar_tempty(acc));
+      if (MODE != kLse) {
+        if (it + 1 < ntiles) cbuf[((it + 1) & 1) * BN + e] = cnext;
+        if (it + 2 < ntiles) cnext = col_const(it + 2);
+      }
+
+      if (MODE == kLse) {
+        const bool ctx = it < n_ctx;
+        const int kb = ctx ? it * BN : a.T + (it - n_ctx) * BN;
+        const int lim = ctx ? a.T : n_k;
+        const bool need_mask = (kb + BN > lim) || (kb + BN - 1 > off + row0);
+        float mt = -CUDART_INF_F;
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          float x = __uint_as_float(v[c]) * sc2;
+          if (need_mask) {
+            const int i = kb + c;
+            if (i >= lim || i > off + jq) x = -CUDART_INF_F;
+          }
+          v[c] = __float_as_uint(x);
+          mt = fmaxf(mt, x);
+        }
+        const float mn = fmaxf(m, mt);
+        ssum *= fast_exp2(m - mn);
+        m = mn;
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+        for (int c = 0; c < BN; c += 4) {
+          s0 += fast_exp2(__uint_as_float(v[c]) - m);
+          s1 += fast_exp2(__uint_as_float(v[c + 1]) - m);
+          s2 += fast_exp2(__uint_as_float(v[c + 2]) - m);
+          s3 += fast_exp2(__uint_as_float(v[c + 3]) - m);
+        }
+        ssum += (s0 + s1) + (s2 + s3);
+      } else if (MODE == kMax) {
+        const float4* c4 = reinterpret_cast<const float4*>(cbuf + (it & 1) * BN);
+        float r0 = r, r1 = -CUDART_INF_F;
+#pragma unroll
+        for (int q = 0; q < BN / 4; ++q) {
+          const float4 cc = c4[q];
+          r0 = fmaxf(r0, fmaxf(fmaf(__uint_as_float(v[4 * q]), scale, cc.x),
+                               fmaf(__uint_as_float(v[4 * q + 1]), scale, cc.y)));
+          r1 = fmaxf(r1, fmaxf(fmaf(__uint_as_float(v[4 * q + 2]), scale, cc.z),
+                               fmaf(__uint_as_float(v[4 * q + 3]), scale, cc.w)));
+        }
+        r = fmaxf(r0, r1);
+        if ((it + 1) % per_head == 0) {  // last query tile of this head
+          float lv = 0.f;
+          if (a.vnorm && ik < a.T)
+            lv = logf(a.vnorm[(size_t)(l * a.Hq + hk * G + it / per_head) * a.T + ik]);
+          tot = fmaxf(tot, r + lv);
+          r = -CUDART_INF_F;
+        }
+      } else {
+        const float4* c4 = reinterpret_cast<const float4*>(cbuf + (it & 1) * BN);
+        const int j0 = (qt_begin + it % per_head) * BN;
+        const bool need_band = j0 < row0 + BM - 1 + a.w;
+        const int jlim = ik + a.w - j0;  // columns c < jlim are inside the window
+        float f0 = 0.f, f1 = 0.f;
+#pragma unroll
+        for (int q = 0; q < BN / 4; ++q) {
+          const float4 cc = c4[q];
+          float e0 = fast_exp2(fmaf(__uint_as_float(v[4 * q]), sc2, cc.x));
+          float e1 = fast_exp2(fmaf(__uint_as_float(v[4 * q + 1]), sc2, cc.y));
+          float e2 = fast_exp2(fmaf(__uint_as_float(v[4 * q + 2]), sc2, cc.z));
+          float e3 = fast_exp2(fmaf(__uint_as_float(v[4 * q + 3]), sc2, cc.w));
+          if (need_band) {
+            if (4 * q < jlim) e0 = 0.f;
+            if (4 * q + 1 < jlim) e1 = 0.f;
+            if (4 * q + 2 < jlim) e2 = 0.f;
+            if (4 * q + 3 < jlim) e3 = 0.f;
+          }
+          f0 += e0 + e1;
+          f1 += e2 + e3;
+        }
+        f += f0 + f1;
+      }
+    }
+
+    if (failed) {
+      atomicCAS(&g_attn_error, 0, (int)kErrWaitTimeout);
+    } else if (MODE == kLse) {
+      if (jq < a.n_q) a.out[(size_t)(l * a.Hq + hq_a) * a.n_q + jq] = (m + fast_log2(ssum)) * kLn2;
+    } else if (MODE == kMax) {
+      if (ik < a.T) {
+        float* o = a.out + (size_t)(l * a.Hkv + hk) * a.T + ik;
+        *o = a.accumulate ? fmaxf(*o, tot) : tot;
+      }
+    } else {
+      if (ik < a.T) a.out[(size_t)(l * a.Hkv + hk) * a.T + ik] = f;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------------ host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 3-D map over [heads][rows][d] bf16 with 128-row x 64-element boxes, 128-byte swizzle;
+// rows past the end read as zeros.
+cudaError_t make_map(CUtensorMap* m, const void* base, int d, int rows, int heads) {
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D, int MODE>
+cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
+  using C = Cfg<D>;
+  CUtensorMap ta, tb, tb2;
+  cudaError_t e;
+  if (MODE == kLse) {
+    e = make_map(&ta, a.q, D, a.n_q, a.L * a.Hq);
+    if (e == cudaSuccess)
+      e = a.T > 0 ? make_map(&tb, a.k_ctx, D, a.T, a.L * a.Hkv) : make_map(&tb, a.q, D, 1, 1);
+    if (e == cudaSuccess)
+      e = a.n_tail > 0 ? make_map(&tb2, a.k_tail, D, a.n_tail, a.L * a.Hkv)
+                       : make_map(&tb2, a.q, D, 1, 1);
+  } else {
+    e = make_map(&ta, a.k_ctx, D, a.T, a.L * a.Hkv);
+    // with no scoring queries no B tile is loaded (every key gets the empty reduction)
+    if (e == cudaSuccess)
+      e = a.n_q > 0 ? make_map(&tb, a.q, D, a.n_q, a.L * a.Hq) : make_map(&tb, a.k_ctx, D, 1, 1);
+    tb2 = tb;
+  }
+  if (e != cudaSuccess) return e;
+  const int rows = (MODE == kLse) ? a.n_q : a.T;
+  dim3 grid((rows + BM - 1) / BM, MODE == kLse ? a.Hq : a.Hkv, a.L);
+  auto kern = attn_tc_kernel<D, MODE>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+  if (e != cudaSuccess) return e;
+  count_launches(1);
+  kern<<<grid, kThreads, C::SMEM, s>>>(ta, tb, tb2, a);
+  return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_mode(const AttnArgs& a, cudaStream_t s) {
+  const int rows = (MODE == kLse) ? a.n_q : a.T;
+  if (rows == 0) return cudaSuccess;
+  return a.d == 128 ? launch_d<128, MODE>(a, s) : launch_d<64, MODE>(a, s);
+}
+
+__global__ void hidden_log_norm_kernel(const bf16_t* __restrict__ h, int rows, int Dh,
+                                       float* __restrict__ out) {
+  const int wg = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (wg >= rows) return;
+  const bf16_t* p = h + (size_t)wg * Dh;
+  float s = 0.f;
+  for (int c = lane * 8; c < Dh; c += 256) {
+    const uint4 u = ld_nc_v4(p + c);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float lo = bf16_lo(w[k]), hi = bf16_hi(w[k]);
+      s = fmaf(lo, lo, s);
+      s = fmaf(hi, hi, s);
+    }
+  }
+  s = warp_sum(s);
+  if (lane == 0) out[wg] = 0.5f * logf(s);
+}
+
+}  // namespace
+
+cudaError_t launch_lse(const AttnArgs& a, cudaStream_t s) { return launch_mode<kLse>(a, s); }
+cudaError_t launch_score_max(const AttnArgs& a, cudaStream_t s) { return launch_mode<kMax>(a, s); }
+cudaError_t launch_future_sum(const AttnArgs& a, cudaStream_t s) {
+  return launch_mode<kFuture>(a, s);
+}
+
+cudaError_t launch_hidden_log_norm(const bf16_t* h, int L, int n, int Dh, float* hlog,
+                                   cudaStream_t s) {
+  const int rows = L * n;
+  if (rows == 0) return cudaSuccess;
+  count_launches(1);
+  hidden_log_norm_kernel<<<(rows + 7) / 8, 256, 0, s>>>(h, rows, Dh, hlog);
+  return cudaGetLastError();
+}
+
+cudaError_t attn_device_error(int* code, bool clear, cudaStream_t s) {
+  cudaError_t e = cudaMemcpyFromSymbolAsync(code, g_attn_error, sizeof(int), 0,
+                                            cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && clear && *code) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_attn_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
+  return e;
+}
+
+}  // namespace kvs

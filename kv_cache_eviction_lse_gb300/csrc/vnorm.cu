@@ -1,127 +1,219 @@
 // Value factor of KVzip+ (KVzap review, 3.2 Eq. 2/Eq. 3): ||W_O^{(h)} v_i||_2.
 //
 // Computed through the Gram matrix of each head's output-projection slice:
-//   G_h = W_h^T W_h  (d x d, fp32; W_h = o_proj.weight[:, h*d:(h+1)*d], D_h x d)
+//   G_h = W_h^T W_h   (d x d; W_h = o_proj.weight[:, h*d:(h+1)*d], D_h x d)
 //   ||W_h v||^2 = v^T G_h v
-// which costs 2 D_h d^2 + 2 T d^2 flops per head instead of 2 T d D_h for the direct
-// product (7x fewer at D_h=1536, T=2048; 28x fewer at D_h=4096, T=32768).
+// which costs 2 D_h d^2 + 4 T d^2 flops per head instead of 2 T d D_h for the direct
+// product (5x fewer at D_h = 1536, T = 2048; 14x fewer at D_h = 4096, T = 32768).
+// Both contractions run on warp MMAs (bf16 in, fp32 accumulate):
+//   gram  G = W_h^T W_h, operands read transposed with ldmatrix.trans; G is stored as a
+//         bf16 pair G = G_hi + G_lo (G_lo = bf16(G - G_hi)), exact to ~2^-17 |G|
+//   quad  u = V (G_hi + G_lo) for a tile of tokens, then v_i . u_i in the epilogue
 #include "common.cuh"
 #include "vnorm.cuh"
 
 namespace kvs {
 namespace {
 
-constexpr int kGramRows = 32;
+constexpr int kKc = 32;  // rows of W_h per pipeline stage
 
-// G[l][hq] = W_h^T W_h.  One block per (head, layer); 256 threads each own a
-// (D/16 x D/16) block of G and stream the D_h rows of W_h through shared memory.
-template <int D>
-__global__ void __launch_bounds__(256) gram_kernel(const bf16_t* __restrict__ w_o, int Dh,
-                                                   int Hq, float* __restrict__ G) {
-  constexpr int TB = D / 16;
-  __shared__ __align__(16) float ws[kGramRows][D];
-  const int hq = blockIdx.x, l = blockIdx.y, tid = threadIdx.x;
-  const int ta = tid / 16, tb = tid % 16;
-  const bf16_t* base = w_o + (size_t)l * Dh * Hq * D + (size_t)hq * D;
-  float acc[TB][TB];
-#pragma unroll
-  for (int i = 0; i < TB; ++i)
-#pragma unroll
-    for (int j = 0; j < TB; ++j) acc[i][j] = 0.f;
-
-  for (int r0 = 0; r0 < Dh; r0 += kGramRows) {
-    for (int idx = tid; idx < kGramRows * D / 8; idx += 256) {
-      const int r = idx / (D / 8), c = (idx % (D / 8)) * 8;
-      uint4 u = make_uint4(0, 0, 0, 0);
-      if (r0 + r < Dh) u = ld_nc_v4(base + (size_t)(r0 + r) * Hq * D + c);
-      float4* dst = reinterpret_cast<float4*>(&ws[r][c]);
-      dst[0] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
-      dst[1] = make_float4(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w));
-    }
-    __syncthreads();
-#pragma unroll 4
-    for (int r = 0; r < kGramRows; ++r) {
-      float va[TB], vb[TB];
-#pragma unroll
-      for (int i = 0; i < TB; ++i) {
-        va[i] = ws[r][ta * TB + i];
-        vb[i] = ws[r][tb * TB + i];
-      }
-#pragma unroll
-      for (int i = 0; i < TB; ++i)
-#pragma unroll
-        for (int j = 0; j < TB; ++j) acc[i][j] = fmaf(va[i], vb[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-  float* Gh = G + ((size_t)l * Hq + hq) * D * D;
-#pragma unroll
-  for (int i = 0; i < TB; ++i)
-#pragma unroll
-    for (int j = 0; j < TB; ++j) Gh[(ta * TB + i) * D + tb * TB + j] = acc[i][j];
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                                  uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
 }
 
-// vn[l][hq][i] = sqrt(v_i^T G_hq v_i); one token per thread, v_i in registers, G in
-// shared memory (read as broadcasts).
+__device__ __forceinline__ uint16_t f2bf(float x) {  // round to nearest even
+  const uint32_t u = __float_as_uint(x);
+  return (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);
+}
+
+// One block per (head, layer): 8 warps as 4 (M) x 2 (N), each a 32 x 64 tile of the
+// 128 x 128 Gram matrix (D = 128), or 16 x 32 for D = 64.  K = D_h streams through a
+// double-buffered cp.async ring of kKc-row slices of W_h.
 template <int D>
-__global__ void __launch_bounds__(128) quad_kernel(const bf16_t* __restrict__ v,
-                                                   const float* __restrict__ G, int T, int Hq,
-                                                   int Hkv, float* __restrict__ vn) {
-  extern __shared__ float4 gs4[];
-  const int hq = blockIdx.y, l = blockIdx.z;
-  const int hk = hq / (Hq / Hkv);
-  const float4* Gh = reinterpret_cast<const float4*>(G + ((size_t)l * Hq + hq) * D * D);
-  for (int idx = threadIdx.x; idx < D * D / 4; idx += blockDim.x) gs4[idx] = Gh[idx];
-  __syncthreads();
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= T) return;
-  const bf16_t* vp = v + ((size_t)(l * Hkv + hk) * T + i) * D;
-  float x[D];
-#pragma unroll
-  for (int c = 0; c < D; c += 8) {
-    const uint4 u = ld_nc_v4(vp + c);
-    x[c + 0] = bf16_lo(u.x); x[c + 1] = bf16_hi(u.x);
-    x[c + 2] = bf16_lo(u.y); x[c + 3] = bf16_hi(u.y);
-    x[c + 4] = bf16_lo(u.z); x[c + 5] = bf16_hi(u.z);
-    x[c + 6] = bf16_lo(u.w); x[c + 7] = bf16_hi(u.w);
-  }
-  float acc = 0.f;
-#pragma unroll 1
-  for (int a2 = 0; a2 < D; ++a2) {
-    const float4* Ga = gs4 + a2 * (D / 4);
-    float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
-#pragma unroll
-    for (int b4 = 0; b4 < D / 4; ++b4) {
-      const float4 gg = Ga[b4];
-      u0 = fmaf(gg.x, x[4 * b4 + 0], u0);
-      u1 = fmaf(gg.y, x[4 * b4 + 1], u1);
-      u2 = fmaf(gg.z, x[4 * b4 + 2], u2);
-      u3 = fmaf(gg.w, x[4 * b4 + 3], u3);
+__global__ void __launch_bounds__(256) gram_mma_kernel(const bf16_t* __restrict__ w_o, int Dh,
+                                                       int Hq, bf16_t* __restrict__ G) {
+  constexpr int MT = D / 64;      // m16 tiles per warp (2 for D=128)
+  constexpr int NT = D / 16;      // n8 tiles per warp (8 for D=128)
+  constexpr int LD = D + 8;
+  __shared__ __align__(16) bf16_t ws[2][kKc][LD];
+  const int hq = blockIdx.x, l = blockIdx.y, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
+  const int wm = warp >> 1, wn = warp & 1;
+  const int m0 = wm * (D / 4), n0 = wn * (D / 2);
+  const bf16_t* base = w_o + (size_t)l * Dh * Hq * D + (size_t)hq * D;
+
+  auto issue = [&](int r0, int buf) {
+    for (int idx = tid; idx < kKc * D / 8; idx += 256) {
+      const int r = idx / (D / 8), c = (idx % (D / 8)) * 8;
+      const bool ok = r0 + r < Dh;
+      cp_async16(smem_u32(&ws[buf][r][c]), ok ? base + (size_t)(r0 + r) * Hq * D + c : base,
+                 ok ? 16 : 0);
     }
-    const float xa = __uint_as_float(static_cast<uint32_t>(vp[a2]) << 16);
-    acc = fmaf(xa, (u0 + u1) + (u2 + u3), acc);
+  };
+
+  float acc[MT][NT][4];
+#pragma unroll
+  for (int i = 0; i < MT; ++i)
+#pragma unroll
+    for (int j = 0; j < NT; ++j) acc[i][j][0] = acc[i][j][1] = acc[i][j][2] = acc[i][j][3] = 0.f;
+
+  const int nchunks = (Dh + kKc - 1) / kKc;
+  issue(0, 0);
+  cp_async_commit();
+  for (int ch = 0; ch < nchunks; ++ch) {
+    const int buf = ch & 1;
+    if (ch + 1 < nchunks) {
+      issue((ch + 1) * kKc, buf ^ 1);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kc = 0; kc < kKc; kc += 16) {
+      // A = W^T: rows of the stored tile are k; .trans gives A[m][k] fragments
+      uint32_t af[MT][4];
+#pragma unroll
+      for (int i = 0; i < MT; ++i) {
+        const int mat = lane >> 3, rr = lane & 7;
+        const int k = kc + (mat >> 1) * 8 + rr;
+        const int m = m0 + i * 16 + (mat & 1) * 8;
+        ldmatrix_x4_trans(smem_u32(&ws[buf][k][m]), af[i][0], af[i][1], af[i][2], af[i][3]);
+      }
+#pragma unroll
+      for (int j = 0; j < NT; j += 2) {
+        // B = W: matrices (k0, n), (k0+8, n), (k0, n+8), (k0+8, n+8)
+        const int mat = lane >> 3, rr = lane & 7;
+        const int k = kc + (mat & 1) * 8 + rr;
+        const int n = n0 + j * 8 + (mat >> 1) * 8;
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4_trans(smem_u32(&ws[buf][k][n]), b0, b1, b2, b3);
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+          mma_bf16_16816(acc[i][j], af[i], b0, b1);
+          mma_bf16_16816(acc[i][j + 1], af[i], b2, b3);
+        }
+      }
+    }
+    __syncthreads();
   }
-  vn[((size_t)l * Hq + hq) * T + i] = sqrtf(fmaxf(acc, 0.f));
+  bf16_t* Gh = G + ((size_t)l * Hq + hq) * 2 * D * D;  // [hi: D x D][lo: D x D]
+#pragma unroll
+  for (int i = 0; i < MT; ++i)
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int row = m0 + i * 16 + g + (e >> 1) * 8;
+        const int col = n0 + j * 8 + 2 * t4 + (e & 1);
+        const float x = acc[i][j][e];
+        const uint16_t hi = f2bf(x);
+        const uint16_t lo = f2bf(x - __uint_as_float((uint32_t)hi << 16));
+        Gh[row * D + col] = hi;
+        Gh[D * D + row * D + col] = lo;
+      }
+}
+
+// vn = sqrt(v^T (G_hi + G_lo) v) for 64-token tiles; G_hi, G_lo (bf16, symmetric, so
+// their rows serve directly as the k-contiguous B operand) stay in shared memory while
+// the block walks kTokTiles consecutive token tiles of one (layer, query head).
+constexpr int kTokTiles = 4;
+
+template <int D>
+__global__ void __launch_bounds__(128) quad_mma_kernel(const bf16_t* __restrict__ v,
+                                                       const bf16_t* __restrict__ G, int T,
+                                                       int Hq, int Hkv, float* __restrict__ vn) {
+  constexpr int LD = D + 8;
+  extern __shared__ __align__(16) uint8_t qsm[];
+  bf16_t(*gs)[LD] = reinterpret_cast<bf16_t(*)[LD]>(qsm);              // [2D][LD]: hi rows, lo rows
+  bf16_t(*vs)[LD] = reinterpret_cast<bf16_t(*)[LD]>(qsm + 2 * D * LD * 2);  // [64][LD]
+  const int hq = blockIdx.y, l = blockIdx.z, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
+  const int hk = hq / (Hq / Hkv);
+  const bf16_t* Gh = G + ((size_t)l * Hq + hq) * 2 * D * D;
+  for (int idx = tid; idx < 2 * D * D / 8; idx += 128) {
+    const int r = idx / (D / 8), c = (idx % (D / 8)) * 8;
+    cp_async16(smem_u32(&gs[r][c]), Gh + (size_t)r * D + c, 16);
+  }
+  cp_async_commit();
+  const bf16_t* vb = v + (size_t)(l * Hkv + hk) * T * D;
+  for (int tt = 0; tt < kTokTiles; ++tt) {
+    const int i0 = (blockIdx.x * kTokTiles + tt) * 64;
+    if (i0 >= T) break;
+    for (int idx = tid; idx < 64 * D / 8; idx += 128) {
+      const int r = idx / (D / 8), c = (idx % (D / 8)) * 8;
+      const bool ok = i0 + r < T;
+      cp_async16(smem_u32(&vs[r][c]), ok ? vb + (size_t)(i0 + r) * D + c : vb, ok ? 16 : 0);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    uint32_t af[D / 16][4];
+#pragma unroll
+    for (int kc = 0; kc < D / 16; ++kc)
+      ldmatrix_x4(smem_u32(&vs[warp * 16 + (lane & 15)][kc * 16 + (lane >> 4) * 8]), af[kc][0],
+                  af[kc][1], af[kc][2], af[kc][3]);
+    float p0 = 0.f, p1 = 0.f;
+#pragma unroll 2
+    for (int nt = 0; nt < D / 8; ++nt) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+#pragma unroll
+        for (int k2 = 0; k2 < D / 32; ++k2) {
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4(smem_u32(&gs[half * D + nt * 8 + (lane & 7)][k2 * 32 + (lane >> 3) * 8]), b0,
+                      b1, b2, b3);
+          mma_bf16_16816(acc, af[2 * k2], b0, b1);
+          mma_bf16_16816(acc, af[2 * k2 + 1], b2, b3);
+        }
+      }
+      const int col = nt * 8 + 2 * t4;
+      const uint32_t va = *reinterpret_cast<const uint32_t*>(&vs[warp * 16 + g][col]);
+      const uint32_t vc = *reinterpret_cast<const uint32_t*>(&vs[warp * 16 + g + 8][col]);
+      p0 = fmaf(acc[0], bf16_lo(va), fmaf(acc[1], bf16_hi(va), p0));
+      p1 = fmaf(acc[2], bf16_lo(vc), fmaf(acc[3], bf16_hi(vc), p1));
+    }
+    p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+    p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
+    p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+    p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+    if (t4 == 0) {
+      float* out = vn + ((size_t)l * Hq + hq) * T;
+      const int ia = i0 + warp * 16 + g, ib = ia + 8;
+      if (ia < T) out[ia] = sqrtf(fmaxf(p0, 0.f));
+      if (ib < T) out[ib] = sqrtf(fmaxf(p1, 0.f));
+    }
+    __syncthreads();
+  }
 }
 
 }  // namespace
 
-size_t vnorm_workspace_bytes(int L, int Hq, int d) { return (size_t)L * Hq * d * d * sizeof(float); }
+size_t vnorm_workspace_bytes(int L, int Hq, int d) {
+  return (size_t)L * Hq * 2 * d * d * sizeof(bf16_t);
+}
 
 cudaError_t launch_vnorm(const bf16_t* v, int L, int Hq, int Hkv, int d, int T, int Dh,
-                         const bf16_t* w_o, float* vn, float* G, cudaStream_t s) {
+                         const bf16_t* w_o, float* vn, void* ws, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  bf16_t* G = static_cast<bf16_t*>(ws);
   dim3 gg(Hq, L);
-  dim3 gq((T + 127) / 128, Hq, L);
-  const size_t smem = (size_t)d * d * sizeof(float);
+  dim3 gq((T + 64 * kTokTiles - 1) / (64 * kTokTiles), Hq, L);
   count_launches(2);
   if (d == 128) {
-    gram_kernel<128><<<gg, 256, 0, s>>>(w_o, Dh, Hq, G);
-    cudaFuncSetAttribute(quad_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    quad_kernel<128><<<gq, 128, smem, s>>>(v, G, T, Hq, Hkv, vn);
+    constexpr size_t smem = (2 * 128 + 64) * (128 + 8) * 2;
+    gram_mma_kernel<128><<<gg, 256, 0, s>>>(w_o, Dh, Hq, G);
+    cudaFuncSetAttribute(quad_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    quad_mma_kernel<128><<<gq, 128, smem, s>>>(v, G, T, Hq, Hkv, vn);
   } else {
-    gram_kernel<64><<<gg, 256, 0, s>>>(w_o, Dh, Hq, G);
-    quad_kernel<64><<<gq, 128, smem, s>>>(v, G, T, Hq, Hkv, vn);
+    constexpr size_t smem = (2 * 64 + 64) * (64 + 8) * 2;
+    gram_mma_kernel<64><<<gg, 256, 0, s>>>(w_o, Dh, Hq, G);
+    quad_mma_kernel<64><<<gq, 128, smem, s>>>(v, G, T, Hq, Hkv, vn);
   }
   return cudaGetLastError();
 }

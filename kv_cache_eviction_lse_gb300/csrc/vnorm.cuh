@@ -8,8 +8,8 @@ namespace kvs {
 
 size_t vnorm_workspace_bytes(int L, int Hq, int d);
 
-// vn [L][Hq][T] = ||W_O^{(hq)} v_i||; G: workspace of vnorm_workspace_bytes() bytes.
+// vn [L][Hq][T] = ||W_O^{(hq)} v_i||; ws: vnorm_workspace_bytes() bytes (Gram matrices).
 cudaError_t launch_vnorm(const bf16_t* v, int L, int Hq, int Hkv, int d, int T, int Dh,
-                         const bf16_t* w_o, float* vn, float* G, cudaStream_t s);
+                         const bf16_t* w_o, float* vn, void* ws, cudaStream_t s);
 
 }  // namespace kvs
