@@ -165,6 +165,26 @@ kvs_status kvs_vnorm(const kvs_dims* dims, const kvs_bf16* v, int32_t T, const k
                      float* vnorm, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------
+ * kvs_vnorm_noalloc -- kvs_vnorm without a caller-provided workspace.  The pages have
+ * no counterpart: this entry point exists for callers that cannot allocate device
+ * memory, e.g. a plugin inside a host framework that owns every device allocation, or
+ * a serving loop that forbids allocation (and its implicit synchronisation) after
+ * warm-up.  It computes the same vnorm as kvs_vnorm (same kernels, same results) and
+ * allocates nothing: the Gram scratch is a device array built into the library, of
+ * 8 MiB, which every GPU that loads the library keeps until the process exits.  Layers
+ * are processed one after another on `stream`, so the limit is per layer:
+ * H_q * d * d * 4 bytes <= 8 MiB (H_q <= 128 at d = 128); larger shapes return
+ * KVS_ERR_CAPACITY.  The first call on each device looks up the array's device
+ * address (once per device); make that first call before capturing a stream into a
+ * graph.  All calls share the one array: calls that overlap on the GPU (other streams,
+ * other host threads) race on it and must be serialised by the caller.  Nothing in it
+ * needs to start at zero: every byte a call reads is written earlier by that call.
+ *   v [L][H_kv][T][d] bf16,  w_o [L][D_h][H_q*d] bf16,  vnorm [L][H_q][T] fp32 output.
+ * ------------------------------------------------------------------------------- */
+kvs_status kvs_vnorm_noalloc(const kvs_dims* dims, const kvs_bf16* v, int32_t T,
+                             const kvs_bf16* w_o, float* vnorm, void* stream);
+
+/* ---------------------------------------------------------------------------------
  * kvs_surrogate -- KVzap-Linear score [KVzap 3.3; Algorithm 1, step 1]: at each
  * position t the hidden state h_t (D_h) maps to one predicted log-score per KV head,
  *

@@ -65,6 +65,7 @@ _SIGS = {
     "kvs_score_future_sum": ([_D, _P, _P, _I, _P, _I, _P, _P], ctypes.c_int),
     "kvs_vnorm_workspace_size": ([_D], _S),
     "kvs_vnorm": ([_D, _P, _I, _P, _P, _P, _S, _P], ctypes.c_int),
+    "kvs_vnorm_noalloc": ([_D, _P, _I, _P, _P, _P], ctypes.c_int),
     "kvs_surrogate": ([_D, _P, _I, _P, _P, _P, _F, _I, _P, _P, _P], ctypes.c_int),
     "kvs_prune_mask": ([_D, _P, _I, _I, _F, _I, _I, _P, _P, _P], ctypes.c_int),
     "kvs_compact_workspace_size": ([_D, _I], _S),
@@ -154,6 +155,12 @@ def kvs_vnorm_workspace_size(dm) -> int:
 def kvs_vnorm(dm, v, T, w_o, vnorm, ws, ws_bytes, stream=None):
     _check(_lib.kvs_vnorm(_d(dm), _ptr(v), T, _ptr(w_o), _ptr(vnorm), _ptr(ws), ws_bytes,
                           _stream(stream)))
+
+
+def kvs_vnorm_noalloc(dm, v, T, w_o, vnorm, stream=None):
+    """kvs_vnorm without a workspace argument: uses the library's built-in device
+    scratch (for callers that cannot allocate device memory; see include/kvs.h)."""
+    _check(_lib.kvs_vnorm_noalloc(_d(dm), _ptr(v), T, _ptr(w_o), _ptr(vnorm), _stream(stream)))
 
 
 def kvs_surrogate(dm, h, T, W, b, score, tau=0.0, w=0, mask=None, keep=None, stream=None):

@@ -204,6 +204,27 @@ kvs_status kvs_vnorm(const kvs_dims* dims, const kvs_bf16* v, int32_t T, const k
                      "kvs_vnorm");
 }
 
+kvs_status kvs_vnorm_noalloc(const kvs_dims* dims, const kvs_bf16* v, int32_t T,
+                             const kvs_bf16* w_o, float* vnorm, void* stream) {
+  kvs_status st = check_dims(dims, __func__);
+  if (st) return st;
+  REQUIRE(T >= 0, KVS_ERR_ARG, "kvs_vnorm_noalloc: negative T");
+  REQUIRE(dims->D_h > 0 && dims->D_h % 8 == 0, KVS_ERR_SHAPE,
+          "kvs_vnorm_noalloc: D_h = %d must be a positive multiple of 8", dims->D_h);
+  const size_t per_layer = kvs::vnorm_workspace_bytes(1, dims->H_q, dims->d);
+  REQUIRE(per_layer <= kvs::vnorm_noalloc_scratch_bytes(), KVS_ERR_CAPACITY,
+          "kvs_vnorm_noalloc: one layer needs %zu bytes of scratch (H_q * d * d * 4) but the "
+          "built-in scratch holds %zu; use kvs_vnorm with a caller workspace",
+          per_layer, kvs::vnorm_noalloc_scratch_bytes());
+  if (T == 0) return ok();
+  REQUIRE_PTR(v);
+  REQUIRE_PTR(w_o);
+  REQUIRE_PTR(vnorm);
+  return cuda_status(kvs::launch_vnorm_noalloc(v, dims->L, dims->H_q, dims->H_kv, dims->d, T,
+                                               dims->D_h, w_o, vnorm, as_stream(stream)),
+                     "kvs_vnorm_noalloc");
+}
+
 kvs_status kvs_surrogate(const kvs_dims* dims, const kvs_bf16* h, int32_t T, const kvs_bf16* W,
                          const float* b, float* score, float tau, int32_t w, uint8_t* mask,
                          int32_t* keep, void* stream) {

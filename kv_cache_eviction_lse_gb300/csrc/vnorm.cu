@@ -9,6 +9,8 @@
 //   gram  G = W_h^T W_h, operands read transposed with ldmatrix.trans; G is stored as a
 //         bf16 pair G = G_hi + G_lo (G_lo = bf16(G - G_hi)), exact to ~2^-17 |G|
 //   quad  u = V (G_hi + G_lo) for a tile of tokens, then v_i . u_i in the epilogue
+#include <mutex>
+
 #include "common.cuh"
 #include "vnorm.cuh"
 
@@ -216,6 +218,60 @@ cudaError_t launch_vnorm(const bf16_t* v, int L, int Hq, int Hkv, int d, int T, 
     quad_mma_kernel<64><<<gq, 128, smem, s>>>(v, G, T, Hq, Hkv, vn);
   }
   return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ allocation-free variant
+//
+// Some callers of this library cannot allocate device memory for the Gram scratch:
+// code that runs as a plugin inside a host framework which owns every device
+// allocation (its caching allocator and memory accounting must see all of them), and
+// latency-critical serving loops that forbid allocation, with its implicit
+// synchronisation, after warm-up.  For them the value norm can use a scratch buffer
+// built into the library: a file-scope device array of kNoAllocScratchBytes, which
+// every GPU that loads the library holds until the process exits.  The layers are
+// processed one after another on the caller's stream, each reusing the array, so the
+// limit is one layer's Gram matrices: H_q * d * d * 4 bytes <= kNoAllocScratchBytes
+// (H_q <= 128 at d = 128).  The array keeps the last call's contents; the Gram kernel
+// overwrites every byte a call reads, so nothing needs clearing, but calls that overlap
+// on the GPU (different streams, or different host threads) race on it.
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) unsigned char g_vnorm_scratch[kNoAllocScratchBytes];
+constexpr int kMaxDevices = 64;
+}  // namespace
+
+size_t vnorm_noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
+
+// Device address of the built-in scratch on the current device, looked up once per
+// device (the first call on a device does the lookup, so it must not be made while a
+// stream is being captured).
+static cudaError_t vnorm_noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_vnorm_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
+cudaError_t launch_vnorm_noalloc(const bf16_t* v, int L, int Hq, int Hkv, int d, int T, int Dh,
+                                 const bf16_t* w_o, float* vn, cudaStream_t s) {
+  void* scratch = nullptr;
+  cudaError_t e = vnorm_noalloc_scratch(&scratch);
+  if (e != cudaSuccess) return e;
+  for (int l = 0; l < L && e == cudaSuccess; ++l)
+    e = launch_vnorm(v + (size_t)l * Hkv * T * d, 1, Hq, Hkv, d, T, Dh,
+                     w_o + (size_t)l * Dh * Hq * d, vn + (size_t)l * Hq * T, scratch, s);
+  return e;
 }
 
 }  // namespace kvs
