@@ -1,19 +1,23 @@
 // Attention-scoring passes on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
-// Pass 1 (LSE) and pass 2 (transposed scoring) share one warp-specialised CTA:
-//   warp 0      TMA producer: loads the CTA's 128-row A tile once, then streams 128-row
-//               B tiles through a STAGES-deep ring of 128-byte-swizzled smem buffers
-//   warp 1      allocates 256 TMEM columns and issues tcgen05.mma (M=128, N=128, K=16,
-//               bf16 x bf16 -> fp32) into one of two TMEM accumulators per B tile
-//   warps 2-5   epilogue: one thread per accumulator row (TMEM lane) reads the 128
-//               columns with tcgen05.ld and reduces them in registers; the other
-//               accumulator is being filled by the MMA meanwhile
+// Pass 1 (LSE) and pass 2 (transposed scoring) share one warp-specialised CTA that owns
+// M = 256 rows of operand A as two 128-row sub-tiles, so every streamed B tile feeds
+// two MMAs (half the B traffic per flop of an M = 128 CTA):
+//   warp 0      TMA producer: loads both A sub-tiles once, then streams 128-row B tiles
+//               through a STAGES-deep ring of 128-byte-swizzled smem buffers
+//   warp 1      allocates all 512 TMEM columns and issues tcgen05.mma (M=128, N=128,
+//               K=16, bf16 x bf16 -> fp32): per B tile one MMA chain per sub-tile into
+//               that sub-tile's current accumulator (two accumulators per sub-tile)
+//   warps 2-9   epilogue, two groups of four warps (one group per sub-tile, two warps
+//               per SM sub-partition): one thread per accumulator row (TMEM lane) reads
+//               the 128 columns with tcgen05.ld and reduces them in registers while
+//               the MMA fills the other accumulator
 // Modes (x = q.k / sqrt(d), never written to memory):
-//   kLse     A = 128 queries,  B = key tiles (context, then tail): online max and
+//   kLse     A = 256 queries,  B = key tiles (context, then tail): online max and
 //            sum of 2^(x log2 e) per query -> ln sum exp(x)
-//   kMax     A = 128 context keys, B = query tiles of every head of the group: per key
+//   kMax     A = 256 context keys, B = query tiles of every head of the group: per key
 //            max of x - lse_j - ln||h_j||, folded per head with ln ||W_O^{(h)} v_i||
-//   kFuture  A = 128 keys, B = query tiles j >= i0 + w: per key sum over the group of
+//   kFuture  A = 256 keys, B = query tiles j >= i0 + w: per key sum over the group of
 //            2^((x - lse_j) log2 e) for j >= i + w
 // Sources: KVpop review, 1. Key Terms (LSE reuse, transposed-attention pass);
 // KVzap review, 3.1 Eq. 1 and 3.2 Eq. 3.
@@ -30,12 +34,13 @@ __device__ int g_attn_error = 0;
 
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 128;
-constexpr int kThreads = 192;
-constexpr int kEpi = 128;
+constexpr int BM = 128;     // rows per A sub-tile = TMEM lanes
+constexpr int MSUB = 2;     // A sub-tiles per CTA
+constexpr int BN = 128;     // rows per B tile = accumulator columns
+constexpr int kGroupThreads = 128;
+constexpr int kThreads = 64 + MSUB * kGroupThreads;
 constexpr uint32_t kBoxBytes = 128 * 128;  // 128 rows x 64 bf16 (one 128-byte swizzle span)
-constexpr uint32_t kTmemCols = 2 * BN;
+constexpr uint32_t kTmemCols = MSUB * 2 * BN;
 constexpr int kErrWaitTimeout = 1;  // a bounded mbarrier wait ran out
 
 enum Mode { kLse = 0, kMax = 1, kFuture = 2 };
@@ -44,12 +49,13 @@ template <int D>
 struct Cfg {
   static constexpr int KH = D / 64;
   static constexpr int STAGES = D == 128 ? 4 : 6;
-  static constexpr uint32_t A_BYTES = KH * kBoxBytes;
+  static constexpr uint32_t A_SUB = KH * kBoxBytes;
+  static constexpr uint32_t A_BYTES = MSUB * A_SUB;
   static constexpr uint32_t B_BYTES = KH * kBoxBytes;
   static constexpr uint32_t OFF_B = A_BYTES;
-  static constexpr uint32_t OFF_C = OFF_B + STAGES * B_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_C + 2 * BN * 4;
-  static constexpr uint32_t NBAR = 1 + 2 * STAGES + 4;
+  static constexpr uint32_t OFF_C = OFF_B + STAGES * B_BYTES;  // [MSUB][2][BN] floats
+  static constexpr uint32_t OFF_BAR = OFF_C + MSUB * 2 * BN * 4;
+  static constexpr uint32_t NBAR = 1 + 2 * STAGES + 4 * MSUB;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
   static constexpr uint32_t IDESC = tc::idesc_bf16(BM, BN);
@@ -58,6 +64,16 @@ struct Cfg {
 __device__ __forceinline__ void fail(volatile uint32_t* abort_flag, int code) {
   *abort_flag = 1u;
   atomicCAS(&g_attn_error, 0, code);
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+__device__ __forceinline__ float2 f2(uint32_t a, uint32_t b) {
+  return make_float2(__uint_as_float(a), __uint_as_float(b));
 }
 
 template <int D, int MODE>
@@ -72,12 +88,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
   const uint32_t sA = sb, sB = sb + C::OFF_B;
-  float* cbuf = reinterpret_cast<float*>(smem + C::OFF_C);
+  float* cbuf_all = reinterpret_cast<float*>(smem + C::OFF_C);
   const uint32_t bar_a = sb + C::OFF_BAR;
   auto bar_full = [&](int s) { return bar_a + 8u * (1 + s); };
   auto bar_empty = [&](int s) { return bar_a + 8u * (1 + S + s); };
-  auto bar_tfull = [&](int x) { return bar_a + 8u * (1 + 2 * S + x); };
-  auto bar_tempty = [&](int x) { return bar_a + 8u * (3 + 2 * S + x); };
+  auto bar_tfull = [&](int u, int x) { return bar_a + 8u * (1 + 2 * S + 2 * u + x); };
+  auto bar_tempty = [&](int u, int x) { return bar_a + 8u * (1 + 2 * S + 2 * MSUB + 2 * u + x); };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
 
@@ -88,14 +104,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int off = n_k - a.n_q;
   const float scale = rsqrtf((float)D);
   const float sc2 = scale * kLog2e;
-  const int row0 = blockIdx.x * BM;
+  const int row0 = blockIdx.x * (BM * MSUB);
   const int hq_a = (MODE == kLse) ? (int)blockIdx.y : 0;
   const int hk = (MODE == kLse) ? hq_a / G : (int)blockIdx.y;
+  const int a_rows = (MODE == kLse) ? a.n_q : a.T;
+  const int nsub = min(MSUB, (a_rows - row0 + BM - 1) / BM);  // sub-tiles with a valid row
 
   // ---------------------------------------------------------------- tile space of B
   int ntiles, n_ctx = 0, per_head = 1, qt_begin = 0;
   if (MODE == kLse) {
-    const int j_last = min(row0 + BM, a.n_q) - 1;
+    const int j_last = min(row0 + BM * MSUB, a.n_q) - 1;
     const int kv_end = off + j_last + 1;  // keys [0, kv_end) are visible to some query
     n_ctx = (min(a.T, kv_end) + BN - 1) / BN;
     const int tail_need = min(a.n_tail, max(0, kv_end - a.T));
@@ -113,10 +131,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(bar_full(s), 1);
       tc::mbar_init(bar_empty(s), 1);
     }
-    for (int x = 0; x < 2; ++x) {
-      tc::mbar_init(bar_tfull(x), 1);
-      tc::mbar_init(bar_tempty(x), kEpi);
-    }
+    for (int u = 0; u < MSUB; ++u)
+      for (int x = 0; x < 2; ++x) {
+        tc::mbar_init(bar_tfull(u, x), 1);
+        tc::mbar_init(bar_tempty(u, x), kGroupThreads);
+      }
     misc[1] = 0u;
     tc::fence_mbar_init();
   }
@@ -139,8 +158,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int a_head = (MODE == kLse) ? l * a.Hq + hq_a : l * a.Hkv + hk;
       tc::mbar_expect_tx(bar_a, C::A_BYTES);
 #pragma unroll
-      for (int kh = 0; kh < C::KH; ++kh)
-        tc::tma_load_3d(sA + kh * kBoxBytes, &tm_a, bar_a, kh * 64, row0, a_head);
+      for (int u = 0; u < MSUB; ++u)
+#pragma unroll
+        for (int kh = 0; kh < C::KH; ++kh)
+          tc::tma_load_3d(sA + u * C::A_SUB + kh * kBoxBytes, &tm_a, bar_a, kh * 64,
+                          row0 + u * BM, a_head);
       int it = 0;
       bool ok = true;
       for (; it < ntiles; ++it) {
@@ -185,27 +207,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = tc::mbar_wait(bar_a, 0);
       int it = 0;
       if (ok) {
-        for (; it < ntiles; ++it) {
+        for (; it < ntiles && ok; ++it) {
           const int s = it % S;
           const uint32_t ph = (uint32_t)(it / S) & 1u;
-          const int acc = it & 1;
-          const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-          if (!tc::mbar_wait(bar_tempty(acc), aph ^ 1u) || !tc::mbar_wait(bar_full(s), ph) ||
-              *abort_flag) {
+          const int buf = it & 1;
+          const uint32_t bph = (uint32_t)(it >> 1) & 1u;
+          if (!tc::mbar_wait(bar_full(s), ph) || *abort_flag) {
             ok = false;
             break;
           }
-          tc::fence_after_sync();
-          const uint32_t d_t = tmem + (uint32_t)(acc * BN);
           const uint32_t b_s = sB + s * C::B_BYTES;
+          for (int u = 0; u < nsub; ++u) {
+            if (!tc::mbar_wait(bar_tempty(u, buf), bph ^ 1u)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+            const uint32_t d_t = tmem + (uint32_t)((2 * u + buf) * BN);
+            const uint32_t a_u = sA + u * C::A_SUB;
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t o = (uint32_t)(k >> 2) * kBoxBytes + (uint32_t)(k & 3) * 32u;
-            tc::mma_bf16(d_t, tc::sdesc_sw128(sA + o), tc::sdesc_sw128(b_s + o), C::IDESC,
-                         k > 0 ? 1u : 0u);
+            for (int k = 0; k < D / 16; ++k) {
+              const uint32_t o = (uint32_t)(k >> 2) * kBoxBytes + (uint32_t)(k & 3) * 32u;
+              tc::mma_bf16(d_t, tc::sdesc_sw128(a_u + o), tc::sdesc_sw128(b_s + o), C::IDESC,
+                           k > 0 ? 1u : 0u);
+            }
+            tc::commit(bar_tfull(u, buf));
           }
           tc::commit(bar_empty(s));
-          tc::commit(bar_tfull(acc));
         }
       }
       if (!ok) fail(abort_flag, kErrWaitTimeout);
@@ -214,135 +242,165 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ============================================================ epilogue
-    const int eq = warp & 3;
-    const int row = eq * 32 + lane;
-    const int e = threadIdx.x - 64;
-    const uint32_t t_lane = tmem + ((uint32_t)(eq * 32) << 16);
+    const int u = (warp - 2) >> 2;          // sub-tile of this group
+    const int eq = warp & 3;                // TMEM lane quarter this warp may access
+    const int row = eq * 32 + lane;         // accumulator row
+    const int e = ((warp - 2) & 3) * 32 + lane;  // index within the group (0..127)
+    const int rbase = row0 + u * BM;        // first A row of the sub-tile
+    const int ra = rbase + row;             // this thread's query (kLse) or key
+    const uint32_t t_lane = tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(2 * u * BN);
+    float* cbuf = cbuf_all + u * 2 * BN;
+    const int bar_id = 1 + u;
 
-    auto col_const = [&](int it) -> float {
-      const int hq = hk * G + it / per_head;
-      const int j = (qt_begin + it % per_head) * BN + e;
-      if (j >= a.n_q) return -CUDART_INF_F;
-      const float lj = a.lse[(size_t)(l * a.Hq + hq) * a.n_q + j];
-      if (MODE == kMax) return -(lj + (a.hlog ? a.hlog[(size_t)l * a.n_q + j] : 0.f));
-      return -lj * kLog2e;
-    };
+    if (u < nsub) {
+      auto col_const = [&](int it) -> float {
+        const int hq = hk * G + it / per_head;
+        const int j = (qt_begin + it % per_head) * BN + e;
+        if (j >= a.n_q) return -CUDART_INF_F;
+        const float lj = a.lse[(size_t)(l * a.Hq + hq) * a.n_q + j];
+        if (MODE == kMax) return -(lj + (a.hlog ? a.hlog[(size_t)l * a.n_q + j] : 0.f));
+        return -lj * kLog2e;
+      };
+      auto ln_vn = [&](int it) -> float {  // ln ||W_O v|| of this key for the head of tile it
+        if (!a.vnorm || ra >= a.T) return 0.f;
+        return logf(a.vnorm[(size_t)(l * a.Hq + hk * G + it / per_head) * a.T + ra]);
+      };
 
-    float m = -1e30f, ssum = 0.f;                       // kLse
-    float r = -CUDART_INF_F, tot = -CUDART_INF_F;       // kMax
-    float f = 0.f;                                      // kFuture
-    const int jq = row0 + row;                          // kLse: this row's query
-    const int ik = row0 + row;                          // pass 2: this row's key
-    float cnext = 0.f;
-    if (MODE != kLse && ntiles > 0) {
-      cbuf[e] = col_const(0);
-      if (ntiles > 1) cnext = col_const(1);
-    }
-    bool failed = false;
-    for (int it = 0; it < ntiles; ++it) {
-      const int acc = it & 1;
-      const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-      const bool ok = tc::mbar_wait(bar_tfull(acc), aph) && !*abort_flag;
-      if (tc::bar_or(1, kEpi, !ok)) {
-        failed = true;
-        break;
+      float m = -1e30f, ssum = 0.f;                  // kLse
+      float r = -CUDART_INF_F, tot = -CUDART_INF_F;  // kMax
+      float lv = 0.f;                                // kMax: ln vnorm of the current head
+      float f = 0.f;                                 // kFuture
+      float cn1 = 0.f, cn2 = 0.f;
+      if (MODE != kLse && ntiles > 0) {
+        cbuf[e] = col_const(0);
+        if (ntiles > 1) cn1 = col_const(1);
+        if (ntiles > 2) cn2 = col_const(2);
       }
-      tc::fence_after_sync();
-      uint32_t v[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) tc::tmem_ld32(t_lane + (uint32_t)(acc * BN + c * 32), v + c * 32);
-      tc::tmem_ld_wait();
-      tc::fence_before_sync();
-      tc::mbar_arrive(bar_tempty(acc));
-      if (MODE != kLse) {
-        if (it + 1 < ntiles) cbuf[((it + 1) & 1) * BN + e] = cnext;
-        if (it + 2 < ntiles) cnext = col_const(it + 2);
-      }
+      if (MODE == kMax && ntiles > 0) lv = ln_vn(0);
 
-      if (MODE == kLse) {
-        const bool ctx = it < n_ctx;
-        const int kb = ctx ? it * BN : a.T + (it - n_ctx) * BN;
-        const int lim = ctx ? a.T : n_k;
-        const bool need_mask = (kb + BN > lim) || (kb + BN - 1 > off + row0);
-        float mt = -CUDART_INF_F;
+      bool failed = false;
+      for (int it = 0; it < ntiles; ++it) {
+        const int buf = it & 1;
+        const uint32_t bph = (uint32_t)(it >> 1) & 1u;
+        const bool ok = tc::mbar_wait(bar_tfull(u, buf), bph) && !*abort_flag;
+        if (tc::bar_or(bar_id, kGroupThreads, !ok)) {
+          failed = true;
+          break;
+        }
+        tc::fence_after_sync();
+        uint32_t v[BN];
 #pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          float x = __uint_as_float(v[c]) * sc2;
-          if (need_mask) {
-            const int i = kb + c;
-            if (i >= lim || i > off + jq) x = -CUDART_INF_F;
+        for (int c = 0; c < BN / 32; ++c)
+          tc::tmem_ld32(t_lane + (uint32_t)(buf * BN + c * 32), v + c * 32);
+        tc::tmem_ld_wait();
+        tc::fence_before_sync();
+        tc::mbar_arrive(bar_tempty(u, buf));
+        if (MODE != kLse) {
+          // the other buffer's readers finished tile it-1 before the barrier above
+          if (it + 1 < ntiles) cbuf[((it + 1) & 1) * BN + e] = cn1;
+          cn1 = cn2;
+          if (it + 3 < ntiles) cn2 = col_const(it + 3);
+        }
+
+        if (MODE == kLse) {
+          const bool ctx = it < n_ctx;
+          const int kb = ctx ? it * BN : a.T + (it - n_ctx) * BN;
+          const int lim = ctx ? a.T : n_k;
+          if ((kb + BN > lim) || (kb + BN - 1 > off + rbase)) {
+#pragma unroll
+            for (int c = 0; c < BN; ++c) {
+              const int i = kb + c;
+              if (i >= lim || i > off + ra) v[c] = __float_as_uint(-CUDART_INF_F);
+            }
           }
-          v[c] = __float_as_uint(x);
-          mt = fmaxf(mt, x);
-        }
-        const float mn = fmaxf(m, mt);
-        ssum *= fast_exp2(m - mn);
-        m = mn;
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+          float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
 #pragma unroll
-        for (int c = 0; c < BN; c += 4) {
-          s0 += fast_exp2(__uint_as_float(v[c]) - m);
-          s1 += fast_exp2(__uint_as_float(v[c + 1]) - m);
-          s2 += fast_exp2(__uint_as_float(v[c + 2]) - m);
-          s3 += fast_exp2(__uint_as_float(v[c + 3]) - m);
+          for (int c = 0; c < BN; c += 8) {
+            mx0 = max3(mx0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+            mx1 = max3(mx1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+            mx2 = max3(mx2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+            mx3 = max3(mx3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
+          }
+          const float mn = fmaxf(m, max3(mx0, mx1, fmaxf(mx2, mx3)) * sc2);
+          ssum *= fast_exp2(m - mn);
+          m = mn;
+          const float2 k2 = make_float2(sc2, sc2), nm = make_float2(-m, -m);
+          float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+#pragma unroll
+          for (int c = 0; c < BN; c += 8) {
+            const float2 y0 = __ffma2_rn(f2(v[c], v[c + 1]), k2, nm);
+            const float2 y1 = __ffma2_rn(f2(v[c + 2], v[c + 3]), k2, nm);
+            const float2 y2 = __ffma2_rn(f2(v[c + 4], v[c + 5]), k2, nm);
+            const float2 y3 = __ffma2_rn(f2(v[c + 6], v[c + 7]), k2, nm);
+            a0 = __fadd2_rn(a0, make_float2(fast_exp2(y0.x), fast_exp2(y0.y)));
+            a1 = __fadd2_rn(a1, make_float2(fast_exp2(y1.x), fast_exp2(y1.y)));
+            a2 = __fadd2_rn(a2, make_float2(fast_exp2(y2.x), fast_exp2(y2.y)));
+            a3 = __fadd2_rn(a3, make_float2(fast_exp2(y3.x), fast_exp2(y3.y)));
+          }
+          a0 = __fadd2_rn(__fadd2_rn(a0, a1), __fadd2_rn(a2, a3));
+          ssum += a0.x + a0.y;
+        } else if (MODE == kMax) {
+          const float4* c4 = reinterpret_cast<const float4*>(cbuf + (it & 1) * BN);
+          const float2 sv = make_float2(scale, scale);
+          float r0 = r, r1 = -CUDART_INF_F, r2 = -CUDART_INF_F, r3 = -CUDART_INF_F;
+#pragma unroll
+          for (int q = 0; q < BN / 4; q += 2) {
+            const float4 ca = c4[q], cb = c4[q + 1];
+            const float2 y0 = __ffma2_rn(f2(v[4 * q], v[4 * q + 1]), sv, make_float2(ca.x, ca.y));
+            const float2 y1 = __ffma2_rn(f2(v[4 * q + 2], v[4 * q + 3]), sv, make_float2(ca.z, ca.w));
+            const float2 y2 = __ffma2_rn(f2(v[4 * q + 4], v[4 * q + 5]), sv, make_float2(cb.x, cb.y));
+            const float2 y3 = __ffma2_rn(f2(v[4 * q + 6], v[4 * q + 7]), sv, make_float2(cb.z, cb.w));
+            r0 = max3(r0, y0.x, y0.y);
+            r1 = max3(r1, y1.x, y1.y);
+            r2 = max3(r2, y2.x, y2.y);
+            r3 = max3(r3, y3.x, y3.y);
+          }
+          r = fmaxf(max3(r0, r1, r2), r3);
+          if ((it + 1) % per_head == 0) {  // last query tile of this head
+            tot = fmaxf(tot, r + lv);
+            r = -CUDART_INF_F;
+            if (it + 1 < ntiles) lv = ln_vn(it + 1);
+          }
+        } else {
+          const float4* c4 = reinterpret_cast<const float4*>(cbuf + (it & 1) * BN);
+          const int j0 = (qt_begin + it % per_head) * BN;
+          const bool need_band = j0 < rbase + BM - 1 + a.w;
+          const int jlim = ra + a.w - j0;  // columns c < jlim are inside the window
+          const float2 k2 = make_float2(sc2, sc2);
+          float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+#pragma unroll
+          for (int q = 0; q < BN / 4; ++q) {
+            const float4 cc = c4[q];
+            const float2 y0 = __ffma2_rn(f2(v[4 * q], v[4 * q + 1]), k2, make_float2(cc.x, cc.y));
+            const float2 y1 = __ffma2_rn(f2(v[4 * q + 2], v[4 * q + 3]), k2, make_float2(cc.z, cc.w));
+            float e0 = fast_exp2(y0.x), e1 = fast_exp2(y0.y);
+            float e2 = fast_exp2(y1.x), e3 = fast_exp2(y1.y);
+            if (need_band) {
+              if (4 * q < jlim) e0 = 0.f;
+              if (4 * q + 1 < jlim) e1 = 0.f;
+              if (4 * q + 2 < jlim) e2 = 0.f;
+              if (4 * q + 3 < jlim) e3 = 0.f;
+            }
+            a0 = __fadd2_rn(a0, make_float2(e0, e1));
+            a1 = __fadd2_rn(a1, make_float2(e2, e3));
+          }
+          a0 = __fadd2_rn(a0, a1);
+          f += a0.x + a0.y;
         }
-        ssum += (s0 + s1) + (s2 + s3);
+      }
+
+      if (failed) {
+        atomicCAS(&g_attn_error, 0, (int)kErrWaitTimeout);
+      } else if (MODE == kLse) {
+        if (ra < a.n_q) a.out[(size_t)(l * a.Hq + hq_a) * a.n_q + ra] = (m + fast_log2(ssum)) * kLn2;
       } else if (MODE == kMax) {
-        const float4* c4 = reinterpret_cast<const float4*>(cbuf + (it & 1) * BN);
-        float r0 = r, r1 = -CUDART_INF_F;
-#pragma unroll
-        for (int q = 0; q < BN / 4; ++q) {
-          const float4 cc = c4[q];
-          r0 = fmaxf(r0, fmaxf(fmaf(__uint_as_float(v[4 * q]), scale, cc.x),
-                               fmaf(__uint_as_float(v[4 * q + 1]), scale, cc.y)));
-          r1 = fmaxf(r1, fmaxf(fmaf(__uint_as_float(v[4 * q + 2]), scale, cc.z),
-                               fmaf(__uint_as_float(v[4 * q + 3]), scale, cc.w)));
-        }
-        r = fmaxf(r0, r1);
-        if ((it + 1) % per_head == 0) {  // last query tile of this head
-          float lv = 0.f;
-          if (a.vnorm && ik < a.T)
-            lv = logf(a.vnorm[(size_t)(l * a.Hq + hk * G + it / per_head) * a.T + ik]);
-          tot = fmaxf(tot, r + lv);
-          r = -CUDART_INF_F;
+        if (ra < a.T) {
+          float* o = a.out + (size_t)(l * a.Hkv + hk) * a.T + ra;
+          *o = a.accumulate ? fmaxf(*o, tot) : tot;
         }
       } else {
-        const float4* c4 = reinterpret_cast<const float4*>(cbuf + (it & 1) * BN);
-        const int j0 = (qt_begin + it % per_head) * BN;
-        const bool need_band = j0 < row0 + BM - 1 + a.w;
-        const int jlim = ik + a.w - j0;  // columns c < jlim are inside the window
-        float f0 = 0.f, f1 = 0.f;
-#pragma unroll
-        for (int q = 0; q < BN / 4; ++q) {
-          const float4 cc = c4[q];
-          float e0 = fast_exp2(fmaf(__uint_as_float(v[4 * q]), sc2, cc.x));
-          float e1 = fast_exp2(fmaf(__uint_as_float(v[4 * q + 1]), sc2, cc.y));
-          float e2 = fast_exp2(fmaf(__uint_as_float(v[4 * q + 2]), sc2, cc.z));
-          float e3 = fast_exp2(fmaf(__uint_as_float(v[4 * q + 3]), sc2, cc.w));
-          if (need_band) {
-            if (4 * q < jlim) e0 = 0.f;
-            if (4 * q + 1 < jlim) e1 = 0.f;
-            if (4 * q + 2 < jlim) e2 = 0.f;
-            if (4 * q + 3 < jlim) e3 = 0.f;
-          }
-          f0 += e0 + e1;
-          f1 += e2 + e3;
-        }
-        f += f0 + f1;
+        if (ra < a.T) a.out[(size_t)(l * a.Hkv + hk) * a.T + ra] = f;
       }
-    }
-
-    if (failed) {
-      atomicCAS(&g_attn_error, 0, (int)kErrWaitTimeout);
-    } else if (MODE == kLse) {
-      if (jq < a.n_q) a.out[(size_t)(l * a.Hq + hq_a) * a.n_q + jq] = (m + fast_log2(ssum)) * kLn2;
-    } else if (MODE == kMax) {
-      if (ik < a.T) {
-        float* o = a.out + (size_t)(l * a.Hkv + hk) * a.T + ik;
-        *o = a.accumulate ? fmaxf(*o, tot) : tot;
-      }
-    } else {
-      if (ik < a.T) a.out[(size_t)(l * a.Hkv + hk) * a.T + ik] = f;
     }
   }
 
@@ -404,7 +462,7 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
   }
   if (e != cudaSuccess) return e;
   const int rows = (MODE == kLse) ? a.n_q : a.T;
-  dim3 grid((rows + BM - 1) / BM, MODE == kLse ? a.Hq : a.Hkv, a.L);
+  dim3 grid((rows + BM * MSUB - 1) / (BM * MSUB), MODE == kLse ? a.Hq : a.Hkv, a.L);
   auto kern = attn_tc_kernel<D, MODE>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
