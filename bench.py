@@ -22,6 +22,9 @@ point is then timed on its own (same rules) for the roofline of the dominant ker
 memory: host->device copies of every input and a device->host read of the results are
 inside the timed region.  `cpu_baseline` times the fp64 CPU oracle on a bounded sample.
 
+The step is replayed from a CUDA graph captured once (``--no-graph`` launches every
+call from Python instead); each entry point's timing also replays its own graph.
+
 `--impl reference` times the CPU oracle itself (the only reference implementation: the
 pages ship no code) on the machine's host cores, each step a bounded sample of the workload.
 Under torchrun (N > 1) every rank runs its own replica of the workload (weak scaling; the
@@ -56,6 +59,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--stage-reps", type=int, default=None)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch every call from Python instead of replaying a CUDA graph")
     return ap.parse_args()
 
 
@@ -113,6 +118,24 @@ def compaction_bytes(p, wl):
 def prune_bytes(p, wl):
     n = len(p.masks) if hasattr(p, "masks") else 1
     return n * p.L * wl.H_kv * wl.T * (4 + 1)
+
+
+# ----------------------------------------------------------------------------- ranks
+
+def max_over_ranks(value, world, device="cpu"):
+    """Maximum of a per-rank timing over all ranks (the slowest rank sets the step)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(units_per_rank, world, ms_step):
+    """Units processed by all ranks per second, timed by the slowest rank."""
+    return world * units_per_rank / (ms_step / 1e3)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -219,13 +242,20 @@ def run_gpu(args, rank, world, local):
     for _ in range(Wm):
         p.step()
     torch.cuda.synchronize()
+    n_before = C.kvs_launch_count()
+    p.step()
+    torch.cuda.synchronize()
+    launches = C.kvs_launch_count() - n_before
+    step_fn = p.step if args.no_graph else capture(p.step)
+    for _ in range(Wm):
+        step_fn()
+    torch.cuda.synchronize()
 
     # ---------------------------------------------------------------- timed steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
     props = torch.cuda.get_device_properties(dev)
     gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else local
-    n0 = C.kvs_launch_count()
     with ClockSampler(gpu_id) as clk:
         barrier()
         torch.cuda.synchronize()
@@ -233,35 +263,32 @@ def run_gpu(args, rank, world, local):
         for i in range(K):
             flush.fill_(float(i))
             ev[i][0].record(stream)
-            p.step()
+            step_fn()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
         t1 = time.time()
         barrier()
-    launches = (C.kvs_launch_count() - n0) // K
-    ms = sum(a.elapsed_time(b) for a, b in ev)
-    if world > 1:
-        tmax = torch.tensor([ms], device=dev)
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-        ms = float(tmax.item())
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), world, dev)
     ms_step = ms / K
-    value = world * wl.T * p.L / (ms_step / 1e3)
+    value = whole_job_value(wl.T * p.L, world, ms_step)
 
     # ---------------------------------------------------------------- per entry point
     reps = args.stage_reps or max(3, min(50, K))
     work = algorithmic_work(wl, p)
     stage_ms = {}
     for name, fn in p.stages():
+        run = fn if args.no_graph else capture(fn)
+        run()
         e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
              for _ in range(reps)]
         for i in range(reps):
             flush.fill_(float(i))
             e[i][0].record(stream)
-            fn()
+            run()
             e[i][1].record(stream)
         torch.cuda.synchronize()
         stage_ms[name] = sum(a.elapsed_time(b) for a, b in e) / reps
-    p.step()  # leave consistent outputs
+    step_fn()  # leave consistent outputs
     torch.cuda.synchronize()
     work["kvs_compact_paged"] = ("hbm", compaction_bytes(p, wl), "byte")
     if "kvs_prune_mask" in stage_ms:
@@ -312,7 +339,7 @@ def run_gpu(args, rank, world, local):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(wl, x, p, dev, K=min(K, 20), units=world * wl.T * p.L, world=world,
-                      flush=flush)
+                      flush=flush, graph=not args.no_graph)
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -321,6 +348,7 @@ def run_gpu(args, rank, world, local):
         "config": {"workload": f"{wl.name}: {wl.title}", "layers": p.L, "T": wl.T,
                    "H_q": wl.H_q, "H_kv": wl.H_kv, "d": wl.d, "D_h": wl.D_h,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "launch": "python calls" if args.no_graph else "CUDA graph of the step",
                    "l2": f"{L2_FLUSH_BYTES >> 20} MB buffer written between timed steps"},
         "roofline": roofline,
         "kernels": kernels,
@@ -331,7 +359,28 @@ def run_gpu(args, rank, world, local):
     return result, wl, p
 
 
-def run_e2e(wl, x, p, dev, K, units, world, flush):
+def capture(fn):
+    """Record the library calls `fn` enqueues into a CUDA graph; returns its replay.
+    The graph holds exactly the kernels (and memsets) that `fn` launches."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    capture.graphs.append(g)
+    return g.replay
+
+
+capture.graphs = []
+
+
+def run_e2e(wl, x, p, dev, K, units, world, flush, graph=True):
     """Same step through the same calls, inputs from pinned host memory: the H2D copies
     of every input and the D2H read of the results are inside the timed region."""
     import torch
@@ -357,6 +406,7 @@ def run_e2e(wl, x, p, dev, K, units, world, flush):
     bi = sum(h.numel() * h.element_size() for h, _ in pairs)
     bo = sum(o.numel() * o.element_size() for o in outs)
     stream = torch.cuda.current_stream()
+    step_fn = capture(p.step) if graph else p.step
     tot = 0.0
     for i in range(K + 2):
         flush.fill_(float(i))
@@ -365,7 +415,7 @@ def run_e2e(wl, x, p, dev, K, units, world, flush):
         a.record(stream)
         for h, d in pairs:
             d.copy_(h, non_blocking=True)
-        p.step()
+        step_fn()
         for o, oh in zip(outs, outs_h):
             oh.copy_(o, non_blocking=True)
         b.record(stream)
@@ -379,52 +429,86 @@ def run_e2e(wl, x, p, dev, K, units, world, flush):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def oracle_sample(wl, x_host_layer):
-    """One bounded sample of the workload on the CPU oracle.  Returns (seconds, tokens
-    scored per layer-equivalent, description)."""
+def oracle_sample(wl, x, frac=1.0):
+    """Time the CPU oracle on a bounded sample of the workload (layer 0).
+
+    kvzip kinds: KV-head group 0 (its g query heads), the first max(1, frac*n_q) scoring
+    queries of the block (tail keys trimmed so the causal offset is unchanged), all T
+    context keys; vnorm of those heads, LSE, score, then top-k/threshold + compaction of
+    the group's score row.  The query-proportional parts are scaled by n_q / n_sub (and
+    the chunks), and everything by the number of groups.  future: the first frac*T tokens
+    of group 0 (cost ~ n^2, scaled by (T/n)^2 and the groups).  kvzap: the first frac*T
+    tokens of layer 0 (all heads), scaled by T/n.
+    Returns (seconds per layer, tokens per layer, description)."""
     import numpy as np
+    import torch
 
     import oracle as O
 
     def f64(t):
-        return O.bf16_bits_to_f64(t.contiguous().view(__import__("torch").int16).numpy()
-                                  .view(np.uint16))
-    x = x_host_layer
-    t0 = time.perf_counter()
-    if wl.kind in ("kvzip", "kvzip_plus"):
-        q, kc, kt = f64(x["q"]), f64(x["k_ctx"]), f64(x["k_tail"])
-        vn = O.value_norm(f64(x["v_ctx"]), f64(x["w_o"]), wl.H_q) if "w_o" in x else None
+        return O.bf16_bits_to_f64(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+
+    def i16(t):
+        return t.contiguous().view(torch.int16).numpy()
+
+    tick = time.perf_counter
+    if wl.kind in ("kvzip", "kvzip_plus", "kvzip_plus_chunked"):
+        g, d = wl.g, wl.d
+        chunked = wl.kind == "kvzip_plus_chunked"
+        q_all = x["q"][0] if chunked else x["q"]
+        kt_all = x["k_tail"][0] if chunked else x["k_tail"]
+        h_all = (x["h"][0] if chunked else x["h"]) if "h" in x else None
+        n_q = q_all.shape[2]
+        n_sub = max(1, min(n_q, int(round(frac * n_q))))
+        trim = n_q - n_sub
+        q = f64(q_all[:, 0:g, :n_sub])
+        kt = f64(kt_all[:, 0:1, : kt_all.shape[2] - trim])
+        kc = f64(x["k_ctx"][:, 0:1])
+        t0 = tick()
+        vn = O.value_norm(f64(x["v_ctx"][:, 0:1]), f64(x["w_o"][:, :, 0:g * d]), g) \
+            if "w_o" in x else None
+        t1 = tick()
         lse = O.lse(q, kc, kt)
-        s = O.kvzip_score(q, kc, kt, lse_=lse, vnorm=vn, h=f64(x["h"]) if "h" in x else None)
-        for r in wl.keep_ratios:
-            m, _ = O.prune_topk(s, wl.topk_budget(r), wl.w)
-            O.compact_paged(x["k_ctx"].view(__import__("torch").int16).numpy(),
-                            x["v_ctx"].view(__import__("torch").int16).numpy(), m, wl.page_size)
-        return time.perf_counter() - t0, wl.T, "1 full layer (all heads): vnorm, lse, " \
-            "score, top-k and compaction at every budget"
-    if wl.kind == "kvzip_plus_chunked":
-        # one chunk of one KV-head group of one layer; scaled by chunks x groups
-        g = wl.g
-        q = f64(x["q"][0][:, 0:g]); kt = f64(x["k_tail"][0][:, 0:1]); kc = f64(x["k_ctx"][:, 0:1])
-        vn = O.value_norm(f64(x["v_ctx"][:, 0:1]), f64(x["w_o"][:, :, 0:g * wl.d]), g)
-        s = O.kvzip_score(q, kc, kt, vnorm=vn, h=f64(x["h"][0]))
-        dt = (time.perf_counter() - t0) * wl.n_chunks * wl.H_kv
-        return dt, wl.T, "1 chunk x 1 KV-head group of layer 0, scaled x(chunks*groups)"
+        s = O.kvzip_score(q, kc, kt, lse_=lse, vnorm=vn,
+                          h=f64(h_all[:, :n_sub]) if h_all is not None else None)
+        t2 = tick()
+        if wl.keep_ratios:
+            for r in wl.keep_ratios:
+                m, _ = O.prune_topk(s, wl.topk_budget(r), wl.w)
+                O.compact_paged(i16(x["k_ctx"][:, 0:1]), i16(x["v_ctx"][:, 0:1]), m, wl.page_size)
+        else:
+            tau = O.quantile_lower(s[..., : wl.T - wl.w], wl.tau_quantile)
+            m, _ = O.prune_threshold(s, tau, wl.w)
+            O.compact_paged(i16(x["k_ctx"][:, 0:1]), i16(x["v_ctx"][:, 0:1]), m, wl.page_size)
+        t3 = tick()
+        chunks = wl.n_chunks if chunked else 1
+        dt = wl.H_kv * ((t1 - t0) + (t2 - t1) * (n_q / n_sub) * chunks + (t3 - t2))
+        desc = (f"layer 0, KV-head group 0 ({g} query heads), {n_sub} of {n_q} scoring queries"
+                f"{' of chunk 0' if chunked else ''}: vnorm, LSE, score, "
+                f"{'top-k' if wl.keep_ratios else 'threshold'} + compaction; query-proportional "
+                f"time scaled x{n_q / n_sub * chunks:g}, all x{wl.H_kv} groups")
+        return dt, wl.T, desc
     if wl.kind == "future":
         g = wl.g
-        q = f64(x["q"][:, 0:g, :4096]); k = f64(x["k"][:, 0:1, :4096])
+        n = max(256, min(wl.T, int(round(frac * wl.T))))
+        t0 = tick()
+        q = f64(x["q"][:, 0:g, :n]); k = f64(x["k"][:, 0:1, :n])
         f = O.future_attention_mass(q, k, wl.w)
-        dt = (time.perf_counter() - t0) * wl.H_kv * (wl.T / 4096) ** 2
-        return dt, wl.T, "first 4096 tokens of 1 KV-head group of layer 0, scaled x(groups*(T/4096)^2)"
+        for r in wl.keep_ratios:
+            m, _ = O.prune_topk(f, int(r * n + 0.5), wl.w)
+            O.compact_paged(i16(x["k"][:, 0:1, :n]), i16(x["v"][:, 0:1, :n]), m, wl.page_size)
+        dt = (tick() - t0) * wl.H_kv * (wl.T / n) ** 2
+        return dt, wl.T, (f"layer 0, KV-head group 0, first {n} of {wl.T} tokens: LSE, future mass, "
+                          f"top-k + compaction; scaled x{wl.H_kv}*(T/{n})^2")
     if wl.kind == "kvzap":
-        n = 16384
+        n = max(1024, min(wl.T, int(round(frac * wl.T))))
+        t0 = tick()
         z = O.linear_surrogate(f64(x["h"][:, :n]), f64(x["W"]), x["b"].double().numpy())
         m, _ = O.prune_threshold(z, wl.tau, wl.w)
-        import torch
-        O.compact_paged(x["k"][:, :, :n].contiguous().view(torch.int16).numpy(),
-                        x["v"][:, :, :n].contiguous().view(torch.int16).numpy(), m, wl.page_size)
-        dt = (time.perf_counter() - t0) * (wl.T / n)
-        return dt, wl.T, f"first {n} tokens of layer 0 (surrogate, threshold, compaction), scaled x(T/{n})"
+        O.compact_paged(i16(x["k"][:, :, :n]), i16(x["v"][:, :, :n]), m, wl.page_size)
+        dt = (tick() - t0) * (wl.T / n)
+        return dt, wl.T, (f"layer 0, first {n} of {wl.T} tokens (all heads): surrogate, threshold, "
+                          f"compaction; scaled x(T/{n})")
     raise ValueError(wl.kind)
 
 
@@ -440,32 +524,48 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+CPU_BASELINE_FRAC = {"c1": 1.0, "c2": 1.0, "c3": 1 / 8, "c4": 1 / 4, "c5": 1 / 8}
+
+
 def run_cpu_baseline(wl):
     x = host_layer0(wl)
-    dt, tokens, desc = oracle_sample(wl, x)
+    dt, tokens, desc = oracle_sample(wl, x, CPU_BASELINE_FRAC[wl.name])
     return {"value": round(tokens / dt, 2), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "sample": desc + f"; {dt:.2f} s per layer-equivalent; numpy fp64 (BLAS threads = "
-                             f"host cores, elementwise single-threaded)"}
+            "sample": desc + f"; {dt:.2f} s per layer; numpy fp64 (BLAS threads = host cores, "
+                             "elementwise single-threaded)"}
+
+
+REFERENCE_BUDGET_S = 120.0
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, timed on the host cores.  The sample of each
+    step shrinks so that warm-up + timed steps take about REFERENCE_BUDGET_S seconds."""
     if rank != 0:
         return None
     from kv_cache_eviction_lse_gb300 import workloads as W
     wl = W.WORKLOADS[args.workload]
     K = args.steps or 3
-    Wm = max(3, args.warmup) if args.warmup is not None else 3
+    Wm = max(3, args.warmup)
     x = host_layer0(wl)
-    for _ in range(Wm if wl.kind in ("kvzip", "kvzap") else 1):
-        oracle_sample(wl, x)
-    times = []
+    frac = CPU_BASELINE_FRAC[wl.name]
+    t = time.perf_counter()
+    oracle_sample(wl, x, frac / 8)
+    probe = time.perf_counter() - t
+    per_step = REFERENCE_BUDGET_S / (K + Wm)
+    frac = max(frac / 64, min(frac, frac / 8 * per_step / max(probe, 1e-6)))
+    for _ in range(Wm):
+        oracle_sample(wl, x, frac)
+    times, wall, desc = [], [], ""
     for _ in range(K):
-        dt, tokens, desc = oracle_sample(wl, x)
+        t = time.perf_counter()
+        dt, tokens, desc = oracle_sample(wl, x, frac)
+        wall.append(time.perf_counter() - t)
         times.append(dt)
     ms = 1e3 * statistics.mean(times)
     value = wl.T / (ms / 1e3)
     cb = {"value": round(value, 2), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-          "sample": desc}
+          "sample": desc + f"; {statistics.mean(wall):.2f} s of CPU work per step"}
     return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
             "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": round(ms, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
