@@ -59,6 +59,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--stage-reps", type=int, default=None)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run only the first N layers (profiling on a smaller case)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every call from Python instead of replaying a CUDA graph")
     return ap.parse_args()
@@ -233,6 +235,8 @@ def run_gpu(args, rank, world, local):
             dist.barrier()
 
     wl = W.WORKLOADS[args.workload]
+    if args.layers:
+        wl = wl.scaled(L=min(args.layers, wl.L))
     K = args.steps or DEFAULT_STEPS[args.workload]
     Wm = max(3, args.warmup)
     x, p = build_pipeline(wl, dev)

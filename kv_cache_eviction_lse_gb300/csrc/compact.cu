@@ -3,7 +3,7 @@
 // lengths need PagedAttention-like storage).
 //
 // Three launches, all bandwidth-bound:
-//   1. seg_count   : kept tokens per (row, 4096-token segment)         reads the mask
+//   1. seg_count   : kept tokens per (row, segment of 1024 or 4096 tokens)  reads the mask
 //   2. page_plan   : per-row exclusive scan of segment counts, page counts
 //                    ceil(kept/page), exclusive scan of pages over rows (layer-major,
 //                    then head), capacity check, seq_lens, needed_pages
@@ -17,8 +17,10 @@
 namespace kvs {
 namespace {
 
-constexpr int kSeg = 4096;      // tokens per segment
-constexpr int kSegThreads = 256;  // 16 mask bytes per thread
+constexpr int kSegThreads = 256;  // P mask bytes per thread, segments of 256 * P tokens
+constexpr int kMinSeg = 1024;     // short rows: P = 4
+constexpr int kMaxSeg = 4096;     // long rows (T >= kLongRow): P = 16, fewer, larger blocks
+constexpr int kLongRow = 8192;
 
 struct Plan {            // lives at the start of the workspace
   int ok;                // total pages <= capacity
@@ -26,25 +28,44 @@ struct Plan {            // lives at the start of the workspace
   int pad[2];
 };
 
-__device__ __forceinline__ int nonzero_bytes(uint32_t w) { return __popc(__vcmpne4(w, 0u)) >> 3; }
+
+// Mask bytes t0 .. t0+P-1 of a row as 0/1 flags (vector loads when T allows).
+template <int P>
+__device__ __forceinline__ void load_flags(const uint8_t* m, int T, int t0, uint8_t* f) {
+  if ((T & (P - 1)) == 0 && t0 < T) {
+    uint32_t wd[P / 4];
+    if constexpr (P == 16) {
+      const uint4 u = *reinterpret_cast<const uint4*>(m + t0);
+      wd[0] = u.x;
+      wd[1] = u.y;
+      wd[2] = u.z;
+      wd[3] = u.w;
+    } else {
+      static_assert(P == 4, "4 or 16 mask bytes per thread");
+      wd[0] = *reinterpret_cast<const uint32_t*>(m + t0);
+    }
+#pragma unroll
+    for (int i = 0; i < P; ++i) f[i] = ((wd[i >> 2] >> (8 * (i & 3))) & 255u) != 0;
+  } else {
+#pragma unroll
+    for (int i = 0; i < P; ++i) f[i] = (t0 + i < T) ? (m[t0 + i] != 0) : 0;
+  }
+}
 
 // Kept count of each (row, segment).
+template <int P>
 __global__ void __launch_bounds__(kSegThreads) seg_count_kernel(const uint8_t* __restrict__ mask,
                                                                 int T, int nseg,
                                                                 int* __restrict__ seg) {
   __shared__ int red[kSegThreads / 32];
   const int s = blockIdx.x, row = blockIdx.y;
   const uint8_t* m = mask + (size_t)row * T;
-  const int t0 = s * kSeg + threadIdx.x * 16;
+  const int t0 = s * (kSegThreads * P) + threadIdx.x * P;
+  uint8_t f[P];
+  load_flags<P>(m, T, t0, f);
   int c = 0;
-  if ((T & 15) == 0) {
-    if (t0 < T) {
-      const uint4 u = *reinterpret_cast<const uint4*>(m + t0);
-      c = nonzero_bytes(u.x) + nonzero_bytes(u.y) + nonzero_bytes(u.z) + nonzero_bytes(u.w);
-    }
-  } else {
-    for (int t = t0; t < min(t0 + 16, T); ++t) c += m[t] != 0;
-  }
+#pragma unroll
+  for (int i = 0; i < P; ++i) c += f[i];
   c = warp_sum_int(c);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = c;
   __syncthreads();
@@ -114,12 +135,14 @@ __global__ void __launch_bounds__(1024) page_plan_kernel(int rows, int nseg, int
   }
 }
 
+template <int P>
 __global__ void __launch_bounds__(kSegThreads) scatter_kernel(
     const bf16_t* __restrict__ k, const bf16_t* __restrict__ v, const uint8_t* __restrict__ mask,
     int T, int d, int nseg, int page_size, const int* __restrict__ seg,
     const int* __restrict__ first_page, const Plan* __restrict__ plan,
     const int* __restrict__ seq_lens, bf16_t* __restrict__ k_pages, bf16_t* __restrict__ v_pages,
     int* __restrict__ block_table, int max_pages) {
+  constexpr int kSeg = kSegThreads * P;
   __shared__ uint16_t list[kSeg];
   __shared__ int red[33];
   const int s = blockIdx.x, row = blockIdx.y;
@@ -141,20 +164,12 @@ __global__ void __launch_bounds__(kSegThreads) scatter_kernel(
 
   // ordered ranks of the kept tokens of this segment
   const uint8_t* m = mask + (size_t)row * T;
-  const int t0 = s * kSeg + threadIdx.x * 16;
-  uint8_t f[16];
-  if ((T & 15) == 0 && t0 < T) {
-    const uint4 u = *reinterpret_cast<const uint4*>(m + t0);
-    const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 16; ++i) f[i] = ((wd[i >> 2] >> (8 * (i & 3))) & 255u) != 0;
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) f[i] = (t0 + i < T) ? (m[t0 + i] != 0) : 0;
-  }
+  const int t0 = s * kSeg + threadIdx.x * P;
+  uint8_t f[P];
+  load_flags<P>(m, T, t0, f);
   int c = 0;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) c += f[i];
+  for (int i = 0; i < P; ++i) c += f[i];
   // block exclusive scan of c
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   int incl = c;
@@ -180,8 +195,8 @@ __global__ void __launch_bounds__(kSegThreads) scatter_kernel(
   int pos = red[warp] + incl - c;
   const int n_local = red[32];
 #pragma unroll
-  for (int i = 0; i < 16; ++i)
-    if (f[i]) list[pos++] = (uint16_t)(threadIdx.x * 16 + i);
+  for (int i = 0; i < P; ++i)
+    if (f[i]) list[pos++] = (uint16_t)(threadIdx.x * P + i);
   __syncthreads();
 
   // cooperative copy: (d/8) 16-byte chunks per kept row, for K and V
@@ -229,7 +244,7 @@ __global__ void __launch_bounds__(kSegThreads) scatter_kernel(
 }  // namespace
 
 size_t compact_workspace_bytes(int rows, int T) {
-  const int nseg = (T + kSeg - 1) / kSeg;
+  const int nseg = (T + kMinSeg - 1) / kMinSeg;  // the finer segmentation bounds both
   return sizeof(Plan) + sizeof(int) * ((size_t)rows * (nseg > 0 ? nseg : 1) + rows);
 }
 
@@ -238,17 +253,27 @@ cudaError_t launch_compact(const bf16_t* k, const bf16_t* v, int rows, int T, in
                            int capacity, int* block_table, int max_pages, int* seq_lens,
                            int* needed, void* ws, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  const int nseg = T > 0 ? (T + kSeg - 1) / kSeg : 1;
+  const bool long_rows = T >= kLongRow;
+  const int seg_len = long_rows ? kMaxSeg : kMinSeg;
+  const int nseg = T > 0 ? (T + seg_len - 1) / seg_len : 1;
   Plan* plan = reinterpret_cast<Plan*>(ws);
   int* seg = reinterpret_cast<int*>(plan + 1);
   int* first = seg + (size_t)rows * nseg;
   count_launches(3);
-  seg_count_kernel<<<dim3(nseg, rows), kSegThreads, 0, s>>>(mask, T, nseg, seg);
+  if (long_rows)
+    seg_count_kernel<16><<<dim3(nseg, rows), kSegThreads, 0, s>>>(mask, T, nseg, seg);
+  else
+    seg_count_kernel<4><<<dim3(nseg, rows), kSegThreads, 0, s>>>(mask, T, nseg, seg);
   page_plan_kernel<<<1, 1024, 0, s>>>(rows, nseg, page_size, capacity, seg, first, plan, seq_lens,
                                       needed);
-  scatter_kernel<<<dim3(nseg, rows), kSegThreads, 0, s>>>(k, v, mask, T, d, nseg, page_size, seg,
-                                                          first, plan, seq_lens, k_pages, v_pages,
-                                                          block_table, max_pages);
+  if (long_rows)
+    scatter_kernel<16><<<dim3(nseg, rows), kSegThreads, 0, s>>>(
+        k, v, mask, T, d, nseg, page_size, seg, first, plan, seq_lens, k_pages, v_pages,
+        block_table, max_pages);
+  else
+    scatter_kernel<4><<<dim3(nseg, rows), kSegThreads, 0, s>>>(
+        k, v, mask, T, d, nseg, page_size, seg, first, plan, seq_lens, k_pages, v_pages,
+        block_table, max_pages);
   return cudaGetLastError();
 }
 

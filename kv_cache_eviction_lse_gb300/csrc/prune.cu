@@ -59,22 +59,49 @@ __device__ int block_excl_scan_flag(bool f, int* red, int* total) {
   return red[warp] + in_warp;
 }
 
-__global__ void __launch_bounds__(kPruneThreads) threshold_kernel(const float* __restrict__ score,
-                                                                  int T, float tau, int w,
-                                                                  uint8_t* __restrict__ mask,
-                                                                  int* __restrict__ keep) {
+constexpr int kThrThreads = 256;
+constexpr int kThrPer = 16;  // tokens per thread
+
+// Grid (chunks of 4096 tokens, rows).  keep[row] must be zero on entry (the launcher
+// clears it); each block adds its count with one atomic.
+__global__ void __launch_bounds__(kThrThreads) threshold_kernel(const float* __restrict__ score,
+                                                                int T, float tau, int w,
+                                                                uint8_t* __restrict__ mask,
+                                                                int* __restrict__ keep) {
   __shared__ int red[33];
-  const size_t row = blockIdx.x;
+  const size_t row = blockIdx.y;
   const float* s = score + row * T;
   uint8_t* m = mask + row * T;
+  const int t0 = (blockIdx.x * kThrThreads + threadIdx.x) * kThrPer;
   int cnt = 0;
-  for (int t = threadIdx.x; t < T; t += blockDim.x) {
-    const int k = (s[t] >= tau) || (t >= T - w);
-    m[t] = (uint8_t)k;
-    cnt += k;
+  if ((T & 15) == 0) {
+    if (t0 < T) {
+      uint32_t mb[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = *reinterpret_cast<const float4*>(s + t0 + 4 * q);
+        const float x[4] = {v.x, v.y, v.z, v.w};
+        uint32_t word = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = t0 + 4 * q + e;
+          const uint32_t k = (x[e] >= tau) || (t >= T - w);
+          word |= k << (8 * e);
+          cnt += (int)k;
+        }
+        mb[q] = word;
+      }
+      *reinterpret_cast<uint4*>(m + t0) = make_uint4(mb[0], mb[1], mb[2], mb[3]);
+    }
+  } else {
+    for (int t = t0; t < min(t0 + kThrPer, T); ++t) {
+      const int k = (s[t] >= tau) || (t >= T - w);
+      m[t] = (uint8_t)k;
+      cnt += k;
+    }
   }
   cnt = block_sum(cnt, red);
-  if (threadIdx.x == 0) keep[row] = cnt;
+  if (threadIdx.x == 0 && cnt) atomicAdd(keep + row, cnt);
 }
 
 __global__ void __launch_bounds__(kPruneThreads) topk_kernel(const float* __restrict__ score,
@@ -109,15 +136,34 @@ __global__ void __launch_bounds__(kPruneThreads) topk_kernel(const float* __rest
         if ((u & hi_mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
       }
       __syncthreads();
-      if (threadIdx.x == 0) {
-        int r = s_rem, cum = 0, dig = 0;
-        for (dig = 255; dig >= 0; --dig) {
-          const int c = (int)hist[dig];
-          if (cum + c >= r) break;
-          cum += c;
+      if (threadIdx.x < 32) {
+        // lane l owns digits 255-8l .. 248-8l; find the digit at which the count of
+        // keys from the top reaches the remaining rank
+        const int lane = threadIdx.x;
+        int c[8], tot = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          c[i] = (int)hist[255 - 8 * lane - i];
+          tot += c[i];
         }
-        s_rem = r - cum;
-        s_prefix = prefix | ((uint32_t)dig << shift);
+        int incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int r = s_rem;
+        const unsigned hit = __ballot_sync(0xffffffffu, incl >= r);
+        const int src = __ffs(hit) - 1;  // first lane whose range reaches rank r
+        if (lane == src) {
+          int cum = incl - tot, i = 0;
+          for (; i < 7; ++i) {
+            if (cum + c[i] >= r) break;
+            cum += c[i];
+          }
+          s_rem = r - cum;
+          s_prefix = prefix | ((uint32_t)(255 - 8 * lane - i) << shift);
+        }
       }
       hi_mask |= 255u << shift;
       __syncthreads();
@@ -157,11 +203,18 @@ __global__ void __launch_bounds__(kPruneThreads) topk_kernel(const float* __rest
 cudaError_t launch_prune(const float* score, int rows, int T, int mode, float tau, int k, int w,
                          uint8_t* mask, int* keep, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  count_launches(1);
-  if (mode == 0)
-    threshold_kernel<<<rows, kPruneThreads, 0, s>>>(score, T, tau, w, mask, keep);
-  else
+  if (mode == 0) {
+    cudaError_t e = cudaMemsetAsync(keep, 0, sizeof(int) * (size_t)rows, s);
+    if (e != cudaSuccess) return e;
+    if (T == 0) return cudaSuccess;
+    const int per_block = kThrThreads * kThrPer;
+    count_launches(1);
+    threshold_kernel<<<dim3((T + per_block - 1) / per_block, rows), kThrThreads, 0, s>>>(
+        score, T, tau, w, mask, keep);
+  } else {
+    count_launches(1);
     topk_kernel<<<rows, kPruneThreads, 0, s>>>(score, T, k, w, mask, keep);
+  }
   return cudaGetLastError();
 }
 

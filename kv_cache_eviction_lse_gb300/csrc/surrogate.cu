@@ -7,8 +7,8 @@
 // HBM bandwidth.  At 8 flop per byte an fp32 CUDA-core dot product would need ~75%
 // of the FMA issue rate just to keep up with HBM, so the per-token contraction
 // against the D_h x H_kv weight runs on warp MMAs (m16n8k16, N = 8 heads).  Each lane
-// loads 64 contiguous bytes of two token rows with 16-byte non-allocating loads and
-// feeds them to the MMA directly as A fragments: the reduction runs over channels,
+// loads 16-byte pieces of two token rows with non-allocating loads and feeds them to
+// the MMA directly as A fragments: the reduction runs over channels,
 // so any channel permutation works as long as the B fragments (W, staged once per
 // block in shared memory) use the same one.  No shared-memory staging of h.
 #include "common.cuh"
@@ -30,8 +30,12 @@ struct SurArgs {
   float tau;
 };
 
-// Shared layout of W: [superblock of 128 channels][n-tile][pair p][lane] x 16 bytes,
-// holding W[sb*128 + 32*t + 8*p + e][nt*8 + g] for e = 0..7 (lane = 4*g + t).
+// Channel permutation: in superblock sb (128 channels), lane (g, t) (lane = 4*g + t) loads
+// channels sb*128 + 32*p + 8*t + e (e = 0..7) of token rows g and g+8 for p = 0..3, so the
+// four lanes of a row read 64 contiguous bytes per load instruction (two full sectors).
+// MMA 2p takes e = 0..3 and MMA 2p+1 takes e = 4..7 as k-slots {2t, 2t+1, 2t+8, 2t+9}.
+// Shared layout of W: [superblock][n-tile][p][lane] x 16 bytes, holding
+// W[sb*128 + 32*p + 8*t + e][nt*8 + g] for e = 0..7: the same permutation.
 template <int NT>
 __global__ void __launch_bounds__(kWarps * 32) surrogate_kernel(const SurArgs a) {
   extern __shared__ uint4 wsm[];
@@ -41,7 +45,7 @@ __global__ void __launch_bounds__(kWarps * 32) surrogate_kernel(const SurArgs a)
   for (int idx = threadIdx.x; idx < nsb * NT * 128; idx += blockDim.x) {
     const int ln = idx & 31, p = (idx >> 5) & 3, nt = (idx >> 7) % NT, sb = (idx >> 7) / NT;
     const int head = nt * 8 + (ln >> 2);
-    const int ch0 = sb * 128 + 32 * (ln & 3) + 8 * p;
+    const int ch0 = sb * 128 + 32 * p + 8 * (ln & 3);
     uint32_t wv[4];
 #pragma unroll
     for (int e2 = 0; e2 < 4; ++e2) {
@@ -67,8 +71,8 @@ __global__ void __launch_bounds__(kWarps * 32) surrogate_kernel(const SurArgs a)
   for (int k = 0; k < a.tiles_per_warp && tile < ntile; ++k, ++tile) {
     const int t0 = tile * 16;
     const int ra = min(t0 + g, a.T - 1), rb = min(t0 + g + 8, a.T - 1);
-    const bf16_t* pa = a.h + ((size_t)l * a.T + ra) * a.Dh + 32 * t4;
-    const bf16_t* pb = a.h + ((size_t)l * a.T + rb) * a.Dh + 32 * t4;
+    const bf16_t* pa = a.h + ((size_t)l * a.T + ra) * a.Dh + 8 * t4;
+    const bf16_t* pb = a.h + ((size_t)l * a.T + rb) * a.Dh + 8 * t4;
     float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
@@ -77,8 +81,8 @@ __global__ void __launch_bounds__(kWarps * 32) surrogate_kernel(const SurArgs a)
       uint4 xa[4], xb[4];
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
-        xa[p] = ld_nc_v4(pa + sb * 128 + 8 * p);
-        xb[p] = ld_nc_v4(pb + sb * 128 + 8 * p);
+        xa[p] = ld_nc_v4(pa + sb * 128 + 32 * p);
+        xb[p] = ld_nc_v4(pb + sb * 128 + 32 * p);
       }
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {

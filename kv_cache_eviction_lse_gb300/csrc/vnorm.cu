@@ -120,10 +120,12 @@ __global__ void __launch_bounds__(256) gram_mma_kernel(const bf16_t* __restrict_
       }
 }
 
-// vn = sqrt(v^T (G_hi + G_lo) v) for 64-token tiles; G_hi, G_lo (bf16, symmetric, so
-// their rows serve directly as the k-contiguous B operand) stay in shared memory while
-// the block walks kTokTiles consecutive token tiles of one (layer, query head).
+// vn = sqrt(v^T (G_hi + G_lo) v) for 128-token tiles (32 per warp, two m16 tiles that
+// share every G fragment); G_hi, G_lo (bf16, symmetric, so their rows serve directly as
+// the k-contiguous B operand) stay in shared memory while the block walks kTokTiles
+// consecutive token tiles of one (layer, query head).
 constexpr int kTokTiles = 4;
+constexpr int kQuadTok = 128;
 
 template <int D>
 __global__ void __launch_bounds__(128) quad_mma_kernel(const bf16_t* __restrict__ v,
@@ -131,8 +133,8 @@ __global__ void __launch_bounds__(128) quad_mma_kernel(const bf16_t* __restrict_
                                                        int Hq, int Hkv, float* __restrict__ vn) {
   constexpr int LD = D + 8;
   extern __shared__ __align__(16) uint8_t qsm[];
-  bf16_t(*gs)[LD] = reinterpret_cast<bf16_t(*)[LD]>(qsm);              // [2D][LD]: hi rows, lo rows
-  bf16_t(*vs)[LD] = reinterpret_cast<bf16_t(*)[LD]>(qsm + 2 * D * LD * 2);  // [64][LD]
+  bf16_t(*gs)[LD] = reinterpret_cast<bf16_t(*)[LD]>(qsm);                   // [2D][LD]
+  bf16_t(*vs)[LD] = reinterpret_cast<bf16_t(*)[LD]>(qsm + 2 * D * LD * 2);  // [128][LD]
   const int hq = blockIdx.y, l = blockIdx.z, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
   const int hk = hq / (Hq / Hkv);
@@ -144,9 +146,9 @@ __global__ void __launch_bounds__(128) quad_mma_kernel(const bf16_t* __restrict_
   cp_async_commit();
   const bf16_t* vb = v + (size_t)(l * Hkv + hk) * T * D;
   for (int tt = 0; tt < kTokTiles; ++tt) {
-    const int i0 = (blockIdx.x * kTokTiles + tt) * 64;
+    const int i0 = (blockIdx.x * kTokTiles + tt) * kQuadTok;
     if (i0 >= T) break;
-    for (int idx = tid; idx < 64 * D / 8; idx += 128) {
+    for (int idx = tid; idx < kQuadTok * D / 8; idx += 128) {
       const int r = idx / (D / 8), c = (idx % (D / 8)) * 8;
       const bool ok = i0 + r < T;
       cp_async16(smem_u32(&vs[r][c]), ok ? vb + (size_t)(i0 + r) * D + c : vb, ok ? 16 : 0);
@@ -154,15 +156,17 @@ __global__ void __launch_bounds__(128) quad_mma_kernel(const bf16_t* __restrict_
     cp_async_commit();
     cp_async_wait<0>();
     __syncthreads();
-    uint32_t af[D / 16][4];
+    uint32_t af[2][D / 16][4];
 #pragma unroll
-    for (int kc = 0; kc < D / 16; ++kc)
-      ldmatrix_x4(smem_u32(&vs[warp * 16 + (lane & 15)][kc * 16 + (lane >> 4) * 8]), af[kc][0],
-                  af[kc][1], af[kc][2], af[kc][3]);
-    float p0 = 0.f, p1 = 0.f;
-#pragma unroll 2
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int kc = 0; kc < D / 16; ++kc)
+        ldmatrix_x4(smem_u32(&vs[warp * 32 + mt * 16 + (lane & 15)][kc * 16 + (lane >> 4) * 8]),
+                    af[mt][kc][0], af[mt][kc][1], af[mt][kc][2], af[mt][kc][3]);
+    float p[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll 1
     for (int nt = 0; nt < D / 8; ++nt) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
 #pragma unroll
@@ -170,26 +174,32 @@ __global__ void __launch_bounds__(128) quad_mma_kernel(const bf16_t* __restrict_
           uint32_t b0, b1, b2, b3;
           ldmatrix_x4(smem_u32(&gs[half * D + nt * 8 + (lane & 7)][k2 * 32 + (lane >> 3) * 8]), b0,
                       b1, b2, b3);
-          mma_bf16_16816(acc, af[2 * k2], b0, b1);
-          mma_bf16_16816(acc, af[2 * k2 + 1], b2, b3);
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            mma_bf16_16816(acc[mt], af[mt][2 * k2], b0, b1);
+            mma_bf16_16816(acc[mt], af[mt][2 * k2 + 1], b2, b3);
+          }
         }
       }
       const int col = nt * 8 + 2 * t4;
-      const uint32_t va = *reinterpret_cast<const uint32_t*>(&vs[warp * 16 + g][col]);
-      const uint32_t vc = *reinterpret_cast<const uint32_t*>(&vs[warp * 16 + g + 8][col]);
-      p0 = fmaf(acc[0], bf16_lo(va), fmaf(acc[1], bf16_hi(va), p0));
-      p1 = fmaf(acc[2], bf16_lo(vc), fmaf(acc[3], bf16_hi(vc), p1));
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const uint32_t va = *reinterpret_cast<const uint32_t*>(&vs[warp * 32 + mt * 16 + g][col]);
+        const uint32_t vc = *reinterpret_cast<const uint32_t*>(&vs[warp * 32 + mt * 16 + g + 8][col]);
+        p[mt][0] = fmaf(acc[mt][0], bf16_lo(va), fmaf(acc[mt][1], bf16_hi(va), p[mt][0]));
+        p[mt][1] = fmaf(acc[mt][2], bf16_lo(vc), fmaf(acc[mt][3], bf16_hi(vc), p[mt][1]));
+      }
     }
-    p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
-    p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
-    p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
-    p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
-    if (t4 == 0) {
-      float* out = vn + ((size_t)l * Hq + hq) * T;
-      const int ia = i0 + warp * 16 + g, ib = ia + 8;
-      if (ia < T) out[ia] = sqrtf(fmaxf(p0, 0.f));
-      if (ib < T) out[ib] = sqrtf(fmaxf(p1, 0.f));
-    }
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float x = p[mt][hh];
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        const int i = i0 + warp * 32 + mt * 16 + g + hh * 8;
+        if (t4 == 0 && i < T) vn[((size_t)l * Hq + hq) * T + i] = sqrtf(fmaxf(x, 0.f));
+      }
     __syncthreads();
   }
 }
@@ -205,16 +215,17 @@ cudaError_t launch_vnorm(const bf16_t* v, int L, int Hq, int Hkv, int d, int T, 
   if (T == 0) return cudaSuccess;
   bf16_t* G = static_cast<bf16_t*>(ws);
   dim3 gg(Hq, L);
-  dim3 gq((T + 64 * kTokTiles - 1) / (64 * kTokTiles), Hq, L);
+  dim3 gq((T + kQuadTok * kTokTiles - 1) / (kQuadTok * kTokTiles), Hq, L);
   count_launches(2);
   if (d == 128) {
-    constexpr size_t smem = (2 * 128 + 64) * (128 + 8) * 2;
+    constexpr size_t smem = (2 * 128 + kQuadTok) * (128 + 8) * 2;
     gram_mma_kernel<128><<<gg, 256, 0, s>>>(w_o, Dh, Hq, G);
     cudaFuncSetAttribute(quad_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     quad_mma_kernel<128><<<gq, 128, smem, s>>>(v, G, T, Hq, Hkv, vn);
   } else {
-    constexpr size_t smem = (2 * 64 + 64) * (64 + 8) * 2;
+    constexpr size_t smem = (2 * 64 + kQuadTok) * (64 + 8) * 2;
     gram_mma_kernel<64><<<gg, 256, 0, s>>>(w_o, Dh, Hq, G);
+    cudaFuncSetAttribute(quad_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     quad_mma_kernel<64><<<gq, 128, smem, s>>>(v, G, T, Hq, Hkv, vn);
   }
   return cudaGetLastError();
