@@ -1,17 +1,18 @@
 // Attention-scoring passes on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
 // Pass 1 (LSE) and pass 2 (transposed scoring) share one warp-specialised CTA that owns
-// M = 256 rows of operand A as two 128-row sub-tiles, so every streamed B tile feeds
-// two MMAs (half the B traffic per flop of an M = 128 CTA):
-//   warp 0      TMA producer: loads both A sub-tiles once, then streams 128-row B tiles
-//               through a STAGES-deep ring of 128-byte-swizzled smem buffers
-//   warp 1      allocates all 512 TMEM columns and issues tcgen05.mma (M=128, N=128,
-//               K=16, bf16 x bf16 -> fp32): per B tile one MMA chain per sub-tile into
-//               that sub-tile's current accumulator (two accumulators per sub-tile)
-//   warps 2-9   epilogue, two groups of four warps (one group per sub-tile, two warps
-//               per SM sub-partition): one thread per accumulator row (TMEM lane) reads
-//               the 128 columns with tcgen05.ld and reduces them in registers while
-//               the MMA fills the other accumulator
+// 128 rows of operand A and streams 256-row tiles of operand B; each B tile is one chain
+// of 128 x 256 x 16 MMAs (the wide N keeps the tensor core's shared-memory operand
+// traffic at 96 bytes per clock):
+//   warp 0      TMA producer: loads the A tile once, then streams B tiles through a
+//               STAGES-deep ring of 128-byte-swizzled smem buffers
+//   warp 1      allocates all 512 TMEM columns (two 256-column accumulators) and issues
+//               tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32) into one of them
+//   warps 2-9   epilogue, two groups of four warps, one per 128-column half of the
+//               accumulator (two warps per SM sub-partition): one thread per row and
+//               half reads its columns with tcgen05.ld (the second 64 in flight while
+//               the first 64 reduce) while the MMA fills the other accumulator; the two
+//               halves of each row are merged through shared memory at the end
 // Modes (x = q.k / sqrt(d), never written to memory):
 //   kLse     A = 256 queries,  B = key tiles (context, then tail): online max and
 //            sum of 2^(x log2 e) per query -> ln sum exp(x)
@@ -34,31 +35,39 @@ __device__ int g_attn_error = 0;
 
 namespace {
 
-constexpr int BM = 128;     // rows per A sub-tile = TMEM lanes
-constexpr int MSUB = 2;     // A sub-tiles per CTA
-constexpr int BN = 128;     // rows per B tile = accumulator columns
+constexpr int BM = 128;     // rows of operand A per CTA = TMEM lanes
+constexpr int BN = 256;     // rows per B tile = accumulator columns (N of each MMA)
+constexpr int HALF = 128;   // accumulator columns per epilogue group
+constexpr int kGroups = 2;  // epilogue groups: column halves of the accumulator
 constexpr int kGroupThreads = 128;
-constexpr int kThreads = 64 + MSUB * kGroupThreads;
-constexpr uint32_t kBoxBytes = 128 * 128;  // 128 rows x 64 bf16 (one 128-byte swizzle span)
-constexpr uint32_t kTmemCols = MSUB * 2 * BN;
-constexpr int kErrWaitTimeout = 1;  // a bounded mbarrier wait ran out
+constexpr int kEpiThreads = kGroups * kGroupThreads;
+constexpr int kThreads = 64 + kEpiThreads;
+constexpr uint32_t kBoxBytesA = 128 * 128;  // 128 rows x 64 bf16 (one 128-byte swizzle span)
+constexpr uint32_t kBoxBytesB = 256 * 128;  // 256 rows x 64 bf16
+constexpr uint32_t kTmemCols = 2 * BN;       // two accumulators of 256 columns
+constexpr int kErrWaitTimeout = 1;   // a bounded mbarrier wait ran out
+constexpr int kErrSmemAlign = 3;     // dynamic shared memory window not 1024-byte aligned
+constexpr uint32_t kMaxSmem = 232448;  // per-block opt-in limit (227 KB)
 
 enum Mode { kLse = 0, kMax = 1, kFuture = 2 };
 
 template <int D>
 struct Cfg {
   static constexpr int KH = D / 64;
-  static constexpr int STAGES = D == 128 ? 4 : 6;
-  static constexpr uint32_t A_SUB = KH * kBoxBytes;
-  static constexpr uint32_t A_BYTES = MSUB * A_SUB;
-  static constexpr uint32_t B_BYTES = KH * kBoxBytes;
+  static constexpr int STAGES = D == 128 ? 3 : 6;
+  static constexpr uint32_t A_BYTES = KH * kBoxBytesA;
+  static constexpr uint32_t B_BYTES = KH * kBoxBytesB;
   static constexpr uint32_t OFF_B = A_BYTES;
-  static constexpr uint32_t OFF_C = OFF_B + STAGES * B_BYTES;  // [MSUB][2][BN] floats
-  static constexpr uint32_t OFF_BAR = OFF_C + MSUB * 2 * BN * 4;
-  static constexpr uint32_t NBAR = 1 + 2 * STAGES + 4 * MSUB;
+  // per-column constants [groups][2][HALF] floats; after its last tile group 1's part is
+  // reused to hand its per-row results ([BM][2] floats) to group 0
+  static constexpr uint32_t OFF_C = OFF_B + STAGES * B_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_C + kGroups * 2 * HALF * 4;
+  static constexpr uint32_t NBAR = 1 + 2 * STAGES + 4;  // a, full[S], empty[S], tfull[2], tempty[2]
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
+  static constexpr uint32_t USED = OFF_MISC + 16;
+  static constexpr uint32_t SMEM = (USED + 1024 <= kMaxSmem) ? USED + 1024 : kMaxSmem;
   static constexpr uint32_t IDESC = tc::idesc_bf16(BM, BN);
+  static_assert(USED <= kMaxSmem, "shared-memory plan exceeds the per-block limit");
 };
 
 __device__ __forceinline__ void fail(volatile uint32_t* abort_flag, int code) {
@@ -76,6 +85,87 @@ __device__ __forceinline__ float2 f2(uint32_t a, uint32_t b) {
   return make_float2(__uint_as_float(a), __uint_as_float(b));
 }
 
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// LSE reduction of 64 columns: running max m (log2 units) and sum s.
+__device__ __forceinline__ void lse_cols(const uint32_t* v, float sc2, float& m, float& ssum) {
+  float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
+#pragma unroll
+  for (int c = 0; c < 64; c += 8) {
+    mx0 = max3(mx0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+    mx1 = max3(mx1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+    mx2 = max3(mx2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+    mx3 = max3(mx3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
+  }
+  const float mn = fmaxf(m, max3(mx0, mx1, fmaxf(mx2, mx3)) * sc2);
+  ssum *= fast_exp2(m - mn);
+  m = mn;
+  const float2 k2 = make_float2(sc2, sc2), nm = make_float2(-m, -m);
+  float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+#pragma unroll
+  for (int c = 0; c < 64; c += 8) {
+    const float2 y0 = __ffma2_rn(f2(v[c], v[c + 1]), k2, nm);
+    const float2 y1 = __ffma2_rn(f2(v[c + 2], v[c + 3]), k2, nm);
+    const float2 y2 = __ffma2_rn(f2(v[c + 4], v[c + 5]), k2, nm);
+    const float2 y3 = __ffma2_rn(f2(v[c + 6], v[c + 7]), k2, nm);
+    a0 = __fadd2_rn(a0, make_float2(fast_exp2(y0.x), fast_exp2(y0.y)));
+    a1 = __fadd2_rn(a1, make_float2(fast_exp2(y1.x), fast_exp2(y1.y)));
+    a2 = __fadd2_rn(a2, make_float2(fast_exp2(y2.x), fast_exp2(y2.y)));
+    a3 = __fadd2_rn(a3, make_float2(fast_exp2(y3.x), fast_exp2(y3.y)));
+  }
+  a0 = __fadd2_rn(__fadd2_rn(a0, a1), __fadd2_rn(a2, a3));
+  ssum += a0.x + a0.y;
+}
+
+// KVzip max of 64 columns: max_c (x_c * scale + c_c).
+__device__ __forceinline__ float max_cols(const uint32_t* v, const float* cc, float scale,
+                                          float r) {
+  const float4* c4 = reinterpret_cast<const float4*>(cc);
+  const float2 sv = make_float2(scale, scale);
+  float r0 = r, r1 = -CUDART_INF_F, r2 = -CUDART_INF_F, r3 = -CUDART_INF_F;
+#pragma unroll
+  for (int q = 0; q < 16; q += 2) {
+    const float4 ca = c4[q], cb = c4[q + 1];
+    const float2 y0 = __ffma2_rn(f2(v[4 * q], v[4 * q + 1]), sv, make_float2(ca.x, ca.y));
+    const float2 y1 = __ffma2_rn(f2(v[4 * q + 2], v[4 * q + 3]), sv, make_float2(ca.z, ca.w));
+    const float2 y2 = __ffma2_rn(f2(v[4 * q + 4], v[4 * q + 5]), sv, make_float2(cb.x, cb.y));
+    const float2 y3 = __ffma2_rn(f2(v[4 * q + 6], v[4 * q + 7]), sv, make_float2(cb.z, cb.w));
+    r0 = max3(r0, y0.x, y0.y);
+    r1 = max3(r1, y1.x, y1.y);
+    r2 = max3(r2, y2.x, y2.y);
+    r3 = max3(r3, y3.x, y3.y);
+  }
+  return fmaxf(max3(r0, r1, r2), r3);
+}
+
+// Future mass of 64 columns: sum_c 2^(x_c * sc2 + c_c), columns c < jlim zeroed.
+__device__ __forceinline__ float future_cols(const uint32_t* v, const float* cc, float sc2,
+                                             bool band, int jlim) {
+  const float4* c4 = reinterpret_cast<const float4*>(cc);
+  const float2 k2 = make_float2(sc2, sc2);
+  float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const float4 c = c4[q];
+    const float2 y0 = __ffma2_rn(f2(v[4 * q], v[4 * q + 1]), k2, make_float2(c.x, c.y));
+    const float2 y1 = __ffma2_rn(f2(v[4 * q + 2], v[4 * q + 3]), k2, make_float2(c.z, c.w));
+    float e0 = fast_exp2(y0.x), e1 = fast_exp2(y0.y);
+    float e2 = fast_exp2(y1.x), e3 = fast_exp2(y1.y);
+    if (band) {
+      if (4 * q < jlim) e0 = 0.f;
+      if (4 * q + 1 < jlim) e1 = 0.f;
+      if (4 * q + 2 < jlim) e2 = 0.f;
+      if (4 * q + 3 < jlim) e3 = 0.f;
+    }
+    a0 = __fadd2_rn(a0, make_float2(e0, e1));
+    a1 = __fadd2_rn(a1, make_float2(e2, e3));
+  }
+  a0 = __fadd2_rn(a0, a1);
+  return a0.x + a0.y;
+}
+
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -85,15 +175,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  if (pad + C::USED > C::SMEM) {  // uniform; never overflow the allocation
+    if (threadIdx.x == 0) atomicCAS(&g_attn_error, 0, kErrSmemAlign);
+    return;
+  }
   uint8_t* smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
   const uint32_t sA = sb, sB = sb + C::OFF_B;
   float* cbuf_all = reinterpret_cast<float*>(smem + C::OFF_C);
+  float* xchg = cbuf_all + 2 * HALF;  // group 1's constants, free once it is done
+  static_assert(2 * HALF >= 2 * BM, "row exchange must fit in one group's constants");
   const uint32_t bar_a = sb + C::OFF_BAR;
   auto bar_full = [&](int s) { return bar_a + 8u * (1 + s); };
   auto bar_empty = [&](int s) { return bar_a + 8u * (1 + S + s); };
-  auto bar_tfull = [&](int u, int x) { return bar_a + 8u * (1 + 2 * S + 2 * u + x); };
-  auto bar_tempty = [&](int u, int x) { return bar_a + 8u * (1 + 2 * S + 2 * MSUB + 2 * u + x); };
+  auto bar_tfull = [&](int x) { return bar_a + 8u * (1 + 2 * S + x); };
+  auto bar_tempty = [&](int x) { return bar_a + 8u * (3 + 2 * S + x); };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
 
@@ -104,16 +200,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int off = n_k - a.n_q;
   const float scale = rsqrtf((float)D);
   const float sc2 = scale * kLog2e;
-  const int row0 = blockIdx.x * (BM * MSUB);
+  const int row0 = blockIdx.x * BM;
   const int hq_a = (MODE == kLse) ? (int)blockIdx.y : 0;
   const int hk = (MODE == kLse) ? hq_a / G : (int)blockIdx.y;
-  const int a_rows = (MODE == kLse) ? a.n_q : a.T;
-  const int nsub = min(MSUB, (a_rows - row0 + BM - 1) / BM);  // sub-tiles with a valid row
 
   // ---------------------------------------------------------------- tile space of B
   int ntiles, n_ctx = 0, per_head = 1, qt_begin = 0;
   if (MODE == kLse) {
-    const int j_last = min(row0 + BM * MSUB, a.n_q) - 1;
+    const int j_last = min(row0 + BM, a.n_q) - 1;
     const int kv_end = off + j_last + 1;  // keys [0, kv_end) are visible to some query
     n_ctx = (min(a.T, kv_end) + BN - 1) / BN;
     const int tail_need = min(a.n_tail, max(0, kv_end - a.T));
@@ -131,11 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(bar_full(s), 1);
       tc::mbar_init(bar_empty(s), 1);
     }
-    for (int u = 0; u < MSUB; ++u)
-      for (int x = 0; x < 2; ++x) {
-        tc::mbar_init(bar_tfull(u, x), 1);
-        tc::mbar_init(bar_tempty(u, x), kGroupThreads);
-      }
+    for (int x = 0; x < 2; ++x) {
+      tc::mbar_init(bar_tfull(x), 1);
+      tc::mbar_init(bar_tempty(x), kEpiThreads);
+    }
     misc[1] = 0u;
     tc::fence_mbar_init();
   }
@@ -158,11 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int a_head = (MODE == kLse) ? l * a.Hq + hq_a : l * a.Hkv + hk;
       tc::mbar_expect_tx(bar_a, C::A_BYTES);
 #pragma unroll
-      for (int u = 0; u < MSUB; ++u)
-#pragma unroll
-        for (int kh = 0; kh < C::KH; ++kh)
-          tc::tma_load_3d(sA + u * C::A_SUB + kh * kBoxBytes, &tm_a, bar_a, kh * 64,
-                          row0 + u * BM, a_head);
+      for (int kh = 0; kh < C::KH; ++kh)
+        tc::tma_load_3d(sA + kh * kBoxBytesA, &tm_a, bar_a, kh * 64, row0, a_head);
       int it = 0;
       bool ok = true;
       for (; it < ntiles; ++it) {
@@ -191,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_expect_tx(bar_full(s), C::B_BYTES);
 #pragma unroll
         for (int kh = 0; kh < C::KH; ++kh)
-          tc::tma_load_3d(sB + s * C::B_BYTES + kh * kBoxBytes, map, bar_full(s), kh * 64, row,
+          tc::tma_load_3d(sB + s * C::B_BYTES + kh * kBoxBytesB, map, bar_full(s), kh * 64, row,
                           head);
       }
       if (!ok) {
@@ -207,33 +297,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = tc::mbar_wait(bar_a, 0);
       int it = 0;
       if (ok) {
-        for (; it < ntiles && ok; ++it) {
+        for (; it < ntiles; ++it) {
           const int s = it % S;
           const uint32_t ph = (uint32_t)(it / S) & 1u;
-          const int buf = it & 1;
-          const uint32_t bph = (uint32_t)(it >> 1) & 1u;
-          if (!tc::mbar_wait(bar_full(s), ph) || *abort_flag) {
+          const int acc = it & 1;
+          const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+          if (!tc::mbar_wait(bar_tempty(acc), aph ^ 1u) || !tc::mbar_wait(bar_full(s), ph) ||
+              *abort_flag) {
             ok = false;
             break;
           }
+          tc::fence_after_sync();
+          const uint32_t d_t = tmem + (uint32_t)(acc * BN);
           const uint32_t b_s = sB + s * C::B_BYTES;
-          for (int u = 0; u < nsub; ++u) {
-            if (!tc::mbar_wait(bar_tempty(u, buf), bph ^ 1u)) {
-              ok = false;
-              break;
-            }
-            tc::fence_after_sync();
-            const uint32_t d_t = tmem + (uint32_t)((2 * u + buf) * BN);
-            const uint32_t a_u = sA + u * C::A_SUB;
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-              const uint32_t o = (uint32_t)(k >> 2) * kBoxBytes + (uint32_t)(k & 3) * 32u;
-              tc::mma_bf16(d_t, tc::sdesc_sw128(a_u + o), tc::sdesc_sw128(b_s + o), C::IDESC,
-                           k > 0 ? 1u : 0u);
-            }
-            tc::commit(bar_tfull(u, buf));
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t kh = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3) * 32u;
+            tc::mma_bf16(d_t, tc::sdesc_sw128(sA + kh * kBoxBytesA + kk),
+                         tc::sdesc_sw128(b_s + kh * kBoxBytesB + kk), C::IDESC, k > 0 ? 1u : 0u);
           }
           tc::commit(bar_empty(s));
+          tc::commit(bar_tfull(acc));
         }
       }
       if (!ok) fail(abort_flag, kErrWaitTimeout);
@@ -242,164 +326,135 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ============================================================ epilogue
-    const int u = (warp - 2) >> 2;          // sub-tile of this group
-    const int eq = warp & 3;                // TMEM lane quarter this warp may access
-    const int row = eq * 32 + lane;         // accumulator row
+    const int h = (warp - 2) >> 2;               // column half of the accumulator
+    const int eq = warp & 3;                     // TMEM lane quarter this warp may access
+    const int row = eq * 32 + lane;              // accumulator row
     const int e = ((warp - 2) & 3) * 32 + lane;  // index within the group (0..127)
-    const int rbase = row0 + u * BM;        // first A row of the sub-tile
-    const int ra = rbase + row;             // this thread's query (kLse) or key
-    const uint32_t t_lane = tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(2 * u * BN);
-    float* cbuf = cbuf_all + u * 2 * BN;
-    const int bar_id = 1 + u;
+    const int ra = row0 + row;                   // this thread's query (kLse) or key
+    const uint32_t t_lane = tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(h * HALF);
+    float* cbuf = cbuf_all + h * 2 * HALF;
+    const int bar_id = 1 + h;
 
-    if (u < nsub) {
-      auto col_const = [&](int it) -> float {
-        const int hq = hk * G + it / per_head;
-        const int j = (qt_begin + it % per_head) * BN + e;
-        if (j >= a.n_q) return -CUDART_INF_F;
-        const float lj = a.lse[(size_t)(l * a.Hq + hq) * a.n_q + j];
-        if (MODE == kMax) return -(lj + (a.hlog ? a.hlog[(size_t)l * a.n_q + j] : 0.f));
-        return -lj * kLog2e;
-      };
-      auto ln_vn = [&](int it) -> float {  // ln ||W_O v|| of this key for the head of tile it
-        if (!a.vnorm || ra >= a.T) return 0.f;
-        return logf(a.vnorm[(size_t)(l * a.Hq + hk * G + it / per_head) * a.T + ra]);
-      };
+    auto col_const = [&](int it) -> float {
+      const int hq = hk * G + it / per_head;
+      const int j = (qt_begin + it % per_head) * BN + h * HALF + e;
+      if (j >= a.n_q) return -CUDART_INF_F;
+      const float lj = a.lse[(size_t)(l * a.Hq + hq) * a.n_q + j];
+      if (MODE == kMax) return -(lj + (a.hlog ? a.hlog[(size_t)l * a.n_q + j] : 0.f));
+      return -lj * kLog2e;
+    };
+    auto ln_vn = [&](int it) -> float {  // ln ||W_O v|| of this key for the head of tile it
+      if (!a.vnorm || ra >= a.T) return 0.f;
+      return logf(a.vnorm[(size_t)(l * a.Hq + hk * G + it / per_head) * a.T + ra]);
+    };
 
-      float m = -1e30f, ssum = 0.f;                  // kLse
-      float r = -CUDART_INF_F, tot = -CUDART_INF_F;  // kMax
-      float lv = 0.f;                                // kMax: ln vnorm of the current head
-      float f = 0.f;                                 // kFuture
-      float cn1 = 0.f, cn2 = 0.f;
-      if (MODE != kLse && ntiles > 0) {
-        cbuf[e] = col_const(0);
-        if (ntiles > 1) cn1 = col_const(1);
-        if (ntiles > 2) cn2 = col_const(2);
+    float m = -1e30f, ssum = 0.f;                  // kLse
+    float r = -CUDART_INF_F, tot = -CUDART_INF_F;  // kMax
+    float lv = 0.f;                                // kMax: ln vnorm of the current head
+    float f = 0.f;                                 // kFuture
+    float cn1 = 0.f, cn2 = 0.f;
+    if (MODE != kLse && ntiles > 0) {
+      cbuf[e] = col_const(0);
+      if (ntiles > 1) cn1 = col_const(1);
+      if (ntiles > 2) cn2 = col_const(2);
+    }
+    if (MODE == kMax && ntiles > 0) lv = ln_vn(0);
+
+    bool failed = false;
+    for (int it = 0; it < ntiles; ++it) {
+      const int acc = it & 1;
+      const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+      const bool ok = tc::mbar_wait(bar_tfull(acc), aph) && !*abort_flag;
+      if (tc::bar_or(bar_id, kGroupThreads, !ok)) {
+        failed = true;
+        break;
       }
-      if (MODE == kMax && ntiles > 0) lv = ln_vn(0);
+      tc::fence_after_sync();
+      const uint32_t ta = t_lane + (uint32_t)(acc * BN);
+      uint32_t v[HALF];
+      tc::tmem_ld32(ta, v);
+      tc::tmem_ld32(ta + 32, v + 32);
+      tc::tmem_ld_wait();
+      tc::tmem_ld32(ta + 64, v + 64);  // in flight while the first 64 columns reduce
+      tc::tmem_ld32(ta + 96, v + 96);
+      if (MODE != kLse) {
+        // the other buffer's readers finished tile it-1 before the barrier above
+        if (it + 1 < ntiles) cbuf[((it + 1) & 1) * HALF + e] = cn1;
+        cn1 = cn2;
+        if (it + 3 < ntiles) cn2 = col_const(it + 3);
+      }
+      const float* cc = cbuf + (it & 1) * HALF;
 
-      bool failed = false;
-      for (int it = 0; it < ntiles; ++it) {
-        const int buf = it & 1;
-        const uint32_t bph = (uint32_t)(it >> 1) & 1u;
-        const bool ok = tc::mbar_wait(bar_tfull(u, buf), bph) && !*abort_flag;
-        if (tc::bar_or(bar_id, kGroupThreads, !ok)) {
-          failed = true;
-          break;
-        }
-        tc::fence_after_sync();
-        uint32_t v[BN];
+      // masks (LSE) / bands (future) per column c of this half: key or query index
+      if (MODE == kLse) {
+        const bool ctx = it < n_ctx;
+        const int kb = (ctx ? it * BN : a.T + (it - n_ctx) * BN) + h * HALF;
+        const int lim = ctx ? a.T : n_k;
+        const bool need_mask = (kb + HALF > lim) || (kb + HALF - 1 > off + row0);
+        if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c)
-          tc::tmem_ld32(t_lane + (uint32_t)(buf * BN + c * 32), v + c * 32);
+          for (int c = 0; c < 64; ++c)
+            if (kb + c >= lim || kb + c > off + ra) v[c] = __float_as_uint(-CUDART_INF_F);
+        }
+        lse_cols(v, sc2, m, ssum);
         tc::tmem_ld_wait();
         tc::fence_before_sync();
-        tc::mbar_arrive(bar_tempty(u, buf));
-        if (MODE != kLse) {
-          // the other buffer's readers finished tile it-1 before the barrier above
-          if (it + 1 < ntiles) cbuf[((it + 1) & 1) * BN + e] = cn1;
-          cn1 = cn2;
-          if (it + 3 < ntiles) cn2 = col_const(it + 3);
+        tc::mbar_arrive(bar_tempty(acc));
+        if (need_mask) {
+#pragma unroll
+          for (int c = 64; c < HALF; ++c)
+            if (kb + c >= lim || kb + c > off + ra) v[c] = __float_as_uint(-CUDART_INF_F);
         }
-
-        if (MODE == kLse) {
-          const bool ctx = it < n_ctx;
-          const int kb = ctx ? it * BN : a.T + (it - n_ctx) * BN;
-          const int lim = ctx ? a.T : n_k;
-          if ((kb + BN > lim) || (kb + BN - 1 > off + rbase)) {
-#pragma unroll
-            for (int c = 0; c < BN; ++c) {
-              const int i = kb + c;
-              if (i >= lim || i > off + ra) v[c] = __float_as_uint(-CUDART_INF_F);
-            }
-          }
-          float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
-#pragma unroll
-          for (int c = 0; c < BN; c += 8) {
-            mx0 = max3(mx0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
-            mx1 = max3(mx1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
-            mx2 = max3(mx2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
-            mx3 = max3(mx3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
-          }
-          const float mn = fmaxf(m, max3(mx0, mx1, fmaxf(mx2, mx3)) * sc2);
-          ssum *= fast_exp2(m - mn);
-          m = mn;
-          const float2 k2 = make_float2(sc2, sc2), nm = make_float2(-m, -m);
-          float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
-#pragma unroll
-          for (int c = 0; c < BN; c += 8) {
-            const float2 y0 = __ffma2_rn(f2(v[c], v[c + 1]), k2, nm);
-            const float2 y1 = __ffma2_rn(f2(v[c + 2], v[c + 3]), k2, nm);
-            const float2 y2 = __ffma2_rn(f2(v[c + 4], v[c + 5]), k2, nm);
-            const float2 y3 = __ffma2_rn(f2(v[c + 6], v[c + 7]), k2, nm);
-            a0 = __fadd2_rn(a0, make_float2(fast_exp2(y0.x), fast_exp2(y0.y)));
-            a1 = __fadd2_rn(a1, make_float2(fast_exp2(y1.x), fast_exp2(y1.y)));
-            a2 = __fadd2_rn(a2, make_float2(fast_exp2(y2.x), fast_exp2(y2.y)));
-            a3 = __fadd2_rn(a3, make_float2(fast_exp2(y3.x), fast_exp2(y3.y)));
-          }
-          a0 = __fadd2_rn(__fadd2_rn(a0, a1), __fadd2_rn(a2, a3));
-          ssum += a0.x + a0.y;
-        } else if (MODE == kMax) {
-          const float4* c4 = reinterpret_cast<const float4*>(cbuf + (it & 1) * BN);
-          const float2 sv = make_float2(scale, scale);
-          float r0 = r, r1 = -CUDART_INF_F, r2 = -CUDART_INF_F, r3 = -CUDART_INF_F;
-#pragma unroll
-          for (int q = 0; q < BN / 4; q += 2) {
-            const float4 ca = c4[q], cb = c4[q + 1];
-            const float2 y0 = __ffma2_rn(f2(v[4 * q], v[4 * q + 1]), sv, make_float2(ca.x, ca.y));
-            const float2 y1 = __ffma2_rn(f2(v[4 * q + 2], v[4 * q + 3]), sv, make_float2(ca.z, ca.w));
-            const float2 y2 = __ffma2_rn(f2(v[4 * q + 4], v[4 * q + 5]), sv, make_float2(cb.x, cb.y));
-            const float2 y3 = __ffma2_rn(f2(v[4 * q + 6], v[4 * q + 7]), sv, make_float2(cb.z, cb.w));
-            r0 = max3(r0, y0.x, y0.y);
-            r1 = max3(r1, y1.x, y1.y);
-            r2 = max3(r2, y2.x, y2.y);
-            r3 = max3(r3, y3.x, y3.y);
-          }
-          r = fmaxf(max3(r0, r1, r2), r3);
-          if ((it + 1) % per_head == 0) {  // last query tile of this head
-            tot = fmaxf(tot, r + lv);
-            r = -CUDART_INF_F;
-            if (it + 1 < ntiles) lv = ln_vn(it + 1);
-          }
-        } else {
-          const float4* c4 = reinterpret_cast<const float4*>(cbuf + (it & 1) * BN);
-          const int j0 = (qt_begin + it % per_head) * BN;
-          const bool need_band = j0 < rbase + BM - 1 + a.w;
-          const int jlim = ra + a.w - j0;  // columns c < jlim are inside the window
-          const float2 k2 = make_float2(sc2, sc2);
-          float2 a0 = make_float2(0.f, 0.f), a1 = a0;
-#pragma unroll
-          for (int q = 0; q < BN / 4; ++q) {
-            const float4 cc = c4[q];
-            const float2 y0 = __ffma2_rn(f2(v[4 * q], v[4 * q + 1]), k2, make_float2(cc.x, cc.y));
-            const float2 y1 = __ffma2_rn(f2(v[4 * q + 2], v[4 * q + 3]), k2, make_float2(cc.z, cc.w));
-            float e0 = fast_exp2(y0.x), e1 = fast_exp2(y0.y);
-            float e2 = fast_exp2(y1.x), e3 = fast_exp2(y1.y);
-            if (need_band) {
-              if (4 * q < jlim) e0 = 0.f;
-              if (4 * q + 1 < jlim) e1 = 0.f;
-              if (4 * q + 2 < jlim) e2 = 0.f;
-              if (4 * q + 3 < jlim) e3 = 0.f;
-            }
-            a0 = __fadd2_rn(a0, make_float2(e0, e1));
-            a1 = __fadd2_rn(a1, make_float2(e2, e3));
-          }
-          a0 = __fadd2_rn(a0, a1);
-          f += a0.x + a0.y;
-        }
-      }
-
-      if (failed) {
-        atomicCAS(&g_attn_error, 0, (int)kErrWaitTimeout);
-      } else if (MODE == kLse) {
-        if (ra < a.n_q) a.out[(size_t)(l * a.Hq + hq_a) * a.n_q + ra] = (m + fast_log2(ssum)) * kLn2;
+        lse_cols(v + 64, sc2, m, ssum);
       } else if (MODE == kMax) {
-        if (ra < a.T) {
-          float* o = a.out + (size_t)(l * a.Hkv + hk) * a.T + ra;
-          *o = a.accumulate ? fmaxf(*o, tot) : tot;
+        r = max_cols(v, cc, scale, r);
+        tc::tmem_ld_wait();
+        tc::fence_before_sync();
+        tc::mbar_arrive(bar_tempty(acc));
+        r = max_cols(v + 64, cc + 64, scale, r);
+        if ((it + 1) % per_head == 0) {  // last query tile of this head
+          tot = fmaxf(tot, r + lv);
+          r = -CUDART_INF_F;
+          if (it + 1 < ntiles) lv = ln_vn(it + 1);
         }
       } else {
-        if (ra < a.T) a.out[(size_t)(l * a.Hkv + hk) * a.T + ra] = f;
+        const int j0 = (qt_begin + it % per_head) * BN + h * HALF;
+        const bool band = j0 < row0 + BM - 1 + a.w;
+        const int jlim = ra + a.w - j0;  // columns c < jlim are inside the window
+        f += future_cols(v, cc, sc2, band, jlim);
+        tc::tmem_ld_wait();
+        tc::fence_before_sync();
+        tc::mbar_arrive(bar_tempty(acc));
+        f += future_cols(v + 64, cc + 64, sc2, band, jlim - 64);
+      }
+    }
+
+    // combine the two column halves of each row
+    if (failed) atomicCAS(&g_attn_error, 0, (int)kErrWaitTimeout);
+    if (h == 1) {
+      named_sync(bar_id, kGroupThreads);  // every group-1 reader of its constants is done
+      if (MODE == kLse) {
+        xchg[row * 2] = m;
+        xchg[row * 2 + 1] = ssum;
+      } else {
+        xchg[row * 2] = (MODE == kMax) ? tot : f;
+      }
+    }
+    named_sync(3, kEpiThreads);
+    if (h == 0 && !failed) {
+      if (MODE == kLse) {
+        const float m1 = xchg[row * 2], s1 = xchg[row * 2 + 1];
+        const float mn = fmaxf(m, m1);
+        const float st = ssum * fast_exp2(m - mn) + s1 * fast_exp2(m1 - mn);
+        if (ra < a.n_q) a.out[(size_t)(l * a.Hq + hq_a) * a.n_q + ra] = (mn + fast_log2(st)) * kLn2;
+      } else if (MODE == kMax) {
+        const float t2 = fmaxf(tot, xchg[row * 2]);
+        if (ra < a.T) {
+          float* o = a.out + (size_t)(l * a.Hkv + hk) * a.T + ra;
+          *o = a.accumulate ? fmaxf(*o, t2) : t2;
+        }
+      } else {
+        if (ra < a.T) a.out[(size_t)(l * a.Hkv + hk) * a.T + ra] = f + xchg[row * 2];
       }
     }
   }
@@ -428,12 +483,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 3-D map over [heads][rows][d] bf16 with 128-row x 64-element boxes, 128-byte swizzle;
 // rows past the end read as zeros.
-cudaError_t make_map(CUtensorMap* m, const void* base, int d, int rows, int heads) {
+cudaError_t make_map(CUtensorMap* m, const void* base, int d, int rows, int heads, int box_rows) {
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -447,22 +502,24 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
   CUtensorMap ta, tb, tb2;
   cudaError_t e;
   if (MODE == kLse) {
-    e = make_map(&ta, a.q, D, a.n_q, a.L * a.Hq);
+    e = make_map(&ta, a.q, D, a.n_q, a.L * a.Hq, BM);
     if (e == cudaSuccess)
-      e = a.T > 0 ? make_map(&tb, a.k_ctx, D, a.T, a.L * a.Hkv) : make_map(&tb, a.q, D, 1, 1);
+      e = a.T > 0 ? make_map(&tb, a.k_ctx, D, a.T, a.L * a.Hkv, BN)
+                  : make_map(&tb, a.q, D, 1, 1, BN);
     if (e == cudaSuccess)
-      e = a.n_tail > 0 ? make_map(&tb2, a.k_tail, D, a.n_tail, a.L * a.Hkv)
-                       : make_map(&tb2, a.q, D, 1, 1);
+      e = a.n_tail > 0 ? make_map(&tb2, a.k_tail, D, a.n_tail, a.L * a.Hkv, BN)
+                       : make_map(&tb2, a.q, D, 1, 1, BN);
   } else {
-    e = make_map(&ta, a.k_ctx, D, a.T, a.L * a.Hkv);
+    e = make_map(&ta, a.k_ctx, D, a.T, a.L * a.Hkv, BM);
     // with no scoring queries no B tile is loaded (every key gets the empty reduction)
     if (e == cudaSuccess)
-      e = a.n_q > 0 ? make_map(&tb, a.q, D, a.n_q, a.L * a.Hq) : make_map(&tb, a.k_ctx, D, 1, 1);
+      e = a.n_q > 0 ? make_map(&tb, a.q, D, a.n_q, a.L * a.Hq, BN)
+                    : make_map(&tb, a.k_ctx, D, 1, 1, BN);
     tb2 = tb;
   }
   if (e != cudaSuccess) return e;
   const int rows = (MODE == kLse) ? a.n_q : a.T;
-  dim3 grid((rows + BM * MSUB - 1) / (BM * MSUB), MODE == kLse ? a.Hq : a.Hkv, a.L);
+  dim3 grid((rows + BM - 1) / BM, MODE == kLse ? a.Hq : a.Hkv, a.L);
   auto kern = attn_tc_kernel<D, MODE>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
