@@ -159,6 +159,7 @@ kvs_status kvs_score_future_sum(const kvs_dims* dims, const kvs_bf16* q, const k
  *   w_o   [L][D_h][H_q*d]   bf16
  *   vnorm [L][H_q][T]       fp32 output
  *   ws    scratch of kvs_vnorm_workspace_size() bytes (4*L*H_q*d*d)
+ * Requires H_q / H_kv <= 16.
  * ------------------------------------------------------------------------------- */
 size_t kvs_vnorm_workspace_size(const kvs_dims* dims);
 kvs_status kvs_vnorm(const kvs_dims* dims, const kvs_bf16* v, int32_t T, const kvs_bf16* w_o,

@@ -189,6 +189,8 @@ kvs_status kvs_vnorm(const kvs_dims* dims, const kvs_bf16* v, int32_t T, const k
   kvs_status st = check_dims(dims, __func__);
   if (st) return st;
   REQUIRE(T >= 0, KVS_ERR_ARG, "kvs_vnorm: negative T");
+  REQUIRE(dims->H_q / dims->H_kv <= 16, KVS_ERR_UNSUPPORTED,
+          "kvs_vnorm: %d query heads per KV head (at most 16)", dims->H_q / dims->H_kv);
   REQUIRE(dims->D_h > 0 && dims->D_h % 8 == 0, KVS_ERR_SHAPE,
           "kvs_vnorm: D_h = %d must be a positive multiple of 8", dims->D_h);
   if (T == 0) return ok();
@@ -216,6 +218,8 @@ kvs_status kvs_vnorm_noalloc(const kvs_dims* dims, const kvs_bf16* v, int32_t T,
           "kvs_vnorm_noalloc: one layer needs %zu bytes of scratch (H_q * d * d * 4) but the "
           "built-in scratch holds %zu; use kvs_vnorm with a caller workspace",
           per_layer, kvs::vnorm_noalloc_scratch_bytes());
+  REQUIRE(dims->H_q / dims->H_kv <= 16, KVS_ERR_UNSUPPORTED,
+          "kvs_vnorm_noalloc: %d query heads per KV head (at most 16)", dims->H_q / dims->H_kv);
   if (T == 0) return ok();
   REQUIRE_PTR(v);
   REQUIRE_PTR(w_o);

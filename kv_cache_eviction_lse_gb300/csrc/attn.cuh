@@ -16,6 +16,7 @@ struct AttnArgs {
   const float* lse = nullptr;      // [L][Hq][n_q]
   const float* vnorm = nullptr;    // [L][Hq][T] or null
   const float* hlog = nullptr;     // [L][n_q] ln||h_j|| or null
+  const bf16_t* gpair = nullptr;   // [L][Hq][2d][d] Gram pairs (hi rows, lo rows); vnorm only
   float* out = nullptr;
   int L = 0, Hq = 0, Hkv = 0, d = 0, n_q = 0, T = 0, n_tail = 0;
   int w = 0, accumulate = 0;
@@ -24,6 +25,10 @@ struct AttnArgs {
 cudaError_t launch_lse(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_score_max(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_future_sum(const AttnArgs& a, cudaStream_t s);
+
+// vn[l][hq][i] = sqrt(v_i^T (G_hi + G_lo) v_i) on tcgen05: k_ctx = v [L][Hkv][T][d],
+// gpair = Gram pairs, out = vn [L][Hq][T]; needs Hq / Hkv <= 16.
+cudaError_t launch_vnorm_quad(const AttnArgs& a, cudaStream_t s);
 
 // Reads (and with `clear` resets) the device error word of the scoring kernels.
 cudaError_t attn_device_error(int* code, bool clear, cudaStream_t s);

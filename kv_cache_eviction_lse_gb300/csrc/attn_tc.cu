@@ -49,19 +49,23 @@ constexpr int kErrWaitTimeout = 1;   // a bounded mbarrier wait ran out
 constexpr int kErrSmemAlign = 3;     // dynamic shared memory window not 1024-byte aligned
 constexpr uint32_t kMaxSmem = 232448;  // per-block opt-in limit (227 KB)
 
-enum Mode { kLse = 0, kMax = 1, kFuture = 2 };
+enum Mode { kLse = 0, kMax = 1, kFuture = 2, kQuad = 3 };
+constexpr int kMaxGroup = 16;  // query heads per KV head handled by kQuad
 
-template <int D>
+template <int D, int MODE>
 struct Cfg {
   static constexpr int KH = D / 64;
-  static constexpr int STAGES = D == 128 ? 3 : 6;
+  // kQuad streams at most g B tiles per CTA: two stages suffice and leave room for the
+  // per-head partial sums
+  static constexpr int STAGES = MODE == kQuad ? 2 : (D == 128 ? 3 : 6);
   static constexpr uint32_t A_BYTES = KH * kBoxBytesA;
   static constexpr uint32_t B_BYTES = KH * kBoxBytesB;
   static constexpr uint32_t OFF_B = A_BYTES;
   // per-column constants [groups][2][HALF] floats; after its last tile group 1's part is
   // reused to hand its per-row results ([BM][2] floats) to group 0
   static constexpr uint32_t OFF_C = OFF_B + STAGES * B_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_C + kGroups * 2 * HALF * 4;
+  static constexpr uint32_t OFF_P = OFF_C + kGroups * 2 * HALF * 4;  // kQuad [2][16][BM] floats
+  static constexpr uint32_t OFF_BAR = OFF_P + (MODE == kQuad ? kGroups * kMaxGroup * BM * 4 : 0);
   static constexpr uint32_t NBAR = 1 + 2 * STAGES + 4;  // a, full[S], empty[S], tfull[2], tempty[2]
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t USED = OFF_MISC + 16;
@@ -170,7 +174,7 @@ template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __grid_constant__ CUtensorMap tm_b2, const AttnArgs a) {
-  using C = Cfg<D>;
+  using C = Cfg<D, MODE>;
   constexpr int S = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -212,6 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     n_ctx = (min(a.T, kv_end) + BN - 1) / BN;
     const int tail_need = min(a.n_tail, max(0, kv_end - a.T));
     ntiles = n_ctx + (tail_need + BN - 1) / BN;
+  } else if (MODE == kQuad) {
+    ntiles = G;  // one B tile (the head's Gram pair) per query head of the group
   } else {
     const int nqt = (a.n_q + BN - 1) / BN;
     if (MODE == kFuture) qt_begin = (row0 + a.w) / BN;
@@ -353,15 +359,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     float lv = 0.f;                                // kMax: ln vnorm of the current head
     float f = 0.f;                                 // kFuture
     float cn1 = 0.f, cn2 = 0.f;
-    if (MODE != kLse && ntiles > 0) {
+    constexpr bool kCols = (MODE == kMax || MODE == kFuture);  // per-column constants
+    if (kCols && ntiles > 0) {
       cbuf[e] = col_const(0);
       if (ntiles > 1) cn1 = col_const(1);
       if (ntiles > 2) cn2 = col_const(2);
     }
     if (MODE == kMax && ntiles > 0) lv = ln_vn(0);
 
+    // kQuad: this thread's D/2 elements of its value row, from the swizzled A tile
+    uint32_t vrow[D / 4];
+    float* part = reinterpret_cast<float*>(smem + C::OFF_P);
     bool failed = false;
-    for (int it = 0; it < ntiles; ++it) {
+    if (MODE == kQuad) {
+      failed = tc::bar_or(bar_id, kGroupThreads, !tc::mbar_wait(bar_a, 0));
+      if (!failed) {
+#pragma unroll
+        for (int jj = 0; jj < D / 16; ++jj) {  // 16-byte chunks of 8 elements
+          const int c = h * (D / 2) + 8 * jj;
+          const uint32_t addr = sA + (uint32_t)(c / 64) * kBoxBytesA + (uint32_t)row * 128u +
+                                ((uint32_t)(((c % 64) / 8) ^ (row & 7)) << 4);
+          uint4 u;
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+                       : "r"(addr));
+          vrow[4 * jj] = u.x;
+          vrow[4 * jj + 1] = u.y;
+          vrow[4 * jj + 2] = u.z;
+          vrow[4 * jj + 3] = u.w;
+        }
+      }
+    }
+    for (int it = 0; it < ntiles && !failed; ++it) {
       const int acc = it & 1;
       const uint32_t aph = (uint32_t)(it >> 1) & 1u;
       const bool ok = tc::mbar_wait(bar_tfull(acc), aph) && !*abort_flag;
@@ -370,14 +399,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc::fence_after_sync();
-      const uint32_t ta = t_lane + (uint32_t)(acc * BN);
       uint32_t v[HALF];
+      if (MODE == kQuad) {
+        // columns [h D/2, (h+1) D/2) of V G_hi and of V G_lo (which starts at column D)
+        const uint32_t tq = tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(acc * BN + h * (D / 2));
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tc::tmem_ld32(tq + 32 * c, v + 32 * c);
+          tc::tmem_ld32(tq + D + 32 * c, v + 64 + 32 * c);
+        }
+        tc::tmem_ld_wait();
+        tc::fence_before_sync();
+        tc::mbar_arrive(bar_tempty(acc));
+        float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < D / 2; c += 2) {
+          const uint32_t pr = vrow[c / 2];
+          p0 = fmaf(__uint_as_float(v[c]) + __uint_as_float(v[64 + c]), bf16_lo(pr), p0);
+          p1 = fmaf(__uint_as_float(v[c + 1]) + __uint_as_float(v[64 + c + 1]), bf16_hi(pr), p1);
+        }
+        part[(h * kMaxGroup + it) * BM + row] = p0 + p1;
+        continue;
+      }
+      const uint32_t ta = t_lane + (uint32_t)(acc * BN);
       tc::tmem_ld32(ta, v);
       tc::tmem_ld32(ta + 32, v + 32);
       tc::tmem_ld_wait();
       tc::tmem_ld32(ta + 64, v + 64);  // in flight while the first 64 columns reduce
       tc::tmem_ld32(ta + 96, v + 96);
-      if (MODE != kLse) {
+      if (kCols) {
         // the other buffer's readers finished tile it-1 before the barrier above
         if (it + 1 < ntiles) cbuf[((it + 1) & 1) * HALF + e] = cn1;
         cn1 = cn2;
@@ -431,7 +481,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // combine the two column halves of each row
     if (failed) atomicCAS(&g_attn_error, 0, (int)kErrWaitTimeout);
-    if (h == 1) {
+    if (MODE == kQuad) {
+      named_sync(3, kEpiThreads);
+      if (h == 0 && !failed && ra < a.T) {
+        for (int it = 0; it < ntiles; ++it) {
+          const float q2 = part[it * BM + row] + part[(kMaxGroup + it) * BM + row];
+          a.out[(size_t)(l * a.Hq + hk * G + it) * a.T + ra] = sqrtf(fmaxf(q2, 0.f));
+        }
+      }
+    } else if (h == 1) {
       named_sync(bar_id, kGroupThreads);  // every group-1 reader of its constants is done
       if (MODE == kLse) {
         xchg[row * 2] = m;
@@ -440,8 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         xchg[row * 2] = (MODE == kMax) ? tot : f;
       }
     }
-    named_sync(3, kEpiThreads);
-    if (h == 0 && !failed) {
+    if (MODE != kQuad) named_sync(3, kEpiThreads);
+    if (MODE != kQuad && h == 0 && !failed) {
       if (MODE == kLse) {
         const float m1 = xchg[row * 2], s1 = xchg[row * 2 + 1];
         const float mn = fmaxf(m, m1);
@@ -498,7 +556,7 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int d, int rows, int head
 
 template <int D, int MODE>
 cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
-  using C = Cfg<D>;
+  using C = Cfg<D, MODE>;
   CUtensorMap ta, tb, tb2;
   cudaError_t e;
   if (MODE == kLse) {
@@ -509,6 +567,10 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
     if (e == cudaSuccess)
       e = a.n_tail > 0 ? make_map(&tb2, a.k_tail, D, a.n_tail, a.L * a.Hkv, BN)
                        : make_map(&tb2, a.q, D, 1, 1, BN);
+  } else if (MODE == kQuad) {
+    e = make_map(&ta, a.k_ctx, D, a.T, a.L * a.Hkv, BM);
+    if (e == cudaSuccess) e = make_map(&tb, a.gpair, D, 2 * D, a.L * a.Hq, BN);
+    tb2 = tb;
   } else {
     e = make_map(&ta, a.k_ctx, D, a.T, a.L * a.Hkv, BM);
     // with no scoring queries no B tile is loaded (every key gets the empty reduction)
@@ -561,6 +623,10 @@ cudaError_t launch_lse(const AttnArgs& a, cudaStream_t s) { return launch_mode<k
 cudaError_t launch_score_max(const AttnArgs& a, cudaStream_t s) { return launch_mode<kMax>(a, s); }
 cudaError_t launch_future_sum(const AttnArgs& a, cudaStream_t s) {
   return launch_mode<kFuture>(a, s);
+}
+cudaError_t launch_vnorm_quad(const AttnArgs& a, cudaStream_t s) {
+  if (a.Hq / a.Hkv > kMaxGroup) return cudaErrorInvalidValue;
+  return launch_mode<kQuad>(a, s);
 }
 
 cudaError_t launch_hidden_log_norm(const bf16_t* h, int L, int n, int Dh, float* hlog,

@@ -5,12 +5,14 @@
 //   ||W_h v||^2 = v^T G_h v
 // which costs 2 D_h d^2 + 4 T d^2 flops per head instead of 2 T d D_h for the direct
 // product (5x fewer at D_h = 1536, T = 2048; 14x fewer at D_h = 4096, T = 32768).
-// Both contractions run on warp MMAs (bf16 in, fp32 accumulate):
-//   gram  G = W_h^T W_h, operands read transposed with ldmatrix.trans; G is stored as a
-//         bf16 pair G = G_hi + G_lo (G_lo = bf16(G - G_hi)), exact to ~2^-17 |G|
-//   quad  u = V (G_hi + G_lo) for a tile of tokens, then v_i . u_i in the epilogue
+// Both contractions run on tensor cores (bf16 in, fp32 accumulate):
+//   gram  G = W_h^T W_h on warp MMAs, operands read transposed with ldmatrix.trans; G is
+//         stored as a bf16 pair G = G_hi + G_lo (G_lo = bf16(G - G_hi)), ~2^-17 |G| exact
+//   quad  [V G_hi | V G_lo] for 128-token tiles on tcgen05 (the scoring kernel's kQuad
+//         mode: one M=128 N=256 MMA chain per query head), then v_i . u_i per token
 #include <mutex>
 
+#include "attn.cuh"
 #include "common.cuh"
 #include "vnorm.cuh"
 
@@ -120,90 +122,6 @@ __global__ void __launch_bounds__(256) gram_mma_kernel(const bf16_t* __restrict_
       }
 }
 
-// vn = sqrt(v^T (G_hi + G_lo) v) for 128-token tiles (32 per warp, two m16 tiles that
-// share every G fragment); G_hi, G_lo (bf16, symmetric, so their rows serve directly as
-// the k-contiguous B operand) stay in shared memory while the block walks kTokTiles
-// consecutive token tiles of one (layer, query head).
-constexpr int kTokTiles = 4;
-constexpr int kQuadTok = 128;
-
-template <int D>
-__global__ void __launch_bounds__(128) quad_mma_kernel(const bf16_t* __restrict__ v,
-                                                       const bf16_t* __restrict__ G, int T,
-                                                       int Hq, int Hkv, float* __restrict__ vn) {
-  constexpr int LD = D + 8;
-  extern __shared__ __align__(16) uint8_t qsm[];
-  bf16_t(*gs)[LD] = reinterpret_cast<bf16_t(*)[LD]>(qsm);                   // [2D][LD]
-  bf16_t(*vs)[LD] = reinterpret_cast<bf16_t(*)[LD]>(qsm + 2 * D * LD * 2);  // [128][LD]
-  const int hq = blockIdx.y, l = blockIdx.z, tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
-  const int hk = hq / (Hq / Hkv);
-  const bf16_t* Gh = G + ((size_t)l * Hq + hq) * 2 * D * D;
-  for (int idx = tid; idx < 2 * D * D / 8; idx += 128) {
-    const int r = idx / (D / 8), c = (idx % (D / 8)) * 8;
-    cp_async16(smem_u32(&gs[r][c]), Gh + (size_t)r * D + c, 16);
-  }
-  cp_async_commit();
-  const bf16_t* vb = v + (size_t)(l * Hkv + hk) * T * D;
-  for (int tt = 0; tt < kTokTiles; ++tt) {
-    const int i0 = (blockIdx.x * kTokTiles + tt) * kQuadTok;
-    if (i0 >= T) break;
-    for (int idx = tid; idx < kQuadTok * D / 8; idx += 128) {
-      const int r = idx / (D / 8), c = (idx % (D / 8)) * 8;
-      const bool ok = i0 + r < T;
-      cp_async16(smem_u32(&vs[r][c]), ok ? vb + (size_t)(i0 + r) * D + c : vb, ok ? 16 : 0);
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
-    uint32_t af[2][D / 16][4];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int kc = 0; kc < D / 16; ++kc)
-        ldmatrix_x4(smem_u32(&vs[warp * 32 + mt * 16 + (lane & 15)][kc * 16 + (lane >> 4) * 8]),
-                    af[mt][kc][0], af[mt][kc][1], af[mt][kc][2], af[mt][kc][3]);
-    float p[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-#pragma unroll 1
-    for (int nt = 0; nt < D / 8; ++nt) {
-      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-#pragma unroll
-        for (int k2 = 0; k2 < D / 32; ++k2) {
-          uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(smem_u32(&gs[half * D + nt * 8 + (lane & 7)][k2 * 32 + (lane >> 3) * 8]), b0,
-                      b1, b2, b3);
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            mma_bf16_16816(acc[mt], af[mt][2 * k2], b0, b1);
-            mma_bf16_16816(acc[mt], af[mt][2 * k2 + 1], b2, b3);
-          }
-        }
-      }
-      const int col = nt * 8 + 2 * t4;
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        const uint32_t va = *reinterpret_cast<const uint32_t*>(&vs[warp * 32 + mt * 16 + g][col]);
-        const uint32_t vc = *reinterpret_cast<const uint32_t*>(&vs[warp * 32 + mt * 16 + g + 8][col]);
-        p[mt][0] = fmaf(acc[mt][0], bf16_lo(va), fmaf(acc[mt][1], bf16_hi(va), p[mt][0]));
-        p[mt][1] = fmaf(acc[mt][2], bf16_lo(vc), fmaf(acc[mt][3], bf16_hi(vc), p[mt][1]));
-      }
-    }
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float x = p[mt][hh];
-        x += __shfl_xor_sync(0xffffffffu, x, 1);
-        x += __shfl_xor_sync(0xffffffffu, x, 2);
-        const int i = i0 + warp * 32 + mt * 16 + g + hh * 8;
-        if (t4 == 0 && i < T) vn[((size_t)l * Hq + hq) * T + i] = sqrtf(fmaxf(x, 0.f));
-      }
-    __syncthreads();
-  }
-}
-
 }  // namespace
 
 size_t vnorm_workspace_bytes(int L, int Hq, int d) {
@@ -215,20 +133,19 @@ cudaError_t launch_vnorm(const bf16_t* v, int L, int Hq, int Hkv, int d, int T, 
   if (T == 0) return cudaSuccess;
   bf16_t* G = static_cast<bf16_t*>(ws);
   dim3 gg(Hq, L);
-  dim3 gq((T + kQuadTok * kTokTiles - 1) / (kQuadTok * kTokTiles), Hq, L);
-  count_launches(2);
-  if (d == 128) {
-    constexpr size_t smem = (2 * 128 + kQuadTok) * (128 + 8) * 2;
+  count_launches(1);
+  if (d == 128)
     gram_mma_kernel<128><<<gg, 256, 0, s>>>(w_o, Dh, Hq, G);
-    cudaFuncSetAttribute(quad_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    quad_mma_kernel<128><<<gq, 128, smem, s>>>(v, G, T, Hq, Hkv, vn);
-  } else {
-    constexpr size_t smem = (2 * 64 + kQuadTok) * (64 + 8) * 2;
+  else
     gram_mma_kernel<64><<<gg, 256, 0, s>>>(w_o, Dh, Hq, G);
-    cudaFuncSetAttribute(quad_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    quad_mma_kernel<64><<<gq, 128, smem, s>>>(v, G, T, Hq, Hkv, vn);
-  }
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  AttnArgs a;  // quadratic form on the tensor cores (tcgen05), see attn_tc.cu
+  a.k_ctx = v;
+  a.gpair = G;
+  a.out = vn;
+  a.L = L; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.T = T;
+  return launch_vnorm_quad(a, s);
 }
 
 // ------------------------------------------------------------------ allocation-free variant
