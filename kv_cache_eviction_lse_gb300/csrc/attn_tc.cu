@@ -1,11 +1,13 @@
 // Attention-scoring passes on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
 // Pass 1 (LSE) and pass 2 (transposed scoring) share one warp-specialised CTA that owns
-// 128 rows of operand A and streams 256-row tiles of operand B; each B tile is one chain
-// of 128 x 256 x 16 MMAs (the wide N keeps the tensor core's shared-memory operand
-// traffic at 96 bytes per clock):
-//   warp 0      TMA producer: loads the A tile once, then streams B tiles through a
-//               STAGES-deep ring of 128-byte-swizzled smem buffers
+// two consecutive 128-row units of operand A and, for each, streams 256-row tiles of
+// operand B; each B tile is one chain of 128 x 256 x 16 MMAs (the wide N keeps the tensor
+// core's shared-memory operand traffic at 96 bytes per clock).  The second unit's MMAs
+// run while the epilogue drains the first, so a CTA's fill and drain are paid once for
+// two units:
+//   warp 0      TMA producer: loads both A tiles up front, then streams B tiles through
+//               a STAGES-deep ring of 128-byte-swizzled smem buffers
 //   warp 1      allocates all 512 TMEM columns (two 256-column accumulators) and issues
 //               tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32) into one of them
 //   warps 2-9   epilogue, two groups of four warps, one per 128-column half of the
@@ -14,11 +16,11 @@
 //               the first 64 reduce) while the MMA fills the other accumulator; the two
 //               halves of each row are merged through shared memory at the end
 // Modes (x = q.k / sqrt(d), never written to memory):
-//   kLse     A = 256 queries,  B = key tiles (context, then tail): online max and
+//   kLse     A = queries,  B = key tiles (context, then tail): online max and
 //            sum of 2^(x log2 e) per query -> ln sum exp(x)
-//   kMax     A = 256 context keys, B = query tiles of every head of the group: per key
+//   kMax     A = context keys, B = query tiles of every head of the group: per key
 //            max of x - lse_j - ln||h_j||, folded per head with ln ||W_O^{(h)} v_i||
-//   kFuture  A = 256 keys, B = query tiles j >= i0 + w: per key sum over the group of
+//   kFuture  A = keys, B = query tiles j >= i0 + w: per key sum over the group of
 //            2^((x - lse_j) log2 e) for j >= i + w
 // Sources: KVpop review, 1. Key Terms (LSE reuse, transposed-attention pass);
 // KVzap review, 3.1 Eq. 1 and 3.2 Eq. 3.
@@ -50,23 +52,25 @@ constexpr int kErrSmemAlign = 3;     // dynamic shared memory window not 1024-by
 constexpr uint32_t kMaxSmem = 232448;  // per-block opt-in limit (227 KB)
 
 enum Mode { kLse = 0, kMax = 1, kFuture = 2, kQuad = 3 };
+// 128-row units of operand A per CTA, each with its own A buffer (loaded up front), so the
+// second unit's MMAs start while the epilogue drains the first.  A buffers are never
+// reused within a CTA, which keeps the kQuad epilogue's reads of A free of races.
+constexpr int kUnits = 2;
 constexpr int kMaxGroup = 16;  // query heads per KV head handled by kQuad
 
 template <int D, int MODE>
 struct Cfg {
   static constexpr int KH = D / 64;
-  // kQuad streams at most g B tiles per CTA: two stages suffice and leave room for the
-  // per-head partial sums
-  static constexpr int STAGES = MODE == kQuad ? 2 : (D == 128 ? 3 : 6);
-  static constexpr uint32_t A_BYTES = KH * kBoxBytesA;
+  static constexpr int STAGES = D == 128 ? 2 : 4;
+  static constexpr uint32_t A_BYTES = KH * kBoxBytesA;  // one of kUnits A buffers
   static constexpr uint32_t B_BYTES = KH * kBoxBytesB;
-  static constexpr uint32_t OFF_B = A_BYTES;
-  // per-column constants [groups][2][HALF] floats; after its last tile group 1's part is
-  // reused to hand its per-row results ([BM][2] floats) to group 0
-  static constexpr uint32_t OFF_C = OFF_B + STAGES * B_BYTES;
-  static constexpr uint32_t OFF_P = OFF_C + kGroups * 2 * HALF * 4;  // kQuad [2][16][BM] floats
+  static constexpr uint32_t OFF_B = kUnits * A_BYTES;
+  static constexpr uint32_t OFF_C = OFF_B + STAGES * B_BYTES;        // [groups][2][HALF] floats
+  static constexpr uint32_t OFF_X = OFF_C + kGroups * 2 * HALF * 4;  // [2][BM][2] floats
+  static constexpr uint32_t OFF_P = OFF_X + 2 * BM * 2 * 4;          // kQuad [2][16][BM] floats
   static constexpr uint32_t OFF_BAR = OFF_P + (MODE == kQuad ? kGroups * kMaxGroup * BM * 4 : 0);
-  static constexpr uint32_t NBAR = 1 + 2 * STAGES + 4;  // a, full[S], empty[S], tfull[2], tempty[2]
+  // a_full[kUnits], full[S], empty[S], tfull[2], tempty[2]
+  static constexpr uint32_t NBAR = kUnits + 2 * STAGES + 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t USED = OFF_MISC + 16;
   static constexpr uint32_t SMEM = (USED + 1024 <= kMaxSmem) ? USED + 1024 : kMaxSmem;
@@ -170,6 +174,35 @@ __device__ __forceinline__ float future_cols(const uint32_t* v, const float* cc,
   return a0.x + a0.y;
 }
 
+// B-tile space of the 128-row unit starting at row0.
+struct Tiles {
+  int row0, ntiles, n_ctx, per_head, qt_begin;
+};
+
+template <int MODE>
+__device__ __forceinline__ Tiles tiles_of(const AttnArgs& a, int row0, int G, int off) {
+  Tiles t;
+  t.row0 = row0;
+  t.n_ctx = 0;
+  t.per_head = 1;
+  t.qt_begin = 0;
+  if (MODE == kLse) {
+    const int j_last = min(row0 + BM, a.n_q) - 1;
+    const int kv_end = off + j_last + 1;  // keys [0, kv_end) are visible to some query
+    t.n_ctx = (min(a.T, kv_end) + BN - 1) / BN;
+    const int tail_need = min(a.n_tail, max(0, kv_end - a.T));
+    t.ntiles = t.n_ctx + (tail_need + BN - 1) / BN;
+  } else if (MODE == kQuad) {
+    t.ntiles = G;  // one B tile (the head's Gram pair) per query head of the group
+  } else {
+    const int nqt = (a.n_q + BN - 1) / BN;
+    if (MODE == kFuture) t.qt_begin = (row0 + a.w) / BN;
+    t.per_head = max(0, nqt - t.qt_begin);
+    t.ntiles = G * t.per_head;
+  }
+  return t;
+}
+
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -187,13 +220,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sb = raw + pad;
   const uint32_t sA = sb, sB = sb + C::OFF_B;
   float* cbuf_all = reinterpret_cast<float*>(smem + C::OFF_C);
-  float* xchg = cbuf_all + 2 * HALF;  // group 1's constants, free once it is done
-  static_assert(2 * HALF >= 2 * BM, "row exchange must fit in one group's constants");
-  const uint32_t bar_a = sb + C::OFF_BAR;
-  auto bar_full = [&](int s) { return bar_a + 8u * (1 + s); };
-  auto bar_empty = [&](int s) { return bar_a + 8u * (1 + S + s); };
-  auto bar_tfull = [&](int x) { return bar_a + 8u * (1 + 2 * S + x); };
-  auto bar_tempty = [&](int x) { return bar_a + 8u * (3 + 2 * S + x); };
+  float* xchg_all = reinterpret_cast<float*>(smem + C::OFF_X);
+  float* part = reinterpret_cast<float*>(smem + C::OFF_P);
+  const uint32_t bar0 = sb + C::OFF_BAR;
+  auto bar_afull = [&](int n) { return bar0 + 8u * n; };
+  auto bar_full = [&](int s) { return bar0 + 8u * (kUnits + s); };
+  auto bar_empty = [&](int s) { return bar0 + 8u * (kUnits + S + s); };
+  auto bar_tfull = [&](int x) { return bar0 + 8u * (kUnits + 2 * S + x); };
+  auto bar_tempty = [&](int x) { return bar0 + 8u * (kUnits + 2 * S + 2 + x); };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
 
@@ -204,29 +238,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int off = n_k - a.n_q;
   const float scale = rsqrtf((float)D);
   const float sc2 = scale * kLog2e;
-  const int row0 = blockIdx.x * BM;
   const int hq_a = (MODE == kLse) ? (int)blockIdx.y : 0;
   const int hk = (MODE == kLse) ? hq_a / G : (int)blockIdx.y;
-
-  // ---------------------------------------------------------------- tile space of B
-  int ntiles, n_ctx = 0, per_head = 1, qt_begin = 0;
-  if (MODE == kLse) {
-    const int j_last = min(row0 + BM, a.n_q) - 1;
-    const int kv_end = off + j_last + 1;  // keys [0, kv_end) are visible to some query
-    n_ctx = (min(a.T, kv_end) + BN - 1) / BN;
-    const int tail_need = min(a.n_tail, max(0, kv_end - a.T));
-    ntiles = n_ctx + (tail_need + BN - 1) / BN;
-  } else if (MODE == kQuad) {
-    ntiles = G;  // one B tile (the head's Gram pair) per query head of the group
-  } else {
-    const int nqt = (a.n_q + BN - 1) / BN;
-    if (MODE == kFuture) qt_begin = (row0 + a.w) / BN;
-    per_head = max(0, nqt - qt_begin);
-    ntiles = G * per_head;
-  }
+  const int a_rows = (MODE == kLse) ? a.n_q : a.T;
+  const int rb0 = blockIdx.x * kUnits;
+  const int nunits = min(kUnits, (a_rows + BM - 1) / BM - rb0);
 
   if (threadIdx.x == 0) {
-    tc::mbar_init(bar_a, 1);
+    for (int n = 0; n < kUnits; ++n) tc::mbar_init(bar_afull(n), 1);
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(bar_full(s), 1);
       tc::mbar_init(bar_empty(s), 1);
@@ -255,59 +274,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================================================ TMA producer
     if (lane == 0) {
       const int a_head = (MODE == kLse) ? l * a.Hq + hq_a : l * a.Hkv + hk;
-      tc::mbar_expect_tx(bar_a, C::A_BYTES);
-#pragma unroll
-      for (int kh = 0; kh < C::KH; ++kh)
-        tc::tma_load_3d(sA + kh * kBoxBytesA, &tm_a, bar_a, kh * 64, row0, a_head);
-      int it = 0;
-      bool ok = true;
-      for (; it < ntiles; ++it) {
-        const int s = it % S;
-        const uint32_t ph = (uint32_t)(it / S) & 1u;
-        if (!tc::mbar_wait(bar_empty(s), ph ^ 1u) || *abort_flag) {
-          ok = false;
-          break;
-        }
-        const CUtensorMap* map;
-        int row, head;
-        if (MODE == kLse) {
-          head = l * a.Hkv + hk;
-          if (it < n_ctx) {
-            map = &tm_b;
-            row = it * BN;
-          } else {
-            map = &tm_b2;
-            row = (it - n_ctx) * BN;
-          }
-        } else {
-          map = &tm_b;
-          head = l * a.Hq + hk * G + it / per_head;
-          row = (qt_begin + it % per_head) * BN;
-        }
-        tc::mbar_expect_tx(bar_full(s), C::B_BYTES);
+      for (int n = 0; n < nunits; ++n) {  // every unit's A tile up front
+        tc::mbar_expect_tx(bar_afull(n), C::A_BYTES);
 #pragma unroll
         for (int kh = 0; kh < C::KH; ++kh)
-          tc::tma_load_3d(sB + s * C::B_BYTES + kh * kBoxBytesB, map, bar_full(s), kh * 64, row,
-                          head);
+          tc::tma_load_3d(sA + n * C::A_BYTES + kh * kBoxBytesA, &tm_a, bar_afull(n), kh * 64,
+                          (rb0 + n) * BM, a_head);
+      }
+      int gt = 0;
+      bool ok = true;
+      for (int n = 0; n < nunits && ok; ++n) {
+        const Tiles U = tiles_of<MODE>(a, (rb0 + n) * BM, G, off);
+        for (int it = 0; it < U.ntiles; ++it, ++gt) {
+          const int s = gt % S;
+          const uint32_t ph = (uint32_t)(gt / S) & 1u;
+          if (!tc::mbar_wait(bar_empty(s), ph ^ 1u) || *abort_flag) {
+            ok = false;
+            break;
+          }
+          const CUtensorMap* map;
+          int row, head;
+          if (MODE == kLse) {
+            head = l * a.Hkv + hk;
+            if (it < U.n_ctx) {
+              map = &tm_b;
+              row = it * BN;
+            } else {
+              map = &tm_b2;
+              row = (it - U.n_ctx) * BN;
+            }
+          } else {
+            map = &tm_b;
+            head = l * a.Hq + hk * G + it / U.per_head;
+            row = (U.qt_begin + it % U.per_head) * BN;
+          }
+          tc::mbar_expect_tx(bar_full(s), C::B_BYTES);
+#pragma unroll
+          for (int kh = 0; kh < C::KH; ++kh)
+            tc::tma_load_3d(sB + s * C::B_BYTES + kh * kBoxBytesB, map, bar_full(s), kh * 64, row,
+                            head);
+        }
       }
       if (!ok) {
         fail(abort_flag, kErrWaitTimeout);
         // let the copies already in flight land before the CTA exits
-        tc::mbar_wait(bar_a, 0);
-        for (int j = max(0, it - S); j < it; ++j) tc::mbar_wait(bar_full(j % S), (j / S) & 1);
+        for (int n = 0; n < nunits; ++n) tc::mbar_wait(bar_afull(n), 0);
+        for (int j = max(0, gt - S); j < gt; ++j) tc::mbar_wait(bar_full(j % S), (j / S) & 1);
       }
     }
   } else if (warp == 1) {
     // ============================================================ MMA issuer
     if (lane == 0) {
-      bool ok = tc::mbar_wait(bar_a, 0);
-      int it = 0;
-      if (ok) {
-        for (; it < ntiles; ++it) {
-          const int s = it % S;
-          const uint32_t ph = (uint32_t)(it / S) & 1u;
-          const int acc = it & 1;
-          const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+      int gt = 0;
+      bool ok = true;
+      for (int n = 0; n < nunits && ok; ++n) {
+        const Tiles U = tiles_of<MODE>(a, (rb0 + n) * BM, G, off);
+        if (!tc::mbar_wait(bar_afull(n), 0)) {
+          ok = false;
+          break;
+        }
+        const uint32_t a_n = sA + n * C::A_BYTES;
+        for (int it = 0; it < U.ntiles; ++it, ++gt) {
+          const int s = gt % S;
+          const uint32_t ph = (uint32_t)(gt / S) & 1u;
+          const int acc = gt & 1;
+          const uint32_t aph = (uint32_t)(gt >> 1) & 1u;
           if (!tc::mbar_wait(bar_tempty(acc), aph ^ 1u) || !tc::mbar_wait(bar_full(s), ph) ||
               *abort_flag) {
             ok = false;
@@ -319,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t kh = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3) * 32u;
-            tc::mma_bf16(d_t, tc::sdesc_sw128(sA + kh * kBoxBytesA + kk),
+            tc::mma_bf16(d_t, tc::sdesc_sw128(a_n + kh * kBoxBytesA + kk),
                          tc::sdesc_sw128(b_s + kh * kBoxBytesB + kk), C::IDESC, k > 0 ? 1u : 0u);
           }
           tc::commit(bar_empty(s));
@@ -327,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) fail(abort_flag, kErrWaitTimeout);
-      if (it > 0) tc::mbar_wait(bar_empty((it - 1) % S), ((it - 1) / S) & 1);
+      if (gt > 0) tc::mbar_wait(bar_empty((gt - 1) % S), ((gt - 1) / S) & 1);
     }
     __syncwarp();
   } else {
@@ -336,48 +367,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int eq = warp & 3;                     // TMEM lane quarter this warp may access
     const int row = eq * 32 + lane;              // accumulator row
     const int e = ((warp - 2) & 3) * 32 + lane;  // index within the group (0..127)
-    const int ra = row0 + row;                   // this thread's query (kLse) or key
     const uint32_t t_lane = tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(h * HALF);
     float* cbuf = cbuf_all + h * 2 * HALF;
     const int bar_id = 1 + h;
-
-    auto col_const = [&](int it) -> float {
-      const int hq = hk * G + it / per_head;
-      const int j = (qt_begin + it % per_head) * BN + h * HALF + e;
-      if (j >= a.n_q) return -CUDART_INF_F;
-      const float lj = a.lse[(size_t)(l * a.Hq + hq) * a.n_q + j];
-      if (MODE == kMax) return -(lj + (a.hlog ? a.hlog[(size_t)l * a.n_q + j] : 0.f));
-      return -lj * kLog2e;
-    };
-    auto ln_vn = [&](int it) -> float {  // ln ||W_O v|| of this key for the head of tile it
-      if (!a.vnorm || ra >= a.T) return 0.f;
-      return logf(a.vnorm[(size_t)(l * a.Hq + hk * G + it / per_head) * a.T + ra]);
-    };
-
-    float m = -1e30f, ssum = 0.f;                  // kLse
-    float r = -CUDART_INF_F, tot = -CUDART_INF_F;  // kMax
-    float lv = 0.f;                                // kMax: ln vnorm of the current head
-    float f = 0.f;                                 // kFuture
-    float cn1 = 0.f, cn2 = 0.f;
     constexpr bool kCols = (MODE == kMax || MODE == kFuture);  // per-column constants
-    if (kCols && ntiles > 0) {
-      cbuf[e] = col_const(0);
-      if (ntiles > 1) cn1 = col_const(1);
-      if (ntiles > 2) cn2 = col_const(2);
-    }
-    if (MODE == kMax && ntiles > 0) lv = ln_vn(0);
-
-    // kQuad: this thread's D/2 elements of its value row, from the swizzled A tile
-    uint32_t vrow[D / 4];
-    float* part = reinterpret_cast<float*>(smem + C::OFF_P);
+    int gt = 0;
     bool failed = false;
-    if (MODE == kQuad) {
-      failed = tc::bar_or(bar_id, kGroupThreads, !tc::mbar_wait(bar_a, 0));
-      if (!failed) {
+
+    for (int n = 0; n < nunits; ++n) {
+      const Tiles U = tiles_of<MODE>(a, (rb0 + n) * BM, G, off);
+      const int ra = U.row0 + row;  // this thread's query (kLse) or key
+
+      auto col_const = [&](int it) -> float {
+        const int hq = hk * G + it / U.per_head;
+        const int j = (U.qt_begin + it % U.per_head) * BN + h * HALF + e;
+        if (j >= a.n_q) return -CUDART_INF_F;
+        const float lj = a.lse[(size_t)(l * a.Hq + hq) * a.n_q + j];
+        if (MODE == kMax) return -(lj + (a.hlog ? a.hlog[(size_t)l * a.n_q + j] : 0.f));
+        return -lj * kLog2e;
+      };
+      auto ln_vn = [&](int it) -> float {  // ln ||W_O v|| of this key for the head of tile it
+        if (!a.vnorm || ra >= a.T) return 0.f;
+        return logf(a.vnorm[(size_t)(l * a.Hq + hk * G + it / U.per_head) * a.T + ra]);
+      };
+
+      float m = -1e30f, ssum = 0.f;                  // kLse
+      float r = -CUDART_INF_F, tot = -CUDART_INF_F;  // kMax
+      float lv = 0.f;                                // kMax: ln vnorm of the current head
+      float f = 0.f;                                 // kFuture
+      float cn1 = 0.f, cn2 = 0.f;
+      if (kCols && U.ntiles > 0) {
+        const float c0 = col_const(0);
+        if (U.ntiles > 1) cn1 = col_const(1);
+        if (U.ntiles > 2) cn2 = col_const(2);
+        cbuf[e] = c0;  // the previous unit's readers passed its end-of-unit vote
+      }
+      if (MODE == kMax && U.ntiles > 0) lv = ln_vn(0);
+
+      // kQuad: this thread's D/2 elements of its value row, from the swizzled A tile
+      uint32_t vrow[D / 4];
+      bool bad = false;  // a wait of this group ran out: skip to the end-of-unit vote
+      if (MODE == kQuad) bad = tc::bar_or(bar_id, kGroupThreads, !tc::mbar_wait(bar_afull(n), 0));
+      if (MODE == kQuad && !bad) {
+        const uint32_t a_n = sA + n * C::A_BYTES;
 #pragma unroll
         for (int jj = 0; jj < D / 16; ++jj) {  // 16-byte chunks of 8 elements
           const int c = h * (D / 2) + 8 * jj;
-          const uint32_t addr = sA + (uint32_t)(c / 64) * kBoxBytesA + (uint32_t)row * 128u +
+          const uint32_t addr = a_n + (uint32_t)(c / 64) * kBoxBytesA + (uint32_t)row * 128u +
                                 ((uint32_t)(((c % 64) / 8) ^ (row & 7)) << 4);
           uint4 u;
           asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -389,132 +425,140 @@ __global__ void __launch_bounds__(kThreads, 1)
           vrow[4 * jj + 3] = u.w;
         }
       }
-    }
-    for (int it = 0; it < ntiles && !failed; ++it) {
-      const int acc = it & 1;
-      const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-      const bool ok = tc::mbar_wait(bar_tfull(acc), aph) && !*abort_flag;
-      if (tc::bar_or(bar_id, kGroupThreads, !ok)) {
+
+      for (int it = 0; it < U.ntiles && !bad; ++it, ++gt) {
+        const int acc = gt & 1;
+        const uint32_t aph = (uint32_t)(gt >> 1) & 1u;
+        const bool ok = tc::mbar_wait(bar_tfull(acc), aph) && !*abort_flag;
+        if (tc::bar_or(bar_id, kGroupThreads, !ok)) {
+          bad = true;
+          break;
+        }
+        tc::fence_after_sync();
+        uint32_t v[HALF];
+        if (MODE == kQuad) {
+          // columns [h D/2, (h+1) D/2) of V G_hi and of V G_lo (which starts at column D)
+          const uint32_t tq =
+              tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(acc * BN + h * (D / 2));
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            tc::tmem_ld32(tq + 32 * c, v + 32 * c);
+            tc::tmem_ld32(tq + D + 32 * c, v + 64 + 32 * c);
+          }
+          tc::tmem_ld_wait();
+          tc::fence_before_sync();
+          tc::mbar_arrive(bar_tempty(acc));
+          float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+          for (int c = 0; c < D / 2; c += 2) {
+            const uint32_t pr = vrow[c / 2];
+            p0 = fmaf(__uint_as_float(v[c]) + __uint_as_float(v[64 + c]), bf16_lo(pr), p0);
+            p1 = fmaf(__uint_as_float(v[c + 1]) + __uint_as_float(v[64 + c + 1]), bf16_hi(pr), p1);
+          }
+          part[(h * kMaxGroup + it) * BM + row] = p0 + p1;
+          continue;
+        }
+        const uint32_t ta = t_lane + (uint32_t)(acc * BN);
+        tc::tmem_ld32(ta, v);
+        tc::tmem_ld32(ta + 32, v + 32);
+        tc::tmem_ld_wait();
+        tc::tmem_ld32(ta + 64, v + 64);  // in flight while the first 64 columns reduce
+        tc::tmem_ld32(ta + 96, v + 96);
+        if (kCols) {
+          // the other buffer's readers finished tile it-1 before the barrier above
+          if (it + 1 < U.ntiles) cbuf[((it + 1) & 1) * HALF + e] = cn1;
+          cn1 = cn2;
+          if (it + 3 < U.ntiles) cn2 = col_const(it + 3);
+        }
+        const float* cc = cbuf + (it & 1) * HALF;
+
+        if (MODE == kLse) {
+          const bool ctx = it < U.n_ctx;
+          const int kb = (ctx ? it * BN : a.T + (it - U.n_ctx) * BN) + h * HALF;
+          const int lim = ctx ? a.T : n_k;
+          const bool need_mask = (kb + HALF > lim) || (kb + HALF - 1 > off + U.row0);
+          if (need_mask) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (kb + c >= lim || kb + c > off + ra) v[c] = __float_as_uint(-CUDART_INF_F);
+          }
+          lse_cols(v, sc2, m, ssum);
+          tc::tmem_ld_wait();
+          tc::fence_before_sync();
+          tc::mbar_arrive(bar_tempty(acc));
+          if (need_mask) {
+#pragma unroll
+            for (int c = 64; c < HALF; ++c)
+              if (kb + c >= lim || kb + c > off + ra) v[c] = __float_as_uint(-CUDART_INF_F);
+          }
+          lse_cols(v + 64, sc2, m, ssum);
+        } else if (MODE == kMax) {
+          r = max_cols(v, cc, scale, r);
+          tc::tmem_ld_wait();
+          tc::fence_before_sync();
+          tc::mbar_arrive(bar_tempty(acc));
+          r = max_cols(v + 64, cc + 64, scale, r);
+          if ((it + 1) % U.per_head == 0) {  // last query tile of this head
+            tot = fmaxf(tot, r + lv);
+            r = -CUDART_INF_F;
+            if (it + 1 < U.ntiles) lv = ln_vn(it + 1);
+          }
+        } else {
+          const int j0 = (U.qt_begin + it % U.per_head) * BN + h * HALF;
+          const bool band = j0 < U.row0 + BM - 1 + a.w;
+          const int jlim = ra + a.w - j0;  // columns c < jlim are inside the window
+          f += future_cols(v, cc, sc2, band, jlim);
+          tc::tmem_ld_wait();
+          tc::fence_before_sync();
+          tc::mbar_arrive(bar_tempty(acc));
+          f += future_cols(v + 64, cc + 64, sc2, band, jlim - 64);
+        }
+      }
+      // results of this unit: combine the two halves of each row (kQuad: the per-head
+      // partial dot products).  Both groups vote on failure here, so they leave the unit
+      // loop together and never wait at a barrier the other has abandoned.
+      float* xchg = xchg_all + (n & 1) * BM * 2;
+      if (MODE != kQuad && h == 1 && !bad) {
+        if (MODE == kLse) {
+          xchg[row * 2] = m;
+          xchg[row * 2 + 1] = ssum;
+        } else {
+          xchg[row * 2] = (MODE == kMax) ? tot : f;
+        }
+      }
+      if (tc::bar_or(3, kEpiThreads, bad)) {
         failed = true;
         break;
       }
-      tc::fence_after_sync();
-      uint32_t v[HALF];
       if (MODE == kQuad) {
-        // columns [h D/2, (h+1) D/2) of V G_hi and of V G_lo (which starts at column D)
-        const uint32_t tq = tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(acc * BN + h * (D / 2));
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          tc::tmem_ld32(tq + 32 * c, v + 32 * c);
-          tc::tmem_ld32(tq + D + 32 * c, v + 64 + 32 * c);
+        if (h == 0 && ra < a.T) {
+          for (int it = 0; it < U.ntiles; ++it) {
+            const float q2 = part[it * BM + row] + part[(kMaxGroup + it) * BM + row];
+            a.out[(size_t)(l * a.Hq + hk * G + it) * a.T + ra] = sqrtf(fmaxf(q2, 0.f));
+          }
         }
-        tc::tmem_ld_wait();
-        tc::fence_before_sync();
-        tc::mbar_arrive(bar_tempty(acc));
-        float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-        for (int c = 0; c < D / 2; c += 2) {
-          const uint32_t pr = vrow[c / 2];
-          p0 = fmaf(__uint_as_float(v[c]) + __uint_as_float(v[64 + c]), bf16_lo(pr), p0);
-          p1 = fmaf(__uint_as_float(v[c + 1]) + __uint_as_float(v[64 + c + 1]), bf16_hi(pr), p1);
-        }
-        part[(h * kMaxGroup + it) * BM + row] = p0 + p1;
+        if (n + 1 < nunits) named_sync(3, kEpiThreads);  // part[] is rewritten by the next unit
         continue;
       }
-      const uint32_t ta = t_lane + (uint32_t)(acc * BN);
-      tc::tmem_ld32(ta, v);
-      tc::tmem_ld32(ta + 32, v + 32);
-      tc::tmem_ld_wait();
-      tc::tmem_ld32(ta + 64, v + 64);  // in flight while the first 64 columns reduce
-      tc::tmem_ld32(ta + 96, v + 96);
-      if (kCols) {
-        // the other buffer's readers finished tile it-1 before the barrier above
-        if (it + 1 < ntiles) cbuf[((it + 1) & 1) * HALF + e] = cn1;
-        cn1 = cn2;
-        if (it + 3 < ntiles) cn2 = col_const(it + 3);
-      }
-      const float* cc = cbuf + (it & 1) * HALF;
-
-      // masks (LSE) / bands (future) per column c of this half: key or query index
-      if (MODE == kLse) {
-        const bool ctx = it < n_ctx;
-        const int kb = (ctx ? it * BN : a.T + (it - n_ctx) * BN) + h * HALF;
-        const int lim = ctx ? a.T : n_k;
-        const bool need_mask = (kb + HALF > lim) || (kb + HALF - 1 > off + row0);
-        if (need_mask) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (kb + c >= lim || kb + c > off + ra) v[c] = __float_as_uint(-CUDART_INF_F);
+      if (h == 0) {
+        if (MODE == kLse) {
+          const float m1 = xchg[row * 2], s1 = xchg[row * 2 + 1];
+          const float mn = fmaxf(m, m1);
+          const float st = ssum * fast_exp2(m - mn) + s1 * fast_exp2(m1 - mn);
+          if (ra < a.n_q)
+            a.out[(size_t)(l * a.Hq + hq_a) * a.n_q + ra] = (mn + fast_log2(st)) * kLn2;
+        } else if (MODE == kMax) {
+          const float t2 = fmaxf(tot, xchg[row * 2]);
+          if (ra < a.T) {
+            float* o = a.out + (size_t)(l * a.Hkv + hk) * a.T + ra;
+            *o = a.accumulate ? fmaxf(*o, t2) : t2;
+          }
+        } else {
+          if (ra < a.T) a.out[(size_t)(l * a.Hkv + hk) * a.T + ra] = f + xchg[row * 2];
         }
-        lse_cols(v, sc2, m, ssum);
-        tc::tmem_ld_wait();
-        tc::fence_before_sync();
-        tc::mbar_arrive(bar_tempty(acc));
-        if (need_mask) {
-#pragma unroll
-          for (int c = 64; c < HALF; ++c)
-            if (kb + c >= lim || kb + c > off + ra) v[c] = __float_as_uint(-CUDART_INF_F);
-        }
-        lse_cols(v + 64, sc2, m, ssum);
-      } else if (MODE == kMax) {
-        r = max_cols(v, cc, scale, r);
-        tc::tmem_ld_wait();
-        tc::fence_before_sync();
-        tc::mbar_arrive(bar_tempty(acc));
-        r = max_cols(v + 64, cc + 64, scale, r);
-        if ((it + 1) % per_head == 0) {  // last query tile of this head
-          tot = fmaxf(tot, r + lv);
-          r = -CUDART_INF_F;
-          if (it + 1 < ntiles) lv = ln_vn(it + 1);
-        }
-      } else {
-        const int j0 = (qt_begin + it % per_head) * BN + h * HALF;
-        const bool band = j0 < row0 + BM - 1 + a.w;
-        const int jlim = ra + a.w - j0;  // columns c < jlim are inside the window
-        f += future_cols(v, cc, sc2, band, jlim);
-        tc::tmem_ld_wait();
-        tc::fence_before_sync();
-        tc::mbar_arrive(bar_tempty(acc));
-        f += future_cols(v + 64, cc + 64, sc2, band, jlim - 64);
       }
     }
-
-    // combine the two column halves of each row
     if (failed) atomicCAS(&g_attn_error, 0, (int)kErrWaitTimeout);
-    if (MODE == kQuad) {
-      named_sync(3, kEpiThreads);
-      if (h == 0 && !failed && ra < a.T) {
-        for (int it = 0; it < ntiles; ++it) {
-          const float q2 = part[it * BM + row] + part[(kMaxGroup + it) * BM + row];
-          a.out[(size_t)(l * a.Hq + hk * G + it) * a.T + ra] = sqrtf(fmaxf(q2, 0.f));
-        }
-      }
-    } else if (h == 1) {
-      named_sync(bar_id, kGroupThreads);  // every group-1 reader of its constants is done
-      if (MODE == kLse) {
-        xchg[row * 2] = m;
-        xchg[row * 2 + 1] = ssum;
-      } else {
-        xchg[row * 2] = (MODE == kMax) ? tot : f;
-      }
-    }
-    if (MODE != kQuad) named_sync(3, kEpiThreads);
-    if (MODE != kQuad && h == 0 && !failed) {
-      if (MODE == kLse) {
-        const float m1 = xchg[row * 2], s1 = xchg[row * 2 + 1];
-        const float mn = fmaxf(m, m1);
-        const float st = ssum * fast_exp2(m - mn) + s1 * fast_exp2(m1 - mn);
-        if (ra < a.n_q) a.out[(size_t)(l * a.Hq + hq_a) * a.n_q + ra] = (mn + fast_log2(st)) * kLn2;
-      } else if (MODE == kMax) {
-        const float t2 = fmaxf(tot, xchg[row * 2]);
-        if (ra < a.T) {
-          float* o = a.out + (size_t)(l * a.Hkv + hk) * a.T + ra;
-          *o = a.accumulate ? fmaxf(*o, t2) : t2;
-        }
-      } else {
-        if (ra < a.T) a.out[(size_t)(l * a.Hkv + hk) * a.T + ra] = f + xchg[row * 2];
-      }
-    }
   }
 
   __syncthreads();
@@ -581,7 +625,7 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
   }
   if (e != cudaSuccess) return e;
   const int rows = (MODE == kLse) ? a.n_q : a.T;
-  dim3 grid((rows + BM - 1) / BM, MODE == kLse ? a.Hq : a.Hkv, a.L);
+  dim3 grid(((rows + BM - 1) / BM + kUnits - 1) / kUnits, MODE == kLse ? a.Hq : a.Hkv, a.L);
   auto kern = attn_tc_kernel<D, MODE>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
