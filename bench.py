@@ -49,6 +49,19 @@ UNIT = "tokens/s/layer"
 L2_FLUSH_BYTES = 512 << 20
 
 
+def read_traffic(workload, stage):
+    """DRAM bytes per launch of `stage` on `workload` from profiles/traffic.txt (an ncu
+    capture of the same kernel), or None when no capture of the current kernel exists."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        f = line.split()
+        if len(f) >= 3 and not f[0].startswith("#") and f[0] == workload and f[1] == stage:
+            return int(f[2])
+    return None
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -330,14 +343,7 @@ def run_gpu(args, rank, world, local):
                 "peak": dk.get("peak"), "unit": dk.get("unit"), "frac": dk.get("frac"),
                 "peak_source": f"{src} (MEASURED_PEAKS.json burst)" if src == "measured" else
                 "fallback", "traffic": None}
-    traffic_file = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(traffic_file):
-        try:
-            tr = json.load(open(traffic_file)).get(f"{wl.name}:{dom}")
-            if tr:
-                roofline["traffic"] = tr
-        except Exception:
-            pass
+    roofline["traffic"] = read_traffic(wl.name, dom)
 
     # ---------------------------------------------------------------- end to end
     e2e = None
