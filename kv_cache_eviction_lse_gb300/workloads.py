@@ -11,6 +11,7 @@ Five workloads are defined, shaped like the models the pages evaluate:
   c3  Qwen3-8B-shaped chunked KVzip+ scoring (36 layers, 8 / 32 heads, T=32768)
   c4  Qwen3-4B-shaped future-attention target (36 layers, 8 / 32 heads, T=16384)
   c5  Llama-3-8B-shaped KVzap linear-surrogate pruning (32 layers, 8 KV heads, T=131072)
+  c6  Qwen3-8B-shaped KVzap MLP-surrogate pruning (36 layers, 8 KV heads, 4096 -> 512 -> 8)
 
 Every layer is drawn from its own generator seeded with
 ``20261202 + 1000 * workload_index + layer``, so any subset of layers can be
@@ -26,6 +27,10 @@ Layouts (row-major, innermost last):
   h        [L][n_q][D_h]           bf16   residual-stream input at the scoring queries
   W        [L][D_h][H_kv]          bf16   linear surrogate weight
   b        [L][H_kv]               fp32   linear surrogate bias
+  W1       [L][D_h/8][D_h]         bf16   MLP surrogate first layer (out, in)
+  b1       [L][D_h/8]              fp32
+  W2       [L][H_kv][D_h/8]        bf16   MLP surrogate second layer (out, in)
+  b2       [L][H_kv]               fp32
 """
 from __future__ import annotations
 
@@ -51,7 +56,7 @@ class Workload:
     d: int
     D_h: int
     T: int                    # context keys scored per (layer, KV head)
-    kind: str                 # kvzip | kvzip_plus | kvzip_plus_chunked | future | kvzap
+    kind: str                 # kvzip | kvzip_plus | kvzip_plus_chunked | future | kvzap | kvzap_mlp
     prefix: int = 0           # repeat-prompt tokens between context and repeated block
     n_rep: int = 0            # scoring queries per call (repeated block, or one chunk)
     n_chunks: int = 1
@@ -69,6 +74,11 @@ class Workload:
     @property
     def g(self) -> int:
         return self.H_q // self.H_kv
+
+    @property
+    def D_mid(self) -> int:
+        """Hidden width of the MLP surrogate: D_h / 8."""
+        return self.D_h // 8
 
     def seed(self, layer: int) -> int:
         return BASE_SEED + 1000 * self.index + layer
@@ -123,6 +133,12 @@ WORKLOADS = {
               "d=128, hidden 4096, T=131072, tau=-5, w=128",
         L=32, H_kv=8, H_q=32, d=128, D_h=4096, T=131072, kind="kvzap",
         w=128, tau=-5.0),
+    "c6": Workload(
+        name="c6", index=6,
+        title="Qwen3-8B-shaped KVzap MLP-surrogate pruning, 36 layers, 8 KV heads, "
+              "d=128, hidden 4096 -> 512 -> 8 (GELU), T=131072, tau=-4, w=128",
+        L=36, H_kv=8, H_q=32, d=128, D_h=4096, T=131072, kind="kvzap_mlp",
+        w=128, tau=-4.0),
 }
 
 
@@ -201,6 +217,8 @@ def generate(wl: Workload, layers=None, device="cpu") -> dict:
         return _generate_future(wl, layers, device)
     if wl.kind == "kvzap":
         return _generate_kvzap(wl, layers, device)
+    if wl.kind == "kvzap_mlp":
+        return _generate_kvzap_mlp(wl, layers, device)
     raise ValueError(wl.kind)
 
 
@@ -285,6 +303,30 @@ def _generate_kvzap(wl: Workload, layers, device):
         k[i] = _bf16(_randn(gen, (Hkv, T, d), device))
         v[i] = _bf16(_randn(gen, (Hkv, T, d), device))
     return dict(h=h, W=W, b=b, k=k, v=v)
+
+
+def _generate_kvzap_mlp(wl: Workload, layers, device):
+    """c6: hidden states, MLP surrogate weights (W1 std 1/sqrt(D_h), b1 std 1/2,
+    W2 std 1/sqrt(D_h/8), b2 ~ N(-4, 1)) and the K/V to compact."""
+    nL, d, Hkv, T, Dh, Dm = len(layers), wl.d, wl.H_kv, wl.T, wl.D_h, wl.D_mid
+    bf = torch.bfloat16
+    h = torch.empty((nL, T, Dh), dtype=bf, device=device)
+    W1 = torch.empty((nL, Dm, Dh), dtype=bf, device=device)
+    b1 = torch.empty((nL, Dm), dtype=torch.float32, device=device)
+    W2 = torch.empty((nL, Hkv, Dm), dtype=bf, device=device)
+    b2 = torch.empty((nL, Hkv), dtype=torch.float32, device=device)
+    k = torch.empty((nL, Hkv, T, d), dtype=bf, device=device)
+    v = torch.empty_like(k)
+    for i, l in enumerate(layers):
+        gen = _gen(wl, l, device)
+        W1[i] = _bf16(_randn(gen, (Dm, Dh), device, std=1.0 / math.sqrt(Dh)))
+        b1[i] = _randn(gen, (Dm,), device, std=0.5)
+        W2[i] = _bf16(_randn(gen, (Hkv, Dm), device, std=1.0 / math.sqrt(Dm)))
+        b2[i] = _randn(gen, (Hkv,), device, mean=-4.0)
+        h[i] = _bf16(_randn(gen, (T, Dh), device))
+        k[i] = _bf16(_randn(gen, (Hkv, T, d), device))
+        v[i] = _bf16(_randn(gen, (Hkv, T, d), device))
+    return dict(h=h, W1=W1, b1=b1, W2=W2, b2=b2, k=k, v=v)
 
 
 def random_kv_inputs(L, H_kv, H_q, d, T, n_tail, n_q, seed, device="cpu", scale=1.0,

@@ -10,7 +10,8 @@ Sources (page title, then section / equation):
 
   [KVzap]  "KVzap: Fast, Adaptive, and Faithful KV Cache Pruning" (Jump2Paper review):
            background (KV cache shape), 3.1 KVzip (Eq. 1), 3.2 KVzip+ (Eq. 2, Eq. 3),
-           3.3 KVzap (surrogate h_t -> R^H), thresholding with a sliding window,
+           3.3 KVzap (surrogate h_t -> R^H), training setup table (MLP width D_h/8),
+           thresholding with a sliding window,
            Algorithm 1 (compress), Appendix B (compute overhead), Table 2.
   [KVpop]  "[Paper review] KVpop -- Key-Value Cache Compression with Predictive Online
            Pruning": 1. Key Terms (future-attention target, transposed-attention pass,
@@ -218,6 +219,37 @@ def linear_surrogate(h, W, b):
     W [L][D_h][H_kv], b [L][H_kv] -> z [L][H_kv][T] (head-major)."""
     L = h.shape[0]
     return np.stack([(h[l] @ W[l] + b[l][None, :]).T for l in range(L)], 0)
+
+
+def _erf(x):
+    try:
+        from scipy.special import erf
+        return erf(x)
+    except ImportError:  # plain per-element fallback
+        return np.vectorize(math.erf, otypes=[np.float64])(x)
+
+
+def gelu(x):
+    """GELU(x) = x Phi(x) = x (1 + erf(x / sqrt 2)) / 2, Phi the standard normal CDF.
+    Reading: the pages do not name the MLP surrogate's activation; the exact (erf)
+    form of GELU is taken."""
+    x = np.asarray(x, dtype=np.float64)
+    return 0.5 * x * (1.0 + _erf(x / math.sqrt(2.0)))
+
+
+def mlp_surrogate(h, W1, b1, W2, b2):
+    """KVzap-MLP [KVzap 3.3; training setup table]: per layer a two-layer MLP
+    D_h -> D_h/8 -> H_kv applied independently at every position,
+    z_t = W2 GELU(W1 h_t + b1) + b2 (a predicted ln s+ per KV head).
+    Weights in the (out, in) layout of a linear layer: W1 [L][D_mid][D_h],
+    b1 [L][D_mid], W2 [L][H_kv][D_mid], b2 [L][H_kv].  h [L][T][D_h] ->
+    z [L][H_kv][T] (head-major, like the linear surrogate)."""
+    L = h.shape[0]
+    out = []
+    for l in range(L):
+        u = h[l] @ W1[l].T + b1[l][None, :]
+        out.append((gelu(u) @ W2[l].T + b2[l][None, :]).T)
+    return np.stack(out, 0)
 
 
 # ----------------------------------------------------------------------------- pruning

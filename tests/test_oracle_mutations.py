@@ -53,6 +53,13 @@ MUTATIONS = [
      "return L * T * H_kv * d * bytes_per_elem"),
     ("mlp cost over 8", "return D_h / 4 * (D_h + H_kv)", "return D_h / 8 * (D_h + H_kv)"),
     ("bf16 shift 15", "<< np.uint32(16)", "<< np.uint32(15)"),
+    ("gelu without 1/sqrt2", "_erf(x / math.sqrt(2.0))", "_erf(x)"),
+    ("gelu tanh form", "return 0.5 * x * (1.0 + _erf(x / math.sqrt(2.0)))",
+     "return 0.5 * x * (1.0 + np.tanh(math.sqrt(2 / math.pi) * (x + 0.044715 * x ** 3)))"),
+    ("mlp relu", "out.append((gelu(u) @ W2[l].T", "out.append((np.maximum(u, 0) @ W2[l].T"),
+    ("mlp drops hidden bias", "u = h[l] @ W1[l].T + b1[l][None, :]", "u = h[l] @ W1[l].T"),
+    ("mlp drops output bias", "@ W2[l].T + b2[l][None, :]).T)", "@ W2[l].T).T)"),
+    ("mlp token-major", "@ W2[l].T + b2[l][None, :]).T)", "@ W2[l].T + b2[l][None, :]))"),
 ]
 
 

@@ -312,6 +312,73 @@ def test_surrogate_small_integers_exact():
             assert z[0, hh, t] == want
 
 
+# ------------------------------------------------------------------ MLP surrogate (GELU)
+
+# standard normal CDF at 1, -1, 2 (normal-table values)
+PHI_1 = 0.8413447460685429
+PHI_M1 = 0.15865525393145707
+PHI_2 = 0.9772498680518208
+
+
+def test_gelu_normal_table_values():
+    g = O.gelu(np.array([0.0, 1.0, -1.0, 2.0, 40.0, -40.0]))
+    assert g[0] == 0.0
+    assert abs(g[1] - PHI_1) < 1e-15 and abs(g[2] + PHI_M1) < 1e-15
+    assert abs(g[3] - 2 * PHI_2) < 1e-15
+    assert g[4] == 40.0 and abs(g[5]) < 1e-300
+
+
+def test_gelu_odd_part_is_identity():
+    # Phi(x) + Phi(-x) = 1  =>  GELU(x) - GELU(-x) = x
+    x = rng.normal(size=50) * 3
+    assert np.allclose(O.gelu(x) - O.gelu(-x), x, rtol=0, atol=1e-14)
+
+
+def _mlp_weights(L, Dh, Dm, H, b1_shift=0.0):
+    W1 = rng.normal(size=(L, Dm, Dh)) / math.sqrt(Dh)
+    b1 = rng.normal(size=(L, Dm)) * 0.5 + b1_shift
+    W2 = rng.normal(size=(L, H, Dm)) / math.sqrt(Dm)
+    b2 = rng.normal(size=(L, H)) - 4.0
+    return W1, b1, W2, b2
+
+
+def test_mlp_in_linear_regime_equals_composed_linear_surrogate():
+    # all pre-activations >> 0: GELU is the identity, so the MLP is the linear
+    # surrogate with W = W1^T W2^T and b = W2 b1 + b2
+    L, T, Dh, Dm, H = 2, 7, 16, 4, 3
+    h = rng.normal(size=(L, T, Dh))
+    W1, b1, W2, b2 = _mlp_weights(L, Dh, Dm, H, b1_shift=60.0)
+    z = O.mlp_surrogate(h, W1, b1, W2, b2)
+    W = np.stack([W1[l].T @ W2[l].T for l in range(L)])
+    b = np.stack([W2[l] @ b1[l] + b2[l] for l in range(L)])
+    assert z.shape == (L, H, T)
+    assert np.allclose(z, O.linear_surrogate(h, W, b), rtol=1e-12, atol=1e-10)
+
+
+def test_mlp_with_dead_hidden_units_gives_output_bias():
+    L, T, Dh, Dm, H = 2, 5, 8, 4, 3
+    h = rng.normal(size=(L, T, Dh))
+    W1, b1, W2, b2 = _mlp_weights(L, Dh, Dm, H, b1_shift=-60.0)
+    z = O.mlp_surrogate(h, W1, b1, W2, b2)
+    assert np.allclose(z, np.broadcast_to(b2[:, :, None], (L, H, T)), rtol=0, atol=1e-12)
+
+
+def test_mlp_brute_force_loops():
+    L, T, Dh, Dm, H = 2, 3, 5, 4, 2
+    h = rng.normal(size=(L, T, Dh))
+    W1, b1, W2, b2 = _mlp_weights(L, Dh, Dm, H)
+    z = O.mlp_surrogate(h, W1, b1, W2, b2)
+    for l in range(L):
+        for t in range(T):
+            hidden = []
+            for m in range(Dm):
+                u = b1[l, m] + sum(W1[l, m, c] * h[l, t, c] for c in range(Dh))
+                hidden.append(u * 0.5 * math.erfc(-u / math.sqrt(2.0)))
+            for hh in range(H):
+                want = b2[l, hh] + sum(W2[l, hh, m] * hidden[m] for m in range(Dm))
+                assert abs(z[l, hh, t] - want) < 1e-12
+
+
 # ----------------------------------------------------------------------------- pruning
 
 def test_threshold_hand_example():

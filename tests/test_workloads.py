@@ -58,3 +58,18 @@ def test_kvzap_keep_fraction_statistics():
             p = 0.5 * math.erfc(-((b[l, hh] + 5.0) / sig) / math.sqrt(2))
             tol = 5 * math.sqrt(max(p * (1 - p), 1e-4) / 4096) + 1e-3
             assert abs(keep[l, hh] / 4096 - p) < tol
+
+
+def test_kvzap_mlp_shapes_and_recipe():
+    wl = W.WORKLOADS["c6"].scaled(L=2, T=256, D_h=512)
+    x = W.generate(wl)
+    assert wl.D_mid == 64
+    assert x["h"].shape == (2, 256, 512) and x["W1"].shape == (2, 64, 512)
+    assert x["b1"].shape == (2, 64) and x["W2"].shape == (2, 8, 64) and x["b2"].shape == (2, 8)
+    assert x["W1"].dtype == torch.bfloat16 and x["b1"].dtype == torch.float32
+    w1 = x["W1"].double()
+    assert abs(w1.std().item() * math.sqrt(512) - 1.0) < 0.05
+    assert abs(x["b2"].mean().item() + 4.0) < 1.5
+    sub = W.generate(wl, layers=[1])
+    for k in x:
+        assert torch.equal(x[k][1:2], sub[k]), k
