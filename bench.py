@@ -11,6 +11,7 @@ One step = one pass of the whole path over one batch of synthetic input (all lay
       once before timing) with w=128 -> compaction
   c4: lse (causal) -> future mass (w=128) -> top-k 25% / 12.5% + window -> compaction
   c5: surrogate (+ fused threshold tau=-5, w=128) -> compaction
+  c6: MLP surrogate 4096 -> 512 -> 8 (+ threshold tau=-4, w=128) -> compaction
 Metric: context KV tokens scored+pruned per second per layer (all heads) = T * L / step time.
 
 Timing: inputs resident in HBM; W warm-up steps; K timed steps, each bracketed by CUDA
@@ -67,7 +68,7 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="c2", choices=["c1", "c2", "c3", "c4", "c5"])
+    ap.add_argument("--workload", default="c2", choices=["c1", "c2", "c3", "c4", "c5", "c6"])
     ap.add_argument("--impl", default="kvs", choices=["kvs", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -79,7 +80,7 @@ def parse_args():
     return ap.parse_args()
 
 
-DEFAULT_STEPS = {"c1": 200, "c2": 200, "c3": 5, "c4": 10, "c5": 20}
+DEFAULT_STEPS = {"c1": 200, "c2": 200, "c3": 5, "c4": 10, "c5": 20, "c6": 10}
 
 
 def dist_env():
@@ -118,6 +119,10 @@ def algorithmic_work(wl, p):
         rows = L * wl.H_kv
         out["kvs_surrogate"] = ("hbm", L * wl.T * wl.D_h * 2 + L * wl.D_h * wl.H_kv * 2
                                 + rows * wl.T * (4 + 1), "byte")
+    if wl.kind == "kvzap_mlp":
+        # two linear layers per token: 2 D_h D_mid + 2 D_mid H = (D_h / 4)(D_h + H)
+        out["kvs_surrogate_mlp"] = ("tensor", L * wl.T * (2 * wl.D_h * wl.D_mid
+                                                          + 2 * wl.D_mid * wl.H_kv), "flop")
     return out
 
 
@@ -448,7 +453,7 @@ def oracle_sample(wl, x, frac=1.0):
     the group's score row.  The query-proportional parts are scaled by n_q / n_sub (and
     the chunks), and everything by the number of groups.  future: the first frac*T tokens
     of group 0 (cost ~ n^2, scaled by (T/n)^2 and the groups).  kvzap: the first frac*T
-    tokens of layer 0 (all heads), scaled by T/n.
+    tokens of layer 0 (all heads), scaled by T/n; kvzap_mlp likewise.
     Returns (seconds per layer, tokens per layer, description)."""
     import numpy as np
     import torch
@@ -519,6 +524,16 @@ def oracle_sample(wl, x, frac=1.0):
         dt = (tick() - t0) * (wl.T / n)
         return dt, wl.T, (f"layer 0, first {n} of {wl.T} tokens (all heads): surrogate, threshold, "
                           f"compaction; scaled x(T/{n})")
+    if wl.kind == "kvzap_mlp":
+        n = max(1024, min(wl.T, int(round(frac * wl.T))))
+        t0 = tick()
+        z = O.mlp_surrogate(f64(x["h"][:, :n]), f64(x["W1"]), x["b1"].double().numpy(),
+                            f64(x["W2"]), x["b2"].double().numpy())
+        m, _ = O.prune_threshold(z, wl.tau, wl.w)
+        O.compact_paged(i16(x["k"][:, :, :n]), i16(x["v"][:, :, :n]), m, wl.page_size)
+        dt = (tick() - t0) * (wl.T / n)
+        return dt, wl.T, (f"layer 0, first {n} of {wl.T} tokens (all heads): MLP surrogate, "
+                          f"threshold, compaction; scaled x(T/{n})")
     raise ValueError(wl.kind)
 
 
@@ -534,7 +549,7 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-CPU_BASELINE_FRAC = {"c1": 1.0, "c2": 1.0, "c3": 1 / 8, "c4": 1 / 4, "c5": 1 / 8}
+CPU_BASELINE_FRAC = {"c1": 1.0, "c2": 1.0, "c3": 1 / 8, "c4": 1 / 4, "c5": 1 / 8, "c6": 1 / 16}
 
 
 def run_cpu_baseline(wl):

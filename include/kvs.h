@@ -61,7 +61,7 @@ typedef struct kvs_dims {
   int32_t H_q;  /* query heads, multiple of H_kv */
   int32_t H_kv; /* key/value heads, >= 1 */
   int32_t d;    /* head dimension: 64 or 128 */
-  int32_t D_h;  /* hidden size (kvs_vnorm, kvs_score_max with h, kvs_surrogate); else ignored */
+  int32_t D_h;  /* hidden size (kvs_vnorm, kvs_score_max with h, kvs_surrogate*); else ignored */
 } kvs_dims;
 
 enum { KVS_THRESHOLD = 0, KVS_TOPK = 1 };
@@ -203,6 +203,34 @@ kvs_status kvs_vnorm_noalloc(const kvs_dims* dims, const kvs_bf16* v, int32_t T,
 kvs_status kvs_surrogate(const kvs_dims* dims, const kvs_bf16* h, int32_t T,
                          const kvs_bf16* W, const float* b, float* score,
                          float tau, int32_t w, uint8_t* mask, int32_t* keep, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * kvs_surrogate_mlp -- KVzap-MLP score [KVzap 3.3; training setup table: a two-layer
+ * MLP per layer, D_h -> D_mid = D_h/8 -> H_kv; Appendix B: cost (D_h/4)(D_h + H)]:
+ *
+ *   u[c]             = sum_k h[l][t][k] * W1[l][c][k] + b1[l][c]        (c < D_mid)
+ *   score[l][hk][t]  = sum_c GELU(u[c]) * W2[l][hk][c] + b2[l][hk]
+ *
+ * GELU(x) = x * Phi(x) (exact, erf form): the pages do not name the activation.
+ * The first layer runs on the tensor cores (bf16 x bf16 -> fp32); GELU and the second
+ * layer are fp32.  score is zeroed and accumulated in place (fp32 atomic adds of the
+ * partial sums of D_mid split into parts of at most 256 columns, each a multiple of
+ * 32).  With at most two parts (D_mid <= 256, or D_mid <= 512 with D_mid / 2 a
+ * multiple of 32, as at D_h = 4096) the result is deterministic.  Optionally fused
+ * with the threshold rule exactly as kvs_surrogate (mask != NULL).
+ *
+ *   h     [L][T][D_h]       bf16
+ *   W1    [L][D_mid][D_h]   bf16 (out, in: a linear layer's weight),  b1 [L][D_mid] fp32
+ *   W2    [L][H_kv][D_mid]  bf16 (out, in),                           b2 [L][H_kv]  fp32
+ *   score [L][H_kv][T]      fp32 output
+ *   mask  [L][H_kv][T]      uint8 output or NULL;  keep [L][H_kv] int32 (required with mask)
+ * Requires D_h a positive multiple of 64, D_mid a positive multiple of 32, and
+ * H_kv in {1, 2, 4, 8, 16}.
+ * ------------------------------------------------------------------------------- */
+kvs_status kvs_surrogate_mlp(const kvs_dims* dims, const kvs_bf16* h, int32_t T, int32_t D_mid,
+                             const kvs_bf16* W1, const float* b1, const kvs_bf16* W2,
+                             const float* b2, float* score, float tau, int32_t w,
+                             uint8_t* mask, int32_t* keep, void* stream);
 
 /* ---------------------------------------------------------------------------------
  * kvs_prune_mask -- keep mask per (layer, KV head) row of T scores.

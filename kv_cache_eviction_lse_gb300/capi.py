@@ -67,6 +67,7 @@ _SIGS = {
     "kvs_vnorm": ([_D, _P, _I, _P, _P, _P, _S, _P], ctypes.c_int),
     "kvs_vnorm_noalloc": ([_D, _P, _I, _P, _P, _P], ctypes.c_int),
     "kvs_surrogate": ([_D, _P, _I, _P, _P, _P, _F, _I, _P, _P, _P], ctypes.c_int),
+    "kvs_surrogate_mlp": ([_D, _P, _I, _I, _P, _P, _P, _P, _P, _F, _I, _P, _P, _P], ctypes.c_int),
     "kvs_prune_mask": ([_D, _P, _I, _I, _F, _I, _I, _P, _P, _P], ctypes.c_int),
     "kvs_compact_workspace_size": ([_D, _I], _S),
     "kvs_compact_paged": ([_D, _P, _P, _I, _P, _I, _P, _P, _I, _P, _I, _P, _P, _P, _S, _P],
@@ -166,6 +167,13 @@ def kvs_vnorm_noalloc(dm, v, T, w_o, vnorm, stream=None):
 def kvs_surrogate(dm, h, T, W, b, score, tau=0.0, w=0, mask=None, keep=None, stream=None):
     _check(_lib.kvs_surrogate(_d(dm), _ptr(h), T, _ptr(W), _ptr(b), _ptr(score), float(tau), w,
                               _ptr(mask), _ptr(keep), _stream(stream)))
+
+
+def kvs_surrogate_mlp(dm, h, T, D_mid, W1, b1, W2, b2, score, tau=0.0, w=0, mask=None, keep=None,
+                      stream=None):
+    _check(_lib.kvs_surrogate_mlp(_d(dm), _ptr(h), T, D_mid, _ptr(W1), _ptr(b1), _ptr(W2),
+                                  _ptr(b2), _ptr(score), float(tau), w, _ptr(mask), _ptr(keep),
+                                  _stream(stream)))
 
 
 def kvs_prune_mask(dm, score, T, mode, tau, k, w, mask, keep, stream=None):

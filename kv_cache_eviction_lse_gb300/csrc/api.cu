@@ -9,6 +9,7 @@
 #include "../../include/kvs.h"
 #include "attn.cuh"
 #include "compact.cuh"
+#include "mlp.cuh"
 #include "prune.cuh"
 #include "surrogate.cuh"
 #include "vnorm.cuh"
@@ -91,10 +92,11 @@ uint64_t kvs_launch_count(void) { return kvs::g_launches.load(std::memory_order_
 
 kvs_status kvs_device_error(int32_t* code_out, int32_t clear, void* stream) {
   REQUIRE(code_out, KVS_ERR_ARG, "kvs_device_error: code_out is NULL");
-  int code = 0;
+  int code = 0, code_mlp = 0;
   cudaError_t e = kvs::attn_device_error(&code, clear != 0, as_stream(stream));
+  if (e == cudaSuccess) e = kvs::mlp_device_error(&code_mlp, clear != 0, as_stream(stream));
   if (e != cudaSuccess) return cuda_status(e, "kvs_device_error");
-  *code_out = code;
+  *code_out = code ? code : code_mlp;
   return ok();
 }
 
@@ -253,6 +255,51 @@ kvs_status kvs_surrogate(const kvs_dims* dims, const kvs_bf16* h, int32_t T, con
   return cuda_status(kvs::launch_surrogate(h, dims->L, T, dims->D_h, dims->H_kv, W, b, score, tau,
                                            w, mask, keep, as_stream(stream)),
                      "kvs_surrogate");
+}
+
+kvs_status kvs_surrogate_mlp(const kvs_dims* dims, const kvs_bf16* h, int32_t T, int32_t D_mid,
+                             const kvs_bf16* W1, const float* b1, const kvs_bf16* W2,
+                             const float* b2, float* score, float tau, int32_t w, uint8_t* mask,
+                             int32_t* keep, void* stream) {
+  kvs_status st = check_dims(dims, __func__, false);
+  if (st) return st;
+  REQUIRE(T >= 0 && w >= 0, KVS_ERR_ARG, "kvs_surrogate_mlp: negative T or w");
+  const int H = dims->H_kv;
+  REQUIRE(H == 1 || H == 2 || H == 4 || H == 8 || H == 16, KVS_ERR_UNSUPPORTED,
+          "kvs_surrogate_mlp: H_kv = %d (supported: 1, 2, 4, 8, 16)", H);
+  REQUIRE(dims->D_h > 0 && dims->D_h % 64 == 0, KVS_ERR_UNSUPPORTED,
+          "kvs_surrogate_mlp: D_h = %d must be a positive multiple of 64", dims->D_h);
+  REQUIRE(kvs::mlp_parts(D_mid) > 0, KVS_ERR_UNSUPPORTED,
+          "kvs_surrogate_mlp: D_mid = %d must be a positive multiple of 32", D_mid);
+  REQUIRE((int64_t)dims->L * H * T <= ((int64_t)1 << 40) && (int64_t)dims->L * T < INT32_MAX,
+          KVS_ERR_UNSUPPORTED, "kvs_surrogate_mlp: L * T too large");
+  if (T == 0) return ok();
+  REQUIRE_PTR(h);
+  REQUIRE_PTR(W1);
+  REQUIRE_PTR(b1);
+  REQUIRE_PTR(W2);
+  REQUIRE_PTR(b2);
+  REQUIRE_PTR(score);
+  if (mask) {
+    REQUIRE_PTR(keep);
+  }
+  kvs::MlpArgs a;
+  a.h = h;
+  a.W1 = W1;
+  a.b1 = b1;
+  a.W2 = W2;
+  a.b2 = b2;
+  a.z = score;
+  a.L = dims->L;
+  a.T = T;
+  a.Dh = dims->D_h;
+  a.Dm = D_mid;
+  a.H = H;
+  cudaError_t e = kvs::launch_mlp_surrogate(a, as_stream(stream));
+  if (e == cudaSuccess && mask)
+    e = kvs::launch_prune(score, dims->L * H, T, KVS_THRESHOLD, tau, 0, w, mask, keep,
+                          as_stream(stream));
+  return cuda_status(e, "kvs_surrogate_mlp");
 }
 
 kvs_status kvs_prune_mask(const kvs_dims* dims, const float* score, int32_t T, int32_t mode,

@@ -663,6 +663,11 @@ __global__ void hidden_log_norm_kernel(const bf16_t* __restrict__ h, int rows, i
 
 }  // namespace
 
+cudaError_t tma_map_bf16_3d(CUtensorMap* m, const void* base, int inner, int rows, int outer,
+                            int box_rows) {
+  return make_map(m, base, inner, rows, outer, box_rows);
+}
+
 cudaError_t launch_lse(const AttnArgs& a, cudaStream_t s) { return launch_mode<kLse>(a, s); }
 cudaError_t launch_score_max(const AttnArgs& a, cudaStream_t s) { return launch_mode<kMax>(a, s); }
 cudaError_t launch_future_sum(const AttnArgs& a, cudaStream_t s) {

@@ -7,6 +7,13 @@
 #include <stdint.h>
 
 namespace kvs {
+
+// Host: 3-D TMA map over a dense bf16 tensor [outer][rows][inner] with boxes of
+// box_rows x 64 elements (one 128-byte swizzle span), 128-byte swizzle; rows past the
+// end read as zeros.  inner must be a multiple of 8 (16-byte row stride).
+cudaError_t tma_map_bf16_3d(CUtensorMap* m, const void* base, int inner, int rows, int outer,
+                            int box_rows);
+
 namespace tc {
 
 // Every wait on an mbarrier gives up after this long (device global timer, ns); the
@@ -139,8 +146,26 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+// 16 consecutive TMEM columns of this thread's lane (32x32b shape, x16).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// Ties 16 registers written by an earlier tcgen05.ld to this point of the program, so
+// that the compiler cannot move their uses above the preceding tcgen05.wait::ld.
+__device__ __forceinline__ void reg_fence16(uint32_t* r) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
 }
 
 // OR of `pred` over the `nthreads` threads that use named barrier `id`.

@@ -279,6 +279,19 @@ class KVzapPipeline:
         self.prune_step()
 
 
+class KVzapMLPPipeline(KVzapPipeline):
+    """c6: KVzap-MLP surrogate (D_h -> D_h/8 -> H_kv) with the threshold + window rule,
+    then compaction."""
+
+    def score_step(self):
+        wl, x = self.wl, self.x
+        C.kvs_surrogate_mlp(self.dm, x["h"], wl.T, wl.D_mid, x["W1"], x["b1"], x["W2"], x["b2"],
+                            self.score, wl.tau, wl.w, self.mask, self.keep)
+
+    def stages(self):
+        return [("kvs_surrogate_mlp", self.score_step), ("kvs_compact_paged", self.prune_step)]
+
+
 def make_pipeline(wl: Workload, x: dict, **kw):
     if wl.kind in ("kvzip", "kvzip_plus"):
         return KVzipPipeline(wl, x, **kw)
@@ -288,4 +301,6 @@ def make_pipeline(wl: Workload, x: dict, **kw):
         return FuturePipeline(wl, x, **kw)
     if wl.kind == "kvzap":
         return KVzapPipeline(wl, x, **kw)
+    if wl.kind == "kvzap_mlp":
+        return KVzapMLPPipeline(wl, x, **kw)
     raise ValueError(wl.kind)

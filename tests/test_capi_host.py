@@ -27,7 +27,7 @@ def declared_symbols():
 
 def test_every_declared_symbol_is_exported(capi):
     syms = declared_symbols()
-    assert len(syms) >= 13
+    assert len(syms) >= 14
     lib = ctypes.CDLL(capi.LIB_PATH)
     for s in syms:
         assert hasattr(lib, s), s
@@ -79,6 +79,17 @@ def test_validation_codes(capi):
     odd = C.dims(1, 8, 8, 128, 100)
     assert lib.kvs_surrogate(ctypes.byref(odd), fake, 10, fake, fake, fake, 0.0, 0, None, None,
                              None) == C.KVS_ERR_UNSUPPORTED
+    # MLP surrogate limits: H_kv not a power of two up to 16, D_mid not a multiple of 32,
+    # D_h not a multiple of 64, misaligned hidden states
+    for H, Dh, Dm in ((3, 256, 64), (32, 256, 64), (8, 256, 48), (8, 96, 64)):
+        bad = C.dims(1, H, H, 128, Dh)
+        assert lib.kvs_surrogate_mlp(ctypes.byref(bad), fake, 10, Dm, fake, fake, fake, fake, fake,
+                                     0.0, 0, None, None, None) == C.KVS_ERR_UNSUPPORTED
+    okd = C.dims(1, 8, 8, 128, 256)
+    assert lib.kvs_surrogate_mlp(ctypes.byref(okd), fake + 2, 10, 64, fake, fake, fake, fake, fake,
+                                 0.0, 0, None, None, None) == C.KVS_ERR_ALIGN
+    assert lib.kvs_surrogate_mlp(ctypes.byref(okd), fake, 10, 64, fake, fake, fake, fake, fake,
+                                 0.0, 0, fake, None, None) == C.KVS_ERR_ARG
     # compaction: max_pages too small, bad page size
     st = lib.kvs_compact_paged(ctypes.byref(dm), fake, fake, 100, fake, 16, fake, fake, 10, fake, 6,
                                fake, fake, fake, 1 << 20, None)

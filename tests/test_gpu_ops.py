@@ -153,6 +153,77 @@ def test_surrogate(C, Hkv, T):
                             MASK_BAND, "surrogate mask", log_domain=True)
 
 
+MLP_SHAPES = [
+    # L, T, D_h, D_mid, H_kv   (parts P of D_mid: <= 256 columns, multiples of 32)
+    (2, 300, 256, 64, 8),      # P=1, N=64, ragged last token tile
+    (2, 1000, 512, 512, 4),    # P=2, N=256
+    (1, 257, 1024, 640, 2),    # P=4, N=160
+    (1, 130, 128, 128, 16),    # 16 heads
+    (3, 1, 64, 32, 1),         # one token, one k-block
+    (1, 384, 4096, 512, 8),    # the Qwen3-8B shape (64 k-blocks), three full tiles
+]
+
+
+def _mlp_parts(Dm):
+    """Column parts of D_mid as kvs.h documents them: the fewest parts of at most 256
+    columns, each a multiple of 32."""
+    P = -(-Dm // 256)
+    while Dm % P or (Dm // P) % 32:
+        P += 1
+    return P
+
+
+def _mlp_inputs(L, T, Dh, Dm, H, seed):
+    gen = torch.Generator().manual_seed(seed)
+    h = torch.randn(L, T, Dh, generator=gen).to(torch.bfloat16)
+    W1 = (torch.randn(L, Dm, Dh, generator=gen) / math.sqrt(Dh)).to(torch.bfloat16)
+    b1 = torch.randn(L, Dm, generator=gen) * 0.5
+    W2 = (torch.randn(L, H, Dm, generator=gen) / math.sqrt(Dm)).to(torch.bfloat16)
+    b2 = torch.randn(L, H, generator=gen) - 4.0
+    return h, W1, b1, W2, b2
+
+
+@pytest.mark.parametrize("shape", MLP_SHAPES, ids=[str(s) for s in MLP_SHAPES])
+def test_surrogate_mlp(C, shape):
+    L, T, Dh, Dm, H = shape
+    w, tau = 5, -4.0
+    h, W1, b1, W2, b2 = _mlp_inputs(L, T, Dh, Dm, H, seed=T * 7 + Dm)
+    dm = C.dims(L, H, H, 128, Dh)
+    args = [t.cuda() for t in (h, W1, b1, W2, b2)]
+    z = torch.full((L, H, T), float("nan"), device="cuda")
+    mask = torch.empty(L, H, T, dtype=torch.uint8, device="cuda")
+    keep = torch.full((L, H), -7, dtype=torch.int32, device="cuda")
+    C.kvs_surrogate_mlp(dm, args[0], T, Dm, *args[1:], z, tau, w, mask, keep)
+    z2 = torch.empty_like(z)
+    C.kvs_surrogate_mlp(dm, args[0], T, Dm, *args[1:], z2)  # unfused
+    torch.cuda.synchronize()
+    want = O.mlp_surrogate(f64(h), f64(W1), b1.double().numpy(), f64(W2), b2.double().numpy())
+    zg = z.cpu().numpy()
+    assert_close_abs(zg, want, LOG_SCORE_ATOL, "mlp surrogate")
+    if _mlp_parts(Dm) <= 2:  # at most two partial sums per score: order-independent
+        assert np.array_equal(zg, z2.cpu().numpy())
+    m_same, k_same = O.prune_threshold(zg.astype(np.float64), np.float32(tau), w)
+    assert np.array_equal(mask.cpu().numpy(), m_same)
+    assert np.array_equal(keep.cpu().numpy(), k_same)
+    m_ref, _ = O.prune_threshold(want, tau, w)
+    assert_masks_match_near(mask.cpu().numpy(), m_ref, want, np.full(want.shape[:-1], tau),
+                            MASK_BAND, "mlp surrogate mask", log_domain=True)
+
+
+def test_surrogate_mlp_empty_and_unsupported(C):
+    h, W1, b1, W2, b2 = (t.cuda() for t in _mlp_inputs(1, 4, 64, 32, 2, seed=3))
+    z = torch.full((1, 2, 4), 5.0, device="cuda")
+    C.kvs_surrogate_mlp(C.dims(1, 2, 2, 128, 64), h, 0, 32, W1, b1, W2, b2, z)  # T = 0: no-op
+    torch.cuda.synchronize()
+    assert (z == 5.0).all()
+    with pytest.raises(C.KvsError) as e:
+        C.kvs_surrogate_mlp(C.dims(1, 3, 3, 128, 64), h, 4, 32, W1, b1, W2, b2, z)
+    assert e.value.status == C.KVS_ERR_UNSUPPORTED
+    with pytest.raises(C.KvsError) as e:
+        C.kvs_surrogate_mlp(C.dims(1, 2, 2, 128, 64), h, 4, 48, W1, b1, W2, b2, z)
+    assert e.value.status == C.KVS_ERR_UNSUPPORTED
+
+
 def _scores_with_ties(shape, seed, levels=None, nan_frac=0.0):
     r = np.random.default_rng(seed)
     s = r.normal(size=shape).astype(np.float32)

@@ -173,3 +173,29 @@ def test_c5_full_layer0(mods):
     npg = -(-sl // wl.page_size)
     assert np.array_equal(first[npg > 0], (np.cumsum(npg) - npg)[npg > 0])
     assert int(p.pages.needed.item()) == int(npg.sum())
+
+
+def test_c6_full_layer0_sampled(mods):
+    pipeline, W = mods
+    wl = W.WORKLOADS["c6"]
+    x = W.generate(wl, device="cuda")
+    p = pipeline.make_pipeline(wl, x)
+    p.step()
+    torch.cuda.synchronize()
+    rows = np.r_[0:4096, wl.T - 4096:wl.T]
+    z = O.mlp_surrogate(f64(x["h"][0:1, rows]), f64(x["W1"][0:1]), x["b1"][0:1].double().cpu().numpy(),
+                        f64(x["W2"][0:1]), x["b2"][0:1].double().cpu().numpy())
+    zg = p.score[0:1].cpu().numpy()
+    assert_close_abs(zg[..., rows], z, LOG_SCORE_ATOL, "c6 MLP surrogate (layer 0, sampled tokens)")
+    mg = p.mask[0:1].cpu().numpy()
+    # the threshold rule applied to the kernel's own fp32 scores, over the whole layer
+    m_same, _ = O.prune_threshold(zg.astype(np.float64), np.float32(wl.tau), wl.w)
+    assert np.array_equal(mg, m_same)
+    # and the oracle's decision on the sampled tokens, except next to tau
+    m_ref, _ = O.prune_threshold(z, wl.tau, 0)
+    m_ref[..., rows >= wl.T - wl.w] = 1
+    assert_masks_match_near(mg[..., rows], m_ref, z, np.full(z.shape[:-1], wl.tau), MASK_BAND,
+                            "c6 mask (sampled tokens)", log_domain=True)
+    assert np.array_equal(p.keep[0:1].cpu().numpy(), mg.sum(-1))
+    for h in range(wl.H_kv):
+        _check_pages(p.pages, 0, h, x["k"][0, h].cpu(), x["v"][0, h].cpu(), mg[0, h])
