@@ -103,6 +103,28 @@ def attention_rows(q: np.ndarray, keys: np.ndarray, lse_rows: np.ndarray) -> np.
     return np.where(causal_visible(n_q, n_k), a, 0.0)
 
 
+def attention_forward(q, k_ctx, k_tail, v_ctx, v_tail):
+    """Attention forward of every query head with its LSE normaliser.  The output of
+    head h at query j is o^h_j = sum_i a_ji v_i, the term that W_O then maps into the
+    residual stream [KVzap 3.2, Eq. 2]; the LSE is the normaliser an attention kernel
+    returns and the transposed pass reuses [KVpop 1. Key Terms].  Keys and values are
+    the concatenated [context | tail] of the head's KV head, bottom-right causal.
+    q [L][H_q][n_q][d], k_*/v_* [L][H_kv][n][d] (tail may be None or empty).
+    Returns (o [L][H_q][n_q][d], lse [L][H_q][n_q])."""
+    L, H_q, n_q, d = q.shape
+    g = _group(H_q, k_ctx.shape[1])
+    has_tail = k_tail is not None and k_tail.shape[2] > 0
+    keys = np.concatenate([k_ctx, k_tail], 2) if has_tail else k_ctx
+    vals = np.concatenate([v_ctx, v_tail], 2) if has_tail else v_ctx
+    lse_ = lse(q, k_ctx, k_tail if has_tail else None)
+    o = np.empty((L, H_q, n_q, d))
+    for l in range(L):
+        for hq in range(H_q):
+            a = attention_rows(q[l, hq], keys[l, hq // g], lse_[l, hq])
+            o[l, hq] = a @ vals[l, hq // g]
+    return o, lse_
+
+
 # ----------------------------------------------------------------------------- norms
 
 def value_norm(v: np.ndarray, w_o: np.ndarray, H_q: int) -> np.ndarray:

@@ -53,6 +53,12 @@ MUTATIONS = [
      "return L * T * H_kv * d * bytes_per_elem"),
     ("mlp cost over 8", "return D_h / 4 * (D_h + H_kv)", "return D_h / 8 * (D_h + H_kv)"),
     ("bf16 shift 15", "<< np.uint32(16)", "<< np.uint32(15)"),
+    ("forward uses modulo kv head for values", "o[l, hq] = a @ vals[l, hq // g]",
+     "o[l, hq] = a @ vals[l, hq % vals.shape[1]]"),
+    ("forward drops tail values", "vals = np.concatenate([v_ctx, v_tail], 2) if has_tail else v_ctx",
+     "vals = np.concatenate([v_ctx, 0 * v_tail], 2) if has_tail else v_ctx"),
+    ("forward transposes the weights", "o[l, hq] = a @ vals[l, hq // g]",
+     "o[l, hq] = (a[:, ::-1] @ vals[l, hq // g][::-1])[::-1]"),
     ("gelu without 1/sqrt2", "_erf(x / math.sqrt(2.0))", "_erf(x)"),
     ("gelu tanh form", "return 0.5 * x * (1.0 + _erf(x / math.sqrt(2.0)))",
      "return 0.5 * x * (1.0 + np.tanh(math.sqrt(2 / math.pi) * (x + 0.044715 * x ** 3)))"),

@@ -312,6 +312,72 @@ def test_surrogate_small_integers_exact():
             assert z[0, hh, t] == want
 
 
+# ------------------------------------------------------------------ attention forward
+
+def test_attention_forward_uniform_rows_give_causal_means():
+    # q = 0: every visible key gets weight 1/(off+j+1), so o_j is the mean of the
+    # values it sees (bottom-right causal)
+    L, Hkv, g, d, T, nt, nq = 1, 2, 2, 4, 5, 3, 4
+    v_ctx = rng.normal(size=(L, Hkv, T, d)); v_tail = rng.normal(size=(L, Hkv, nt, d))
+    k_ctx = rng.normal(size=(L, Hkv, T, d)); k_tail = rng.normal(size=(L, Hkv, nt, d))
+    q = np.zeros((L, Hkv * g, nq, d))
+    o, l_ = O.attention_forward(q, k_ctx, k_tail, v_ctx, v_tail)
+    off = T + nt - nq
+    vals = np.concatenate([v_ctx, v_tail], 2)
+    for hq in range(Hkv * g):
+        for j in range(nq):
+            want = vals[0, hq // g, : off + j + 1].mean(axis=0)
+            assert np.allclose(o[0, hq, j], want, rtol=0, atol=1e-13)
+            assert abs(l_[0, hq, j] - math.log(off + j + 1)) < 1e-13
+
+
+def test_attention_forward_constant_values_pass_through():
+    L, Hkv, Hq, d, T, nt, nq = 2, 1, 3, 8, 9, 4, 6
+    c = rng.normal(size=d)
+    q = rng.normal(size=(L, Hq, nq, d)) * 2
+    k_ctx = rng.normal(size=(L, Hkv, T, d)); k_tail = rng.normal(size=(L, Hkv, nt, d))
+    v_ctx = np.broadcast_to(c, (L, Hkv, T, d)).copy(); v_tail = np.broadcast_to(c, (L, Hkv, nt, d)).copy()
+    o, _ = O.attention_forward(q, k_ctx, k_tail, v_ctx, v_tail)
+    assert np.allclose(o, np.broadcast_to(c, o.shape), rtol=0, atol=1e-13)
+
+
+def test_attention_forward_one_hot_keys_copy_values():
+    # orthonormal keys scaled by alpha and q_j = alpha * e_pi(j): the visible key pi(j)
+    # takes essentially all the weight, so o_j = v_pi(j)
+    d, n, alpha = 8, 8, 40.0
+    keys = np.eye(n, d)[None, None] * alpha
+    vals = rng.normal(size=(1, 1, n, d))
+    pi = [0, 1, 0, 3, 2, 5, 4, 7]                       # pi(j) <= j: visible causally
+    q = np.stack([np.eye(n, d)[p] * alpha for p in pi])[None, None]
+    o, _ = O.attention_forward(q, keys, None, vals, None)
+    for j, p in enumerate(pi):
+        assert np.allclose(o[0, 0, j], vals[0, 0, p], rtol=0, atol=1e-9)
+
+
+def test_attention_forward_brute_force_loops():
+    L, Hkv, g, d, T, nt, nq = 1, 2, 2, 3, 4, 2, 3
+    q = rng.normal(size=(L, Hkv * g, nq, d))
+    k_ctx = rng.normal(size=(L, Hkv, T, d)); k_tail = rng.normal(size=(L, Hkv, nt, d))
+    v_ctx = rng.normal(size=(L, Hkv, T, d)); v_tail = rng.normal(size=(L, Hkv, nt, d))
+    o, l_ = O.attention_forward(q, k_ctx, k_tail, v_ctx, v_tail)
+    nk = T + nt
+    for hq in range(Hkv * g):
+        kv = hq // g
+        for j in range(nq):
+            ws, vs = [], []
+            for i in range(nk):
+                if i > nk - nq + j:
+                    continue
+                k = k_ctx[0, kv, i] if i < T else k_tail[0, kv, i - T]
+                v = v_ctx[0, kv, i] if i < T else v_tail[0, kv, i - T]
+                ws.append(math.exp(sum(q[0, hq, j, c] * k[c] for c in range(d)) / math.sqrt(d)))
+                vs.append(v)
+            z = sum(ws)
+            assert abs(l_[0, hq, j] - math.log(z)) < 1e-12
+            for c in range(d):
+                assert abs(o[0, hq, j, c] - sum(w * v[c] for w, v in zip(ws, vs)) / z) < 1e-12
+
+
 # ------------------------------------------------------------------ MLP surrogate (GELU)
 
 # standard normal CDF at 1, -1, 2 (normal-table values)
