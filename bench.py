@@ -10,6 +10,7 @@ One step = one pass of the whole path over one batch of synthetic input (all lay
   c3: vnorm -> 16 x (lse -> score_max) -> per-layer threshold (25th percentile, calibrated
       once before timing) with w=128 -> compaction
   c4: lse (causal) -> future mass (w=128) -> top-k 25% / 12.5% + window -> compaction
+      (--attn-forward: pass 1 is the attention forward, output + LSE, instead)
   c5: surrogate (+ fused threshold tau=-5, w=128) -> compaction
   c6: MLP surrogate 4096 -> 512 -> 8 (+ threshold tau=-4, w=128) -> compaction
 Metric: context KV tokens scored+pruned per second per layer (all heads) = T * L / step time.
@@ -70,6 +71,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="c2", choices=["c1", "c2", "c3", "c4", "c5", "c6"])
     ap.add_argument("--impl", default="kvs", choices=["kvs", "reference"])
+    ap.add_argument("--attn-forward", action="store_true",
+                    help="c4: pass 1 is the attention forward (output + LSE) instead of the "
+                         "LSE-only pass")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--stage-reps", type=int, default=None)
@@ -114,6 +118,7 @@ def algorithmic_work(wl, p):
         m = max(0, n - w)
         el2 = L * wl.H_q * m * (m + 1) // 2
         out["kvs_lse"] = ("tensor", 2 * d * el1, "flop")
+        out["kvs_attn_fwd"] = ("tensor", 4 * d * el1, "flop")  # S = Q K^T and O = P V
         out["kvs_score_future_sum"] = ("tensor", 2 * d * el2, "flop")
     if wl.kind == "kvzap":
         rows = L * wl.H_kv
@@ -219,10 +224,11 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def build_pipeline(wl, device):
+def build_pipeline(wl, device, attn_forward=False):
     from kv_cache_eviction_lse_gb300 import pipeline, workloads as W
     x = W.generate(wl, device=device)
-    p = pipeline.make_pipeline(wl, x)
+    p = pipeline.make_pipeline(wl, x, attn_forward=True) if attn_forward else \
+        pipeline.make_pipeline(wl, x)
     if wl.kind == "kvzip_plus_chunked":
         # calibrate the per-layer threshold once (25th percentile of the non-window
         # scores of each layer), then keep it fixed for the timed steps
@@ -257,7 +263,7 @@ def run_gpu(args, rank, world, local):
         wl = wl.scaled(L=min(args.layers, wl.L))
     K = args.steps or DEFAULT_STEPS[args.workload]
     Wm = max(3, args.warmup)
-    x, p = build_pipeline(wl, dev)
+    x, p = build_pipeline(wl, dev, attn_forward=args.attn_forward)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -364,6 +370,8 @@ def run_gpu(args, rank, world, local):
                    "H_q": wl.H_q, "H_kv": wl.H_kv, "d": wl.d, "D_h": wl.D_h,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "launch": "python calls" if args.no_graph else "CUDA graph of the step",
+                   "pass1": "attention forward (output + LSE)" if args.attn_forward
+                   else "LSE-only pass",
                    "l2": f"{L2_FLUSH_BYTES >> 20} MB buffer written between timed steps"},
         "roofline": roofline,
         "kernels": kernels,

@@ -99,6 +99,31 @@ kvs_status kvs_lse(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
                    float* lse, void* stream);
 
 /* ---------------------------------------------------------------------------------
+ * kvs_attn_fwd -- attention forward that also returns its LSE normaliser, so that a
+ * caller running attention anyway gets pass 1 for free [KVpop 1. Key Terms: the
+ * transposed pass reuses the LSE the attention kernel returns; KVzap 3.2, Eq. 2: the
+ * output of head hq at query j is sum_i a_ji v_i].
+ *
+ *   o[l][hq][j]   = sum_{i <= off + j} a_ji v_i,  a_ji = exp(q_j . key_i / sqrt(d) - lse_j)
+ *   lse[l][hq][j] = exactly as kvs_lse
+ *
+ * Keys and values are [k_ctx | k_tail] and [v_ctx | v_tail] of KV head hq / g, with the
+ * bottom-right causal alignment of kvs_lse.  The softmax weights are rounded to bf16
+ * before they multiply V on the tensor cores; o is fp32-accumulated and stored as bf16.
+ *
+ *   q              [L][H_q][n_q][d]      bf16
+ *   k_ctx, v_ctx   [L][H_kv][T][d]       bf16   (may be NULL when T == 0)
+ *   k_tail, v_tail [L][H_kv][n_tail][d]  bf16   (may be NULL when n_tail == 0)
+ *   o              [L][H_q][n_q][d]      bf16   output
+ *   lse            [L][H_q][n_q]         fp32   output
+ * Requires n_q <= T + n_tail.
+ * ------------------------------------------------------------------------------- */
+kvs_status kvs_attn_fwd(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
+                        const kvs_bf16* k_ctx, const kvs_bf16* v_ctx, int32_t T,
+                        const kvs_bf16* k_tail, const kvs_bf16* v_tail, int32_t n_tail,
+                        kvs_bf16* o, float* lse, void* stream);
+
+/* ---------------------------------------------------------------------------------
  * kvs_score_max -- pass 2, KVzip / KVzip+ reduction [KVzap 3.1 Eq. 1, 3.2 Eq. 3].
  * Recomputes a_ji = exp(q_j . k_i / sqrt(d) - lse_j) tile by tile (the dense matrix
  * is never formed) and reduces each context key over the scoring queries and over

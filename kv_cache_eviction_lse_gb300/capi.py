@@ -66,6 +66,7 @@ _SIGS = {
     "kvs_vnorm_workspace_size": ([_D], _S),
     "kvs_vnorm": ([_D, _P, _I, _P, _P, _P, _S, _P], ctypes.c_int),
     "kvs_vnorm_noalloc": ([_D, _P, _I, _P, _P, _P], ctypes.c_int),
+    "kvs_attn_fwd": ([_D, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _P], ctypes.c_int),
     "kvs_surrogate": ([_D, _P, _I, _P, _P, _P, _F, _I, _P, _P, _P], ctypes.c_int),
     "kvs_surrogate_mlp": ([_D, _P, _I, _I, _P, _P, _P, _P, _P, _F, _I, _P, _P, _P], ctypes.c_int),
     "kvs_prune_mask": ([_D, _P, _I, _I, _F, _I, _I, _P, _P, _P], ctypes.c_int),
@@ -162,6 +163,11 @@ def kvs_vnorm_noalloc(dm, v, T, w_o, vnorm, stream=None):
     """kvs_vnorm without a workspace argument: uses the library's built-in device
     scratch (for callers that cannot allocate device memory; see include/kvs.h)."""
     _check(_lib.kvs_vnorm_noalloc(_d(dm), _ptr(v), T, _ptr(w_o), _ptr(vnorm), _stream(stream)))
+
+
+def kvs_attn_fwd(dm, q, n_q, k_ctx, v_ctx, T, k_tail, v_tail, n_tail, o, lse, stream=None):
+    _check(_lib.kvs_attn_fwd(_d(dm), _ptr(q), n_q, _ptr(k_ctx), _ptr(v_ctx), T, _ptr(k_tail),
+                             _ptr(v_tail), n_tail, _ptr(o), _ptr(lse), _stream(stream)))
 
 
 def kvs_surrogate(dm, h, T, W, b, score, tau=0.0, w=0, mask=None, keep=None, stream=None):

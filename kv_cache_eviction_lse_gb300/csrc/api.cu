@@ -92,11 +92,12 @@ uint64_t kvs_launch_count(void) { return kvs::g_launches.load(std::memory_order_
 
 kvs_status kvs_device_error(int32_t* code_out, int32_t clear, void* stream) {
   REQUIRE(code_out, KVS_ERR_ARG, "kvs_device_error: code_out is NULL");
-  int code = 0, code_mlp = 0;
+  int code = 0, code_mlp = 0, code_fwd = 0;
   cudaError_t e = kvs::attn_device_error(&code, clear != 0, as_stream(stream));
   if (e == cudaSuccess) e = kvs::mlp_device_error(&code_mlp, clear != 0, as_stream(stream));
+  if (e == cudaSuccess) e = kvs::fwd_device_error(&code_fwd, clear != 0, as_stream(stream));
   if (e != cudaSuccess) return cuda_status(e, "kvs_device_error");
-  *code_out = code ? code : code_mlp;
+  *code_out = code ? code : (code_mlp ? code_mlp : code_fwd);
   return ok();
 }
 
@@ -122,6 +123,35 @@ kvs_status kvs_lse(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q, const k
 size_t kvs_score_max_workspace_size(const kvs_dims* dims, int32_t n_q, int32_t with_h) {
   if (!dims || !with_h || n_q <= 0 || dims->L <= 0) return 0;
   return (size_t)dims->L * n_q * sizeof(float);
+}
+
+kvs_status kvs_attn_fwd(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
+                        const kvs_bf16* k_ctx, const kvs_bf16* v_ctx, int32_t T,
+                        const kvs_bf16* k_tail, const kvs_bf16* v_tail, int32_t n_tail,
+                        kvs_bf16* o, float* lse, void* stream) {
+  kvs_status st = check_dims(dims, __func__);
+  if (st) return st;
+  REQUIRE(n_q >= 0 && T >= 0 && n_tail >= 0, KVS_ERR_ARG, "kvs_attn_fwd: negative size");
+  REQUIRE(n_q <= T + n_tail, KVS_ERR_SHAPE, "kvs_attn_fwd: n_q = %d exceeds keys T + n_tail = %d",
+          n_q, T + n_tail);
+  if (n_q == 0) return ok();
+  REQUIRE_PTR(q);
+  REQUIRE_PTR(o);
+  REQUIRE_PTR(lse);
+  if (T > 0) {
+    REQUIRE_PTR(k_ctx);
+    REQUIRE_PTR(v_ctx);
+  }
+  if (n_tail > 0) {
+    REQUIRE_PTR(k_tail);
+    REQUIRE_PTR(v_tail);
+  }
+  kvs::FwdArgs a;
+  a.q = q; a.k_ctx = k_ctx; a.v_ctx = v_ctx; a.k_tail = k_tail; a.v_tail = v_tail;
+  a.o = o; a.lse = lse;
+  a.L = dims->L; a.Hq = dims->H_q; a.Hkv = dims->H_kv; a.d = dims->d;
+  a.n_q = n_q; a.T = T; a.n_tail = n_tail;
+  return cuda_status(kvs::launch_attn_fwd(a, as_stream(stream)), "kvs_attn_fwd");
 }
 
 kvs_status kvs_score_max(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,

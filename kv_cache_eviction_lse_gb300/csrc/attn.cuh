@@ -30,6 +30,21 @@ cudaError_t launch_future_sum(const AttnArgs& a, cudaStream_t s);
 // gpair = Gram pairs, out = vn [L][Hq][T]; needs Hq / Hkv <= 16.
 cudaError_t launch_vnorm_quad(const AttnArgs& a, cudaStream_t s);
 
+struct FwdArgs {
+  const bf16_t* q = nullptr;       // [L][Hq][n_q][d]
+  const bf16_t* k_ctx = nullptr;   // [L][Hkv][T][d]
+  const bf16_t* v_ctx = nullptr;   // [L][Hkv][T][d]
+  const bf16_t* k_tail = nullptr;  // [L][Hkv][n_tail][d]
+  const bf16_t* v_tail = nullptr;  // [L][Hkv][n_tail][d]
+  bf16_t* o = nullptr;             // [L][Hq][n_q][d]
+  float* lse = nullptr;            // [L][Hq][n_q]
+  int L = 0, Hq = 0, Hkv = 0, d = 0, n_q = 0, T = 0, n_tail = 0;
+};
+
+// Attention forward (bottom-right causal over [context | tail]) with its LSE.
+cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t s);
+cudaError_t fwd_device_error(int* code, bool clear, cudaStream_t s);
+
 // Reads (and with `clear` resets) the device error word of the scoring kernels.
 cudaError_t attn_device_error(int* code, bool clear, cudaStream_t s);
 

@@ -1,0 +1,413 @@
+// Attention forward that returns its LSE normaliser, on the 5th-generation tensor cores.
+//
+// For every query head h and query j (bottom-right causal over the concatenated
+// [context | tail] keys of the head's KV head):
+//   o^h_j = sum_i a_ji v_i,   a_ji = exp(q_j.k_i / sqrt d - LSE_j)
+// [KVzap review 3.2, Eq. 2: the head output that W_O maps into the residual stream]
+// together with LSE_j, the normaliser the transposed scoring pass reuses [KVpop review,
+// 1. Key Terms], so that pruning pays only for pass 2 when the attention runs anyway.
+//
+// One CTA per 128 queries of one head; keys in tiles of 128 (online softmax):
+//   warp 0      TMA: the Q tile once, then K and V tiles through a 2-stage ring
+//   warp 1      owns TMEM (S double buffer: 2 x 128 columns; O: d columns) and issues
+//               S(j) = Q K(j)^T, then O += P(j-1) V(j-1) (P from shared memory,
+//               V as an MN-major operand straight from its TMA box)
+//   warps 2-9   softmax, two threads per query row (one per 64-key half): read S with
+//               tcgen05.ld, agree on the row max through shared memory, p = 2^(x - m)
+//               with one ex2 each, write P (bf16, 128-byte swizzled K-major) for the
+//               MMA, and rescale O in TMEM when the running max grows by more than
+//               2^8 (otherwise the stale max is kept: p <= 256 stays exact enough in
+//               bf16 and the final normalisation uses the same max)
+// The epilogue divides O by the row sum, writes it as bf16 and writes the LSE.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <math_constants.h>
+
+#include "attn.cuh"
+#include "tc.cuh"
+
+namespace kvs {
+
+__device__ int g_fwd_error = 0;
+
+namespace {
+
+constexpr int BM = 128;  // queries per CTA = TMEM lanes
+constexpr int BN = 128;  // keys per tile
+constexpr int kSoftThreads = 256;
+constexpr int kThreads = 64 + kSoftThreads;
+constexpr uint32_t kBox = 128 * 128;  // 128 rows x 64 bf16 (one 128-byte swizzle span)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kMaxSmem = 232448;
+constexpr int kErrWaitTimeout = 1;
+constexpr int kErrSmemAlign = 3;
+constexpr float kRescale = 8.f;  // log2 growth of the row max that forces a rescale of O
+
+template <int D>
+struct FCfg {
+  static constexpr int KH = D / 64;
+  static constexpr uint32_t TILE = KH * kBox;  // one K or V tile, or the Q tile
+  static constexpr uint32_t OFF_K = TILE;       // Q at 0
+  static constexpr uint32_t OFF_V = OFF_K + 2 * TILE;
+  static constexpr uint32_t OFF_P = OFF_V + 2 * TILE;  // P: 2 boxes of 64 keys
+  static constexpr uint32_t OFF_XM = OFF_P + 2 * kBox;  // row max exchange [2][2][BM]
+  static constexpr uint32_t OFF_XL = OFF_XM + 4 * BM * 4;  // row sum exchange [2][BM]
+  static constexpr uint32_t OFF_BAR = OFF_XL + 2 * BM * 4;
+  // q_full, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full, o_ready, done
+  static constexpr uint32_t NBAR = 12;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t USED = OFF_MISC + 16;
+  static constexpr uint32_t SMEM = (USED + 1024 <= kMaxSmem) ? USED + 1024 : kMaxSmem;
+  static_assert(USED <= kMaxSmem, "shared-memory plan exceeds the per-block limit");
+};
+
+__device__ __forceinline__ void fail(volatile uint32_t* abort_flag, int code) {
+  *abort_flag = 1u;
+  atomicCAS(&g_fwd_error, 0, code);
+}
+
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kt,
+                    const __grid_constant__ CUtensorMap tm_vt, const FwdArgs a) {
+  using C = FCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  if (pad + C::USED > C::SMEM) {
+    if (threadIdx.x == 0) atomicCAS(&g_fwd_error, 0, kErrSmemAlign);
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sb = raw + pad;
+  const uint32_t sQ = sb, sK = sb + C::OFF_K, sV = sb + C::OFF_V, sP = sb + C::OFF_P;
+  float* xm = reinterpret_cast<float*>(smem + C::OFF_XM);
+  float* xl = reinterpret_cast<float*>(smem + C::OFF_XL);
+  const uint32_t bar0 = sb + C::OFF_BAR;
+  const uint32_t bar_q = bar0;
+  auto bar_kvfull = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto bar_kvempty = [&](int s) { return bar0 + 8u * (3 + s); };
+  auto bar_sfull = [&](int s) { return bar0 + 8u * (5 + s); };
+  auto bar_sempty = [&](int s) { return bar0 + 8u * (7 + s); };
+  const uint32_t bar_p = bar0 + 8u * 9;
+  const uint32_t bar_o = bar0 + 8u * 10;
+  const uint32_t bar_done = bar0 + 8u * 11;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile uint32_t* abort_flag = misc + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int l = blockIdx.z, hq = blockIdx.y;
+  const int G = a.Hq / a.Hkv;
+  const int hk = hq / G;
+  const int n_k = a.T + a.n_tail;
+  const int off = n_k - a.n_q;
+  const int row0 = blockIdx.x * BM;
+  // key tiles this query tile sees: context tiles, then tail tiles
+  const int kv_end = off + min(row0 + BM, a.n_q);  // keys [0, kv_end) are visible to some query
+  const int n_ctx = (min(a.T, kv_end) + BN - 1) / BN;
+  const int ntiles = n_ctx + (min(a.n_tail, max(0, kv_end - a.T)) + BN - 1) / BN;
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(bar_q, 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(bar_kvfull(s), 1);
+      tc::mbar_init(bar_kvempty(s), 1);
+      tc::mbar_init(bar_sfull(s), 1);
+      tc::mbar_init(bar_sempty(s), kSoftThreads);
+    }
+    tc::mbar_init(bar_p, kSoftThreads);
+    tc::mbar_init(bar_o, 1);
+    tc::mbar_init(bar_done, 1);
+    misc[1] = 0u;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(sb + C::OFF_MISC, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch_desc(&tm_q);
+    tc::tma_prefetch_desc(&tm_k);
+    tc::tma_prefetch_desc(&tm_v);
+  }
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = misc[0];
+  const uint32_t t_o = tmem + 2 * BN;  // O accumulator columns [256, 256 + D)
+
+  if (warp == 0) {
+    // ============================================================ TMA producer
+    if (lane == 0) {
+      tc::mbar_expect_tx(bar_q, C::TILE);
+#pragma unroll
+      for (int kh = 0; kh < C::KH; ++kh)
+        tc::tma_load_3d(sQ + kh * kBox, &tm_q, bar_q, kh * 64, row0, l * a.Hq + hq);
+      int j = 0;
+      bool ok = true;
+      for (; j < ntiles; ++j) {
+        const int s = j & 1;
+        if (!tc::mbar_wait(bar_kvempty(s), ((j >> 1) & 1) ^ 1u) || *abort_flag) {
+          ok = false;
+          break;
+        }
+        const bool ctx = j < n_ctx;
+        const CUtensorMap* mk = ctx ? &tm_k : &tm_kt;
+        const CUtensorMap* mv = ctx ? &tm_v : &tm_vt;
+        const int row = ctx ? j * BN : (j - n_ctx) * BN;
+        const int head = l * a.Hkv + hk;
+        tc::mbar_expect_tx(bar_kvfull(s), 2 * C::TILE);
+#pragma unroll
+        for (int kh = 0; kh < C::KH; ++kh) {
+          tc::tma_load_3d(sK + s * C::TILE + kh * kBox, mk, bar_kvfull(s), kh * 64, row, head);
+          tc::tma_load_3d(sV + s * C::TILE + kh * kBox, mv, bar_kvfull(s), kh * 64, row, head);
+        }
+      }
+      if (!ok) {
+        fail(abort_flag, kErrWaitTimeout);
+        tc::mbar_wait(bar_q, 0);
+        for (int i = max(0, j - 2); i < j; ++i) tc::mbar_wait(bar_kvfull(i & 1), (i >> 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = tc::idesc_bf16(BM, BN);
+      constexpr uint32_t idesc_o = tc::idesc_bf16_bmn(BM, D);
+      bool ok = tc::mbar_wait(bar_q, 0);
+      int issued = 0;  // MMA groups issued (for the final drain)
+      for (int j = 0; ok && j <= ntiles; ++j) {
+        if (j < ntiles) {  // S(j) = Q K(j)^T
+          const int s = j & 1;
+          const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+          if (!tc::mbar_wait(bar_kvfull(s), ph) || !tc::mbar_wait(bar_sempty(s), ph ^ 1u) ||
+              *abort_flag) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t d_s = tmem + (uint32_t)(s * BN);
+          const uint32_t k_s = sK + s * C::TILE;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t o = (uint32_t)(k >> 2) * kBox + (uint32_t)(k & 3) * 32u;
+            tc::mma_bf16(d_s, tc::sdesc_sw128(sQ + o), tc::sdesc_sw128(k_s + o), idesc_s,
+                         k > 0 ? 1u : 0u);
+          }
+          tc::commit(bar_sfull(s));
+          ++issued;
+        }
+        if (j >= 1) {  // O += P(j-1) V(j-1)
+          const int jj = j - 1, s = jj & 1;
+          if (!tc::mbar_wait(bar_p, (uint32_t)jj & 1u) || *abort_flag) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t v_s = sV + s * C::TILE;
+#pragma unroll
+          for (int k = 0; k < BN / 16; ++k) {
+            const uint32_t pa = sP + (uint32_t)(k >> 2) * kBox + (uint32_t)(k & 3) * 32u;
+            tc::mma_bf16(t_o, tc::sdesc_sw128(pa), tc::sdesc_sw128_mn(v_s + 2048u * k, kBox),
+                         idesc_o, (jj > 0 || k > 0) ? 1u : 0u);
+          }
+          tc::commit(bar_kvempty(s));
+          tc::commit(bar_o);
+          ++issued;
+        }
+      }
+      if (!ok) fail(abort_flag, kErrWaitTimeout);
+      // drain: every MMA issued so far has completed once this commit lands
+      if (issued > 0) {
+        tc::commit(bar_done);
+        tc::mbar_wait(bar_done, 0);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ============================================================ softmax + epilogue
+    const int h = (warp - 2) >> 2;      // 64-key half of each tile (and D/2 half of O)
+    const int eq = warp & 3;            // TMEM lane quarter
+    const int row = eq * 32 + lane;     // query row within the tile
+    const int qr = row0 + row;          // query index
+    const uint32_t lane_off = (uint32_t)(eq * 32) << 16;
+    const float sc2 = rsqrtf((float)D) * kLog2e;
+    float m_used = -1e30f, lsum = 0.f;
+    bool failed = false;
+    for (int j = 0; j < ntiles; ++j) {
+      const int s = j & 1;
+      bool ok = tc::mbar_wait(bar_sfull(s), (uint32_t)(j >> 1) & 1u) && !*abort_flag;
+      if (tc::bar_or(2, kSoftThreads, !ok)) {
+        failed = true;
+        break;
+      }
+      tc::fence_after_sync();
+      uint32_t v[64];
+      const uint32_t ts = tmem + lane_off + (uint32_t)(s * BN + h * 64);
+      tc::tmem_ld32(ts, v);
+      tc::tmem_ld32(ts + 32, v + 32);
+      tc::tmem_ld_wait();
+      tc::fence_before_sync();
+      tc::mbar_arrive(bar_sempty(s));
+
+      const bool ctx = j < n_ctx;
+      const int kb = (ctx ? j * BN : a.T + (j - n_ctx) * BN) + h * 64;
+      const int lim = ctx ? a.T : n_k;
+      if (kb + 64 > lim || kb + 63 > off + qr) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (kb + c >= lim || kb + c > off + qr) v[c] = __float_as_uint(-CUDART_INF_F);
+      }
+      float mx = -CUDART_INF_F;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(v[c]));
+      float* xmj = xm + s * 2 * BM;
+      xmj[h * BM + row] = mx * sc2;
+      named_sync(1, kSoftThreads);
+      const float mt = fmaxf(mx * sc2, xmj[(1 - h) * BM + row]);
+      const bool need = mt > m_used + kRescale;
+      float factor = 1.f;
+      if (need) {
+        factor = fast_exp2(m_used - mt);
+        m_used = mt;
+        lsum *= factor;
+      }
+      uint32_t pk[32];
+      float ps = 0.f;
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        const float p0 = fast_exp2(fmaf(__uint_as_float(v[c]), sc2, -m_used));
+        const float p1 = fast_exp2(fmaf(__uint_as_float(v[c + 1]), sc2, -m_used));
+        ps += p0 + p1;
+        pk[c / 2] = pack_bf16(p0, p1);
+      }
+      lsum += ps;
+
+      if (j > 0) {  // O and the P buffer are free once O += P(j-1) V(j-1) has completed
+        ok = tc::mbar_wait(bar_o, (uint32_t)(j - 1) & 1u) && !*abort_flag;
+        if (tc::bar_or(2, kSoftThreads, !ok)) {
+          failed = true;
+          break;
+        }
+        tc::fence_after_sync();
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int cb = 0; cb < D / 64; ++cb) {
+            const uint32_t to = t_o + lane_off + (uint32_t)(h * (D / 2) + 32 * cb);
+            tc::tmem_ld32(to, v);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * factor);
+            tc::tmem_st32(to, v);
+          }
+          tc::tmem_st_wait();
+        }
+      }
+      // P row half: keys h*64 .. h*64+63 = box h, 8 chunks of 16 B, 128-byte swizzle
+      uint8_t* prow = smem + C::OFF_P + h * kBox + row * 128;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        uint4 u = make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+        *reinterpret_cast<uint4*>(prow + ((c8 ^ (row & 7)) << 4)) = u;
+      }
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      tc::mbar_arrive(bar_p);
+    }
+    if (!failed && ntiles > 0) {
+      const bool ok = tc::mbar_wait(bar_o, (uint32_t)(ntiles - 1) & 1u) && !*abort_flag;
+      failed = tc::bar_or(2, kSoftThreads, !ok);
+      if (!failed) {
+        tc::fence_after_sync();
+        xl[h * BM + row] = lsum;
+        named_sync(1, kSoftThreads);
+        const float ltot = lsum + xl[(1 - h) * BM + row];
+        const float inv = 1.f / ltot;
+        uint32_t v[32];
+        uint32_t ob[D / 4];
+#pragma unroll
+        for (int cb = 0; cb < D / 64; ++cb) {
+          tc::tmem_ld32(t_o + lane_off + (uint32_t)(h * (D / 2) + 32 * cb), v);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; c += 2)
+            ob[cb * 16 + c / 2] =
+                pack_bf16(__uint_as_float(v[c]) * inv, __uint_as_float(v[c + 1]) * inv);
+        }
+        if (qr < a.n_q) {
+          uint4* dst = reinterpret_cast<uint4*>(
+              a.o + ((size_t)(l * a.Hq + hq) * a.n_q + qr) * D + h * (D / 2));
+#pragma unroll
+          for (int c = 0; c < D / 16; ++c)
+            dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+          if (h == 0) a.lse[(size_t)(l * a.Hq + hq) * a.n_q + qr] = (m_used + fast_log2(ltot)) * kLn2;
+        }
+      }
+    }
+    if (failed) atomicCAS(&g_fwd_error, 0, (int)kErrWaitTimeout);
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
+  using C = FCfg<D>;
+  CUtensorMap tq, tk, tv, tkt, tvt;
+  cudaError_t e = tma_map_bf16_3d(&tq, a.q, D, a.n_q, a.L * a.Hq, BM);
+  if (e == cudaSuccess)
+    e = a.T > 0 ? tma_map_bf16_3d(&tk, a.k_ctx, D, a.T, a.L * a.Hkv, BN)
+                : tma_map_bf16_3d(&tk, a.q, D, 1, 1, BN);
+  if (e == cudaSuccess)
+    e = a.T > 0 ? tma_map_bf16_3d(&tv, a.v_ctx, D, a.T, a.L * a.Hkv, BN)
+                : tma_map_bf16_3d(&tv, a.q, D, 1, 1, BN);
+  if (e == cudaSuccess)
+    e = a.n_tail > 0 ? tma_map_bf16_3d(&tkt, a.k_tail, D, a.n_tail, a.L * a.Hkv, BN)
+                     : tma_map_bf16_3d(&tkt, a.q, D, 1, 1, BN);
+  if (e == cudaSuccess)
+    e = a.n_tail > 0 ? tma_map_bf16_3d(&tvt, a.v_tail, D, a.n_tail, a.L * a.Hkv, BN)
+                     : tma_map_bf16_3d(&tvt, a.q, D, 1, 1, BN);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.n_q + BM - 1) / BM, a.Hq, a.L);
+  auto kern = attn_fwd_kernel<D>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+  if (e != cudaSuccess) return e;
+  count_launches(1);
+  kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tkt, tvt, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t s) {
+  if (a.n_q == 0) return cudaSuccess;
+  return a.d == 128 ? launch_fwd_d<128>(a, s) : launch_fwd_d<64>(a, s);
+}
+
+cudaError_t fwd_device_error(int* code, bool clear, cudaStream_t s) {
+  cudaError_t e = cudaMemcpyFromSymbolAsync(code, g_fwd_error, sizeof(int), 0,
+                                            cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && clear && *code) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_fwd_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
+  return e;
+}
+
+}  // namespace kvs

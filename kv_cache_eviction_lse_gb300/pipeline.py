@@ -198,13 +198,17 @@ class ChunkedKVzipPipeline:
 class FuturePipeline:
     """c4: KVpop future-attention target, then top-k budgets plus the window."""
 
-    def __init__(self, wl: Workload, x: dict, ratios=None):
+    def __init__(self, wl: Workload, x: dict, ratios=None, attn_forward=False):
         self.wl, self.x = wl, x
         dev = x["q"].device
         L = x["q"].shape[0]
         self.L = L
         self.dm = C.dims(L, wl.H_q, wl.H_kv, wl.d, 0)
         self.lse = _empty((L, wl.H_q, wl.T), torch.float32, dev)
+        # attn_forward: pass 1 is the attention forward itself (output + LSE), as in a
+        # model that runs attention anyway and hands its LSE to the transposed pass
+        self.attn_forward = attn_forward
+        self.o = _empty((L, wl.H_q, wl.T, wl.d), torch.bfloat16, dev) if attn_forward else None
         self.score = _empty((L, wl.H_kv, wl.T), torch.float32, dev)
         self.ratios = tuple(ratios if ratios is not None else wl.keep_ratios)
         self.masks = [_empty((L, wl.H_kv, wl.T), torch.uint8, dev) for _ in self.ratios]
@@ -215,6 +219,10 @@ class FuturePipeline:
     def _lse(self):
         wl, x, dm = self.wl, self.x, self.dm
         C.kvs_lse(dm, x["q"], wl.T, x["k"], wl.T, None, 0, self.lse)
+
+    def _forward(self):
+        wl, x, dm = self.wl, self.x, self.dm
+        C.kvs_attn_fwd(dm, x["q"], wl.T, x["k"], x["v"], wl.T, None, None, 0, self.o, self.lse)
 
     def _future(self):
         wl, x, dm = self.wl, self.x, self.dm
@@ -230,8 +238,11 @@ class FuturePipeline:
         for m, pg in zip(self.masks, self.pages):
             compact_into(dm, x["k"], x["v"], wl.T, m, pg, self.cws)
 
+    def _pass1(self):
+        return ("kvs_attn_fwd", self._forward) if self.attn_forward else ("kvs_lse", self._lse)
+
     def score_step(self):
-        self._lse()
+        self._pass1()[1]()
         self._future()
 
     def prune_step(self):
@@ -239,7 +250,7 @@ class FuturePipeline:
         self._compact()
 
     def stages(self):
-        return [("kvs_lse", self._lse), ("kvs_score_future_sum", self._future),
+        return [self._pass1(), ("kvs_score_future_sum", self._future),
                 ("kvs_prune_mask", self._prune), ("kvs_compact_paged", self._compact)]
 
     def step(self):

@@ -52,6 +52,80 @@ def test_lse(C, shape, scale):
     assert_close_abs(out.cpu().numpy(), want, LSE_ATOL, "lse")
 
 
+FWD_SHAPES = [
+    # L, Hkv, Hq, d, T, n_tail, n_q
+    (2, 2, 6, 128, 150, 79, 70),
+    (1, 1, 2, 64, 256, 264, 256),
+    (2, 2, 4, 128, 300, 0, 300),     # causal self-attention, ragged tiles
+    (1, 3, 3, 64, 1, 0, 1),          # single key
+    (1, 1, 4, 128, 0, 97, 97),       # no context keys
+    (3, 1, 2, 128, 333, 5, 1),       # one query
+    (1, 2, 4, 128, 700, 20, 400),    # several key tiles per query tile, two query tiles
+]
+
+
+def _fwd_inputs(shape, seed, scale):
+    L, Hkv, Hq, d, T, nt, nq = shape
+    x = _inputs(*shape, seed=seed, scale=scale)
+    gen = torch.Generator().manual_seed(seed + 1)
+    x["v_tail"] = torch.randn(L, Hkv, nt, d, generator=gen).to(torch.bfloat16)
+    return x
+
+
+def _o_tolerance(o_ref, v_ctx, v_tail, g):
+    """Bound on |o_gpu - o_ref|: the softmax weights are rounded to bf16 (relative
+    2^-9 each, so at most 2^-9 max|v| on any output) and o is stored as bf16 (2^-9
+    |o|); the fp32 accumulation and ex2.approx add far less.  Twice that bound."""
+    vals = np.concatenate([v_ctx, v_tail], 2) if v_tail.shape[2] else v_ctx
+    vmax = np.abs(vals).max(axis=(2, 3)) if vals.shape[2] else np.zeros(vals.shape[:2])
+    vmax = np.repeat(vmax, g, axis=1)[:, :, None, None]
+    return 2.0 ** -8 * (np.abs(o_ref) + vmax)
+
+
+@pytest.mark.parametrize("shape", FWD_SHAPES, ids=[str(s) for s in FWD_SHAPES])
+@pytest.mark.parametrize("scale", [1.0, 2.5])
+def test_attn_fwd(C, shape, scale):
+    L, Hkv, Hq, d, T, nt, nq = shape
+    x = _fwd_inputs(shape, seed=23 + T + nq, scale=scale)
+    g = cuda(x)
+    o = torch.full((L, Hq, nq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((L, Hq, nq), float("nan"), device="cuda")
+    C.kvs_attn_fwd(C.dims(L, Hq, Hkv, d), g["q"], nq, g["k_ctx"] if T else None,
+                   g["v_ctx"] if T else None, T, g["k_tail"] if nt else None,
+                   g["v_tail"] if nt else None, nt, o, lse)
+    lse_only = torch.empty_like(lse)
+    C.kvs_lse(C.dims(L, Hq, Hkv, d), g["q"], nq, g["k_ctx"] if T else None, T,
+              g["k_tail"] if nt else None, nt, lse_only)
+    torch.cuda.synchronize()
+    vc, vt = f64(x["v_ctx"]), f64(x["v_tail"])
+    o_ref, lse_ref = O.attention_forward(f64(x["q"]), f64(x["k_ctx"]), f64(x["k_tail"]), vc, vt)
+    assert_close_abs(lse.cpu().numpy(), lse_ref, LSE_ATOL, "forward lse")
+    assert_close_abs(lse.cpu().numpy(), lse_only.cpu().numpy(), LSE_ATOL, "forward lse vs kvs_lse")
+    err = np.abs(f64(o) - o_ref)
+    tol = _o_tolerance(o_ref, vc, vt, Hq // Hkv)
+    assert (err <= tol).all(), f"forward o: {(err > tol).sum()} beyond bound; max err {err.max()}"
+
+
+def test_attn_fwd_growing_logits_rescale(C):
+    # keys grow along the sequence, so the row max keeps rising across key tiles and O
+    # is rescaled in TMEM many times
+    L, Hkv, Hq, d, T = 1, 1, 2, 128, 1024
+    gen = torch.Generator().manual_seed(5)
+    ramp = torch.linspace(0.2, 3.0, T)[None, None, :, None]
+    k = (torch.randn(L, Hkv, T, d, generator=gen) * ramp).to(torch.bfloat16)
+    v = torch.randn(L, Hkv, T, d, generator=gen).to(torch.bfloat16)
+    q = (torch.randn(L, Hq, T, d, generator=gen) * 2).to(torch.bfloat16)
+    o = torch.empty(L, Hq, T, d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(L, Hq, T, device="cuda")
+    C.kvs_attn_fwd(C.dims(L, Hq, Hkv, d), q.cuda(), T, k.cuda(), v.cuda(), T, None, None, 0, o, lse)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = O.attention_forward(f64(q), f64(k), None, f64(v), None)
+    assert_close_abs(lse.cpu().numpy(), lse_ref, LSE_ATOL, "forward lse (growing logits)")
+    err = np.abs(f64(o) - o_ref)
+    tol = _o_tolerance(o_ref, f64(v), f64(v)[:, :, :0], Hq // Hkv)
+    assert (err <= tol).all(), f"forward o: {(err > tol).sum()} beyond bound; max err {err.max()}"
+
+
 SCORE_SHAPES = [
     (2, 2, 6, 128, 150, 79, 70, 192),
     (1, 1, 2, 64, 256, 264, 256, 0),

@@ -199,3 +199,29 @@ def test_c6_full_layer0_sampled(mods):
     assert np.array_equal(p.keep[0:1].cpu().numpy(), mg.sum(-1))
     for h in range(wl.H_kv):
         _check_pages(p.pages, 0, h, x["k"][0, h].cpu(), x["v"][0, h].cpu(), mg[0, h])
+
+
+def test_c4_attention_forward_sampled_rows(mods):
+    """The attention forward (output + LSE) as pass 1 of the c4 step: the first and the
+    last 256 queries of layer 0, KV-head group 0, against the oracle, and its LSE
+    against the LSE-only pass 1 everywhere."""
+    pipeline, W = mods
+    wl = W.WORKLOADS["c4"]
+    x = W.generate(wl, device="cuda")
+    p = pipeline.make_pipeline(wl, x, attn_forward=True)
+    p.step()
+    ref = pipeline.make_pipeline(wl, x)
+    ref.score_step()
+    torch.cuda.synchronize()
+    assert_close_abs(p.lse.cpu().numpy(), ref.lse.cpu().numpy(), LSE_ATOL, "c4 forward lse vs kvs_lse")
+    g, T, n = wl.g, wl.T, 256
+    for lo in (0, T - n):
+        q = f64(x["q"][0:1, 0:g, lo:lo + n])
+        k = f64(x["k"][0:1, 0:1, : lo + n])
+        v = f64(x["v"][0:1, 0:1, : lo + n])
+        o_ref, lse_ref = O.attention_forward(q, k, None, v, None)
+        assert_close_abs(p.lse[0:1, 0:g, lo:lo + n].cpu().numpy(), lse_ref, LSE_ATOL, "c4 forward lse")
+        err = np.abs(f64(p.o[0:1, 0:g, lo:lo + n]) - o_ref)
+        vmax = np.abs(v).max()
+        tol = 2.0 ** -8 * (np.abs(o_ref) + vmax)
+        assert (err <= tol).all(), f"c4 forward o rows {lo}: max err {err.max()}"
