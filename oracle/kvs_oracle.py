@@ -363,6 +363,29 @@ def compact_paged(k, v, mask, page_size=16, max_pages=None):
     return k_pages, v_pages, block_table, seq_lens, total
 
 
+def decode_prune(score, tau, w):
+    """Decode-time pruning at the window boundary [KVzap: the criterion is
+    phase-agnostic and works while decoding; KVpop 1. Key Terms: a token's fate is
+    decided when it leaves the protected window].  Tokens arrive one per step; when
+    token t arrives, token t - w leaves the window and is appended to its row's cache
+    iff its score >= tau (a NaN score is dropped).  With w = 0 a token is decided on
+    arrival.  Every row (a (layer, KV head, sequence) stream) is independent.
+    score [R][T] -> (kept: per row the appended positions in append order,
+    window: per row the positions still in the window after the last step)."""
+    score = np.asarray(score, dtype=np.float64)
+    R, T = score.shape
+    kept = [[] for _ in range(R)]
+    window = [[] for _ in range(R)]
+    for t in range(T):
+        for r in range(R):
+            window[r].append(t)
+            if len(window[r]) > w:
+                leaving = window[r].pop(0)
+                if score[r, leaving] >= tau:
+                    kept[r].append(leaving)
+    return kept, window
+
+
 # ----------------------------------------------------------------------------- formulas
 
 def kv_cache_bytes(L, T, H_kv, d, bytes_per_elem):

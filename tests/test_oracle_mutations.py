@@ -59,6 +59,9 @@ MUTATIONS = [
      "vals = np.concatenate([v_ctx, 0 * v_tail], 2) if has_tail else v_ctx"),
     ("forward transposes the weights", "o[l, hq] = a @ vals[l, hq // g]",
      "o[l, hq] = (a[:, ::-1] @ vals[l, hq // g][::-1])[::-1]"),
+    ("decode strict threshold", "if score[r, leaving] >= tau:", "if score[r, leaving] > tau:"),
+    ("decode evicts the newest", "leaving = window[r].pop(0)", "leaving = window[r].pop()"),
+    ("decode window one short", "if len(window[r]) > w:", "if len(window[r]) >= w:"),
     ("gelu without 1/sqrt2", "_erf(x / math.sqrt(2.0))", "_erf(x)"),
     ("gelu tanh form", "return 0.5 * x * (1.0 + _erf(x / math.sqrt(2.0)))",
      "return 0.5 * x * (1.0 + np.tanh(math.sqrt(2 / math.pi) * (x + 0.044715 * x ** 3)))"),

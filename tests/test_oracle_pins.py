@@ -378,6 +378,35 @@ def test_attention_forward_brute_force_loops():
                 assert abs(o[0, hq, j, c] - sum(w * v[c] for w, v in zip(ws, vs)) / z) < 1e-12
 
 
+# ------------------------------------------------------------------ decode-time pruning
+
+def test_decode_prune_hand_example():
+    kept, window = O.decode_prune(np.array([[0.0, 5.0, -1.0, 3.0, 7.0]]), 2.0, 2)
+    assert kept == [[1]] and window == [[3, 4]]
+    kept, window = O.decode_prune(np.array([[0.0, 5.0, -1.0, 3.0, 7.0]]), 2.0, 0)
+    assert kept == [[1, 3, 4]] and window == [[]]
+
+
+def test_decode_prune_equals_prefill_threshold():
+    # phase-agnostic: deciding each token as it leaves the window keeps exactly what the
+    # prefill threshold rule keeps (kept tokens plus the final window)
+    for w in (0, 1, 5, 40, 100):
+        r = np.random.default_rng(w)
+        T = 60
+        s = np.round(r.normal(size=(4, T)) * 2) / 2
+        s[r.random(s.shape) < 0.05] = np.nan
+        tau = 0.5
+        kept, window = O.decode_prune(s, tau, w)
+        mask, keep = O.prune_threshold(s, tau, w)
+        for row in range(4):
+            assert kept[row] == sorted(kept[row])
+            assert window[row] == list(range(max(0, T - w), T))
+            got = np.zeros(T, dtype=np.uint8)
+            got[kept[row] + window[row]] = 1
+            assert np.array_equal(got, mask[row])
+            assert len(kept[row]) + len(window[row]) == keep[row]
+
+
 # ------------------------------------------------------------------ MLP surrogate (GELU)
 
 # standard normal CDF at 1, -1, 2 (normal-table values)
