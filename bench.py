@@ -13,6 +13,8 @@ One step = one pass of the whole path over one batch of synthetic input (all lay
       (--attn-forward: pass 1 is the attention forward, output + LSE, instead)
   c5: surrogate (+ fused threshold tau=-5, w=128) -> compaction
   c6: MLP surrogate 4096 -> 512 -> 8 (+ threshold tau=-4, w=128) -> compaction
+  c7: decode step of 64 sequences: surrogate score of the arriving tokens -> window-boundary
+      threshold + append to the paged cache (metric: tokens decided per second per layer)
 Metric: context KV tokens scored+pruned per second per layer (all heads) = T * L / step time.
 
 Timing: inputs resident in HBM; W warm-up steps; K timed steps, each bracketed by CUDA
@@ -69,7 +71,7 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="c2", choices=["c1", "c2", "c3", "c4", "c5", "c6"])
+    ap.add_argument("--workload", default="c2", choices=["c1", "c2", "c3", "c4", "c5", "c6", "c7"])
     ap.add_argument("--impl", default="kvs", choices=["kvs", "reference"])
     ap.add_argument("--attn-forward", action="store_true",
                     help="c4: pass 1 is the attention forward (output + LSE) instead of the "
@@ -84,7 +86,7 @@ def parse_args():
     return ap.parse_args()
 
 
-DEFAULT_STEPS = {"c1": 200, "c2": 200, "c3": 5, "c4": 10, "c5": 20, "c6": 10}
+DEFAULT_STEPS = {"c1": 200, "c2": 200, "c3": 5, "c4": 10, "c5": 20, "c6": 10, "c7": 200}
 
 
 def dist_env():
@@ -124,11 +126,27 @@ def algorithmic_work(wl, p):
         rows = L * wl.H_kv
         out["kvs_surrogate"] = ("hbm", L * wl.T * wl.D_h * 2 + L * wl.D_h * wl.H_kv * 2
                                 + rows * wl.T * (4 + 1), "byte")
+    if wl.kind == "decode":
+        B, H = wl.batch, wl.H_kv
+        out["kvs_surrogate"] = ("hbm", L * B * wl.D_h * 2 + L * wl.D_h * H * 2 + L * H * B * 4,
+                                "byte")
+        # per row: the arriving K/V read and written into the ring, the leaving K/V read,
+        # the appended fraction written to a page, plus the scalars
+        rows = L * H * B
+        steps = max(1, int(p.pos[0].item()) - wl.w)
+        frac = float(p.seq_lens.sum().item()) / (rows * steps)
+        out["kvs_decode_step"] = ("hbm", int(rows * (4 * wl.d * (3 + frac) + 16)), "byte")
     if wl.kind == "kvzap_mlp":
         # two linear layers per token: 2 D_h D_mid + 2 D_mid H = (D_h / 4)(D_h + H)
         out["kvs_surrogate_mlp"] = ("tensor", L * wl.T * (2 * wl.D_h * wl.D_mid
                                                           + 2 * wl.D_mid * wl.H_kv), "flop")
     return out
+
+
+def units_per_step(wl, p):
+    """Context tokens a step scores and prunes in each layer (decode: one arriving token
+    per sequence), times the layers."""
+    return (wl.batch if wl.kind == "decode" else wl.T) * p.L
 
 
 def compaction_bytes(p, wl):
@@ -298,7 +316,7 @@ def run_gpu(args, rank, world, local):
         barrier()
     ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), world, dev)
     ms_step = ms / K
-    value = whole_job_value(wl.T * p.L, world, ms_step)
+    value = whole_job_value(units_per_step(wl, p), world, ms_step)
 
     # ---------------------------------------------------------------- per entry point
     reps = args.stage_reps or max(3, min(50, K))
@@ -318,7 +336,8 @@ def run_gpu(args, rank, world, local):
         stage_ms[name] = sum(a.elapsed_time(b) for a, b in e) / reps
     step_fn()  # leave consistent outputs
     torch.cuda.synchronize()
-    work["kvs_compact_paged"] = ("hbm", compaction_bytes(p, wl), "byte")
+    if "kvs_compact_paged" in stage_ms:
+        work["kvs_compact_paged"] = ("hbm", compaction_bytes(p, wl), "byte")
     if "kvs_prune_mask" in stage_ms:
         work["kvs_prune_mask"] = ("hbm", prune_bytes(p, wl), "byte")
 
@@ -359,7 +378,7 @@ def run_gpu(args, rank, world, local):
     # ---------------------------------------------------------------- end to end
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(wl, x, p, dev, K=min(K, 20), units=world * wl.T * p.L, world=world,
+        e2e = run_e2e(wl, x, p, dev, K=min(K, 20), units=world * units_per_step(wl, p), world=world,
                       flush=flush, graph=not args.no_graph)
 
     result = {
@@ -422,9 +441,12 @@ def run_e2e(wl, x, p, dev, K, units, world, flush, graph=True):
         h.copy_(t.cpu())
         pairs.append((h, t))
     outs = [p.score]
-    pages = p.pages if isinstance(p.pages, list) else [p.pages]
-    for pg in pages:
-        outs += [pg.seq_lens, pg.block_table]
+    if hasattr(p, "pages"):
+        pages = p.pages if isinstance(p.pages, list) else [p.pages]
+        for pg in pages:
+            outs += [pg.seq_lens, pg.block_table]
+    else:  # decode: the step's decisions
+        outs += [p.seq_lens]
     outs_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
     bi = sum(h.numel() * h.element_size() for h, _ in pairs)
     bo = sum(o.numel() * o.element_size() for o in outs)
@@ -532,6 +554,20 @@ def oracle_sample(wl, x, frac=1.0):
         dt = (tick() - t0) * (wl.T / n)
         return dt, wl.T, (f"layer 0, first {n} of {wl.T} tokens (all heads): surrogate, threshold, "
                           f"compaction; scaled x(T/{n})")
+    if wl.kind == "decode":
+        steps = 2 * wl.w
+        t0 = tick()
+        # the same surrogate on every step's arriving tokens (the inputs repeat), then
+        # the window-boundary decisions of every (head, sequence) row over `steps` steps
+        z = None
+        for _ in range(steps):
+            z = O.linear_surrogate(f64(x["h"]), f64(x["W"]), x["b"].double().numpy())
+        rows = np.repeat(z.reshape(-1, 1), steps, axis=1)
+        O.decode_prune(rows, wl.tau, wl.w)
+        dt = tick() - t0
+        return dt / steps, wl.batch, (f"layer 0, {wl.batch} sequences x {wl.H_kv} KV heads, "
+                                      f"{steps} decode steps: surrogate of the arriving tokens "
+                                      f"and window-boundary decisions; per step")
     if wl.kind == "kvzap_mlp":
         n = max(1024, min(wl.T, int(round(frac * wl.T))))
         t0 = tick()
@@ -557,7 +593,8 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-CPU_BASELINE_FRAC = {"c1": 1.0, "c2": 1.0, "c3": 1 / 8, "c4": 1 / 4, "c5": 1 / 8, "c6": 1 / 16}
+CPU_BASELINE_FRAC = {"c1": 1.0, "c2": 1.0, "c3": 1 / 8, "c4": 1 / 4, "c5": 1 / 8, "c6": 1 / 16,
+                     "c7": 1.0}
 
 
 def run_cpu_baseline(wl):
@@ -596,7 +633,7 @@ def run_reference(args, rank, world):
         wall.append(time.perf_counter() - t)
         times.append(dt)
     ms = 1e3 * statistics.mean(times)
-    value = wl.T / (ms / 1e3)
+    value = tokens / (ms / 1e3)
     cb = {"value": round(value, 2), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
           "sample": desc + f"; {statistics.mean(wall):.2f} s of CPU work per step"}
     return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,

@@ -74,7 +74,9 @@ const char* kvs_last_error(void);
 uint64_t kvs_launch_count(void);
 
 /* Device-side error word shared by all kernels of the library on the current device
- * (0 = none).  Reading synchronises `stream`; `clear` != 0 resets it to 0. */
+ * (0 = none; 1 = a bounded wait of a tensor-core kernel ran out, 3 = shared-memory
+ * window misaligned, 4/5 = kvs_decode_step out of pages).  Reading synchronises
+ * `stream`; `clear` != 0 resets it to 0. */
 kvs_status kvs_device_error(int32_t* code_out, int32_t clear, void* stream);
 
 /* ---------------------------------------------------------------------------------
@@ -270,6 +272,45 @@ kvs_status kvs_surrogate_mlp(const kvs_dims* dims, const kvs_bf16* h, int32_t T,
 kvs_status kvs_prune_mask(const kvs_dims* dims, const float* score, int32_t T, int32_t mode,
                           float tau, int32_t k, int32_t w, uint8_t* mask, int32_t* keep,
                           void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * kvs_decode_step -- decode-time pruning at the window boundary [KVzap: the threshold
+ * criterion is phase-agnostic and prunes while decoding; KVpop 1. Key Terms: a token is
+ * decided when it leaves the protected window].  One call = one decode step of B
+ * sequences, for every (layer, KV head, sequence) row r = (l * H_kv + hk) * B + b:
+ *
+ *   the token arriving now (position pos[b]) enters the row's ring of the last w
+ *   tokens at slot pos[b] % w; the token it displaces (position pos[b] - w, present
+ *   once pos[b] >= w) is appended to the row's paged cache iff its score >= tau
+ *   (NaN never passes).  With w == 0 the arriving token itself is decided.
+ *
+ * Over a whole sequence this keeps exactly the tokens that the prefill threshold rule
+ * (kvs_prune_mask, KVS_THRESHOLD) keeps: the appended ones plus the final ring.
+ * Pages: a row appends in position order into its own pages; when a row needs a new
+ * page it takes next_page[0] (an atomic add on a device counter shared by all rows, so
+ * page ids depend on the order rows run in; a row's contents do not), records it in
+ * block_table[r][seq_lens[r] / page_size] and zero-fills it.  If the pool
+ * (capacity_pages) or the row's block table (max_pages) is full the token is not
+ * appended and the device error word is set (kvs_device_error: 4 = pool full,
+ * 5 = block table full).  With advance_pos != 0, pos[b] += 1 after the step.
+ *
+ *   pos          [B]                     int32 (device; read, advanced if asked)
+ *   new_score    [L][H_kv][B]            fp32  score of the arriving token
+ *   new_k, new_v [L][H_kv][B][d]         bf16
+ *   ring_score   [L][H_kv][B][w]         fp32  state (NULL when w == 0)
+ *   ring_k, ring_v [L][H_kv][B][w][d]    bf16  state (NULL when w == 0)
+ *   k_pages, v_pages [capacity_pages][page_size][d] bf16 state
+ *   next_page    [1] int32 state;  block_table [L][H_kv][B][max_pages] int32 state
+ *   seq_lens     [L][H_kv][B] int32 state (tokens appended so far)
+ * Start a stream with pos = 0, seq_lens = 0, next_page = 0 and block_table = -1.
+ * ------------------------------------------------------------------------------- */
+kvs_status kvs_decode_step(const kvs_dims* dims, int32_t B, int32_t w, int32_t* pos,
+                           const float* new_score, const kvs_bf16* new_k, const kvs_bf16* new_v,
+                           float* ring_score, kvs_bf16* ring_k, kvs_bf16* ring_v, float tau,
+                           int32_t page_size, kvs_bf16* k_pages, kvs_bf16* v_pages,
+                           int32_t capacity_pages, int32_t* next_page, int32_t* block_table,
+                           int32_t max_pages, int32_t* seq_lens, int32_t advance_pos,
+                           void* stream);
 
 /* ---------------------------------------------------------------------------------
  * kvs_compact_paged -- gather of the kept K/V rows [KVzap Algorithm 1: keys[indices],

@@ -66,6 +66,8 @@ _SIGS = {
     "kvs_vnorm_workspace_size": ([_D], _S),
     "kvs_vnorm": ([_D, _P, _I, _P, _P, _P, _S, _P], ctypes.c_int),
     "kvs_vnorm_noalloc": ([_D, _P, _I, _P, _P, _P], ctypes.c_int),
+    "kvs_decode_step": ([_D, _I, _I, _P, _P, _P, _P, _P, _P, _P, _F, _I, _P, _P, _I, _P, _P, _I,
+                         _P, _I, _P], ctypes.c_int),
     "kvs_attn_fwd": ([_D, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _P], ctypes.c_int),
     "kvs_surrogate": ([_D, _P, _I, _P, _P, _P, _F, _I, _P, _P, _P], ctypes.c_int),
     "kvs_surrogate_mlp": ([_D, _P, _I, _I, _P, _P, _P, _P, _P, _F, _I, _P, _P, _P], ctypes.c_int),
@@ -168,6 +170,16 @@ def kvs_vnorm_noalloc(dm, v, T, w_o, vnorm, stream=None):
 def kvs_attn_fwd(dm, q, n_q, k_ctx, v_ctx, T, k_tail, v_tail, n_tail, o, lse, stream=None):
     _check(_lib.kvs_attn_fwd(_d(dm), _ptr(q), n_q, _ptr(k_ctx), _ptr(v_ctx), T, _ptr(k_tail),
                              _ptr(v_tail), n_tail, _ptr(o), _ptr(lse), _stream(stream)))
+
+
+def kvs_decode_step(dm, B, w, pos, new_score, new_k, new_v, ring_score, ring_k, ring_v, tau,
+                    page_size, k_pages, v_pages, capacity_pages, next_page, block_table,
+                    max_pages, seq_lens, advance_pos=True, stream=None):
+    _check(_lib.kvs_decode_step(_d(dm), B, w, _ptr(pos), _ptr(new_score), _ptr(new_k),
+                                _ptr(new_v), _ptr(ring_score), _ptr(ring_k), _ptr(ring_v),
+                                float(tau), page_size, _ptr(k_pages), _ptr(v_pages),
+                                capacity_pages, _ptr(next_page), _ptr(block_table), max_pages,
+                                _ptr(seq_lens), 1 if advance_pos else 0, _stream(stream)))
 
 
 def kvs_surrogate(dm, h, T, W, b, score, tau=0.0, w=0, mask=None, keep=None, stream=None):

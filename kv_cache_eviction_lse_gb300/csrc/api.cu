@@ -9,6 +9,7 @@
 #include "../../include/kvs.h"
 #include "attn.cuh"
 #include "compact.cuh"
+#include "decode.cuh"
 #include "mlp.cuh"
 #include "prune.cuh"
 #include "surrogate.cuh"
@@ -92,12 +93,15 @@ uint64_t kvs_launch_count(void) { return kvs::g_launches.load(std::memory_order_
 
 kvs_status kvs_device_error(int32_t* code_out, int32_t clear, void* stream) {
   REQUIRE(code_out, KVS_ERR_ARG, "kvs_device_error: code_out is NULL");
-  int code = 0, code_mlp = 0, code_fwd = 0;
-  cudaError_t e = kvs::attn_device_error(&code, clear != 0, as_stream(stream));
-  if (e == cudaSuccess) e = kvs::mlp_device_error(&code_mlp, clear != 0, as_stream(stream));
-  if (e == cudaSuccess) e = kvs::fwd_device_error(&code_fwd, clear != 0, as_stream(stream));
+  int codes[4] = {0, 0, 0, 0};
+  cudaError_t e = kvs::attn_device_error(&codes[0], clear != 0, as_stream(stream));
+  if (e == cudaSuccess) e = kvs::mlp_device_error(&codes[1], clear != 0, as_stream(stream));
+  if (e == cudaSuccess) e = kvs::fwd_device_error(&codes[2], clear != 0, as_stream(stream));
+  if (e == cudaSuccess) e = kvs::decode_device_error(&codes[3], clear != 0, as_stream(stream));
   if (e != cudaSuccess) return cuda_status(e, "kvs_device_error");
-  *code_out = code ? code : (code_mlp ? code_mlp : code_fwd);
+  *code_out = 0;
+  for (int c : codes)
+    if (c && !*code_out) *code_out = c;
   return ok();
 }
 
@@ -330,6 +334,52 @@ kvs_status kvs_surrogate_mlp(const kvs_dims* dims, const kvs_bf16* h, int32_t T,
     e = kvs::launch_prune(score, dims->L * H, T, KVS_THRESHOLD, tau, 0, w, mask, keep,
                           as_stream(stream));
   return cuda_status(e, "kvs_surrogate_mlp");
+}
+
+kvs_status kvs_decode_step(const kvs_dims* dims, int32_t B, int32_t w, int32_t* pos,
+                           const float* new_score, const kvs_bf16* new_k, const kvs_bf16* new_v,
+                           float* ring_score, kvs_bf16* ring_k, kvs_bf16* ring_v, float tau,
+                           int32_t page_size, kvs_bf16* k_pages, kvs_bf16* v_pages,
+                           int32_t capacity_pages, int32_t* next_page, int32_t* block_table,
+                           int32_t max_pages, int32_t* seq_lens, int32_t advance_pos,
+                           void* stream) {
+  kvs_status st = check_dims(dims, __func__, false);
+  if (st) return st;
+  REQUIRE(dims->d == 64 || dims->d == 128, KVS_ERR_UNSUPPORTED,
+          "kvs_decode_step: head dim d = %d (supported: 64, 128)", dims->d);
+  REQUIRE(B >= 0 && w >= 0 && capacity_pages >= 0, KVS_ERR_ARG, "kvs_decode_step: negative size");
+  REQUIRE(page_size >= 1 && page_size <= 4096, KVS_ERR_UNSUPPORTED,
+          "kvs_decode_step: page_size = %d (1..4096)", page_size);
+  REQUIRE(max_pages >= 1, KVS_ERR_SHAPE, "kvs_decode_step: max_pages = %d must be >= 1", max_pages);
+  REQUIRE((int64_t)dims->L * dims->H_kv * B < INT32_MAX / 32, KVS_ERR_UNSUPPORTED,
+          "kvs_decode_step: too many rows");
+  if (B == 0) return ok();
+  REQUIRE_PTR(pos);
+  REQUIRE_PTR(new_score);
+  REQUIRE_PTR(new_k);
+  REQUIRE_PTR(new_v);
+  if (w > 0) {
+    REQUIRE_PTR(ring_score);
+    REQUIRE_PTR(ring_k);
+    REQUIRE_PTR(ring_v);
+  }
+  REQUIRE_PTR(next_page);
+  REQUIRE_PTR(block_table);
+  REQUIRE_PTR(seq_lens);
+  if (capacity_pages > 0) {
+    REQUIRE_PTR(k_pages);
+    REQUIRE_PTR(v_pages);
+  }
+  kvs::DecodeArgs a;
+  a.rows = dims->L * dims->H_kv * B;
+  a.B = B; a.w = w; a.d = dims->d; a.page_size = page_size; a.max_pages = max_pages;
+  a.capacity = capacity_pages; a.tau = tau;
+  a.pos = pos; a.new_score = new_score; a.new_k = new_k; a.new_v = new_v;
+  a.ring_score = ring_score; a.ring_k = ring_k; a.ring_v = ring_v;
+  a.k_pages = k_pages; a.v_pages = v_pages; a.next_page = next_page;
+  a.block_table = block_table; a.seq_lens = seq_lens;
+  return cuda_status(kvs::launch_decode_step(a, advance_pos != 0, as_stream(stream)),
+                     "kvs_decode_step");
 }
 
 kvs_status kvs_prune_mask(const kvs_dims* dims, const float* score, int32_t T, int32_t mode,

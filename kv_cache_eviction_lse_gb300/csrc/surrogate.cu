@@ -28,6 +28,8 @@ struct SurArgs {
   int* keep;
   int T, Dh, Hkv, w, tiles_per_warp;
   float tau;
+  int ksplit;  // 1: each warp owns whole token tiles; kWarps: the warps of a block split
+               // the channels of one tile (few tokens, e.g. one per sequence in decode)
 };
 
 // Channel permutation: in superblock sb (128 channels), lane (g, t) (lane = 4*g + t) loads
@@ -42,6 +44,30 @@ __global__ void __launch_bounds__(kWarps * 32) surrogate_kernel(const SurArgs a)
   const int l = blockIdx.y;
   const int nsb = a.Dh / 128;
   const bf16_t* Wl = a.W + (size_t)l * a.Dh * a.Hkv;
+  if (NT == 1 && a.Hkv == 8) {
+    // 8 heads: a channel's weights are one 16-byte row.  Each thread reads the 8 rows of
+    // one group of 8 channels (128 contiguous bytes) and writes its 8 x 8 transpose:
+    // one 16-byte entry (8 channels of one head) per head
+    for (int grp = threadIdx.x; grp < nsb * 16; grp += blockDim.x) {
+      const int sb = grp >> 4, p = (grp >> 2) & 3, t = grp & 3;
+      const uint4* src = reinterpret_cast<const uint4*>(Wl + (size_t)(sb * 128 + 32 * p + 8 * t) * 8);
+      uint32_t r[8][4];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint4 u = __ldg(src + e);
+        r[e][0] = u.x; r[e][1] = u.y; r[e][2] = u.z; r[e][3] = u.w;
+      }
+#pragma unroll
+      for (int gg = 0; gg < 8; ++gg) {
+        const int sh = (gg & 1) * 16;
+        uint32_t wv[4];
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2)
+          wv[e2] = ((r[2 * e2][gg >> 1] >> sh) & 0xffffu) | (((r[2 * e2 + 1][gg >> 1] >> sh) & 0xffffu) << 16);
+        wsm[(sb * 4 + p) * 32 + 4 * gg + t] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      }
+    }
+  } else
   for (int idx = threadIdx.x; idx < nsb * NT * 128; idx += blockDim.x) {
     const int ln = idx & 31, p = (idx >> 5) & 3, nt = (idx >> 7) % NT, sb = (idx >> 7) / NT;
     const int head = nt * 8 + (ln >> 2);
@@ -67,17 +93,15 @@ __global__ void __launch_bounds__(kWarps * 32) surrogate_kernel(const SurArgs a)
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) cnt[nt][0] = cnt[nt][1] = 0;
 
-  int tile = (blockIdx.x * kWarps + warp) * a.tiles_per_warp;
-  for (int k = 0; k < a.tiles_per_warp && tile < ntile; ++k, ++tile) {
-    const int t0 = tile * 16;
+  // partial sums of the channel superblocks [sb0, sb1) of token tile t0
+  auto contract = [&](int t0, int sb0, int sb1, float (*acc)[4]) {
     const int ra = min(t0 + g, a.T - 1), rb = min(t0 + g + 8, a.T - 1);
     const bf16_t* pa = a.h + ((size_t)l * a.T + ra) * a.Dh + 8 * t4;
     const bf16_t* pb = a.h + ((size_t)l * a.T + rb) * a.Dh + 8 * t4;
-    float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 #pragma unroll 2
-    for (int sb = 0; sb < nsb; ++sb) {
+    for (int sb = sb0; sb < sb1; ++sb) {
       uint4 xa[4], xb[4];
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
@@ -96,6 +120,9 @@ __global__ void __launch_bounds__(kWarps * 32) surrogate_kernel(const SurArgs a)
         }
       }
     }
+  };
+  // bias, score store and the fused threshold of one finished tile
+  auto finish = [&](int t0, float (*acc)[4]) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -113,6 +140,38 @@ __global__ void __launch_bounds__(kWarps * 32) surrogate_kernel(const SurArgs a)
           }
         }
       }
+    }
+  };
+
+  if (a.ksplit > 1) {
+    // one tile per block; warp w contracts the w-th slice of the channel superblocks and
+    // warp 0 adds the slices up (fixed order: deterministic)
+    float* red = reinterpret_cast<float*>(wsm + (size_t)nsb * NT * 128);
+    const int t0 = blockIdx.x * 16;
+    float acc[NT][4];
+    contract(t0, warp * nsb / kWarps, (warp + 1) * nsb / kWarps, acc);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) red[((warp * NT + nt) * 4 + e) * 32 + lane] = acc[nt][e];
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float sum = 0.f;
+          for (int w8 = 0; w8 < kWarps; ++w8) sum += red[((w8 * NT + nt) * 4 + e) * 32 + lane];
+          acc[nt][e] = sum;
+        }
+      finish(t0, acc);
+    }
+  } else {
+    int tile = (blockIdx.x * kWarps + warp) * a.tiles_per_warp;
+    for (int k = 0; k < a.tiles_per_warp && tile < ntile; ++k, ++tile) {
+      float acc[NT][4];
+      contract(tile * 16, 0, nsb, acc);
+      finish(tile * 16, acc);
     }
   }
   if (a.mask) {
@@ -143,14 +202,19 @@ cudaError_t launch_surrogate(const bf16_t* h, int L, int T, int Dh, int Hkv, con
     cudaError_t e = cudaMemsetAsync(keep, 0, sizeof(int) * (size_t)L * Hkv, s);
     if (e != cudaSuccess) return e;
   }
-  SurArgs a{h, W, b, z, mask, keep, T, Dh, Hkv, w, 8, tau};
+  SurArgs a{h, W, b, z, mask, keep, T, Dh, Hkv, w, 8, tau, 1};
   const int ntile = (T + 15) / 16;
+  // few token tiles (decode: one token per sequence): split each tile's channels over
+  // the warps of a block instead of leaving most of the GPU idle
+  if ((long)L * ntile < 304) a.ksplit = kWarps;
   // fewer tiles per warp when the grid would not fill the GPU twice over
   while (a.tiles_per_warp > 1 &&
          (long)L * ((ntile + kWarps * a.tiles_per_warp - 1) / (kWarps * a.tiles_per_warp)) < 304)
     a.tiles_per_warp >>= 1;
-  dim3 grid((ntile + kWarps * a.tiles_per_warp - 1) / (kWarps * a.tiles_per_warp), L);
-  const size_t smem = surrogate_smem_bytes(Dh, Hkv);
+  dim3 grid(a.ksplit > 1 ? ntile : (ntile + kWarps * a.tiles_per_warp - 1) /
+                                        (kWarps * a.tiles_per_warp), L);
+  size_t smem = surrogate_smem_bytes(Dh, Hkv);
+  if (a.ksplit > 1) smem += (size_t)kWarps * ((Hkv + 7) / 8) * 4 * 32 * sizeof(float);
   count_launches(1);
   if (Hkv <= 8) {
     cudaFuncSetAttribute(surrogate_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -303,6 +303,59 @@ class KVzapMLPPipeline(KVzapPipeline):
         return [("kvs_surrogate_mlp", self.score_step), ("kvs_compact_paged", self.prune_step)]
 
 
+class DecodePipeline:
+    """c7: one decode step of `batch` sequences per call: the KVzap-Linear score of the
+    arriving token (the surrogate over the batch's hidden states), then the window-
+    boundary decision and append (kvs_decode_step).  State (ring, pages, positions)
+    lives on the device and advances with every step; `reset` starts over."""
+
+    def __init__(self, wl: Workload, x: dict, max_steps=4096):
+        self.wl, self.x = wl, x
+        dev = x["h"].device
+        L, H, B, d, w = x["h"].shape[0], wl.H_kv, wl.batch, wl.d, wl.w
+        self.L, self.B = L, B
+        self.dm = C.dims(L, wl.H_q, H, d, wl.D_h)
+        self.rows = L * H * B
+        self.max_pages = -(-max_steps // wl.page_size) + 1
+        self.capacity = self.rows * self.max_pages
+        self.score = _empty((L, H, B), torch.float32, dev)
+        self.pos = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.ring_score = _empty((L, H, B, w), torch.float32, dev)
+        self.ring_k = _empty((L, H, B, w, d), torch.bfloat16, dev)
+        self.ring_v = _empty((L, H, B, w, d), torch.bfloat16, dev)
+        self.k_pages = _empty((self.capacity, wl.page_size, d), torch.bfloat16, dev)
+        self.v_pages = _empty((self.capacity, wl.page_size, d), torch.bfloat16, dev)
+        self.next_page = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.block_table = torch.full((L, H, B, self.max_pages), -1, dtype=torch.int32, device=dev)
+        self.seq_lens = torch.zeros((L, H, B), dtype=torch.int32, device=dev)
+        self.reset()
+
+    def reset(self):
+        self.pos.zero_()
+        self.next_page.zero_()
+        self.seq_lens.zero_()
+        self.block_table.fill_(-1)
+        self.ring_score.fill_(float("nan"))
+
+    def _score(self):
+        wl, x = self.wl, self.x
+        C.kvs_surrogate(self.dm, x["h"], self.B, x["W"], x["b"], self.score)
+
+    def _decide(self):
+        wl, x = self.wl, self.x
+        C.kvs_decode_step(self.dm, self.B, wl.w, self.pos, self.score, x["k"], x["v"],
+                          self.ring_score, self.ring_k, self.ring_v, wl.tau, wl.page_size,
+                          self.k_pages, self.v_pages, self.capacity, self.next_page,
+                          self.block_table, self.max_pages, self.seq_lens)
+
+    def stages(self):
+        return [("kvs_surrogate", self._score), ("kvs_decode_step", self._decide)]
+
+    def step(self):
+        self._score()
+        self._decide()
+
+
 def make_pipeline(wl: Workload, x: dict, **kw):
     if wl.kind in ("kvzip", "kvzip_plus"):
         return KVzipPipeline(wl, x, **kw)
@@ -314,4 +367,6 @@ def make_pipeline(wl: Workload, x: dict, **kw):
         return KVzapPipeline(wl, x, **kw)
     if wl.kind == "kvzap_mlp":
         return KVzapMLPPipeline(wl, x, **kw)
+    if wl.kind == "decode":
+        return DecodePipeline(wl, x, **kw)
     raise ValueError(wl.kind)

@@ -12,6 +12,8 @@ Five workloads are defined, shaped like the models the pages evaluate:
   c4  Qwen3-4B-shaped future-attention target (36 layers, 8 / 32 heads, T=16384)
   c5  Llama-3-8B-shaped KVzap linear-surrogate pruning (32 layers, 8 KV heads, T=131072)
   c6  Qwen3-8B-shaped KVzap MLP-surrogate pruning (36 layers, 8 KV heads, 4096 -> 512 -> 8)
+  c7  Llama-3-8B-shaped decode-time pruning: 64 sequences, one token per step, KVzap-Linear
+      score of the arriving token, window w=128 ring, threshold at the window boundary
 
 Every layer is drawn from its own generator seeded with
 ``20261202 + 1000 * workload_index + layer``, so any subset of layers can be
@@ -56,7 +58,8 @@ class Workload:
     d: int
     D_h: int
     T: int                    # context keys scored per (layer, KV head)
-    kind: str                 # kvzip | kvzip_plus | kvzip_plus_chunked | future | kvzap | kvzap_mlp
+    kind: str                 # kvzip | kvzip_plus | kvzip_plus_chunked | future | kvzap | kvzap_mlp | decode
+    batch: int = 0            # decode: sequences advanced together, one token each per step
     prefix: int = 0           # repeat-prompt tokens between context and repeated block
     n_rep: int = 0            # scoring queries per call (repeated block, or one chunk)
     n_chunks: int = 1
@@ -139,6 +142,13 @@ WORKLOADS = {
               "d=128, hidden 4096 -> 512 -> 8 (GELU), T=131072, tau=-4, w=128",
         L=36, H_kv=8, H_q=32, d=128, D_h=4096, T=131072, kind="kvzap_mlp",
         w=128, tau=-4.0),
+    "c7": Workload(
+        name="c7", index=7,
+        title="Llama-3-8B-shaped decode-time pruning, 32 layers, 8 KV heads, d=128, "
+              "hidden 4096, 64 sequences x 1 token per step, KVzap-Linear score, w=128 "
+              "ring, tau=-5 at the window boundary, pages of 16",
+        L=32, H_kv=8, H_q=32, d=128, D_h=4096, T=1, kind="decode", batch=64,
+        w=128, tau=-5.0),
 }
 
 
@@ -219,6 +229,8 @@ def generate(wl: Workload, layers=None, device="cpu") -> dict:
         return _generate_kvzap(wl, layers, device)
     if wl.kind == "kvzap_mlp":
         return _generate_kvzap_mlp(wl, layers, device)
+    if wl.kind == "decode":
+        return _generate_decode(wl, layers, device)
     raise ValueError(wl.kind)
 
 
@@ -327,6 +339,26 @@ def _generate_kvzap_mlp(wl: Workload, layers, device):
         k[i] = _bf16(_randn(gen, (Hkv, T, d), device))
         v[i] = _bf16(_randn(gen, (Hkv, T, d), device))
     return dict(h=h, W1=W1, b1=b1, W2=W2, b2=b2, k=k, v=v)
+
+
+def _generate_decode(wl: Workload, layers, device):
+    """c7: the linear surrogate of c5 and the inputs of one decode step: the arriving
+    token's hidden state per sequence and its K/V per (layer, KV head, sequence)."""
+    nL, d, Hkv, Dh, B = len(layers), wl.d, wl.H_kv, wl.D_h, wl.batch
+    bf = torch.bfloat16
+    h = torch.empty((nL, B, Dh), dtype=bf, device=device)
+    W = torch.empty((nL, Dh, Hkv), dtype=bf, device=device)
+    b = torch.empty((nL, Hkv), dtype=torch.float32, device=device)
+    k = torch.empty((nL, Hkv, B, d), dtype=bf, device=device)
+    v = torch.empty_like(k)
+    for i, l in enumerate(layers):
+        gen = _gen(wl, l, device)
+        W[i] = _bf16(_randn(gen, (Dh, Hkv), device, std=1.0 / 64.0))
+        b[i] = _randn(gen, (Hkv,), device, mean=-4.0)
+        h[i] = _bf16(_randn(gen, (B, Dh), device))
+        k[i] = _bf16(_randn(gen, (Hkv, B, d), device))
+        v[i] = _bf16(_randn(gen, (Hkv, B, d), device))
+    return dict(h=h, W=W, b=b, k=k, v=v)
 
 
 def random_kv_inputs(L, H_kv, H_q, d, T, n_tail, n_q, seed, device="cpu", scale=1.0,

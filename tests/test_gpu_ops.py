@@ -198,7 +198,7 @@ def test_future_sum(C, d, T, w):
 
 
 @pytest.mark.parametrize("Hkv", [8, 3, 12])
-@pytest.mark.parametrize("T", [1000, 16, 1])
+@pytest.mark.parametrize("T", [40000, 1000, 16, 1])  # 40000: whole tiles per warp; else split
 def test_surrogate(C, Hkv, T):
     L, Dh, w, tau = 2, 256, 7, -4.5
     gen = torch.Generator().manual_seed(Hkv * 1000 + T)
@@ -392,3 +392,91 @@ def test_compact_capacity_overflow(C):
     assert bool((pages.block_table == -1).all())
     assert pages.seq_lens.cpu().tolist() == [[100, 100]]
     assert bool((pages.k_pages == 3.0).all())
+
+
+# ----------------------------------------------------------------------------- decode
+
+def _decode_run(C, L, H, B, d, T, w, page, tau, scores, k, v, capacity, max_pages):
+    """Feed T tokens of every row one decode step at a time (graph-free)."""
+    rows = L * H * B
+    dev = "cuda"
+    pos = torch.zeros(B, dtype=torch.int32, device=dev)
+    ring_s = torch.full((L, H, B, max(w, 1)), float("nan"), device=dev)
+    ring_k = torch.zeros(L, H, B, max(w, 1), d, dtype=torch.bfloat16, device=dev)
+    ring_v = torch.zeros_like(ring_k)
+    kp = torch.full((capacity, page, d), 7, dtype=torch.bfloat16, device=dev)
+    vp = torch.full_like(kp, 7)
+    nxt = torch.zeros(1, dtype=torch.int32, device=dev)
+    bt = torch.full((L, H, B, max_pages), -1, dtype=torch.int32, device=dev)
+    sl = torch.zeros(L, H, B, dtype=torch.int32, device=dev)
+    sc, kc, vc = scores.cuda(), k.cuda(), v.cuda()
+    dm = C.dims(L, H, H, d)
+    for t in range(T):
+        C.kvs_decode_step(dm, B, w, pos, sc[..., t].contiguous(), kc[..., t, :].contiguous(),
+                          vc[..., t, :].contiguous(), ring_s if w else None,
+                          ring_k if w else None, ring_v if w else None, tau, page, kp, vp,
+                          capacity, nxt, bt, max_pages, sl)
+    torch.cuda.synchronize()
+    return dict(pos=pos, ring_s=ring_s, ring_k=ring_k, kp=kp, vp=vp, nxt=nxt, bt=bt, sl=sl)
+
+
+@pytest.mark.parametrize("w,page,d", [(16, 16, 128), (0, 16, 128), (5, 1, 64), (40, 16, 64)])
+def test_decode_step_matches_oracle(C, w, page, d):
+    L, H, B, T, tau = 2, 3, 4, 150, 0.25
+    gen = torch.Generator().manual_seed(w * 100 + page + d)
+    scores = torch.round(torch.randn(L, H, B, T, generator=gen) * 2) / 2
+    scores[torch.rand(L, H, B, T, generator=gen) < 0.03] = float("nan")
+    k = torch.randn(L, H, B, T, d, generator=gen).to(torch.bfloat16)
+    v = torch.randn(L, H, B, T, d, generator=gen).to(torch.bfloat16)
+    max_pages = -(-T // page)
+    capacity = L * H * B * max_pages
+    st = _decode_run(C, L, H, B, d, T, w, page, tau, scores, k, v, capacity, max_pages)
+    assert (st["pos"].cpu() == T).all()
+    kept, window = O.decode_prune(scores.reshape(-1, T).double().numpy(), tau, w)
+    sl = st["sl"].cpu().reshape(-1).numpy()
+    bt = st["bt"].cpu().reshape(-1, max_pages).numpy()
+    kp, vp = st["kp"].cpu(), st["vp"].cpu()
+    kr, vr = k.reshape(-1, T, d), v.reshape(-1, T, d)
+    used = []
+    for r in range(L * H * B):
+        n = len(kept[r])
+        assert sl[r] == n
+        npg = -(-n // page)
+        ids = bt[r]
+        assert (ids[:npg] >= 0).all() and (ids[npg:] == -1).all()
+        used += list(ids[:npg])
+        got_k = kp[ids[:npg]].reshape(-1, d)
+        got_v = vp[ids[:npg]].reshape(-1, d)
+        assert torch.equal(got_k[:n].view(torch.int16), kr[r, kept[r]].view(torch.int16))
+        assert torch.equal(got_v[:n].view(torch.int16), vr[r, kept[r]].view(torch.int16))
+        assert (got_k[n:].float() == 0).all() and (got_v[n:].float() == 0).all()
+        if w:
+            rk = st["ring_k"].cpu().reshape(-1, w, d)[r]
+            for t in window[r]:
+                assert torch.equal(rk[t % w].view(torch.int16), kr[r, t].view(torch.int16))
+    assert sorted(used) == list(range(int(st["nxt"].item())))  # each page handed out once
+    code = C.kvs_device_error(clear=True)
+    assert code == 0
+
+
+def test_decode_step_pool_exhaustion_is_reported(C):
+    L, H, B, d, T, w, page, tau = 1, 2, 2, 128, 40, 4, 4, -100.0   # keeps everything
+    gen = torch.Generator().manual_seed(9)
+    scores = torch.zeros(L, H, B, T)
+    k = torch.randn(L, H, B, T, d, generator=gen).to(torch.bfloat16)
+    v = torch.randn(L, H, B, T, d, generator=gen).to(torch.bfloat16)
+    capacity = 5   # far fewer pages than the 4 rows need
+    st = _decode_run(C, L, H, B, d, T, w, page, tau, scores, k, v, capacity, max_pages=16)
+    assert int(st["nxt"].item()) >= capacity
+    sl = st["sl"].cpu().reshape(-1)
+    assert int(sl.sum()) <= capacity * page
+    assert C.kvs_device_error(clear=True) == 4
+    # what was appended is still right: each row's first tokens in order
+    bt = st["bt"].cpu().reshape(-1, 16).numpy()
+    kr = k.reshape(-1, T, d)
+    for r in range(L * H * B):
+        n = int(sl[r])
+        ids = bt[r][: -(-n // page)]
+        assert (ids < capacity).all()
+        got = st["kp"].cpu()[ids].reshape(-1, d)[:n]
+        assert torch.equal(got.view(torch.int16), kr[r, :n].view(torch.int16))

@@ -225,3 +225,45 @@ def test_c4_attention_forward_sampled_rows(mods):
         vmax = np.abs(v).max()
         tol = 2.0 ** -8 * (np.abs(o_ref) + vmax)
         assert (err <= tol).all(), f"c4 forward o rows {lo}: max err {err.max()}"
+
+
+def test_c7_decode_steps_full_size(mods):
+    """c7 at full size (32 layers x 8 KV heads x 64 sequences): the surrogate score of
+    the arriving tokens against the oracle, then 2w + 37 decode steps.  The synthetic
+    step repeats the same arriving token, so a row keeps every token that leaves its
+    window (steps - w of them) iff its score passes tau; pages hold copies of that
+    token's K and V."""
+    pipeline, W = mods
+    wl = W.WORKLOADS["c7"]
+    x = W.generate(wl, device="cuda")
+    p = pipeline.make_pipeline(wl, x, max_steps=512)
+    steps = 2 * wl.w + 37
+    for _ in range(steps):
+        p.step()
+    torch.cuda.synchronize()
+    z = O.linear_surrogate(f64(x["h"]), f64(x["W"]), x["b"].double().cpu().numpy())
+    zg = p.score.cpu().numpy()
+    assert_close_abs(zg, z, LOG_SCORE_ATOL, "c7 surrogate of the arriving tokens")
+    assert (p.pos.cpu() == steps).all()
+    keep_row = (zg.astype(np.float64) >= np.float32(wl.tau))
+    sl = p.seq_lens.cpu().numpy()
+    assert np.array_equal(sl, np.where(keep_row, steps - wl.w, 0))
+    kept, window = O.decode_prune(np.repeat(zg.reshape(-1, 1).astype(np.float64), steps, 1),
+                                  np.float32(wl.tau), wl.w)
+    assert [len(k) for k in kept] == list(sl.reshape(-1))
+    bt = p.block_table.cpu().numpy()
+    kpages = p.k_pages
+    for l in (0, wl.L - 1):
+        for h in range(wl.H_kv):
+            for b in (0, wl.batch - 1):
+                n = int(sl[l, h, b])
+                ids = bt[l, h, b, : -(-n // wl.page_size)]
+                got = kpages[torch.as_tensor(ids, device="cuda").long()].reshape(-1, wl.d)[:n]
+                want = x["k"][l, h, b][None].expand(n, wl.d)
+                assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    assert C_error_clear() == 0
+
+
+def C_error_clear():
+    from kv_cache_eviction_lse_gb300 import capi
+    return capi.kvs_device_error(clear=True)
