@@ -363,6 +363,47 @@ def compact_paged(k, v, mask, page_size=16, max_pages=None):
     return k_pages, v_pages, block_table, seq_lens, total
 
 
+def value_refit(q, k_ctx, v_ctx, mask, lam):
+    """Closed-form value refit on the kept keys [KVSculpt summary, 2. Method: with the
+    keys fixed, the attention weights they induce are fixed and the values follow in
+    closed form by least squares with ridge regularisation; Select+Fit is attention-score
+    selection plus this value fit].
+
+    Readings: the training queries are the scoring queries q of the KV head's g query
+    heads, stacked (n = g n_q rows); each sees every context key (the repeat block
+    follows the whole context).  The target is the attention output over the full
+    context, O = softmax(q K^T / sqrt d) V; the kept keys K_S (mask != 0, in position
+    order) induce A_S = softmax(q K_S^T / sqrt d) over the kept keys alone; the ridge
+    penalty is lam ||V'||^2:
+        V' = argmin ||A_S V' - O||_F^2 + lam ||V'||_F^2 = (A_S^T A_S + lam I)^-1 A_S^T O.
+    q [L][H_q][n_q][d], k_ctx, v_ctx [L][H_kv][T][d], mask [L][H_kv][T], lam > 0.
+    Returns per (l, hk) the refitted values [k][d] (a list of lists) and the pieces
+    (A_S, O) of the least-squares problem for checking."""
+    L, H_q, n_q, d = q.shape
+    H_kv, T = k_ctx.shape[1], k_ctx.shape[2]
+    g = _group(H_q, H_kv)
+    out, parts = [], []
+    for l in range(L):
+        row_v, row_p = [], []
+        for hk in range(H_kv):
+            Q = q[l, hk * g:(hk + 1) * g].reshape(g * n_q, d)
+            K, V = k_ctx[l, hk], v_ctx[l, hk]
+            idx = np.nonzero(mask[l, hk])[0]
+            x = attention_logits(Q, K)
+            a_full = np.exp(x - x.max(axis=1, keepdims=True))
+            a_full /= a_full.sum(axis=1, keepdims=True)
+            O_t = a_full @ V
+            xs = x[:, idx]
+            a_s = np.exp(xs - xs.max(axis=1, keepdims=True))
+            a_s /= a_s.sum(axis=1, keepdims=True)
+            M = a_s.T @ a_s + lam * np.eye(len(idx))
+            row_v.append(np.linalg.solve(M, a_s.T @ O_t))
+            row_p.append((a_s, O_t))
+        out.append(row_v)
+        parts.append(row_p)
+    return out, parts
+
+
 def decode_prune(score, tau, w):
     """Decode-time pruning at the window boundary [KVzap: the criterion is
     phase-agnostic and works while decoding; KVpop 1. Key Terms: a token's fate is

@@ -59,6 +59,13 @@ MUTATIONS = [
      "vals = np.concatenate([v_ctx, 0 * v_tail], 2) if has_tail else v_ctx"),
     ("forward transposes the weights", "o[l, hq] = a @ vals[l, hq // g]",
      "o[l, hq] = (a[:, ::-1] @ vals[l, hq // g][::-1])[::-1]"),
+    ("refit uses kv-head rows only", "Q = q[l, hk * g:(hk + 1) * g].reshape(g * n_q, d)",
+     "Q = np.concatenate([q[l, hk * g]] * g).reshape(g * n_q, d)"),
+    ("refit normalises over all keys", "a_s /= a_s.sum(axis=1, keepdims=True)",
+     "a_s /= np.exp(x - xs.max(axis=1, keepdims=True)).sum(axis=1, keepdims=True)"),
+    ("refit drops the ridge", "M = a_s.T @ a_s + lam * np.eye(len(idx))", "M = a_s.T @ a_s + 1e-14 * np.eye(len(idx))"),
+    ("refit solves a scaled system", "row_v.append(np.linalg.solve(M, a_s.T @ O_t))",
+     "row_v.append(np.linalg.solve(M.T * 1.01, a_s.T @ O_t))"),
     ("decode strict threshold", "if score[r, leaving] >= tau:", "if score[r, leaving] > tau:"),
     ("decode evicts the newest", "leaving = window[r].pop(0)", "leaving = window[r].pop()"),
     ("decode window one short", "if len(window[r]) > w:", "if len(window[r]) >= w:"),

@@ -378,6 +378,68 @@ def test_attention_forward_brute_force_loops():
                 assert abs(o[0, hq, j, c] - sum(w * v[c] for w, v in zip(ws, vs)) / z) < 1e-12
 
 
+# ------------------------------------------------------------------ value refit
+
+def _refit_case(seed, T=12, n_q=7, g=2, d=4, keep=5):
+    r = np.random.default_rng(seed)
+    q = r.normal(size=(1, g, n_q, d)); k = r.normal(size=(1, 1, T, d)); v = r.normal(size=(1, 1, T, d))
+    mask = np.zeros((1, 1, T), dtype=np.uint8)
+    mask[0, 0, r.choice(T, keep, replace=False)] = 1
+    return q, k, v, mask
+
+
+def test_value_refit_keeping_everything_at_small_lambda_recovers_values():
+    # with every key kept, A_S is the full softmax and V itself fits exactly; as lam -> 0
+    # the ridge solution tends to V wherever A_S has full column rank (n >= T rows)
+    q, k, v, _ = _refit_case(1, T=6, n_q=8, g=2)
+    mask = np.ones((1, 1, 6), dtype=np.uint8)
+    vv, _ = O.value_refit(q * 3, k, v, mask, 1e-12)
+    assert np.allclose(vv[0][0], v[0, 0], rtol=0, atol=1e-4)
+
+
+def test_value_refit_normal_equations_and_optimality():
+    # the refit satisfies A^T (A V' - O) + lam V' = 0, and any perturbation raises the
+    # ridge objective (it is strictly convex)
+    q, k, v, mask = _refit_case(2)
+    lam = 0.05
+    vv, parts = O.value_refit(q, k, v, mask, lam)
+    A, Ot = parts[0][0]
+    Vp = vv[0][0]
+    grad = A.T @ (A @ Vp - Ot) + lam * Vp
+    assert np.abs(grad).max() < 1e-12
+    f = lambda X: ((A @ X - Ot) ** 2).sum() + lam * (X ** 2).sum()
+    r = np.random.default_rng(3)
+    for _ in range(5):
+        assert f(Vp + 1e-3 * r.normal(size=Vp.shape)) > f(Vp)
+
+
+def test_value_refit_single_kept_key_closed_form():
+    # one kept key: A_S is the all-ones column, so V' = sum_j O_j / (n + lam)
+    q, k, v, _ = _refit_case(4, T=9, n_q=5, g=3)
+    mask = np.zeros((1, 1, 9), dtype=np.uint8); mask[0, 0, 4] = 1
+    lam = 0.3
+    vv, _ = O.value_refit(q, k, v, mask, lam)
+    x = (q[0].reshape(15, -1) @ k[0, 0].T) / 2.0
+    a = np.exp(x - x.max(1, keepdims=True)); a /= a.sum(1, keepdims=True)
+    Ot = a @ v[0, 0]
+    assert np.allclose(vv[0][0][0], Ot.sum(0) / (15 + lam), rtol=0, atol=1e-12)
+
+
+def test_value_refit_gqa_rows_and_kept_order():
+    # the g query heads of a group are stacked as training rows; kept keys in position order
+    L, Hkv, g, n_q, d, T = 1, 2, 2, 3, 4, 7
+    r = np.random.default_rng(5)
+    q = r.normal(size=(L, Hkv * g, n_q, d)); k = r.normal(size=(L, Hkv, T, d)); v = r.normal(size=(L, Hkv, T, d))
+    mask = np.zeros((L, Hkv, T), dtype=np.uint8); mask[0, 0, [1, 4, 6]] = 1; mask[0, 1, [0, 2]] = 1
+    vv, parts = O.value_refit(q, k, v, mask, 0.1)
+    assert vv[0][0].shape == (3, d) and vv[0][1].shape == (2, d)
+    A, Ot = parts[0][1]
+    assert A.shape == (g * n_q, 2)
+    x = (q[0, 2] @ k[0, 1, [0, 2]].T) / 2.0          # head 2 is the first of group 1
+    a = np.exp(x - x.max(1, keepdims=True)); a /= a.sum(1, keepdims=True)
+    assert np.allclose(A[:n_q], a, rtol=0, atol=1e-14)
+
+
 # ------------------------------------------------------------------ decode-time pruning
 
 def test_decode_prune_hand_example():
