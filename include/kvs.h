@@ -75,7 +75,8 @@ uint64_t kvs_launch_count(void);
 
 /* Device-side error word shared by all kernels of the library on the current device
  * (0 = none; 1 = a bounded wait of a tensor-core kernel ran out, 3 = shared-memory
- * window misaligned, 4/5 = kvs_decode_step out of pages).  Reading synchronises
+ * window misaligned, 4/5 = kvs_decode_step out of pages, 6 = kvs_value_refit met a
+ * non-positive pivot).  Reading synchronises
  * `stream`; `clear` != 0 resets it to 0. */
 kvs_status kvs_device_error(int32_t* code_out, int32_t clear, void* stream);
 
@@ -272,6 +273,35 @@ kvs_status kvs_surrogate_mlp(const kvs_dims* dims, const kvs_bf16* h, int32_t T,
 kvs_status kvs_prune_mask(const kvs_dims* dims, const float* score, int32_t T, int32_t mode,
                           float tau, int32_t k, int32_t w, uint8_t* mask, int32_t* keep,
                           void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * kvs_value_refit -- closed-form value refit on the kept keys [KVSculpt summary,
+ * 2. Method: with the keys fixed, the attention weights they induce are fixed and the
+ * values follow by ridge least squares; Select+Fit = attention-score selection plus
+ * this value fit].  Per (layer, KV head), with the g query heads' n_q scoring queries
+ * stacked as n = g * n_q training rows, each seeing every context key:
+ *
+ *   O   = softmax(q K_ctx^T / sqrt d) V_ctx                  (full-context output, n x d)
+ *   A_S = softmax(q K_kept^T / sqrt d) over the k kept keys  (n x k)
+ *   v_fit = argmin ||A_S V - O||^2 + lam ||V||^2 = (A_S^T A_S + lam I)^-1 A_S^T O
+ *   lam = lambda_rel * mean of the diagonal of A_S^T A_S
+ *
+ * O comes from the attention forward (bf16), A_S is formed on the tensor cores and
+ * kept as bf16 hi + lo parts so that the Gram matrix and the right-hand side carry
+ * ~2^-16 relative error; the ridge system is solved by an fp32 Cholesky factorisation.
+ *
+ *   q      [L][H_q][n_q][d]    bf16    k_ctx, v_ctx [L][H_kv][T][d] bf16
+ *   k_kept [L][H_kv][k][d]     bf16    the kept keys in position order (for instance
+ *                                      kvs_compact_paged with page_size = k)
+ *   v_fit  [L][H_kv][k][d]     fp32    output
+ *   ws     scratch of kvs_value_refit_workspace_size() bytes
+ * Requires k <= T and k <= 2048.
+ * ------------------------------------------------------------------------------- */
+size_t kvs_value_refit_workspace_size(const kvs_dims* dims, int32_t n_q, int32_t k);
+kvs_status kvs_value_refit(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
+                           const kvs_bf16* k_ctx, const kvs_bf16* v_ctx, int32_t T,
+                           const kvs_bf16* k_kept, int32_t k, float lambda_rel, float* v_fit,
+                           void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------
  * kvs_decode_step -- decode-time pruning at the window boundary [KVzap: the threshold

@@ -66,6 +66,9 @@ _SIGS = {
     "kvs_vnorm_workspace_size": ([_D], _S),
     "kvs_vnorm": ([_D, _P, _I, _P, _P, _P, _S, _P], ctypes.c_int),
     "kvs_vnorm_noalloc": ([_D, _P, _I, _P, _P, _P], ctypes.c_int),
+    "kvs_value_refit_workspace_size": ([_D, _I, _I], ctypes.c_size_t),
+    "kvs_value_refit": ([_D, _P, _I, _P, _P, _I, _P, _I, _F, _P, _P, ctypes.c_size_t, _P],
+                        ctypes.c_int),
     "kvs_decode_step": ([_D, _I, _I, _P, _P, _P, _P, _P, _P, _P, _F, _I, _P, _P, _I, _P, _P, _I,
                          _P, _I, _P], ctypes.c_int),
     "kvs_attn_fwd": ([_D, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _P], ctypes.c_int),
@@ -170,6 +173,17 @@ def kvs_vnorm_noalloc(dm, v, T, w_o, vnorm, stream=None):
 def kvs_attn_fwd(dm, q, n_q, k_ctx, v_ctx, T, k_tail, v_tail, n_tail, o, lse, stream=None):
     _check(_lib.kvs_attn_fwd(_d(dm), _ptr(q), n_q, _ptr(k_ctx), _ptr(v_ctx), T, _ptr(k_tail),
                              _ptr(v_tail), n_tail, _ptr(o), _ptr(lse), _stream(stream)))
+
+
+def kvs_value_refit_workspace_size(dm, n_q, k):
+    return int(_lib.kvs_value_refit_workspace_size(_d(dm), n_q, k))
+
+
+def kvs_value_refit(dm, q, n_q, k_ctx, v_ctx, T, k_kept, k, lambda_rel, v_fit, ws, ws_bytes,
+                    stream=None):
+    _check(_lib.kvs_value_refit(_d(dm), _ptr(q), n_q, _ptr(k_ctx), _ptr(v_ctx), T, _ptr(k_kept),
+                                k, float(lambda_rel), _ptr(v_fit), _ptr(ws), ws_bytes,
+                                _stream(stream)))
 
 
 def kvs_decode_step(dm, B, w, pos, new_score, new_k, new_v, ring_score, ring_k, ring_v, tau,

@@ -10,6 +10,7 @@
 #include "attn.cuh"
 #include "compact.cuh"
 #include "decode.cuh"
+#include "gram.cuh"
 #include "mlp.cuh"
 #include "prune.cuh"
 #include "surrogate.cuh"
@@ -93,11 +94,13 @@ uint64_t kvs_launch_count(void) { return kvs::g_launches.load(std::memory_order_
 
 kvs_status kvs_device_error(int32_t* code_out, int32_t clear, void* stream) {
   REQUIRE(code_out, KVS_ERR_ARG, "kvs_device_error: code_out is NULL");
-  int codes[4] = {0, 0, 0, 0};
+  int codes[6] = {0, 0, 0, 0, 0, 0};
   cudaError_t e = kvs::attn_device_error(&codes[0], clear != 0, as_stream(stream));
   if (e == cudaSuccess) e = kvs::mlp_device_error(&codes[1], clear != 0, as_stream(stream));
   if (e == cudaSuccess) e = kvs::fwd_device_error(&codes[2], clear != 0, as_stream(stream));
   if (e == cudaSuccess) e = kvs::decode_device_error(&codes[3], clear != 0, as_stream(stream));
+  if (e == cudaSuccess) e = kvs::gram_device_error(&codes[4], clear != 0, as_stream(stream));
+  if (e == cudaSuccess) e = kvs::chol_device_error(&codes[5], clear != 0, as_stream(stream));
   if (e != cudaSuccess) return cuda_status(e, "kvs_device_error");
   *code_out = 0;
   for (int c : codes)
@@ -380,6 +383,99 @@ kvs_status kvs_decode_step(const kvs_dims* dims, int32_t B, int32_t w, int32_t* 
   a.block_table = block_table; a.seq_lens = seq_lens;
   return cuda_status(kvs::launch_decode_step(a, advance_pos != 0, as_stream(stream)),
                      "kvs_decode_step");
+}
+
+namespace {
+struct RefitPlan {
+  int g, rows, k_ld;
+  size_t off_o, off_lse, off_ahi, off_alo, off_g, off_r, total;
+};
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+RefitPlan refit_plan(const kvs_dims* dm, int n_q, int k) {
+  RefitPlan p{};
+  p.g = dm->H_q / dm->H_kv;
+  p.rows = p.g * n_q;
+  p.k_ld = (k + 63) / 64 * 64;
+  const size_t nq_all = (size_t)dm->L * dm->H_q * n_q, batch = (size_t)dm->L * dm->H_kv;
+  size_t o = 0;
+  p.off_o = o;   o = align256(o + nq_all * dm->d * 2);
+  p.off_lse = o; o = align256(o + nq_all * 4);
+  p.off_ahi = o; o = align256(o + nq_all * p.k_ld * 2);
+  p.off_alo = o; o = align256(o + nq_all * p.k_ld * 2);
+  p.off_g = o;   o = align256(o + batch * p.k_ld * p.k_ld * 4);
+  p.off_r = o;   o = align256(o + batch * p.k_ld * dm->d * 4);
+  p.total = o;
+  return p;
+}
+}  // namespace
+
+size_t kvs_value_refit_workspace_size(const kvs_dims* dims, int32_t n_q, int32_t k) {
+  if (!dims || dims->L <= 0 || dims->H_kv <= 0 || dims->H_q <= 0 || dims->H_q % dims->H_kv ||
+      n_q < 0 || k < 0)
+    return 0;
+  return refit_plan(dims, n_q, k).total;
+}
+
+kvs_status kvs_value_refit(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
+                           const kvs_bf16* k_ctx, const kvs_bf16* v_ctx, int32_t T,
+                           const kvs_bf16* k_kept, int32_t k, float lambda_rel, float* v_fit,
+                           void* ws, size_t ws_bytes, void* stream) {
+  kvs_status st = check_dims(dims, __func__);
+  if (st) return st;
+  REQUIRE(n_q >= 0 && T >= 0 && k >= 0, KVS_ERR_ARG, "kvs_value_refit: negative size");
+  REQUIRE(k <= T, KVS_ERR_SHAPE, "kvs_value_refit: k = %d kept keys exceed T = %d", k, T);
+  REQUIRE(lambda_rel >= 0.f, KVS_ERR_ARG, "kvs_value_refit: lambda_rel = %g < 0",
+          (double)lambda_rel);
+  REQUIRE((k + 63) / 64 * 64 <= kvs::kCholMaxM, KVS_ERR_UNSUPPORTED,
+          "kvs_value_refit: k = %d above %d", k, kvs::kCholMaxM);
+  if (n_q == 0 || k == 0) return ok();
+  const RefitPlan pl = refit_plan(dims, n_q, k);
+  REQUIRE((int64_t)pl.rows * pl.k_ld < INT32_MAX, KVS_ERR_UNSUPPORTED,
+          "kvs_value_refit: n_q * g * k too large");
+  REQUIRE_PTR(q);
+  REQUIRE_PTR(k_ctx);
+  REQUIRE_PTR(v_ctx);
+  REQUIRE_PTR(k_kept);
+  REQUIRE_PTR(v_fit);
+  REQUIRE_PTR(ws);
+  REQUIRE(ws_bytes >= pl.total, KVS_ERR_CAPACITY,
+          "kvs_value_refit: workspace of %zu bytes, %zu needed", ws_bytes, pl.total);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  auto* o_ws = reinterpret_cast<kvs::bf16_t*>(w + pl.off_o);
+  auto* lse_ws = reinterpret_cast<float*>(w + pl.off_lse);
+  auto* ahi = reinterpret_cast<kvs::bf16_t*>(w + pl.off_ahi);
+  auto* alo = reinterpret_cast<kvs::bf16_t*>(w + pl.off_alo);
+  auto* gm = reinterpret_cast<float*>(w + pl.off_g);
+  auto* rm = reinterpret_cast<float*>(w + pl.off_r);
+  cudaStream_t s = as_stream(stream);
+  const int L = dims->L, Hq = dims->H_q, Hkv = dims->H_kv, d = dims->d;
+  // 1. target: attention output of every scoring query over the whole context
+  kvs::FwdArgs f;
+  f.q = q; f.k_ctx = k_ctx; f.v_ctx = v_ctx; f.o = o_ws; f.lse = lse_ws;
+  f.L = L; f.Hq = Hq; f.Hkv = Hkv; f.d = d; f.n_q = n_q; f.T = T; f.causal = 0;
+  cudaError_t e = kvs::launch_attn_fwd(f, s);
+  // 2. softmax rows over the kept keys: their LSE, then the rows as bf16 hi + lo
+  kvs::AttnArgs r;
+  r.q = q; r.k_ctx = k_kept; r.lse = lse_ws; r.out = lse_ws;
+  r.L = L; r.Hq = Hq; r.Hkv = Hkv; r.d = d; r.n_q = n_q; r.T = k; r.causal = 0;
+  r.rows_hi = ahi; r.rows_lo = alo; r.rows_ld = pl.k_ld;
+  if (e == cudaSuccess) e = kvs::launch_lse(r, s);
+  if (e == cudaSuccess) e = kvs::launch_softmax_rows(r, s);
+  // 3. normal equations: Gram (upper block triangle) and right-hand side
+  kvs::GramArgs gg;
+  gg.x_hi = ahi; gg.x_lo = alo; gg.y_hi = ahi; gg.y_lo = alo; gg.c = gm;
+  gg.batch = L * Hkv; gg.rows = pl.rows; gg.M = gg.N = pl.k_ld;
+  gg.ldx = gg.ldy = gg.ldc = pl.k_ld; gg.upper = 1;
+  if (e == cudaSuccess) e = kvs::launch_gram(gg, s);
+  kvs::GramArgs rr = gg;
+  rr.y_hi = o_ws; rr.y_lo = nullptr; rr.c = rm; rr.N = d; rr.ldy = d; rr.ldc = d; rr.upper = 0;
+  if (e == cudaSuccess) e = kvs::launch_gram(rr, s);
+  // 4. ridge solve per (layer, KV head)
+  kvs::CholArgs c;
+  c.g = gm; c.r = rm; c.x = v_fit; c.batch = L * Hkv; c.M = pl.k_ld; c.ldg = pl.k_ld;
+  c.k = k; c.d = d; c.lam_rel = lambda_rel;
+  if (e == cudaSuccess) e = kvs::launch_chol_solve(c, s);
+  return cuda_status(e, "kvs_value_refit");
 }
 
 kvs_status kvs_prune_mask(const kvs_dims* dims, const float* score, int32_t T, int32_t mode,

@@ -20,9 +20,16 @@ struct AttnArgs {
   float* out = nullptr;
   int L = 0, Hq = 0, Hkv = 0, d = 0, n_q = 0, T = 0, n_tail = 0;
   int w = 0, accumulate = 0;
+  int causal = 1;                  // 0: every query sees every key (internal callers)
+  bf16_t* rows_hi = nullptr;       // softmax rows: [L][Hq][n_q][rows_ld] bf16 hi / lo parts
+  bf16_t* rows_lo = nullptr;
+  int rows_ld = 0;                 // padded row length (multiple of 64, >= T)
 };
 
 cudaError_t launch_lse(const AttnArgs& a, cudaStream_t s);
+// Softmax rows a_ji = exp(x_ji - lse_j) over the T context keys (lse given), written as
+// bf16 hi/lo parts into rows_hi / rows_lo (zero past T up to rows_ld); no tail keys.
+cudaError_t launch_softmax_rows(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_score_max(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_future_sum(const AttnArgs& a, cudaStream_t s);
 
@@ -39,6 +46,7 @@ struct FwdArgs {
   bf16_t* o = nullptr;             // [L][Hq][n_q][d]
   float* lse = nullptr;            // [L][Hq][n_q]
   int L = 0, Hq = 0, Hkv = 0, d = 0, n_q = 0, T = 0, n_tail = 0;
+  int causal = 1;                  // 0: every query sees every key (internal callers)
 };
 
 // Attention forward (bottom-right causal over [context | tail]) with its LSE.

@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = a.Hq / a.Hkv;
   const int hk = hq / G;
   const int n_k = a.T + a.n_tail;
-  const int off = n_k - a.n_q;
+  const int off = a.causal ? n_k - a.n_q : n_k;  // non-causal: every key is visible
   const int row0 = blockIdx.x * BM;
   // key tiles this query tile sees: context tiles, then tail tiles
   const int kv_end = off + min(row0 + BM, a.n_q);  // keys [0, kv_end) are visible to some query

@@ -26,6 +26,7 @@
 // KVzap review, 3.1 Eq. 1 and 3.2 Eq. 3.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <math_constants.h>
 
 #include "attn.cuh"
@@ -51,7 +52,10 @@ constexpr int kErrWaitTimeout = 1;   // a bounded mbarrier wait ran out
 constexpr int kErrSmemAlign = 3;     // dynamic shared memory window not 1024-byte aligned
 constexpr uint32_t kMaxSmem = 232448;  // per-block opt-in limit (227 KB)
 
-enum Mode { kLse = 0, kMax = 1, kFuture = 2, kQuad = 3 };
+enum Mode { kLse = 0, kMax = 1, kFuture = 2, kQuad = 3, kRows = 4 };
+// modes whose operand A is a tile of queries (B: key tiles)
+template <int MODE>
+__host__ __device__ constexpr bool a_is_queries() { return MODE == kLse || MODE == kRows; }
 // 128-row units of operand A per CTA, each with its own A buffer (loaded up front), so the
 // second unit's MMAs start while the epilogue drains the first.  A buffers are never
 // reused within a CTA, which keeps the kQuad epilogue's reads of A free of races.
@@ -174,6 +178,39 @@ __device__ __forceinline__ float future_cols(const uint32_t* v, const float* cc,
   return a0.x + a0.y;
 }
 
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// Softmax weights of 64 columns (keys kb .. kb+63) of one query row, written as bf16
+// hi and lo parts (p = hi + lo to ~2^-17): p = 2^(x sc2 - l2), 0 for keys >= lim.
+// Columns at or past ld (the padded row length) are not written.
+__device__ __forceinline__ void rows_cols(const uint32_t* v, int kb, int lim, float l2, float sc2,
+                                          bf16_t* hi, bf16_t* lo, int ld, bool valid) {
+  if (!valid) return;
+#pragma unroll
+  for (int c8 = 0; c8 < 8; ++c8) {
+    const int k0 = kb + 8 * c8;
+    if (k0 >= ld) break;
+    uint32_t wh[4], wl[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float p[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int c = 8 * c8 + 2 * e + u;
+        p[u] = (k0 + 2 * e + u < lim) ? fast_exp2(fmaf(__uint_as_float(v[c]), sc2, -l2)) : 0.f;
+      }
+      wh[e] = pack2_bf16(p[0], p[1]);
+      const float h0 = __uint_as_float(wh[e] << 16), h1 = __uint_as_float(wh[e] & 0xffff0000u);
+      wl[e] = pack2_bf16(p[0] - h0, p[1] - h1);
+    }
+    *reinterpret_cast<uint4*>(hi + k0) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+    *reinterpret_cast<uint4*>(lo + k0) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+  }
+}
+
 // B-tile space of the 128-row unit starting at row0.
 struct Tiles {
   int row0, ntiles, n_ctx, per_head, qt_begin;
@@ -186,7 +223,7 @@ __device__ __forceinline__ Tiles tiles_of(const AttnArgs& a, int row0, int G, in
   t.n_ctx = 0;
   t.per_head = 1;
   t.qt_begin = 0;
-  if (MODE == kLse) {
+  if (a_is_queries<MODE>()) {
     const int j_last = min(row0 + BM, a.n_q) - 1;
     const int kv_end = off + j_last + 1;  // keys [0, kv_end) are visible to some query
     t.n_ctx = (min(a.T, kv_end) + BN - 1) / BN;
@@ -235,12 +272,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int l = blockIdx.z;
   const int G = a.Hq / a.Hkv;
   const int n_k = a.T + a.n_tail;
-  const int off = n_k - a.n_q;
+  const int off = a.causal ? n_k - a.n_q : n_k;  // non-causal: every key is visible
   const float scale = rsqrtf((float)D);
   const float sc2 = scale * kLog2e;
-  const int hq_a = (MODE == kLse) ? (int)blockIdx.y : 0;
-  const int hk = (MODE == kLse) ? hq_a / G : (int)blockIdx.y;
-  const int a_rows = (MODE == kLse) ? a.n_q : a.T;
+  constexpr bool kQ = a_is_queries<MODE>();
+  const int hq_a = kQ ? (int)blockIdx.y : 0;
+  const int hk = kQ ? hq_a / G : (int)blockIdx.y;
+  const int a_rows = kQ ? a.n_q : a.T;
   const int rb0 = blockIdx.x * kUnits;
   const int nunits = min(kUnits, (a_rows + BM - 1) / BM - rb0);
 
@@ -264,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tc::tma_prefetch_desc(&tm_a);
     tc::tma_prefetch_desc(&tm_b);
-    if (MODE == kLse) tc::tma_prefetch_desc(&tm_b2);
+    if (kQ) tc::tma_prefetch_desc(&tm_b2);
   }
   __syncthreads();
   tc::fence_after_sync();
@@ -273,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ============================================================ TMA producer
     if (lane == 0) {
-      const int a_head = (MODE == kLse) ? l * a.Hq + hq_a : l * a.Hkv + hk;
+      const int a_head = kQ ? l * a.Hq + hq_a : l * a.Hkv + hk;
       for (int n = 0; n < nunits; ++n) {  // every unit's A tile up front
         tc::mbar_expect_tx(bar_afull(n), C::A_BYTES);
 #pragma unroll
@@ -294,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const CUtensorMap* map;
           int row, head;
-          if (MODE == kLse) {
+          if (kQ) {
             head = l * a.Hkv + hk;
             if (it < U.n_ctx) {
               map = &tm_b;
@@ -376,7 +414,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     for (int n = 0; n < nunits; ++n) {
       const Tiles U = tiles_of<MODE>(a, (rb0 + n) * BM, G, off);
-      const int ra = U.row0 + row;  // this thread's query (kLse) or key
+      const int ra = U.row0 + row;  // this thread's query (kLse, kRows) or key
+      float l2row = 0.f;              // kRows: this query's LSE in log2 units
+      bf16_t *rhi = nullptr, *rlo = nullptr;
+      if (MODE == kRows && ra < a.n_q) {
+        const size_t r = (size_t)(l * a.Hq + hq_a) * a.n_q + ra;
+        l2row = a.lse[r] * kLog2e;
+        rhi = a.rows_hi + r * a.rows_ld;
+        rlo = a.rows_lo + r * a.rows_ld;
+      }
 
       auto col_const = [&](int it) -> float {
         const int hq = hk * G + it / U.per_head;
@@ -492,6 +538,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (kb + c >= lim || kb + c > off + ra) v[c] = __float_as_uint(-CUDART_INF_F);
           }
           lse_cols(v + 64, sc2, m, ssum);
+        } else if (MODE == kRows) {
+          // softmax weights 2^(x sc2 - lse log2 e) of this row, as bf16 hi + lo parts
+          const int kb = it * BN + h * HALF;
+          rows_cols(v, kb, a.T, l2row, sc2, rhi, rlo, a.rows_ld, ra < a.n_q);
+          tc::tmem_ld_wait();
+          tc::fence_before_sync();
+          tc::mbar_arrive(bar_tempty(acc));
+          rows_cols(v + 64, kb + 64, a.T, l2row, sc2, rhi, rlo, a.rows_ld, ra < a.n_q);
         } else if (MODE == kMax) {
           r = max_cols(v, cc, scale, r);
           tc::tmem_ld_wait();
@@ -518,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // partial dot products).  Both groups vote on failure here, so they leave the unit
       // loop together and never wait at a barrier the other has abandoned.
       float* xchg = xchg_all + (n & 1) * BM * 2;
-      if (MODE != kQuad && h == 1 && !bad) {
+      if (MODE != kQuad && MODE != kRows && h == 1 && !bad) {
         if (MODE == kLse) {
           xchg[row * 2] = m;
           xchg[row * 2 + 1] = ssum;
@@ -530,6 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         failed = true;
         break;
       }
+      if (MODE == kRows) continue;  // rows were written tile by tile
       if (MODE == kQuad) {
         if (h == 0 && ra < a.T) {
           for (int it = 0; it < U.ntiles; ++it) {
@@ -603,7 +658,7 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
   using C = Cfg<D, MODE>;
   CUtensorMap ta, tb, tb2;
   cudaError_t e;
-  if (MODE == kLse) {
+  if (a_is_queries<MODE>()) {
     e = make_map(&ta, a.q, D, a.n_q, a.L * a.Hq, BM);
     if (e == cudaSuccess)
       e = a.T > 0 ? make_map(&tb, a.k_ctx, D, a.T, a.L * a.Hkv, BN)
@@ -624,8 +679,9 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
     tb2 = tb;
   }
   if (e != cudaSuccess) return e;
-  const int rows = (MODE == kLse) ? a.n_q : a.T;
-  dim3 grid(((rows + BM - 1) / BM + kUnits - 1) / kUnits, MODE == kLse ? a.Hq : a.Hkv, a.L);
+  const int rows = a_is_queries<MODE>() ? a.n_q : a.T;
+  dim3 grid(((rows + BM - 1) / BM + kUnits - 1) / kUnits, a_is_queries<MODE>() ? a.Hq : a.Hkv,
+            a.L);
   auto kern = attn_tc_kernel<D, MODE>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
@@ -636,7 +692,7 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
 
 template <int MODE>
 cudaError_t launch_mode(const AttnArgs& a, cudaStream_t s) {
-  const int rows = (MODE == kLse) ? a.n_q : a.T;
+  const int rows = a_is_queries<MODE>() ? a.n_q : a.T;
   if (rows == 0) return cudaSuccess;
   return a.d == 128 ? launch_d<128, MODE>(a, s) : launch_d<64, MODE>(a, s);
 }
@@ -669,6 +725,9 @@ cudaError_t tma_map_bf16_3d(CUtensorMap* m, const void* base, int inner, int row
 }
 
 cudaError_t launch_lse(const AttnArgs& a, cudaStream_t s) { return launch_mode<kLse>(a, s); }
+cudaError_t launch_softmax_rows(const AttnArgs& a, cudaStream_t s) {
+  return launch_mode<kRows>(a, s);
+}
 cudaError_t launch_score_max(const AttnArgs& a, cudaStream_t s) { return launch_mode<kMax>(a, s); }
 cudaError_t launch_future_sum(const AttnArgs& a, cudaStream_t s) {
   return launch_mode<kFuture>(a, s);

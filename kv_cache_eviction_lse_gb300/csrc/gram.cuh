@@ -1,0 +1,38 @@
+// Launchers of the value refit's linear algebra: the batched X^T Y products on the
+// tensor cores and the per-problem Cholesky solve of the ridge normal equations.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace kvs {
+
+struct GramArgs {
+  const bf16_t* x_hi = nullptr;  // [batch][rows][ldx], columns >= M are zero
+  const bf16_t* x_lo = nullptr;
+  const bf16_t* y_hi = nullptr;  // [batch][rows][ldy]
+  const bf16_t* y_lo = nullptr;  // nullable: Y taken as one bf16 part
+  float* c = nullptr;            // [batch][M][ldc]
+  int batch = 0, rows = 0, M = 0, N = 0, ldx = 0, ldy = 0, ldc = 0;
+  int upper = 0;                 // Y == X: write only the upper block triangle (M == N)
+};
+
+cudaError_t launch_gram(const GramArgs& a, cudaStream_t s);
+cudaError_t gram_device_error(int* code, bool clear, cudaStream_t s);
+
+struct CholArgs {
+  float* g = nullptr;      // [batch][M][ldg]: Gram (upper block triangle), overwritten by U
+  float* r = nullptr;      // [batch][M][d]: right-hand sides, overwritten by the solution
+  float* x = nullptr;      // [batch][k][d]: output, the first k rows of the solution
+  int batch = 0, M = 0, ldg = 0, k = 0, d = 0;
+  float lam_rel = 0.f;     // ridge weight relative to the mean of the first k diagonal entries
+};
+
+// Solves (G + lam I) X = R per problem, lam = lam_rel * trace(G[:k, :k]) / k, by an
+// upper Cholesky factorisation in fp32 (one CTA per problem).  M <= kCholMaxM.
+constexpr int kCholMaxM = 2048;
+cudaError_t launch_chol_solve(const CholArgs& a, cudaStream_t s);
+cudaError_t chol_device_error(int* code, bool clear, cudaStream_t s);
+
+}  // namespace kvs

@@ -1,0 +1,223 @@
+// Batched C = X^T Y with fp32-level accuracy from bf16 tensor cores (tcgen05 + TMEM + TMA),
+// for the normal equations of the value refit: X = the softmax rows A_S of the kept keys
+// ([rows][M], split as hi + lo bf16 parts), Y = A_S itself (Gram matrix, upper block
+// triangle only) or the attention output O ([rows][N], one bf16 part).
+//
+//   C[b][m][n] = sum_r X[b][r][m] Y[b][r][n]
+//             ~= sum_r Xhi Yhi + Xhi Ylo + Xlo Yhi   (Y split)    or   Xhi Y + Xlo Y
+//
+// Both operands are read MN-major straight from their row-major [rows][cols] storage:
+// a TMA box of 64 rows x 64 columns is one 128-byte-swizzled MN-major atom column, so
+// a 128-column tile is two boxes (leading byte offset 8 KB) and each MMA takes 16 rows.
+// One CTA per 128 x 128 output tile; warp 0 streams 64-row k-blocks through a 3-stage
+// ring, warp 1 issues the MMAs into one TMEM accumulator, warps 2-5 write the tile.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "gram.cuh"
+#include "tc.cuh"
+
+namespace kvs {
+
+__device__ int g_gram_error = 0;
+
+namespace {
+
+constexpr int BT = 128;                 // output tile edge
+constexpr int BK = 64;                  // rows per k-block
+constexpr uint32_t kBox = 64 * 128;     // 64 rows x 64 bf16 = 8 KB
+constexpr uint32_t kOp = 2 * kBox;      // one 128-column operand tile of a k-block
+constexpr int kStages = 3;
+constexpr uint32_t kStage = 4 * kOp;    // X hi, X lo, Y hi, Y lo
+constexpr int kThreads = 64 + 128;
+constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t OFF_BAR = kStages * kStage;
+constexpr uint32_t NBAR = 2 * kStages + 1;  // full[S], empty[S], done
+constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+constexpr uint32_t USED = OFF_MISC + 16;
+constexpr uint32_t SMEM = USED + 1024;
+static_assert(SMEM <= 232448, "shared-memory plan exceeds the per-block limit");
+constexpr int kErrWaitTimeout = 1;
+constexpr int kErrSmemAlign = 3;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gram_tc_kernel(const __grid_constant__ CUtensorMap tm_xhi, const __grid_constant__ CUtensorMap tm_xlo,
+                   const __grid_constant__ CUtensorMap tm_yhi, const __grid_constant__ CUtensorMap tm_ylo,
+                   const GramArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  if (pad + USED > SMEM) {
+    if (threadIdx.x == 0) atomicCAS(&g_gram_error, 0, kErrSmemAlign);
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sb = raw + pad;
+  const uint32_t bar0 = sb + OFF_BAR;
+  auto bar_full = [&](int s) { return bar0 + 8u * s; };
+  auto bar_empty = [&](int s) { return bar0 + 8u * (kStages + s); };
+  const uint32_t bar_done = bar0 + 8u * (2 * kStages);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // output tile: the upper block triangle when Y is X (symmetric result)
+  int tm, tn;
+  if (a.upper) {
+    int t = blockIdx.x, row = 0, nt = (a.M + BT - 1) / BT;
+    while (t >= nt - row) {
+      t -= nt - row;
+      ++row;
+    }
+    tm = row;
+    tn = row + t;
+  } else {
+    tm = blockIdx.x / ((a.N + BT - 1) / BT);
+    tn = blockIdx.x % ((a.N + BT - 1) / BT);
+  }
+  const int b = blockIdx.y;
+  const int nkb = (a.rows + BK - 1) / BK;
+  const bool y_split = a.y_lo != nullptr;
+  const uint32_t stage_bytes = (y_split ? 4 : 3) * kOp;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(bar_full(s), 1);
+      tc::mbar_init(bar_empty(s), 1);
+    }
+    tc::mbar_init(bar_done, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(sb + OFF_MISC, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = misc[0];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int kb = 0;
+      bool ok = true;
+      for (; kb < nkb; ++kb) {
+        const int s = kb % kStages;
+        if (!tc::mbar_wait(bar_empty(s), ((kb / kStages) & 1) ^ 1u)) {
+          ok = false;
+          break;
+        }
+        const uint32_t st = sb + s * kStage;
+        tc::mbar_expect_tx(bar_full(s), stage_bytes);
+        for (int c = 0; c < 2; ++c) {  // two 64-column boxes per operand tile
+          tc::tma_load_3d(st + c * kBox, &tm_xhi, bar_full(s), tm * BT + 64 * c, kb * BK, b);
+          tc::tma_load_3d(st + kOp + c * kBox, &tm_xlo, bar_full(s), tm * BT + 64 * c, kb * BK, b);
+          tc::tma_load_3d(st + 2 * kOp + c * kBox, &tm_yhi, bar_full(s), tn * BT + 64 * c, kb * BK,
+                          b);
+          if (y_split)
+            tc::tma_load_3d(st + 3 * kOp + c * kBox, &tm_ylo, bar_full(s), tn * BT + 64 * c,
+                            kb * BK, b);
+        }
+      }
+      if (!ok) {
+        atomicCAS(&g_gram_error, 0, kErrWaitTimeout);
+        for (int j = max(0, kb - kStages); j < kb; ++j)
+          tc::mbar_wait(bar_full(j % kStages), (j / kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_bmn(BT, BT) | (1u << 15);  // A and B MN-major
+      int kb = 0;
+      bool ok = true;
+      for (; kb < nkb; ++kb) {
+        const int s = kb % kStages;
+        if (!tc::mbar_wait(bar_full(s), (kb / kStages) & 1)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t st = sb + s * kStage;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          const uint32_t o = 2048u * k;  // 16 rows of 128 bytes
+          const uint64_t xh = tc::sdesc_sw128_mn(st + o, kBox), xl = tc::sdesc_sw128_mn(st + kOp + o, kBox);
+          const uint64_t yh = tc::sdesc_sw128_mn(st + 2 * kOp + o, kBox);
+          tc::mma_bf16(tmem, xh, yh, idesc, (kb | k) != 0 ? 1u : 0u);
+          tc::mma_bf16(tmem, xl, yh, idesc, 1u);
+          if (y_split) tc::mma_bf16(tmem, xh, tc::sdesc_sw128_mn(st + 3 * kOp + o, kBox), idesc, 1u);
+        }
+        tc::commit(bar_empty(s));
+      }
+      if (!ok) atomicCAS(&g_gram_error, 0, kErrWaitTimeout);
+      tc::commit(bar_done);  // lands once every MMA above has completed
+      tc::mbar_wait(bar_done, 0);
+    }
+    __syncwarp();
+  } else {
+    // epilogue: warp w reads TMEM lanes 32 (w % 4) ..; row m of the tile per thread
+    const int eq = warp & 3;
+    const int m = tm * BT + eq * 32 + lane;
+    const bool ok = tc::mbar_wait(bar_done, 0);
+    if (!ok) atomicCAS(&g_gram_error, 0, kErrWaitTimeout);
+    tc::fence_after_sync();
+    float* crow = a.c + ((size_t)b * a.M + m) * a.ldc + tn * BT;
+    const int nmax = min(BT, a.N - tn * BT);
+#pragma unroll
+    for (int cb = 0; cb < BT / 32; ++cb) {
+      uint32_t v[32];
+      tc::tmem_ld32(tmem + ((uint32_t)(eq * 32) << 16) + 32u * cb, v);
+      tc::tmem_ld_wait();
+      if (ok && m < a.M) {
+        if (32 * cb + 32 <= nmax) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 4)
+            *reinterpret_cast<float4*>(crow + 32 * cb + c) =
+                make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]),
+                            __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+        } else {
+          for (int c = 0; c < 32 && 32 * cb + c < nmax; ++c) crow[32 * cb + c] = __uint_as_float(v[c]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gram(const GramArgs& a, cudaStream_t s) {
+  if (a.M <= 0 || a.N <= 0 || a.batch <= 0) return cudaSuccess;
+  if (a.upper && a.M != a.N) return cudaErrorInvalidValue;
+  if (a.ldx % 8 || a.ldy % 8 || a.ldc % 4) return cudaErrorInvalidValue;
+  CUtensorMap xh, xl, yh, yl;
+  cudaError_t e = tma_map_bf16_3d(&xh, a.x_hi, a.ldx, a.rows, a.batch, BK);
+  if (e == cudaSuccess) e = tma_map_bf16_3d(&xl, a.x_lo, a.ldx, a.rows, a.batch, BK);
+  if (e == cudaSuccess) e = tma_map_bf16_3d(&yh, a.y_hi, a.ldy, a.rows, a.batch, BK);
+  if (e == cudaSuccess)
+    e = tma_map_bf16_3d(&yl, a.y_lo ? a.y_lo : a.y_hi, a.ldy, a.rows, a.batch, BK);
+  if (e != cudaSuccess) return e;
+  const int tmn = (a.M + BT - 1) / BT, tnn = (a.N + BT - 1) / BT;
+  const int tiles = a.upper ? tmn * (tmn + 1) / 2 : tmn * tnn;
+  e = cudaFuncSetAttribute(gram_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+  if (e != cudaSuccess) return e;
+  count_launches(1);
+  gram_tc_kernel<<<dim3(tiles, a.batch), kThreads, SMEM, s>>>(xh, xl, yh, yl, a);
+  return cudaGetLastError();
+}
+
+cudaError_t gram_device_error(int* code, bool clear, cudaStream_t s) {
+  cudaError_t e = cudaMemcpyFromSymbolAsync(code, g_gram_error, sizeof(int), 0,
+                                            cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && clear && *code) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_gram_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
+  return e;
+}
+
+}  // namespace kvs

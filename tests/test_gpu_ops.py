@@ -480,3 +480,61 @@ def test_decode_step_pool_exhaustion_is_reported(C):
         assert (ids < capacity).all()
         got = st["kp"].cpu()[ids].reshape(-1, d)[:n]
         assert torch.equal(got.view(torch.int16), kr[r, :n].view(torch.int16))
+
+
+# ----------------------------------------------------------------------------- value refit
+
+REFIT_SHAPES = [
+    # L, Hkv, Hq, d, T, n_q, k
+    (1, 2, 4, 128, 300, 200, 100),
+    (2, 1, 2, 64, 130, 70, 77),       # k not a multiple of 64, d = 64
+    (1, 1, 3, 128, 520, 257, 1),      # a single kept key
+    (1, 2, 2, 128, 700, 300, 333),    # several 128-row tiles of the Gram matrix
+]
+
+
+def _refit_objective(A, Ot, lam, V):
+    return float(((A @ V - Ot) ** 2).sum() + lam * (V ** 2).sum())
+
+
+@pytest.mark.parametrize("shape", REFIT_SHAPES, ids=[str(s) for s in REFIT_SHAPES])
+def test_value_refit(C, shape):
+    """The refit reaches the oracle's ridge optimum: the objective of the GPU solution,
+    evaluated in fp64 with the oracle's A_S, O and lam, exceeds the optimum by at most
+    2^-16 ||O||^2.  The GPU's O is bf16 (relative 2^-9, so ||dO||^2 <= 2^-18 ||O||^2,
+    and a least-squares solution moves the objective by at most ||dO||^2); the hi/lo
+    Gram and the fp32 Cholesky add far less.  Four times that bound."""
+    L, Hkv, Hq, d, T, nq, k = shape
+    lam_rel = 1e-3
+    x = _inputs(L, Hkv, Hq, d, T, 0, nq, seed=T + k)
+    gen = torch.Generator().manual_seed(k)
+    mask = torch.zeros(L, Hkv, T, dtype=torch.uint8)
+    for l in range(L):
+        for h in range(Hkv):
+            mask[l, h, torch.randperm(T, generator=gen)[:k]] = 1
+    idx = [[torch.nonzero(mask[l, h]).flatten() for h in range(Hkv)] for l in range(L)]
+    k_kept = torch.stack([torch.stack([x["k_ctx"][l, h, idx[l][h]] for h in range(Hkv)])
+                          for l in range(L)]).contiguous()
+    g = cuda(dict(q=x["q"], k_ctx=x["k_ctx"], v_ctx=x["v_ctx"], k_kept=k_kept))
+    dm = C.dims(L, Hq, Hkv, d)
+    nbytes = C.kvs_value_refit_workspace_size(dm, nq, k)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    vfit = torch.full((L, Hkv, k, d), float("nan"), device="cuda")
+    C.kvs_value_refit(dm, g["q"], nq, g["k_ctx"], g["v_ctx"], T, g["k_kept"], k, lam_rel, vfit,
+                      ws, nbytes)
+    torch.cuda.synchronize()
+    assert C.kvs_device_error(clear=True) == 0
+    q64, k64, v64 = f64(x["q"]), f64(x["k_ctx"]), f64(x["v_ctx"])
+    _, parts = O.value_refit(q64, k64, v64, mask.numpy(), 1.0)  # A_S and O only
+    vg = vfit.cpu().double().numpy()
+    for l in range(L):
+        for h in range(Hkv):
+            A, Ot = parts[l][h]
+            lam = lam_rel * float((A * A).sum()) / k
+            vv, _ = O.value_refit(q64[l:l + 1, h * (Hq // Hkv):(h + 1) * (Hq // Hkv)],
+                                  k64[l:l + 1, h:h + 1], v64[l:l + 1, h:h + 1],
+                                  mask[l:l + 1, h:h + 1].numpy(), lam)
+            best = _refit_objective(A, Ot, lam, vv[0][0])
+            got = _refit_objective(A, Ot, lam, vg[l, h])
+            assert np.isfinite(vg[l, h]).all()
+            assert got - best <= 2.0 ** -16 * float((Ot ** 2).sum()), (l, h, got, best)
