@@ -11,6 +11,7 @@ One step = one pass of the whole path over one batch of synthetic input (all lay
       once before timing) with w=128 -> compaction
   c4: lse (causal) -> future mass (w=128) -> top-k 25% / 12.5% + window -> compaction
       (--attn-forward: pass 1 is the attention forward, output + LSE, instead)
+  c2 --refit: adds the closed-form value refit (Select+Fit) of the r=0.3 budget's kept keys
   c5: surrogate (+ fused threshold tau=-5, w=128) -> compaction
   c6: MLP surrogate 4096 -> 512 -> 8 (+ threshold tau=-4, w=128) -> compaction
   c7: decode step of 64 sequences: surrogate score of the arriving tokens -> window-boundary
@@ -76,6 +77,8 @@ def parse_args():
     ap.add_argument("--attn-forward", action="store_true",
                     help="c4: pass 1 is the attention forward (output + LSE) instead of the "
                          "LSE-only pass")
+    ap.add_argument("--refit", action="store_true",
+                    help="c1/c2: add the closed-form value refit on the first budget's kept keys")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--stage-reps", type=int, default=None)
@@ -114,6 +117,13 @@ def algorithmic_work(wl, p):
         out["kvs_score_max"] = ("tensor", 2 * d * el2, "flop")
         if wl.kind != "kvzip":
             out["kvs_vnorm"] = ("tensor", 2 * L * wl.H_q * d * d * (wl.D_h + wl.T), "flop")
+        if getattr(p, "refit", False):
+            # forward over the context (S and P V), S and softmax over the kept keys, the
+            # symmetric Gram, the right-hand side, Cholesky and the two triangular solves
+            k, n, B = p.k_fit, wl.g * nq, L * wl.H_kv
+            out["kvs_value_refit"] = ("tensor", B * (4 * d * n * wl.T + 2 * d * n * k
+                                                     + n * k * (k + 1) + 2 * n * k * d
+                                                     + k ** 3 // 3 + 2 * k * k * d), "flop")
     if wl.kind == "future":
         n, w = wl.T, wl.w
         el1 = L * wl.H_q * n * (n + 1) // 2
@@ -242,11 +252,15 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def build_pipeline(wl, device, attn_forward=False):
+def build_pipeline(wl, device, attn_forward=False, refit=False):
     from kv_cache_eviction_lse_gb300 import pipeline, workloads as W
     x = W.generate(wl, device=device)
-    p = pipeline.make_pipeline(wl, x, attn_forward=True) if attn_forward else \
-        pipeline.make_pipeline(wl, x)
+    kw = {}
+    if attn_forward:
+        kw["attn_forward"] = True
+    if refit:
+        kw["refit"] = True
+    p = pipeline.make_pipeline(wl, x, **kw)
     if wl.kind == "kvzip_plus_chunked":
         # calibrate the per-layer threshold once (25th percentile of the non-window
         # scores of each layer), then keep it fixed for the timed steps
@@ -281,7 +295,7 @@ def run_gpu(args, rank, world, local):
         wl = wl.scaled(L=min(args.layers, wl.L))
     K = args.steps or DEFAULT_STEPS[args.workload]
     Wm = max(3, args.warmup)
-    x, p = build_pipeline(wl, dev, attn_forward=args.attn_forward)
+    x, p = build_pipeline(wl, dev, attn_forward=args.attn_forward, refit=args.refit)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -391,6 +405,7 @@ def run_gpu(args, rank, world, local):
                    "launch": "python calls" if args.no_graph else "CUDA graph of the step",
                    "pass1": "attention forward (output + LSE)" if args.attn_forward
                    else "LSE-only pass",
+                   "value_refit": bool(args.refit),
                    "l2": f"{L2_FLUSH_BYTES >> 20} MB buffer written between timed steps"},
         "roofline": roofline,
         "kernels": kernels,

@@ -51,7 +51,11 @@ def compact_into(dm, k, v, T, mask, pages: Pages, ws):
 class KVzipPipeline:
     """c1 / c2: KVzip (plain) or KVzip+ scoring of the context, then top-k budgets."""
 
-    def __init__(self, wl: Workload, x: dict, ratios=None):
+    # ridge weight of the value refit relative to the mean diagonal of A_S^T A_S (reading:
+    # the pages name ridge regression but no weight)
+    REFIT_LAMBDA_REL = 1e-3
+
+    def __init__(self, wl: Workload, x: dict, ratios=None, refit=False):
         self.wl, self.x = wl, x
         dev = x["q"].device
         L = x["q"].shape[0]
@@ -72,6 +76,27 @@ class KVzipPipeline:
         self.keeps = [_empty((L, wl.H_kv), torch.int32, dev) for _ in self.ratios]
         self.pages = [Pages(L, wl.H_kv, wl.T, wl.d, wl.page_size, dev) for _ in self.ratios]
         self.cws = _empty((C.kvs_compact_workspace_size(self.dm, wl.T),), torch.uint8, dev)
+        # refit: Select+Fit on the first budget -- the kept keys gathered densely (one
+        # page of exactly k rows per head), then their values refitted in closed form
+        self.refit = refit
+        if refit:
+            self.k_fit = wl.topk_budget(self.ratios[0]) + wl.w
+            self.dense = Pages(L, wl.H_kv, wl.T, wl.d, self.k_fit, dev)
+            self.v_fit = _empty((L, wl.H_kv, self.k_fit, wl.d), torch.float32, dev)
+            n = C.kvs_value_refit_workspace_size(self.dm, self.n_q, self.k_fit)
+            self.rws = _empty((n,), torch.uint8, dev)
+
+    def k_kept(self):
+        """The kept keys of the first budget as [L][H_kv][k][d] (refit only)."""
+        wl = self.wl
+        return self.dense.k_pages[: self.L * wl.H_kv].view(self.L, wl.H_kv, self.k_fit, wl.d)
+
+    def _refit(self):
+        wl, x, dm = self.wl, self.x, self.dm
+        compact_into(dm, x["k_ctx"], x["v_ctx"], wl.T, self.masks[0], self.dense, self.cws)
+        C.kvs_value_refit(dm, x["q"], self.n_q, x["k_ctx"], x["v_ctx"], wl.T, self.k_kept(),
+                          self.k_fit, self.REFIT_LAMBDA_REL, self.v_fit, self.rws,
+                          self.rws.numel())
 
     def score_step(self):
         if self.plus:
@@ -113,8 +138,9 @@ class KVzipPipeline:
     def stages(self):
         """(name, callable) per library entry point, in step order."""
         st = [("kvs_vnorm", self._vnorm)] if self.plus else []
-        return st + [("kvs_lse", self._lse), ("kvs_score_max", self._score),
-                     ("kvs_prune_mask", self._prune), ("kvs_compact_paged", self._compact)]
+        st += [("kvs_lse", self._lse), ("kvs_score_max", self._score),
+               ("kvs_prune_mask", self._prune), ("kvs_compact_paged", self._compact)]
+        return st + ([("kvs_value_refit", self._refit)] if self.refit else [])
 
     def step(self):
         for _, fn in self.stages():

@@ -267,3 +267,36 @@ def test_c7_decode_steps_full_size(mods):
 def C_error_clear():
     from kv_cache_eviction_lse_gb300 import capi
     return capi.kvs_device_error(clear=True)
+
+
+def test_c2_value_refit_layer0(mods):
+    """Select+Fit at c2 size: the r = 0.3 top-k keys (614 per head) of every layer and
+    head, refitted; layer 0's two KV heads reach the fp64 ridge optimum within the bound
+    of the per-op test (objective excess <= 2^-16 ||O||^2)."""
+    pipeline, W = mods
+    wl = W.WORKLOADS["c2"]
+    x = W.generate(wl)
+    p = pipeline.make_pipeline(wl, cuda(x), refit=True)
+    p.step()
+    torch.cuda.synchronize()
+    from kv_cache_eviction_lse_gb300 import capi
+    assert capi.kvs_device_error(clear=True) == 0
+    k = p.k_fit
+    mask = p.masks[0][0:1].cpu().numpy()
+    assert (mask.sum(-1) == k).all()
+    q64, k64, v64 = f64(x["q"][0:1]), f64(x["k_ctx"][0:1]), f64(x["v_ctx"][0:1])
+    # the dense gather is the kept keys in position order
+    for h in range(wl.H_kv):
+        idx = np.nonzero(mask[0, h])[0]
+        assert np.array_equal(p.k_kept()[0, h].cpu().view(torch.int16).numpy(),
+                              x["k_ctx"][0, h][idx].view(torch.int16).numpy())
+    _, parts = O.value_refit(q64, k64, v64, mask, 1.0)
+    vg = p.v_fit[0].cpu().double().numpy()
+    g = wl.g
+    for h in range(wl.H_kv):
+        A, Ot = parts[0][h]
+        lam = p.REFIT_LAMBDA_REL * float((A * A).sum()) / k
+        vv, _ = O.value_refit(q64[:, h * g:(h + 1) * g], k64[:, h:h + 1], v64[:, h:h + 1],
+                              mask[:, h:h + 1], lam)
+        f = lambda V: float(((A @ V - Ot) ** 2).sum() + lam * (V ** 2).sum())
+        assert f(vg[h]) - f(vv[0][0]) <= 2.0 ** -16 * float((Ot ** 2).sum())
