@@ -40,11 +40,8 @@ namespace {
 
 constexpr int BM = 128;     // rows of operand A per CTA = TMEM lanes
 constexpr int BN = 256;     // rows per B tile = accumulator columns (N of each MMA)
-constexpr int HALF = 128;   // accumulator columns per epilogue group
-constexpr int kGroups = 2;  // epilogue groups: column halves of the accumulator
-constexpr int kGroupThreads = 128;
-constexpr int kEpiThreads = kGroups * kGroupThreads;
-constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kGroupThreads = 128;  // one epilogue group: a warp per TMEM lane quarter
+constexpr int kAllBar = 6;          // named barrier of all epilogue warps (groups use 1..4)
 constexpr uint32_t kBoxBytesA = 128 * 128;  // 128 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr uint32_t kBoxBytesB = 256 * 128;  // 256 rows x 64 bf16
 constexpr uint32_t kTmemCols = 2 * BN;       // two accumulators of 256 columns
@@ -64,15 +61,22 @@ constexpr int kMaxGroup = 16;  // query heads per KV head handled by kQuad
 
 template <int D, int MODE>
 struct Cfg {
+  // epilogue groups, each owning COLS accumulator columns of every row: four groups of
+  // 64 columns (four warps per SM sub-partition to hide the reductions' latency); the
+  // quadratic form needs its rows' halves and keeps two
+  static constexpr int NG = MODE == kQuad ? 2 : 4;
+  static constexpr int COLS = BN / NG;
+  static constexpr int EPI = NG * kGroupThreads;
+  static constexpr int THREADS = 64 + EPI;
   static constexpr int KH = D / 64;
   static constexpr int STAGES = D == 128 ? 2 : 4;
   static constexpr uint32_t A_BYTES = KH * kBoxBytesA;  // one of kUnits A buffers
   static constexpr uint32_t B_BYTES = KH * kBoxBytesB;
   static constexpr uint32_t OFF_B = kUnits * A_BYTES;
-  static constexpr uint32_t OFF_C = OFF_B + STAGES * B_BYTES;        // [groups][2][HALF] floats
-  static constexpr uint32_t OFF_X = OFF_C + kGroups * 2 * HALF * 4;  // [2][BM][2] floats
-  static constexpr uint32_t OFF_P = OFF_X + 2 * BM * 2 * 4;          // kQuad [2][16][BM] floats
-  static constexpr uint32_t OFF_BAR = OFF_P + (MODE == kQuad ? kGroups * kMaxGroup * BM * 4 : 0);
+  static constexpr uint32_t OFF_C = OFF_B + STAGES * B_BYTES;  // [NG][2][COLS] floats
+  static constexpr uint32_t OFF_X = OFF_C + 2 * BN * 4;          // [2][NG-1][BM][2] floats
+  static constexpr uint32_t OFF_P = OFF_X + 2 * (NG - 1) * BM * 2 * 4;  // kQuad [2][16][BM]
+  static constexpr uint32_t OFF_BAR = OFF_P + (MODE == kQuad ? 2 * kMaxGroup * BM * 4 : 0);
   // a_full[kUnits], full[S], empty[S], tfull[2], tempty[2]
   static constexpr uint32_t NBAR = kUnits + 2 * STAGES + 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
@@ -241,7 +245,7 @@ __device__ __forceinline__ Tiles tiles_of(const AttnArgs& a, int row0, int G, in
 }
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __grid_constant__ CUtensorMap tm_b2, const AttnArgs a) {
   using C = Cfg<D, MODE>;
@@ -290,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       tc::mbar_init(bar_tfull(x), 1);
-      tc::mbar_init(bar_tempty(x), kEpiThreads);
+      tc::mbar_init(bar_tempty(x), C::EPI);
     }
     misc[1] = 0u;
     tc::fence_mbar_init();
@@ -401,12 +405,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ============================================================ epilogue
-    const int h = (warp - 2) >> 2;               // column half of the accumulator
+    constexpr int NG = C::NG, COLS = C::COLS, EPI = C::EPI;
+    const int h = (warp - 2) >> 2;               // epilogue group: columns [h COLS, (h+1) COLS)
     const int eq = warp & 3;                     // TMEM lane quarter this warp may access
     const int row = eq * 32 + lane;              // accumulator row
     const int e = ((warp - 2) & 3) * 32 + lane;  // index within the group (0..127)
-    const uint32_t t_lane = tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(h * HALF);
-    float* cbuf = cbuf_all + h * 2 * HALF;
+    const uint32_t t_lane = tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(h * COLS);
+    float* cbuf = cbuf_all + h * 2 * COLS;
     const int bar_id = 1 + h;
     constexpr bool kCols = (MODE == kMax || MODE == kFuture);  // per-column constants
     int gt = 0;
@@ -426,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       auto col_const = [&](int it) -> float {
         const int hq = hk * G + it / U.per_head;
-        const int j = (U.qt_begin + it % U.per_head) * BN + h * HALF + e;
+        const int j = (U.qt_begin + it % U.per_head) * BN + h * COLS + e;
         if (j >= a.n_q) return -CUDART_INF_F;
         const float lj = a.lse[(size_t)(l * a.Hq + hq) * a.n_q + j];
         if (MODE == kMax) return -(lj + (a.hlog ? a.hlog[(size_t)l * a.n_q + j] : 0.f));
@@ -442,7 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float lv = 0.f;                                // kMax: ln vnorm of the current head
       float f = 0.f;                                 // kFuture
       float cn1 = 0.f, cn2 = 0.f;
-      if (kCols && U.ntiles > 0) {
+      // threads e < COLS of a group own one column constant each
+      if (kCols && U.ntiles > 0 && e < COLS) {
         const float c0 = col_const(0);
         if (U.ntiles > 1) cn1 = col_const(1);
         if (U.ntiles > 2) cn2 = col_const(2);
@@ -451,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (MODE == kMax && U.ntiles > 0) lv = ln_vn(0);
 
       // kQuad: this thread's D/2 elements of its value row, from the swizzled A tile
-      uint32_t vrow[D / 4];
+      uint32_t vrow[MODE == kQuad ? D / 4 : 1];
       bool bad = false;  // a wait of this group ran out: skip to the end-of-unit vote
       if (MODE == kQuad) bad = tc::bar_or(bar_id, kGroupThreads, !tc::mbar_wait(bar_afull(n), 0));
       if (MODE == kQuad && !bad) {
@@ -481,8 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc::fence_after_sync();
-        uint32_t v[HALF];
-        if (MODE == kQuad) {
+        if constexpr (MODE == kQuad) {
+          uint32_t v[128];
           // columns [h D/2, (h+1) D/2) of V G_hi and of V G_lo (which starts at column D)
           const uint32_t tq =
               tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(acc * BN + h * (D / 2));
@@ -503,84 +509,69 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           part[(h * kMaxGroup + it) * BM + row] = p0 + p1;
           continue;
-        }
-        const uint32_t ta = t_lane + (uint32_t)(acc * BN);
-        tc::tmem_ld32(ta, v);
-        tc::tmem_ld32(ta + 32, v + 32);
-        tc::tmem_ld_wait();
-        tc::tmem_ld32(ta + 64, v + 64);  // in flight while the first 64 columns reduce
-        tc::tmem_ld32(ta + 96, v + 96);
-        if (kCols) {
-          // the other buffer's readers finished tile it-1 before the barrier above
-          if (it + 1 < U.ntiles) cbuf[((it + 1) & 1) * HALF + e] = cn1;
-          cn1 = cn2;
-          if (it + 3 < U.ntiles) cn2 = col_const(it + 3);
-        }
-        const float* cc = cbuf + (it & 1) * HALF;
-
-        if (MODE == kLse) {
-          const bool ctx = it < U.n_ctx;
-          const int kb = (ctx ? it * BN : a.T + (it - U.n_ctx) * BN) + h * HALF;
-          const int lim = ctx ? a.T : n_k;
-          const bool need_mask = (kb + HALF > lim) || (kb + HALF - 1 > off + U.row0);
-          if (need_mask) {
+        } else {
+          // this group's COLS columns; the accumulator is released as soon as they are in
+          // registers, so the MMA of tile it+2 can start while they reduce
+          uint32_t v[COLS];
+          const uint32_t ta = t_lane + (uint32_t)(acc * BN);
 #pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if (kb + c >= lim || kb + c > off + ra) v[c] = __float_as_uint(-CUDART_INF_F);
+          for (int c = 0; c < COLS; c += 32) tc::tmem_ld32(ta + c, v + c);
+          if (kCols) {
+            // the other buffer's readers finished tile it-1 before the barrier above
+            if (it + 1 < U.ntiles && e < COLS) cbuf[((it + 1) & 1) * COLS + e] = cn1;
+            cn1 = cn2;
+            if (it + 3 < U.ntiles && e < COLS) cn2 = col_const(it + 3);
           }
-          lse_cols(v, sc2, m, ssum);
           tc::tmem_ld_wait();
           tc::fence_before_sync();
           tc::mbar_arrive(bar_tempty(acc));
-          if (need_mask) {
+          const float* cc = cbuf + (it & 1) * COLS;
 #pragma unroll
-            for (int c = 64; c < HALF; ++c)
-              if (kb + c >= lim || kb + c > off + ra) v[c] = __float_as_uint(-CUDART_INF_F);
+          for (int c0 = 0; c0 < COLS; c0 += 64) {
+            uint32_t* w = v + c0;
+            if (MODE == kLse) {
+              const bool ctx = it < U.n_ctx;
+              const int kb = (ctx ? it * BN : a.T + (it - U.n_ctx) * BN) + h * COLS + c0;
+              const int lim = ctx ? a.T : n_k;
+              if (kb + 64 > lim || kb + 63 > off + ra) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                  if (kb + c >= lim || kb + c > off + ra) w[c] = __float_as_uint(-CUDART_INF_F);
+              }
+              lse_cols(w, sc2, m, ssum);
+            } else if (MODE == kRows) {
+              // softmax weights 2^(x sc2 - lse log2 e) of this row, as bf16 hi + lo parts
+              rows_cols(w, it * BN + h * COLS + c0, a.T, l2row, sc2, rhi, rlo, a.rows_ld,
+                        ra < a.n_q);
+            } else if (MODE == kMax) {
+              r = max_cols(w, cc + c0, scale, r);
+            } else {
+              const int j0 = (U.qt_begin + it % U.per_head) * BN + h * COLS + c0;
+              const bool band = j0 < U.row0 + BM - 1 + a.w;
+              f += future_cols(w, cc + c0, sc2, band, ra + a.w - j0);
+            }
           }
-          lse_cols(v + 64, sc2, m, ssum);
-        } else if (MODE == kRows) {
-          // softmax weights 2^(x sc2 - lse log2 e) of this row, as bf16 hi + lo parts
-          const int kb = it * BN + h * HALF;
-          rows_cols(v, kb, a.T, l2row, sc2, rhi, rlo, a.rows_ld, ra < a.n_q);
-          tc::tmem_ld_wait();
-          tc::fence_before_sync();
-          tc::mbar_arrive(bar_tempty(acc));
-          rows_cols(v + 64, kb + 64, a.T, l2row, sc2, rhi, rlo, a.rows_ld, ra < a.n_q);
-        } else if (MODE == kMax) {
-          r = max_cols(v, cc, scale, r);
-          tc::tmem_ld_wait();
-          tc::fence_before_sync();
-          tc::mbar_arrive(bar_tempty(acc));
-          r = max_cols(v + 64, cc + 64, scale, r);
-          if ((it + 1) % U.per_head == 0) {  // last query tile of this head
+          if (MODE == kMax && (it + 1) % U.per_head == 0) {  // last query tile of this head
             tot = fmaxf(tot, r + lv);
             r = -CUDART_INF_F;
             if (it + 1 < U.ntiles) lv = ln_vn(it + 1);
           }
-        } else {
-          const int j0 = (U.qt_begin + it % U.per_head) * BN + h * HALF;
-          const bool band = j0 < U.row0 + BM - 1 + a.w;
-          const int jlim = ra + a.w - j0;  // columns c < jlim are inside the window
-          f += future_cols(v, cc, sc2, band, jlim);
-          tc::tmem_ld_wait();
-          tc::fence_before_sync();
-          tc::mbar_arrive(bar_tempty(acc));
-          f += future_cols(v + 64, cc + 64, sc2, band, jlim - 64);
         }
       }
-      // results of this unit: combine the two halves of each row (kQuad: the per-head
-      // partial dot products).  Both groups vote on failure here, so they leave the unit
-      // loop together and never wait at a barrier the other has abandoned.
-      float* xchg = xchg_all + (n & 1) * BM * 2;
-      if (MODE != kQuad && MODE != kRows && h == 1 && !bad) {
+      // results of this unit: combine the groups' partial results of each row (kQuad:
+      // the per-head partial dot products).  All groups vote on failure here, so they
+      // leave the unit loop together and never wait at a barrier another has abandoned.
+      float* xchg = xchg_all + (n & 1) * (NG - 1) * BM * 2;
+      if (MODE != kQuad && MODE != kRows && h > 0 && !bad) {
+        float* xg = xchg + (h - 1) * BM * 2;
         if (MODE == kLse) {
-          xchg[row * 2] = m;
-          xchg[row * 2 + 1] = ssum;
+          xg[row * 2] = m;
+          xg[row * 2 + 1] = ssum;
         } else {
-          xchg[row * 2] = (MODE == kMax) ? tot : f;
+          xg[row * 2] = (MODE == kMax) ? tot : f;
         }
       }
-      if (tc::bar_or(3, kEpiThreads, bad)) {
+      if (tc::bar_or(kAllBar, EPI, bad)) {
         failed = true;
         break;
       }
@@ -592,24 +583,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             a.out[(size_t)(l * a.Hq + hk * G + it) * a.T + ra] = sqrtf(fmaxf(q2, 0.f));
           }
         }
-        if (n + 1 < nunits) named_sync(3, kEpiThreads);  // part[] is rewritten by the next unit
+        if (n + 1 < nunits) named_sync(kAllBar, EPI);  // part[] is rewritten by the next unit
         continue;
       }
       if (h == 0) {
         if (MODE == kLse) {
-          const float m1 = xchg[row * 2], s1 = xchg[row * 2 + 1];
-          const float mn = fmaxf(m, m1);
-          const float st = ssum * fast_exp2(m - mn) + s1 * fast_exp2(m1 - mn);
+          float mn = m;
+#pragma unroll
+          for (int g2 = 0; g2 < NG - 1; ++g2) mn = fmaxf(mn, xchg[g2 * BM * 2 + row * 2]);
+          float st = ssum * fast_exp2(m - mn);
+#pragma unroll
+          for (int g2 = 0; g2 < NG - 1; ++g2)
+            st += xchg[g2 * BM * 2 + row * 2 + 1] * fast_exp2(xchg[g2 * BM * 2 + row * 2] - mn);
           if (ra < a.n_q)
             a.out[(size_t)(l * a.Hq + hq_a) * a.n_q + ra] = (mn + fast_log2(st)) * kLn2;
         } else if (MODE == kMax) {
-          const float t2 = fmaxf(tot, xchg[row * 2]);
+          float t2 = tot;
+#pragma unroll
+          for (int g2 = 0; g2 < NG - 1; ++g2) t2 = fmaxf(t2, xchg[g2 * BM * 2 + row * 2]);
           if (ra < a.T) {
             float* o = a.out + (size_t)(l * a.Hkv + hk) * a.T + ra;
             *o = a.accumulate ? fmaxf(*o, t2) : t2;
           }
         } else {
-          if (ra < a.T) a.out[(size_t)(l * a.Hkv + hk) * a.T + ra] = f + xchg[row * 2];
+          float ft = f;
+#pragma unroll
+          for (int g2 = 0; g2 < NG - 1; ++g2) ft += xchg[g2 * BM * 2 + row * 2];
+          if (ra < a.T) a.out[(size_t)(l * a.Hkv + hk) * a.T + ra] = ft;
         }
       }
     }
@@ -686,7 +686,7 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   count_launches(1);
-  kern<<<grid, kThreads, C::SMEM, s>>>(ta, tb, tb2, a);
+  kern<<<grid, C::THREADS, C::SMEM, s>>>(ta, tb, tb2, a);
   return cudaGetLastError();
 }
 

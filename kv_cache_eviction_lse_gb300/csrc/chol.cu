@@ -17,7 +17,7 @@ __device__ int g_chol_error = 0;
 namespace {
 
 constexpr int NB = 16;
-constexpr int kThreads = 256;
+constexpr int kThreads = 1024;
 constexpr int kErrNotSpd = 6;  // a pivot of the factorisation was not positive
 
 // Upper-triangle index of micro-tile t among the n x n tiles with tj >= ti (row-major).
@@ -141,12 +141,24 @@ __global__ void __launch_bounds__(kThreads) chol_solve_kernel(const CholArgs a) 
 #pragma unroll
           for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(xi[u], xj[v], acc[u][v]);
       }
+      const bool full = i0 + 4 <= nrest && j0 + 4 <= nrest && tj > ti && ((p + nb + j0) & 3) == 0 &&
+                        (ld & 3) == 0;
+      if (full) {  // an off-diagonal micro-tile: four 16-byte read-modify-writes
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < 4; ++u) {
+          float4* gp = reinterpret_cast<float4*>(G + (size_t)(p + nb + i0 + u) * ld + p + nb + j0);
+          float4 g4 = *gp;
+          g4.x -= acc[u][0]; g4.y -= acc[u][1]; g4.z -= acc[u][2]; g4.w -= acc[u][3];
+          *gp = g4;
+        }
+      } else {
 #pragma unroll
-        for (int v = 0; v < 4; ++v)
-          if (i0 + u < nrest && j0 + v < nrest && j0 + v >= i0 + u)
-            G[(size_t)(p + nb + i0 + u) * ld + p + nb + j0 + v] -= acc[u][v];
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            if (i0 + u < nrest && j0 + v < nrest && j0 + v >= i0 + u)
+              G[(size_t)(p + nb + i0 + u) * ld + p + nb + j0 + v] -= acc[u][v];
+      }
     }
   }
   __syncthreads();
