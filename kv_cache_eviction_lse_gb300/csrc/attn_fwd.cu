@@ -8,11 +8,11 @@
 // 1. Key Terms], so that pruning pays only for pass 2 when the attention runs anyway.
 //
 // One CTA per 128 queries of one head; keys in tiles of 128 (online softmax):
-//   warp 0      TMA: the Q tile once, then K and V tiles through a 2-stage ring
+//   warp 0      TMA: the Q tile once, then K and V tiles through two 2-stage rings
 //   warp 1      owns TMEM (S double buffer: 2 x 128 columns; O: d columns) and issues
 //               S(j) = Q K(j)^T, then O += P(j-1) V(j-1) (P from shared memory,
 //               V as an MN-major operand straight from its TMA box)
-//   warps 2-9   softmax, two threads per query row (one per 64-key half): read S with
+//   warps 2-17  softmax, four threads per query row (one per 32-key quarter): read S with
 //               tcgen05.ld, agree on the row max through shared memory, p = 2^(x - m)
 //               with one ex2 each, write P (bf16, 128-byte swizzled K-major) for the
 //               MMA, and rescale O in TMEM when the running max grows by more than
@@ -35,7 +35,9 @@ namespace {
 
 constexpr int BM = 128;  // queries per CTA = TMEM lanes
 constexpr int BN = 128;  // keys per tile
-constexpr int kSoftThreads = 256;
+constexpr int NQ = 4;          // softmax threads per query row: one per 32-key quarter
+constexpr int KC = BN / NQ;    // keys per softmax thread and tile
+constexpr int kSoftThreads = NQ * 128;
 constexpr int kThreads = 64 + kSoftThreads;
 constexpr uint32_t kBox = 128 * 128;  // 128 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr uint32_t kTmemCols = 512;
@@ -50,12 +52,14 @@ struct FCfg {
   static constexpr uint32_t TILE = KH * kBox;  // one K or V tile, or the Q tile
   static constexpr uint32_t OFF_K = TILE;       // Q at 0
   static constexpr uint32_t OFF_V = OFF_K + 2 * TILE;
-  static constexpr uint32_t OFF_P = OFF_V + 2 * TILE;  // P: 2 boxes of 64 keys
-  static constexpr uint32_t OFF_XM = OFF_P + 2 * kBox;  // row max exchange [2][2][BM]
-  static constexpr uint32_t OFF_XL = OFF_XM + 4 * BM * 4;  // row sum exchange [2][BM]
-  static constexpr uint32_t OFF_BAR = OFF_XL + 2 * BM * 4;
-  // q_full, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full, o_ready, done
-  static constexpr uint32_t NBAR = 12;
+  // separate K and V rings: K(j) is released as soon as S(j) = Q K(j)^T is done, so the
+  // load of K(j+2) overlaps the softmax and P V of tile j; V(j) is held until P V(j)
+  static constexpr uint32_t OFF_P = OFF_V + 2 * TILE;      // P: 2 boxes of 64 keys
+  static constexpr uint32_t OFF_XM = OFF_P + 2 * kBox;     // row max exchange [2][NQ][BM]
+  static constexpr uint32_t OFF_XL = OFF_XM + 2 * NQ * BM * 4;  // row sum exchange [NQ][BM]
+  static constexpr uint32_t OFF_BAR = OFF_XL + NQ * BM * 4;
+  // q, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p, o, done
+  static constexpr uint32_t NBAR = 16;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t USED = OFF_MISC + 16;
   static constexpr uint32_t SMEM = (USED + 1024 <= kMaxSmem) ? USED + 1024 : kMaxSmem;
@@ -96,13 +100,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* xl = reinterpret_cast<float*>(smem + C::OFF_XL);
   const uint32_t bar0 = sb + C::OFF_BAR;
   const uint32_t bar_q = bar0;
-  auto bar_kvfull = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto bar_kvempty = [&](int s) { return bar0 + 8u * (3 + s); };
-  auto bar_sfull = [&](int s) { return bar0 + 8u * (5 + s); };
-  auto bar_sempty = [&](int s) { return bar0 + 8u * (7 + s); };
-  const uint32_t bar_p = bar0 + 8u * 9;
-  const uint32_t bar_o = bar0 + 8u * 10;
-  const uint32_t bar_done = bar0 + 8u * 11;
+  auto bar_kfull = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto bar_kempty = [&](int s) { return bar0 + 8u * (3 + s); };
+  auto bar_vfull = [&](int s) { return bar0 + 8u * (5 + s); };
+  auto bar_vempty = [&](int s) { return bar0 + 8u * (7 + s); };
+  auto bar_sfull = [&](int s) { return bar0 + 8u * (9 + s); };
+  auto bar_sempty = [&](int s) { return bar0 + 8u * (11 + s); };
+  const uint32_t bar_p = bar0 + 8u * 13;
+  const uint32_t bar_o = bar0 + 8u * 14;
+  const uint32_t bar_done = bar0 + 8u * 15;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
 
@@ -121,8 +127,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     tc::mbar_init(bar_q, 1);
     for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(bar_kvfull(s), 1);
-      tc::mbar_init(bar_kvempty(s), 1);
+      tc::mbar_init(bar_kfull(s), 1);
+      tc::mbar_init(bar_kempty(s), 1);
+      tc::mbar_init(bar_vfull(s), 1);
+      tc::mbar_init(bar_vempty(s), 1);
       tc::mbar_init(bar_sfull(s), 1);
       tc::mbar_init(bar_sempty(s), kSoftThreads);
     }
@@ -153,30 +161,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kh = 0; kh < C::KH; ++kh)
         tc::tma_load_3d(sQ + kh * kBox, &tm_q, bar_q, kh * 64, row0, l * a.Hq + hq);
-      int j = 0;
-      bool ok = true;
-      for (; j < ntiles; ++j) {
+      // loads in the order the MMAs use them: K(0), K(1), V(0), K(2), V(1), ...
+      const int head = l * a.Hkv + hk;
+      auto load = [&](bool is_v, int j) -> bool {
         const int s = j & 1;
-        if (!tc::mbar_wait(bar_kvempty(s), ((j >> 1) & 1) ^ 1u) || *abort_flag) {
-          ok = false;
-          break;
-        }
+        const uint32_t empty = is_v ? bar_vempty(s) : bar_kempty(s);
+        if (!tc::mbar_wait(empty, ((j >> 1) & 1) ^ 1u) || *abort_flag) return false;
         const bool ctx = j < n_ctx;
-        const CUtensorMap* mk = ctx ? &tm_k : &tm_kt;
-        const CUtensorMap* mv = ctx ? &tm_v : &tm_vt;
+        const CUtensorMap* m = is_v ? (ctx ? &tm_v : &tm_vt) : (ctx ? &tm_k : &tm_kt);
         const int row = ctx ? j * BN : (j - n_ctx) * BN;
-        const int head = l * a.Hkv + hk;
-        tc::mbar_expect_tx(bar_kvfull(s), 2 * C::TILE);
+        const uint32_t full = is_v ? bar_vfull(s) : bar_kfull(s);
+        const uint32_t dst = (is_v ? sV : sK) + s * C::TILE;
+        tc::mbar_expect_tx(full, C::TILE);
 #pragma unroll
-        for (int kh = 0; kh < C::KH; ++kh) {
-          tc::tma_load_3d(sK + s * C::TILE + kh * kBox, mk, bar_kvfull(s), kh * 64, row, head);
-          tc::tma_load_3d(sV + s * C::TILE + kh * kBox, mv, bar_kvfull(s), kh * 64, row, head);
+        for (int kh = 0; kh < C::KH; ++kh) tc::tma_load_3d(dst + kh * kBox, m, full, kh * 64, row, head);
+        return true;
+      };
+      int nk = 0, nv = 0;  // loads issued
+      bool ok = true;
+      for (int t = 0; ok && t <= ntiles; ++t) {
+        if (t < ntiles) {
+          ok = load(false, t);
+          if (ok) ++nk;
+        }
+        if (ok && t >= 1) {
+          ok = load(true, t - 1);
+          if (ok) ++nv;
         }
       }
       if (!ok) {
         fail(abort_flag, kErrWaitTimeout);
+        // let the copies already in flight land before the CTA exits
         tc::mbar_wait(bar_q, 0);
-        for (int i = max(0, j - 2); i < j; ++i) tc::mbar_wait(bar_kvfull(i & 1), (i >> 1) & 1);
+        for (int i = max(0, nk - 2); i < nk; ++i) tc::mbar_wait(bar_kfull(i & 1), (i >> 1) & 1);
+        for (int i = max(0, nv - 2); i < nv; ++i) tc::mbar_wait(bar_vfull(i & 1), (i >> 1) & 1);
       }
     }
   } else if (warp == 1) {
@@ -190,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j < ntiles) {  // S(j) = Q K(j)^T
           const int s = j & 1;
           const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-          if (!tc::mbar_wait(bar_kvfull(s), ph) || !tc::mbar_wait(bar_sempty(s), ph ^ 1u) ||
+          if (!tc::mbar_wait(bar_kfull(s), ph) || !tc::mbar_wait(bar_sempty(s), ph ^ 1u) ||
               *abort_flag) {
             ok = false;
             break;
@@ -205,11 +223,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                          k > 0 ? 1u : 0u);
           }
           tc::commit(bar_sfull(s));
+          tc::commit(bar_kempty(s));
           ++issued;
         }
         if (j >= 1) {  // O += P(j-1) V(j-1)
           const int jj = j - 1, s = jj & 1;
-          if (!tc::mbar_wait(bar_p, (uint32_t)jj & 1u) || *abort_flag) {
+          if (!tc::mbar_wait(bar_p, (uint32_t)jj & 1u) ||
+              !tc::mbar_wait(bar_vfull(s), (uint32_t)(jj >> 1) & 1u) || *abort_flag) {
             ok = false;
             break;
           }
@@ -221,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_bf16(t_o, tc::sdesc_sw128(pa), tc::sdesc_sw128_mn(v_s + 2048u * k, kBox),
                          idesc_o, (jj > 0 || k > 0) ? 1u : 0u);
           }
-          tc::commit(bar_kvempty(s));
+          tc::commit(bar_vempty(s));
           tc::commit(bar_o);
           ++issued;
         }
@@ -236,45 +256,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ============================================================ softmax + epilogue
-    const int h = (warp - 2) >> 2;      // 64-key half of each tile (and D/2 half of O)
+    constexpr int OC = D / NQ;          // O columns of this thread in the rescale / epilogue
+    const int h = (warp - 2) >> 2;      // 32-key quarter of each tile (and D/4 of O)
     const int eq = warp & 3;            // TMEM lane quarter
     const int row = eq * 32 + lane;     // query row within the tile
     const int qr = row0 + row;          // query index
     const uint32_t lane_off = (uint32_t)(eq * 32) << 16;
     const float sc2 = rsqrtf((float)D) * kLog2e;
     float m_used = -1e30f, lsum = 0.f;
-    bool failed = false;
+    bool failed = false, wait_failed = false;
     for (int j = 0; j < ntiles; ++j) {
       const int s = j & 1;
       bool ok = tc::mbar_wait(bar_sfull(s), (uint32_t)(j >> 1) & 1u) && !*abort_flag;
-      if (tc::bar_or(2, kSoftThreads, !ok)) {
+      if (tc::bar_or(2, kSoftThreads, !ok || wait_failed)) {
         failed = true;
         break;
       }
       tc::fence_after_sync();
-      uint32_t v[64];
-      const uint32_t ts = tmem + lane_off + (uint32_t)(s * BN + h * 64);
-      tc::tmem_ld32(ts, v);
-      tc::tmem_ld32(ts + 32, v + 32);
+      uint32_t v[KC];
+      tc::tmem_ld32(tmem + lane_off + (uint32_t)(s * BN + h * KC), v);
       tc::tmem_ld_wait();
       tc::fence_before_sync();
       tc::mbar_arrive(bar_sempty(s));
 
       const bool ctx = j < n_ctx;
-      const int kb = (ctx ? j * BN : a.T + (j - n_ctx) * BN) + h * 64;
+      const int kb = (ctx ? j * BN : a.T + (j - n_ctx) * BN) + h * KC;
       const int lim = ctx ? a.T : n_k;
-      if (kb + 64 > lim || kb + 63 > off + qr) {
+      if (kb + KC > lim || kb + KC - 1 > off + qr) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < KC; ++c)
           if (kb + c >= lim || kb + c > off + qr) v[c] = __float_as_uint(-CUDART_INF_F);
       }
-      float mx = -CUDART_INF_F;
+      float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(v[c]));
-      float* xmj = xm + s * 2 * BM;
-      xmj[h * BM + row] = mx * sc2;
+      for (int c = 0; c < KC; c += 2) {
+        mx0 = fmaxf(mx0, __uint_as_float(v[c]));
+        mx1 = fmaxf(mx1, __uint_as_float(v[c + 1]));
+      }
+      const float mine = fmaxf(mx0, mx1) * sc2;
+      float* xmj = xm + s * NQ * BM;
+      xmj[h * BM + row] = mine;
       named_sync(1, kSoftThreads);
-      const float mt = fmaxf(mx * sc2, xmj[(1 - h) * BM + row]);
+      float mt = mine;
+#pragma unroll
+      for (int g = 1; g < NQ; ++g) mt = fmaxf(mt, xmj[((h + g) % NQ) * BM + row]);
       const bool need = mt > m_used + kRescale;
       float factor = 1.f;
       if (need) {
@@ -282,42 +307,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = mt;
         lsum *= factor;
       }
-      uint32_t pk[32];
-      float ps = 0.f;
+      uint32_t pk[KC / 2];
+      float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
+      for (int c = 0; c < KC; c += 2) {
         const float p0 = fast_exp2(fmaf(__uint_as_float(v[c]), sc2, -m_used));
         const float p1 = fast_exp2(fmaf(__uint_as_float(v[c + 1]), sc2, -m_used));
-        ps += p0 + p1;
+        ps0 += p0;
+        ps1 += p1;
         pk[c / 2] = pack_bf16(p0, p1);
       }
-      lsum += ps;
+      lsum += ps0 + ps1;
 
-      if (j > 0) {  // O and the P buffer are free once O += P(j-1) V(j-1) has completed
+      // the P buffer and O are free once O += P(j-1) V(j-1) has completed; O is rescaled
+      // only when this row's max grew past the threshold
+      if (j > 0) {
         ok = tc::mbar_wait(bar_o, (uint32_t)(j - 1) & 1u) && !*abort_flag;
-        if (tc::bar_or(2, kSoftThreads, !ok)) {
-          failed = true;
-          break;
-        }
+        if (!ok) wait_failed = true;  // reported at the next vote
         tc::fence_after_sync();
-        if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-          for (int cb = 0; cb < D / 64; ++cb) {
-            const uint32_t to = t_o + lane_off + (uint32_t)(h * (D / 2) + 32 * cb);
+        if (ok && __any_sync(0xffffffffu, need)) {
+          const uint32_t to = t_o + lane_off + (uint32_t)(h * OC);
+          if constexpr (OC == 32) {
             tc::tmem_ld32(to, v);
             tc::tmem_ld_wait();
 #pragma unroll
             for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * factor);
             tc::tmem_st32(to, v);
+          } else {
+            tc::tmem_ld16(to, v);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * factor);
+            tc::tmem_st16(to, v);
           }
           tc::tmem_st_wait();
         }
       }
-      // P row half: keys h*64 .. h*64+63 = box h, 8 chunks of 16 B, 128-byte swizzle
-      uint8_t* prow = smem + C::OFF_P + h * kBox + row * 128;
+      // P row quarter: keys h*32 .. h*32+31 = chunks 4(h&1) .. 4(h&1)+3 of box h/2
+      uint8_t* prow = smem + C::OFF_P + (h >> 1) * kBox + row * 128;
+      tc::fence_proxy_async_smem();  // the tensor core's reads of this buffer came before
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        uint4 u = make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const int c8 = 4 * (h & 1) + c4;
+        uint4 u = make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
         *reinterpret_cast<uint4*>(prow + ((c8 ^ (row & 7)) << 4)) = u;
       }
       tc::fence_proxy_async_smem();
@@ -326,29 +358,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!failed && ntiles > 0) {
       const bool ok = tc::mbar_wait(bar_o, (uint32_t)(ntiles - 1) & 1u) && !*abort_flag;
-      failed = tc::bar_or(2, kSoftThreads, !ok);
+      failed = tc::bar_or(2, kSoftThreads, !ok || wait_failed);
       if (!failed) {
         tc::fence_after_sync();
         xl[h * BM + row] = lsum;
         named_sync(1, kSoftThreads);
-        const float ltot = lsum + xl[(1 - h) * BM + row];
+        float ltot = lsum;
+#pragma unroll
+        for (int g = 1; g < NQ; ++g) ltot += xl[((h + g) % NQ) * BM + row];
         const float inv = 1.f / ltot;
-        uint32_t v[32];
-        uint32_t ob[D / 4];
+        uint32_t v[OC];
+        uint32_t ob[OC / 2];
+        if constexpr (OC == 32)
+          tc::tmem_ld32(t_o + lane_off + (uint32_t)(h * OC), v);
+        else
+          tc::tmem_ld16(t_o + lane_off + (uint32_t)(h * OC), v);
+        tc::tmem_ld_wait();
 #pragma unroll
-        for (int cb = 0; cb < D / 64; ++cb) {
-          tc::tmem_ld32(t_o + lane_off + (uint32_t)(h * (D / 2) + 32 * cb), v);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 32; c += 2)
-            ob[cb * 16 + c / 2] =
-                pack_bf16(__uint_as_float(v[c]) * inv, __uint_as_float(v[c + 1]) * inv);
-        }
+        for (int c = 0; c < OC; c += 2)
+          ob[c / 2] = pack_bf16(__uint_as_float(v[c]) * inv, __uint_as_float(v[c + 1]) * inv);
         if (qr < a.n_q) {
           uint4* dst = reinterpret_cast<uint4*>(
-              a.o + ((size_t)(l * a.Hq + hq) * a.n_q + qr) * D + h * (D / 2));
+              a.o + ((size_t)(l * a.Hq + hq) * a.n_q + qr) * D + h * OC);
 #pragma unroll
-          for (int c = 0; c < D / 16; ++c)
+          for (int c = 0; c < OC / 8; ++c)
             dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
           if (h == 0) a.lse[(size_t)(l * a.Hq + hq) * a.n_q + qr] = (m_used + fast_log2(ltot)) * kLn2;
         }
