@@ -12,7 +12,7 @@
 //   warp 1      owns TMEM (S double buffer: 2 x 128 columns; O: d columns) and issues
 //               S(j) = Q K(j)^T, then O += P(j-1) V(j-1) (P from shared memory,
 //               V as an MN-major operand straight from its TMA box)
-//   warps 2-17  softmax, four threads per query row (one per 32-key quarter): read S with
+//   warps 2-9   softmax, two threads per query row (one per 64-key half): read S with
 //               tcgen05.ld, agree on the row max through shared memory, p = 2^(x - m)
 //               with one ex2 each, write P (bf16, 128-byte swizzled K-major) for the
 //               MMA, and rescale O in TMEM when the running max grows by more than
@@ -35,7 +35,7 @@ namespace {
 
 constexpr int BM = 128;  // queries per CTA = TMEM lanes
 constexpr int BN = 128;  // keys per tile
-constexpr int NQ = 4;          // softmax threads per query row: one per 32-key quarter
+constexpr int NQ = 2;          // softmax threads per query row, each on BN / NQ keys
 constexpr int KC = BN / NQ;    // keys per softmax thread and tile
 constexpr int kSoftThreads = NQ * 128;
 constexpr int kThreads = 64 + kSoftThreads;
@@ -274,7 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::fence_after_sync();
       uint32_t v[KC];
-      tc::tmem_ld32(tmem + lane_off + (uint32_t)(s * BN + h * KC), v);
+#pragma unroll
+      for (int c = 0; c < KC; c += 32) tc::tmem_ld32(tmem + lane_off + (uint32_t)(s * BN + h * KC + c), v + c);
       tc::tmem_ld_wait();
       tc::fence_before_sync();
       tc::mbar_arrive(bar_sempty(s));
@@ -327,12 +328,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         if (ok && __any_sync(0xffffffffu, need)) {
           const uint32_t to = t_o + lane_off + (uint32_t)(h * OC);
-          if constexpr (OC == 32) {
-            tc::tmem_ld32(to, v);
-            tc::tmem_ld_wait();
+          if constexpr (OC >= 32) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * factor);
-            tc::tmem_st32(to, v);
+            for (int cb = 0; cb < OC; cb += 32) {
+              tc::tmem_ld32(to + cb, v);
+              tc::tmem_ld_wait();
+#pragma unroll
+              for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * factor);
+              tc::tmem_st32(to + cb, v);
+            }
           } else {
             tc::tmem_ld16(to, v);
             tc::tmem_ld_wait();
@@ -343,12 +347,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_st_wait();
         }
       }
-      // P row quarter: keys h*32 .. h*32+31 = chunks 4(h&1) .. 4(h&1)+3 of box h/2
-      uint8_t* prow = smem + C::OFF_P + (h >> 1) * kBox + row * 128;
+      // this thread's keys h*KC .. h*KC+KC-1: 16-byte chunks of 8 keys in box (h KC)/64,
+      // 128-byte swizzle
+      uint8_t* prow = smem + C::OFF_P + (h * KC / 64) * kBox + row * 128;
       tc::fence_proxy_async_smem();  // the tensor core's reads of this buffer came before
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        const int c8 = 4 * (h & 1) + c4;
+      for (int c4 = 0; c4 < KC / 8; ++c4) {
+        const int c8 = (h * KC % 64) / 8 + c4;
         uint4 u = make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
         *reinterpret_cast<uint4*>(prow + ((c8 ^ (row & 7)) << 4)) = u;
       }
@@ -369,10 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv = 1.f / ltot;
         uint32_t v[OC];
         uint32_t ob[OC / 2];
-        if constexpr (OC == 32)
-          tc::tmem_ld32(t_o + lane_off + (uint32_t)(h * OC), v);
-        else
+        if constexpr (OC >= 32) {
+#pragma unroll
+          for (int cb = 0; cb < OC; cb += 32) tc::tmem_ld32(t_o + lane_off + (uint32_t)(h * OC + cb), v + cb);
+        } else {
           tc::tmem_ld16(t_o + lane_off + (uint32_t)(h * OC), v);
+        }
         tc::tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < OC; c += 2)
