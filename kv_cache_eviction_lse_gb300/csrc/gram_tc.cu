@@ -9,9 +9,11 @@
 // Both operands are read MN-major straight from their row-major [rows][cols] storage:
 // a TMA box of 64 rows x 64 columns is one 128-byte-swizzled MN-major atom column, so
 // a 128-column tile is two boxes (leading byte offset 8 KB) and each MMA takes 16 rows.
-// One CTA per 128 x 128 output tile; warp 0 streams 64-row k-blocks through a 3-stage
-// ring, warp 1 issues the MMAs into one TMEM accumulator, warps 2-5 write the tile.
+// One CTA per 128 x 128 output tile; warp 0 streams 64-row k-blocks through a ring of 3
+// to 12 stages (as many as the operand tiles a product needs allow), warp 1 issues the
+// MMAs into one TMEM accumulator, warps 2-5 write the tile.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
 #include "gram.cuh"
@@ -27,14 +29,15 @@ constexpr int BT = 128;                 // output tile edge
 constexpr int BK = 64;                  // rows per k-block
 constexpr uint32_t kBox = 64 * 128;     // 64 rows x 64 bf16 = 8 KB
 constexpr uint32_t kOp = 2 * kBox;      // one 128-column operand tile of a k-block
-constexpr int kStages = 3;
-constexpr uint32_t kStage = 4 * kOp;    // X hi, X lo, Y hi, Y lo
+constexpr uint32_t kRing = 3 * 4 * kOp;  // operand ring: 192 KB
+constexpr int kMaxStages = 12;          // stages of (X hi, [X lo], [Y hi], [Y lo]) tiles
 constexpr int kThreads = 64 + 128;
 constexpr uint32_t kTmemCols = 128;
-constexpr uint32_t OFF_BAR = kStages * kStage;
-constexpr uint32_t NBAR = 2 * kStages + 1;  // full[S], empty[S], done
+constexpr uint32_t OFF_BAR = kRing;
+constexpr uint32_t NBAR = 2 * kMaxStages + 1;  // full[S], empty[S], done
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr uint32_t USED = OFF_MISC + 16;
+static_assert(kRing % (4 * kOp) == 0 && kRing / kOp <= 3 * 4, "operand ring");
 constexpr uint32_t SMEM = USED + 1024;
 static_assert(SMEM <= 232448, "shared-memory plan exceeds the per-block limit");
 constexpr int kErrWaitTimeout = 1;
@@ -55,14 +58,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sb = raw + pad;
   const uint32_t bar0 = sb + OFF_BAR;
   auto bar_full = [&](int s) { return bar0 + 8u * s; };
-  auto bar_empty = [&](int s) { return bar0 + 8u * (kStages + s); };
-  const uint32_t bar_done = bar0 + 8u * (2 * kStages);
+  auto bar_empty = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
+  const uint32_t bar_done = bar0 + 8u * (2 * kMaxStages);
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // output tile: the upper block triangle when Y is X (symmetric result)
+  const bool diag = a.pair != nullptr;  // Y == X, diagonal tiles, bf16 pairs out
   int tm, tn;
-  if (a.upper) {
+  if (diag) {
+    tm = tn = blockIdx.x;
+  } else if (a.upper) {
     int t = blockIdx.x, row = 0, nt = (a.M + BT - 1) / BT;
     while (t >= nt - row) {
       t -= nt - row;
@@ -76,11 +82,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int b = blockIdx.y;
   const int nkb = (a.rows + BK - 1) / BK;
-  const bool y_split = a.y_lo != nullptr;
-  const uint32_t stage_bytes = (y_split ? 4 : 3) * kOp;
+  const bool y_split = a.y_lo != nullptr, x_split = a.x_lo != nullptr;
+  // a stage holds only the operand tiles this product needs, so fewer operands mean a
+  // deeper ring (3 stages for the split Gram, up to 12 for the value-norm Gram)
+  const int nop = 1 + (x_split ? 1 : 0) + (diag ? 0 : 1) + (y_split ? 1 : 0);
+  const uint32_t stage_bytes = nop * kOp;
+  const int kStages = min(kMaxStages, (int)(kRing / stage_bytes));
+  const uint32_t o_xlo = kOp, o_yhi = (1 + (x_split ? 1 : 0)) * kOp, o_ylo = o_yhi + kOp;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kMaxStages; ++s) {
       tc::mbar_init(bar_full(s), 1);
       tc::mbar_init(bar_empty(s), 1);
     }
@@ -105,15 +116,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const uint32_t st = sb + s * kStage;
+        const uint32_t st = sb + s * stage_bytes;
         tc::mbar_expect_tx(bar_full(s), stage_bytes);
         for (int c = 0; c < 2; ++c) {  // two 64-column boxes per operand tile
           tc::tma_load_3d(st + c * kBox, &tm_xhi, bar_full(s), tm * BT + 64 * c, kb * BK, b);
-          tc::tma_load_3d(st + kOp + c * kBox, &tm_xlo, bar_full(s), tm * BT + 64 * c, kb * BK, b);
-          tc::tma_load_3d(st + 2 * kOp + c * kBox, &tm_yhi, bar_full(s), tn * BT + 64 * c, kb * BK,
-                          b);
+          if (x_split)
+            tc::tma_load_3d(st + o_xlo + c * kBox, &tm_xlo, bar_full(s), tm * BT + 64 * c,
+                            kb * BK, b);
+          if (!diag)
+            tc::tma_load_3d(st + o_yhi + c * kBox, &tm_yhi, bar_full(s), tn * BT + 64 * c,
+                            kb * BK, b);
           if (y_split)
-            tc::tma_load_3d(st + 3 * kOp + c * kBox, &tm_ylo, bar_full(s), tn * BT + 64 * c,
+            tc::tma_load_3d(st + o_ylo + c * kBox, &tm_ylo, bar_full(s), tn * BT + 64 * c,
                             kb * BK, b);
         }
       }
@@ -135,15 +149,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc::fence_after_sync();
-        const uint32_t st = sb + s * kStage;
+        const uint32_t st = sb + s * stage_bytes;
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k) {
           const uint32_t o = 2048u * k;  // 16 rows of 128 bytes
-          const uint64_t xh = tc::sdesc_sw128_mn(st + o, kBox), xl = tc::sdesc_sw128_mn(st + kOp + o, kBox);
-          const uint64_t yh = tc::sdesc_sw128_mn(st + 2 * kOp + o, kBox);
+          const uint64_t xh = tc::sdesc_sw128_mn(st + o, kBox), xl = tc::sdesc_sw128_mn(st + o_xlo + o, kBox);
+          const uint64_t yh = diag ? xh : tc::sdesc_sw128_mn(st + o_yhi + o, kBox);
           tc::mma_bf16(tmem, xh, yh, idesc, (kb | k) != 0 ? 1u : 0u);
-          tc::mma_bf16(tmem, xl, yh, idesc, 1u);
-          if (y_split) tc::mma_bf16(tmem, xh, tc::sdesc_sw128_mn(st + 3 * kOp + o, kBox), idesc, 1u);
+          if (x_split) tc::mma_bf16(tmem, xl, yh, idesc, 1u);
+          if (y_split) tc::mma_bf16(tmem, xh, tc::sdesc_sw128_mn(st + o_ylo + o, kBox), idesc, 1u);
         }
         tc::commit(bar_empty(s));
       }
@@ -159,6 +173,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool ok = tc::mbar_wait(bar_done, 0);
     if (!ok) atomicCAS(&g_gram_error, 0, kErrWaitTimeout);
     tc::fence_after_sync();
+    if (diag) {
+      // row m of the tile belongs to slice (head) r = m_local / d; write that slice's row
+      // of its d x d Gram block as bf16 hi and lo parts
+      const int dd = a.pair_d, ml = eq * 32 + lane, r = ml / dd, i = ml % dd;
+      const int head = (tm * BT) / dd + r, nheads = a.M / dd;
+      bf16_t* gh = a.pair + (((size_t)b * nheads + head) * 2 * dd + i) * dd;
+#pragma unroll
+      for (int cb = 0; cb < BT / 32; ++cb) {
+        uint32_t v[32];
+        tc::tmem_ld32(tmem + ((uint32_t)(eq * 32) << 16) + 32u * cb, v);
+        tc::tmem_ld_wait();
+        const int c0 = 32 * cb - r * dd;  // column within the slice
+        if (ok && head < nheads && c0 >= 0 && c0 < dd) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float x0 = __uint_as_float(v[c + 2 * e]), x1 = __uint_as_float(v[c + 2 * e + 1]);
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+              hi[e] = *reinterpret_cast<uint32_t*>(&h2);
+              __nv_bfloat162 l2 = __floats2bfloat162_rn(x0 - __low2float(h2), x1 - __high2float(h2));
+              lo[e] = *reinterpret_cast<uint32_t*>(&l2);
+            }
+            *reinterpret_cast<uint4*>(gh + c0 + c) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(gh + (size_t)dd * dd + c0 + c) =
+                make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
+        }
+      }
+    } else {
     float* crow = a.c + ((size_t)b * a.M + m) * a.ldc + tn * BT;
     const int nmax = min(BT, a.N - tn * BT);
 #pragma unroll
@@ -178,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    }
   }
   __syncthreads();
   if (warp == 1) {
@@ -190,17 +236,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_gram(const GramArgs& a, cudaStream_t s) {
   if (a.M <= 0 || a.N <= 0 || a.batch <= 0) return cudaSuccess;
-  if (a.upper && a.M != a.N) return cudaErrorInvalidValue;
-  if (a.ldx % 8 || a.ldy % 8 || a.ldc % 4) return cudaErrorInvalidValue;
+  const bool diag = a.pair != nullptr;
+  if ((a.upper || diag) && a.M != a.N) return cudaErrorInvalidValue;
+  if (diag && (a.pair_d <= 0 || BT % a.pair_d || a.M % a.pair_d || a.pair_d % 8))
+    return cudaErrorInvalidValue;
+  if (a.ldx % 8 || a.ldy % 8 || (!diag && a.ldc % 4)) return cudaErrorInvalidValue;
   CUtensorMap xh, xl, yh, yl;
   cudaError_t e = tma_map_bf16_3d(&xh, a.x_hi, a.ldx, a.rows, a.batch, BK);
-  if (e == cudaSuccess) e = tma_map_bf16_3d(&xl, a.x_lo, a.ldx, a.rows, a.batch, BK);
+  if (e == cudaSuccess)
+    e = tma_map_bf16_3d(&xl, a.x_lo ? a.x_lo : a.x_hi, a.ldx, a.rows, a.batch, BK);
   if (e == cudaSuccess) e = tma_map_bf16_3d(&yh, a.y_hi, a.ldy, a.rows, a.batch, BK);
   if (e == cudaSuccess)
     e = tma_map_bf16_3d(&yl, a.y_lo ? a.y_lo : a.y_hi, a.ldy, a.rows, a.batch, BK);
   if (e != cudaSuccess) return e;
   const int tmn = (a.M + BT - 1) / BT, tnn = (a.N + BT - 1) / BT;
-  const int tiles = a.upper ? tmn * (tmn + 1) / 2 : tmn * tnn;
+  const int tiles = diag ? tmn : a.upper ? tmn * (tmn + 1) / 2 : tmn * tnn;
   e = cudaFuncSetAttribute(gram_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
   if (e != cudaSuccess) return e;
   count_launches(1);
