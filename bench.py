@@ -82,6 +82,8 @@ def parse_args():
     ap.add_argument("--e2e-groups", type=int, default=4,
                     help="layer groups of the end-to-end run: copies of one group overlap the "
                          "kernels of the previous one (1: copy everything, then compute)")
+    ap.add_argument("--e2e-copy-streams", type=int, default=1,
+                    help="streams the host-to-device copies of a layer group are spread over")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--stage-reps", type=int, default=None)
@@ -407,7 +409,8 @@ def run_gpu(args, rank, world, local):
             return pg
         groups = 1 if wl.kind == "decode" else min(args.e2e_groups, p.L)
         e2e = run_e2e(wl, x, p, dev, K=min(K, 20), units=world * units_per_step(wl, p), world=world,
-                      flush=flush, graph=not args.no_graph, groups=groups, make_group=make_group)
+                      flush=flush, graph=not args.no_graph, groups=groups, make_group=make_group,
+                      copy_streams=args.e2e_copy_streams)
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -469,7 +472,8 @@ def _step_outputs(p):
     return outs
 
 
-def run_e2e(wl, x, p, dev, K, units, world, flush, graph=True, groups=1, make_group=None):
+def run_e2e(wl, x, p, dev, K, units, world, flush, graph=True, groups=1, make_group=None,
+            copy_streams=1):
     """Same step through the same calls, inputs from pinned host memory: the H2D copies
     of every input and the D2H read of the results are inside the timed region.
 
@@ -509,24 +513,30 @@ def run_e2e(wl, x, p, dev, K, units, world, flush, graph=True, groups=1, make_gr
     bi = sum(h.numel() * h.element_size() for pr in parts for h, _ in pr[0])
     bo = sum(o.numel() * o.element_size() for pr in parts for o in pr[2])
     stream = torch.cuda.current_stream()
-    copy_stream = torch.cuda.Stream() if groups > 1 else stream
+    nstreams = max(1, copy_streams) if groups > 1 else 1
+    copy_ss = [torch.cuda.Stream() for _ in range(nstreams)] if groups > 1 else [stream]
     tot = 0.0
     for i in range(K + 2):
         flush.fill_(float(i))
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        copy_stream.wait_event(a)
+        for cs in copy_ss:
+            cs.wait_event(a)
         ready = []
         for pairs, _, _, _ in parts:
-            with torch.cuda.stream(copy_stream):
-                for h, d in pairs:
-                    d.copy_(h, non_blocking=True)
-            ev = torch.cuda.Event()
-            ev.record(copy_stream)
-            ready.append(ev)
-        for (pairs, step_fn, outs, outs_h), ev in zip(parts, ready):
-            stream.wait_event(ev)
+            evs = []
+            for j, cs in enumerate(copy_ss):  # a group's tensors, spread over the copy streams
+                with torch.cuda.stream(cs):
+                    for h, d in pairs[j::len(copy_ss)]:
+                        d.copy_(h, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cs)
+                evs.append(ev)
+            ready.append(evs)
+        for (pairs, step_fn, outs, outs_h), evs in zip(parts, ready):
+            for ev in evs:
+                stream.wait_event(ev)
             step_fn()
             for o, oh in zip(outs, outs_h):
                 oh.copy_(o, non_blocking=True)
@@ -539,8 +549,8 @@ def run_e2e(wl, x, p, dev, K, units, world, flush, graph=True, groups=1, make_gr
     out = {"value": round(units / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
     if groups > 1:
-        out["overlap"] = (f"layers in {groups} groups: the H2D copies of group g+1 overlap "
-                          f"the kernels of group g")
+        out["overlap"] = (f"layers in {groups} groups: the H2D copies of group g+1 (on "
+                          f"{len(copy_ss)} copy streams) overlap the kernels of group g")
     return out
 
 
