@@ -481,10 +481,21 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
       for (int it = 0; it < U.ntiles && !bad; ++it, ++gt) {
         const int acc = gt & 1;
         const uint32_t aph = (uint32_t)(gt >> 1) & 1u;
-        const bool ok = tc::mbar_wait(bar_tfull(acc), aph) && !*abort_flag;
-        if (tc::bar_or(bar_id, kGroupThreads, !ok)) {
-          bad = true;
-          break;
+        if constexpr (kCols) {
+          // the group barrier also orders the shared per-column constants (below)
+          const bool ok = tc::mbar_wait(bar_tfull(acc), aph) && !*abort_flag;
+          if (tc::bar_or(bar_id, kGroupThreads, !ok)) {
+            bad = true;
+            break;
+          }
+        } else {
+          // no shared state per tile: a wait that runs out raises the CTA's abort flag, so
+          // every other thread leaves at its next wait and all meet at the end-of-unit vote
+          if (!tc::mbar_wait(bar_tfull(acc), aph) || *abort_flag) {
+            *abort_flag = 1u;
+            bad = true;
+            break;
+          }
         }
         tc::fence_after_sync();
         if constexpr (MODE == kQuad) {
