@@ -128,8 +128,8 @@ kvs_status kvs_lse(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q, const k
 }
 
 size_t kvs_score_max_workspace_size(const kvs_dims* dims, int32_t n_q, int32_t with_h) {
-  if (!dims || !with_h || n_q <= 0 || dims->L <= 0) return 0;
-  return (size_t)dims->L * n_q * sizeof(float);
+  if (!dims || n_q <= 0 || dims->L <= 0 || dims->H_q <= 0) return 0;
+  return kvs::score_max_ws_bytes(dims->L, dims->H_q, n_q, with_h != 0);
 }
 
 kvs_status kvs_attn_fwd(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
@@ -180,22 +180,35 @@ kvs_status kvs_score_max(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
   if (h) {
     REQUIRE(dims->D_h > 0 && dims->D_h % 8 == 0, KVS_ERR_SHAPE,
             "kvs_score_max: D_h = %d must be a positive multiple of 8 when h is given", dims->D_h);
-    const size_t need = kvs_score_max_workspace_size(dims, n_q, 1);
-    REQUIRE(ws || need == 0, KVS_ERR_ARG, "kvs_score_max: workspace is NULL");
+  }
+  const size_t need = kvs_score_max_workspace_size(dims, n_q, h != nullptr);
+  if (n_q > 0) {
+    REQUIRE_PTR(ws);
     REQUIRE(ws_bytes >= need, KVS_ERR_CAPACITY,
             "kvs_score_max: workspace of %zu bytes, %zu needed", ws_bytes, need);
-    REQUIRE_OPT_PTR(ws);
   }
   cudaStream_t s = as_stream(stream);
   kvs::AttnArgs a;
   a.q = q; a.k_ctx = k_ctx; a.lse = lse; a.vnorm = vnorm; a.out = log_score;
   a.L = dims->L; a.Hq = dims->H_q; a.Hkv = dims->H_kv; a.d = dims->d;
   a.n_q = n_q; a.T = T; a.accumulate = accumulate != 0;
-  if (h && n_q > 0) {
-    float* hlog = static_cast<float*>(ws);
-    cudaError_t e = kvs::launch_hidden_log_norm(h, dims->L, n_q, dims->D_h, hlog, s);
-    if (e != cudaSuccess) return cuda_status(e, "kvs_score_max (hidden norm)");
-    a.hlog = hlog;
+  if (n_q > 0) {
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    float* hlog = nullptr;
+    size_t off = 0;
+    if (h) {
+      hlog = reinterpret_cast<float*>(w);
+      cudaError_t e = kvs::launch_hidden_log_norm(h, dims->L, n_q, dims->D_h, hlog, s);
+      if (e != cudaSuccess) return cuda_status(e, "kvs_score_max (hidden norm)");
+      off = kvs::score_max_ccol_offset(dims->L, n_q);
+    }
+    auto* ccol = reinterpret_cast<kvs::bf16_t*>(w + off);
+    auto* ones = reinterpret_cast<kvs::bf16_t*>(w + need - 128 * 32);
+    cudaError_t e = kvs::launch_score_constants(lse, hlog, dims->L, dims->H_q, n_q, dims->d, ccol,
+                                                ones, s);
+    if (e != cudaSuccess) return cuda_status(e, "kvs_score_max (constants)");
+    a.ccol = ccol;
+    a.ones = ones;
   }
   return cuda_status(kvs::launch_score_max(a, s), "kvs_score_max");
 }

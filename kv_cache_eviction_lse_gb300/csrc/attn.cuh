@@ -24,7 +24,21 @@ struct AttnArgs {
   bf16_t* rows_hi = nullptr;       // softmax rows: [L][Hq][n_q][rows_ld] bf16 hi / lo parts
   bf16_t* rows_lo = nullptr;
   int rows_ld = 0;                 // padded row length (multiple of 64, >= T)
+  // KVzip max (pass 2): per-query constants -(lse_j + ln||h_j||) / sqrt(d), split into
+  // three bf16 parts [L][Hq][n_q_pad][16] (n_q_pad = n_q rounded up to 256; padding rows
+  // hold -1e30), and a [128][16] tile of (1, 1, 1, 0, ...) rows: one extra K = 16 MMA
+  // step adds the constant to every accumulator column
+  const bf16_t* ccol = nullptr;
+  const bf16_t* ones = nullptr;
 };
+
+// Score-max workspace layout (kvs_score_max): ln||h|| [L][n_q] fp32 (with h), then the
+// constants and the ones tile above.
+size_t score_max_ccol_offset(int L, int n_q);
+size_t score_max_ws_bytes(int L, int Hq, int n_q, bool with_h);
+// Writes the constants and the ones tile (lse, hlog optional) into the workspace.
+cudaError_t launch_score_constants(const float* lse, const float* hlog, int L, int Hq, int n_q,
+                                   int d, bf16_t* ccol, bf16_t* ones, cudaStream_t s);
 
 cudaError_t launch_lse(const AttnArgs& a, cudaStream_t s);
 // Softmax rows a_ji = exp(x_ji - lse_j) over the T context keys (lse given), written as

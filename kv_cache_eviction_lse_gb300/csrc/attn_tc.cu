@@ -19,7 +19,10 @@
 //   kLse     A = queries,  B = key tiles (context, then tail): online max and
 //            sum of 2^(x log2 e) per query -> ln sum exp(x)
 //   kMax     A = context keys, B = query tiles of every head of the group: per key
-//            max of x - lse_j - ln||h_j||, folded per head with ln ||W_O^{(h)} v_i||
+//            max of x - lse_j - ln||h_j||, folded per head with ln ||W_O^{(h)} v_i||; the
+//            per-query constant enters the accumulator through one extra K = 16 MMA
+//            step (a ones tile against the constant split into three bf16 parts), so
+//            the epilogue is a plain 3-input max
 //   kFuture  A = keys, B = query tiles j >= i0 + w: per key sum over the group of
 //            2^((x - lse_j) log2 e) for j >= i + w
 // Sources: KVpop review, 1. Key Terms (LSE reuse, transposed-attention pass);
@@ -73,7 +76,13 @@ struct Cfg {
   static constexpr uint32_t A_BYTES = KH * kBoxBytesA;  // one of kUnits A buffers
   static constexpr uint32_t B_BYTES = KH * kBoxBytesB;
   static constexpr uint32_t OFF_B = kUnits * A_BYTES;
-  static constexpr uint32_t OFF_C = OFF_B + STAGES * B_BYTES;  // [NG][2][COLS] floats
+  // kMax: the K = 16 operands of the constant-adding MMA step: a ones tile for A and,
+  // per stage, the B tile's per-query constants (32-byte rows, 32-byte swizzle)
+  static constexpr bool AUG = MODE == kMax;
+  static constexpr uint32_t AUG_A_BYTES = BM * 32, AUG_B_BYTES = BN * 32;
+  static constexpr uint32_t OFF_AUG_A = OFF_B + STAGES * B_BYTES;
+  static constexpr uint32_t OFF_AUG_B = OFF_AUG_A + (AUG ? AUG_A_BYTES : 0);
+  static constexpr uint32_t OFF_C = OFF_AUG_B + (AUG ? STAGES * AUG_B_BYTES : 0);  // [NG][2][COLS]
   static constexpr uint32_t OFF_X = OFF_C + 2 * BN * 4;          // [2][NG-1][BM][2] floats
   static constexpr uint32_t OFF_P = OFF_X + 2 * (NG - 1) * BM * 2 * 4;  // kQuad [2][16][BM]
   static constexpr uint32_t OFF_BAR = OFF_P + (MODE == kQuad ? 2 * kMaxGroup * BM * 4 : 0);
@@ -135,23 +144,15 @@ __device__ __forceinline__ void lse_cols(const uint32_t* v, float sc2, float& m,
   ssum += a0.x + a0.y;
 }
 
-// KVzip max of 64 columns: max_c (x_c * scale + c_c).
-__device__ __forceinline__ float max_cols(const uint32_t* v, const float* cc, float scale,
-                                          float r) {
-  const float4* c4 = reinterpret_cast<const float4*>(cc);
-  const float2 sv = make_float2(scale, scale);
+// Max of 64 raw accumulator columns (the KVzip max with the constants folded in).
+__device__ __forceinline__ float max_raw_cols(const uint32_t* v, float r) {
   float r0 = r, r1 = -CUDART_INF_F, r2 = -CUDART_INF_F, r3 = -CUDART_INF_F;
 #pragma unroll
-  for (int q = 0; q < 16; q += 2) {
-    const float4 ca = c4[q], cb = c4[q + 1];
-    const float2 y0 = __ffma2_rn(f2(v[4 * q], v[4 * q + 1]), sv, make_float2(ca.x, ca.y));
-    const float2 y1 = __ffma2_rn(f2(v[4 * q + 2], v[4 * q + 3]), sv, make_float2(ca.z, ca.w));
-    const float2 y2 = __ffma2_rn(f2(v[4 * q + 4], v[4 * q + 5]), sv, make_float2(cb.x, cb.y));
-    const float2 y3 = __ffma2_rn(f2(v[4 * q + 6], v[4 * q + 7]), sv, make_float2(cb.z, cb.w));
-    r0 = max3(r0, y0.x, y0.y);
-    r1 = max3(r1, y1.x, y1.y);
-    r2 = max3(r2, y2.x, y2.y);
-    r3 = max3(r3, y3.x, y3.y);
+  for (int c = 0; c < 64; c += 8) {
+    r0 = max3(r0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+    r1 = max3(r1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+    r2 = max3(r2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+    r3 = max3(r3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
   }
   return fmaxf(max3(r0, r1, r2), r3);
 }
@@ -247,7 +248,8 @@ __device__ __forceinline__ Tiles tiles_of(const AttnArgs& a, int row0, int G, in
 template <int D, int MODE>
 __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                   const __grid_constant__ CUtensorMap tm_b2, const AttnArgs a) {
+                   const __grid_constant__ CUtensorMap tm_b2, const __grid_constant__ CUtensorMap tm_auga,
+                   const __grid_constant__ CUtensorMap tm_augb, const AttnArgs a) {
   using C = Cfg<D, MODE>;
   constexpr int S = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -317,7 +319,8 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
     if (lane == 0) {
       const int a_head = kQ ? l * a.Hq + hq_a : l * a.Hkv + hk;
       for (int n = 0; n < nunits; ++n) {  // every unit's A tile up front
-        tc::mbar_expect_tx(bar_afull(n), C::A_BYTES);
+        tc::mbar_expect_tx(bar_afull(n), C::A_BYTES + (C::AUG && n == 0 ? C::AUG_A_BYTES : 0));
+        if (C::AUG && n == 0) tc::tma_load_3d(sb + C::OFF_AUG_A, &tm_auga, bar_afull(0), 0, 0, 0);
 #pragma unroll
         for (int kh = 0; kh < C::KH; ++kh)
           tc::tma_load_3d(sA + n * C::A_BYTES + kh * kBoxBytesA, &tm_a, bar_afull(n), kh * 64,
@@ -350,10 +353,13 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
             head = l * a.Hq + hk * G + it / U.per_head;
             row = (U.qt_begin + it % U.per_head) * BN;
           }
-          tc::mbar_expect_tx(bar_full(s), C::B_BYTES);
+          tc::mbar_expect_tx(bar_full(s), C::B_BYTES + (C::AUG ? C::AUG_B_BYTES : 0));
 #pragma unroll
           for (int kh = 0; kh < C::KH; ++kh)
             tc::tma_load_3d(sB + s * C::B_BYTES + kh * kBoxBytesB, map, bar_full(s), kh * 64, row,
+                            head);
+          if (C::AUG)  // the tile's per-query constants (rows padded to whole tiles)
+            tc::tma_load_3d(sb + C::OFF_AUG_B + s * C::AUG_B_BYTES, &tm_augb, bar_full(s), 0, row,
                             head);
         }
       }
@@ -395,6 +401,9 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
             tc::mma_bf16(d_t, tc::sdesc_sw128(a_n + kh * kBoxBytesA + kk),
                          tc::sdesc_sw128(b_s + kh * kBoxBytesB + kk), C::IDESC, k > 0 ? 1u : 0u);
           }
+          if (C::AUG)  // + (1,1,1,0..) . (c_hi, c_mid, c_lo, 0..): the column's constant
+            tc::mma_bf16(d_t, tc::sdesc_sw32(sb + C::OFF_AUG_A),
+                         tc::sdesc_sw32(sb + C::OFF_AUG_B + s * C::AUG_B_BYTES), C::IDESC, 1u);
           tc::commit(bar_empty(s));
           tc::commit(bar_tfull(acc));
         }
@@ -413,7 +422,8 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
     const uint32_t t_lane = tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(h * COLS);
     float* cbuf = cbuf_all + h * 2 * COLS;
     const int bar_id = 1 + h;
-    constexpr bool kCols = (MODE == kMax || MODE == kFuture);  // per-column constants
+    // per-column constants in shared memory (the KVzip max gets them from its MMA)
+    constexpr bool kCols = MODE == kFuture;
     int gt = 0;
     bool failed = false;
 
@@ -555,7 +565,7 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
               rows_cols(w, it * BN + h * COLS + c0, a.T, l2row, sc2, rhi, rlo, a.rows_ld,
                         ra < a.n_q);
             } else if (MODE == kMax) {
-              r = max_cols(w, cc + c0, scale, r);
+              r = max_raw_cols(w, r);  // q.k / scale-units minus the column's constant
             } else {
               const int j0 = (U.qt_begin + it % U.per_head) * BN + h * COLS + c0;
               const bool band = j0 < U.row0 + BM - 1 + a.w;
@@ -563,7 +573,7 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
             }
           }
           if (MODE == kMax && (it + 1) % U.per_head == 0) {  // last query tile of this head
-            tot = fmaxf(tot, r + lv);
+            tot = fmaxf(tot, r * scale + lv);
             r = -CUDART_INF_F;
             if (it + 1 < U.ntiles) lv = ln_vn(it + 1);
           }
@@ -649,6 +659,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// 3-D map over [heads][rows][16] bf16 with box_rows x 16 boxes, 32-byte swizzle.
+cudaError_t make_map_k16(CUtensorMap* m, const void* base, int rows, int heads, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {16, (cuuint64_t)rows, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {32, (cuuint64_t)rows * 32};
+  cuuint32_t box[3] = {16, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // 3-D map over [heads][rows][d] bf16 with 128-row x 64-element boxes, 128-byte swizzle;
 // rows past the end read as zeros.
 cudaError_t make_map(CUtensorMap* m, const void* base, int d, int rows, int heads, int box_rows) {
@@ -690,6 +714,14 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
     tb2 = tb;
   }
   if (e != cudaSuccess) return e;
+  CUtensorMap tauga = ta, taugb = ta;  // the constant-adding operands (kMax only)
+  if (C::AUG) {
+    if (!a.ccol || !a.ones) return cudaErrorInvalidValue;
+    const int nq_pad = (a.n_q + BN - 1) / BN * BN;
+    e = make_map_k16(&taugb, a.ccol, nq_pad, a.L * a.Hq, BN);
+    if (e == cudaSuccess) e = make_map_k16(&tauga, a.ones, BM, 1, BM);
+    if (e != cudaSuccess) return e;
+  }
   const int rows = a_is_queries<MODE>() ? a.n_q : a.T;
   dim3 grid(((rows + BM - 1) / BM + kUnits - 1) / kUnits, a_is_queries<MODE>() ? a.Hq : a.Hkv,
             a.L);
@@ -697,7 +729,7 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   count_launches(1);
-  kern<<<grid, C::THREADS, C::SMEM, s>>>(ta, tb, tb2, a);
+  kern<<<grid, C::THREADS, C::SMEM, s>>>(ta, tb, tb2, tauga, taugb, a);
   return cudaGetLastError();
 }
 
@@ -733,6 +765,69 @@ __global__ void hidden_log_norm_kernel(const bf16_t* __restrict__ h, int rows, i
 cudaError_t tma_map_bf16_3d(CUtensorMap* m, const void* base, int inner, int rows, int outer,
                             int box_rows) {
   return make_map(m, base, inner, rows, outer, box_rows);
+}
+
+cudaError_t tma_map_bf16_k16(CUtensorMap* m, const void* base, int rows, int outer, int box_rows) {
+  return make_map_k16(m, base, rows, outer, box_rows);
+}
+
+namespace {
+
+// Row (l, hq, j) of the KVzip max constants: -(lse_j + ln||h_j||) / scale as a sum of
+// three bf16 (hi, mid, lo: ~24 bits), then zeros; rows past n_q hold -1e30 (they are
+// padding queries and must never win the max).  Block 0 also writes the ones tile.
+__global__ void __launch_bounds__(256) score_constants_kernel(const float* __restrict__ lse,
+                                                              const float* __restrict__ hlog,
+                                                              int L, int Hq, int n_q, int nq_pad,
+                                                              float inv_scale, bf16_t* ccol,
+                                                              bf16_t* ones) {
+  const size_t row = (size_t)blockIdx.x * 256 + threadIdx.x;
+  if (blockIdx.x == 0 && threadIdx.x < BM) {
+    const uint32_t one = 0x3F80u;  // bf16 1.0
+    uint4* o = reinterpret_cast<uint4*>(ones + threadIdx.x * 16);
+    o[0] = make_uint4(one | (one << 16), one, 0u, 0u);
+    o[1] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (row >= (size_t)L * Hq * nq_pad) return;
+  const int j = (int)(row % nq_pad);
+  const size_t lh = row / nq_pad;  // l * Hq + hq
+  float v = -1e30f;
+  if (j < n_q) {
+    const int l = (int)(lh / Hq);
+    const float c = lse[lh * n_q + j] + (hlog ? hlog[(size_t)l * n_q + j] : 0.f);
+    v = -c * inv_scale;
+  }
+  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+  const float r1 = v - __bfloat162float(hi);
+  const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+  const uint32_t w0 = (uint32_t)__bfloat16_as_ushort(hi) | ((uint32_t)__bfloat16_as_ushort(mid) << 16);
+  const uint32_t w1 = (uint32_t)__bfloat16_as_ushort(lo);
+  uint4* o = reinterpret_cast<uint4*>(ccol + row * 16);
+  o[0] = make_uint4(w0, w1, 0u, 0u);
+  o[1] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+size_t score_max_ccol_offset(int L, int n_q) { return align256((size_t)L * n_q * sizeof(float)); }
+
+size_t score_max_ws_bytes(int L, int Hq, int n_q, bool with_h) {
+  const size_t nq_pad = (size_t)(n_q + BN - 1) / BN * BN;
+  return (with_h ? score_max_ccol_offset(L, n_q) : 0) + align256((size_t)L * Hq * nq_pad * 32) +
+         (size_t)BM * 32;
+}
+
+cudaError_t launch_score_constants(const float* lse, const float* hlog, int L, int Hq, int n_q,
+                                   int d, bf16_t* ccol, bf16_t* ones, cudaStream_t s) {
+  const int nq_pad = (n_q + BN - 1) / BN * BN;
+  const size_t rows = (size_t)L * Hq * nq_pad;
+  count_launches(1);
+  score_constants_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(
+      lse, hlog, L, Hq, n_q, nq_pad, sqrtf((float)d), ccol, ones);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_lse(const AttnArgs& a, cudaStream_t s) { return launch_mode<kLse>(a, s); }

@@ -13,6 +13,9 @@ namespace kvs {
 // end read as zeros.  inner must be a multiple of 8 (16-byte row stride).
 cudaError_t tma_map_bf16_3d(CUtensorMap* m, const void* base, int inner, int rows, int outer,
                             int box_rows);
+// Host: the same over a [outer][rows][16] bf16 tensor with 16 x box_rows boxes and 32-byte
+// swizzle (operands of one K = 16 MMA step).
+cudaError_t tma_map_bf16_k16(CUtensorMap* m, const void* base, int rows, int outer, int box_rows);
 
 namespace tc {
 
@@ -130,6 +133,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   d |= (uint64_t)(1024 >> 4) << 32;           // stride byte offset: 8 rows x 128 B
   d |= (uint64_t)1 << 46;                     // descriptor version
   d |= (uint64_t)2 << 61;                     // swizzle: 128 B
+  return d;
+}
+
+// Shared-memory matrix descriptor: K-major operand of exactly 16 bf16 per row in the
+// 32-byte swizzled layout that a TMA load with CU_TENSOR_MAP_SWIZZLE_32B of a 16-element
+// box writes (rows of 32 B, 8-row atoms of 256 B, atoms contiguous).
+__device__ __forceinline__ uint64_t sdesc_sw32(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;              // leading byte offset (unused): 16 B
+  d |= (uint64_t)(256 >> 4) << 32;     // stride byte offset: 8 rows x 32 B
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)6 << 61;              // swizzle: 32 B
   return d;
 }
 

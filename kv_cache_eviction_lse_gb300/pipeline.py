@@ -69,8 +69,8 @@ class KVzipPipeline:
         if self.plus:
             self.vnorm = _empty((L, wl.H_q, wl.T), torch.float32, dev)
             self.vws = _empty((C.kvs_vnorm_workspace_size(self.dm),), torch.uint8, dev)
-            self.sws = _empty((max(16, C.kvs_score_max_workspace_size(self.dm, self.n_q, 1)),),
-                              torch.uint8, dev)
+        self.sws = _empty((max(16, C.kvs_score_max_workspace_size(self.dm, self.n_q, self.plus)),),
+                          torch.uint8, dev)
         self.ratios = tuple(ratios if ratios is not None else wl.keep_ratios)
         self.masks = [_empty((L, wl.H_kv, wl.T), torch.uint8, dev) for _ in self.ratios]
         self.keeps = [_empty((L, wl.H_kv), torch.int32, dev) for _ in self.ratios]
@@ -123,7 +123,7 @@ class KVzipPipeline:
                             self.score, self.sws, self.sws.numel())
         else:
             C.kvs_score_max(dm, x["q"], self.n_q, x["k_ctx"], wl.T, self.lse, None, None, 0,
-                            self.score, None, 0)
+                            self.score, self.sws, self.sws.numel())
 
     def _prune(self):
         wl, dm = self.wl, self.dm

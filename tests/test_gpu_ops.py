@@ -151,7 +151,9 @@ def test_vnorm_lse_score_max(C, shape):
         sws = torch.empty(C.kvs_score_max_workspace_size(dm, nq, 1), dtype=torch.uint8, device="cuda")
         C.kvs_score_max(dm, g["q"], nq, g["k_ctx"], T, lse, vn, g["h"], 0, score, sws, sws.numel())
     else:
-        C.kvs_score_max(dm, g["q"], nq, g["k_ctx"], T, lse, None, None, 0, score, None, 0)
+        sws = torch.empty(max(16, C.kvs_score_max_workspace_size(dm, nq, 0)), dtype=torch.uint8,
+                          device="cuda")
+        C.kvs_score_max(dm, g["q"], nq, g["k_ctx"], T, lse, None, None, 0, score, sws, sws.numel())
     torch.cuda.synchronize()
     q, kc, kt = f64(x["q"]), f64(x["k_ctx"]), f64(x["k_tail"])
     vref = O.value_norm(f64(x["v_ctx"]), f64(x["w_o"]), Hq) if Dh else None
@@ -172,7 +174,9 @@ def test_score_max_accumulate(C):
         g = cuda(x)
         lse = torch.empty((L, Hq, nq), device="cuda")
         C.kvs_lse(dm, g["q"], nq, g["k_ctx"], T, g["k_tail"], nt, lse)
-        C.kvs_score_max(dm, g["q"], nq, g["k_ctx"], T, lse, None, None, i, score, None, 0)
+        sws = torch.empty(C.kvs_score_max_workspace_size(dm, nq, 0), dtype=torch.uint8,
+                          device="cuda")
+        C.kvs_score_max(dm, g["q"], nq, g["k_ctx"], T, lse, None, None, i, score, sws, sws.numel())
     torch.cuda.synchronize()
     want = O.kvzip_score_chunked([f64(xa["q"]), f64(xb["q"])], f64(xa["k_ctx"]),
                                  [f64(xa["k_tail"]), f64(xb["k_tail"])])
