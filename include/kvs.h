@@ -169,11 +169,15 @@ kvs_status kvs_score_max(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
  *   q     [L][H_q][T][d]  bf16,  k [L][H_kv][T][d] bf16
  *   lse   [L][H_q][T]     fp32   from kvs_lse(q, n_q = T, k_ctx = k, T, n_tail = 0)
  *   score [L][H_kv][T]    fp32   output (linear mass, not a log); keys i > T-1-w get 0
+ *   ws    scratch of kvs_score_future_sum_workspace_size() bytes: the per-query
+ *         constants -lse_j sqrt(d) as three bf16 parts, added to every accumulator
+ *         column by one extra K = 16 MMA step
  * Requires w >= 0.
  * ------------------------------------------------------------------------------- */
+size_t kvs_score_future_sum_workspace_size(const kvs_dims* dims, int32_t T);
 kvs_status kvs_score_future_sum(const kvs_dims* dims, const kvs_bf16* q, const kvs_bf16* k,
-                                int32_t T, const float* lse, int32_t w, float* score,
-                                void* stream);
+                                int32_t T, const float* lse, int32_t w, float* score, void* ws,
+                                size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------
  * kvs_vnorm -- value factor of KVzip+ [KVzap 3.2, Eq. 2 and Eq. 3]:

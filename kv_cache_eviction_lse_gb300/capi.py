@@ -62,7 +62,8 @@ _SIGS = {
     "kvs_lse": ([_D, _P, _I, _P, _I, _P, _I, _P, _P], ctypes.c_int),
     "kvs_score_max_workspace_size": ([_D, _I, _I], _S),
     "kvs_score_max": ([_D, _P, _I, _P, _I, _P, _P, _P, _I, _P, _P, _S, _P], ctypes.c_int),
-    "kvs_score_future_sum": ([_D, _P, _P, _I, _P, _I, _P, _P], ctypes.c_int),
+    "kvs_score_future_sum_workspace_size": ([_D, _I], ctypes.c_size_t),
+    "kvs_score_future_sum": ([_D, _P, _P, _I, _P, _I, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "kvs_vnorm_workspace_size": ([_D], _S),
     "kvs_vnorm": ([_D, _P, _I, _P, _P, _P, _S, _P], ctypes.c_int),
     "kvs_vnorm_noalloc": ([_D, _P, _I, _P, _P, _P], ctypes.c_int),
@@ -150,9 +151,13 @@ def kvs_score_max(dm, q, n_q, k_ctx, T, lse, vnorm, h, accumulate, log_score, ws
                               _stream(stream)))
 
 
-def kvs_score_future_sum(dm, q, k, T, lse, w, score, stream=None):
+def kvs_score_future_sum_workspace_size(dm, T):
+    return int(_lib.kvs_score_future_sum_workspace_size(_d(dm), T))
+
+
+def kvs_score_future_sum(dm, q, k, T, lse, w, score, ws, ws_bytes, stream=None):
     _check(_lib.kvs_score_future_sum(_d(dm), _ptr(q), _ptr(k), T, _ptr(lse), w, _ptr(score),
-                                     _stream(stream)))
+                                     _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def kvs_vnorm_workspace_size(dm) -> int:

@@ -213,9 +213,14 @@ kvs_status kvs_score_max(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
   return cuda_status(kvs::launch_score_max(a, s), "kvs_score_max");
 }
 
+size_t kvs_score_future_sum_workspace_size(const kvs_dims* dims, int32_t T) {
+  if (!dims || T <= 0 || dims->L <= 0 || dims->H_q <= 0) return 0;
+  return kvs::score_max_ws_bytes(dims->L, dims->H_q, T, false);
+}
+
 kvs_status kvs_score_future_sum(const kvs_dims* dims, const kvs_bf16* q, const kvs_bf16* k,
-                                int32_t T, const float* lse, int32_t w, float* score,
-                                void* stream) {
+                                int32_t T, const float* lse, int32_t w, float* score, void* ws,
+                                size_t ws_bytes, void* stream) {
   kvs_status st = check_dims(dims, __func__);
   if (st) return st;
   REQUIRE(T >= 0 && w >= 0, KVS_ERR_ARG, "kvs_score_future_sum: negative T or w");
@@ -224,11 +229,22 @@ kvs_status kvs_score_future_sum(const kvs_dims* dims, const kvs_bf16* q, const k
   REQUIRE_PTR(k);
   REQUIRE_PTR(lse);
   REQUIRE_PTR(score);
+  REQUIRE_PTR(ws);
+  const size_t need = kvs_score_future_sum_workspace_size(dims, T);
+  REQUIRE(ws_bytes >= need, KVS_ERR_CAPACITY,
+          "kvs_score_future_sum: workspace of %zu bytes, %zu needed", ws_bytes, need);
+  cudaStream_t s = as_stream(stream);
+  auto* ccol = static_cast<kvs::bf16_t*>(ws);
+  auto* ones = reinterpret_cast<kvs::bf16_t*>(static_cast<uint8_t*>(ws) + need - 128 * 32);
+  cudaError_t e = kvs::launch_score_constants(lse, nullptr, dims->L, dims->H_q, T, dims->d, ccol,
+                                              ones, s);
+  if (e != cudaSuccess) return cuda_status(e, "kvs_score_future_sum (constants)");
   kvs::AttnArgs a;
   a.q = q; a.k_ctx = k; a.lse = lse; a.out = score;
   a.L = dims->L; a.Hq = dims->H_q; a.Hkv = dims->H_kv; a.d = dims->d;
   a.n_q = T; a.T = T; a.w = w;
-  return cuda_status(kvs::launch_future_sum(a, as_stream(stream)), "kvs_score_future_sum");
+  a.ccol = ccol; a.ones = ones;
+  return cuda_status(kvs::launch_future_sum(a, s), "kvs_score_future_sum");
 }
 
 size_t kvs_vnorm_workspace_size(const kvs_dims* dims) {

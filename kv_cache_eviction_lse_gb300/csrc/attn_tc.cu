@@ -24,7 +24,8 @@
 //            step (a ones tile against the constant split into three bf16 parts), so
 //            the epilogue is a plain 3-input max
 //   kFuture  A = keys, B = query tiles j >= i0 + w: per key sum over the group of
-//            2^((x - lse_j) log2 e) for j >= i + w
+//            2^((x - lse_j) log2 e) for j >= i + w, with -lse_j sqrt(d) folded into the
+//            accumulator by the same extra MMA step as kMax
 // Sources: KVpop review, 1. Key Terms (LSE reuse, transposed-attention pass);
 // KVzap review, 3.1 Eq. 1 and 3.2 Eq. 3.
 #include <cuda.h>
@@ -78,12 +79,11 @@ struct Cfg {
   static constexpr uint32_t OFF_B = kUnits * A_BYTES;
   // kMax: the K = 16 operands of the constant-adding MMA step: a ones tile for A and,
   // per stage, the B tile's per-query constants (32-byte rows, 32-byte swizzle)
-  static constexpr bool AUG = MODE == kMax;
+  static constexpr bool AUG = MODE == kMax || MODE == kFuture;
   static constexpr uint32_t AUG_A_BYTES = BM * 32, AUG_B_BYTES = BN * 32;
   static constexpr uint32_t OFF_AUG_A = OFF_B + STAGES * B_BYTES;
   static constexpr uint32_t OFF_AUG_B = OFF_AUG_A + (AUG ? AUG_A_BYTES : 0);
-  static constexpr uint32_t OFF_C = OFF_AUG_B + (AUG ? STAGES * AUG_B_BYTES : 0);  // [NG][2][COLS]
-  static constexpr uint32_t OFF_X = OFF_C + 2 * BN * 4;          // [2][NG-1][BM][2] floats
+  static constexpr uint32_t OFF_X = OFF_AUG_B + (AUG ? STAGES * AUG_B_BYTES : 0);  // [2][NG-1][BM][2]
   static constexpr uint32_t OFF_P = OFF_X + 2 * (NG - 1) * BM * 2 * 4;  // kQuad [2][16][BM]
   static constexpr uint32_t OFF_BAR = OFF_P + (MODE == kQuad ? 2 * kMaxGroup * BM * 4 : 0);
   // a_full[kUnits], full[S], empty[S], tfull[2], tempty[2]
@@ -157,17 +157,15 @@ __device__ __forceinline__ float max_raw_cols(const uint32_t* v, float r) {
   return fmaxf(max3(r0, r1, r2), r3);
 }
 
-// Future mass of 64 columns: sum_c 2^(x_c * sc2 + c_c), columns c < jlim zeroed.
-__device__ __forceinline__ float future_cols(const uint32_t* v, const float* cc, float sc2,
-                                             bool band, int jlim) {
-  const float4* c4 = reinterpret_cast<const float4*>(cc);
+// Future mass of 64 columns: sum_c 2^(acc_c * sc2) (the column's -lse_j sqrt(d) is in the
+// accumulator), columns c < jlim zeroed.
+__device__ __forceinline__ float future_cols(const uint32_t* v, float sc2, bool band, int jlim) {
   const float2 k2 = make_float2(sc2, sc2);
   float2 a0 = make_float2(0.f, 0.f), a1 = a0;
 #pragma unroll
   for (int q = 0; q < 16; ++q) {
-    const float4 c = c4[q];
-    const float2 y0 = __ffma2_rn(f2(v[4 * q], v[4 * q + 1]), k2, make_float2(c.x, c.y));
-    const float2 y1 = __ffma2_rn(f2(v[4 * q + 2], v[4 * q + 3]), k2, make_float2(c.z, c.w));
+    const float2 y0 = __fmul2_rn(f2(v[4 * q], v[4 * q + 1]), k2);
+    const float2 y1 = __fmul2_rn(f2(v[4 * q + 2], v[4 * q + 3]), k2);
     float e0 = fast_exp2(y0.x), e1 = fast_exp2(y0.y);
     float e2 = fast_exp2(y1.x), e3 = fast_exp2(y1.y);
     if (band) {
@@ -262,7 +260,6 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
   uint8_t* smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
   const uint32_t sA = sb, sB = sb + C::OFF_B;
-  float* cbuf_all = reinterpret_cast<float*>(smem + C::OFF_C);
   float* xchg_all = reinterpret_cast<float*>(smem + C::OFF_X);
   float* part = reinterpret_cast<float*>(smem + C::OFF_P);
   const uint32_t bar0 = sb + C::OFF_BAR;
@@ -418,12 +415,8 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
     const int h = (warp - 2) >> 2;               // epilogue group: columns [h COLS, (h+1) COLS)
     const int eq = warp & 3;                     // TMEM lane quarter this warp may access
     const int row = eq * 32 + lane;              // accumulator row
-    const int e = ((warp - 2) & 3) * 32 + lane;  // index within the group (0..127)
     const uint32_t t_lane = tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(h * COLS);
-    float* cbuf = cbuf_all + h * 2 * COLS;
     const int bar_id = 1 + h;
-    // per-column constants in shared memory (the KVzip max gets them from its MMA)
-    constexpr bool kCols = MODE == kFuture;
     int gt = 0;
     bool failed = false;
 
@@ -439,14 +432,6 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
         rlo = a.rows_lo + r * a.rows_ld;
       }
 
-      auto col_const = [&](int it) -> float {
-        const int hq = hk * G + it / U.per_head;
-        const int j = (U.qt_begin + it % U.per_head) * BN + h * COLS + e;
-        if (j >= a.n_q) return -CUDART_INF_F;
-        const float lj = a.lse[(size_t)(l * a.Hq + hq) * a.n_q + j];
-        if (MODE == kMax) return -(lj + (a.hlog ? a.hlog[(size_t)l * a.n_q + j] : 0.f));
-        return -lj * kLog2e;
-      };
       auto ln_vn = [&](int it) -> float {  // ln ||W_O v|| of this key for the head of tile it
         if (!a.vnorm || ra >= a.T) return 0.f;
         return logf(a.vnorm[(size_t)(l * a.Hq + hk * G + it / U.per_head) * a.T + ra]);
@@ -456,14 +441,6 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
       float r = -CUDART_INF_F, tot = -CUDART_INF_F;  // kMax
       float lv = 0.f;                                // kMax: ln vnorm of the current head
       float f = 0.f;                                 // kFuture
-      float cn1 = 0.f, cn2 = 0.f;
-      // threads e < COLS of a group own one column constant each
-      if (kCols && U.ntiles > 0 && e < COLS) {
-        const float c0 = col_const(0);
-        if (U.ntiles > 1) cn1 = col_const(1);
-        if (U.ntiles > 2) cn2 = col_const(2);
-        cbuf[e] = c0;  // the previous unit's readers passed its end-of-unit vote
-      }
       if (MODE == kMax && U.ntiles > 0) lv = ln_vn(0);
 
       // kQuad: this thread's D/2 elements of its value row, from the swizzled A tile
@@ -491,21 +468,12 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
       for (int it = 0; it < U.ntiles && !bad; ++it, ++gt) {
         const int acc = gt & 1;
         const uint32_t aph = (uint32_t)(gt >> 1) & 1u;
-        if constexpr (kCols) {
-          // the group barrier also orders the shared per-column constants (below)
-          const bool ok = tc::mbar_wait(bar_tfull(acc), aph) && !*abort_flag;
-          if (tc::bar_or(bar_id, kGroupThreads, !ok)) {
-            bad = true;
-            break;
-          }
-        } else {
-          // no shared state per tile: a wait that runs out raises the CTA's abort flag, so
-          // every other thread leaves at its next wait and all meet at the end-of-unit vote
-          if (!tc::mbar_wait(bar_tfull(acc), aph) || *abort_flag) {
-            *abort_flag = 1u;
-            bad = true;
-            break;
-          }
+        // a wait that runs out raises the CTA's abort flag, so every other thread leaves
+        // at its next wait and all meet at the end-of-unit vote
+        if (!tc::mbar_wait(bar_tfull(acc), aph) || *abort_flag) {
+          *abort_flag = 1u;
+          bad = true;
+          break;
         }
         tc::fence_after_sync();
         if constexpr (MODE == kQuad) {
@@ -537,16 +505,9 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
           const uint32_t ta = t_lane + (uint32_t)(acc * BN);
 #pragma unroll
           for (int c = 0; c < COLS; c += 32) tc::tmem_ld32(ta + c, v + c);
-          if (kCols) {
-            // the other buffer's readers finished tile it-1 before the barrier above
-            if (it + 1 < U.ntiles && e < COLS) cbuf[((it + 1) & 1) * COLS + e] = cn1;
-            cn1 = cn2;
-            if (it + 3 < U.ntiles && e < COLS) cn2 = col_const(it + 3);
-          }
           tc::tmem_ld_wait();
           tc::fence_before_sync();
           tc::mbar_arrive(bar_tempty(acc));
-          const float* cc = cbuf + (it & 1) * COLS;
 #pragma unroll
           for (int c0 = 0; c0 < COLS; c0 += 64) {
             uint32_t* w = v + c0;
@@ -569,7 +530,7 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
             } else {
               const int j0 = (U.qt_begin + it % U.per_head) * BN + h * COLS + c0;
               const bool band = j0 < U.row0 + BM - 1 + a.w;
-              f += future_cols(w, cc + c0, sc2, band, ra + a.w - j0);
+              f += future_cols(w, sc2, band, ra + a.w - j0);
             }
           }
           if (MODE == kMax && (it + 1) % U.per_head == 0) {  // last query tile of this head

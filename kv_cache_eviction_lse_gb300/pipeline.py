@@ -236,6 +236,7 @@ class FuturePipeline:
         self.attn_forward = attn_forward
         self.o = _empty((L, wl.H_q, wl.T, wl.d), torch.bfloat16, dev) if attn_forward else None
         self.score = _empty((L, wl.H_kv, wl.T), torch.float32, dev)
+        self.fws = _empty((C.kvs_score_future_sum_workspace_size(self.dm, wl.T),), torch.uint8, dev)
         self.ratios = tuple(ratios if ratios is not None else wl.keep_ratios)
         self.masks = [_empty((L, wl.H_kv, wl.T), torch.uint8, dev) for _ in self.ratios]
         self.keeps = [_empty((L, wl.H_kv), torch.int32, dev) for _ in self.ratios]
@@ -252,7 +253,8 @@ class FuturePipeline:
 
     def _future(self):
         wl, x, dm = self.wl, self.x, self.dm
-        C.kvs_score_future_sum(dm, x["q"], x["k"], wl.T, self.lse, wl.w, self.score)
+        C.kvs_score_future_sum(dm, x["q"], x["k"], wl.T, self.lse, wl.w, self.score, self.fws,
+                               self.fws.numel())
 
     def _prune(self):
         wl, dm = self.wl, self.dm

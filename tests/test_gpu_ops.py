@@ -193,7 +193,8 @@ def test_future_sum(C, d, T, w):
     lse = torch.empty((L, Hq, T), device="cuda")
     C.kvs_lse(dm, g["q"], T, g["k_ctx"], T, None, 0, lse)
     f = torch.full((L, Hkv, T), float("nan"), device="cuda")
-    C.kvs_score_future_sum(dm, g["q"], g["k_ctx"], T, lse, w, f)
+    fws = torch.empty(C.kvs_score_future_sum_workspace_size(dm, T), dtype=torch.uint8, device="cuda")
+    C.kvs_score_future_sum(dm, g["q"], g["k_ctx"], T, lse, w, f, fws, fws.numel())
     torch.cuda.synchronize()
     want = O.future_attention_mass(f64(x["q"]), f64(x["k_ctx"]), w)
     got = f.cpu().numpy()
