@@ -3,7 +3,7 @@
 // lengths need PagedAttention-like storage).
 //
 // Three launches, all bandwidth-bound:
-//   1. seg_count   : kept tokens per (row, segment of 1024 or 4096 tokens)  reads the mask
+//   1. seg_count   : kept tokens per (row, segment of 256, 1024 or 4096 tokens)  reads the mask
 //   2. page_plan   : per-row exclusive scan of segment counts, page counts
 //                    ceil(kept/page), exclusive scan of pages over rows (layer-major,
 //                    then head), capacity check, seq_lens, needed_pages
@@ -18,8 +18,10 @@ namespace kvs {
 namespace {
 
 constexpr int kSegThreads = 256;  // P mask bytes per thread, segments of 256 * P tokens
-constexpr int kMinSeg = 1024;     // short rows: P = 4
+constexpr int kTinySeg = 256;     // short rows (T <= kShortRow): P = 1, more blocks
+constexpr int kMinSeg = 1024;     // medium rows: P = 4
 constexpr int kMaxSeg = 4096;     // long rows (T >= kLongRow): P = 16, fewer, larger blocks
+constexpr int kShortRow = 4096;
 constexpr int kLongRow = 8192;
 
 struct Plan {            // lives at the start of the workspace
@@ -32,7 +34,10 @@ struct Plan {            // lives at the start of the workspace
 // Mask bytes t0 .. t0+P-1 of a row as 0/1 flags (vector loads when T allows).
 template <int P>
 __device__ __forceinline__ void load_flags(const uint8_t* m, int T, int t0, uint8_t* f) {
-  if ((T & (P - 1)) == 0 && t0 < T) {
+  if constexpr (P == 1) {
+    f[0] = t0 < T ? (m[t0] != 0) : 0;
+    return;
+  } else if ((T & (P - 1)) == 0 && t0 < T) {
     uint32_t wd[P / 4];
     if constexpr (P == 16) {
       const uint4 u = *reinterpret_cast<const uint4*>(m + t0);
@@ -41,7 +46,7 @@ __device__ __forceinline__ void load_flags(const uint8_t* m, int T, int t0, uint
       wd[2] = u.z;
       wd[3] = u.w;
     } else {
-      static_assert(P == 4, "4 or 16 mask bytes per thread");
+      static_assert(P == 4, "1, 4 or 16 mask bytes per thread");
       wd[0] = *reinterpret_cast<const uint32_t*>(m + t0);
     }
 #pragma unroll
@@ -244,7 +249,7 @@ __global__ void __launch_bounds__(kSegThreads) scatter_kernel(
 }  // namespace
 
 size_t compact_workspace_bytes(int rows, int T) {
-  const int nseg = (T + kMinSeg - 1) / kMinSeg;  // the finer segmentation bounds both
+  const int nseg = (T + kTinySeg - 1) / kTinySeg;  // the finest segmentation bounds all
   return sizeof(Plan) + sizeof(int) * ((size_t)rows * (nseg > 0 ? nseg : 1) + rows);
 }
 
@@ -253,8 +258,8 @@ cudaError_t launch_compact(const bf16_t* k, const bf16_t* v, int rows, int T, in
                            int capacity, int* block_table, int max_pages, int* seq_lens,
                            int* needed, void* ws, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  const bool long_rows = T >= kLongRow;
-  const int seg_len = long_rows ? kMaxSeg : kMinSeg;
+  const bool long_rows = T >= kLongRow, short_rows = T <= kShortRow;
+  const int seg_len = long_rows ? kMaxSeg : short_rows ? kTinySeg : kMinSeg;
   const int nseg = T > 0 ? (T + seg_len - 1) / seg_len : 1;
   Plan* plan = reinterpret_cast<Plan*>(ws);
   int* seg = reinterpret_cast<int*>(plan + 1);
@@ -262,12 +267,18 @@ cudaError_t launch_compact(const bf16_t* k, const bf16_t* v, int rows, int T, in
   count_launches(3);
   if (long_rows)
     seg_count_kernel<16><<<dim3(nseg, rows), kSegThreads, 0, s>>>(mask, T, nseg, seg);
+  else if (short_rows)
+    seg_count_kernel<1><<<dim3(nseg, rows), kSegThreads, 0, s>>>(mask, T, nseg, seg);
   else
     seg_count_kernel<4><<<dim3(nseg, rows), kSegThreads, 0, s>>>(mask, T, nseg, seg);
   page_plan_kernel<<<1, 1024, 0, s>>>(rows, nseg, page_size, capacity, seg, first, plan, seq_lens,
                                       needed);
   if (long_rows)
     scatter_kernel<16><<<dim3(nseg, rows), kSegThreads, 0, s>>>(
+        k, v, mask, T, d, nseg, page_size, seg, first, plan, seq_lens, k_pages, v_pages,
+        block_table, max_pages);
+  else if (short_rows)
+    scatter_kernel<1><<<dim3(nseg, rows), kSegThreads, 0, s>>>(
         k, v, mask, T, d, nseg, page_size, seg, first, plan, seq_lens, k_pages, v_pages,
         block_table, max_pages);
   else
