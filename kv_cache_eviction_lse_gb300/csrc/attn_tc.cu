@@ -28,6 +28,7 @@
 //            accumulator by the same extra MMA step as kMax
 // Sources: KVpop review, 1. Key Terms (LSE reuse, transposed-attention pass);
 // KVzap review, 3.1 Eq. 1 and 3.2 Eq. 3.
+#include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -86,8 +87,8 @@ struct Cfg {
   static constexpr uint32_t OFF_X = OFF_AUG_B + (AUG ? STAGES * AUG_B_BYTES : 0);  // [2][NG-1][BM][2]
   static constexpr uint32_t OFF_P = OFF_X + 2 * (NG - 1) * BM * 2 * 4;  // kQuad [2][16][BM]
   static constexpr uint32_t OFF_BAR = OFF_P + (MODE == kQuad ? 2 * kMaxGroup * BM * 4 : 0);
-  // a_full[kUnits], full[S], empty[S], tfull[2], tempty[2]
-  static constexpr uint32_t NBAR = kUnits + 2 * STAGES + 4;
+  // a_full[kUnits], full[S], empty[S], tfull[2], tempty[2], a_empty[kUnits]
+  static constexpr uint32_t NBAR = 2 * kUnits + 2 * STAGES + 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t USED = OFF_MISC + 16;
   static constexpr uint32_t SMEM = (USED + 1024 <= kMaxSmem) ? USED + 1024 : kMaxSmem;
@@ -247,7 +248,8 @@ template <int D, int MODE>
 __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __grid_constant__ CUtensorMap tm_b2, const __grid_constant__ CUtensorMap tm_auga,
-                   const __grid_constant__ CUtensorMap tm_augb, const AttnArgs a) {
+                   const __grid_constant__ CUtensorMap tm_augb, const AttnArgs a,
+                   const int strided) {
   using C = Cfg<D, MODE>;
   constexpr int S = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -263,30 +265,63 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
   float* xchg_all = reinterpret_cast<float*>(smem + C::OFF_X);
   float* part = reinterpret_cast<float*>(smem + C::OFF_P);
   const uint32_t bar0 = sb + C::OFF_BAR;
-  auto bar_afull = [&](int n) { return bar0 + 8u * n; };
+  auto bar_afull = [&](int b) { return bar0 + 8u * b; };
   auto bar_full = [&](int s) { return bar0 + 8u * (kUnits + s); };
   auto bar_empty = [&](int s) { return bar0 + 8u * (kUnits + S + s); };
   auto bar_tfull = [&](int x) { return bar0 + 8u * (kUnits + 2 * S + x); };
   auto bar_tempty = [&](int x) { return bar0 + 8u * (kUnits + 2 * S + 2 + x); };
+  auto bar_aempty = [&](int b) { return bar0 + 8u * (kUnits + 2 * S + 4 + b); };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int l = blockIdx.z;
   const int G = a.Hq / a.Hkv;
   const int n_k = a.T + a.n_tail;
   const int off = a.causal ? n_k - a.n_q : n_k;  // non-causal: every key is visible
   const float scale = rsqrtf((float)D);
   const float sc2 = scale * kLog2e;
   constexpr bool kQ = a_is_queries<MODE>();
-  const int hq_a = kQ ? (int)blockIdx.y : 0;
-  const int hk = kQ ? hq_a / G : (int)blockIdx.y;
   const int a_rows = kQ ? a.n_q : a.T;
-  const int rb0 = blockIdx.x * kUnits;
-  const int nunits = min(kUnits, (a_rows + BM - 1) / BM - rb0);
+  const int nrb = (a_rows + BM - 1) / BM;  // 128-row units per (layer, head)
+  const int NH = kQ ? a.Hq : a.Hkv;
+  // The CTA's units.  Strided (a persistent grid of one CTA per SM): units blockIdx.x,
+  // blockIdx.x + gridDim.x, ... of all (layer, head, row block), row block fastest, the
+  // two A buffers alternating, the setup paid once per SM.  Blocked (grid = row-block
+  // pairs x heads x layers): two consecutive row blocks of one (layer, head), balanced by
+  // the hardware's block scheduler.
+  const int nunits = strided ? (nrb * NH * a.L - (int)blockIdx.x + (int)gridDim.x - 1) /
+                                      (int)gridDim.x
+                                : min(kUnits, nrb - (int)blockIdx.x * kUnits);
+  // A CTA's units visit one residue class of row blocks modulo dg = gcd(grid, row blocks);
+  // the cost of a causal unit grows (or falls) with its row block, so odd groups of dg
+  // row blocks are taken in reverse order, giving every residue class the same mean cost.
+  int dg = strided ? (int)gridDim.x : 1;
+  for (int x = nrb; x > 0;) {
+    const int t = dg % x;
+    dg = x;
+    x = t;
+  }
+  auto unit_of = [&](int n, int& l, int& hy) -> int {  // returns the unit's first row
+    int rb;
+    if (strided) {
+      const int u = (int)blockIdx.x + n * (int)gridDim.x;
+      const int r = u % nrb, k = r / dg, sr = r - k * dg;
+      rb = k * dg + ((k & 1) ? dg - 1 - sr : sr);
+      hy = (u / nrb) % NH;
+      l = u / (nrb * NH);
+    } else {
+      rb = (int)blockIdx.x * kUnits + n;
+      hy = blockIdx.y;
+      l = blockIdx.z;
+    }
+    return rb * BM;
+  };
 
   if (threadIdx.x == 0) {
-    for (int n = 0; n < kUnits; ++n) tc::mbar_init(bar_afull(n), 1);
+    for (int n = 0; n < kUnits; ++n) {
+      tc::mbar_init(bar_afull(n), 1);
+      tc::mbar_init(bar_aempty(n), 1);
+    }
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(bar_full(s), 1);
       tc::mbar_init(bar_empty(s), 1);
@@ -314,20 +349,38 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
   if (warp == 0) {
     // ============================================================ TMA producer
     if (lane == 0) {
-      const int a_head = kQ ? l * a.Hq + hq_a : l * a.Hkv + hk;
-      for (int n = 0; n < nunits; ++n) {  // every unit's A tile up front
-        tc::mbar_expect_tx(bar_afull(n), C::A_BYTES + (C::AUG && n == 0 ? C::AUG_A_BYTES : 0));
-        if (C::AUG && n == 0) tc::tma_load_3d(sb + C::OFF_AUG_A, &tm_auga, bar_afull(0), 0, 0, 0);
+      int gt = 0, na = 0;  // B tiles and A tiles issued
+      // A tile of unit na into buffer na & 1, whose previous unit (na - 2) is done: the
+      // MMA issuer commits a_empty of the buffer once that unit's products complete
+      auto issue_a = [&]() {
+        int l, hy;
+        const int row0 = unit_of(na, l, hy);
+        const int b = na & 1;
+        tc::mbar_expect_tx(bar_afull(b), C::A_BYTES + (C::AUG && na == 0 ? C::AUG_A_BYTES : 0));
+        if (C::AUG && na == 0) tc::tma_load_3d(sb + C::OFF_AUG_A, &tm_auga, bar_afull(0), 0, 0, 0);
 #pragma unroll
         for (int kh = 0; kh < C::KH; ++kh)
-          tc::tma_load_3d(sA + n * C::A_BYTES + kh * kBoxBytesA, &tm_a, bar_afull(n), kh * 64,
-                          (rb0 + n) * BM, a_head);
-      }
-      int gt = 0;
+          tc::tma_load_3d(sA + b * C::A_BYTES + kh * kBoxBytesA, &tm_a, bar_afull(b), kh * 64, row0,
+                          l * (kQ ? a.Hq : a.Hkv) + hy);
+        ++na;
+      };
       bool ok = true;
       for (int n = 0; n < nunits && ok; ++n) {
-        const Tiles U = tiles_of<MODE>(a, (rb0 + n) * BM, G, off);
+        int l, hy;
+        const int row0 = unit_of(n, l, hy);
+        const int hk = kQ ? hy / G : hy;
+        if (na == n) {  // not prefetched: wait for the buffer
+          if (!tc::mbar_wait(bar_aempty(n & 1), ((n >> 1) & 1) ^ 1u) || *abort_flag) {
+            ok = false;
+            break;
+          }
+          issue_a();
+        }
+        const Tiles U = tiles_of<MODE>(a, row0, G, off);
         for (int it = 0; it < U.ntiles; ++it, ++gt) {
+          // prefetch the next unit's A tile as soon as its buffer is free
+          if (na == n + 1 && na < nunits && tc::mbar_test(bar_aempty(na & 1), ((na >> 1) & 1) ^ 1u))
+            issue_a();
           const int s = gt % S;
           const uint32_t ph = (uint32_t)(gt / S) & 1u;
           if (!tc::mbar_wait(bar_empty(s), ph ^ 1u) || *abort_flag) {
@@ -363,7 +416,7 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
       if (!ok) {
         fail(abort_flag, kErrWaitTimeout);
         // let the copies already in flight land before the CTA exits
-        for (int n = 0; n < nunits; ++n) tc::mbar_wait(bar_afull(n), 0);
+        for (int n = max(0, na - 2); n < na; ++n) tc::mbar_wait(bar_afull(n & 1), (n >> 1) & 1);
         for (int j = max(0, gt - S); j < gt; ++j) tc::mbar_wait(bar_full(j % S), (j / S) & 1);
       }
     }
@@ -373,12 +426,14 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
       int gt = 0;
       bool ok = true;
       for (int n = 0; n < nunits && ok; ++n) {
-        const Tiles U = tiles_of<MODE>(a, (rb0 + n) * BM, G, off);
-        if (!tc::mbar_wait(bar_afull(n), 0)) {
+        int l, hy;
+        const Tiles U = tiles_of<MODE>(a, unit_of(n, l, hy), G, off);
+        const int b = n & 1;
+        if (!tc::mbar_wait(bar_afull(b), (n >> 1) & 1)) {
           ok = false;
           break;
         }
-        const uint32_t a_n = sA + n * C::A_BYTES;
+        const uint32_t a_n = sA + b * C::A_BYTES;
         for (int it = 0; it < U.ntiles; ++it, ++gt) {
           const int s = gt % S;
           const uint32_t ph = (uint32_t)(gt / S) & 1u;
@@ -404,6 +459,9 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
           tc::commit(bar_empty(s));
           tc::commit(bar_tfull(acc));
         }
+        // the producer reuses this A buffer for unit n + 2 once the unit's MMAs complete
+        // (no commit after the last use, so nothing arrives once the CTA may have exited)
+        if (n + 2 < nunits) tc::commit(bar_aempty(b));
       }
       if (!ok) fail(abort_flag, kErrWaitTimeout);
       if (gt > 0) tc::mbar_wait(bar_empty((gt - 1) % S), ((gt - 1) / S) & 1);
@@ -421,7 +479,10 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
     bool failed = false;
 
     for (int n = 0; n < nunits; ++n) {
-      const Tiles U = tiles_of<MODE>(a, (rb0 + n) * BM, G, off);
+      int l, hy;
+      const Tiles U = tiles_of<MODE>(a, unit_of(n, l, hy), G, off);
+      const int hq_a = kQ ? hy : 0;
+      const int hk = kQ ? hy / G : hy;
       const int ra = U.row0 + row;  // this thread's query (kLse, kRows) or key
       float l2row = 0.f;              // kRows: this query's LSE in log2 units
       bf16_t *rhi = nullptr, *rlo = nullptr;
@@ -446,9 +507,10 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
       // kQuad: this thread's D/2 elements of its value row, from the swizzled A tile
       uint32_t vrow[MODE == kQuad ? D / 4 : 1];
       bool bad = false;  // a wait of this group ran out: skip to the end-of-unit vote
-      if (MODE == kQuad) bad = tc::bar_or(bar_id, kGroupThreads, !tc::mbar_wait(bar_afull(n), 0));
+      if (MODE == kQuad)
+        bad = tc::bar_or(bar_id, kGroupThreads, !tc::mbar_wait(bar_afull(n & 1), (n >> 1) & 1));
       if (MODE == kQuad && !bad) {
-        const uint32_t a_n = sA + n * C::A_BYTES;
+        const uint32_t a_n = sA + (n & 1) * C::A_BYTES;
 #pragma unroll
         for (int jj = 0; jj < D / 16; ++jj) {  // 16-byte chunks of 8 elements
           const int c = h * (D / 2) + 8 * jj;
@@ -684,13 +746,28 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   const int rows = a_is_queries<MODE>() ? a.n_q : a.T;
-  dim3 grid(((rows + BM - 1) / BM + kUnits - 1) / kUnits, a_is_queries<MODE>() ? a.Hq : a.Hkv,
-            a.L);
+  const int nrb = (rows + BM - 1) / BM, nh = a_is_queries<MODE>() ? a.Hq : a.Hkv;
+  dim3 grid((nrb + kUnits - 1) / kUnits, nh, a.L);
+  // Persistent where it measured faster: the query-side passes, and the key-side maximum
+  // once every SM has 16 or more units.  The quadratic form (whose epilogue reads A) never
+  // reuses an A buffer, so it stays blocked.
+  int strided = 0;
+  if (MODE != kQuad) {
+    static int nsm[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!nsm[dev]) cudaDeviceGetAttribute(&nsm[dev], cudaDevAttrMultiProcessorCount, dev);
+    const long units = (long)nrb * nh * a.L, sms = std::max(1, nsm[dev]);
+    if (a_is_queries<MODE>() || (MODE == kMax && units >= 16 * sms)) {
+      strided = 1;
+      grid = dim3((unsigned)std::min(units, sms), 1, 1);
+    }
+  }
   auto kern = attn_tc_kernel<D, MODE>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   count_launches(1);
-  kern<<<grid, C::THREADS, C::SMEM, s>>>(ta, tb, tb2, tauga, taugb, a);
+  kern<<<grid, C::THREADS, C::SMEM, s>>>(ta, tb, tb2, tauga, taugb, a, strided);
   return cudaGetLastError();
 }
 
