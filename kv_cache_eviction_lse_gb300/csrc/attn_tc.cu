@@ -74,7 +74,15 @@ struct Cfg {
   static constexpr int EPI = NG * kGroupThreads;
   static constexpr int THREADS = 64 + EPI;
   static constexpr int KH = D / 64;
-  static constexpr int STAGES = D == 128 ? 2 : 4;
+  static constexpr int STAGES = D == 128 ? 2 : 4;  // B tiles in the ring
+  // Ring slots per B tile.  The key-side maximum (light epilogue, MMA-bound) hands the
+  // ring out by box (64 columns of d): a tile's first box is refilled while the MMAs read
+  // its second, so the loads lead the MMAs by 1.5 tiles at d = 128 instead of one.  The
+  // other modes keep whole-tile slots: their epilogues bound them and the extra barrier
+  // traffic of box slots costs them more than the deeper lead gains.
+  static constexpr int PARTS = MODE == kMax ? KH : 1;
+  static constexpr int NS = STAGES * PARTS;
+  static constexpr uint32_t SLOT_BYTES = KH / PARTS * kBoxBytesB;
   static constexpr uint32_t A_BYTES = KH * kBoxBytesA;  // one of kUnits A buffers
   static constexpr uint32_t B_BYTES = KH * kBoxBytesB;
   static constexpr uint32_t OFF_B = kUnits * A_BYTES;
@@ -87,8 +95,8 @@ struct Cfg {
   static constexpr uint32_t OFF_X = OFF_AUG_B + (AUG ? STAGES * AUG_B_BYTES : 0);  // [2][NG-1][BM][2]
   static constexpr uint32_t OFF_P = OFF_X + 2 * (NG - 1) * BM * 2 * 4;  // kQuad [2][16][BM]
   static constexpr uint32_t OFF_BAR = OFF_P + (MODE == kQuad ? 2 * kMaxGroup * BM * 4 : 0);
-  // a_full[kUnits], full[S], empty[S], tfull[2], tempty[2], a_empty[kUnits]
-  static constexpr uint32_t NBAR = 2 * kUnits + 2 * STAGES + 4;
+  // a_full[kUnits], full[NS], empty[NS], tfull[2], tempty[2], a_empty[kUnits]
+  static constexpr uint32_t NBAR = 2 * kUnits + 2 * NS + 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t USED = OFF_MISC + 16;
   static constexpr uint32_t SMEM = (USED + 1024 <= kMaxSmem) ? USED + 1024 : kMaxSmem;
@@ -266,11 +274,12 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
   float* part = reinterpret_cast<float*>(smem + C::OFF_P);
   const uint32_t bar0 = sb + C::OFF_BAR;
   auto bar_afull = [&](int b) { return bar0 + 8u * b; };
-  auto bar_full = [&](int s) { return bar0 + 8u * (kUnits + s); };
-  auto bar_empty = [&](int s) { return bar0 + 8u * (kUnits + S + s); };
-  auto bar_tfull = [&](int x) { return bar0 + 8u * (kUnits + 2 * S + x); };
-  auto bar_tempty = [&](int x) { return bar0 + 8u * (kUnits + 2 * S + 2 + x); };
-  auto bar_aempty = [&](int b) { return bar0 + 8u * (kUnits + 2 * S + 4 + b); };
+  constexpr int NS = C::NS;  // box slots of the B ring
+  auto bar_full = [&](int j) { return bar0 + 8u * (kUnits + j); };
+  auto bar_empty = [&](int j) { return bar0 + 8u * (kUnits + NS + j); };
+  auto bar_tfull = [&](int x) { return bar0 + 8u * (kUnits + 2 * NS + x); };
+  auto bar_tempty = [&](int x) { return bar0 + 8u * (kUnits + 2 * NS + 2 + x); };
+  auto bar_aempty = [&](int b) { return bar0 + 8u * (kUnits + 2 * NS + 4 + b); };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
 
@@ -322,9 +331,9 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
       tc::mbar_init(bar_afull(n), 1);
       tc::mbar_init(bar_aempty(n), 1);
     }
-    for (int s = 0; s < S; ++s) {
-      tc::mbar_init(bar_full(s), 1);
-      tc::mbar_init(bar_empty(s), 1);
+    for (int j = 0; j < NS; ++j) {
+      tc::mbar_init(bar_full(j), 1);
+      tc::mbar_init(bar_empty(j), 1);
     }
     for (int x = 0; x < 2; ++x) {
       tc::mbar_init(bar_tfull(x), 1);
@@ -349,7 +358,7 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
   if (warp == 0) {
     // ============================================================ TMA producer
     if (lane == 0) {
-      int gt = 0, na = 0;  // B tiles and A tiles issued
+      int gt = 0, na = 0, nb = 0;  // B tiles, A tiles and B boxes issued
       // A tile of unit na into buffer na & 1, whose previous unit (na - 2) is done: the
       // MMA issuer commits a_empty of the buffer once that unit's products complete
       auto issue_a = [&]() {
@@ -377,16 +386,10 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
           issue_a();
         }
         const Tiles U = tiles_of<MODE>(a, row0, G, off);
-        for (int it = 0; it < U.ntiles; ++it, ++gt) {
+        for (int it = 0; it < U.ntiles && ok; ++it, ++gt) {
           // prefetch the next unit's A tile as soon as its buffer is free
           if (na == n + 1 && na < nunits && tc::mbar_test(bar_aempty(na & 1), ((na >> 1) & 1) ^ 1u))
             issue_a();
-          const int s = gt % S;
-          const uint32_t ph = (uint32_t)(gt / S) & 1u;
-          if (!tc::mbar_wait(bar_empty(s), ph ^ 1u) || *abort_flag) {
-            ok = false;
-            break;
-          }
           const CUtensorMap* map;
           int row, head;
           if (kQ) {
@@ -403,27 +406,37 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
             head = l * a.Hq + hk * G + it / U.per_head;
             row = (U.qt_begin + it % U.per_head) * BN;
           }
-          tc::mbar_expect_tx(bar_full(s), C::B_BYTES + (C::AUG ? C::AUG_B_BYTES : 0));
+          constexpr int BPP = C::KH / C::PARTS;  // boxes per slot
 #pragma unroll
-          for (int kh = 0; kh < C::KH; ++kh)
-            tc::tma_load_3d(sB + s * C::B_BYTES + kh * kBoxBytesB, map, bar_full(s), kh * 64, row,
-                            head);
-          if (C::AUG)  // the tile's per-query constants (rows padded to whole tiles)
-            tc::tma_load_3d(sb + C::OFF_AUG_B + s * C::AUG_B_BYTES, &tm_augb, bar_full(s), 0, row,
-                            head);
+          for (int pt = 0; pt < C::PARTS; ++pt, ++nb) {  // part pt of the tile into slot nb % NS
+            const int j = nb % NS;
+            if (!tc::mbar_wait(bar_empty(j), (uint32_t)((nb / NS) & 1) ^ 1u) || *abort_flag) {
+              ok = false;
+              break;
+            }
+            const bool last = pt == C::PARTS - 1;
+            tc::mbar_expect_tx(bar_full(j), C::SLOT_BYTES + (C::AUG && last ? C::AUG_B_BYTES : 0));
+#pragma unroll
+            for (int q = 0; q < BPP; ++q)
+              tc::tma_load_3d(sB + j * C::SLOT_BYTES + q * kBoxBytesB, map, bar_full(j),
+                              (pt * BPP + q) * 64, row, head);
+            if (C::AUG && last)  // the tile's per-query constants (rows padded to whole tiles)
+              tc::tma_load_3d(sb + C::OFF_AUG_B + (gt % S) * C::AUG_B_BYTES, &tm_augb, bar_full(j),
+                              0, row, head);
+          }
         }
       }
       if (!ok) {
         fail(abort_flag, kErrWaitTimeout);
         // let the copies already in flight land before the CTA exits
         for (int n = max(0, na - 2); n < na; ++n) tc::mbar_wait(bar_afull(n & 1), (n >> 1) & 1);
-        for (int j = max(0, gt - S); j < gt; ++j) tc::mbar_wait(bar_full(j % S), (j / S) & 1);
+        for (int u = max(0, nb - NS); u < nb; ++u) tc::mbar_wait(bar_full(u % NS), (u / NS) & 1);
       }
     }
   } else if (warp == 1) {
     // ============================================================ MMA issuer
     if (lane == 0) {
-      int gt = 0;
+      int gt = 0, nb = 0;  // B tiles and boxes consumed
       bool ok = true;
       for (int n = 0; n < nunits && ok; ++n) {
         int l, hy;
@@ -434,37 +447,46 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
           break;
         }
         const uint32_t a_n = sA + b * C::A_BYTES;
-        for (int it = 0; it < U.ntiles; ++it, ++gt) {
-          const int s = gt % S;
-          const uint32_t ph = (uint32_t)(gt / S) & 1u;
+        for (int it = 0; it < U.ntiles && ok; ++it, ++gt) {
           const int acc = gt & 1;
           const uint32_t aph = (uint32_t)(gt >> 1) & 1u;
-          if (!tc::mbar_wait(bar_tempty(acc), aph ^ 1u) || !tc::mbar_wait(bar_full(s), ph) ||
-              *abort_flag) {
+          if (!tc::mbar_wait(bar_tempty(acc), aph ^ 1u) || *abort_flag) {
             ok = false;
             break;
           }
-          tc::fence_after_sync();
           const uint32_t d_t = tmem + (uint32_t)(acc * BN);
-          const uint32_t b_s = sB + s * C::B_BYTES;
+          constexpr int BPP = C::KH / C::PARTS;  // boxes per slot
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t kh = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3) * 32u;
-            tc::mma_bf16(d_t, tc::sdesc_sw128(a_n + kh * kBoxBytesA + kk),
-                         tc::sdesc_sw128(b_s + kh * kBoxBytesB + kk), C::IDESC, k > 0 ? 1u : 0u);
+          for (int pt = 0; pt < C::PARTS; ++pt, ++nb) {  // part pt of the tile, in slot nb % NS
+            const int j = nb % NS;
+            if (!tc::mbar_wait(bar_full(j), (uint32_t)(nb / NS) & 1u) || *abort_flag) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+            const uint32_t b_j = sB + j * C::SLOT_BYTES;
+#pragma unroll
+            for (int k = 0; k < 4 * BPP; ++k) {  // 16 columns of d per MMA
+              const int kh = pt * BPP + (k >> 2);  // box of the tile
+              const uint32_t kk = (uint32_t)(k & 3) * 32u;
+              tc::mma_bf16(d_t, tc::sdesc_sw128(a_n + kh * kBoxBytesA + kk),
+                           tc::sdesc_sw128(b_j + (k >> 2) * kBoxBytesB + kk), C::IDESC,
+                           (pt | k) ? 1u : 0u);
+            }
+            if (C::AUG && pt == C::PARTS - 1)  // + (1,1,1,0..) . (c_hi, c_mid, c_lo, 0..)
+              tc::mma_bf16(d_t, tc::sdesc_sw32(sb + C::OFF_AUG_A),
+                           tc::sdesc_sw32(sb + C::OFF_AUG_B + (gt % S) * C::AUG_B_BYTES),
+                           C::IDESC, 1u);
+            tc::commit(bar_empty(j));  // the slot is free once these MMAs complete
           }
-          if (C::AUG)  // + (1,1,1,0..) . (c_hi, c_mid, c_lo, 0..): the column's constant
-            tc::mma_bf16(d_t, tc::sdesc_sw32(sb + C::OFF_AUG_A),
-                         tc::sdesc_sw32(sb + C::OFF_AUG_B + s * C::AUG_B_BYTES), C::IDESC, 1u);
-          tc::commit(bar_empty(s));
-          tc::commit(bar_tfull(acc));
+          if (ok) tc::commit(bar_tfull(acc));
         }
         // the producer reuses this A buffer for unit n + 2 once the unit's MMAs complete
         // (no commit after the last use, so nothing arrives once the CTA may have exited)
         if (n + 2 < nunits) tc::commit(bar_aempty(b));
       }
       if (!ok) fail(abort_flag, kErrWaitTimeout);
-      if (gt > 0) tc::mbar_wait(bar_empty((gt - 1) % S), ((gt - 1) / S) & 1);
+      if (nb > 0) tc::mbar_wait(bar_empty((nb - 1) % NS), (uint32_t)((nb - 1) / NS) & 1u);
     }
     __syncwarp();
   } else {
