@@ -770,9 +770,10 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
   const int rows = a_is_queries<MODE>() ? a.n_q : a.T;
   const int nrb = (rows + BM - 1) / BM, nh = a_is_queries<MODE>() ? a.Hq : a.Hkv;
   dim3 grid((nrb + kUnits - 1) / kUnits, nh, a.L);
-  // Persistent where it measured faster: the query-side passes, and the key-side maximum
-  // once every SM has 16 or more units.  The quadratic form (whose epilogue reads A) never
-  // reuses an A buffer, so it stays blocked.
+  // Persistent where it measured faster: the query-side passes and the key-side maximum.
+  // The future mass runs two units per CTA (its unit costs spread widely and the hardware
+  // scheduler balances them better), and the quadratic form (whose epilogue reads A)
+  // never reuses an A buffer, so it stays blocked.
   int strided = 0;
   if (MODE != kQuad) {
     static int nsm[64] = {0};
@@ -780,7 +781,7 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!nsm[dev]) cudaDeviceGetAttribute(&nsm[dev], cudaDevAttrMultiProcessorCount, dev);
     const long units = (long)nrb * nh * a.L, sms = std::max(1, nsm[dev]);
-    if (a_is_queries<MODE>() || (MODE == kMax && units >= 16 * sms)) {
+    if (a_is_queries<MODE>() || MODE == kMax) {
       strided = 1;
       grid = dim3((unsigned)std::min(units, sms), 1, 1);
     }
