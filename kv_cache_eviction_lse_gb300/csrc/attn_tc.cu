@@ -58,9 +58,9 @@ enum Mode { kLse = 0, kMax = 1, kFuture = 2, kQuad = 3, kRows = 4 };
 // modes whose operand A is a tile of queries (B: key tiles)
 template <int MODE>
 __host__ __device__ constexpr bool a_is_queries() { return MODE == kLse || MODE == kRows; }
-// 128-row units of operand A per CTA, each with its own A buffer (loaded up front), so the
-// second unit's MMAs start while the epilogue drains the first.  A buffers are never
-// reused within a CTA, which keeps the kQuad epilogue's reads of A free of races.
+// Two A buffers per CTA, alternating between consecutive units, so the next unit's MMAs
+// start while the epilogue drains the current one (and, on a blocked grid, a CTA's two
+// units each have their own).
 constexpr int kUnits = 2;
 constexpr int kMaxGroup = 16;  // query heads per KV head handled by kQuad
 
@@ -329,7 +329,9 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int n = 0; n < kUnits; ++n) {
       tc::mbar_init(bar_afull(n), 1);
-      tc::mbar_init(bar_aempty(n), 1);
+      // the quadratic form's epilogue reads its value rows from A, so its threads also
+      // release the buffer
+      tc::mbar_init(bar_aempty(n), MODE == kQuad ? 1 + C::EPI : 1);
     }
     for (int j = 0; j < NS; ++j) {
       tc::mbar_init(bar_full(j), 1);
@@ -547,6 +549,8 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
           vrow[4 * jj + 2] = u.z;
           vrow[4 * jj + 3] = u.w;
         }
+        // the rows are in registers: the buffer may take unit n + 2 once the MMAs are done
+        if (n + 2 < nunits) tc::mbar_arrive(bar_aempty(n & 1));
       }
 
       for (int it = 0; it < U.ntiles && !bad; ++it, ++gt) {
@@ -770,18 +774,17 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
   const int rows = a_is_queries<MODE>() ? a.n_q : a.T;
   const int nrb = (rows + BM - 1) / BM, nh = a_is_queries<MODE>() ? a.Hq : a.Hkv;
   dim3 grid((nrb + kUnits - 1) / kUnits, nh, a.L);
-  // Persistent where it measured faster: the query-side passes and the key-side maximum.
-  // The future mass runs two units per CTA (its unit costs spread widely and the hardware
-  // scheduler balances them better), and the quadratic form (whose epilogue reads A)
-  // never reuses an A buffer, so it stays blocked.
+  // Persistent where it measured faster: the query-side passes, the key-side maximum and
+  // the quadratic form.  The future mass runs two units per CTA (its unit costs spread
+  // widely and the hardware scheduler balances them better).
   int strided = 0;
-  if (MODE != kQuad) {
+  {
     static int nsm[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!nsm[dev]) cudaDeviceGetAttribute(&nsm[dev], cudaDevAttrMultiProcessorCount, dev);
     const long units = (long)nrb * nh * a.L, sms = std::max(1, nsm[dev]);
-    if (a_is_queries<MODE>() || MODE == kMax) {
+    if (MODE != kFuture) {
       strided = 1;
       grid = dim3((unsigned)std::min(units, sms), 1, 1);
     }
