@@ -29,28 +29,33 @@ constexpr int BT = 128;                 // output tile edge
 constexpr int BK = 64;                  // rows per k-block
 constexpr uint32_t kBox = 64 * 128;     // 64 rows x 64 bf16 = 8 KB
 constexpr uint32_t kOp = 2 * kBox;      // one 128-column operand tile of a k-block
-constexpr uint32_t kRing = 3 * 4 * kOp;  // operand ring: 192 KB
+constexpr uint32_t kRing = 3 * 4 * kOp;  // operand ring of the refit products: 192 KB
+// The value-norm Gram streams one operand (16 KB per k-block) straight from HBM; a
+// 4-stage ring lets three CTAs share an SM, so all (layer, head) tiles of a call run at
+// once and the heads of a layer walk the rows of o_proj.weight together.
+constexpr uint32_t kRingDiag = 4 * kOp;
 constexpr int kMaxStages = 12;          // stages of (X hi, [X lo], [Y hi], [Y lo]) tiles
 constexpr int kThreads = 64 + 128;
 constexpr uint32_t kTmemCols = 128;
-constexpr uint32_t OFF_BAR = kRing;
+constexpr uint32_t OFF_BAR = 0;  // barriers and the TMEM address first, the ring after
 constexpr uint32_t NBAR = 2 * kMaxStages + 1;  // full[S], empty[S], done
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr uint32_t USED = OFF_MISC + 16;
+constexpr uint32_t OFF_RING = 1024;
+static_assert(OFF_MISC + 16 <= OFF_RING, "barrier block");
 static_assert(kRing % (4 * kOp) == 0 && kRing / kOp <= 3 * 4, "operand ring");
-constexpr uint32_t SMEM = USED + 1024;
-static_assert(SMEM <= 232448, "shared-memory plan exceeds the per-block limit");
+__host__ __device__ constexpr uint32_t smem_bytes(uint32_t ring) { return OFF_RING + ring + 1024; }
+static_assert(smem_bytes(kRing) <= 232448, "shared-memory plan exceeds the per-block limit");
 constexpr int kErrWaitTimeout = 1;
 constexpr int kErrSmemAlign = 3;
 
 __global__ void __launch_bounds__(kThreads, 1)
     gram_tc_kernel(const __grid_constant__ CUtensorMap tm_xhi, const __grid_constant__ CUtensorMap tm_xlo,
                    const __grid_constant__ CUtensorMap tm_yhi, const __grid_constant__ CUtensorMap tm_ylo,
-                   const GramArgs a) {
+                   const GramArgs a, const uint32_t ring) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-  if (pad + USED > SMEM) {
+  if (pad + OFF_RING + ring > smem_bytes(ring)) {
     if (threadIdx.x == 0) atomicCAS(&g_gram_error, 0, kErrSmemAlign);
     return;
   }
@@ -87,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // deeper ring (3 stages for the split Gram, up to 12 for the value-norm Gram)
   const int nop = 1 + (x_split ? 1 : 0) + (diag ? 0 : 1) + (y_split ? 1 : 0);
   const uint32_t stage_bytes = nop * kOp;
-  const int kStages = min(kMaxStages, (int)(kRing / stage_bytes));
+  const int kStages = min(kMaxStages, (int)(ring / stage_bytes));
   const uint32_t o_xlo = kOp, o_yhi = (1 + (x_split ? 1 : 0)) * kOp, o_ylo = o_yhi + kOp;
 
   if (threadIdx.x == 0) {
@@ -116,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const uint32_t st = sb + s * stage_bytes;
+        const uint32_t st = sb + OFF_RING + s * stage_bytes;
         tc::mbar_expect_tx(bar_full(s), stage_bytes);
         for (int c = 0; c < 2; ++c) {  // two 64-column boxes per operand tile
           tc::tma_load_3d(st + c * kBox, &tm_xhi, bar_full(s), tm * BT + 64 * c, kb * BK, b);
@@ -149,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc::fence_after_sync();
-        const uint32_t st = sb + s * stage_bytes;
+        const uint32_t st = sb + OFF_RING + s * stage_bytes;
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k) {
           const uint32_t o = 2048u * k;  // 16 rows of 128 bytes
@@ -251,10 +256,12 @@ cudaError_t launch_gram(const GramArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int tmn = (a.M + BT - 1) / BT, tnn = (a.N + BT - 1) / BT;
   const int tiles = diag ? tmn : a.upper ? tmn * (tmn + 1) / 2 : tmn * tnn;
-  e = cudaFuncSetAttribute(gram_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+  const uint32_t ring = diag ? kRingDiag : kRing, smem = smem_bytes(ring);
+  e = cudaFuncSetAttribute(gram_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_bytes(kRing));
   if (e != cudaSuccess) return e;
   count_launches(1);
-  gram_tc_kernel<<<dim3(tiles, a.batch), kThreads, SMEM, s>>>(xh, xl, yh, yl, a);
+  gram_tc_kernel<<<dim3(tiles, a.batch), kThreads, smem, s>>>(xh, xl, yh, yl, a, ring);
   return cudaGetLastError();
 }
 
