@@ -51,62 +51,117 @@ __global__ void __launch_bounds__(256) shift_kernel(const CholArgs a) {
     R[(size_t)a.k * a.d + idx] = 0.f;
 }
 
-// Cholesky of the diagonal block at p (upper, in place), one CTA per problem
-__global__ void __launch_bounds__(256) potrf_kernel(const CholArgs a, int p) {
+// The diagonal-block kernels run once per panel with one small CTA per problem, so they
+// are latency chains and their code is fetched once per launch: fully unrolled 64 x 64
+// loops (thousands of instructions) are bound by that fetch.  Each keeps a column in
+// registers under a rolled pivot loop instead: the column is shifted by one register per
+// step (x[i] holds row r + i), fused with the update x[i-1] = x[i] - w[i] x[0], so the
+// pivot is always x[0] and the step's line of U is staged pre-shifted (w[i] = U[r][r+i])
+// for aligned 16-byte reads.
+
+// Cholesky of the diagonal block at p (upper, in place), one CTA of 64 threads per
+// problem: thread c keeps column c of the block in registers; per pivot r the owner of
+// column r takes the square root, every later column scales its row-r entry, stores it
+// and publishes it, and each column applies the rank-1 update to its own entries.
+__global__ void __launch_bounds__(NB) potrf_kernel(const CholArgs a, int p) {
   float* G = prob(a.g, (size_t)a.M * a.ldg) + (size_t)p * a.ldg + p;
-  __shared__ float u[NB][NB + 1];
-  for (int idx = threadIdx.x; idx < NB * NB; idx += 256) {
-    const int r = idx / NB, c = idx % NB;
-    u[r][c] = c >= r ? G[(size_t)r * a.ldg + c] : 0.f;
+  const int c = threadIdx.x;
+  __shared__ __align__(16) float prow[NB];  // prow[i] = U[r][r + i] (i >= 1), 0 past the block
+  __shared__ float pinv;
+  float x[NB];
+#pragma unroll
+  for (int i = 0; i < NB; ++i) x[i] = i <= c ? G[(size_t)i * a.ldg + c] : 0.f;
+  prow[c] = 0.f;
+#pragma unroll 1
+  for (int r = 0; r < NB; ++r) {
+    if (c == r) {
+      const float v = x[0];
+      if (!(v > 0.f)) atomicCAS(&g_chol_error, 0, kErrNotSpd);
+      const float piv = sqrtf(fmaxf(v, 1e-30f));
+      G[(size_t)r * a.ldg + r] = piv;
+      pinv = 1.f / piv;
+    }
+    __syncthreads();
+    float xr = 0.f;
+    if (c > r) {
+      xr = x[0] * pinv;
+      G[(size_t)r * a.ldg + c] = xr;
+      prow[c - r] = xr;
+    }
+    __syncthreads();
+    // columns c > r: rows r+1 .. c; past c the registers hold nothing that is stored
+#pragma unroll
+    for (int i4 = 0; i4 < NB; i4 += 4) {
+      const float4 w = *reinterpret_cast<const float4*>(&prow[i4]);
+      const float wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (i4 + e >= 1) x[i4 + e - 1] = fmaf(-wv[e], xr, x[i4 + e]);
+    }
+    x[NB - 1] = 0.f;
+    __syncthreads();  // prow is rewritten by the next pivot
+    if (c > r) prow[c - r] = 0.f;
+  }
+}
+
+// Triangular solve of 64 rows in registers against the staged diagonal block (rows of w
+// pre-shifted as above, dinv = 1 / diag), one column per thread; row r of the solution
+// is written to out[r * ld] as soon as it is final.  Forward: U^T y = x with x[i] = row i
+// initially; backward: U y = x with x[i] = row 63 - i initially.
+template <bool BACKWARD>
+__device__ __forceinline__ void tri_solve_col(float (&x)[NB], const float (*w)[NB],
+                                              const float* dinv, float* out, size_t ld) {
+#pragma unroll 1
+  for (int k = 0; k < NB; ++k) {
+    const int r = BACKWARD ? NB - 1 - k : k;
+    const float xr = x[0] * dinv[r];
+    out[(size_t)r * ld] = xr;
+#pragma unroll
+    for (int i4 = 0; i4 < NB; i4 += 4) {
+      const float4 q = *reinterpret_cast<const float4*>(&w[r][i4]);
+      const float qv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (i4 + e >= 1) x[i4 + e - 1] = fmaf(-qv[e], xr, x[i4 + e]);
+    }
+    x[NB - 1] = 0.f;
+  }
+}
+
+// Stages the diagonal block at p pre-shifted for a forward solve (w[r][i] = U[r][r+i]) or
+// a backward one (w[r][i] = U[r-i][r]), zero past the block, and 1 / diag (nt threads).
+__device__ __forceinline__ void load_diag_block(const float* G, int ldg, int p, int nt,
+                                                bool backward, float (*w)[NB], float* dinv) {
+  for (int idx = threadIdx.x; idx < NB * NB; idx += nt) w[idx / NB][idx % NB] = 0.f;
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < NB * NB; idx += nt) {
+    const int r = idx / NB, c = idx % NB;  // U[r][c], c >= r
+    if (c >= r) {
+      const float v = G[(size_t)(p + r) * ldg + p + c];
+      if (backward)
+        w[c][c - r] = v;
+      else
+        w[r][c - r] = v;
+    }
   }
   __syncthreads();
-  for (int r = 0; r < NB; ++r) {
-    if (threadIdx.x == 0) {
-      const float v = u[r][r];
-      if (!(v > 0.f)) atomicCAS(&g_chol_error, 0, kErrNotSpd);
-      u[r][r] = sqrtf(fmaxf(v, 1e-30f));
-    }
-    __syncthreads();
-    const float piv = u[r][r];
-    if (threadIdx.x > r && threadIdx.x < NB) u[r][threadIdx.x] /= piv;
-    __syncthreads();
-    // rank-1 update of rows s > r, columns c >= s
-    for (int idx = threadIdx.x; idx < NB * NB; idx += 256) {
-      const int s = idx / NB, c = idx % NB;
-      if (s > r && c >= s) u[s][c] -= u[r][s] * u[r][c];
-    }
-    __syncthreads();
-  }
-  for (int idx = threadIdx.x; idx < NB * NB; idx += 256) {
-    const int r = idx / NB, c = idx % NB;
-    if (c >= r) G[(size_t)r * a.ldg + c] = u[r][c];
-  }
+  if (threadIdx.x < NB) dinv[threadIdx.x] = 1.f / w[threadIdx.x][0];
+  __syncthreads();
 }
 
 // Row panel: G[p..p+64][j] = U_pp^-T G[p..p+64][j] for the 64 columns j of block
 // blockIdx.x after the diagonal block; one thread per column
-__global__ void __launch_bounds__(64) trsm_row_kernel(const CholArgs a, int p) {
+__global__ void __launch_bounds__(NB) trsm_row_kernel(const CholArgs a, int p) {
   float* G = prob(a.g, (size_t)a.M * a.ldg);
   const int j = p + NB + blockIdx.x * NB + threadIdx.x;
-  __shared__ float u[NB][NB + 1];
-  for (int idx = threadIdx.x; idx < NB * NB; idx += 64) {
-    const int r = idx / NB, c = idx % NB;
-    u[r][c] = c >= r ? G[(size_t)(p + r) * a.ldg + p + c] : 0.f;
-  }
-  __syncthreads();
+  __shared__ __align__(16) float w[NB][NB];
+  __shared__ float dinv[NB];
+  load_diag_block(G, a.ldg, p, NB, false, w, dinv);
   if (j >= a.M) return;
   float x[NB];
 #pragma unroll
   for (int r = 0; r < NB; ++r) x[r] = G[(size_t)(p + r) * a.ldg + j];
-#pragma unroll
-  for (int r = 0; r < NB; ++r) {
-    float v = x[r];
-#pragma unroll
-    for (int s = 0; s < r; ++s) v = fmaf(-u[s][r], x[s], v);
-    x[r] = v / u[r][r];
-  }
-#pragma unroll
-  for (int r = 0; r < NB; ++r) G[(size_t)(p + r) * a.ldg + j] = x[r];
+  tri_solve_col<false>(x, w, dinv, G + (size_t)p * a.ldg + j, a.ldg);
 }
 
 // Trailing update of the upper triangle after panel p: tile (ti, tj), ti <= tj, of the
@@ -154,39 +209,19 @@ __global__ void __launch_bounds__(256) syrk_kernel(const CholArgs a, int p) {
 
 // Triangular solve of block row p of the right-hand sides, one thread per column:
 // forward (U_pp^T y = r) or backward (U_pp x = y)
-__global__ void __launch_bounds__(128) solve_diag_kernel(const CholArgs a, int p, int backward) {
+template <bool BACKWARD>
+__global__ void __launch_bounds__(128) solve_diag_kernel(const CholArgs a, int p) {
   const float* G = prob(a.g, (size_t)a.M * a.ldg);
   float* R = prob(a.r, (size_t)a.M * a.d);
-  __shared__ float u[NB][NB + 1];
-  for (int idx = threadIdx.x; idx < NB * NB; idx += 128) {
-    const int r = idx / NB, c = idx % NB;
-    u[r][c] = c >= r ? G[(size_t)(p + r) * a.ldg + p + c] : 0.f;
-  }
-  __syncthreads();
+  __shared__ __align__(16) float w[NB][NB];
+  __shared__ float dinv[NB];
+  load_diag_block(G, a.ldg, p, 128, BACKWARD, w, dinv);
   const int c = blockIdx.x * 128 + threadIdx.x;
   if (c >= a.d) return;
   float x[NB];
 #pragma unroll
-  for (int r = 0; r < NB; ++r) x[r] = R[(size_t)(p + r) * a.d + c];
-  if (!backward) {
-#pragma unroll
-    for (int r = 0; r < NB; ++r) {
-      float v = x[r];
-#pragma unroll
-      for (int s = 0; s < r; ++s) v = fmaf(-u[s][r], x[s], v);
-      x[r] = v / u[r][r];
-    }
-  } else {
-#pragma unroll
-    for (int r = NB - 1; r >= 0; --r) {
-      float v = x[r];
-#pragma unroll
-      for (int s = r + 1; s < NB; ++s) v = fmaf(-u[r][s], x[s], v);
-      x[r] = v / u[r][r];
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < NB; ++r) R[(size_t)(p + r) * a.d + c] = x[r];
+  for (int i = 0; i < NB; ++i) x[i] = R[(size_t)(p + (BACKWARD ? NB - 1 - i : i)) * a.d + c];
+  tri_solve_col<BACKWARD>(x, w, dinv, R + (size_t)p * a.d + c, a.d);
 }
 
 // Update of the block rows after (forward) or before (backward) block p:
@@ -200,9 +235,12 @@ __global__ void __launch_bounds__(256) solve_update_kernel(const CholArgs a, int
   __shared__ __align__(16) float us[NB][NB + 4];  // [r][q]: coefficient of row r of block p in row q
   __shared__ __align__(16) float ys[NB][NB + 4];  // [r][c]: solved rows of block p
   for (int idx = threadIdx.x; idx < NB * NB; idx += 256) {
-    const int r = idx / NB, q = idx % NB;
-    us[r][q] = backward ? G[(size_t)(q0 + q) * a.ldg + p + r] : G[(size_t)(p + r) * a.ldg + q0 + q];
-    ys[r][q] = R[(size_t)(p + r) * a.d + c0 + q];
+    const int i = idx / NB, j = idx % NB;  // consecutive threads read consecutive addresses
+    if (backward)
+      us[j][i] = G[(size_t)(q0 + i) * a.ldg + p + j];
+    else
+      us[i][j] = G[(size_t)(p + i) * a.ldg + q0 + j];
+    ys[i][j] = R[(size_t)(p + i) * a.d + c0 + j];
   }
   __syncthreads();
   const int tq = (threadIdx.x / 16) * 4, tc = (threadIdx.x % 16) * 4;
@@ -247,17 +285,17 @@ cudaError_t launch_chol_solve(const CholArgs& a, cudaStream_t s) {
   ++launches;
   for (int b = 0; b < nb; ++b) {  // G + lam I = U^T U
     const int p = b * NB, rest = nb - b - 1;
-    potrf_kernel<<<dim3(1, B), 256, 0, s>>>(a, p);
+    potrf_kernel<<<dim3(1, B), NB, 0, s>>>(a, p);
     ++launches;
     if (rest > 0) {
-      trsm_row_kernel<<<dim3(rest, B), 64, 0, s>>>(a, p);
+      trsm_row_kernel<<<dim3(rest, B), NB, 0, s>>>(a, p);
       syrk_kernel<<<dim3(rest * (rest + 1) / 2, B), 256, 0, s>>>(a, p);
       launches += 2;
     }
   }
   for (int b = 0; b < nb; ++b) {  // U^T Y = R
     const int p = b * NB, rest = nb - b - 1;
-    solve_diag_kernel<<<dim3((a.d + 127) / 128, B), 128, 0, s>>>(a, p, 0);
+    solve_diag_kernel<false><<<dim3((a.d + 127) / 128, B), 128, 0, s>>>(a, p);
     ++launches;
     if (rest > 0) {
       solve_update_kernel<<<dim3(rest, B, dcb), 256, 0, s>>>(a, p, 0);
@@ -266,7 +304,7 @@ cudaError_t launch_chol_solve(const CholArgs& a, cudaStream_t s) {
   }
   for (int b = nb - 1; b >= 0; --b) {  // U X = Y
     const int p = b * NB;
-    solve_diag_kernel<<<dim3((a.d + 127) / 128, B), 128, 0, s>>>(a, p, 1);
+    solve_diag_kernel<true><<<dim3((a.d + 127) / 128, B), 128, 0, s>>>(a, p);
     ++launches;
     if (b > 0) {
       solve_update_kernel<<<dim3(b, B, dcb), 256, 0, s>>>(a, p, 1);
