@@ -93,7 +93,11 @@ struct Cfg {
   static constexpr uint32_t OFF_AUG_A = OFF_B + STAGES * B_BYTES;
   static constexpr uint32_t OFF_AUG_B = OFF_AUG_A + (AUG ? AUG_A_BYTES : 0);
   static constexpr uint32_t OFF_X = OFF_AUG_B + (AUG ? STAGES * AUG_B_BYTES : 0);  // [2][NG-1][BM][2]
-  static constexpr uint32_t OFF_P = OFF_X + 2 * (NG - 1) * BM * 2 * 4;  // kQuad [2][16][BM]
+  // the softmax rows need no exchange of partials; their warps stage 32 rows x 64 bytes
+  // each instead, so the rows leave in whole 64-byte segments
+  static constexpr uint32_t ROWS_STAGE = 32 * 64;
+  static constexpr uint32_t OFF_P =
+      OFF_X + (MODE == kRows ? (EPI / 32) * ROWS_STAGE : 2 * (NG - 1) * BM * 2 * 4);  // kQuad [2][16][BM]
   static constexpr uint32_t OFF_BAR = OFF_P + (MODE == kQuad ? 2 * kMaxGroup * BM * 4 : 0);
   // a_full[kUnits], full[NS], empty[NS], tfull[2], tempty[2], a_empty[kUnits]
   static constexpr uint32_t NBAR = 2 * kUnits + 2 * NS + 4;
@@ -195,31 +199,56 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
-// Softmax weights of 64 columns (keys kb .. kb+63) of one query row, written as bf16
-// hi and lo parts (p = hi + lo to ~2^-17): p = 2^(x sc2 - l2), 0 for keys >= lim.
-// Columns at or past ld (the padded row length) are not written.
+// Softmax weights of 32 columns (keys kb .. kb+31) of the warp's 32 query rows, written
+// as bf16 hi and lo parts (p = hi + lo to ~2^-17): p = 2^(x sc2 - l2), 0 for keys >= lim.
+// Each thread computes its own row; the rows then pass through the warp's 2 KB stage (32
+// rows x 64 bytes), so every store instruction writes eight whole 64-byte row segments
+// (a thread writing 16 bytes into each of 32 rows would make 32 transactions).
+// row_base = element offset of the warp's first row (row stride ld); rows at or past
+// nvalid (from the warp's first row) and columns at or past ld are not written.
 __device__ __forceinline__ void rows_cols(const uint32_t* v, int kb, int lim, float l2, float sc2,
-                                          bf16_t* hi, bf16_t* lo, int ld, bool valid) {
-  if (!valid) return;
+                                          bf16_t* hi, bf16_t* lo, size_t row_base, int ld,
+                                          int nvalid, uint8_t* stage, int lane) {
+  if (kb >= ld) return;  // warp-uniform: ld is a multiple of 64, kb of 32
+  const uint32_t sbase = smem_u32(stage);
+  {
+    float pv[32];
 #pragma unroll
-  for (int c8 = 0; c8 < 8; ++c8) {
-    const int k0 = kb + 8 * c8;
-    if (k0 >= ld) break;
-    uint32_t wh[4], wl[4];
+    for (int c = 0; c < 32; ++c)
+      pv[c] = (kb + c < lim) ? fast_exp2(fmaf(__uint_as_float(v[c]), sc2, -l2)) : 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float p[2];
+    for (int part = 0; part < 2; ++part) {
+      // this row's 64 bytes into the stage, 16-byte chunk j at position j ^ (row & 3)
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int c = 8 * c8 + 2 * e + u;
-        p[u] = (k0 + 2 * e + u < lim) ? fast_exp2(fmaf(__uint_as_float(v[c]), sc2, -l2)) : 0.f;
+      for (int j = 0; j < 4; ++j) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = pv[8 * j + 2 * e], p1 = pv[8 * j + 2 * e + 1];
+          const uint32_t h = pack2_bf16(p0, p1);
+          w4[e] = part ? pack2_bf16(p0 - __uint_as_float(h << 16),
+                                    p1 - __uint_as_float(h & 0xffff0000u))
+                       : h;
+        }
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                         sbase + (uint32_t)(lane * 64 + ((j ^ (lane & 3)) << 4))),
+                     "r"(w4[0]), "r"(w4[1]), "r"(w4[2]), "r"(w4[3])
+                     : "memory");
       }
-      wh[e] = pack2_bf16(p[0], p[1]);
-      const float h0 = __uint_as_float(wh[e] << 16), h1 = __uint_as_float(wh[e] & 0xffff0000u);
-      wl[e] = pack2_bf16(p[0] - h0, p[1] - h1);
+      __syncwarp();
+      bf16_t* out = (part ? lo : hi) + row_base + kb;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {  // lanes 4i..4i+3 write row 8q + i, 16 bytes each
+        const int r = 8 * q + (lane >> 2), j = lane & 3;
+        uint4 u;
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+                     : "r"(sbase + (uint32_t)(r * 64 + ((j ^ (r & 3)) << 4)))
+                     : "memory");
+        if (r < nvalid) *reinterpret_cast<uint4*>(out + (size_t)r * ld + 8 * j) = u;
+      }
+      __syncwarp();
     }
-    *reinterpret_cast<uint4*>(hi + k0) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-    *reinterpret_cast<uint4*>(lo + k0) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
   }
 }
 
@@ -509,13 +538,10 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
       const int hk = kQ ? hy / G : hy;
       const int ra = U.row0 + row;  // this thread's query (kLse, kRows) or key
       float l2row = 0.f;              // kRows: this query's LSE in log2 units
-      bf16_t *rhi = nullptr, *rlo = nullptr;
-      if (MODE == kRows && ra < a.n_q) {
-        const size_t r = (size_t)(l * a.Hq + hq_a) * a.n_q + ra;
-        l2row = a.lse[r] * kLog2e;
-        rhi = a.rows_hi + r * a.rows_ld;
-        rlo = a.rows_lo + r * a.rows_ld;
-      }
+      // kRows: the warp's first row (of 32) in the output and how many of its rows exist
+      const int warp_row0 = U.row0 + eq * 32;
+      const size_t rows_base = ((size_t)(l * a.Hq + hq_a) * a.n_q + warp_row0) * a.rows_ld;
+      if (MODE == kRows && ra < a.n_q) l2row = a.lse[(size_t)(l * a.Hq + hq_a) * a.n_q + ra] * kLog2e;
 
       auto ln_vn = [&](int it) -> float {  // ln ||W_O v|| of this key for the head of tile it
         if (!a.vnorm || ra >= a.T) return 0.f;
@@ -589,42 +615,55 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
         } else {
           // this group's COLS columns; the accumulator is released as soon as they are in
           // registers, so the MMA of tile it+2 can start while they reduce
-          uint32_t v[COLS];
           const uint32_t ta = t_lane + (uint32_t)(acc * BN);
-#pragma unroll
-          for (int c = 0; c < COLS; c += 32) tc::tmem_ld32(ta + c, v + c);
-          tc::tmem_ld_wait();
-          tc::fence_before_sync();
-          tc::mbar_arrive(bar_tempty(acc));
-#pragma unroll
-          for (int c0 = 0; c0 < COLS; c0 += 64) {
-            uint32_t* w = v + c0;
-            if (MODE == kLse) {
-              const bool ctx = it < U.n_ctx;
-              const int kb = (ctx ? it * BN : a.T + (it - U.n_ctx) * BN) + h * COLS + c0;
-              const int lim = ctx ? a.T : n_k;
-              if (kb + 64 > lim || kb + 63 > off + ra) {
-#pragma unroll
-                for (int c = 0; c < 64; ++c)
-                  if (kb + c >= lim || kb + c > off + ra) w[c] = __float_as_uint(-CUDART_INF_F);
-              }
-              lse_cols(w, sc2, m, ssum);
-            } else if (MODE == kRows) {
-              // softmax weights 2^(x sc2 - lse log2 e) of this row, as bf16 hi + lo parts
-              rows_cols(w, it * BN + h * COLS + c0, a.T, l2row, sc2, rhi, rlo, a.rows_ld,
-                        ra < a.n_q);
-            } else if (MODE == kMax) {
-              r = max_raw_cols(w, r);  // q.k / scale-units minus the column's constant
-            } else {
-              const int j0 = (U.qt_begin + it % U.per_head) * BN + h * COLS + c0;
-              const bool band = j0 < U.row0 + BM - 1 + a.w;
-              f += future_cols(w, sc2, band, ra + a.w - j0);
+          if constexpr (MODE == kRows) {
+            // softmax weights of this tile's columns, 32 at a time (their registers are the
+            // kernel's tightest), written through the warp's stage; then the accumulator
+            // is released
+#pragma unroll 1
+            for (int c = 0; c < COLS; c += 32) {
+              uint32_t v32[32];
+              tc::tmem_ld32(ta + c, v32);
+              tc::tmem_ld_wait();
+              rows_cols(v32, it * BN + h * COLS + c, a.T, l2row, sc2, a.rows_hi, a.rows_lo,
+                        rows_base, a.rows_ld, a.n_q - warp_row0,
+                        smem + C::OFF_X + (warp - 2) * C::ROWS_STAGE, lane);
             }
-          }
-          if (MODE == kMax && (it + 1) % U.per_head == 0) {  // last query tile of this head
-            tot = fmaxf(tot, r * scale + lv);
-            r = -CUDART_INF_F;
-            if (it + 1 < U.ntiles) lv = ln_vn(it + 1);
+            tc::fence_before_sync();
+            tc::mbar_arrive(bar_tempty(acc));
+          } else {
+            uint32_t v[COLS];
+#pragma unroll
+            for (int c = 0; c < COLS; c += 32) tc::tmem_ld32(ta + c, v + c);
+            tc::tmem_ld_wait();
+            tc::fence_before_sync();
+            tc::mbar_arrive(bar_tempty(acc));
+#pragma unroll
+            for (int c0 = 0; c0 < COLS; c0 += 64) {
+              uint32_t* w = v + c0;
+              if (MODE == kLse) {
+                const bool ctx = it < U.n_ctx;
+                const int kb = (ctx ? it * BN : a.T + (it - U.n_ctx) * BN) + h * COLS + c0;
+                const int lim = ctx ? a.T : n_k;
+                if (kb + 64 > lim || kb + 63 > off + ra) {
+#pragma unroll
+                  for (int c = 0; c < 64; ++c)
+                    if (kb + c >= lim || kb + c > off + ra) w[c] = __float_as_uint(-CUDART_INF_F);
+                }
+                lse_cols(w, sc2, m, ssum);
+              } else if (MODE == kMax) {
+                r = max_raw_cols(w, r);  // q.k / scale-units minus the column's constant
+              } else {
+                const int j0 = (U.qt_begin + it % U.per_head) * BN + h * COLS + c0;
+                const bool band = j0 < U.row0 + BM - 1 + a.w;
+                f += future_cols(w, sc2, band, ra + a.w - j0);
+              }
+            }
+            if (MODE == kMax && (it + 1) % U.per_head == 0) {  // last query tile of this head
+              tot = fmaxf(tot, r * scale + lv);
+              r = -CUDART_INF_F;
+              if (it + 1 < U.ntiles) lv = ln_vn(it + 1);
+            }
           }
         }
       }
