@@ -9,15 +9,18 @@
 //
 // One CTA per 128 queries of one head; keys in tiles of 128 (online softmax):
 //   warp 0      TMA: the Q tile once, then K and V tiles through two 2-stage rings
-//   warp 1      owns TMEM (S double buffer: 2 x 128 columns; O: d columns) and issues
-//               S(j) = Q K(j)^T, then O += P(j-1) V(j-1) (P from shared memory,
-//               V as an MN-major operand straight from its TMA box)
+//   warp 1      owns TMEM (three S/P buffers: 3 x 128 columns; O: d columns) and issues
+//               S(j) = Q K(j)^T, then O += P(j-1) V(j-1) with P read from TMEM as the A
+//               operand and V as an MN-major operand straight from its TMA box
 //   warps 2-9   softmax, two threads per query row (one per 64-key half): read S with
 //               tcgen05.ld, agree on the row max through shared memory, p = 2^(x - m)
-//               with one ex2 each, write P (bf16, 128-byte swizzled K-major) for the
-//               MMA, and rescale O in TMEM when the running max grows by more than
-//               2^8 (otherwise the stale max is kept: p <= 256 stays exact enough in
-//               bf16 and the final normalisation uses the same max)
+//               with one ex2 each, store P as bf16 over the S columns just read
+//               (tcgen05.st), and rescale O in TMEM when the running max grows by more
+//               than 2^8 (otherwise the stale max is kept: p <= 256 stays exact enough
+//               in bf16 and the final normalisation uses the same max)
+// P never leaves TMEM, so the softmax of tile j only waits for O += P(j-1) V(j-1) when
+// it has to rescale O; an S/P buffer is released by the MMA that consumed its P, and with
+// three buffers S(j) waits for P V(j-3), which the tensor pipe finished long before.
 // The epilogue divides O by the row sum, writes it as bf16 and writes the LSE.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -41,6 +44,7 @@ constexpr int kSoftThreads = NQ * 128;
 constexpr int kThreads = 64 + kSoftThreads;
 constexpr uint32_t kBox = 128 * 128;  // 128 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr uint32_t kTmemCols = 512;
+constexpr int NSB = 3;  // S/P buffers in TMEM (O takes the columns after them)
 constexpr uint32_t kMaxSmem = 232448;
 constexpr int kErrWaitTimeout = 1;
 constexpr int kErrSmemAlign = 3;
@@ -54,12 +58,12 @@ struct FCfg {
   static constexpr uint32_t OFF_V = OFF_K + 2 * TILE;
   // separate K and V rings: K(j) is released as soon as S(j) = Q K(j)^T is done, so the
   // load of K(j+2) overlaps the softmax and P V of tile j; V(j) is held until P V(j)
-  static constexpr uint32_t OFF_P = OFF_V + 2 * TILE;      // P: 2 boxes of 64 keys
-  static constexpr uint32_t OFF_XM = OFF_P + 2 * kBox;     // row max exchange [2][NQ][BM]
+  static constexpr uint32_t OFF_XM = OFF_V + 2 * TILE;     // row max exchange [2][NQ][BM]
   static constexpr uint32_t OFF_XL = OFF_XM + 2 * NQ * BM * 4;  // row sum exchange [NQ][BM]
   static constexpr uint32_t OFF_BAR = OFF_XL + NQ * BM * 4;
-  // q, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p, o, done
-  static constexpr uint32_t NBAR = 16;
+  // q, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[3], s_empty[3], p[2], o[2], done
+  static constexpr uint32_t NBAR = 20;
+  static_assert(NSB * BN + D <= (int)kTmemCols, "TMEM plan");
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t USED = OFF_MISC + 16;
   static constexpr uint32_t SMEM = (USED + 1024 <= kMaxSmem) ? USED + 1024 : kMaxSmem;
@@ -95,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   uint8_t* smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
-  const uint32_t sQ = sb, sK = sb + C::OFF_K, sV = sb + C::OFF_V, sP = sb + C::OFF_P;
+  const uint32_t sQ = sb, sK = sb + C::OFF_K, sV = sb + C::OFF_V;
   float* xm = reinterpret_cast<float*>(smem + C::OFF_XM);
   float* xl = reinterpret_cast<float*>(smem + C::OFF_XL);
   const uint32_t bar0 = sb + C::OFF_BAR;
@@ -104,11 +108,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_kempty = [&](int s) { return bar0 + 8u * (3 + s); };
   auto bar_vfull = [&](int s) { return bar0 + 8u * (5 + s); };
   auto bar_vempty = [&](int s) { return bar0 + 8u * (7 + s); };
-  auto bar_sfull = [&](int s) { return bar0 + 8u * (9 + s); };
-  auto bar_sempty = [&](int s) { return bar0 + 8u * (11 + s); };
-  const uint32_t bar_p = bar0 + 8u * 13;
-  const uint32_t bar_o = bar0 + 8u * 14;
-  const uint32_t bar_done = bar0 + 8u * 15;
+  auto bar_sfull = [&](int s) { return bar0 + 8u * (9 + s); };    // S buffer s = j % NSB
+  auto bar_sempty = [&](int s) { return bar0 + 8u * (12 + s); };
+  // P(i) is ready on p[i & 1] and O += P(i) V(i) completes on o[i & 1]: with the softmax
+  // free to run a tile ahead of the MMAs (and to skip its waits for O), alternating
+  // barriers keep every parity wait unambiguous: P(i+2) needs S(i+2), issued only after
+  // the wait for P(i), and S(i+1) implies that P V(i-1) is done
+  auto bar_p = [&](int i) { return bar0 + 8u * (15 + (i & 1)); };
+  auto bar_o = [&](int i) { return bar0 + 8u * (17 + (i & 1)); };
+  const uint32_t bar_done = bar0 + 8u * 19;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
 
@@ -131,11 +139,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(bar_kempty(s), 1);
       tc::mbar_init(bar_vfull(s), 1);
       tc::mbar_init(bar_vempty(s), 1);
-      tc::mbar_init(bar_sfull(s), 1);
-      tc::mbar_init(bar_sempty(s), kSoftThreads);
+      tc::mbar_init(bar_o(s), 1);
+      tc::mbar_init(bar_p(s), kSoftThreads);
     }
-    tc::mbar_init(bar_p, kSoftThreads);
-    tc::mbar_init(bar_o, 1);
+    for (int s = 0; s < NSB; ++s) {
+      tc::mbar_init(bar_sfull(s), 1);
+      tc::mbar_init(bar_sempty(s), 1);  // released by the MMA that read P from it
+    }
     tc::mbar_init(bar_done, 1);
     misc[1] = 0u;
     tc::fence_mbar_init();
@@ -152,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = misc[0];
-  const uint32_t t_o = tmem + 2 * BN;  // O accumulator columns [256, 256 + D)
+  const uint32_t t_o = tmem + NSB * BN;  // O accumulator columns [384, 384 + D)
 
   if (warp == 0) {
     // ============================================================ TMA producer
@@ -205,16 +215,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = tc::mbar_wait(bar_q, 0);
       int issued = 0;  // MMA groups issued (for the final drain)
       for (int j = 0; ok && j <= ntiles; ++j) {
-        if (j < ntiles) {  // S(j) = Q K(j)^T
-          const int s = j & 1;
+        if (j < ntiles) {  // S(j) = Q K(j)^T into S/P buffer j % NSB
+          const int s = j & 1, sb3 = j % NSB;
           const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-          if (!tc::mbar_wait(bar_kfull(s), ph) || !tc::mbar_wait(bar_sempty(s), ph ^ 1u) ||
-              *abort_flag) {
+          if (!tc::mbar_wait(bar_kfull(s), ph) ||
+              !tc::mbar_wait(bar_sempty(sb3), ((uint32_t)(j / NSB) & 1u) ^ 1u) || *abort_flag) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          const uint32_t d_s = tmem + (uint32_t)(s * BN);
+          const uint32_t d_s = tmem + (uint32_t)(sb3 * BN);
           const uint32_t k_s = sK + s * C::TILE;
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
@@ -222,27 +232,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_bf16(d_s, tc::sdesc_sw128(sQ + o), tc::sdesc_sw128(k_s + o), idesc_s,
                          k > 0 ? 1u : 0u);
           }
-          tc::commit(bar_sfull(s));
+          tc::commit(bar_sfull(sb3));
           tc::commit(bar_kempty(s));
           ++issued;
         }
         if (j >= 1) {  // O += P(j-1) V(j-1)
           const int jj = j - 1, s = jj & 1;
-          if (!tc::mbar_wait(bar_p, (uint32_t)jj & 1u) ||
+          if (!tc::mbar_wait(bar_p(jj), (uint32_t)(jj >> 1) & 1u) ||
               !tc::mbar_wait(bar_vfull(s), (uint32_t)(jj >> 1) & 1u) || *abort_flag) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
           const uint32_t v_s = sV + s * C::TILE;
+          const uint32_t p_t = tmem + (uint32_t)((jj % NSB) * BN);  // P(jj): 64 columns, bf16 pairs
 #pragma unroll
-          for (int k = 0; k < BN / 16; ++k) {
-            const uint32_t pa = sP + (uint32_t)(k >> 2) * kBox + (uint32_t)(k & 3) * 32u;
-            tc::mma_bf16(t_o, tc::sdesc_sw128(pa), tc::sdesc_sw128_mn(v_s + 2048u * k, kBox),
-                         idesc_o, (jj > 0 || k > 0) ? 1u : 0u);
-          }
+          for (int k = 0; k < BN / 16; ++k)
+            tc::mma_bf16_ts(t_o, p_t + 8u * k, tc::sdesc_sw128_mn(v_s + 2048u * k, kBox), idesc_o,
+                            (jj > 0 || k > 0) ? 1u : 0u);
           tc::commit(bar_vempty(s));
-          tc::commit(bar_o);
+          tc::commit(bar_o(jj));
+          tc::commit(bar_sempty(jj % NSB));  // the S/P buffer is free for S(jj + NSB)
           ++issued;
         }
       }
@@ -266,8 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_used = -1e30f, lsum = 0.f;
     bool failed = false, wait_failed = false;
     for (int j = 0; j < ntiles; ++j) {
-      const int s = j & 1;
-      bool ok = tc::mbar_wait(bar_sfull(s), (uint32_t)(j >> 1) & 1u) && !*abort_flag;
+      const int s = j & 1, sb3 = j % NSB;  // max-exchange buffer, S/P buffer
+      bool ok = tc::mbar_wait(bar_sfull(sb3), (uint32_t)(j / NSB) & 1u) && !*abort_flag;
       if (tc::bar_or(2, kSoftThreads, !ok || wait_failed)) {
         failed = true;
         break;
@@ -275,10 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_after_sync();
       uint32_t v[KC];
 #pragma unroll
-      for (int c = 0; c < KC; c += 32) tc::tmem_ld32(tmem + lane_off + (uint32_t)(s * BN + h * KC + c), v + c);
+      for (int c = 0; c < KC; c += 32)
+        tc::tmem_ld32(tmem + lane_off + (uint32_t)(sb3 * BN + h * KC + c), v + c);
       tc::tmem_ld_wait();
-      tc::fence_before_sync();
-      tc::mbar_arrive(bar_sempty(s));
 
       const bool ctx = j < n_ctx;
       const int kb = (ctx ? j * BN : a.T + (j - n_ctx) * BN) + h * KC;
@@ -320,13 +329,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       lsum += ps0 + ps1;
 
-      // the P buffer and O are free once O += P(j-1) V(j-1) has completed; O is rescaled
-      // only when this row's max grew past the threshold
-      if (j > 0) {
-        ok = tc::mbar_wait(bar_o, (uint32_t)(j - 1) & 1u) && !*abort_flag;
+      // O is rescaled only when this row's max grew past the threshold, and only then
+      // does the softmax wait for O += P(j-1) V(j-1)
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        ok = tc::mbar_wait(bar_o(j - 1), (uint32_t)((j - 1) >> 1) & 1u) && !*abort_flag;
         if (!ok) wait_failed = true;  // reported at the next vote
         tc::fence_after_sync();
-        if (ok && __any_sync(0xffffffffu, need)) {
+        if (ok) {
           const uint32_t to = t_o + lane_off + (uint32_t)(h * OC);
           if constexpr (OC >= 32) {
 #pragma unroll
@@ -347,22 +356,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_st_wait();
         }
       }
-      // this thread's keys h*KC .. h*KC+KC-1: 16-byte chunks of 8 keys in box (h KC)/64,
-      // 128-byte swizzle
-      uint8_t* prow = smem + C::OFF_P + (h * KC / 64) * kBox + row * 128;
-      tc::fence_proxy_async_smem();  // the tensor core's reads of this buffer came before
-#pragma unroll
-      for (int c4 = 0; c4 < KC / 8; ++c4) {
-        const int c8 = (h * KC % 64) / 8 + c4;
-        uint4 u = make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
-        *reinterpret_cast<uint4*>(prow + ((c8 ^ (row & 7)) << 4)) = u;
-      }
-      tc::fence_proxy_async_smem();
+      // P of this thread's keys h*KC .. h*KC+KC-1 as bf16 pairs into columns h*KC/2 .. of
+      // the S buffer: both threads of the row read their S before the max exchange above
+      static_assert(KC == 64, "one 32-column TMEM store of P per thread");
+      tc::tmem_st32(tmem + lane_off + (uint32_t)(sb3 * BN + h * (KC / 2)), pk);
+      tc::tmem_st_wait();
       tc::fence_before_sync();
-      tc::mbar_arrive(bar_p);
+      tc::mbar_arrive(bar_p(j));
     }
     if (!failed && ntiles > 0) {
-      const bool ok = tc::mbar_wait(bar_o, (uint32_t)(ntiles - 1) & 1u) && !*abort_flag;
+      // the last two P V products (on o[0] and o[1]) complete O
+      bool ok = ntiles < 2 || tc::mbar_wait(bar_o(ntiles - 2), (uint32_t)((ntiles - 2) >> 1) & 1u);
+      ok = ok && tc::mbar_wait(bar_o(ntiles - 1), (uint32_t)((ntiles - 1) >> 1) & 1u) &&
+           !*abort_flag;
       failed = tc::bar_or(2, kSoftThreads, !ok || wait_failed);
       if (!failed) {
         tc::fence_after_sync();
