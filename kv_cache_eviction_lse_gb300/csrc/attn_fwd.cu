@@ -358,8 +358,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // P of this thread's keys h*KC .. h*KC+KC-1 as bf16 pairs into columns h*KC/2 .. of
       // the S buffer: both threads of the row read their S before the max exchange above
-      static_assert(KC == 64, "one 32-column TMEM store of P per thread");
-      tc::tmem_st32(tmem + lane_off + (uint32_t)(sb3 * BN + h * (KC / 2)), pk);
+      if constexpr (KC == 64)
+        tc::tmem_st32(tmem + lane_off + (uint32_t)(sb3 * BN + h * (KC / 2)), pk);
+      else
+        tc::tmem_st16(tmem + lane_off + (uint32_t)(sb3 * BN + h * (KC / 2)), pk);
       tc::tmem_st_wait();
       tc::fence_before_sync();
       tc::mbar_arrive(bar_p(j));
