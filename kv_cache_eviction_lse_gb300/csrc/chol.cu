@@ -1,14 +1,15 @@
 // Ridge solve of the value refit's normal equations, batched over (layer, KV head):
 //   (G + lam I) X = R,   lam = lam_rel * mean(diag G[:k, :k])
 // by a blocked right-looking upper Cholesky factorisation G + lam I = U^T U in fp32
-// and two blocked triangular solves U^T Y = R, U X = Y.  Every step is one launch over
-// all problems, so the trailing updates (the bulk of the work) spread over the whole
-// GPU instead of one CTA per problem:
+// and two blocked triangular solves U^T Y = R, U X = Y.  Every factorisation step is one
+// launch over all problems, so the trailing updates (the bulk of the work) spread over
+// the whole GPU instead of one CTA per problem:
 //   per 64-row panel p:  factor the diagonal block (one CTA per problem), solve the row
 //                        panel U_pp^T X = G[p][p+64:] (CTAs over 64-column blocks), update
 //                        the trailing upper triangle G -= X^T X (CTAs over 64 x 64 tiles)
-//   per 64-row block of the solves: the diagonal block's triangular solve, then the
-//                        update of every remaining block row (64 x 64 x 64 products)
+// The solves then run as one launch: the 64-column blocks of right-hand sides are
+// independent, so one CTA per (problem, column block) takes both sweeps, each a diagonal
+// block's triangular solve followed by the update of every remaining block row.
 // G arrives as its upper block triangle (the Gram kernel writes only those tiles); the
 // lower triangle is never read.  Rows/columns k .. M-1 (padding of the kept-key
 // dimension) are decoupled: their diagonal becomes 1 and their right-hand side 0.
@@ -23,6 +24,7 @@ __device__ int g_chol_error = 0;
 namespace {
 
 constexpr int NB = 64;         // panel / block size (M is a multiple of 64)
+constexpr int kLd = NB + 4;    // row stride of staged 64 x 64 blocks: 16-byte aligned rows
 constexpr int kErrNotSpd = 6;  // a pivot of the factorisation was not positive
 
 __device__ __forceinline__ float* prob(float* base, size_t stride) {
@@ -207,69 +209,79 @@ __global__ void __launch_bounds__(256) syrk_kernel(const CholArgs a, int p) {
   }
 }
 
-// Triangular solve of block row p of the right-hand sides, one thread per column:
-// forward (U_pp^T y = r) or backward (U_pp x = y)
-template <bool BACKWARD>
-__global__ void __launch_bounds__(128) solve_diag_kernel(const CholArgs a, int p) {
+// Both triangular solves (U^T Y = R, then U X = Y) of one problem and one 64-column block
+// of right-hand sides; the column blocks are independent, so each CTA runs the whole
+// chain with no other launch.  Per 64-row block p (forward ascending, backward
+// descending): the diagonal solve in registers (threads 0..63, one column each) into the
+// stage ys, then every remaining block row q is updated, forward R[q] -= U[p][q]^T Y[p],
+// backward R[q] -= U[q][p] X[p] (64 x 64 x 64, a 4 x 4 tile per thread).  Y goes back to
+// R; X rows below k go to the output.
+__global__ void __launch_bounds__(256) solve_kernel(const CholArgs a) {
   const float* G = prob(a.g, (size_t)a.M * a.ldg);
   float* R = prob(a.r, (size_t)a.M * a.d);
-  __shared__ __align__(16) float w[NB][NB];
-  __shared__ float dinv[NB];
-  load_diag_block(G, a.ldg, p, 128, BACKWARD, w, dinv);
-  const int c = blockIdx.x * 128 + threadIdx.x;
-  if (c >= a.d) return;
-  float x[NB];
-#pragma unroll
-  for (int i = 0; i < NB; ++i) x[i] = R[(size_t)(p + (BACKWARD ? NB - 1 - i : i)) * a.d + c];
-  tri_solve_col<BACKWARD>(x, w, dinv, R + (size_t)p * a.d + c, a.d);
-}
-
-// Update of the block rows after (forward) or before (backward) block p:
-//   forward:  R[q] -= U[p][q]^T Y[p]  for q > p      backward: R[q] -= U[q][p] X[p]  for q < p
-// CTA (q block, 64 right-hand-side columns); 256 threads, 4 x 4 each
-__global__ void __launch_bounds__(256) solve_update_kernel(const CholArgs a, int p, int backward) {
-  const float* G = prob(a.g, (size_t)a.M * a.ldg);
-  float* R = prob(a.r, (size_t)a.M * a.d);
-  const int q0 = backward ? blockIdx.x * NB : p + NB + blockIdx.x * NB;
-  const int c0 = blockIdx.z * NB;
-  __shared__ __align__(16) float us[NB][NB + 4];  // [r][q]: coefficient of row r of block p in row q
-  __shared__ __align__(16) float ys[NB][NB + 4];  // [r][c]: solved rows of block p
-  for (int idx = threadIdx.x; idx < NB * NB; idx += 256) {
-    const int i = idx / NB, j = idx % NB;  // consecutive threads read consecutive addresses
-    if (backward)
-      us[j][i] = G[(size_t)(q0 + i) * a.ldg + p + j];
-    else
-      us[i][j] = G[(size_t)(p + i) * a.ldg + q0 + j];
-    ys[i][j] = R[(size_t)(p + i) * a.d + c0 + j];
-  }
-  __syncthreads();
-  const int tq = (threadIdx.x / 16) * 4, tc = (threadIdx.x % 16) * 4;
-  float acc[4][4] = {};
-#pragma unroll 8
-  for (int r = 0; r < NB; ++r) {
-    const float4 a4 = *reinterpret_cast<const float4*>(&us[r][tq]);
-    const float4 b4 = *reinterpret_cast<const float4*>(&ys[r][tc]);
-    const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
-  }
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    float4* rp = reinterpret_cast<float4*>(R + (size_t)(q0 + tq + u) * a.d + c0 + tc);
-    float4 r4 = *rp;
-    r4.x -= acc[u][0]; r4.y -= acc[u][1]; r4.z -= acc[u][2]; r4.w -= acc[u][3];
-    *rp = r4;
-  }
-}
-
-__global__ void __launch_bounds__(256) copy_out_kernel(const CholArgs a) {
-  const float* R = prob(a.r, (size_t)a.M * a.d);
   float* X = prob(a.x, (size_t)a.k * a.d);
-  for (size_t idx = (size_t)blockIdx.x * 256 + threadIdx.x; idx < (size_t)a.k * a.d;
-       idx += (size_t)gridDim.x * 256)
-    X[idx] = R[idx];
+  const int c0 = blockIdx.x * NB, tid = threadIdx.x, nb = a.M / NB;
+  __shared__ __align__(16) float w[NB][NB];   // diagonal block, pre-shifted
+  __shared__ float dinv[NB];
+  __shared__ __align__(16) float ys[NB][kLd];  // solved rows of block p
+  __shared__ __align__(16) float us[NB][kLd];  // coefficients of block p in block row q
+  const int tq = (tid / 16) * 4, tc = (tid % 16) * 4;
+  for (int pass = 0; pass < 2; ++pass) {
+    const bool back = pass == 1;
+    for (int bi = 0; bi < nb; ++bi) {
+      const int p = (back ? nb - 1 - bi : bi) * NB;
+      __syncthreads();  // the previous block's reads of w, ys and us are done
+      load_diag_block(G, a.ldg, p, 256, back, w, dinv);
+      if (tid < NB) {
+        float x[NB];
+#pragma unroll
+        for (int i = 0; i < NB; ++i)
+          x[i] = R[(size_t)(p + (back ? NB - 1 - i : i)) * a.d + c0 + tid];
+        if (back)
+          tri_solve_col<true>(x, w, dinv, &ys[0][tid], kLd);
+        else
+          tri_solve_col<false>(x, w, dinv, &ys[0][tid], kLd);
+      }
+      __syncthreads();
+      for (int idx = tid; idx < NB * NB; idx += 256) {
+        const int r = idx / NB, c = idx % NB;
+        if (!back)
+          R[(size_t)(p + r) * a.d + c0 + c] = ys[r][c];
+        else if (p + r < a.k)
+          X[(size_t)(p + r) * a.d + c0 + c] = ys[r][c];
+      }
+      const int q_begin = back ? 0 : p + NB, q_end = back ? p : a.M;
+      for (int q = q_begin; q < q_end; q += NB) {
+        for (int idx = tid; idx < NB * NB; idx += 256) {
+          const int i = idx / NB, j = idx % NB;  // consecutive threads read consecutive addresses
+          if (back)
+            us[j][i] = G[(size_t)(q + i) * a.ldg + p + j];  // U[q+i][p+j]
+          else
+            us[i][j] = G[(size_t)(p + i) * a.ldg + q + j];  // U[p+i][q+j]
+        }
+        __syncthreads();
+        float acc[4][4] = {};
+#pragma unroll 8
+        for (int r = 0; r < NB; ++r) {
+          const float4 a4 = *reinterpret_cast<const float4*>(&us[r][tq]);
+          const float4 b4 = *reinterpret_cast<const float4*>(&ys[r][tc]);
+          const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float4* rp = reinterpret_cast<float4*>(R + (size_t)(q + tq + u) * a.d + c0 + tc);
+          float4 r4 = *rp;
+          r4.x -= acc[u][0]; r4.y -= acc[u][1]; r4.z -= acc[u][2]; r4.w -= acc[u][3];
+          *rp = r4;
+        }
+        __syncthreads();  // us is reloaded for the next block row
+      }
+    }
+  }
 }
 
 }  // namespace
@@ -293,25 +305,7 @@ cudaError_t launch_chol_solve(const CholArgs& a, cudaStream_t s) {
       launches += 2;
     }
   }
-  for (int b = 0; b < nb; ++b) {  // U^T Y = R
-    const int p = b * NB, rest = nb - b - 1;
-    solve_diag_kernel<false><<<dim3((a.d + 127) / 128, B), 128, 0, s>>>(a, p);
-    ++launches;
-    if (rest > 0) {
-      solve_update_kernel<<<dim3(rest, B, dcb), 256, 0, s>>>(a, p, 0);
-      ++launches;
-    }
-  }
-  for (int b = nb - 1; b >= 0; --b) {  // U X = Y
-    const int p = b * NB;
-    solve_diag_kernel<true><<<dim3((a.d + 127) / 128, B), 128, 0, s>>>(a, p);
-    ++launches;
-    if (b > 0) {
-      solve_update_kernel<<<dim3(b, B, dcb), 256, 0, s>>>(a, p, 1);
-      ++launches;
-    }
-  }
-  copy_out_kernel<<<dim3(64, B), 256, 0, s>>>(a);
+  solve_kernel<<<dim3(dcb, B), 256, 0, s>>>(a);  // U^T Y = R, U X = Y, X = rows < k
   ++launches;
   count_launches(launches);
   return cudaGetLastError();
