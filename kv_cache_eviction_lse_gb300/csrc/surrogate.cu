@@ -11,6 +11,8 @@
 // the MMA directly as A fragments: the reduction runs over channels,
 // so any channel permutation works as long as the B fragments (W, staged once per
 // block in shared memory) use the same one.  No shared-memory staging of h.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "surrogate.cuh"
 
@@ -190,6 +192,139 @@ __global__ void __launch_bounds__(kWarps * 32) surrogate_kernel(const SurArgs a)
   }
 }
 
+// W fragments of superblock sb for up to 8 heads (the B-operand layout of
+// surrogate_kernel: entry (p, lane) = W[sb*128 + 32p + 8t + e][g] for e = 0..7, lane =
+// 4g + t), written by one warp into dst[4 * 32].
+__device__ __forceinline__ void stage_w_superblock(const bf16_t* Wl, int Hkv, int sb, uint4* dst,
+                                                   int lane) {
+  if (Hkv == 8) {
+    // a channel's weights are one 16-byte row: lanes 0..15 each read the 8 rows of one
+    // group of 8 channels and write their 8 x 8 transpose
+    if (lane < 16) {
+      const int p = lane >> 2, t = lane & 3;
+      const uint4* src = reinterpret_cast<const uint4*>(Wl + (size_t)(sb * 128 + 32 * p + 8 * t) * 8);
+      uint32_t r[8][4];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint4 u = __ldg(src + e);
+        r[e][0] = u.x; r[e][1] = u.y; r[e][2] = u.z; r[e][3] = u.w;
+      }
+#pragma unroll
+      for (int gg = 0; gg < 8; ++gg) {
+        const int sh = (gg & 1) * 16;
+        uint32_t wv[4];
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2)
+          wv[e2] = ((r[2 * e2][gg >> 1] >> sh) & 0xffffu) | (((r[2 * e2 + 1][gg >> 1] >> sh) & 0xffffu) << 16);
+        dst[p * 32 + 4 * gg + t] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      }
+    }
+  } else {
+    for (int idx = lane; idx < 4 * 32; idx += 32) {
+      const int ln = idx & 31, p = idx >> 5, head = ln >> 2;
+      const int ch0 = sb * 128 + 32 * p + 8 * (ln & 3);
+      uint32_t wv[4];
+#pragma unroll
+      for (int e2 = 0; e2 < 4; ++e2) {
+        uint32_t lo = 0, hi = 0;
+        if (head < Hkv) {
+          lo = Wl[(size_t)(ch0 + 2 * e2) * Hkv + head];
+          hi = Wl[(size_t)(ch0 + 2 * e2 + 1) * Hkv + head];
+        }
+        wv[e2] = lo | (hi << 16);
+      }
+      dst[idx] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    }
+  }
+  __syncwarp();
+}
+
+// Few tokens (decode: one per sequence), up to 8 heads: a cluster of kSplit blocks per
+// (layer, 16-token tile) splits the channels.  Block rank r takes superblocks
+// [r nsb / kSplit, (r+1) nsb / kSplit), its warps one superblock at a time (each stages
+// only that superblock's W, 2 KB); the warps' partial sums meet in shared memory and the
+// blocks' partials in the rank-0 block's shared memory (distributed shared memory),
+// which adds them in rank order (deterministic) and applies bias, threshold and window.
+constexpr int kSplit = 4;
+__global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kWarps * 32)
+    surrogate_split_kernel(const SurArgs a) {
+  namespace cg = cooperative_groups;
+  __shared__ uint4 wst[kWarps][4 * 32];          // per warp: one superblock's W fragments
+  __shared__ float red[kWarps][4][32];            // per warp partial sums
+  __shared__ float cred[kSplit][4][32];           // rank 0: the blocks' partial sums
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int l = blockIdx.y, t0 = (blockIdx.x / kSplit) * 16;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  const int nsb = a.Dh / 128;
+  const bf16_t* Wl = a.W + (size_t)l * a.Dh * a.Hkv;
+  const int ra = min(t0 + g, a.T - 1), rb = min(t0 + g + 8, a.T - 1);
+  const bf16_t* pa = a.h + ((size_t)l * a.T + ra) * a.Dh + 8 * t4;
+  const bf16_t* pb = a.h + ((size_t)l * a.T + rb) * a.Dh + 8 * t4;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int sb = rank * nsb / kSplit + warp; sb < (rank + 1) * nsb / kSplit; sb += kWarps) {
+    uint4 xa[4], xb[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {  // issue the token loads before staging W
+      xa[p] = ld_nc_v4(pa + sb * 128 + 32 * p);
+      xb[p] = ld_nc_v4(pb + sb * 128 + 32 * p);
+    }
+    stage_w_superblock(Wl, a.Hkv, sb, wst[warp], lane);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const uint4 wv = wst[warp][p * 32 + lane];
+      const uint32_t A0[4] = {xa[p].x, xb[p].x, xa[p].y, xb[p].y};
+      mma_bf16_16816(acc, A0, wv.x, wv.y);
+      const uint32_t A1[4] = {xa[p].z, xb[p].z, xa[p].w, xb[p].w};
+      mma_bf16_16816(acc, A1, wv.z, wv.w);
+    }
+    __syncwarp();  // wst[warp] is restaged for the next superblock
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) red[warp][e][lane] = acc[e];
+  __syncthreads();
+  if (warp == 0) {
+    float* dst = cluster.map_shared_rank(&cred[0][0][0], 0);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float sum = 0.f;
+      for (int w8 = 0; w8 < kWarps; ++w8) sum += red[w8][e][lane];
+      dst[(rank * 4 + e) * 32 + lane] = sum;
+    }
+  }
+  cluster.sync();  // every block reaches it once: the partials are in rank 0
+  if (rank != 0 || warp != 0) return;
+  const float* bl = a.b + (size_t)l * a.Hkv;
+  int cnt[2] = {0, 0};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float zz = 0.f;
+    for (int r = 0; r < kSplit; ++r) zz += cred[r][e][lane];
+    const int head = 2 * t4 + (e & 1), tok = t0 + g + (e >> 1) * 8;
+    if (head < a.Hkv && tok < a.T) {
+      zz += bl[head];
+      const size_t o = ((size_t)l * a.Hkv + head) * a.T + tok;
+      a.z[o] = zz;
+      if (a.mask) {
+        const int kp = (zz >= a.tau) || (tok >= a.T - a.w);
+        a.mask[o] = (uint8_t)kp;
+        cnt[e & 1] += kp;
+      }
+    }
+  }
+  if (a.mask) {
+#pragma unroll
+    for (int e2 = 0; e2 < 2; ++e2) {
+      int c = cnt[e2];
+      c += __shfl_xor_sync(0xffffffffu, c, 4);
+      c += __shfl_xor_sync(0xffffffffu, c, 8);
+      c += __shfl_xor_sync(0xffffffffu, c, 16);
+      const int head = 2 * t4 + e2;
+      if (g == 0 && head < a.Hkv && c) atomicAdd(a.keep + (size_t)l * a.Hkv + head, c);
+    }
+  }
+}
+
 }  // namespace
 
 size_t surrogate_smem_bytes(int Dh, int Hkv) { return (size_t)Dh * ((Hkv + 7) / 8) * 16; }
@@ -205,8 +340,16 @@ cudaError_t launch_surrogate(const bf16_t* h, int L, int T, int Dh, int Hkv, con
   SurArgs a{h, W, b, z, mask, keep, T, Dh, Hkv, w, 8, tau, 1};
   const int ntile = (T + 15) / 16;
   // few token tiles (decode: one token per sequence): split each tile's channels over
-  // the warps of a block instead of leaving most of the GPU idle
-  if ((long)L * ntile < 304) a.ksplit = kWarps;
+  // the blocks of a cluster (up to 8 heads) or the warps of a block, instead of leaving
+  // most of the GPU idle
+  if ((long)L * ntile < 304) {
+    if (Hkv <= 8 && Dh % (128 * kSplit) == 0) {
+      count_launches(1);
+      surrogate_split_kernel<<<dim3(ntile * kSplit, L), kWarps * 32, 0, s>>>(a);
+      return cudaGetLastError();
+    }
+    a.ksplit = kWarps;
+  }
   // fewer tiles per warp when the grid would not fill the GPU twice over
   while (a.tiles_per_warp > 1 &&
          (long)L * ((ntile + kWarps * a.tiles_per_warp - 1) / (kWarps * a.tiles_per_warp)) < 304)
