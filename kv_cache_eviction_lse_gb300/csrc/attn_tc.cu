@@ -645,6 +645,7 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
                 const bool ctx = it < U.n_ctx;
                 const int kb = (ctx ? it * BN : a.T + (it - U.n_ctx) * BN) + h * COLS + c0;
                 const int lim = ctx ? a.T : n_k;
+                if (kb >= lim || kb > off + ra) continue;  // no visible key in these 64
                 if (kb + 64 > lim || kb + 63 > off + ra) {
 #pragma unroll
                   for (int c = 0; c < 64; ++c)
