@@ -657,6 +657,7 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
               } else {
                 const int j0 = (U.qt_begin + it % U.per_head) * BN + h * COLS + c0;
                 const bool band = j0 < U.row0 + BM - 1 + a.w;
+                if (band && ra + a.w - j0 >= 64) continue;  // all 64 queries in the window
                 f += future_cols(w, sc2, band, ra + a.w - j0);
               }
             }
