@@ -194,18 +194,14 @@ kvs_status kvs_score_max(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
   a.n_q = n_q; a.T = T; a.accumulate = accumulate != 0;
   if (n_q > 0) {
     uint8_t* w = static_cast<uint8_t*>(ws);
-    float* hlog = nullptr;
-    size_t off = 0;
-    if (h) {
-      hlog = reinterpret_cast<float*>(w);
-      cudaError_t e = kvs::launch_hidden_log_norm(h, dims->L, n_q, dims->D_h, hlog, s);
-      if (e != cudaSuccess) return cuda_status(e, "kvs_score_max (hidden norm)");
-      off = kvs::score_max_ccol_offset(dims->L, n_q);
-    }
+    const size_t off = h ? kvs::score_max_ccol_offset(dims->L, n_q) : 0;
     auto* ccol = reinterpret_cast<kvs::bf16_t*>(w + off);
     auto* ones = reinterpret_cast<kvs::bf16_t*>(w + need - 128 * 32);
-    cudaError_t e = kvs::launch_score_constants(lse, hlog, dims->L, dims->H_q, n_q, dims->d, ccol,
-                                                ones, s);
+    // the per-query constants lse_j (+ ln ||h_j||) of the folded MMA step
+    cudaError_t e = h ? kvs::launch_hidden_constants(h, dims->D_h, lse, dims->L, dims->H_q, n_q,
+                                                     dims->d, ccol, ones, s)
+                      : kvs::launch_score_constants(lse, nullptr, dims->L, dims->H_q, n_q,
+                                                    dims->d, ccol, ones, s);
     if (e != cudaSuccess) return cuda_status(e, "kvs_score_max (constants)");
     a.ccol = ccol;
     a.ones = ones;

@@ -70,8 +70,9 @@ cudaError_t fwd_device_error(int* code, bool clear, cudaStream_t s);
 // Reads (and with `clear` resets) the device error word of the scoring kernels.
 cudaError_t attn_device_error(int* code, bool clear, cudaStream_t s);
 
-// hlog[l][j] = ln ||h[l][j]||_2 over D_h bf16 channels.
-cudaError_t launch_hidden_log_norm(const bf16_t* h, int L, int n, int Dh, float* hlog,
-                                   cudaStream_t s);
+// The same constants with the hidden-state factor ln ||h[l][j]||_2 (over D_h bf16
+// channels) reduced from h in the same pass.
+cudaError_t launch_hidden_constants(const bf16_t* h, int Dh, const float* lse, int L, int Hq,
+                                    int n_q, int d, bf16_t* ccol, bf16_t* ones, cudaStream_t s);
 
 }  // namespace kvs

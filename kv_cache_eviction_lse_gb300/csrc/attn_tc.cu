@@ -845,24 +845,50 @@ cudaError_t launch_mode(const AttnArgs& a, cudaStream_t s) {
   return a.d == 128 ? launch_d<128, MODE>(a, s) : launch_d<64, MODE>(a, s);
 }
 
-__global__ void hidden_log_norm_kernel(const bf16_t* __restrict__ h, int rows, int Dh,
-                                       float* __restrict__ out) {
-  const int wg = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (wg >= rows) return;
-  const bf16_t* p = h + (size_t)wg * Dh;
-  float s = 0.f;
-  for (int c = lane * 8; c < Dh; c += 256) {
-    const uint4 u = ld_nc_v4(p + c);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float lo = bf16_lo(w[k]), hi = bf16_hi(w[k]);
-      s = fmaf(lo, lo, s);
-      s = fmaf(hi, hi, s);
-    }
+// The per-query constants of the maximum with the hidden-state factor, from h directly:
+// one warp per (layer, query row j) reduces ln ||h_j|| and writes the constants of all
+// H_q query heads for that row, so ||h_j|| never makes a round trip through memory.
+__global__ void __launch_bounds__(256) hidden_constants_kernel(
+    const bf16_t* __restrict__ h, int Dh, const float* __restrict__ lse, int L, int Hq, int n_q,
+    int nq_pad, float inv_scale, bf16_t* ccol, bf16_t* ones) {
+  if (blockIdx.x == 0 && threadIdx.x < BM) {
+    const uint32_t one = 0x3F80u;  // bf16 1.0
+    uint4* o = reinterpret_cast<uint4*>(ones + threadIdx.x * 16);
+    o[0] = make_uint4(one | (one << 16), one, 0u, 0u);
+    o[1] = make_uint4(0u, 0u, 0u, 0u);
   }
-  s = warp_sum(s);
-  if (lane == 0) out[wg] = 0.5f * logf(s);
+  const int wg = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (wg >= L * nq_pad) return;
+  const int l = wg / nq_pad, j = wg % nq_pad;
+  float hl = 0.f;
+  if (j < n_q) {
+    const bf16_t* p = h + ((size_t)l * n_q + j) * Dh;
+    float s = 0.f;
+    for (int c = lane * 8; c < Dh; c += 256) {
+      const uint4 u = ld_nc_v4(p + c);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float lo = bf16_lo(w[k]), hi = bf16_hi(w[k]);
+        s = fmaf(lo, lo, s);
+        s = fmaf(hi, hi, s);
+      }
+    }
+    hl = 0.5f * logf(warp_sum(s));
+  }
+  for (int hq = lane; hq < Hq; hq += 32) {
+    const size_t lh = (size_t)l * Hq + hq;
+    const float v = j < n_q ? -(lse[lh * n_q + j] + hl) * inv_scale : -1e30f;
+    const __nv_bfloat16 bh = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(bh);
+    const __nv_bfloat16 bm = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 bl = __float2bfloat16_rn(r1 - __bfloat162float(bm));
+    const uint32_t w0 = (uint32_t)__bfloat16_as_ushort(bh) | ((uint32_t)__bfloat16_as_ushort(bm) << 16);
+    const uint32_t w1 = (uint32_t)__bfloat16_as_ushort(bl);
+    uint4* o = reinterpret_cast<uint4*>(ccol + (lh * nq_pad + j) * 16);
+    o[0] = make_uint4(w0, w1, 0u, 0u);
+    o[1] = make_uint4(0u, 0u, 0u, 0u);
+  }
 }
 
 }  // namespace
@@ -935,6 +961,16 @@ cudaError_t launch_score_constants(const float* lse, const float* hlog, int L, i
   return cudaGetLastError();
 }
 
+cudaError_t launch_hidden_constants(const bf16_t* h, int Dh, const float* lse, int L, int Hq,
+                                    int n_q, int d, bf16_t* ccol, bf16_t* ones, cudaStream_t s) {
+  const int nq_pad = (n_q + BN - 1) / BN * BN;
+  const size_t warps = (size_t)L * nq_pad;
+  count_launches(1);
+  hidden_constants_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(h, Dh, lse, L, Hq, n_q, nq_pad,
+                                                                      sqrtf((float)d), ccol, ones);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_lse(const AttnArgs& a, cudaStream_t s) { return launch_mode<kLse>(a, s); }
 cudaError_t launch_softmax_rows(const AttnArgs& a, cudaStream_t s) {
   return launch_mode<kRows>(a, s);
@@ -946,15 +982,6 @@ cudaError_t launch_future_sum(const AttnArgs& a, cudaStream_t s) {
 cudaError_t launch_vnorm_quad(const AttnArgs& a, cudaStream_t s) {
   if (a.Hq / a.Hkv > kMaxGroup) return cudaErrorInvalidValue;
   return launch_mode<kQuad>(a, s);
-}
-
-cudaError_t launch_hidden_log_norm(const bf16_t* h, int L, int n, int Dh, float* hlog,
-                                   cudaStream_t s) {
-  const int rows = L * n;
-  if (rows == 0) return cudaSuccess;
-  count_launches(1);
-  hidden_log_norm_kernel<<<(rows + 7) / 8, 256, 0, s>>>(h, rows, Dh, hlog);
-  return cudaGetLastError();
 }
 
 cudaError_t attn_device_error(int* code, bool clear, cudaStream_t s) {
