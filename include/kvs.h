@@ -148,9 +148,10 @@ kvs_status kvs_attn_fwd(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
  *   log_score [L][H_kv][T]      fp32   output; with accumulate != 0 the result is
  *                                      max(previous contents, new score) (chunked
  *                                      reconstruction [KVzip technical details])
- *   ws        scratch of kvs_score_max_workspace_size(dims, n_q, h != NULL) bytes: ln||h_j||
- *             and the per-query constants -(lse_j + ln||h_j||) sqrt(d) as three bf16
- *             parts, which one extra K = 16 MMA step adds to every accumulator column
+ *   ws        scratch of kvs_score_max_workspace_size(dims, n_q, h != NULL) bytes: the
+ *             per-query constants -(lse_j + ln||h_j||) sqrt(d) as three bf16 parts,
+ *             which one extra K = 16 MMA step adds to every accumulator column (the
+ *             size does not depend on h)
  * ------------------------------------------------------------------------------- */
 size_t kvs_score_max_workspace_size(const kvs_dims* dims, int32_t n_q, int32_t with_h);
 kvs_status kvs_score_max(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,

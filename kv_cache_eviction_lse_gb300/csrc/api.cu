@@ -129,7 +129,8 @@ kvs_status kvs_lse(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q, const k
 
 size_t kvs_score_max_workspace_size(const kvs_dims* dims, int32_t n_q, int32_t with_h) {
   if (!dims || n_q <= 0 || dims->L <= 0 || dims->H_q <= 0) return 0;
-  return kvs::score_max_ws_bytes(dims->L, dims->H_q, n_q, with_h != 0);
+  (void)with_h;  // ln ||h_j|| is folded into the constants in the same pass: same size
+  return kvs::score_max_ws_bytes(dims->L, dims->H_q, n_q);
 }
 
 kvs_status kvs_attn_fwd(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
@@ -194,14 +195,13 @@ kvs_status kvs_score_max(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
   a.n_q = n_q; a.T = T; a.accumulate = accumulate != 0;
   if (n_q > 0) {
     uint8_t* w = static_cast<uint8_t*>(ws);
-    const size_t off = h ? kvs::score_max_ccol_offset(dims->L, n_q) : 0;
-    auto* ccol = reinterpret_cast<kvs::bf16_t*>(w + off);
+    auto* ccol = reinterpret_cast<kvs::bf16_t*>(w);
     auto* ones = reinterpret_cast<kvs::bf16_t*>(w + need - 128 * 32);
     // the per-query constants lse_j (+ ln ||h_j||) of the folded MMA step
     cudaError_t e = h ? kvs::launch_hidden_constants(h, dims->D_h, lse, dims->L, dims->H_q, n_q,
                                                      dims->d, ccol, ones, s)
-                      : kvs::launch_score_constants(lse, nullptr, dims->L, dims->H_q, n_q,
-                                                    dims->d, ccol, ones, s);
+                      : kvs::launch_score_constants(lse, dims->L, dims->H_q, n_q, dims->d, ccol,
+                                                    ones, s);
     if (e != cudaSuccess) return cuda_status(e, "kvs_score_max (constants)");
     a.ccol = ccol;
     a.ones = ones;
@@ -211,7 +211,7 @@ kvs_status kvs_score_max(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
 
 size_t kvs_score_future_sum_workspace_size(const kvs_dims* dims, int32_t T) {
   if (!dims || T <= 0 || dims->L <= 0 || dims->H_q <= 0) return 0;
-  return kvs::score_max_ws_bytes(dims->L, dims->H_q, T, false);
+  return kvs::score_max_ws_bytes(dims->L, dims->H_q, T);
 }
 
 kvs_status kvs_score_future_sum(const kvs_dims* dims, const kvs_bf16* q, const kvs_bf16* k,
@@ -232,8 +232,7 @@ kvs_status kvs_score_future_sum(const kvs_dims* dims, const kvs_bf16* q, const k
   cudaStream_t s = as_stream(stream);
   auto* ccol = static_cast<kvs::bf16_t*>(ws);
   auto* ones = reinterpret_cast<kvs::bf16_t*>(static_cast<uint8_t*>(ws) + need - 128 * 32);
-  cudaError_t e = kvs::launch_score_constants(lse, nullptr, dims->L, dims->H_q, T, dims->d, ccol,
-                                              ones, s);
+  cudaError_t e = kvs::launch_score_constants(lse, dims->L, dims->H_q, T, dims->d, ccol, ones, s);
   if (e != cudaSuccess) return cuda_status(e, "kvs_score_future_sum (constants)");
   kvs::AttnArgs a;
   a.q = q; a.k_ctx = k; a.lse = lse; a.out = score;

@@ -32,12 +32,10 @@ struct AttnArgs {
   const bf16_t* ones = nullptr;
 };
 
-// Score-max workspace layout (kvs_score_max): ln||h|| [L][n_q] fp32 (with h), then the
-// constants and the ones tile above.
-size_t score_max_ccol_offset(int L, int n_q);
-size_t score_max_ws_bytes(int L, int Hq, int n_q, bool with_h);
-// Writes the constants and the ones tile (lse, hlog optional) into the workspace.
-cudaError_t launch_score_constants(const float* lse, const float* hlog, int L, int Hq, int n_q,
+// Score-max / future-mass workspace: the constants, then the ones tile above.
+size_t score_max_ws_bytes(int L, int Hq, int n_q);
+// Writes the constants -lse_j sqrt(d) and the ones tile into the workspace.
+cudaError_t launch_score_constants(const float* lse, int L, int Hq, int n_q,
                                    int d, bf16_t* ccol, bf16_t* ones, cudaStream_t s);
 
 cudaError_t launch_lse(const AttnArgs& a, cudaStream_t s);

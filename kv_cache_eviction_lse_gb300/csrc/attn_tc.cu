@@ -908,7 +908,6 @@ namespace {
 // three bf16 (hi, mid, lo: ~24 bits), then zeros; rows past n_q hold -1e30 (they are
 // padding queries and must never win the max).  Block 0 also writes the ones tile.
 __global__ void __launch_bounds__(256) score_constants_kernel(const float* __restrict__ lse,
-                                                              const float* __restrict__ hlog,
                                                               int L, int Hq, int n_q, int nq_pad,
                                                               float inv_scale, bf16_t* ccol,
                                                               bf16_t* ones) {
@@ -923,11 +922,7 @@ __global__ void __launch_bounds__(256) score_constants_kernel(const float* __res
   const int j = (int)(row % nq_pad);
   const size_t lh = row / nq_pad;  // l * Hq + hq
   float v = -1e30f;
-  if (j < n_q) {
-    const int l = (int)(lh / Hq);
-    const float c = lse[lh * n_q + j] + (hlog ? hlog[(size_t)l * n_q + j] : 0.f);
-    v = -c * inv_scale;
-  }
+  if (j < n_q) v = -lse[lh * n_q + j] * inv_scale;
   const __nv_bfloat16 hi = __float2bfloat16_rn(v);
   const float r1 = v - __bfloat162float(hi);
   const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
@@ -943,21 +938,18 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 
-size_t score_max_ccol_offset(int L, int n_q) { return align256((size_t)L * n_q * sizeof(float)); }
-
-size_t score_max_ws_bytes(int L, int Hq, int n_q, bool with_h) {
+size_t score_max_ws_bytes(int L, int Hq, int n_q) {
   const size_t nq_pad = (size_t)(n_q + BN - 1) / BN * BN;
-  return (with_h ? score_max_ccol_offset(L, n_q) : 0) + align256((size_t)L * Hq * nq_pad * 32) +
-         (size_t)BM * 32;
+  return align256((size_t)L * Hq * nq_pad * 32) + (size_t)BM * 32;
 }
 
-cudaError_t launch_score_constants(const float* lse, const float* hlog, int L, int Hq, int n_q,
+cudaError_t launch_score_constants(const float* lse, int L, int Hq, int n_q,
                                    int d, bf16_t* ccol, bf16_t* ones, cudaStream_t s) {
   const int nq_pad = (n_q + BN - 1) / BN * BN;
   const size_t rows = (size_t)L * Hq * nq_pad;
   count_launches(1);
   score_constants_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(
-      lse, hlog, L, Hq, n_q, nq_pad, sqrtf((float)d), ccol, ones);
+      lse, L, Hq, n_q, nq_pad, sqrtf((float)d), ccol, ones);
   return cudaGetLastError();
 }
 

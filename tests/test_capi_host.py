@@ -105,7 +105,7 @@ def test_workspace_sizes(capi):
     assert C.kvs_vnorm_workspace_size(dm) == 36 * 32 * 128 * 128 * 4
     # ln||h|| [L][n_q] (256-byte aligned), constants [L][H_q][n_q rounded to 256][16] bf16,
     # a 128 x 16 bf16 ones tile
-    assert C.kvs_score_max_workspace_size(dm, 2048, 1) == 36 * 2048 * 4 + 36 * 32 * 2048 * 32 + 4096
+    assert C.kvs_score_max_workspace_size(dm, 2048, 1) == 36 * 32 * 2048 * 32 + 4096
     assert C.kvs_score_max_workspace_size(dm, 2048, 0) == 36 * 32 * 2048 * 32 + 4096
     assert C.kvs_score_max_workspace_size(dm, 100, 0) == 36 * 32 * 256 * 32 + 4096
     assert C.kvs_compact_workspace_size(dm, 32768) >= 36 * 8 * (8 + 1) * 4
