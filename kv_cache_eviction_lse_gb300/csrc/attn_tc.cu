@@ -58,10 +58,9 @@ enum Mode { kLse = 0, kMax = 1, kFuture = 2, kQuad = 3, kRows = 4 };
 // modes whose operand A is a tile of queries (B: key tiles)
 template <int MODE>
 __host__ __device__ constexpr bool a_is_queries() { return MODE == kLse || MODE == kRows; }
-// Two A buffers per CTA, alternating between consecutive units, so the next unit's MMAs
-// start while the epilogue drains the current one (and, on a blocked grid, a CTA's two
-// units each have their own).
-constexpr int kUnits = 2;
+// Two A buffers per CTA, alternating between consecutive units, so the next unit's A tile
+// loads and its MMAs start while the epilogue drains the current one.
+constexpr int kABufs = 2;
 constexpr int kMaxGroup = 16;  // query heads per KV head handled by kQuad
 
 template <int D, int MODE>
@@ -83,9 +82,9 @@ struct Cfg {
   static constexpr int PARTS = MODE == kMax ? KH : 1;
   static constexpr int NS = STAGES * PARTS;
   static constexpr uint32_t SLOT_BYTES = KH / PARTS * kBoxBytesB;
-  static constexpr uint32_t A_BYTES = KH * kBoxBytesA;  // one of kUnits A buffers
+  static constexpr uint32_t A_BYTES = KH * kBoxBytesA;  // one of kABufs A buffers
   static constexpr uint32_t B_BYTES = KH * kBoxBytesB;
-  static constexpr uint32_t OFF_B = kUnits * A_BYTES;
+  static constexpr uint32_t OFF_B = kABufs * A_BYTES;
   // kMax: the K = 16 operands of the constant-adding MMA step: a ones tile for A and,
   // per stage, the B tile's per-query constants (32-byte rows, 32-byte swizzle)
   static constexpr bool AUG = MODE == kMax || MODE == kFuture;
@@ -99,8 +98,8 @@ struct Cfg {
   static constexpr uint32_t OFF_P =
       OFF_X + (MODE == kRows ? (EPI / 32) * ROWS_STAGE : 2 * (NG - 1) * BM * 2 * 4);  // kQuad [2][16][BM]
   static constexpr uint32_t OFF_BAR = OFF_P + (MODE == kQuad ? 2 * kMaxGroup * BM * 4 : 0);
-  // a_full[kUnits], full[NS], empty[NS], tfull[2], tempty[2], a_empty[kUnits]
-  static constexpr uint32_t NBAR = 2 * kUnits + 2 * NS + 4;
+  // a_full[kABufs], full[NS], empty[NS], tfull[2], tempty[2], a_empty[kABufs]
+  static constexpr uint32_t NBAR = 2 * kABufs + 2 * NS + 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t USED = OFF_MISC + 16;
   static constexpr uint32_t SMEM = (USED + 1024 <= kMaxSmem) ? USED + 1024 : kMaxSmem;
@@ -285,8 +284,7 @@ template <int D, int MODE>
 __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __grid_constant__ CUtensorMap tm_b2, const __grid_constant__ CUtensorMap tm_auga,
-                   const __grid_constant__ CUtensorMap tm_augb, const AttnArgs a,
-                   const int strided) {
+                   const __grid_constant__ CUtensorMap tm_augb, const AttnArgs a) {
   using C = Cfg<D, MODE>;
   constexpr int S = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -304,11 +302,11 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
   const uint32_t bar0 = sb + C::OFF_BAR;
   auto bar_afull = [&](int b) { return bar0 + 8u * b; };
   constexpr int NS = C::NS;  // box slots of the B ring
-  auto bar_full = [&](int j) { return bar0 + 8u * (kUnits + j); };
-  auto bar_empty = [&](int j) { return bar0 + 8u * (kUnits + NS + j); };
-  auto bar_tfull = [&](int x) { return bar0 + 8u * (kUnits + 2 * NS + x); };
-  auto bar_tempty = [&](int x) { return bar0 + 8u * (kUnits + 2 * NS + 2 + x); };
-  auto bar_aempty = [&](int b) { return bar0 + 8u * (kUnits + 2 * NS + 4 + b); };
+  auto bar_full = [&](int j) { return bar0 + 8u * (kABufs + j); };
+  auto bar_empty = [&](int j) { return bar0 + 8u * (kABufs + NS + j); };
+  auto bar_tfull = [&](int x) { return bar0 + 8u * (kABufs + 2 * NS + x); };
+  auto bar_tempty = [&](int x) { return bar0 + 8u * (kABufs + 2 * NS + 2 + x); };
+  auto bar_aempty = [&](int b) { return bar0 + 8u * (kABufs + 2 * NS + 4 + b); };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
 
@@ -322,41 +320,31 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
   const int a_rows = kQ ? a.n_q : a.T;
   const int nrb = (a_rows + BM - 1) / BM;  // 128-row units per (layer, head)
   const int NH = kQ ? a.Hq : a.Hkv;
-  // The CTA's units.  Strided (a persistent grid of one CTA per SM): units blockIdx.x,
-  // blockIdx.x + gridDim.x, ... of all (layer, head, row block), row block fastest, the
-  // two A buffers alternating, the setup paid once per SM.  Blocked (grid = row-block
-  // pairs x heads x layers): two consecutive row blocks of one (layer, head), balanced by
-  // the hardware's block scheduler.
-  const int nunits = strided ? (nrb * NH * a.L - (int)blockIdx.x + (int)gridDim.x - 1) /
-                                      (int)gridDim.x
-                                : min(kUnits, nrb - (int)blockIdx.x * kUnits);
+  // The CTA's units (a persistent grid of one CTA per SM): units blockIdx.x,
+  // blockIdx.x + gridDim.x, ... of all (layer, head, row block), row block fastest, the two
+  // A buffers alternating, the setup paid once per SM.
+  const int nunits = (nrb * NH * a.L - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
   // A CTA's units visit one residue class of row blocks modulo dg = gcd(grid, row blocks);
   // the cost of a causal unit grows (or falls) with its row block, so odd groups of dg
   // row blocks are taken in reverse order, giving every residue class the same mean cost.
-  int dg = strided ? (int)gridDim.x : 1;
+  int dg = (int)gridDim.x;
   for (int x = nrb; x > 0;) {
     const int t = dg % x;
     dg = x;
     x = t;
   }
   auto unit_of = [&](int n, int& l, int& hy) -> int {  // returns the unit's first row
-    int rb;
-    if (strided) {
-      const int u = (int)blockIdx.x + n * (int)gridDim.x;
-      const int r = u % nrb, k = r / dg, sr = r - k * dg;
-      rb = k * dg + ((k & 1) ? dg - 1 - sr : sr);
-      hy = (u / nrb) % NH;
-      l = u / (nrb * NH);
-    } else {
-      rb = (int)blockIdx.x * kUnits + n;
-      hy = blockIdx.y;
-      l = blockIdx.z;
-    }
+    const int u = (int)blockIdx.x + n * (int)gridDim.x;
+    const int r = u % nrb, k = r / dg, sr = r - k * dg;
+    const int rb = k * dg + ((k & 1) ? dg - 1 - sr : sr);
+    hy = (u / nrb) % NH;
+    l = u / (nrb * NH);
     return rb * BM;
   };
 
+
   if (threadIdx.x == 0) {
-    for (int n = 0; n < kUnits; ++n) {
+    for (int n = 0; n < kABufs; ++n) {
       tc::mbar_init(bar_afull(n), 1);
       // the quadratic form's epilogue reads its value rows from A, so its threads also
       // release the buffer
@@ -814,27 +802,18 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
   }
   const int rows = a_is_queries<MODE>() ? a.n_q : a.T;
   const int nrb = (rows + BM - 1) / BM, nh = a_is_queries<MODE>() ? a.Hq : a.Hkv;
-  dim3 grid((nrb + kUnits - 1) / kUnits, nh, a.L);
-  // Persistent where it measured faster: the query-side passes, the key-side maximum and
-  // the quadratic form.  The future mass runs two units per CTA (its unit costs spread
-  // widely and the hardware scheduler balances them better).
-  int strided = 0;
-  {
-    static int nsm[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!nsm[dev]) cudaDeviceGetAttribute(&nsm[dev], cudaDevAttrMultiProcessorCount, dev);
-    const long units = (long)nrb * nh * a.L, sms = std::max(1, nsm[dev]);
-    if (MODE != kFuture) {
-      strided = 1;
-      grid = dim3((unsigned)std::min(units, sms), 1, 1);
-    }
-  }
+  // one CTA per SM (fewer when there are fewer units), each looping over its units
+  static int nsm[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!nsm[dev]) cudaDeviceGetAttribute(&nsm[dev], cudaDevAttrMultiProcessorCount, dev);
+  const long units = (long)nrb * nh * a.L;
+  const dim3 grid((unsigned)std::min(units, (long)std::max(1, nsm[dev])), 1, 1);
   auto kern = attn_tc_kernel<D, MODE>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   count_launches(1);
-  kern<<<grid, C::THREADS, C::SMEM, s>>>(ta, tb, tb2, tauga, taugb, a, strided);
+  kern<<<grid, C::THREADS, C::SMEM, s>>>(ta, tb, tb2, tauga, taugb, a);
   return cudaGetLastError();
 }
 
