@@ -1,20 +1,21 @@
 // Attention-scoring passes on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
-// Pass 1 (LSE) and pass 2 (transposed scoring) share one warp-specialised CTA that owns
-// two consecutive 128-row units of operand A and, for each, streams 256-row tiles of
-// operand B; each B tile is one chain of 128 x 256 x 16 MMAs (the wide N keeps the tensor
-// core's shared-memory operand traffic at 96 bytes per clock).  The second unit's MMAs
-// run while the epilogue drains the first, so a CTA's fill and drain are paid once for
-// two units:
-//   warp 0      TMA producer: loads both A tiles up front, then streams B tiles through
-//               a STAGES-deep ring of 128-byte-swizzled smem buffers
+// Every pass runs one warp-specialised CTA per SM (a persistent grid).  A CTA takes
+// 128-row units of operand A round-robin over (layer, head, row block) and, for each,
+// streams 256-row tiles of operand B; each B tile is one chain of 128 x 256 x 16 MMAs
+// (the wide N keeps the tensor core's shared-memory operand traffic at 96 bytes per
+// clock).  Two A buffers alternate between consecutive units, the next unit's A tile
+// loading as soon as its buffer's previous unit has finished its MMAs:
+//   warp 0      TMA producer: A tiles into the two A buffers, B tiles through a ring of
+//               two 64 KB tiles at d = 128 (four at d = 64), handed out per 64-column box
+//               for the key-side maximum so that its loads lead the MMAs by 1.5 tiles
 //   warp 1      allocates all 512 TMEM columns (two 256-column accumulators) and issues
 //               tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32) into one of them
-//   warps 2-9   epilogue, two groups of four warps, one per 128-column half of the
-//               accumulator (two warps per SM sub-partition): one thread per row and
-//               half reads its columns with tcgen05.ld (the second 64 in flight while
-//               the first 64 reduce) while the MMA fills the other accumulator; the two
-//               halves of each row are merged through shared memory at the end
+//   warps 2-17  epilogue, four groups of four warps (one warp per TMEM lane quarter per
+//               group), 64 accumulator columns each: a thread reads its row's columns
+//               with tcgen05.ld, releases the accumulator, and reduces them while the
+//               MMA fills the other accumulator; the groups' partials of each row meet in
+//               shared memory at the end of the unit (the quadratic form keeps two groups)
 // Modes (x = q.k / sqrt(d), never written to memory):
 //   kLse     A = queries,  B = key tiles (context, then tail): online max and
 //            sum of 2^(x log2 e) per query -> ln sum exp(x)
@@ -26,6 +27,10 @@
 //   kFuture  A = keys, B = query tiles j >= i0 + w: per key sum over the group of
 //            2^((x - lse_j) log2 e) for j >= i + w, with -lse_j sqrt(d) folded into the
 //            accumulator by the same extra MMA step as kMax
+//   kQuad    A = values, B = the head's Gram pair [G_hi | G_lo]: v^T G v per key and
+//            query head of the group (the value norms)
+//   kRows    A = queries, B = kept keys: the softmax rows 2^(x log2 e - lse_j log2 e) as
+//            bf16 hi + lo parts, written through a per-warp stage (value refit)
 // Sources: KVpop review, 1. Key Terms (LSE reuse, transposed-attention pass);
 // KVzap review, 3.1 Eq. 1 and 3.2 Eq. 3.
 #include <algorithm>
