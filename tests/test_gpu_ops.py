@@ -495,6 +495,8 @@ REFIT_SHAPES = [
     (2, 1, 2, 64, 130, 70, 77),       # k not a multiple of 64, d = 64
     (1, 1, 3, 128, 520, 257, 1),      # a single kept key
     (1, 2, 2, 128, 700, 300, 333),    # several 128-row tiles of the Gram matrix
+    (1, 1, 2, 128, 1600, 300, 1500),  # 24 Cholesky panels, more kept keys than rows
+    (1, 1, 2, 64, 2100, 150, 2048),   # the largest supported k (32 panels)
 ]
 
 
