@@ -479,6 +479,16 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
             break;
           }
           const uint32_t d_t = tmem + (uint32_t)(acc * BN);
+          uint32_t idesc = C::IDESC;
+          if constexpr (MODE == kLse) {
+            // a tile past the causal limit of the unit's last query (or past the end of its
+            // key range) is multiplied only up to its last visible column, rounded up to
+            // 16; the epilogue masks or skips every column past it
+            const bool ctx = it < U.n_ctx;
+            const int kb0 = ctx ? it * BN : a.T + (it - U.n_ctx) * BN;
+            const int vis = min(ctx ? a.T : n_k, off + min(U.row0 + BM, a.n_q)) - kb0;
+            if (vis < BN) idesc = tc::idesc_bf16(BM, max(16, (vis + 15) & ~15));
+          }
           constexpr int BPP = C::KH / C::PARTS;  // boxes per slot
 #pragma unroll
           for (int pt = 0; pt < C::PARTS; ++pt, ++nb) {  // part pt of the tile, in slot nb % NS
@@ -494,7 +504,7 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
               const int kh = pt * BPP + (k >> 2);  // box of the tile
               const uint32_t kk = (uint32_t)(k & 3) * 32u;
               tc::mma_bf16(d_t, tc::sdesc_sw128(a_n + kh * kBoxBytesA + kk),
-                           tc::sdesc_sw128(b_j + (k >> 2) * kBoxBytesB + kk), C::IDESC,
+                           tc::sdesc_sw128(b_j + (k >> 2) * kBoxBytesB + kk), idesc,
                            (pt | k) ? 1u : 0u);
             }
             if (C::AUG && pt == C::PARTS - 1)  // + (1,1,1,0..) . (c_hi, c_mid, c_lo, 0..)
