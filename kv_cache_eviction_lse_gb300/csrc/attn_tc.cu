@@ -480,10 +480,10 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
           }
           const uint32_t d_t = tmem + (uint32_t)(acc * BN);
           uint32_t idesc = C::IDESC;
-          if constexpr (MODE == kLse) {
+          if constexpr (MODE == kLse || MODE == kRows) {
             // a tile past the causal limit of the unit's last query (or past the end of its
             // key range) is multiplied only up to its last visible column, rounded up to
-            // 16; the epilogue masks or skips every column past it
+            // 16; the epilogue masks, skips or zeroes every column past it
             const bool ctx = it < U.n_ctx;
             const int kb0 = ctx ? it * BN : a.T + (it - U.n_ctx) * BN;
             const int vis = min(ctx ? a.T : n_k, off + min(U.row0 + BM, a.n_q)) - kb0;
