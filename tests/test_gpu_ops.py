@@ -349,7 +349,8 @@ def test_prune_topk_exact(C, T, levels, nan_frac):
 
 
 @pytest.mark.parametrize("T,page", [(1, 16), (100, 16), (4096, 16), (5000, 16), (9000, 7),
-                                    (333, 1), (17, 4096)])
+                                    (333, 1), (17, 4096), (48, 16), (2048, 16), (6144, 8),
+                                    (8192, 16), (45056, 16)])
 @pytest.mark.parametrize("d", [64, 128])
 def test_compact_exact(C, T, page, d):
     L, H = 2, 3
