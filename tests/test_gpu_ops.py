@@ -329,7 +329,10 @@ def test_prune_threshold_exact(C, T, levels, nan_frac):
         assert np.array_equal(keep.cpu().numpy(), k_ref), (tau, w)
 
 
-@pytest.mark.parametrize("T", [1, 7, 300, 2048, 16384])
+# row lengths on both sides of every register-resident width (1, 2, 4, 8, 16 tokens per
+# thread, with and without 16-byte rows) and past it (rows re-read from global memory)
+@pytest.mark.parametrize("T", [1, 7, 300, 1024, 1025, 2048, 3001, 4096, 6002, 8192, 16383,
+                               16384, 20000])
 @pytest.mark.parametrize("levels,nan_frac", [(None, 0.0), (3, 0.0), (4, 0.05)])
 def test_prune_topk_exact(C, T, levels, nan_frac):
     L, H = 2, 3
