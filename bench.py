@@ -31,7 +31,7 @@ The step is replayed from a CUDA graph captured once (``--no-graph`` launches ev
 call from Python instead); each entry point's timing also replays its own graph.
 
 `--impl reference` times the CPU oracle itself (the only reference implementation: the
-pages ship no code) on the machine's host cores, each step a bounded sample of the workload.
+pages ship no code) on the host's CPU cores, each step a bounded sample of the workload.
 Under torchrun (N > 1) every rank runs its own replica of the workload (weak scaling; the
 path shards by independent problems and needs no data exchange).
 """
