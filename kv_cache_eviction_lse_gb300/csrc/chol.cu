@@ -5,15 +5,20 @@
 // launch over all problems, so the trailing updates (the bulk of the work) spread over
 // the whole GPU instead of one CTA per problem:
 //   per 64-row panel p:  factor the diagonal block (one CTA per problem), solve the row
-//                        panel U_pp^T X = G[p][p+64:] (CTAs over 64-column blocks), update
-//                        the trailing upper triangle G -= X^T X (CTAs over 64 x 64 tiles)
-// The solves then run as one launch: the 64-column blocks of right-hand sides are
-// independent, so one CTA per (problem, column block) takes both sweeps, each a diagonal
-// block's triangular solve followed by the update of every remaining block row.
+//                        panel U_pp^T X = [G[p][p+64:] | R[p]] (CTAs over 64-column
+//                        blocks), update the trailing upper triangle G -= X^T X and the
+//                        trailing rows of R (CTAs over 64 x 64 tiles)
+// R rides along as extra columns of the factorised matrix, so the forward solve U^T Y = R
+// is done when the factorisation is.  The backward solve U X = Y then runs as one launch:
+// the column blocks of right-hand sides are independent, so one CTA per (problem, column
+// block) takes the whole sweep, each diagonal block's triangular solve followed by the
+// update of every block row above it.
 // G arrives as its upper block triangle (the Gram kernel writes only those tiles); the
 // lower triangle is never read.  Rows/columns k .. M-1 (padding of the kept-key
 // dimension) are decoupled: their diagonal becomes 1 and their right-hand side 0.
 #include <math.h>
+
+#include <algorithm>
 
 #include "gram.cuh"
 
@@ -151,33 +156,58 @@ __device__ __forceinline__ void load_diag_block(const float* G, int ldg, int p, 
   __syncthreads();
 }
 
-// Row panel: G[p..p+64][j] = U_pp^-T G[p..p+64][j] for the 64 columns j of block
-// blockIdx.x after the diagonal block; one thread per column
-__global__ void __launch_bounds__(NB) trsm_row_kernel(const CholArgs a, int p) {
+// Row panel: X = U_pp^-T B for the 64 columns of block blockIdx.x of [G[p][p+64:] | R[p]]
+// (the first `rest` blocks are G's, the next d / 64 are R's); one thread per column
+__global__ void __launch_bounds__(NB) trsm_row_kernel(const CholArgs a, int p, int rest) {
   float* G = prob(a.g, (size_t)a.M * a.ldg);
-  const int j = p + NB + blockIdx.x * NB + threadIdx.x;
+  float* R = prob(a.r, (size_t)a.M * a.d);
+  const bool in_r = (int)blockIdx.x >= rest;
+  float* col = in_r ? R + (size_t)p * a.d + (blockIdx.x - rest) * NB + threadIdx.x
+                    : G + (size_t)p * a.ldg + p + NB + blockIdx.x * NB + threadIdx.x;
+  const size_t ld = in_r ? (size_t)a.d : (size_t)a.ldg;
   __shared__ __align__(16) float w[NB][NB];
   __shared__ float dinv[NB];
   load_diag_block(G, a.ldg, p, NB, false, w, dinv);
-  if (j >= a.M) return;
   float x[NB];
 #pragma unroll
-  for (int r = 0; r < NB; ++r) x[r] = G[(size_t)(p + r) * a.ldg + j];
-  tri_solve_col<false>(x, w, dinv, G + (size_t)p * a.ldg + j, a.ldg);
+  for (int r = 0; r < NB; ++r) x[r] = col[(size_t)r * ld];
+  tri_solve_col<false>(x, w, dinv, col, ld);
 }
 
-// Trailing update of the upper triangle after panel p: tile (ti, tj), ti <= tj, of the
-// trailing 64-blocks: G[i][j] -= sum_r U[p+r][i] U[p+r][j]; 256 threads, 4 x 4 each
+// Trailing update after panel p, 256 threads, 4 x 4 each.  Blocks below nt (nt + 1) / 2:
+// tile (ti, tj), ti <= tj, of the trailing 64-blocks, G[i][j] -= sum_r U[p+r][i] U[p+r][j];
+// the rest: tile (ti, column block cb) of R's trailing rows, R[i][c] -= sum_r U[p+r][i] Y[p+r][c]
 __global__ void __launch_bounds__(256) syrk_kernel(const CholArgs a, int p) {
   float* G = prob(a.g, (size_t)a.M * a.ldg);
+  float* R = prob(a.r, (size_t)a.M * a.d);
   const int q0 = p + NB, nt = (a.M - q0) / NB;
   int t = blockIdx.x, ti = 0;
-  while (t >= nt - ti) {
-    t -= nt - ti;
-    ++ti;
+  const bool in_r = t >= nt * (nt + 1) / 2;
+  const float* src_j;  // rows p .. p+63 of the right factor, and its row stride
+  size_t ldj;
+  float* dst;          // the updated tile and its row stride
+  size_t ldd;
+  if (in_r) {
+    t -= nt * (nt + 1) / 2;
+    const int ncb = a.d / NB;
+    ti = t / ncb;
+    const int c0 = (t % ncb) * NB;
+    src_j = R + (size_t)p * a.d + c0;
+    ldj = a.d;
+    dst = R + (size_t)(q0 + ti * NB) * a.d + c0;
+    ldd = a.d;
+  } else {
+    while (t >= nt - ti) {
+      t -= nt - ti;
+      ++ti;
+    }
+    const int j0 = q0 + (ti + t) * NB;
+    src_j = G + (size_t)p * a.ldg + j0;
+    ldj = a.ldg;
+    dst = G + (size_t)(q0 + ti * NB) * a.ldg + j0;
+    ldd = a.ldg;
   }
-  const int tj = ti + t;
-  const int i0 = q0 + ti * NB, j0 = q0 + tj * NB;
+  const int i0 = q0 + ti * NB;
   __shared__ __align__(16) float xi[NB][NB + 4];  // [r][column]
   __shared__ __align__(16) float xj[NB][NB + 4];
   for (int idx = threadIdx.x; idx < NB * NB / 4; idx += 256) {
@@ -185,7 +215,7 @@ __global__ void __launch_bounds__(256) syrk_kernel(const CholArgs a, int p) {
     *reinterpret_cast<float4*>(&xi[r][c]) =
         *reinterpret_cast<const float4*>(G + (size_t)(p + r) * a.ldg + i0 + c);
     *reinterpret_cast<float4*>(&xj[r][c]) =
-        *reinterpret_cast<const float4*>(G + (size_t)(p + r) * a.ldg + j0 + c);
+        *reinterpret_cast<const float4*>(src_j + (size_t)r * ldj + c);
   }
   __syncthreads();
   const int tr = (threadIdx.x / 16) * 4, tc = (threadIdx.x % 16) * 4;
@@ -202,84 +232,97 @@ __global__ void __launch_bounds__(256) syrk_kernel(const CholArgs a, int p) {
   }
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
-    float4* gp = reinterpret_cast<float4*>(G + (size_t)(i0 + tr + u) * a.ldg + j0 + tc);
+    float4* gp = reinterpret_cast<float4*>(dst + (size_t)(tr + u) * ldd + tc);
     float4 g4 = *gp;
     g4.x -= acc[u][0]; g4.y -= acc[u][1]; g4.z -= acc[u][2]; g4.w -= acc[u][3];
     *gp = g4;  // entries below the diagonal of a diagonal tile are never read
   }
 }
 
-// Both triangular solves (U^T Y = R, then U X = Y) of one problem and one 64-column block
-// of right-hand sides; the column blocks are independent, so each CTA runs the whole
-// chain with no other launch.  Per 64-row block p (forward ascending, backward
-// descending): the diagonal solve in registers (threads 0..63, one column each) into the
-// stage ys, then every remaining block row q is updated, forward R[q] -= U[p][q]^T Y[p],
-// backward R[q] -= U[q][p] X[p] (64 x 64 x 64, a 4 x 4 tile per thread).  Y goes back to
-// R; X rows below k go to the output.
-__global__ void __launch_bounds__(256) solve_kernel(const CholArgs a) {
+// Backward solve U X = Y of one problem and one block of CB right-hand-side columns (Y
+// is in R: the forward solve rode along with the factorisation); the column blocks are
+// independent, so each CTA runs the whole chain with no other launch (narrow blocks give
+// more CTAs, whose latency chains overlap).  Per 64-row block p, descending: the diagonal
+// solve in registers (threads 0..CB-1, one column each) into the stage ys, then every
+// block row q above it is updated, R[q] -= U[q][p] X[p] (64 x 64 x CB; a thread owns
+// CB/16 rows x 4 columns).  The next block row's U block is loaded into registers while
+// the current one is multiplied, and a thread's R tile is read before the products so
+// that its loads overlap them.  X rows below k go to the output.
+template <int CB>
+__global__ void __launch_bounds__(256, CB == 64 ? 1 : 2) solve_kernel(const CholArgs a) {
+  constexpr int CG = CB / 4;      // groups of 4 columns
+  constexpr int RPT = CB / 16;    // rows per thread in the updates
+  constexpr int LDY = CB + 4;     // ys row stride (16-byte aligned rows)
+  constexpr int UPT = NB * NB / 256;  // U block elements per thread
+  static_assert(RPT >= 1 && (256 / CG) * RPT == NB, "column block of 16, 32 or 64");
   const float* G = prob(a.g, (size_t)a.M * a.ldg);
   float* R = prob(a.r, (size_t)a.M * a.d);
   float* X = prob(a.x, (size_t)a.k * a.d);
-  const int c0 = blockIdx.x * NB, tid = threadIdx.x, nb = a.M / NB;
+  const int c0 = blockIdx.x * CB, tid = threadIdx.x, nb = a.M / NB;
   __shared__ __align__(16) float w[NB][NB];   // diagonal block, pre-shifted
   __shared__ float dinv[NB];
-  __shared__ __align__(16) float ys[NB][kLd];  // solved rows of block p
-  __shared__ __align__(16) float us[NB][kLd];  // coefficients of block p in block row q
-  const int tq = (tid / 16) * 4, tc = (tid % 16) * 4;
-  for (int pass = 0; pass < 2; ++pass) {
-    const bool back = pass == 1;
-    for (int bi = 0; bi < nb; ++bi) {
-      const int p = (back ? nb - 1 - bi : bi) * NB;
-      __syncthreads();  // the previous block's reads of w, ys and us are done
-      load_diag_block(G, a.ldg, p, 256, back, w, dinv);
-      if (tid < NB) {
-        float x[NB];
+  __shared__ __align__(16) float ys[NB][LDY];  // solved rows of block p
+  __shared__ __align__(16) float us[NB][kLd];  // us[r][i] = U[q+i][p+r]
+  const int tq = (tid / CG) * RPT, tc = (tid % CG) * 4;
+  for (int p = (nb - 1) * NB; p >= 0; p -= NB) {
+    // the previous block's reads of w, ys and us are done and its updates of R visible
+    __syncthreads();
+    float x[NB];
+    if (tid < CB) {  // the block's right-hand sides, in flight while w is staged
 #pragma unroll
-        for (int i = 0; i < NB; ++i)
-          x[i] = R[(size_t)(p + (back ? NB - 1 - i : i)) * a.d + c0 + tid];
-        if (back)
-          tri_solve_col<true>(x, w, dinv, &ys[0][tid], kLd);
-        else
-          tri_solve_col<false>(x, w, dinv, &ys[0][tid], kLd);
+      for (int i = 0; i < NB; ++i) x[i] = R[(size_t)(p + NB - 1 - i) * a.d + c0 + tid];
+    }
+    load_diag_block(G, a.ldg, p, 256, true, w, dinv);
+    if (tid < CB) tri_solve_col<true>(x, w, dinv, &ys[0][tid], LDY);
+    __syncthreads();
+    for (int idx = tid; idx < NB * CB; idx += 256) {
+      const int r = idx / CB, c = idx % CB;
+      if (p + r < a.k) X[(size_t)(p + r) * a.d + c0 + c] = ys[r][c];
+    }
+    // U[q+i][p+j] of block row q (consecutive threads read consecutive addresses)
+    float ureg[UPT];
+    auto load_u = [&](int q) {
+#pragma unroll
+      for (int e = 0; e < UPT; ++e) {
+        const int idx = tid + 256 * e, i = idx / NB, j = idx % NB;
+        ureg[e] = G[(size_t)(q + i) * a.ldg + p + j];
       }
+    };
+    if (p > 0) load_u(0);
+    for (int q = 0; q < p; q += NB) {
+#pragma unroll
+      for (int e = 0; e < UPT; ++e) {
+        const int idx = tid + 256 * e, i = idx / NB, j = idx % NB;
+        us[j][i] = ureg[e];
+      }
+      float4 r4[RPT];
+#pragma unroll
+      for (int u = 0; u < RPT; ++u)
+        r4[u] = *reinterpret_cast<const float4*>(R + (size_t)(q + tq + u) * a.d + c0 + tc);
       __syncthreads();
-      for (int idx = tid; idx < NB * NB; idx += 256) {
-        const int r = idx / NB, c = idx % NB;
-        if (!back)
-          R[(size_t)(p + r) * a.d + c0 + c] = ys[r][c];
-        else if (p + r < a.k)
-          X[(size_t)(p + r) * a.d + c0 + c] = ys[r][c];
-      }
-      const int q_begin = back ? 0 : p + NB, q_end = back ? p : a.M;
-      for (int q = q_begin; q < q_end; q += NB) {
-        for (int idx = tid; idx < NB * NB; idx += 256) {
-          const int i = idx / NB, j = idx % NB;  // consecutive threads read consecutive addresses
-          if (back)
-            us[j][i] = G[(size_t)(q + i) * a.ldg + p + j];  // U[q+i][p+j]
-          else
-            us[i][j] = G[(size_t)(p + i) * a.ldg + q + j];  // U[p+i][q+j]
-        }
-        __syncthreads();
-        float acc[4][4] = {};
+      if (q + NB < p) load_u(q + NB);  // in flight during the products
+      float acc[RPT][4] = {};
 #pragma unroll 8
-        for (int r = 0; r < NB; ++r) {
-          const float4 a4 = *reinterpret_cast<const float4*>(&us[r][tq]);
-          const float4 b4 = *reinterpret_cast<const float4*>(&ys[r][tc]);
-          const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
+      for (int r = 0; r < NB; ++r) {
+        const float4 b4 = *reinterpret_cast<const float4*>(&ys[r][tc]);
+        const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+        float av[RPT];
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < RPT; ++u) av[u] = us[r][tq + u];
 #pragma unroll
-            for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
-        }
+        for (int u = 0; u < RPT; ++u)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          float4* rp = reinterpret_cast<float4*>(R + (size_t)(q + tq + u) * a.d + c0 + tc);
-          float4 r4 = *rp;
-          r4.x -= acc[u][0]; r4.y -= acc[u][1]; r4.z -= acc[u][2]; r4.w -= acc[u][3];
-          *rp = r4;
-        }
-        __syncthreads();  // us is reloaded for the next block row
+          for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
       }
+#pragma unroll
+      for (int u = 0; u < RPT; ++u) {
+        r4[u].x -= acc[u][0];
+        r4[u].y -= acc[u][1];
+        r4[u].z -= acc[u][2];
+        r4[u].w -= acc[u][3];
+        *reinterpret_cast<float4*>(R + (size_t)(q + tq + u) * a.d + c0 + tc) = r4[u];
+      }
+      __syncthreads();  // us is rewritten for the next block row
     }
   }
 }
@@ -295,17 +338,29 @@ cudaError_t launch_chol_solve(const CholArgs& a, cudaStream_t s) {
   int launches = 0;
   shift_kernel<<<dim3(1, B), 256, 0, s>>>(a);
   ++launches;
-  for (int b = 0; b < nb; ++b) {  // G + lam I = U^T U
+  for (int b = 0; b < nb; ++b) {  // G + lam I = U^T U, and Y = U^-T R alongside
     const int p = b * NB, rest = nb - b - 1;
     potrf_kernel<<<dim3(1, B), NB, 0, s>>>(a, p);
-    ++launches;
+    trsm_row_kernel<<<dim3(rest + dcb, B), NB, 0, s>>>(a, p, rest);
+    launches += 2;
     if (rest > 0) {
-      trsm_row_kernel<<<dim3(rest, B), NB, 0, s>>>(a, p);
-      syrk_kernel<<<dim3(rest * (rest + 1) / 2, B), 256, 0, s>>>(a, p);
-      launches += 2;
+      syrk_kernel<<<dim3(rest * (rest + 1) / 2 + rest * dcb, B), 256, 0, s>>>(a, p);
+      ++launches;
     }
   }
-  solve_kernel<<<dim3(dcb, B), 256, 0, s>>>(a);  // U^T Y = R, U X = Y, X = rows < k
+  // U X = Y, X = rows < k: the narrowest right-hand-side blocks (16 or 32
+  // columns) whose CTAs are all resident at once (two per SM), else blocks of 64 columns
+  static int nsm[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!nsm[dev]) cudaDeviceGetAttribute(&nsm[dev], cudaDevAttrMultiProcessorCount, dev);
+  const size_t resident = 2 * (size_t)std::max(1, nsm[dev]);
+  if ((size_t)dcb * 4 * B <= resident)
+    solve_kernel<16><<<dim3(dcb * 4, B), 256, 0, s>>>(a);
+  else if ((size_t)dcb * 2 * B <= resident)
+    solve_kernel<32><<<dim3(dcb * 2, B), 256, 0, s>>>(a);
+  else
+    solve_kernel<64><<<dim3(dcb, B), 256, 0, s>>>(a);
   ++launches;
   count_launches(launches);
   return cudaGetLastError();
