@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(NB) potrf_kernel(const CholArgs a, int p) {
 // is written to out[r * ld] as soon as it is final.  Forward: U^T y = x with x[i] = row i
 // initially; backward: U y = x with x[i] = row 63 - i initially.
 template <bool BACKWARD>
-__device__ __forceinline__ void tri_solve_col(float (&x)[NB], const float (*w)[NB],
+__device__ __forceinline__ void tri_solve_col(float (&x)[NB], const float (*w)[kLd],
                                               const float* dinv, float* out, size_t ld) {
 #pragma unroll 1
   for (int k = 0; k < NB; ++k) {
@@ -136,19 +136,33 @@ __device__ __forceinline__ void tri_solve_col(float (&x)[NB], const float (*w)[N
 }
 
 // Stages the diagonal block at p pre-shifted for a forward solve (w[r][i] = U[r][r+i]) or
-// a backward one (w[r][i] = U[r-i][r]), zero past the block, and 1 / diag (nt threads).
-__device__ __forceinline__ void load_diag_block(const float* G, int ldg, int p, int nt,
-                                                bool backward, float (*w)[NB], float* dinv) {
-  for (int idx = threadIdx.x; idx < NB * NB; idx += nt) w[idx / NB][idx % NB] = 0.f;
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < NB * NB; idx += nt) {
-    const int r = idx / NB, c = idx % NB;  // U[r][c], c >= r
-    if (c >= r) {
-      const float v = G[(size_t)(p + r) * ldg + p + c];
-      if (backward)
-        w[c][c - r] = v;
+// a backward one (w[r][i] = U[r-i][r]), zero past the block, and 1 / diag, with NT
+// threads in one pass: each thread issues all its (coalesced) loads before it stores, and
+// the lower-triangle positions it visits map one to one onto the zero slots (forward:
+// (r, c < r) -> w[r][63 - c]; backward: (r > c, c) -> w[c][r]).
+template <int NT, bool BACKWARD>
+__device__ __forceinline__ void load_diag_block(const float* G, int ldg, int p,
+                                                float (*w)[kLd], float* dinv) {
+  constexpr int PER = NB * NB / NT;
+  float v[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const int idx = (int)threadIdx.x + e * NT, r = idx / NB, c = idx % NB;
+    v[e] = c >= r ? G[(size_t)(p + r) * ldg + p + c] : 0.f;
+  }
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const int idx = (int)threadIdx.x + e * NT, r = idx / NB, c = idx % NB;
+    if (BACKWARD) {
+      if (c >= r)
+        w[c][c - r] = v[e];
       else
-        w[r][c - r] = v;
+        w[c][r] = 0.f;
+    } else {
+      if (c >= r)
+        w[r][c - r] = v[e];
+      else
+        w[r][NB - 1 - c] = 0.f;
     }
   }
   __syncthreads();
@@ -165,9 +179,9 @@ __global__ void __launch_bounds__(NB) trsm_row_kernel(const CholArgs a, int p, i
   float* col = in_r ? R + (size_t)p * a.d + (blockIdx.x - rest) * NB + threadIdx.x
                     : G + (size_t)p * a.ldg + p + NB + blockIdx.x * NB + threadIdx.x;
   const size_t ld = in_r ? (size_t)a.d : (size_t)a.ldg;
-  __shared__ __align__(16) float w[NB][NB];
+  __shared__ __align__(16) float w[NB][kLd];
   __shared__ float dinv[NB];
-  load_diag_block(G, a.ldg, p, NB, false, w, dinv);
+  load_diag_block<NB, false>(G, a.ldg, p, w, dinv);
   float x[NB];
 #pragma unroll
   for (int r = 0; r < NB; ++r) x[r] = col[(size_t)r * ld];
@@ -259,7 +273,7 @@ __global__ void __launch_bounds__(256, CB == 64 ? 1 : 2) solve_kernel(const Chol
   float* R = prob(a.r, (size_t)a.M * a.d);
   float* X = prob(a.x, (size_t)a.k * a.d);
   const int c0 = blockIdx.x * CB, tid = threadIdx.x, nb = a.M / NB;
-  __shared__ __align__(16) float w[NB][NB];   // diagonal block, pre-shifted
+  __shared__ __align__(16) float w[NB][kLd];  // diagonal block, pre-shifted
   __shared__ float dinv[NB];
   __shared__ __align__(16) float ys[NB][LDY];  // solved rows of block p
   __shared__ __align__(16) float us[NB][kLd];  // us[r][i] = U[q+i][p+r]
@@ -272,7 +286,7 @@ __global__ void __launch_bounds__(256, CB == 64 ? 1 : 2) solve_kernel(const Chol
 #pragma unroll
       for (int i = 0; i < NB; ++i) x[i] = R[(size_t)(p + NB - 1 - i) * a.d + c0 + tid];
     }
-    load_diag_block(G, a.ldg, p, 256, true, w, dinv);
+    load_diag_block<256, true>(G, a.ldg, p, w, dinv);
     if (tid < CB) tri_solve_col<true>(x, w, dinv, &ys[0][tid], LDY);
     __syncthreads();
     for (int idx = tid; idx < NB * CB; idx += 256) {
