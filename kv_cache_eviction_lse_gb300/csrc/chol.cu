@@ -64,7 +64,51 @@ __global__ void __launch_bounds__(256) shift_kernel(const CholArgs a) {
 // registers under a rolled pivot loop instead: the column is shifted by one register per
 // step (x[i] holds row r + i), fused with the update x[i-1] = x[i] - w[i] x[0], so the
 // pivot is always x[0] and the step's line of U is staged pre-shifted (w[i] = U[r][r+i])
-// for aligned 16-byte reads.
+// for aligned 16-byte reads.  After 16 steps the top 16 registers hold only finished
+// rows, so the 64 steps run as four rolled loops over 64, 48, 32 and 16 registers.
+static_assert(NB == 64, "the diagonal-block chains run in four phases of 16 steps");
+
+// x[i-1] = x[i] - wrow[i] xr for i = 1 .. W-1, x[W-1] = 0 (wrow 16-byte aligned)
+template <int W>
+__device__ __forceinline__ void shift_axpy(float (&x)[NB], const float* wrow, float xr) {
+#pragma unroll
+  for (int i4 = 0; i4 < W; i4 += 4) {
+    const float4 q = *reinterpret_cast<const float4*>(&wrow[i4]);
+    const float qv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (i4 + e >= 1) x[i4 + e - 1] = fmaf(-qv[e], xr, x[i4 + e]);
+  }
+  x[W - 1] = 0.f;
+}
+
+// Pivots r0 .. r0+15 of the diagonal block (see potrf_kernel); W registers are live.
+template <int W>
+__device__ __forceinline__ void potrf_steps(float (&x)[NB], int r0, int c, float* G, int ldg,
+                                            float* prow, float* pinv) {
+#pragma unroll 1
+  for (int r = r0; r < r0 + 16; ++r) {
+    if (c == r) {
+      const float v = x[0];
+      if (!(v > 0.f)) atomicCAS(&g_chol_error, 0, kErrNotSpd);
+      const float piv = sqrtf(fmaxf(v, 1e-30f));
+      G[(size_t)r * ldg + r] = piv;
+      *pinv = 1.f / piv;
+    }
+    __syncthreads();
+    float xr = 0.f;
+    if (c > r) {
+      xr = x[0] * *pinv;
+      G[(size_t)r * ldg + c] = xr;
+      prow[c - r] = xr;
+    }
+    __syncthreads();
+    // columns c > r: rows r+1 .. c; past c the registers hold nothing that is stored
+    shift_axpy<W>(x, prow, xr);
+    __syncthreads();  // prow is rewritten by the next pivot
+    if (c > r) prow[c - r] = 0.f;
+  }
+}
 
 // Cholesky of the diagonal block at p (upper, in place), one CTA of 64 threads per
 // problem: thread c keeps column c of the block in registers; per pivot r the owner of
@@ -79,60 +123,35 @@ __global__ void __launch_bounds__(NB) potrf_kernel(const CholArgs a, int p) {
 #pragma unroll
   for (int i = 0; i < NB; ++i) x[i] = i <= c ? G[(size_t)i * a.ldg + c] : 0.f;
   prow[c] = 0.f;
-#pragma unroll 1
-  for (int r = 0; r < NB; ++r) {
-    if (c == r) {
-      const float v = x[0];
-      if (!(v > 0.f)) atomicCAS(&g_chol_error, 0, kErrNotSpd);
-      const float piv = sqrtf(fmaxf(v, 1e-30f));
-      G[(size_t)r * a.ldg + r] = piv;
-      pinv = 1.f / piv;
-    }
-    __syncthreads();
-    float xr = 0.f;
-    if (c > r) {
-      xr = x[0] * pinv;
-      G[(size_t)r * a.ldg + c] = xr;
-      prow[c - r] = xr;
-    }
-    __syncthreads();
-    // columns c > r: rows r+1 .. c; past c the registers hold nothing that is stored
-#pragma unroll
-    for (int i4 = 0; i4 < NB; i4 += 4) {
-      const float4 w = *reinterpret_cast<const float4*>(&prow[i4]);
-      const float wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (i4 + e >= 1) x[i4 + e - 1] = fmaf(-wv[e], xr, x[i4 + e]);
-    }
-    x[NB - 1] = 0.f;
-    __syncthreads();  // prow is rewritten by the next pivot
-    if (c > r) prow[c - r] = 0.f;
-  }
+  potrf_steps<64>(x, 0, c, G, a.ldg, prow, &pinv);
+  potrf_steps<48>(x, 16, c, G, a.ldg, prow, &pinv);
+  potrf_steps<32>(x, 32, c, G, a.ldg, prow, &pinv);
+  potrf_steps<16>(x, 48, c, G, a.ldg, prow, &pinv);
 }
 
 // Triangular solve of 64 rows in registers against the staged diagonal block (rows of w
 // pre-shifted as above, dinv = 1 / diag), one column per thread; row r of the solution
 // is written to out[r * ld] as soon as it is final.  Forward: U^T y = x with x[i] = row i
 // initially; backward: U y = x with x[i] = row 63 - i initially.
-template <bool BACKWARD>
-__device__ __forceinline__ void tri_solve_col(float (&x)[NB], const float (*w)[kLd],
-                                              const float* dinv, float* out, size_t ld) {
+template <bool BACKWARD, int W>
+__device__ __forceinline__ void tri_steps(float (&x)[NB], const float (*w)[kLd],
+                                          const float* dinv, float* out, size_t ld, int k0) {
 #pragma unroll 1
-  for (int k = 0; k < NB; ++k) {
+  for (int k = k0; k < k0 + 16; ++k) {
     const int r = BACKWARD ? NB - 1 - k : k;
     const float xr = x[0] * dinv[r];
     out[(size_t)r * ld] = xr;
-#pragma unroll
-    for (int i4 = 0; i4 < NB; i4 += 4) {
-      const float4 q = *reinterpret_cast<const float4*>(&w[r][i4]);
-      const float qv[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (i4 + e >= 1) x[i4 + e - 1] = fmaf(-qv[e], xr, x[i4 + e]);
-    }
-    x[NB - 1] = 0.f;
+    shift_axpy<W>(x, w[r], xr);
   }
+}
+
+template <bool BACKWARD>
+__device__ __forceinline__ void tri_solve_col(float (&x)[NB], const float (*w)[kLd],
+                                              const float* dinv, float* out, size_t ld) {
+  tri_steps<BACKWARD, 64>(x, w, dinv, out, ld, 0);
+  tri_steps<BACKWARD, 48>(x, w, dinv, out, ld, 16);
+  tri_steps<BACKWARD, 32>(x, w, dinv, out, ld, 32);
+  tri_steps<BACKWARD, 16>(x, w, dinv, out, ld, 48);
 }
 
 // Stages the diagonal block at p pre-shifted for a forward solve (w[r][i] = U[r][r+i]) or
