@@ -28,14 +28,15 @@ cudaError_t gram_device_error(int* code, bool clear, cudaStream_t s);
 
 struct CholArgs {
   float* g = nullptr;      // [batch][M][ldg]: Gram (upper block triangle), overwritten by U
-  float* r = nullptr;      // [batch][M][d]: right-hand sides, overwritten by the solution
+  float* r = nullptr;      // [batch][M][d]: right-hand sides, used as scratch by the solves
   float* x = nullptr;      // [batch][k][d]: output, the first k rows of the solution
   int batch = 0, M = 0, ldg = 0, k = 0, d = 0;
   float lam_rel = 0.f;     // ridge weight relative to the mean of the first k diagonal entries
 };
 
-// Solves (G + lam I) X = R per problem, lam = lam_rel * trace(G[:k, :k]) / k, by an
-// upper Cholesky factorisation in fp32 (one CTA per problem).  M <= kCholMaxM.
+// Solves (G + lam I) X = R per problem, lam = lam_rel * trace(G[:k, :k]) / k, by a blocked
+// upper Cholesky factorisation in fp32 (one launch per step over all problems; R rides
+// along as extra columns) and one backward-solve launch.  M <= kCholMaxM.
 constexpr int kCholMaxM = 2048;
 cudaError_t launch_chol_solve(const CholArgs& a, cudaStream_t s);
 cudaError_t chol_device_error(int* code, bool clear, cudaStream_t s);
