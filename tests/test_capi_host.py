@@ -1,6 +1,6 @@
 """The C-ABI library builds, loads and exports every symbol include/kvs.h declares; its
 host-side validation rejects bad arguments with the documented status codes.  No GPU:
-every call here fails validation before anything is enqueued."""
+every call here fails validation, or is an empty call, before anything is enqueued."""
 import ctypes
 import os
 import re
@@ -97,6 +97,64 @@ def test_validation_codes(capi):
     st = lib.kvs_compact_paged(ctypes.byref(dm), fake, fake, 100, fake, 0, fake, fake, 10, fake, 7,
                                fake, fake, fake, 1 << 20, None)
     assert st == C.KVS_ERR_UNSUPPORTED
+
+
+def test_validation_codes_next_rows(capi):
+    """The attention forward, pass-2 reductions, value refit and decode step."""
+    C = capi
+    lib = C._lib
+    by = ctypes.byref
+    dm = C.dims(1, 4, 2, 128, 0)
+    fake = 1 << 20  # never dereferenced
+    # attention forward: more queries than keys, missing output, missing tail, empty call
+    assert lib.kvs_attn_fwd(by(dm), fake, 20, fake, fake, 10, fake, fake, 5, fake, fake,
+                            None) == C.KVS_ERR_SHAPE
+    assert lib.kvs_attn_fwd(by(dm), fake, 4, fake, fake, 10, None, None, 0, None, fake,
+                            None) == C.KVS_ERR_ARG
+    assert lib.kvs_attn_fwd(by(dm), fake, 4, fake, fake, 10, None, None, 2, fake, fake,
+                            None) == C.KVS_ERR_ARG
+    assert lib.kvs_attn_fwd(by(dm), None, 0, None, None, 10, None, None, 0, None, None,
+                            None) == C.KVS_OK
+    # KVzip(+) maximum: hidden states without D_h, short workspace, empty call
+    assert lib.kvs_score_max(by(dm), fake, 4, fake, 10, fake, None, fake, 0, fake, fake, 1 << 30,
+                             None) == C.KVS_ERR_SHAPE
+    need = lib.kvs_score_max_workspace_size(by(dm), 4, 0)
+    assert lib.kvs_score_max(by(dm), fake, 4, fake, 10, fake, None, None, 0, fake, fake, need - 1,
+                             None) == C.KVS_ERR_CAPACITY
+    assert lib.kvs_score_max(by(dm), None, 4, None, 0, None, None, None, 0, None, None, 0,
+                             None) == C.KVS_OK
+    # future mass: negative window, short workspace
+    assert lib.kvs_score_future_sum(by(dm), fake, fake, 10, fake, -1, fake, fake, 1 << 30,
+                                    None) == C.KVS_ERR_ARG
+    need = lib.kvs_score_future_sum_workspace_size(by(dm), 10)
+    assert need > 0
+    assert lib.kvs_score_future_sum(by(dm), fake, fake, 10, fake, 0, fake, fake, need - 1,
+                                    None) == C.KVS_ERR_CAPACITY
+    # value refit: more kept keys than keys, negative ridge, k past the largest
+    # factorisation, short workspace, empty call
+    assert lib.kvs_value_refit(by(dm), fake, 10, fake, fake, 10, fake, 11, 1e-3, fake, fake,
+                               1 << 30, None) == C.KVS_ERR_SHAPE
+    assert lib.kvs_value_refit(by(dm), fake, 10, fake, fake, 100, fake, 50, -1.0, fake, fake,
+                               1 << 30, None) == C.KVS_ERR_ARG
+    assert lib.kvs_value_refit(by(dm), fake, 10, fake, fake, 3000, fake, 2049, 1e-3, fake, fake,
+                               1 << 30, None) == C.KVS_ERR_UNSUPPORTED
+    need = lib.kvs_value_refit_workspace_size(by(dm), 10, 100)
+    # O bf16 [40][128], lse fp32 [40], A_S hi and lo bf16 [40][128], Gram fp32 [2][128][128],
+    # right-hand sides fp32 [2][128][128], each rounded up to 256 bytes
+    assert need == 10240 + 256 + 10240 + 10240 + 131072 + 131072
+    assert lib.kvs_value_refit(by(dm), fake, 10, fake, fake, 200, fake, 100, 1e-3, fake, fake,
+                               need - 1, None) == C.KVS_ERR_CAPACITY
+    assert lib.kvs_value_refit(by(dm), None, 0, None, None, 200, None, 100, 1e-3, None, None, 0,
+                               None) == C.KVS_OK
+    # decode step: head dim, page size, block-table width, negative batch, empty call
+    dd = C.dims(1, 2, 2, 128, 0)
+    args = lambda B, page, maxp, d=dd: (by(d), B, 4, fake, fake, fake, fake, fake, fake, fake,
+                                        0.0, page, fake, fake, 8, fake, fake, maxp, fake, 1, None)
+    assert lib.kvs_decode_step(*args(2, 16, 4, C.dims(1, 2, 2, 96, 0))) == C.KVS_ERR_UNSUPPORTED
+    assert lib.kvs_decode_step(*args(2, 0, 4)) == C.KVS_ERR_UNSUPPORTED
+    assert lib.kvs_decode_step(*args(2, 16, 0)) == C.KVS_ERR_SHAPE
+    assert lib.kvs_decode_step(*args(-1, 16, 4)) == C.KVS_ERR_ARG
+    assert lib.kvs_decode_step(*args(0, 16, 4)) == C.KVS_OK
 
 
 def test_workspace_sizes(capi):
