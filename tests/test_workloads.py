@@ -73,3 +73,37 @@ def test_kvzap_mlp_shapes_and_recipe():
     sub = W.generate(wl, layers=[1])
     for k in x:
         assert torch.equal(x[k][1:2], sub[k]), k
+
+
+def test_kvzip_plus_recipe():
+    """c2: W_O std 1/sqrt(D_h), h std sqrt(D_h), per-channel log-uniform [0.5, 4] scales of
+    q, k and v (the channel spreads of the generated rows cover that range)."""
+    wl = W.WORKLOADS["c2"]
+    x = W.generate(wl, layers=[0])
+    w_o, h = x["w_o"].double(), x["h"].double()
+    assert abs(w_o.std().item() * math.sqrt(wl.D_h) - 1.0) < 0.02
+    assert abs(h.std().item() / math.sqrt(wl.D_h) - 1.0) < 0.02
+    for key in ("q", "k_ctx", "v_ctx"):
+        ch = x[key].double()[0].std(dim=1)  # [heads][d]: per-channel std over tokens
+        assert 0.45 < ch.min().item() < 0.6 and 3.4 < ch.max().item() < 4.4, key
+        # log-uniform: the median channel scale sits near sqrt(0.5 * 4)
+        assert abs(math.log(ch.median().item()) - math.log(math.sqrt(2.0))) < 0.2, key
+
+
+def test_future_low_rank_component_is_shared():
+    """c4: q, k and v of a KV head share one rank-8 component of unit variance per element
+    (q through every head of the group); the other KV heads' components are independent."""
+    wl = W.WORKLOADS["c4"].scaled(L=1, T=4096)
+    x = W.generate(wl)
+    q, k, v = (x[n].double()[0] for n in ("q", "k", "v"))
+    assert abs(k.var().item() - 2.0) < 0.1 and abs(v.var().item() - 2.0) < 0.1
+
+    def corr(a, b):
+        a, b = a.flatten() - a.mean(), b.flatten() - b.mean()
+        return float((a * b).sum() / (a.norm() * b.norm()))
+
+    g = wl.g
+    assert abs(corr(k[0], v[0]) - 0.5) < 0.05
+    assert abs(corr(q[g - 1], k[0]) - 0.5) < 0.05        # last head of group 0
+    assert abs(corr(q[g], k[0])) < 0.05                  # first head of group 1
+    assert abs(corr(k[0], k[1])) < 0.05
