@@ -176,3 +176,51 @@ def test_binding_rejects_host_tensors(capi):
     q = torch.zeros(1, 2, 4, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         C.kvs_lse(dm, q, 4, q, 4, None, 0, q, stream=0)
+
+
+def _prototypes():
+    """name -> (return type, [parameter types]) of every function declared in kvs.h."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    out = {}
+    for ret, name, params in re.findall(r"([A-Za-z_][\w ]*?[\s\*]+)(kvs_[a-z_]+)\s*\(([^;{]*?)\)\s*;",
+                                        text):
+        plist = [p.strip() for p in params.split(",") if p.strip() and p.strip() != "void"]
+        # drop the parameter name: what remains is the type
+        out[name] = (ret.strip(), [re.sub(r"\s*\b\w+$", "", p).strip() if not p.endswith("*")
+                                   else p for p in plist])
+    return out
+
+
+def _kind(ctype_or_c):
+    """Coarse kind of a C type string or a ctypes type: ptr, f32, i32, u64, str."""
+    if isinstance(ctype_or_c, str):
+        t = ctype_or_c.replace("const", "").strip()
+        if "char" in t and "*" in t:
+            return "str"
+        if "*" in t:
+            return "ptr"
+        # size_t and uint64_t are the same 64-bit unsigned type on LP64 (and in ctypes)
+        return {"float": "f32", "int32_t": "i32", "int": "i32", "size_t": "u64",
+                "uint64_t": "u64", "kvs_status": "i32"}[t]
+    c = ctype_or_c
+    if c is ctypes.c_char_p:
+        return "str"
+    if c in (ctypes.c_void_p,) or (isinstance(c, type) and issubclass(c, ctypes._Pointer)):
+        return "ptr"
+    if c is ctypes.c_float:
+        return "f32"
+    if c in (ctypes.c_int32, ctypes.c_int):
+        return "i32"
+    if c in (ctypes.c_size_t, ctypes.c_uint64):
+        return "u64"
+    raise AssertionError(c)
+
+
+def test_binding_signatures_match_the_header(capi):
+    protos = _prototypes()
+    assert set(protos) == set(capi._SIGS), set(protos) ^ set(capi._SIGS)
+    for name, (ret, params) in protos.items():
+        args, res = capi._SIGS[name]
+        assert [_kind(p) for p in params] == [_kind(a) for a in args], name
+        assert _kind(ret) == _kind(res), name
