@@ -10,7 +10,9 @@
 //               two 64 KB tiles at d = 128 (four at d = 64), handed out per 64-column box
 //               for the key-side maximum so that its loads lead the MMAs by 1.5 tiles
 //   warp 1      allocates all 512 TMEM columns (two 256-column accumulators) and issues
-//               tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32) into one of them
+//               tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32) into one of them;
+//               with A = queries, a key tile reaching past the unit's causal limit is
+//               multiplied only up to its last visible column (N rounded up to 16)
 //   warps 2-17  epilogue, four groups of four warps (one warp per TMEM lane quarter per
 //               group), 64 accumulator columns each: a thread reads its row's columns
 //               with tcgen05.ld, releases the accumulator, and reduces them while the
