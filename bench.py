@@ -4,11 +4,12 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2] [--impl kvs|reference]
 
 One step = one pass of the whole path over one batch of synthetic input (all layers):
-  c2 (default; Qwen2.5-1.5B-shaped KVzip+): vnorm -> lse -> score_max -> top-k at
-     r = 0.3 / 0.5 / 0.7 -> paged compaction of each
-  c1: lse -> score_max -> top-k 25% + w=16 -> compaction
-  c3: vnorm -> 16 x (lse -> score_max) -> per-layer threshold (25th percentile, calibrated
+  c3 (default; the largest single-GPU workload, Qwen3-8B-shaped chunked KVzip+):
+      vnorm -> 16 x (lse -> score_max) -> per-layer threshold (25th percentile, calibrated
       once before timing) with w=128 -> compaction
+  c1: lse -> score_max -> top-k 25% + w=16 -> compaction
+  c2: (Qwen2.5-1.5B-shaped KVzip+) vnorm -> lse -> score_max -> top-k at
+      r = 0.3 / 0.5 / 0.7 -> paged compaction of each
   c4: lse (causal) -> future mass (w=128) -> top-k 25% / 12.5% + window -> compaction
       (--attn-forward: pass 1 is the attention forward, output + LSE, instead)
   c2 --refit: adds the closed-form value refit (Select+Fit) of the r=0.3 budget's kept keys
@@ -31,7 +32,9 @@ The step is replayed from a CUDA graph captured once (``--no-graph`` launches ev
 call from Python instead); each entry point's timing also replays its own graph.
 
 `--impl reference` times the CPU oracle itself (the only reference implementation: the
-pages ship no code) on the host's CPU cores, each step a bounded sample of the workload.
+pages ship no code) on the host's CPU cores, each step a bounded sample of the workload:
+its `steps` and `ms_per_step` are the samples it ran and their measured wall time, and
+the line's `extrapolation` states how a sample's time converts to a layer's.
 Under torchrun (N > 1) every rank runs its own replica of the workload (weak scaling; the
 path shards by independent problems and needs no data exchange).
 """
@@ -72,7 +75,7 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="c2", choices=["c1", "c2", "c3", "c4", "c5", "c6", "c7"])
+    ap.add_argument("--workload", default="c3", choices=["c1", "c2", "c3", "c4", "c5", "c6", "c7"])
     ap.add_argument("--impl", default="kvs", choices=["kvs", "reference"])
     ap.add_argument("--attn-forward", action="store_true",
                     help="c4: pass 1 is the attention forward (output + LSE) instead of the "
@@ -94,7 +97,7 @@ def parse_args():
     return ap.parse_args()
 
 
-DEFAULT_STEPS = {"c1": 200, "c2": 200, "c3": 5, "c4": 10, "c5": 20, "c6": 10, "c7": 200}
+DEFAULT_STEPS = {"c1": 200, "c2": 200, "c3": 10, "c4": 10, "c5": 20, "c6": 10, "c7": 200}
 
 
 def dist_env():
@@ -106,7 +109,10 @@ def dist_env():
 
 def algorithmic_work(wl, p):
     """Algorithmic flops / bytes of one call of each library entry point of a step,
-    summed over the step (see the roofline section of the design doc)."""
+    summed over the step: 2 d flops per query-key element that the method defines (the
+    visible pairs of the causal rule, every context key for the maximum, the band
+    j >= i + w for the future mass), the Gram form of the value norms, and the bytes an
+    HBM-bound kernel must move at least once."""
     d, L = wl.d, p.L
     out = {}
     if wl.kind in ("kvzip", "kvzip_plus", "kvzip_plus_chunked"):
@@ -194,6 +200,16 @@ def max_over_ranks(value, world, device="cpu"):
 def whole_job_value(units_per_rank, world, ms_step):
     """Units processed by all ranks per second, timed by the slowest rank."""
     return world * units_per_rank / (ms_step / 1e3)
+
+
+def run_config(wl, args, world, layers):
+    """The workload description that both arms print, with the same keys and values, so
+    that their lines name the same configuration."""
+    return {"workload": f"{wl.name}: {wl.title}", "layers": layers, "T": wl.T, "H_q": wl.H_q,
+            "H_kv": wl.H_kv, "d": wl.d, "D_h": wl.D_h, "parallelism": f"replicas x{world}",
+            "pass1": "attention forward (output + LSE)" if args.attn_forward else "LSE-only pass",
+            "value_refit": bool(args.refit),
+            "l2": f"GPU arm: a {L2_FLUSH_BYTES >> 20} MB buffer is written between timed steps"}
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -369,6 +385,7 @@ def run_gpu(args, rank, world, local):
         src = "fallback"
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
     tc_peak = peaks.get("bf16_tflops", 1900.0)
+    tc_sus = peaks.get("bf16_tflops_sustained", 1700.0)
     kernels = {}
     for name, t in stage_ms.items():
         bound, amount, unit = work.get(name, ("hbm", None, "byte"))
@@ -377,21 +394,25 @@ def run_gpu(args, rank, world, local):
             if unit == "flop":
                 ach = amount / (t / 1e3) / 1e12
                 k.update(bound="tensor", achieved=round(ach, 2), unit="TFLOP/s",
-                         peak=tc_peak, frac=round(ach / tc_peak, 4))
+                         peak=tc_peak, frac=round(ach / tc_peak, 4),
+                         frac_sustained=round(ach / tc_sus, 4))
             else:
                 ach = amount / (t / 1e3) / 1e9
                 k.update(bound="hbm", achieved=round(ach, 1), unit="GB/s",
                          peak=hbm_peak, frac=round(ach / hbm_peak, 4))
         kernels[name] = k
-    tot = sum(stage_ms.values())
+    # each stage is replayed on its own; its share is of the graph-replayed step, so the
+    # shares need not add up to one (a stage alone pays its own graph launch and tail)
     for k in kernels.values():
-        k["share"] = round(k["ms"] / tot, 4)
+        k["share"] = round(k["ms"] / ms_step, 4)
     dom = max(kernels, key=lambda n: kernels[n]["ms"])
     dk = kernels[dom]
     roofline = {"kernel": dom, "bound": dk.get("bound"), "achieved": dk.get("achieved"),
                 "peak": dk.get("peak"), "unit": dk.get("unit"), "frac": dk.get("frac"),
                 "peak_source": f"{src} (MEASURED_PEAKS.json burst)" if src == "measured" else
                 "fallback", "traffic": None}
+    if dk.get("bound") == "tensor":
+        roofline.update(peak_sustained=tc_sus, frac_sustained=dk.get("frac_sustained"))
     roofline["traffic"] = read_traffic(wl.name, dom)
 
     # ---------------------------------------------------------------- end to end
@@ -416,16 +437,13 @@ def run_gpu(args, rank, world, local):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": Wm, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{wl.name}: {wl.title}", "layers": p.L, "T": wl.T,
-                   "H_q": wl.H_q, "H_kv": wl.H_kv, "d": wl.d, "D_h": wl.D_h,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "launch": "python calls" if args.no_graph else "CUDA graph of the step",
-                   "pass1": "attention forward (output + LSE)" if args.attn_forward
-                   else "LSE-only pass",
-                   "value_refit": bool(args.refit),
-                   "l2": f"{L2_FLUSH_BYTES >> 20} MB buffer written between timed steps"},
+        "config": run_config(wl, args, world, p.L),
+        "launch": "python calls" if args.no_graph else "CUDA graph of the step",
         "roofline": roofline,
         "kernels": kernels,
+        "kernels_share_basis": (f"stage time (each stage replayed alone) / step time "
+                                f"{ms_step:.4f} ms; the stages sum to "
+                                f"{sum(stage_ms.values()):.4f} ms"),
         "gpu_launches": launches,
         "clocks": clk.summary(t0, t1),
         "e2e": e2e,
@@ -691,12 +709,20 @@ REFERENCE_BUDGET_S = 120.0
 
 
 def run_reference(args, rank, world):
-    """The reference arm: the CPU oracle, timed on the host cores.  The sample of each
-    step shrinks so that warm-up + timed steps take about REFERENCE_BUDGET_S seconds."""
+    """The reference arm: the CPU oracle, timed on the host cores.
+
+    Each step is one bounded sample of the workload (oracle_sample), sized so that the
+    warm-up and timed samples take about REFERENCE_BUDGET_S seconds.  `steps` is the
+    number of samples timed and `ms_per_step` their measured mean wall time, so that
+    steps x ms_per_step is the timed region.  `value` converts a sample's time to the
+    time of one whole layer (the rule is in the line's `extrapolation`) and divides the
+    layer's context tokens by it."""
     if rank != 0:
         return None
     from kv_cache_eviction_lse_gb300 import workloads as W
     wl = W.WORKLOADS[args.workload]
+    if args.layers:
+        wl = wl.scaled(L=min(args.layers, wl.L))
     K = args.steps or 3
     Wm = max(3, args.warmup)
     x = host_layer0(wl)
@@ -708,23 +734,28 @@ def run_reference(args, rank, world):
     frac = max(frac / 64, min(frac, frac / 8 * per_step / max(probe, 1e-6)))
     for _ in range(Wm):
         oracle_sample(wl, x, frac)
-    times, wall, desc = [], [], ""
+    layer_s, wall, desc, tokens = [], [], "", wl.T
     for _ in range(K):
         t = time.perf_counter()
         dt, tokens, desc = oracle_sample(wl, x, frac)
         wall.append(time.perf_counter() - t)
-        times.append(dt)
-    ms = 1e3 * statistics.mean(times)
-    value = tokens / (ms / 1e3)
+        layer_s.append(dt)
+    ms_sample = 1e3 * statistics.mean(wall)
+    ms_layer = 1e3 * statistics.mean(layer_s)
+    value = tokens / (ms_layer / 1e3)
     cb = {"value": round(value, 2), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-          "sample": desc + f"; {statistics.mean(wall):.2f} s of CPU work per step"}
+          "sample": desc + f"; {ms_sample / 1e3:.2f} s of CPU work per step"}
     return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
-            "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": round(ms, 3),
+            "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": round(ms_sample, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": f"{wl.name}: {wl.title}", "layers": wl.L, "T": wl.T,
-                       "H_q": wl.H_q, "H_kv": wl.H_kv, "d": wl.d, "D_h": wl.D_h,
-                       "parallelism": "host cores (oracle)"},
+            "config": run_config(wl, args, world, wl.L),
+            "extrapolation": {
+                "measured_ms_per_step": round(ms_sample, 3),
+                "layer_equivalent_ms": round(ms_layer, 3),
+                "tokens_per_layer": tokens,
+                "rule": ("value = tokens_per_layer / layer_equivalent_ms; each step times one "
+                         "sample and scales its parts to a whole layer: " + desc)},
             "cpu_baseline": cb,
             "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}

@@ -210,9 +210,11 @@ kvs_status kvs_vnorm(const kvs_dims* dims, const kvs_bf16* v, int32_t T, const k
  * 8 MiB, which every GPU that loads the library keeps until the process exits.  Layers
  * are processed one after another on `stream`, so the limit is per layer:
  * H_q * d * d * 4 bytes <= 8 MiB (H_q <= 128 at d = 128); larger shapes return
- * KVS_ERR_CAPACITY.  The first call on each device looks up the array's device
- * address (once per device); make that first call before capturing a stream into a
- * graph.  All calls share the one array: calls that overlap on the GPU (other streams,
+ * KVS_ERR_CAPACITY.  The first call in each CUDA context looks up the array's device
+ * address and caches it with the context's id: once per device, and once more after
+ * the device's context is re-created (cudaDeviceReset), since the old address belongs
+ * to the destroyed context.  Make each such first call before capturing a stream into
+ * a graph.  All calls share the one array: calls that overlap on the GPU (other streams,
  * other host threads) race on it and must be serialised by the caller.  Nothing in it
  * needs to start at zero: every byte a call reads is written earlier by that call.
  *   v [L][H_kv][T][d] bf16,  w_o [L][D_h][H_q*d] bf16,  vnorm [L][H_q][T] fp32 output.

@@ -13,6 +13,9 @@
 //         mode: one M=128 N=256 MMA chain per query head), then v_i . u_i per token
 #include <mutex>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "attn.cuh"
 #include "common.cuh"
 #include "gram.cuh"
@@ -65,22 +68,65 @@ constexpr int kMaxDevices = 64;
 
 size_t vnorm_noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
 
-// Device address of the built-in scratch on the current device, looked up once per
-// device (the first call on a device does the lookup, so it must not be made while a
-// stream is being captured).
+// The driver's current-context calls, fetched through the runtime (the library links no
+// driver library directly).
+struct CtxFns {
+  PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  PFN_cuCtxGetId_v12000 get_id = nullptr;
+};
+
+static const CtxFns& ctx_fns() {
+  static CtxFns f = [] {
+    CtxFns r;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      r.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      r.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    return r;
+  }();
+  return f;
+}
+
+// Unique id of the calling thread's current CUDA context (0 when there is none yet).
+// Context ids are never reused within a process, unlike context handles.
+static cudaError_t current_ctx_id(unsigned long long* id) {
+  const CtxFns& f = ctx_fns();
+  if (!f.get_current || !f.get_id) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (f.get_current(&ctx) != CUDA_SUCCESS) return cudaErrorUnknown;
+  *id = 0;
+  if (ctx && f.get_id(ctx, id) != CUDA_SUCCESS) return cudaErrorUnknown;
+  return cudaSuccess;
+}
+
+// Device address of the built-in scratch in the current context.  It is looked up on
+// the first call in each context and cached with that context's id; a call in a new
+// context (another device, or the same device after cudaDeviceReset re-created its
+// context) looks it up again.  A lookup must not happen while a stream is being captured.
 static cudaError_t vnorm_noalloc_scratch(void** out) {
   static std::mutex mu;
   static void* addr[kMaxDevices] = {};
+  static unsigned long long ctx_of[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  unsigned long long id = 0;
+  e = current_ctx_id(&id);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  if (!addr[dev] || id == 0 || ctx_of[dev] != id) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_vnorm_scratch);
+    e = cudaGetSymbolAddress(&p, g_vnorm_scratch);  // makes the device's context current
+    if (e != cudaSuccess) return e;
+    e = current_ctx_id(&id);
     if (e != cudaSuccess) return e;
     addr[dev] = p;
+    ctx_of[dev] = id;
   }
   *out = addr[dev];
   return cudaSuccess;

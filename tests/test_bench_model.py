@@ -65,3 +65,23 @@ def test_units_are_context_tokens_per_layer():
     wl = W.WORKLOADS["c2"]
     assert bench.units_per_step(wl, _p(wl)) == wl.T * wl.L
     assert bench.whole_job_value(1000, 4, 2.0) == pytest.approx(4 * 1000 / 2e-3)
+
+
+def test_reference_arm_reports_what_it_timed():
+    """The reference arm's steps x ms_per_step is time it really spent (it fits inside
+    the wall time of the call), and its config is the one the GPU arm prints."""
+    import time
+    args = types.SimpleNamespace(workload="c1", layers=None, steps=2, warmup=3,
+                                 attn_forward=False, refit=False)
+    t0 = time.perf_counter()
+    res = bench.run_reference(args, 0, 1)
+    wall_ms = 1e3 * (time.perf_counter() - t0)
+    assert res["steps"] == 2 and res["warmup"] == 3
+    assert res["steps"] * res["ms_per_step"] <= wall_ms
+    assert res["extrapolation"]["measured_ms_per_step"] == res["ms_per_step"]
+    wl = W.WORKLOADS["c1"]
+    ex = res["extrapolation"]
+    assert res["value"] == pytest.approx(ex["tokens_per_layer"] / (ex["layer_equivalent_ms"] / 1e3),
+                                         rel=1e-3)
+    assert res["config"] == bench.run_config(wl, args, 1, wl.L)
+    assert res["cpu_baseline"]["value"] == res["value"]

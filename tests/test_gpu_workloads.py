@@ -1,7 +1,8 @@
 """Parity of the whole path on the five workloads at their full sizes, in the launch
 configuration the benchmark times (every layer in one call).  The oracle checks sampled
-outputs it can afford: all of c1, layers {0, 27} of c2, layer 0 / KV head 0 of c3 and
-c4, layer 0 of c5; compaction is checked bit-exactly given the kernel's mask."""
+outputs it can afford: all of c1, layers {0, 27} of c2, (layer 0, KV head 0) and (last
+layer, last KV head) of c3 and c4, layer 0 of c5; compaction is checked bit-exactly
+given the kernel's mask."""
 import gc
 
 import numpy as np
@@ -94,40 +95,81 @@ def test_c2_full(mods):
                 _check_pages(pg, l, h, x["k_ctx"][l, h], x["v_ctx"][l, h], m[l, h].cpu().numpy())
 
 
-def test_c3_full_layer0_head0(mods):
+def _layer_tau(score_l, T, w, qtl):
+    """Reading of the c3 threshold: the lower nearest-rank quantile qtl of the layer's
+    non-window scores over all its KV heads, sorted[floor(qtl (N - 1))], taken from the
+    kernel's fp32 scores (a workload parameter, then used by both sides)."""
+    flat = score_l[:, : T - w].flatten()
+    k = int(np.floor(qtl * (flat.numel() - 1))) + 1
+    return float(torch.kthvalue(flat.float().cpu(), k).values)
+
+
+def _c3_oracle_row(x, wl, l, hk, keys=None):
+    """The oracle's chunked KVzip+ log score of KV head hk of layer l, on the context keys
+    `keys` (all when None).  Each chunk's LSE runs over every key its queries see (the
+    full context and the chunk's tail); the score of a key needs only its own column of
+    the attention rows, so the context passed to the score holds just the sampled keys
+    (every context key is visible to every scoring query, so their visibility and the
+    tail's causal offsets are unchanged)."""
+    g, d = wl.g, wl.d
+    hs = slice(hk * g, (hk + 1) * g)
+    sl = slice(l, l + 1)
+    kc = f64(x["k_ctx"][sl, hk:hk + 1])
+    ks = kc if keys is None else kc[:, :, keys]
+    v = f64(x["v_ctx"][sl, hk:hk + 1])
+    vn = O.value_norm(v if keys is None else v[:, :, keys],
+                      f64(x["w_o"][sl, :, hk * g * d:(hk + 1) * g * d]), g)
+    best = None
+    for c in range(wl.n_chunks):
+        q = f64(x["q"][c][sl, hs])
+        tail = f64(x["k_tail"][c][sl, hk:hk + 1])
+        lse_c = O.lse(q, kc, tail)
+        s = O.kvzip_score(q, ks, tail, lse_=lse_c, vnorm=vn, h=f64(x["h"][c][sl]), log=False)
+        best = s if best is None else np.maximum(best, s)
+    with np.errstate(divide="ignore"):
+        return vn, np.log(best)
+
+
+def test_c3_full_corners(mods):
+    """c3 at full size: (layer 0, KV head 0) on every context key, and the far corner
+    (last layer, last KV head) on its first and last 2048 keys, against the oracle;
+    the per-layer threshold at the 25th percentile of the layer's non-window scores
+    over all 8 KV heads, then the masks and pages of both rows."""
     pipeline, W = mods
     wl = W.WORKLOADS["c3"]
     x = W.generate(wl, device="cuda")
     p = pipeline.make_pipeline(wl, x)
     p.score_step()
     torch.cuda.synchronize()
-    g = wl.g
-    hs = slice(0, g)
-    d = wl.d
-    qs = [f64(x["q"][c][0:1, hs]) for c in range(wl.n_chunks)]
-    tails = [f64(x["k_tail"][c][0:1, 0:1]) for c in range(wl.n_chunks)]
-    hh = [f64(x["h"][c][0:1]) for c in range(wl.n_chunks)]
-    kc = f64(x["k_ctx"][0:1, 0:1])
-    vn = O.value_norm(f64(x["v_ctx"][0:1, 0:1]), f64(x["w_o"][0:1, :, 0:g * d]), g)
-    assert_close_rel(p.vnorm[0:1, hs].cpu().numpy(), vn, 1e-4, "c3 vnorm")
-    s = O.kvzip_score_chunked(qs, kc, tails, vnorm=vn, h_chunks=hh)
-    got = p.score[0:1, 0:1].cpu().numpy()
-    assert_close_abs(got, s, LOG_SCORE_ATOL, "c3 log score (layer 0, head 0)")
-    # threshold at the 25th percentile of the non-window scores (of this sampled row)
-    tau0 = O.quantile_lower(s[..., : wl.T - wl.w], wl.tau_quantile)
-    taus = [tau0] + [float(torch.quantile(p.score[l, :, : wl.T - wl.w].flatten()[:16_000_000], 0.25))
-                     for l in range(1, wl.L)]
-    p.tau = taus
+    g, T, w = wl.g, wl.T, wl.w
+    p.tau = [_layer_tau(p.score[l], T, w, wl.tau_quantile) for l in range(wl.L)]
     p.prune_step()
     torch.cuda.synchronize()
-    m_ref, _ = O.prune_threshold(s, tau0, wl.w)
-    assert_masks_match_near(p.mask[0:1, 0:1].cpu().numpy(), m_ref, s, np.full((1, 1), tau0),
-                            MASK_BAND, "c3 mask", log_domain=True)
-    _check_pages(p.pages, 0, 0, x["k_ctx"][0, 0].cpu(), x["v_ctx"][0, 0].cpu(),
-                 p.mask[0, 0].cpu().numpy())
+    keys_far = np.r_[0:2048, T - 2048:T]
+    for l, hk, keys in ((0, 0, None), (wl.L - 1, wl.H_kv - 1, keys_far)):
+        vn, s = _c3_oracle_row(x, wl, l, hk, keys)
+        cols = slice(None) if keys is None else keys
+        vg = p.vnorm[l:l + 1, hk * g:(hk + 1) * g].cpu().numpy()[..., cols]
+        assert_close_rel(vg, vn, 1e-4, f"c3 vnorm (layer {l}, head {hk})")
+        got = p.score[l:l + 1, hk:hk + 1].cpu().numpy()[..., cols]
+        assert_close_abs(got, s, LOG_SCORE_ATOL, f"c3 log score (layer {l}, head {hk})")
+        tau = p.tau[l]
+        m_ref, _ = O.prune_threshold(s, tau, 0)
+        pos = np.arange(T)[cols]
+        m_ref[..., pos >= T - w] = 1  # the window (positions of the sampled keys)
+        mg = p.mask[l:l + 1, hk:hk + 1].cpu().numpy()
+        assert_masks_match_near(mg[..., cols], m_ref, s, np.full((1, 1), tau), MASK_BAND,
+                                f"c3 mask (layer {l}, head {hk})", log_domain=True)
+        # the whole row's mask is the threshold rule on the kernel's own fp32 scores
+        m_same, _ = O.prune_threshold(p.score[l:l + 1, hk:hk + 1].cpu().numpy().astype(np.float64),
+                                      np.float32(tau), w)
+        assert np.array_equal(mg, m_same)
+        _check_pages(p.pages, l, hk, x["k_ctx"][l, hk].cpu(), x["v_ctx"][l, hk].cpu(), mg[0, 0])
 
 
-def test_c4_full_layer0_head0(mods):
+def test_c4_full_corners(mods):
+    """c4 at full size: LSE, future mass, top-k masks and pages of (layer 0, KV head 0)
+    and of the far corner (last layer, last KV head) against the oracle."""
     pipeline, W = mods
     wl = W.WORKLOADS["c4"]
     x = W.generate(wl, device="cuda")
@@ -135,19 +177,23 @@ def test_c4_full_layer0_head0(mods):
     p.step()
     torch.cuda.synchronize()
     g = wl.g
-    q = f64(x["q"][0:1, 0:g])
-    k = f64(x["k"][0:1, 0:1])
-    lse = O.lse(q, k, None)
-    assert_close_abs(p.lse[0:1, 0:g].cpu().numpy(), lse, LSE_ATOL, "c4 lse")
-    f = O.future_attention_mass(q, k, wl.w, lse_=lse)
-    assert_close_rel(p.score[0:1, 0:1].cpu().numpy(), f, SCORE_RTOL, "c4 future mass")
-    for r, m, kp, pg in zip(p.ratios, p.masks, p.keeps, p.pages):
-        kk = wl.topk_budget(r)
-        m_ref, k_ref = O.prune_topk(f, kk, wl.w)
-        assert int(kp[0, 0].item()) == int(k_ref[0, 0]) == kk + wl.w
-        assert_masks_match_near(m[0:1, 0:1].cpu().numpy(), m_ref, f, kth_value(f, kk, wl.w),
-                                MASK_BAND, f"c4 mask r={r}", log_domain=False)
-        _check_pages(pg, 0, 0, x["k"][0, 0].cpu(), x["v"][0, 0].cpu(), m[0, 0].cpu().numpy())
+    for l, hk in ((0, 0), (wl.L - 1, wl.H_kv - 1)):
+        sl, hs = slice(l, l + 1), slice(hk * g, (hk + 1) * g)
+        q = f64(x["q"][sl, hs])
+        k = f64(x["k"][sl, hk:hk + 1])
+        lse = O.lse(q, k, None)
+        assert_close_abs(p.lse[sl, hs].cpu().numpy(), lse, LSE_ATOL, f"c4 lse (layer {l}, head {hk})")
+        f = O.future_attention_mass(q, k, wl.w, lse_=lse)
+        assert_close_rel(p.score[sl, hk:hk + 1].cpu().numpy(), f, SCORE_RTOL,
+                         f"c4 future mass (layer {l}, head {hk})")
+        for r, m, kp, pg in zip(p.ratios, p.masks, p.keeps, p.pages):
+            kk = wl.topk_budget(r)
+            m_ref, k_ref = O.prune_topk(f, kk, wl.w)
+            assert int(kp[l, hk].item()) == int(k_ref[0, 0]) == kk + wl.w
+            assert_masks_match_near(m[sl, hk:hk + 1].cpu().numpy(), m_ref, f,
+                                    kth_value(f, kk, wl.w), MASK_BAND,
+                                    f"c4 mask r={r} (layer {l}, head {hk})", log_domain=False)
+            _check_pages(pg, l, hk, x["k"][l, hk].cpu(), x["v"][l, hk].cpu(), m[l, hk].cpu().numpy())
 
 
 def test_c5_full_layer0(mods):

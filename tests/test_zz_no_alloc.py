@@ -37,6 +37,28 @@ def _inputs(L, Hkv, Hq, d, T, Dh, seed):
 
 def test_vnorm_noalloc_matches_workspace_version_twice(C):
     shapes = [(3, 2, 6, 128, 300, 192, 1), (2, 4, 32, 128, 1000, 512, 2)]
+    _compare(C, shapes)
+
+
+def test_vnorm_noalloc_at_the_capacity_limit_and_small_shapes(C):
+    """One layer that fills the built-in scratch exactly (H_q d d 4 bytes = 8 MiB at
+    H_q = 128, d = 128), a head dimension of 64, and a single layer."""
+    shapes = [(1, 8, 128, 128, 260, 256, 3), (2, 2, 8, 64, 777, 320, 4), (1, 1, 4, 64, 129, 64, 5)]
+    assert 128 * 128 * 128 * 4 == 8 << 20  # the documented size of the built-in scratch
+    _compare(C, shapes)
+
+
+def test_vnorm_noalloc_empty_context_writes_nothing(C):
+    """T = 0: the call succeeds and leaves the output as it was."""
+    dm = C.dims(2, 8, 2, 128, 256)
+    t = torch.empty(16, dtype=torch.bfloat16, device="cuda")
+    out = torch.full((64,), 7.0, device="cuda")
+    C.kvs_vnorm_noalloc(dm, t, 0, t, out)
+    torch.cuda.synchronize()
+    assert (out.cpu() == 7.0).all()
+
+
+def _compare(C, shapes):
     for L, Hkv, Hq, d, T, Dh, seed in shapes:
         v, w_o = _inputs(L, Hkv, Hq, d, T, Dh, seed)
         dm = C.dims(L, Hq, Hkv, d, Dh)
