@@ -471,6 +471,27 @@ def compression_factor(ratio_removed):
 
 def quantile_lower(values, qtl):
     """Lower nearest-rank quantile sorted[floor(qtl * (N - 1))] (reading for the
-    threshold set at the 25th percentile of the scores of a layer)."""
-    s = np.sort(np.asarray(values, dtype=np.float64).ravel())
+    threshold set at the 25th percentile of the scores of a layer).  NaN ranks below
+    every number, as in the top-k ranking."""
+    v = np.asarray(values, dtype=np.float64).ravel()
+    nan = np.isnan(v)
+    s = np.concatenate([v[nan], np.sort(v[~nan])])
     return float(s[int(math.floor(qtl * (s.size - 1)))])
+
+
+def prune_quantile(score, qtl, w):
+    """Threshold pruning with tau set per layer at a quantile of the layer's scores
+    [KVzip Methods: ratio-based threshold; reading: tau_l is the lower nearest-rank
+    quantile ``qtl`` of the non-window scores of all KV heads of layer l], then the
+    KVzap threshold rule with the window [KVzap, thresholding; Algorithm 1].
+    score [L][H_kv][T] -> (mask, keep, tau [L]); with no candidate (w >= T) tau is +inf
+    and only the window is kept."""
+    score = np.asarray(score, dtype=np.float64)
+    L, H, T = score.shape
+    wn = min(max(w, 0), T)
+    tau = np.full(L, np.inf)
+    for l in range(L):
+        if T - wn > 0:
+            tau[l] = quantile_lower(score[l, :, : T - wn], qtl)
+    masks, keeps = zip(*[prune_threshold(score[l], tau[l], w) for l in range(L)])
+    return np.stack(masks), np.stack(keeps), tau

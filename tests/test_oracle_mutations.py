@@ -47,6 +47,12 @@ MUTATIONS = [
     ("topk ties to later tokens", "return np.lexsort((pos, key, nan))", "return np.lexsort((-pos, key, nan))"),
     ("topk nan ranks high", "key = np.where(nan, 0.0, -row)", "key = np.where(nan, -np.inf, -row)\n    nan = nan & False"),
     ("topk ignores window", "mask[r, T - wn:] = 1", "mask[r, T - wn:] = 0"),
+    ("quantile upper rank", "s[int(math.floor(qtl * (s.size - 1)))]", "s[int(math.ceil(qtl * (s.size - 1)))]"),
+    ("quantile nan ranks high", "s = np.concatenate([v[nan], np.sort(v[~nan])])", "s = np.sort(v)"),
+    ("quantile over the window too", "tau[l] = quantile_lower(score[l, :, : T - wn], qtl)",
+     "tau[l] = quantile_lower(score[l], qtl)"),
+    ("quantile per head 0 only", "tau[l] = quantile_lower(score[l, :, : T - wn], qtl)",
+     "tau[l] = quantile_lower(score[l, 0, : T - wn], qtl)"),
     ("compaction descending", "idx = np.nonzero(mask[l, hh])[0]", "idx = np.nonzero(mask[l, hh])[0][::-1]"),
     ("compaction head-major pages", "block_table[l, hh, p] = first + p", "block_table[l, hh, p] = first + p + 1"),
     ("kv bytes without K and V", "return 2 * L * T * H_kv * d * bytes_per_elem",

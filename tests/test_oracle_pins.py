@@ -667,3 +667,48 @@ def test_quantile_lower_nearest_rank():
     assert O.quantile_lower([3, 1, 2, 4], 0.25) == 1
     assert O.quantile_lower([3, 1, 2, 4], 0.5) == 2
     assert O.quantile_lower(np.arange(101), 0.25) == 25
+    assert O.quantile_lower([5.0, 0.0, 1.0], 0.0) == 0.0 and O.quantile_lower([5.0, 0.0, 1.0], 1.0) == 5.0
+    # NaN below every number: [nan, nan, -1, 2, 7] by rank
+    v = [2.0, np.nan, 7.0, -1.0, np.nan]
+    assert np.isnan(O.quantile_lower(v, 0.25))        # rank floor(0.25 * 4) = 1
+    assert O.quantile_lower(v, 0.5) == -1.0           # rank 2
+    assert O.quantile_lower(v, 0.8) == 2.0            # rank 3
+
+
+def test_quantile_rank_brute_force():
+    """The nearest-rank property by counting: with r = floor(q (N - 1)), at most r values
+    lie below tau and more than r lie at or below it; tau is one of the values."""
+    rng = np.random.default_rng(7)
+    for N, levels in [(1, None), (10, None), (999, None), (1000, 4), (257, 2)]:
+        v = rng.normal(size=N)
+        if levels:
+            v = np.round(v * levels) / levels
+        for q in (0.0, 0.1, 0.25, 0.5, 0.999, 1.0):
+            tau = O.quantile_lower(v, q)
+            r = int(math.floor(q * (N - 1)))
+            assert (v < tau).sum() <= r < (v <= tau).sum()
+            assert tau in v
+
+
+def test_prune_quantile_per_layer():
+    """Per layer: tau from that layer's non-window scores of every head (window scores,
+    however small, never move it); the mask is the threshold rule with that tau; the
+    keep count is at least (1 - q) of the candidates plus the window."""
+    rng = np.random.default_rng(3)
+    L, H, T, w, q = 3, 4, 50, 7, 0.25
+    s = rng.normal(size=(L, H, T))
+    s[1] += 10.0                      # a shifted layer gets its own tau
+    s[:, :, T - w:] = -100.0          # window scores are excluded from the quantile
+    m, k, tau = O.prune_quantile(s, q, w)
+    for l in range(L):
+        cand = s[l, :, : T - w].ravel()
+        assert tau[l] == np.sort(cand)[int(math.floor(q * (cand.size - 1)))]
+        m_ref, k_ref = O.prune_threshold(s[l], tau[l], w)
+        assert np.array_equal(m[l], m_ref) and np.array_equal(k[l], k_ref)
+        assert k[l].sum() >= math.ceil((1 - q) * cand.size) + H * w
+    assert tau[1] > tau[0] + 5 and tau[1] > tau[2] + 5
+    # everything in the window: no candidate, tau = +inf, only the window kept
+    m, k, tau = O.prune_quantile(s, q, T)
+    assert np.isinf(tau).all() and (k == T).all()
+    m, k, tau = O.prune_quantile(s, q, 0)
+    assert (k.sum(axis=1) >= math.ceil((1 - q) * H * T)).all()
