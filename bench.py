@@ -5,8 +5,8 @@
 
 One step = one pass of the whole path over one batch of synthetic input (all layers):
   c3 (default; the largest single-GPU workload, Qwen3-8B-shaped chunked KVzip+):
-      vnorm -> 16 x (lse -> score_max) -> per-layer threshold (25th percentile, calibrated
-      once before timing) with w=128 -> compaction
+      vnorm -> 16 x (lse -> score_max) -> threshold at each layer's 25th score percentile
+      (selected on the GPU in every step) with w=128 -> compaction
   c1: lse -> score_max -> top-k 25% + w=16 -> compaction
   c2: (Qwen2.5-1.5B-shaped KVzip+) vnorm -> lse -> score_max -> top-k at
       r = 0.3 / 0.5 / 0.7 -> paged compaction of each
@@ -282,15 +282,6 @@ def build_pipeline(wl, device, attn_forward=False, refit=False):
     if refit:
         kw["refit"] = True
     p = pipeline.make_pipeline(wl, x, **kw)
-    if wl.kind == "kvzip_plus_chunked":
-        # calibrate the per-layer threshold once (25th percentile of the non-window
-        # scores of each layer), then keep it fixed for the timed steps
-        import torch
-        p.score_step()
-        T = wl.T - wl.w
-        p.tau = [float(torch.kthvalue(p.score[l, :, :T].flatten().float(),
-                                      max(1, int(wl.tau_quantile * (wl.H_kv * T - 1)) + 1)).values)
-                 for l in range(p.L)]
     return x, p
 
 
@@ -371,10 +362,11 @@ def run_gpu(args, rank, world, local):
         stage_ms[name] = sum(a.elapsed_time(b) for a, b in e) / reps
     step_fn()  # leave consistent outputs
     torch.cuda.synchronize()
-    if "kvs_compact_paged" in stage_ms:
-        work["kvs_compact_paged"] = ("hbm", compaction_bytes(p, wl), "byte")
-    if "kvs_prune_mask" in stage_ms:
-        work["kvs_prune_mask"] = ("hbm", prune_bytes(p, wl), "byte")
+    for name in stage_ms:
+        if name.startswith("kvs_compact_paged"):
+            work[name] = ("hbm", compaction_bytes(p, wl), "byte")
+        if name.startswith("kvs_prune"):
+            work[name] = ("hbm", prune_bytes(p, wl), "byte")
 
     peaks = {}
     try:
@@ -424,10 +416,7 @@ def run_gpu(args, rank, world, local):
             kw["refit"] = True
 
         def make_group(xg, l0, l1):
-            pg = PL.make_pipeline(wl, xg, **kw)
-            if getattr(p, "tau", None) is not None and isinstance(p.tau, list):
-                pg.tau = p.tau[l0:l1]
-            return pg
+            return PL.make_pipeline(wl, xg, **kw)
         groups = 1 if wl.kind == "decode" else min(args.e2e_groups, p.L)
         e2e = run_e2e(wl, x, p, dev, K=min(K, 20), units=world * units_per_step(wl, p), world=world,
                       flush=flush, graph=not args.no_graph, groups=groups, make_group=make_group,
@@ -622,8 +611,7 @@ def oracle_sample(wl, x, frac=1.0):
                 m, _ = O.prune_topk(s, wl.topk_budget(r), wl.w)
                 O.compact_paged(i16(x["k_ctx"][:, 0:1]), i16(x["v_ctx"][:, 0:1]), m, wl.page_size)
         else:
-            tau = O.quantile_lower(s[..., : wl.T - wl.w], wl.tau_quantile)
-            m, _ = O.prune_threshold(s, tau, wl.w)
+            m, _, _ = O.prune_quantile(s, wl.tau_quantile, wl.w)
             O.compact_paged(i16(x["k_ctx"][:, 0:1]), i16(x["v_ctx"][:, 0:1]), m, wl.page_size)
         t3 = tick()
         chunks = wl.n_chunks if chunked else 1

@@ -284,6 +284,35 @@ kvs_status kvs_prune_mask(const kvs_dims* dims, const float* score, int32_t T, i
                           void* stream);
 
 /* ---------------------------------------------------------------------------------
+ * kvs_prune_quantile -- threshold pruning with a per-layer threshold set at a quantile
+ * of the layer's own scores [KVzip Methods: tau chosen so that a ratio of the scores
+ * falls below it; KVzap thresholding with a sliding window; Algorithm 1].  Per layer l:
+ *   tau[l] = the lower nearest-rank quantile q of the N = H_kv (T - w) non-window
+ *            scores of all KV heads of layer l: the element of rank floor(q (N - 1))
+ *            (0-based, ascending, computed in double from the fp32 q), NaN ranked
+ *            below every number; +inf when N = 0
+ *   keep t of head h  <=>  score[l][h][t] >= tau[l]  or  t >= T - w
+ *   score [L][H_kv][T] fp32;  tau [L] fp32 output (device);  mask [L][H_kv][T] uint8
+ *   output;  keep [L][H_kv] int32 output.  0 <= q <= 1, else KVS_ERR_ARG.
+ * ------------------------------------------------------------------------------- */
+kvs_status kvs_prune_quantile(const kvs_dims* dims, const float* score, int32_t T, float q,
+                              int32_t w, float* tau, uint8_t* mask, int32_t* keep, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * kvs_prune_topk_multi -- the KVS_TOPK rule of kvs_prune_mask for several budgets over
+ * the same scores in one launch [KVpop 3. Method: per-head top-k within a fixed
+ * budget; KVzap 3.1: KVzip at fixed keep ratios].  For budget b the result equals
+ * kvs_prune_mask(..., KVS_TOPK, k = k[b], w, ...) written at mask + b L H_kv T and
+ * keep + b L H_kv.
+ *   score [L][H_kv][T] fp32;  k [n_budgets] int32 in HOST memory, each >= 0;
+ *   masks [n_budgets][L][H_kv][T] uint8 output;  keeps [n_budgets][L][H_kv] int32 output.
+ * 1 <= n_budgets <= 8 (else KVS_ERR_UNSUPPORTED).
+ * ------------------------------------------------------------------------------- */
+kvs_status kvs_prune_topk_multi(const kvs_dims* dims, const float* score, int32_t T,
+                                int32_t n_budgets, const int32_t* k, int32_t w, uint8_t* masks,
+                                int32_t* keeps, void* stream);
+
+/* ---------------------------------------------------------------------------------
  * kvs_value_refit -- closed-form value refit on the kept keys [KVSculpt summary,
  * 2. Method: with the keys fixed, the attention weights they induce are fixed and the
  * values follow by ridge least squares; Select+Fit = attention-score selection plus
@@ -378,6 +407,26 @@ kvs_status kvs_compact_paged(const kvs_dims* dims, const kvs_bf16* k, const kvs_
                              kvs_bf16* k_pages, kvs_bf16* v_pages, int32_t capacity_pages,
                              int32_t* block_table, int32_t max_pages, int32_t* seq_lens,
                              int32_t* needed_pages, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * kvs_compact_paged_multi -- kvs_compact_paged for n_masks masks over the same K/V
+ * (for instance one per top-k budget) in one set of launches, into one shared page
+ * pool.  The result is that of kvs_compact_paged over n_masks L "layers" whose K/V
+ * rows repeat every L layers: rows are taken mask-major, then layer, then head, so the
+ * pages of mask b follow all pages of masks 0 .. b-1.
+ *   masks        [n_masks][L][H_kv][T] uint8
+ *   block_table  [n_masks][L][H_kv][max_pages] int32;  seq_lens [n_masks][L][H_kv] int32
+ *   needed_pages [1] int32: total pages of all masks
+ *   ws           scratch of kvs_compact_multi_workspace_size(dims, T, n_masks) bytes
+ * Other arguments, the capacity rule and the errors as kvs_compact_paged; n_masks >= 1.
+ * ------------------------------------------------------------------------------- */
+size_t kvs_compact_multi_workspace_size(const kvs_dims* dims, int32_t T, int32_t n_masks);
+kvs_status kvs_compact_paged_multi(const kvs_dims* dims, const kvs_bf16* k, const kvs_bf16* v,
+                                   int32_t T, int32_t n_masks, const uint8_t* masks,
+                                   int32_t page_size, kvs_bf16* k_pages, kvs_bf16* v_pages,
+                                   int32_t capacity_pages, int32_t* block_table, int32_t max_pages,
+                                   int32_t* seq_lens, int32_t* needed_pages, void* ws,
+                                   size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus
 }

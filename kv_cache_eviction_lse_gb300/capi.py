@@ -79,6 +79,11 @@ _SIGS = {
     "kvs_compact_workspace_size": ([_D, _I], _S),
     "kvs_compact_paged": ([_D, _P, _P, _I, _P, _I, _P, _P, _I, _P, _I, _P, _P, _P, _S, _P],
                           ctypes.c_int),
+    "kvs_prune_quantile": ([_D, _P, _I, _F, _I, _P, _P, _P, _P], ctypes.c_int),
+    "kvs_prune_topk_multi": ([_D, _P, _I, _I, _P, _I, _P, _P, _P], ctypes.c_int),
+    "kvs_compact_multi_workspace_size": ([_D, _I, _I], _S),
+    "kvs_compact_paged_multi": ([_D, _P, _P, _I, _I, _P, _I, _P, _P, _I, _P, _I, _P, _P, _P, _S,
+                                 _P], ctypes.c_int),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -216,6 +221,32 @@ def kvs_surrogate_mlp(dm, h, T, D_mid, W1, b1, W2, b2, score, tau=0.0, w=0, mask
 def kvs_prune_mask(dm, score, T, mode, tau, k, w, mask, keep, stream=None):
     _check(_lib.kvs_prune_mask(_d(dm), _ptr(score), T, mode, float(tau), k, w, _ptr(mask),
                                _ptr(keep), _stream(stream)))
+
+
+def kvs_prune_quantile(dm, score, T, q, w, tau, mask, keep, stream=None):
+    _check(_lib.kvs_prune_quantile(_d(dm), _ptr(score), T, float(q), w, _ptr(tau), _ptr(mask),
+                                   _ptr(keep), _stream(stream)))
+
+
+def kvs_prune_topk_multi(dm, score, T, ks, w, masks, keeps, stream=None):
+    """ks: a sequence of budgets (marshalled into a host int32 array)."""
+    arr = (ctypes.c_int32 * max(1, len(ks)))(*[int(k) for k in ks])
+    _check(_lib.kvs_prune_topk_multi(_d(dm), _ptr(score), T, len(ks), ctypes.cast(arr, _P), w,
+                                     _ptr(masks),
+                                     _ptr(keeps), _stream(stream)))
+
+
+def kvs_compact_multi_workspace_size(dm, T, n_masks) -> int:
+    return _lib.kvs_compact_multi_workspace_size(_d(dm), T, n_masks)
+
+
+def kvs_compact_paged_multi(dm, k, v, T, n_masks, masks, page_size, k_pages, v_pages,
+                            capacity_pages, block_table, max_pages, seq_lens, needed_pages, ws,
+                            ws_bytes, stream=None):
+    _check(_lib.kvs_compact_paged_multi(_d(dm), _ptr(k), _ptr(v), T, n_masks, _ptr(masks),
+                                        page_size, _ptr(k_pages), _ptr(v_pages), capacity_pages,
+                                        _ptr(block_table), max_pages, _ptr(seq_lens),
+                                        _ptr(needed_pages), _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def kvs_compact_workspace_size(dm, T) -> int:

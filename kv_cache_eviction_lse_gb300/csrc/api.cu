@@ -520,9 +520,77 @@ kvs_status kvs_prune_mask(const kvs_dims* dims, const float* score, int32_t T, i
                      "kvs_prune_mask");
 }
 
+kvs_status kvs_prune_quantile(const kvs_dims* dims, const float* score, int32_t T, float q,
+                              int32_t w, float* tau, uint8_t* mask, int32_t* keep, void* stream) {
+  kvs_status st = check_dims(dims, __func__, false);
+  if (st) return st;
+  REQUIRE(T >= 0 && w >= 0, KVS_ERR_ARG, "kvs_prune_quantile: negative T or w");
+  REQUIRE(q >= 0.f && q <= 1.f, KVS_ERR_ARG, "kvs_prune_quantile: q = %g outside [0, 1]", (double)q);
+  REQUIRE_PTR(tau);
+  REQUIRE_PTR(keep);
+  if (T > 0) {
+    REQUIRE_PTR(score);
+    REQUIRE_PTR(mask);
+  }
+  return cuda_status(kvs::launch_prune_quantile(score, dims->L, dims->H_kv, T, q, w, tau, mask,
+                                                keep, as_stream(stream)),
+                     "kvs_prune_quantile");
+}
+
 size_t kvs_compact_workspace_size(const kvs_dims* dims, int32_t T) {
-  if (!dims || dims->L <= 0 || dims->H_kv <= 0 || T < 0) return 0;
-  return kvs::compact_workspace_bytes(dims->L * dims->H_kv, T);
+  return kvs_compact_multi_workspace_size(dims, T, 1);
+}
+
+size_t kvs_compact_multi_workspace_size(const kvs_dims* dims, int32_t T, int32_t n_masks) {
+  if (!dims || dims->L <= 0 || dims->H_kv <= 0 || T < 0 || n_masks < 1) return 0;
+  return kvs::compact_workspace_bytes(dims->L * dims->H_kv * n_masks, T);
+}
+
+static kvs_status compact_paged(const char* fn, const kvs_dims* dims, const kvs_bf16* k,
+                                const kvs_bf16* v, int32_t T, int32_t n_masks, const uint8_t* mask,
+                                int32_t page_size, kvs_bf16* k_pages, kvs_bf16* v_pages,
+                                int32_t capacity_pages, int32_t* block_table, int32_t max_pages,
+                                int32_t* seq_lens, int32_t* needed_pages, void* ws,
+                                size_t ws_bytes, void* stream) {
+  kvs_status st = check_dims(dims, fn, false);
+  if (st) return st;
+  REQUIRE(dims->d == 64 || dims->d == 128, KVS_ERR_UNSUPPORTED,
+          "%s: head dim d = %d (supported: 64, 128)", fn, dims->d);
+  REQUIRE(T >= 0 && capacity_pages >= 0, KVS_ERR_ARG, "%s: negative size", fn);
+  REQUIRE(n_masks >= 1, KVS_ERR_ARG, "%s: n_masks = %d (at least 1)", fn, n_masks);
+  REQUIRE((long long)dims->L * dims->H_kv * n_masks <= (1LL << 30), KVS_ERR_SHAPE,
+          "%s: %d masks of %d rows", fn, n_masks, dims->L * dims->H_kv);
+  REQUIRE(page_size >= 1 && page_size <= 4096, KVS_ERR_UNSUPPORTED,
+          "%s: page_size = %d (1..4096)", fn, page_size);
+  REQUIRE(max_pages >= (T + page_size - 1) / page_size, KVS_ERR_SHAPE,
+          "%s: max_pages = %d below ceil(T / page_size) = %d", fn, max_pages,
+          (T + page_size - 1) / page_size);
+  if (!seq_lens) return fail(KVS_ERR_ARG, "%s: seq_lens is NULL", fn);
+  if (!needed_pages) return fail(KVS_ERR_ARG, "%s: needed_pages is NULL", fn);
+  if (!ws) return fail(KVS_ERR_ARG, "%s: ws is NULL", fn);
+  if (!aligned16(seq_lens) || !aligned16(needed_pages) || !aligned16(ws))
+    return fail(KVS_ERR_ALIGN, "%s: seq_lens, needed_pages or ws is not 16-byte aligned", fn);
+  if (max_pages > 0) {
+    if (!block_table) return fail(KVS_ERR_ARG, "%s: block_table is NULL", fn);
+    if (!aligned16(block_table)) return fail(KVS_ERR_ALIGN, "%s: block_table is not 16-byte aligned", fn);
+  }
+  if (T > 0) {
+    if (!k || !v || !mask) return fail(KVS_ERR_ARG, "%s: k, v or mask is NULL", fn);
+    if (!aligned16(k) || !aligned16(v) || !aligned16(mask))
+      return fail(KVS_ERR_ALIGN, "%s: k, v or mask is not 16-byte aligned", fn);
+  }
+  if (capacity_pages > 0) {
+    if (!k_pages || !v_pages) return fail(KVS_ERR_ARG, "%s: k_pages or v_pages is NULL", fn);
+    if (!aligned16(k_pages) || !aligned16(v_pages))
+      return fail(KVS_ERR_ALIGN, "%s: k_pages or v_pages is not 16-byte aligned", fn);
+  }
+  const size_t need = kvs_compact_multi_workspace_size(dims, T, n_masks);
+  REQUIRE(ws_bytes >= need, KVS_ERR_CAPACITY, "%s: workspace of %zu bytes, %zu needed", fn,
+          ws_bytes, need);
+  return cuda_status(kvs::launch_compact(k, v, dims->L * dims->H_kv, n_masks, T, dims->d, mask,
+                                         page_size, k_pages, v_pages, capacity_pages, block_table,
+                                         max_pages, seq_lens, needed_pages, ws, as_stream(stream)),
+                     fn);
 }
 
 kvs_status kvs_compact_paged(const kvs_dims* dims, const kvs_bf16* k, const kvs_bf16* v, int32_t T,
@@ -530,36 +598,44 @@ kvs_status kvs_compact_paged(const kvs_dims* dims, const kvs_bf16* k, const kvs_
                              kvs_bf16* v_pages, int32_t capacity_pages, int32_t* block_table,
                              int32_t max_pages, int32_t* seq_lens, int32_t* needed_pages,
                              void* ws, size_t ws_bytes, void* stream) {
+  return compact_paged(__func__, dims, k, v, T, 1, mask, page_size, k_pages, v_pages,
+                       capacity_pages, block_table, max_pages, seq_lens, needed_pages, ws,
+                       ws_bytes, stream);
+}
+
+kvs_status kvs_compact_paged_multi(const kvs_dims* dims, const kvs_bf16* k, const kvs_bf16* v,
+                                   int32_t T, int32_t n_masks, const uint8_t* masks,
+                                   int32_t page_size, kvs_bf16* k_pages, kvs_bf16* v_pages,
+                                   int32_t capacity_pages, int32_t* block_table, int32_t max_pages,
+                                   int32_t* seq_lens, int32_t* needed_pages, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  return compact_paged(__func__, dims, k, v, T, n_masks, masks, page_size, k_pages, v_pages,
+                       capacity_pages, block_table, max_pages, seq_lens, needed_pages, ws,
+                       ws_bytes, stream);
+}
+
+kvs_status kvs_prune_topk_multi(const kvs_dims* dims, const float* score, int32_t T,
+                                int32_t n_budgets, const int32_t* k, int32_t w, uint8_t* masks,
+                                int32_t* keeps, void* stream) {
   kvs_status st = check_dims(dims, __func__, false);
   if (st) return st;
-  REQUIRE(dims->d == 64 || dims->d == 128, KVS_ERR_UNSUPPORTED,
-          "kvs_compact_paged: head dim d = %d (supported: 64, 128)", dims->d);
-  REQUIRE(T >= 0 && capacity_pages >= 0, KVS_ERR_ARG, "kvs_compact_paged: negative size");
-  REQUIRE(page_size >= 1 && page_size <= 4096, KVS_ERR_UNSUPPORTED,
-          "kvs_compact_paged: page_size = %d (1..4096)", page_size);
-  REQUIRE(max_pages >= (T + page_size - 1) / page_size, KVS_ERR_SHAPE,
-          "kvs_compact_paged: max_pages = %d below ceil(T / page_size) = %d", max_pages,
-          (T + page_size - 1) / page_size);
-  REQUIRE_PTR(seq_lens);
-  REQUIRE_PTR(needed_pages);
-  REQUIRE_PTR(ws);
-  if (max_pages > 0) REQUIRE_PTR(block_table);
+  REQUIRE(T >= 0 && w >= 0, KVS_ERR_ARG, "kvs_prune_topk_multi: negative T or w");
+  REQUIRE(n_budgets >= 1 && n_budgets <= kvs::kMaxTopkBudgets, KVS_ERR_UNSUPPORTED,
+          "kvs_prune_topk_multi: n_budgets = %d (1..%d)", n_budgets, kvs::kMaxTopkBudgets);
+  REQUIRE(k != nullptr, KVS_ERR_ARG, "kvs_prune_topk_multi: k is NULL");
+  kvs::TopkBudgets kb = {};
+  for (int b = 0; b < n_budgets; ++b) {
+    REQUIRE(k[b] >= 0, KVS_ERR_ARG, "kvs_prune_topk_multi: k[%d] = %d is negative", b, k[b]);
+    kb.k[b] = k[b];
+  }
+  REQUIRE_PTR(keeps);
   if (T > 0) {
-    REQUIRE_PTR(k);
-    REQUIRE_PTR(v);
-    REQUIRE_PTR(mask);
+    REQUIRE_PTR(score);
+    REQUIRE_PTR(masks);
   }
-  if (capacity_pages > 0) {
-    REQUIRE_PTR(k_pages);
-    REQUIRE_PTR(v_pages);
-  }
-  const size_t need = kvs_compact_workspace_size(dims, T);
-  REQUIRE(ws_bytes >= need, KVS_ERR_CAPACITY,
-          "kvs_compact_paged: workspace of %zu bytes, %zu needed", ws_bytes, need);
-  return cuda_status(kvs::launch_compact(k, v, dims->L * dims->H_kv, T, dims->d, mask, page_size,
-                                         k_pages, v_pages, capacity_pages, block_table, max_pages,
-                                         seq_lens, needed_pages, ws, as_stream(stream)),
-                     "kvs_compact_paged");
+  return cuda_status(kvs::launch_topk(score, dims->L * dims->H_kv, T, n_budgets, kb, w, masks,
+                                      keeps, as_stream(stream)),
+                     "kvs_prune_topk_multi");
 }
 
 }  // extern "C"

@@ -177,8 +177,11 @@ __device__ __forceinline__ float max_raw_cols(const uint32_t* v, float r) {
 }
 
 // Future mass of 64 columns: sum_c 2^(acc_c * sc2) (the column's -lse_j sqrt(d) is in the
-// accumulator), columns c < jlim zeroed.
-__device__ __forceinline__ float future_cols(const uint32_t* v, float sc2, bool band, int jlim) {
+// accumulator); in a band chunk (BAND) the columns c < jlim are zeroed.  The band test is
+// a template argument so that the chunks off the band (nearly all) carry no per-column
+// compare and select.
+template <bool BAND>
+__device__ __forceinline__ float future_cols(const uint32_t* v, float sc2, int jlim) {
   const float2 k2 = make_float2(sc2, sc2);
   float2 a0 = make_float2(0.f, 0.f), a1 = a0;
 #pragma unroll
@@ -187,7 +190,7 @@ __device__ __forceinline__ float future_cols(const uint32_t* v, float sc2, bool 
     const float2 y1 = __fmul2_rn(f2(v[4 * q + 2], v[4 * q + 3]), k2);
     float e0 = fast_exp2(y0.x), e1 = fast_exp2(y0.y);
     float e2 = fast_exp2(y1.x), e3 = fast_exp2(y1.y);
-    if (band) {
+    if constexpr (BAND) {
       if (4 * q < jlim) e0 = 0.f;
       if (4 * q + 1 < jlim) e1 = 0.f;
       if (4 * q + 2 < jlim) e2 = 0.f;
@@ -662,8 +665,12 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
               } else {
                 const int j0 = (U.qt_begin + it % U.per_head) * BN + h * COLS + c0;
                 const bool band = j0 < U.row0 + BM - 1 + a.w;
-                if (band && ra + a.w - j0 >= 64) continue;  // all 64 queries in the window
-                f += future_cols(w, sc2, band, ra + a.w - j0);
+                if (band) {
+                  if (ra + a.w - j0 >= 64) continue;  // all 64 queries in the window
+                  f += future_cols<true>(w, sc2, ra + a.w - j0);
+                } else {
+                  f += future_cols<false>(w, sc2, 0);
+                }
               }
             }
             if (MODE == kMax && (it + 1) % U.per_head == 0) {  // last query tile of this head

@@ -2,7 +2,9 @@
 // Algorithm 1: keys[indices], values[indices]; limitation 3: non-uniform head
 // lengths need PagedAttention-like storage).
 //
-// Three launches, all bandwidth-bound:
+// Any number of masks over the same K/V rows go through one set of launches: mask row r
+// takes its K/V from row r % (L H_kv), and the pages of all masks share one pool, in
+// mask-major order.  Three launches, all bandwidth-bound:
 //   1. seg_count   : kept tokens per (row, segment of 256, 1024 or 4096 tokens)  reads the mask
 //   2. page_plan   : per-row exclusive scan of segment counts, page counts
 //                    ceil(kept/page), exclusive scan of pages over rows (layer-major,
@@ -143,7 +145,7 @@ __global__ void __launch_bounds__(1024) page_plan_kernel(int rows, int nseg, int
 template <int P>
 __global__ void __launch_bounds__(kSegThreads) scatter_kernel(
     const bf16_t* __restrict__ k, const bf16_t* __restrict__ v, const uint8_t* __restrict__ mask,
-    int T, int d, int nseg, int page_size, const int* __restrict__ seg,
+    int T, int d, int nseg, int kv_rows, int page_size, const int* __restrict__ seg,
     const int* __restrict__ first_page, const Plan* __restrict__ plan,
     const int* __restrict__ seq_lens, bf16_t* __restrict__ k_pages, bf16_t* __restrict__ v_pages,
     int* __restrict__ block_table, int max_pages) {
@@ -207,7 +209,7 @@ __global__ void __launch_bounds__(kSegThreads) scatter_kernel(
   // cooperative copy: (d/8) 16-byte chunks per kept row, for K and V
   const int base_rank = seg[(size_t)row * nseg + s];
   const int cpr = d / 8;
-  const size_t src_row0 = (size_t)row * T + (size_t)s * kSeg;
+  const size_t src_row0 = (size_t)(row % kv_rows) * T + (size_t)s * kSeg;  // mask row -> K/V row
   const int total = n_local * cpr;
   constexpr int U = 4;
   for (int i0 = threadIdx.x; i0 < total; i0 += blockDim.x * U) {
@@ -253,10 +255,11 @@ size_t compact_workspace_bytes(int rows, int T) {
   return sizeof(Plan) + sizeof(int) * ((size_t)rows * (nseg > 0 ? nseg : 1) + rows);
 }
 
-cudaError_t launch_compact(const bf16_t* k, const bf16_t* v, int rows, int T, int d,
+cudaError_t launch_compact(const bf16_t* k, const bf16_t* v, int kv_rows, int n_masks, int T, int d,
                            const uint8_t* mask, int page_size, bf16_t* k_pages, bf16_t* v_pages,
                            int capacity, int* block_table, int max_pages, int* seq_lens,
                            int* needed, void* ws, cudaStream_t s) {
+  const int rows = kv_rows * n_masks;  // mask rows: mask-major, then the K/V rows
   if (rows == 0) return cudaSuccess;
   const bool long_rows = T >= kLongRow, short_rows = T <= kShortRow;
   const int seg_len = long_rows ? kMaxSeg : short_rows ? kTinySeg : kMinSeg;
@@ -275,15 +278,15 @@ cudaError_t launch_compact(const bf16_t* k, const bf16_t* v, int rows, int T, in
                                       needed);
   if (long_rows)
     scatter_kernel<16><<<dim3(nseg, rows), kSegThreads, 0, s>>>(
-        k, v, mask, T, d, nseg, page_size, seg, first, plan, seq_lens, k_pages, v_pages,
+        k, v, mask, T, d, nseg, kv_rows, page_size, seg, first, plan, seq_lens, k_pages, v_pages,
         block_table, max_pages);
   else if (short_rows)
     scatter_kernel<1><<<dim3(nseg, rows), kSegThreads, 0, s>>>(
-        k, v, mask, T, d, nseg, page_size, seg, first, plan, seq_lens, k_pages, v_pages,
+        k, v, mask, T, d, nseg, kv_rows, page_size, seg, first, plan, seq_lens, k_pages, v_pages,
         block_table, max_pages);
   else
     scatter_kernel<4><<<dim3(nseg, rows), kSegThreads, 0, s>>>(
-        k, v, mask, T, d, nseg, page_size, seg, first, plan, seq_lens, k_pages, v_pages,
+        k, v, mask, T, d, nseg, kv_rows, page_size, seg, first, plan, seq_lens, k_pages, v_pages,
         block_table, max_pages);
   return cudaGetLastError();
 }

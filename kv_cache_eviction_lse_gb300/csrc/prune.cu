@@ -3,10 +3,14 @@
 //              Algorithm 1 sets the window scores to +inf and keeps scores >= threshold)
 //   top-k:     keep the window plus the k best of the other T - w tokens
 //              (KVpop review, 3. Method: per-head top-k within a fixed budget)
+//   quantile:  threshold with tau_l = the lower nearest-rank quantile q of the layer's
+//              non-window scores over all its KV heads (KVzip review, Methods: a
+//              ratio-based threshold; the threshold rule as above)
 // Top-k ranks by (score descending, position ascending) with NaN below everything;
 // the k-th key is found by an exact 4-pass radix select on order-preserving 32-bit
 // keys (shared-memory histograms), then ties at the k-th key go to the lowest
-// positions via a block-wide ordered scan.  Deterministic, no sorting.
+// positions via a block-wide ordered scan.  Deterministic, no sorting.  One launch
+// selects any number (up to kMaxTopkBudgets) of budgets over the same scores.
 #include "common.cuh"
 #include "prune.cuh"
 
@@ -14,9 +18,12 @@ namespace kvs {
 namespace {
 
 constexpr int kPruneThreads = 1024;
+constexpr int kStageMaxT = 16384;  // rows staged in shared memory (64 KB of order keys)
 
+// Order-preserving 32-bit key of a score: -0 and +0 get the same key (they compare equal,
+// so a tie between them goes to the earlier position like any other tie).
 __device__ __forceinline__ uint32_t order_key(float f) {
-  const uint32_t b = __float_as_uint(f);
+  const uint32_t b = f == 0.f ? 0u : __float_as_uint(f);
   if (f != f) return 0u;  // NaN below -inf (whose key is 0x007fffff)
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
@@ -64,12 +71,16 @@ constexpr int kThrPer = 16;  // tokens per thread
 
 // Grid (chunks of 4096 tokens, rows).  keep[row] must be zero on entry (the launcher
 // clears it); each block adds its count with one atomic.
+// With tau_l != NULL the threshold of row r is tau_l[r / rows_per_tau] (per layer).
 __global__ void __launch_bounds__(kThrThreads) threshold_kernel(const float* __restrict__ score,
-                                                                int T, float tau, int w,
+                                                                int T, float tau_c, int w,
+                                                                const float* __restrict__ tau_l,
+                                                                int rows_per_tau,
                                                                 uint8_t* __restrict__ mask,
                                                                 int* __restrict__ keep) {
   __shared__ int red[33];
   const size_t row = blockIdx.y;
+  const float tau = tau_l ? tau_l[row / rows_per_tau] : tau_c;
   const float* s = score + row * T;
   uint8_t* m = mask + row * T;
   const int t0 = (blockIdx.x * kThrThreads + threadIdx.x) * kThrPer;
@@ -104,23 +115,122 @@ __global__ void __launch_bounds__(kThrThreads) threshold_kernel(const float* __r
   if (threadIdx.x == 0 && cnt) atomicAdd(keep + row, cnt);
 }
 
+// Float value of an order key (the inverse of order_key; key 0 is NaN).
+__device__ __forceinline__ float key_value(uint32_t k) {
+  if (k == 0u) return __uint_as_float(0x7fc00000u);
+  return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
+}
+
+// One block per layer: tau[l] = the rank-r smallest (0-based, r = floor(q (N - 1))) of
+// the layer's N = H_kv (T - w) non-window scores, NaN lowest, by an exact 4-pass radix
+// select from the bottom (shared-memory histograms over order keys).  N = 0: +inf.
+__global__ void __launch_bounds__(kPruneThreads) quantile_kernel(const float* __restrict__ score,
+                                                                 int Hkv, int T, int w, float q,
+                                                                 float* __restrict__ tau) {
+  __shared__ unsigned hist[256];
+  __shared__ uint32_t s_prefix;
+  __shared__ long long s_rem;
+  const int l = blockIdx.x;
+  const int n = T - min(max(w, 0), T);
+  const long long N = (long long)Hkv * n;
+  if (N <= 0) {
+    if (threadIdx.x == 0) tau[l] = __uint_as_float(0x7f800000u);
+    return;
+  }
+  const float* s = score + (size_t)l * Hkv * T;
+  if (threadIdx.x == 0) {
+    s_prefix = 0u;
+    s_rem = (long long)floor((double)q * (double)(N - 1));
+  }
+  uint32_t hi_mask = 0u;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0u;
+    __syncthreads();
+    const uint32_t prefix = s_prefix;
+    for (int h = 0; h < Hkv; ++h)
+      for (int t = threadIdx.x; t < n; t += blockDim.x) {
+        const uint32_t u = order_key(s[(size_t)h * T + t]);
+        if ((u & hi_mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+      }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      // lane l owns digits 8l .. 8l+7; find the digit at which the count of keys from the
+      // bottom passes the remaining rank
+      const int lane = threadIdx.x;
+      long long c[8], tot = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = hist[8 * lane + i];
+        tot += c[i];
+      }
+      long long incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const long long r = s_rem;
+      const unsigned hit = __ballot_sync(0xffffffffu, incl > r);
+      const int src = __ffs(hit) - 1;  // first lane whose range passes rank r
+      if (lane == src) {
+        long long cum = incl - tot;
+        int i = 0;
+        for (; i < 7; ++i) {
+          if (cum + c[i] > r) break;
+          cum += c[i];
+        }
+        s_rem = r - cum;
+        s_prefix = prefix | ((uint32_t)(8 * lane + i) << shift);
+      }
+    }
+    hi_mask |= 255u << shift;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) tau[l] = key_value(s_prefix);
+}
+
+// One block per (row, budget): grid (rows, n_budgets).  Rows of up to kStageMaxT scores
+// are staged once in shared memory as order keys (the radix passes then read shared
+// memory); longer rows are read from global memory in every pass.  The last radix pass
+// also counts the candidates equal to the k-th key: when all of them are kept (no tie
+// crosses the budget, the usual case) the mask is a plain u >= kth compare, written four
+// tokens per store; otherwise the ties go to the lowest positions by an ordered scan.
+// keep = min(k, T - w) + min(w, T) exactly: top-k keeps that many by construction.
 __global__ void __launch_bounds__(kPruneThreads) topk_kernel(const float* __restrict__ score,
-                                                             int T, int k, int w,
-                                                             uint8_t* __restrict__ mask,
+                                                             int rows, int T, TopkBudgets kb,
+                                                             int w, uint8_t* __restrict__ mask,
                                                              int* __restrict__ keep) {
+  extern __shared__ uint32_t keys_s[];
   __shared__ unsigned hist[256];
   __shared__ int red[33];
   __shared__ uint32_t s_prefix;
-  __shared__ int s_rem;
+  __shared__ int s_rem, s_eq;
+  const int b = blockIdx.y;
   const size_t row = blockIdx.x;
   const float* s = score + row * T;
-  uint8_t* m = mask + row * T;
+  uint8_t* m = mask + ((size_t)b * rows + row) * T;
   const int wn = min(max(w, 0), T);
-  const int n = T - wn;              // candidate tokens (outside the window)
-  const int kk = min(max(k, 0), n);  // how many of them to keep
+  const int n = T - wn;                    // candidate tokens (outside the window)
+  const int kk = min(max(kb.k[b], 0), n);  // how many of them to keep
+  const bool staged = T <= kStageMaxT;
+  const bool vec = (T & 3) == 0;
+  if (staged && kk > 0 && kk < n) {
+    if (vec) {
+      for (int t4 = threadIdx.x; 4 * t4 < n; t4 += blockDim.x) {
+        const float4 x = *reinterpret_cast<const float4*>(s + 4 * t4);
+        *reinterpret_cast<uint4*>(keys_s + 4 * t4) =
+            make_uint4(order_key(x.x), order_key(x.y), order_key(x.z), order_key(x.w));
+      }
+    } else {
+      for (int t = threadIdx.x; t < n; t += blockDim.x) keys_s[t] = order_key(s[t]);
+    }
+    __syncthreads();
+  }
+  auto key_at = [&](int t) -> uint32_t { return staged ? keys_s[t] : order_key(s[t]); };
 
   uint32_t kth = 0;  // key of the kk-th best candidate
   int rem = 0;       // how many candidates equal to kth to keep
+  int eq_all = 0;    // how many candidates equal kth
   if (kk > 0 && kk < n) {
     if (threadIdx.x == 0) {
       s_prefix = 0u;
@@ -132,7 +242,7 @@ __global__ void __launch_bounds__(kPruneThreads) topk_kernel(const float* __rest
       __syncthreads();
       const uint32_t prefix = s_prefix;
       for (int t = threadIdx.x; t < n; t += blockDim.x) {
-        const uint32_t u = order_key(s[t]);
+        const uint32_t u = key_at(t);
         if ((u & hi_mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
       }
       __syncthreads();
@@ -162,6 +272,7 @@ __global__ void __launch_bounds__(kPruneThreads) topk_kernel(const float* __rest
             cum += c[i];
           }
           s_rem = r - cum;
+          s_eq = c[i];  // after the last pass: the candidates whose key equals kth
           s_prefix = prefix | ((uint32_t)(255 - 8 * lane - i) << shift);
         }
       }
@@ -170,32 +281,46 @@ __global__ void __launch_bounds__(kPruneThreads) topk_kernel(const float* __rest
     }
     kth = s_prefix;
     rem = s_rem;
+    eq_all = s_eq;
+  }
+  if (threadIdx.x == 0) keep[(size_t)b * rows + row] = kk + wn;
+
+  if (kk == 0 || kk == n || rem == eq_all) {
+    // every candidate at or above the k-th key is kept (kk == n: all, kk == 0: none)
+    const uint32_t lo = kk == 0 ? 0xffffffffu : kk == n ? 0u : kth;
+    auto kept = [&](int t) -> uint32_t {
+      if (t >= n) return 1u;
+      if (kk == 0) return 0u;
+      if (kk == n) return 1u;
+      return key_at(t) >= lo ? 1u : 0u;
+    };
+    if (vec) {
+      for (int t4 = threadIdx.x; 4 * t4 < T; t4 += blockDim.x) {
+        const int t = 4 * t4;
+        const uint32_t word = kept(t) | (kept(t + 1) << 8) | (kept(t + 2) << 16) | (kept(t + 3) << 24);
+        *reinterpret_cast<uint32_t*>(m + t) = word;
+      }
+    } else {
+      for (int t = threadIdx.x; t < T; t += blockDim.x) m[t] = (uint8_t)kept(t);
+    }
+    return;
   }
 
-  int cnt = 0, carry = 0;
+  // ties at the k-th key cross the budget: they go to the lowest positions
+  int carry = 0;
   for (int base = 0; base < T; base += blockDim.x) {
     const int t = base + threadIdx.x;
     bool gt = false, eq = false;
-    if (t < n && kk > 0) {
-      if (kk == n) {
-        gt = true;
-      } else {
-        const uint32_t u = order_key(s[t]);
-        gt = u > kth;
-        eq = u == kth;
-      }
+    if (t < n) {
+      const uint32_t u = key_at(t);
+      gt = u > kth;
+      eq = u == kth;
     }
     int tot;
     const int rank = block_excl_scan_flag(eq, red, &tot) + carry;
     carry += tot;
-    if (t < T) {
-      const int kp = (t >= n) || gt || (eq && rank < rem);
-      m[t] = (uint8_t)kp;
-      cnt += kp;
-    }
+    if (t < T) m[t] = (uint8_t)((t >= n) || gt || (eq && rank < rem));
   }
-  cnt = block_sum(cnt, red);
-  if (threadIdx.x == 0) keep[row] = cnt;
 }
 
 }  // namespace
@@ -210,11 +335,39 @@ cudaError_t launch_prune(const float* score, int rows, int T, int mode, float ta
     const int per_block = kThrThreads * kThrPer;
     count_launches(1);
     threshold_kernel<<<dim3((T + per_block - 1) / per_block, rows), kThrThreads, 0, s>>>(
-        score, T, tau, w, mask, keep);
-  } else {
-    count_launches(1);
-    topk_kernel<<<rows, kPruneThreads, 0, s>>>(score, T, k, w, mask, keep);
+        score, T, tau, w, nullptr, 1, mask, keep);
+    return cudaGetLastError();
   }
+  TopkBudgets kb;
+  kb.k[0] = k;
+  return launch_topk(score, rows, T, 1, kb, w, mask, keep, s);
+}
+
+cudaError_t launch_topk(const float* score, int rows, int T, int n_budgets, const TopkBudgets& kb,
+                        int w, uint8_t* mask, int* keep, cudaStream_t s) {
+  if (rows == 0 || n_budgets == 0) return cudaSuccess;
+  if (n_budgets < 0 || n_budgets > kMaxTopkBudgets) return cudaErrorInvalidValue;
+  const size_t smem = T <= kStageMaxT ? (size_t)T * sizeof(uint32_t) : 0;
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)(kStageMaxT * sizeof(uint32_t)));
+  if (e != cudaSuccess) return e;
+  count_launches(1);
+  topk_kernel<<<dim3(rows, n_budgets), kPruneThreads, smem, s>>>(score, rows, T, kb, w, mask, keep);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prune_quantile(const float* score, int L, int Hkv, int T, float q, int w,
+                                  float* tau, uint8_t* mask, int* keep, cudaStream_t s) {
+  if (L == 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(keep, 0, sizeof(int) * (size_t)L * Hkv, s);
+  if (e != cudaSuccess) return e;
+  count_launches(1);
+  quantile_kernel<<<L, kPruneThreads, 0, s>>>(score, Hkv, T, w, q, tau);
+  if (T == 0) return cudaGetLastError();
+  const int per_block = kThrThreads * kThrPer;
+  count_launches(1);
+  threshold_kernel<<<dim3((T + per_block - 1) / per_block, L * Hkv), kThrThreads, 0, s>>>(
+      score, T, 0.f, w, tau, Hkv, mask, keep);
   return cudaGetLastError();
 }
 

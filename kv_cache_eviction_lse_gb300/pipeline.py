@@ -6,12 +6,14 @@ method happens here, only call sequencing and buffer management.
 
   KVzip / KVzip+ (c1, c2)   [vnorm] -> lse -> score_max -> top-k per budget -> compact
   chunked KVzip+  (c3)      vnorm -> per chunk (lse -> score_max, max-accumulated)
-                            -> threshold (per-layer tau) -> compact
+                            -> threshold at the layer's score quantile -> compact
   KVpop target    (c4)      lse (causal self-attention) -> future_sum -> top-k per budget
                             -> compact
   KVzap           (c5)      surrogate (+ fused threshold) -> compact
 """
 from __future__ import annotations
+
+import types
 
 import torch
 
@@ -42,13 +44,64 @@ class Pages:
         return int(self.seq_lens.sum().item()) * 2 * d * 2
 
 
+class PagePool:
+    """One paged cache for n masks over the same [L][H][T][d] K/V pair: the pages of mask
+    b follow those of masks 0 .. b-1 in one pool; ``view(b)`` exposes mask b's block
+    table and lengths (absolute page ids into the shared pool)."""
+
+    def __init__(self, n, L, H, T, d, page_size, device):
+        self.n = n
+        self.page_size = page_size
+        self.max_pages = -(-T // page_size)
+        self.capacity = n * L * H * self.max_pages
+        self.k_pages = _empty((self.capacity, page_size, d), torch.bfloat16, device)
+        self.v_pages = _empty((self.capacity, page_size, d), torch.bfloat16, device)
+        self.block_table = _empty((n, L, H, self.max_pages), torch.int32, device)
+        self.seq_lens = _empty((n, L, H), torch.int32, device)
+        self.needed = _empty((4,), torch.int32, device)
+
+    def view(self, b):
+        return types.SimpleNamespace(page_size=self.page_size, max_pages=self.max_pages,
+                                     capacity=self.capacity, k_pages=self.k_pages,
+                                     v_pages=self.v_pages, block_table=self.block_table[b],
+                                     seq_lens=self.seq_lens[b], needed=self.needed)
+
+
+def compact_multi_into(dm, k, v, T, masks, pool: PagePool, ws):
+    C.kvs_compact_paged_multi(dm, k, v, T, pool.n, masks, pool.page_size, pool.k_pages,
+                              pool.v_pages, pool.capacity, pool.block_table, pool.max_pages,
+                              pool.seq_lens, pool.needed, ws, ws.numel())
+
+
 def compact_into(dm, k, v, T, mask, pages: Pages, ws):
     C.kvs_compact_paged(dm, k, v, T, mask, pages.page_size, pages.k_pages, pages.v_pages,
                         pages.capacity, pages.block_table, pages.max_pages, pages.seq_lens,
                         pages.needed, ws, ws.numel())
 
 
-class KVzipPipeline:
+class _Budgets:
+    """Top-k budgets over one score tensor: all masks in one [n][L][H_kv][T] tensor, all
+    pages in one pool, each selected and compacted by one library call."""
+
+    def _budgets(self, wl, L, dev, ratios):
+        self.ratios = tuple(ratios if ratios is not None else wl.keep_ratios)
+        n = len(self.ratios)
+        self.mask_all = _empty((n, L, wl.H_kv, wl.T), torch.uint8, dev)
+        self.keep_all = _empty((n, L, wl.H_kv), torch.int32, dev)
+        self.masks = [self.mask_all[b] for b in range(n)]
+        self.keeps = [self.keep_all[b] for b in range(n)]
+        self.pool = PagePool(n, L, wl.H_kv, wl.T, wl.d, wl.page_size, dev)
+        self.pages = [self.pool.view(b) for b in range(n)]
+        self.cws = _empty((C.kvs_compact_multi_workspace_size(self.dm, wl.T, n),), torch.uint8, dev)
+
+
+def _prune_budgets(p):
+    wl = p.wl
+    C.kvs_prune_topk_multi(p.dm, p.score, wl.T, [wl.topk_budget(r) for r in p.ratios], wl.w,
+                           p.mask_all, p.keep_all)
+
+
+class KVzipPipeline(_Budgets):
     """c1 / c2: KVzip (plain) or KVzip+ scoring of the context, then top-k budgets."""
 
     # ridge weight of the value refit relative to the mean diagonal of A_S^T A_S (reading:
@@ -71,11 +124,7 @@ class KVzipPipeline:
             self.vws = _empty((C.kvs_vnorm_workspace_size(self.dm),), torch.uint8, dev)
         self.sws = _empty((max(16, C.kvs_score_max_workspace_size(self.dm, self.n_q, self.plus)),),
                           torch.uint8, dev)
-        self.ratios = tuple(ratios if ratios is not None else wl.keep_ratios)
-        self.masks = [_empty((L, wl.H_kv, wl.T), torch.uint8, dev) for _ in self.ratios]
-        self.keeps = [_empty((L, wl.H_kv), torch.int32, dev) for _ in self.ratios]
-        self.pages = [Pages(L, wl.H_kv, wl.T, wl.d, wl.page_size, dev) for _ in self.ratios]
-        self.cws = _empty((C.kvs_compact_workspace_size(self.dm, wl.T),), torch.uint8, dev)
+        self._budgets(wl, L, dev, ratios)
         # refit: Select+Fit on the first budget -- the kept keys gathered densely (one
         # page of exactly k rows per head), then their values refitted in closed form
         self.refit = refit
@@ -126,20 +175,18 @@ class KVzipPipeline:
                             self.score, self.sws, self.sws.numel())
 
     def _prune(self):
-        wl, dm = self.wl, self.dm
-        for r, m, kp in zip(self.ratios, self.masks, self.keeps):
-            C.kvs_prune_mask(dm, self.score, wl.T, C.KVS_TOPK, 0.0, wl.topk_budget(r), wl.w, m, kp)
+        _prune_budgets(self)
 
     def _compact(self):
-        wl, x, dm = self.wl, self.x, self.dm
-        for m, pg in zip(self.masks, self.pages):
-            compact_into(dm, x["k_ctx"], x["v_ctx"], wl.T, m, pg, self.cws)
+        x = self.x
+        compact_multi_into(self.dm, x["k_ctx"], x["v_ctx"], self.wl.T, self.mask_all, self.pool,
+                           self.cws)
 
     def stages(self):
         """(name, callable) per library entry point, in step order."""
         st = [("kvs_vnorm", self._vnorm)] if self.plus else []
         st += [("kvs_lse", self._lse), ("kvs_score_max", self._score),
-               ("kvs_prune_mask", self._prune), ("kvs_compact_paged", self._compact)]
+               ("kvs_prune_topk_multi", self._prune), ("kvs_compact_paged_multi", self._compact)]
         return st + ([("kvs_value_refit", self._refit)] if self.refit else [])
 
     def step(self):
@@ -163,7 +210,11 @@ class ChunkedKVzipPipeline:
         self.vws = _empty((C.kvs_vnorm_workspace_size(self.dm),), torch.uint8, dev)
         self.sws = _empty((max(16, C.kvs_score_max_workspace_size(self.dm, wl.n_rep, 1)),),
                           torch.uint8, dev)
-        self.tau = tau  # per-layer list of floats, set by the caller (calibrate_tau)
+        # per-layer threshold: the tau_quantile of the layer's non-window scores, set on
+        # the device by kvs_prune_quantile in every step; a caller may instead fix it
+        # (a list of floats, one per layer), as a model-specific tau would be
+        self.tau = tau
+        self.tau_dev = _empty((max(L, 4),), torch.float32, dev)
         self.mask = _empty((L, wl.H_kv, wl.T), torch.uint8, dev)
         self.keep = _empty((L, wl.H_kv), torch.int32, dev)
         self.pages = Pages(L, wl.H_kv, wl.T, wl.d, wl.page_size, dev)
@@ -191,6 +242,10 @@ class ChunkedKVzipPipeline:
 
     def _prune(self):
         wl = self.wl
+        if self.tau is None:
+            C.kvs_prune_quantile(self.dm, self.score, wl.T, wl.tau_quantile, wl.w, self.tau_dev,
+                                 self.mask, self.keep)
+            return
         for l in range(self.L):
             C.kvs_prune_mask(self.dm1, self.score[l], wl.T, C.KVS_THRESHOLD, float(self.tau[l]), 0,
                              wl.w, self.mask[l], self.keep[l])
@@ -213,15 +268,16 @@ class ChunkedKVzipPipeline:
         def score_all():
             for c in range(self.wl.n_chunks):
                 self._score(c)
+        prune = "kvs_prune_quantile" if self.tau is None else "kvs_prune_mask"
         return [("kvs_vnorm", self._vnorm), ("kvs_lse", lse_all), ("kvs_score_max", score_all),
-                ("kvs_prune_mask", self._prune), ("kvs_compact_paged", self._compact)]
+                (prune, self._prune), ("kvs_compact_paged", self._compact)]
 
     def step(self):
         self.score_step()
         self.prune_step()
 
 
-class FuturePipeline:
+class FuturePipeline(_Budgets):
     """c4: KVpop future-attention target, then top-k budgets plus the window."""
 
     def __init__(self, wl: Workload, x: dict, ratios=None, attn_forward=False):
@@ -237,11 +293,7 @@ class FuturePipeline:
         self.o = _empty((L, wl.H_q, wl.T, wl.d), torch.bfloat16, dev) if attn_forward else None
         self.score = _empty((L, wl.H_kv, wl.T), torch.float32, dev)
         self.fws = _empty((C.kvs_score_future_sum_workspace_size(self.dm, wl.T),), torch.uint8, dev)
-        self.ratios = tuple(ratios if ratios is not None else wl.keep_ratios)
-        self.masks = [_empty((L, wl.H_kv, wl.T), torch.uint8, dev) for _ in self.ratios]
-        self.keeps = [_empty((L, wl.H_kv), torch.int32, dev) for _ in self.ratios]
-        self.pages = [Pages(L, wl.H_kv, wl.T, wl.d, wl.page_size, dev) for _ in self.ratios]
-        self.cws = _empty((C.kvs_compact_workspace_size(self.dm, wl.T),), torch.uint8, dev)
+        self._budgets(wl, L, dev, ratios)
 
     def _lse(self):
         wl, x, dm = self.wl, self.x, self.dm
@@ -257,14 +309,11 @@ class FuturePipeline:
                                self.fws.numel())
 
     def _prune(self):
-        wl, dm = self.wl, self.dm
-        for r, m, kp in zip(self.ratios, self.masks, self.keeps):
-            C.kvs_prune_mask(dm, self.score, wl.T, C.KVS_TOPK, 0.0, wl.topk_budget(r), wl.w, m, kp)
+        _prune_budgets(self)
 
     def _compact(self):
-        wl, x, dm = self.wl, self.x, self.dm
-        for m, pg in zip(self.masks, self.pages):
-            compact_into(dm, x["k"], x["v"], wl.T, m, pg, self.cws)
+        x = self.x
+        compact_multi_into(self.dm, x["k"], x["v"], self.wl.T, self.mask_all, self.pool, self.cws)
 
     def _pass1(self):
         return ("kvs_attn_fwd", self._forward) if self.attn_forward else ("kvs_lse", self._lse)
@@ -279,7 +328,7 @@ class FuturePipeline:
 
     def stages(self):
         return [self._pass1(), ("kvs_score_future_sum", self._future),
-                ("kvs_prune_mask", self._prune), ("kvs_compact_paged", self._compact)]
+                ("kvs_prune_topk_multi", self._prune), ("kvs_compact_paged_multi", self._compact)]
 
     def step(self):
         for _, fn in self.stages():

@@ -386,6 +386,134 @@ def test_compact_exact(C, T, page, d):
         assert bool((pages.k_pages[tot:] == 7.0).all())
 
 
+@pytest.mark.parametrize("L,H,T,w", [(1, 1, 1, 0), (2, 3, 300, 16), (3, 8, 2048, 128),
+                                     (2, 2, 5000, 5000), (1, 4, 20001, 7)])
+@pytest.mark.parametrize("levels,nan_frac", [(None, 0.0), (3, 0.0), (4, 0.05)])
+def test_prune_quantile_exact(C, L, H, T, w, levels, nan_frac):
+    """The per-layer tau is exactly the oracle's order statistic of the same fp32 scores
+    (NaN lowest) and the masks and counts are the threshold rule with it."""
+    s = _scores_with_ties((L, H, T), L * T + H, levels, nan_frac)
+    s[-1] += 3.0  # the last layer's scores sit higher: its own tau
+    for q in (0.25, 0.0, 1.0, 0.5):
+        tau = torch.full((L,), 123.0, device="cuda")
+        mask = torch.full((L, H, T), 9, dtype=torch.uint8, device="cuda")
+        keep = torch.full((L, H), -1, dtype=torch.int32, device="cuda")
+        C.kvs_prune_quantile(C.dims(L, H, H, 128), torch.from_numpy(s).cuda(), T, q, w, tau, mask,
+                             keep)
+        torch.cuda.synchronize()
+        m_ref, k_ref, t_ref = O.prune_quantile(s.astype(np.float64), q, w)
+        tg = tau.cpu().double().numpy()
+        assert np.array_equal(np.isnan(tg), np.isnan(t_ref)), (q, tg, t_ref)
+        ok = ~np.isnan(t_ref)
+        assert np.array_equal(tg[ok], t_ref[ok]), (q, tg, t_ref)
+        assert np.array_equal(mask.cpu().numpy(), m_ref), q
+        assert np.array_equal(keep.cpu().numpy(), k_ref), q
+
+
+def test_prune_quantile_rejects_bad_q(C):
+    t = torch.empty(64, device="cuda")
+    m = torch.empty(64, dtype=torch.uint8, device="cuda")
+    kp = torch.empty(16, dtype=torch.int32, device="cuda")
+    for q in (-0.1, 1.5, float("nan")):
+        with pytest.raises(C.KvsError) as e:
+            C.kvs_prune_quantile(C.dims(1, 1, 1, 128), t, 8, q, 0, t, m, kp)
+        assert e.value.status == C.KVS_ERR_ARG
+
+
+# several budgets in one launch: row lengths on both sides of the shared-memory staging
+# limit (16384), ties crossing the k-th value, NaN, windows, k = 0 and k >= T - w
+@pytest.mark.parametrize("T", [1, 7, 300, 2048, 4097, 16384, 20000])
+@pytest.mark.parametrize("levels,nan_frac", [(None, 0.0), (3, 0.0), (4, 0.05)])
+def test_prune_topk_multi_exact(C, T, levels, nan_frac):
+    L, H = 2, 3
+    s = _scores_with_ties((L, H, T), T + 7, levels, nan_frac)
+    for w, ks in [(0, [T // 4, T // 2, 0, T]), (16, [1, T // 3, T + 3]), (T // 3, [T // 2]),
+                  (T, [5, 0]), (0, [3, 3, 3, 3, 3, 3, 3, 3])]:
+        nb = len(ks)
+        masks = torch.full((nb, L, H, T), 9, dtype=torch.uint8, device="cuda")
+        keeps = torch.full((nb, L, H), -1, dtype=torch.int32, device="cuda")
+        C.kvs_prune_topk_multi(C.dims(L, H, H, 128), torch.from_numpy(s).cuda(), T, ks, w, masks,
+                               keeps)
+        torch.cuda.synchronize()
+        for b, k in enumerate(ks):
+            m_ref, k_ref = O.prune_topk(s.astype(np.float64), k, w)
+            assert np.array_equal(masks[b].cpu().numpy(), m_ref), (w, ks, b)
+            assert np.array_equal(keeps[b].cpu().numpy(), k_ref), (w, ks, b)
+
+
+def test_prune_topk_signed_zero_ties(C):
+    """-0 and +0 are equal scores: a tie between them goes to the earlier position, in
+    both the single-budget and the multi-budget selection."""
+    T = 9
+    s = np.array([[[-0.0, 0.0, 1.0, -0.0, 2.0, 0.0, -1.0, 0.0, -0.0]]], dtype=np.float32)
+    for k in range(T + 1):
+        m_ref, _ = O.prune_topk(s.astype(np.float64), k, 0)
+        mask = torch.empty(1, 1, T, dtype=torch.uint8, device="cuda")
+        keep = torch.empty(1, 1, dtype=torch.int32, device="cuda")
+        C.kvs_prune_mask(C.dims(1, 1, 1, 128), torch.from_numpy(s).cuda(), T, C.KVS_TOPK, 0.0, k, 0,
+                         mask, keep)
+        masks = torch.empty(2, 1, 1, T, dtype=torch.uint8, device="cuda")
+        keeps = torch.empty(2, 1, 1, dtype=torch.int32, device="cuda")
+        C.kvs_prune_topk_multi(C.dims(1, 1, 1, 128), torch.from_numpy(s).cuda(), T, [k, k], 0,
+                               masks, keeps)
+        torch.cuda.synchronize()
+        assert np.array_equal(mask.cpu().numpy(), m_ref), k
+        assert np.array_equal(masks[1].cpu().numpy(), m_ref), k
+
+
+def test_prune_topk_multi_rejects_bad_budgets(C):
+    t = torch.empty(64, device="cuda")
+    m = torch.empty(64, dtype=torch.uint8, device="cuda")
+    kp = torch.empty(16, dtype=torch.int32, device="cuda")
+    for ks, st in [([], C.KVS_ERR_UNSUPPORTED), ([1] * 9, C.KVS_ERR_UNSUPPORTED),
+                   ([2, -1], C.KVS_ERR_ARG)]:
+        with pytest.raises(C.KvsError) as e:
+            C.kvs_prune_topk_multi(C.dims(1, 1, 1, 128), t, 8, ks, 0, m, kp)
+        assert e.value.status == st
+
+
+@pytest.mark.parametrize("T,page,n_masks", [(1, 16, 2), (300, 16, 3), (2048, 16, 3),
+                                            (5000, 7, 2), (16384, 16, 2), (100, 4096, 4)])
+@pytest.mark.parametrize("d", [64, 128])
+def test_compact_multi_exact(C, T, page, n_masks, d):
+    """n masks over the same K/V in one call: equal to the oracle's compaction of the
+    masks stacked as n L layers over K/V repeated n times (pages mask-major)."""
+    L, H = 2, 3
+    r = np.random.default_rng(T + page + d + n_masks)
+    p_keep = r.uniform(0.0, 1.0, size=(n_masks, L, H, 1))
+    masks = (r.random((n_masks, L, H, T)) < p_keep).astype(np.uint8)
+    masks[0, 0, 0] = 1
+    masks[-1, 1, 2] = 0
+    gen = torch.Generator().manual_seed(T + d)
+    k = torch.randn(L, H, T, d, generator=gen).to(torch.bfloat16)
+    v = torch.randn(L, H, T, d, generator=gen).to(torch.bfloat16)
+    dm = C.dims(L, H, H, d)
+    max_pages = -(-T // page)
+    cap = n_masks * L * H * max_pages
+    kp = torch.full((cap, page, d), 7.0, dtype=torch.bfloat16, device="cuda")
+    vp = torch.full((cap, page, d), 7.0, dtype=torch.bfloat16, device="cuda")
+    bt = torch.empty((n_masks, L, H, max_pages), dtype=torch.int32, device="cuda")
+    sl = torch.empty((n_masks, L, H), dtype=torch.int32, device="cuda")
+    need = torch.empty(4, dtype=torch.int32, device="cuda")
+    nws = C.kvs_compact_multi_workspace_size(dm, T, n_masks)
+    assert nws >= C.kvs_compact_workspace_size(dm, T)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    C.kvs_compact_paged_multi(dm, k.cuda(), v.cuda(), T, n_masks, torch.from_numpy(masks).cuda(),
+                              page, kp, vp, cap, bt, max_pages, sl, need, ws, nws)
+    torch.cuda.synchronize()
+    kb = np.concatenate([k.view(torch.int16).numpy()] * n_masks)
+    vb = np.concatenate([v.view(torch.int16).numpy()] * n_masks)
+    kr, vr, btr, slr, tot = O.compact_paged(kb, vb, masks.reshape(n_masks * L, H, T), page,
+                                            max_pages)
+    assert int(need[0].item()) == tot
+    assert np.array_equal(sl.cpu().numpy().reshape(n_masks * L, H), slr)
+    assert np.array_equal(bt.cpu().numpy().reshape(n_masks * L, H, max_pages), btr)
+    assert np.array_equal(kp[:tot].cpu().view(torch.int16).numpy(), kr)
+    assert np.array_equal(vp[:tot].cpu().view(torch.int16).numpy(), vr)
+    if tot < cap:
+        assert bool((kp[tot:] == 7.0).all())
+
+
 def test_compact_capacity_overflow(C):
     L, H, T, d, page = 1, 2, 100, 128, 16
     mask = torch.ones(L, H, T, dtype=torch.uint8)

@@ -134,17 +134,18 @@ def test_c3_full_corners(mods):
     """c3 at full size: (layer 0, KV head 0) on every context key, and the far corner
     (last layer, last KV head) on its first and last 2048 keys, against the oracle;
     the per-layer threshold at the 25th percentile of the layer's non-window scores
-    over all 8 KV heads, then the masks and pages of both rows."""
+    over all 8 KV heads (selected on the GPU in the step, checked against the same
+    order statistic of the kernel's scores), then the masks and pages of both rows."""
     pipeline, W = mods
     wl = W.WORKLOADS["c3"]
     x = W.generate(wl, device="cuda")
     p = pipeline.make_pipeline(wl, x)
-    p.score_step()
+    p.step()
     torch.cuda.synchronize()
     g, T, w = wl.g, wl.T, wl.w
-    p.tau = [_layer_tau(p.score[l], T, w, wl.tau_quantile) for l in range(wl.L)]
-    p.prune_step()
-    torch.cuda.synchronize()
+    # the step selects tau on the GPU: exactly the quantile of the kernel's own scores
+    tau_gpu = p.tau_dev[: wl.L].cpu().tolist()
+    assert tau_gpu == [_layer_tau(p.score[l], T, w, wl.tau_quantile) for l in range(wl.L)]
     keys_far = np.r_[0:2048, T - 2048:T]
     for l, hk, keys in ((0, 0, None), (wl.L - 1, wl.H_kv - 1, keys_far)):
         vn, s = _c3_oracle_row(x, wl, l, hk, keys)
@@ -153,7 +154,7 @@ def test_c3_full_corners(mods):
         assert_close_rel(vg, vn, 1e-4, f"c3 vnorm (layer {l}, head {hk})")
         got = p.score[l:l + 1, hk:hk + 1].cpu().numpy()[..., cols]
         assert_close_abs(got, s, LOG_SCORE_ATOL, f"c3 log score (layer {l}, head {hk})")
-        tau = p.tau[l]
+        tau = tau_gpu[l]
         m_ref, _ = O.prune_threshold(s, tau, 0)
         pos = np.arange(T)[cols]
         m_ref[..., pos >= T - w] = 1  # the window (positions of the sampled keys)
