@@ -47,6 +47,12 @@ MUTATIONS = [
     ("topk ties to later tokens", "return np.lexsort((pos, key, nan))", "return np.lexsort((-pos, key, nan))"),
     ("topk nan ranks high", "key = np.where(nan, 0.0, -row)", "key = np.where(nan, -np.inf, -row)\n    nan = nan & False"),
     ("topk ignores window", "mask[r, T - wn:] = 1", "mask[r, T - wn:] = 0"),
+    ("chunked sum over chunks", "best = s if best is None else np.maximum(best, s)",
+     "best = s if best is None else best + s"),
+    ("chunked first chunk only", "best = s if best is None else np.maximum(best, s)",
+     "best = s if best is None else best"),
+    ("chunked last chunk only", "best = s if best is None else np.maximum(best, s)",
+     "best = s"),
     ("quantile upper rank", "s[int(math.floor(qtl * (s.size - 1)))]", "s[int(math.ceil(qtl * (s.size - 1)))]"),
     ("quantile nan ranks high", "s = np.concatenate([v[nan], np.sort(v[~nan])])", "s = np.sort(v)"),
     ("quantile over the window too", "tau[l] = quantile_lower(score[l, :, : T - wn], qtl)",

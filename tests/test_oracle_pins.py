@@ -193,6 +193,39 @@ def test_kvzip_chunked_is_max_over_chunks():
     assert np.array_equal(sc, per.max(axis=0))
 
 
+def test_kvzip_chunked_zero_queries_closed_form():
+    """q = 0: every visible key gets 1 / (number of keys the query sees).  Chunk c's
+    query j sees the T context keys, the chunk's tail before its block and the block up
+    to j: T + (tail_c - n) + j + 1 keys, so the score of a context key is the max over
+    chunks of 1 / (T + tail_c - n + 1): the chunk with the shortest tail decides.  With
+    constant value norms vn and hidden norms hn the KVzip+ score is that times vn / hn."""
+    L, Hq, Hkv, d, T, n = 1, 4, 2, 8, 13, 5
+    kc = rng.normal(size=(L, Hkv, T, d))
+    tails_len = (n + 3, n + 7, n + 2)          # prefix + carry + block; chunk 2 is shortest
+    qs = [np.zeros((L, Hq, n, d)) for _ in tails_len]
+    tails = [rng.normal(size=(L, Hkv, m, d)) for m in tails_len]
+    s = O.kvzip_score_chunked(qs, kc, tails, log=False)
+    assert np.allclose(s, 1.0 / (T + min(tails_len) - n + 1), rtol=0, atol=1e-14)
+    vn = np.full((L, Hq, T), 3.0)
+    hs = [np.full((L, n, 16), 0.5) for _ in tails_len]   # ||h_j|| = 0.5 * 4 = 2
+    s_plus = O.kvzip_score_chunked(qs, kc, tails, vnorm=vn, h_chunks=hs, log=False)
+    assert np.allclose(s_plus, s * 3.0 / 2.0, rtol=1e-13, atol=0)
+
+
+def test_kvzip_chunked_copy_in_one_chunk():
+    """A query of chunk 1 (one head of the group) that copies context key i with a large
+    gain gives s_i -> 1, whichever chunk it sits in; the other keys stay far below it."""
+    L, Hq, Hkv, d, T, n = 1, 2, 1, 16, 12, 4
+    kc = np.eye(d)[None, None, :T] * 1.0             # orthonormal context keys
+    tails = [np.zeros((L, Hkv, n + 2, d)) for _ in range(3)]
+    qs = [np.zeros((L, Hq, n, d)) for _ in range(3)]
+    qs[1][0, 1, 2] = 60.0 * np.sqrt(d) * kc[0, 0, 7]  # chunk 1, head 1, query 2 copies key 7
+    s = O.kvzip_score_chunked(qs, kc, tails, log=False)
+    assert s[0, 0, 7] > 1 - 1e-12
+    others = np.delete(s[0, 0], 7)
+    assert (others < 0.1).all()
+
+
 # ----------------------------------------------------------------------------- future mass
 
 def test_future_mass_zero_queries_harmonic():
