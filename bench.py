@@ -82,7 +82,7 @@ def parse_args():
                          "LSE-only pass")
     ap.add_argument("--refit", action="store_true",
                     help="c1/c2: add the closed-form value refit on the first budget's kept keys")
-    ap.add_argument("--e2e-groups", type=int, default=4,
+    ap.add_argument("--e2e-groups", type=int, default=12,
                     help="layer groups of the end-to-end run: copies of one group overlap the "
                          "kernels of the previous one (1: copy everything, then compute)")
     ap.add_argument("--e2e-copy-streams", type=int, default=1,

@@ -333,7 +333,7 @@ kvs_status kvs_prune_topk_multi(const kvs_dims* dims, const float* score, int32_
  *                                      kvs_compact_paged with page_size = k)
  *   v_fit  [L][H_kv][k][d]     fp32    output
  *   ws     scratch of kvs_value_refit_workspace_size() bytes
- * Requires k <= T and k <= 2048.
+ * Requires k <= T and k <= 8192.
  * ------------------------------------------------------------------------------- */
 size_t kvs_value_refit_workspace_size(const kvs_dims* dims, int32_t n_q, int32_t k);
 kvs_status kvs_value_refit(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,

@@ -77,7 +77,15 @@ struct Cfg {
   // quadratic form needs its rows' halves and keeps two
   static constexpr int NG = MODE == kQuad ? 2 : 4;
   static constexpr int COLS = BN / NG;
+  // The maximum and the future mass split the tiles between two pairs of groups: pair p
+  // takes the tiles of accumulator p (every other tile), each group of the pair 128 of
+  // the 256 columns in two chunks of 64, so the pairs run half a tile apart and one
+  // pair's TMEM loads overlap the other's arithmetic.  (The LSE pass measured slower
+  // that way: its rescaled online sum pays per chunk, and its accumulator is released
+  // later; it keeps every group on every tile.)
+  static constexpr bool PAIRED = MODE == kMax || MODE == kFuture;
   static constexpr int EPI = NG * kGroupThreads;
+  static constexpr int TEMPTY = PAIRED ? EPI / 2 : EPI;  // arrivals that release an accumulator
   static constexpr int THREADS = 64 + EPI;
   static constexpr int KH = D / 64;
   static constexpr int STAGES = D == 128 ? 2 : 4;  // B tiles in the ring
@@ -366,7 +374,7 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
     }
     for (int x = 0; x < 2; ++x) {
       tc::mbar_init(bar_tfull(x), 1);
-      tc::mbar_init(bar_tempty(x), C::EPI);
+      tc::mbar_init(bar_tempty(x), C::TEMPTY);
     }
     misc[1] = 0u;
     tc::fence_mbar_init();
@@ -559,8 +567,8 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
       float m = -1e30f, ssum = 0.f;                  // kLse
       float r = -CUDART_INF_F, tot = -CUDART_INF_F;  // kMax
       float lv = 0.f;                                // kMax: ln vnorm of the current head
+      int cur_head = -1;                             // kMax: head of r (-1: none yet)
       float f = 0.f;                                 // kFuture
-      if (MODE == kMax && U.ntiles > 0) lv = ln_vn(0);
 
       // kQuad: this thread's D/2 elements of its value row, from the swizzled A tile
       uint32_t vrow[MODE == kQuad ? D / 4 : 1];
@@ -590,6 +598,7 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
       for (int it = 0; it < U.ntiles && !bad; ++it, ++gt) {
         const int acc = gt & 1;
         const uint32_t aph = (uint32_t)(gt >> 1) & 1u;
+        if (C::PAIRED && acc != (h >> 1)) continue;  // the other pair's tile
         // a wait that runs out raises the CTA's abort flag, so every other thread leaves
         // at its next wait and all meet at the end-of-unit vote
         if (!tc::mbar_wait(bar_tfull(acc), aph) || *abort_flag) {
@@ -640,18 +649,36 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
             tc::fence_before_sync();
             tc::mbar_arrive(bar_tempty(acc));
           } else {
-            uint32_t v[COLS];
-#pragma unroll
-            for (int c = 0; c < COLS; c += 32) tc::tmem_ld32(ta + c, v + c);
-            tc::tmem_ld_wait();
-            tc::fence_before_sync();
-            tc::mbar_arrive(bar_tempty(acc));
-#pragma unroll
-            for (int c0 = 0; c0 < COLS; c0 += 64) {
-              uint32_t* w = v + c0;
+            if (MODE == kMax) {  // a new query head: fold the previous head's maximum
+              const int hd = it / U.per_head;
+              if (hd != cur_head) {
+                if (cur_head >= 0) tot = fmaxf(tot, r * scale + lv);
+                r = -CUDART_INF_F;
+                lv = ln_vn(it);
+                cur_head = hd;
+              }
+            }
+            // paired modes: this group's 128 columns in two chunks of 64; otherwise its 64
+            // columns in one chunk.  The accumulator is released once the last chunk is in
+            // registers.
+            constexpr int NCH = C::PAIRED ? 2 : 1;
+            const int cbase = C::PAIRED ? (h & 1) * 128 : h * COLS;
+            const uint32_t ta2 =
+                tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(acc * BN) + (uint32_t)cbase;
+#pragma unroll 1
+            for (int ch = 0; ch < NCH; ++ch) {
+              uint32_t w[64];
+              tc::tmem_ld32(ta2 + 64 * ch, w);
+              tc::tmem_ld32(ta2 + 64 * ch + 32, w + 32);
+              tc::tmem_ld_wait();
+              if (ch == NCH - 1) {
+                tc::fence_before_sync();
+                tc::mbar_arrive(bar_tempty(acc));
+              }
+              const int c0 = cbase + 64 * ch;  // first column of the chunk in the tile
               if (MODE == kLse) {
                 const bool ctx = it < U.n_ctx;
-                const int kb = (ctx ? it * BN : a.T + (it - U.n_ctx) * BN) + h * COLS + c0;
+                const int kb = (ctx ? it * BN : a.T + (it - U.n_ctx) * BN) + c0;
                 const int lim = ctx ? a.T : n_k;
                 if (kb >= lim || kb > off + ra) continue;  // no visible key in these 64
                 if (kb + 64 > lim || kb + 63 > off + ra) {
@@ -663,7 +690,7 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
               } else if (MODE == kMax) {
                 r = max_raw_cols(w, r);  // q.k / scale-units minus the column's constant
               } else {
-                const int j0 = (U.qt_begin + it % U.per_head) * BN + h * COLS + c0;
+                const int j0 = (U.qt_begin + it % U.per_head) * BN + c0;
                 const bool band = j0 < U.row0 + BM - 1 + a.w;
                 if (band) {
                   if (ra + a.w - j0 >= 64) continue;  // all 64 queries in the window
@@ -673,17 +700,13 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
                 }
               }
             }
-            if (MODE == kMax && (it + 1) % U.per_head == 0) {  // last query tile of this head
-              tot = fmaxf(tot, r * scale + lv);
-              r = -CUDART_INF_F;
-              if (it + 1 < U.ntiles) lv = ln_vn(it + 1);
-            }
           }
         }
       }
       // results of this unit: combine the groups' partial results of each row (kQuad:
       // the per-head partial dot products).  All groups vote on failure here, so they
       // leave the unit loop together and never wait at a barrier another has abandoned.
+      if (MODE == kMax && cur_head >= 0) tot = fmaxf(tot, r * scale + lv);
       float* xchg = xchg_all + (n & 1) * (NG - 1) * BM * 2;
       if (MODE != kQuad && MODE != kRows && h > 0 && !bad) {
         float* xg = xchg + (h - 1) * BM * 2;

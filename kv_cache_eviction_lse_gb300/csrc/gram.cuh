@@ -37,7 +37,7 @@ struct CholArgs {
 // Solves (G + lam I) X = R per problem, lam = lam_rel * trace(G[:k, :k]) / k, by a blocked
 // upper Cholesky factorisation in fp32 (one launch per step over all problems; R rides
 // along as extra columns) and one backward-solve launch.  M <= kCholMaxM.
-constexpr int kCholMaxM = 2048;
+constexpr int kCholMaxM = 8192;
 cudaError_t launch_chol_solve(const CholArgs& a, cudaStream_t s);
 cudaError_t chol_device_error(int* code, bool clear, cudaStream_t s);
 

@@ -136,7 +136,7 @@ def test_validation_codes_next_rows(capi):
                                1 << 30, None) == C.KVS_ERR_SHAPE
     assert lib.kvs_value_refit(by(dm), fake, 10, fake, fake, 100, fake, 50, -1.0, fake, fake,
                                1 << 30, None) == C.KVS_ERR_ARG
-    assert lib.kvs_value_refit(by(dm), fake, 10, fake, fake, 3000, fake, 2049, 1e-3, fake, fake,
+    assert lib.kvs_value_refit(by(dm), fake, 10, fake, fake, 9000, fake, 8193, 1e-3, fake, fake,
                                1 << 30, None) == C.KVS_ERR_UNSUPPORTED
     need = lib.kvs_value_refit_workspace_size(by(dm), 10, 100)
     # O bf16 [40][128], lse fp32 [40], A_S hi and lo bf16 [40][128], Gram fp32 [2][128][128],

@@ -628,7 +628,8 @@ REFIT_SHAPES = [
     (1, 1, 3, 128, 520, 257, 1),      # a single kept key
     (1, 2, 2, 128, 700, 300, 333),    # several 128-row tiles of the Gram matrix
     (1, 1, 2, 128, 1600, 300, 1500),  # 24 Cholesky panels, more kept keys than rows
-    (1, 1, 2, 64, 2100, 150, 2048),   # the largest supported k (32 panels)
+    (1, 1, 2, 64, 2100, 150, 2048),   # 32 panels
+    (1, 2, 4, 128, 4400, 160, 4224),  # c4's 25 % budget plus its window (66 panels)
     # many problems: on 152 SMs the triangular solves take right-hand-side blocks of 32,
     # then 64 columns (16 above)
     (2, 40, 40, 64, 200, 70, 150),
