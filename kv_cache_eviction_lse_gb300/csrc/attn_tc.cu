@@ -89,12 +89,13 @@ struct Cfg {
   static constexpr int THREADS = 64 + EPI;
   static constexpr int KH = D / 64;
   static constexpr int STAGES = D == 128 ? 2 : 4;  // B tiles in the ring
-  // Ring slots per B tile.  The key-side maximum (light epilogue, MMA-bound) hands the
+  // Ring slots per B tile.  The key-side passes (the maximum and the future mass) hand the
   // ring out by box (64 columns of d): a tile's first box is refilled while the MMAs read
-  // its second, so the loads lead the MMAs by 1.5 tiles at d = 128 instead of one.  The
-  // other modes keep whole-tile slots: their epilogues bound them and the extra barrier
-  // traffic of box slots costs them more than the deeper lead gains.
-  static constexpr int PARTS = MODE == kMax ? KH : 1;
+  // its second, so the loads lead the MMAs by 1.5 tiles at d = 128 instead of one (the
+  // future mass ran 4 % faster on c4 that way).  The other modes keep whole-tile slots:
+  // their epilogues bound them and the extra barrier traffic of box slots costs them more
+  // than the deeper lead gains (the LSE pass measured 2.5 % slower with box slots).
+  static constexpr int PARTS = (MODE == kMax || MODE == kFuture) ? KH : 1;
   static constexpr int NS = STAGES * PARTS;
   static constexpr uint32_t SLOT_BYTES = KH / PARTS * kBoxBytesB;
   static constexpr uint32_t A_BYTES = KH * kBoxBytesA;  // one of kABufs A buffers
