@@ -324,9 +324,10 @@ kvs_status kvs_prune_topk_multi(const kvs_dims* dims, const float* score, int32_
  *   v_fit = argmin ||A_S V - O||^2 + lam ||V||^2 = (A_S^T A_S + lam I)^-1 A_S^T O
  *   lam = lambda_rel * mean of the diagonal of A_S^T A_S
  *
- * O comes from the attention forward (bf16), A_S is formed on the tensor cores and
- * kept as bf16 hi + lo parts so that the Gram matrix and the right-hand side carry
- * ~2^-16 relative error; the ridge system is solved by an fp32 Cholesky factorisation.
+ * O comes from the attention forward and A_S from the tensor cores, both kept in fp16
+ * (weights in [0, 1] and attention outputs: 2^-12 relative each), so that the Gram
+ * matrix and the right-hand side, accumulated in fp32 on the tensor cores, carry
+ * ~2^-11 relative error; the ridge system is solved by an fp32 Cholesky factorisation.
  *
  *   q      [L][H_q][n_q][d]    bf16    k_ctx, v_ctx [L][H_kv][T][d] bf16
  *   k_kept [L][H_kv][k][d]     bf16    the kept keys in position order (for instance

@@ -412,7 +412,7 @@ kvs_status kvs_decode_step(const kvs_dims* dims, int32_t B, int32_t w, int32_t* 
 namespace {
 struct RefitPlan {
   int g, rows, k_ld;
-  size_t off_o, off_lse, off_ahi, off_alo, off_g, off_r, total;
+  size_t off_o, off_lse, off_a, off_g, off_r, total;
 };
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 RefitPlan refit_plan(const kvs_dims* dm, int n_q, int k) {
@@ -424,8 +424,7 @@ RefitPlan refit_plan(const kvs_dims* dm, int n_q, int k) {
   size_t o = 0;
   p.off_o = o;   o = align256(o + nq_all * dm->d * 2);
   p.off_lse = o; o = align256(o + nq_all * 4);
-  p.off_ahi = o; o = align256(o + nq_all * p.k_ld * 2);
-  p.off_alo = o; o = align256(o + nq_all * p.k_ld * 2);
+  p.off_a = o;   o = align256(o + nq_all * p.k_ld * 2);
   p.off_g = o;   o = align256(o + batch * p.k_ld * p.k_ld * 4);
   p.off_r = o;   o = align256(o + batch * p.k_ld * dm->d * 4);
   p.total = o;
@@ -467,8 +466,7 @@ kvs_status kvs_value_refit(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
   uint8_t* w = static_cast<uint8_t*>(ws);
   auto* o_ws = reinterpret_cast<kvs::bf16_t*>(w + pl.off_o);
   auto* lse_ws = reinterpret_cast<float*>(w + pl.off_lse);
-  auto* ahi = reinterpret_cast<kvs::bf16_t*>(w + pl.off_ahi);
-  auto* alo = reinterpret_cast<kvs::bf16_t*>(w + pl.off_alo);
+  auto* a_s = reinterpret_cast<uint16_t*>(w + pl.off_a);  // fp16 softmax rows
   auto* gm = reinterpret_cast<float*>(w + pl.off_g);
   auto* rm = reinterpret_cast<float*>(w + pl.off_r);
   cudaStream_t s = as_stream(stream);
@@ -476,18 +474,19 @@ kvs_status kvs_value_refit(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
   // 1. target: attention output of every scoring query over the whole context
   kvs::FwdArgs f;
   f.q = q; f.k_ctx = k_ctx; f.v_ctx = v_ctx; f.o = o_ws; f.lse = lse_ws;
-  f.L = L; f.Hq = Hq; f.Hkv = Hkv; f.d = d; f.n_q = n_q; f.T = T; f.causal = 0;
+  f.L = L; f.Hq = Hq; f.Hkv = Hkv; f.d = d; f.n_q = n_q; f.T = T; f.causal = 0; f.o_f16 = 1;
   cudaError_t e = kvs::launch_attn_fwd(f, s);
-  // 2. softmax rows over the kept keys: their LSE, then the rows as bf16 hi + lo
+  // 2. softmax rows over the kept keys: their LSE, then the rows as fp16
   kvs::AttnArgs r;
   r.q = q; r.k_ctx = k_kept; r.lse = lse_ws; r.out = lse_ws;
   r.L = L; r.Hq = Hq; r.Hkv = Hkv; r.d = d; r.n_q = n_q; r.T = k; r.causal = 0;
-  r.rows_hi = ahi; r.rows_lo = alo; r.rows_ld = pl.k_ld;
+  r.rows = a_s; r.rows_ld = pl.k_ld;
   if (e == cudaSuccess) e = kvs::launch_lse(r, s);
   if (e == cudaSuccess) e = kvs::launch_softmax_rows(r, s);
   // 3. normal equations: Gram (upper block triangle) and right-hand side
   kvs::GramArgs gg;
-  gg.x_hi = ahi; gg.x_lo = alo; gg.y_hi = ahi; gg.y_lo = alo; gg.c = gm;
+  const auto* a16 = reinterpret_cast<const kvs::bf16_t*>(a_s);  // 16-bit words (fp16)
+  gg.x_hi = a16; gg.y_hi = a16; gg.c = gm; gg.f16 = 1;
   gg.batch = L * Hkv; gg.rows = pl.rows; gg.M = gg.N = pl.k_ld;
   gg.ldx = gg.ldy = gg.ldc = pl.k_ld; gg.upper = 1;
   if (e == cudaSuccess) e = kvs::launch_gram(gg, s);

@@ -21,8 +21,7 @@ struct AttnArgs {
   int L = 0, Hq = 0, Hkv = 0, d = 0, n_q = 0, T = 0, n_tail = 0;
   int w = 0, accumulate = 0;
   int causal = 1;                  // 0: every query sees every key (internal callers)
-  bf16_t* rows_hi = nullptr;       // softmax rows: [L][Hq][n_q][rows_ld] bf16 hi / lo parts
-  bf16_t* rows_lo = nullptr;
+  uint16_t* rows = nullptr;        // softmax rows: [L][Hq][n_q][rows_ld] fp16
   int rows_ld = 0;                 // padded row length (multiple of 64, >= T)
   // KVzip max (pass 2): per-query constants -(lse_j + ln||h_j||) / sqrt(d), split into
   // three bf16 parts [L][Hq][n_q_pad][16] (n_q_pad = n_q rounded up to 256; padding rows
@@ -40,7 +39,7 @@ cudaError_t launch_score_constants(const float* lse, int L, int Hq, int n_q,
 
 cudaError_t launch_lse(const AttnArgs& a, cudaStream_t s);
 // Softmax rows a_ji = exp(x_ji - lse_j) over the T context keys (lse given), written as
-// bf16 hi/lo parts into rows_hi / rows_lo (zero past T up to rows_ld); no tail keys.
+// fp16 into rows (zero past T up to rows_ld); no tail keys.
 cudaError_t launch_softmax_rows(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_score_max(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_future_sum(const AttnArgs& a, cudaStream_t s);
@@ -55,7 +54,8 @@ struct FwdArgs {
   const bf16_t* v_ctx = nullptr;   // [L][Hkv][T][d]
   const bf16_t* k_tail = nullptr;  // [L][Hkv][n_tail][d]
   const bf16_t* v_tail = nullptr;  // [L][Hkv][n_tail][d]
-  bf16_t* o = nullptr;             // [L][Hq][n_q][d]
+  bf16_t* o = nullptr;             // [L][Hq][n_q][d], bf16 (fp16 when o_f16)
+  int o_f16 = 0;                   // write O as fp16 (the value refit's target)
   float* lse = nullptr;            // [L][Hq][n_q]
   int L = 0, Hq = 0, Hkv = 0, d = 0, n_q = 0, T = 0, n_tail = 0;
   int causal = 1;                  // 0: every query sees every key (internal callers)

@@ -24,6 +24,7 @@
 // The epilogue divides O by the row sum, writes it as bf16 and writes the LSE.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 #include <math_constants.h>
 
@@ -79,6 +80,10 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 p = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&p);
@@ -389,9 +394,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_ld16(t_o + lane_off + (uint32_t)(h * OC), v);
         }
         tc::tmem_ld_wait();
+        if (a.o_f16) {
 #pragma unroll
-        for (int c = 0; c < OC; c += 2)
-          ob[c / 2] = pack_bf16(__uint_as_float(v[c]) * inv, __uint_as_float(v[c + 1]) * inv);
+          for (int c = 0; c < OC; c += 2)
+            ob[c / 2] = pack_f16(__uint_as_float(v[c]) * inv, __uint_as_float(v[c + 1]) * inv);
+        } else {
+#pragma unroll
+          for (int c = 0; c < OC; c += 2)
+            ob[c / 2] = pack_bf16(__uint_as_float(v[c]) * inv, __uint_as_float(v[c + 1]) * inv);
+        }
         if (qr < a.n_q) {
           uint4* dst = reinterpret_cast<uint4*>(
               a.o + ((size_t)(l * a.Hq + hq) * a.n_q + qr) * D + h * OC);

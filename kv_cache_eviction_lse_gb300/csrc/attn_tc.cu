@@ -32,13 +32,14 @@
 //   kQuad    A = values, B = the head's Gram pair [G_hi | G_lo]: v^T G v per key and
 //            query head of the group (the value norms)
 //   kRows    A = queries, B = kept keys: the softmax rows 2^(x log2 e - lse_j log2 e) as
-//            bf16 hi + lo parts, written through a per-warp stage (value refit)
+//            fp16, written through a per-warp stage (value refit)
 // Sources: KVpop review, 1. Key Terms (LSE reuse, transposed-attention pass);
 // KVzap review, 3.1 Eq. 1 and 3.2 Eq. 3.
 #include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math_constants.h>
 
 #include "attn.cuh"
@@ -212,62 +213,52 @@ __device__ __forceinline__ float future_cols(const uint32_t* v, float sc2, int j
   return a0.x + a0.y;
 }
 
-__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
-  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+__device__ __forceinline__ uint32_t pack2_f16(float lo, float hi) {
+  __half2 p = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
 // Softmax weights of 32 columns (keys kb .. kb+31) of the warp's 32 query rows, written
-// as bf16 hi and lo parts (p = hi + lo to ~2^-17): p = 2^(x sc2 - l2), 0 for keys >= lim.
-// Each thread computes its own row; the rows then pass through the warp's 2 KB stage (32
-// rows x 64 bytes), so every store instruction writes eight whole 64-byte row segments
-// (a thread writing 16 bytes into each of 32 rows would make 32 transactions).
-// row_base = element offset of the warp's first row (row stride ld); rows at or past
-// nvalid (from the warp's first row) and columns at or past ld are not written.
+// as fp16 (weights in [0, 1]: 11 significant bits, 2^-12 relative): p = 2^(x sc2 - l2),
+// 0 for keys >= lim.  Each thread computes its own row; the rows then pass through the
+// warp's 2 KB stage (32 rows x 64 bytes), so every store instruction writes eight whole
+// 64-byte row segments (a thread writing 16 bytes into each of 32 rows would make 32
+// transactions).  row_base = element offset of the warp's first row (row stride ld);
+// rows at or past nvalid (from the warp's first row) and columns at or past ld are not
+// written.
 __device__ __forceinline__ void rows_cols(const uint32_t* v, int kb, int lim, float l2, float sc2,
-                                          bf16_t* hi, bf16_t* lo, size_t row_base, int ld,
-                                          int nvalid, uint8_t* stage, int lane) {
+                                          uint16_t* rows, size_t row_base, int ld, int nvalid,
+                                          uint8_t* stage, int lane) {
   if (kb >= ld) return;  // warp-uniform: ld is a multiple of 64, kb of 32
   const uint32_t sbase = smem_u32(stage);
-  {
-    float pv[32];
+  float pv[32];
 #pragma unroll
-    for (int c = 0; c < 32; ++c)
-      pv[c] = (kb + c < lim) ? fast_exp2(fmaf(__uint_as_float(v[c]), sc2, -l2)) : 0.f;
+  for (int c = 0; c < 32; ++c)
+    pv[c] = (kb + c < lim) ? fast_exp2(fmaf(__uint_as_float(v[c]), sc2, -l2)) : 0.f;
+  // this row's 64 bytes into the stage, 16-byte chunk j at position j ^ (row & 3)
 #pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      // this row's 64 bytes into the stage, 16-byte chunk j at position j ^ (row & 3)
+  for (int j = 0; j < 4; ++j) {
+    uint32_t w4[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t w4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = pv[8 * j + 2 * e], p1 = pv[8 * j + 2 * e + 1];
-          const uint32_t h = pack2_bf16(p0, p1);
-          w4[e] = part ? pack2_bf16(p0 - __uint_as_float(h << 16),
-                                    p1 - __uint_as_float(h & 0xffff0000u))
-                       : h;
-        }
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
-                         sbase + (uint32_t)(lane * 64 + ((j ^ (lane & 3)) << 4))),
-                     "r"(w4[0]), "r"(w4[1]), "r"(w4[2]), "r"(w4[3])
-                     : "memory");
-      }
-      __syncwarp();
-      bf16_t* out = (part ? lo : hi) + row_base + kb;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {  // lanes 4i..4i+3 write row 8q + i, 16 bytes each
-        const int r = 8 * q + (lane >> 2), j = lane & 3;
-        uint4 u;
-        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
-                     : "r"(sbase + (uint32_t)(r * 64 + ((j ^ (r & 3)) << 4)))
-                     : "memory");
-        if (r < nvalid) *reinterpret_cast<uint4*>(out + (size_t)r * ld + 8 * j) = u;
-      }
-      __syncwarp();
-    }
+    for (int e = 0; e < 4; ++e) w4[e] = pack2_f16(pv[8 * j + 2 * e], pv[8 * j + 2 * e + 1]);
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                     sbase + (uint32_t)(lane * 64 + ((j ^ (lane & 3)) << 4))),
+                 "r"(w4[0]), "r"(w4[1]), "r"(w4[2]), "r"(w4[3])
+                 : "memory");
   }
+  __syncwarp();
+  uint16_t* out = rows + row_base + kb;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {  // lanes 4i..4i+3 write row 8q + i, 16 bytes each
+    const int r = 8 * q + (lane >> 2), j = lane & 3;
+    uint4 u;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+                 : "r"(sbase + (uint32_t)(r * 64 + ((j ^ (r & 3)) << 4)))
+                 : "memory");
+    if (r < nvalid) *reinterpret_cast<uint4*>(out + (size_t)r * ld + 8 * j) = u;
+  }
+  __syncwarp();
 }
 
 // B-tile space of the 128-row unit starting at row0.
@@ -643,7 +634,7 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
               uint32_t v32[32];
               tc::tmem_ld32(ta + c, v32);
               tc::tmem_ld_wait();
-              rows_cols(v32, it * BN + h * COLS + c, a.T, l2row, sc2, a.rows_hi, a.rows_lo,
+              rows_cols(v32, it * BN + h * COLS + c, a.T, l2row, sc2, a.rows,
                         rows_base, a.rows_ld, a.n_q - warp_row0,
                         smem + C::OFF_X + (warp - 2) * C::ROWS_STAGE, lane);
             }

@@ -1,5 +1,8 @@
 // Launchers of the value refit's linear algebra: the batched X^T Y products on the
 // tensor cores and the per-problem Cholesky solve of the ridge normal equations.
+// The refit's products run on fp16 operands (softmax weights in [0, 1] and the attention
+// output, 2^-12 relative each) with fp32 accumulation; the value-norm Gram of o_proj
+// runs on bf16 with its result split into bf16 hi/lo pairs.
 #pragma once
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -16,6 +19,7 @@ struct GramArgs {
   float* c = nullptr;            // [batch][M][ldc]
   int batch = 0, rows = 0, M = 0, N = 0, ldx = 0, ldy = 0, ldc = 0;
   int upper = 0;                 // Y == X: write only the upper block triangle (M == N)
+  int f16 = 0;                   // operands are fp16 (else bf16); parts and layouts as above
   // Y == X, diagonal d x d blocks only (the Gram matrix of each d-column slice of X):
   // written as bf16 pairs pair[batch][M / d][2][d][d] (hi rows, then lo = bf16(G - hi))
   // instead of into c

@@ -1,7 +1,8 @@
-// Batched C = X^T Y with fp32-level accuracy from bf16 tensor cores (tcgen05 + TMEM + TMA),
-// for the normal equations of the value refit: X = the softmax rows A_S of the kept keys
-// ([rows][M], split as hi + lo bf16 parts), Y = A_S itself (Gram matrix, upper block
-// triangle only) or the attention output O ([rows][N], one bf16 part).
+// Batched C = X^T Y on the tensor cores (tcgen05 + TMEM + TMA), fp32 accumulation, bf16 or
+// fp16 operands, each optionally split into hi + lo parts: for the normal equations of
+// the value refit X = the fp16 softmax rows A_S of the kept keys ([rows][M]), Y = A_S
+// itself (Gram matrix, upper block triangle only) or the fp16 attention output O
+// ([rows][N]); for the value norms the diagonal d x d blocks of o_proj^T o_proj (bf16).
 //
 //   C[b][m][n] = sum_r X[b][r][m] Y[b][r][n]
 //             ~= sum_r Xhi Yhi + Xhi Ylo + Xlo Yhi   (Y split)    or   Xhi Y + Xlo Y
@@ -144,7 +145,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = tc::idesc_bf16_bmn(BT, BT) | (1u << 15);  // A and B MN-major
+      // A and B MN-major; the A and B format fields (bits 7-9, 10-12) say bf16 (1) or fp16 (0)
+      const uint32_t idesc = (tc::idesc_bf16_bmn(BT, BT) | (1u << 15)) &
+                             (a.f16 ? ~((1u << 7) | (1u << 10)) : ~0u);
       int kb = 0;
       bool ok = true;
       for (; kb < nkb; ++kb) {

@@ -645,9 +645,10 @@ def _refit_objective(A, Ot, lam, V):
 def test_value_refit(C, shape):
     """The refit reaches the oracle's ridge optimum: the objective of the GPU solution,
     evaluated in fp64 with the oracle's A_S, O and lam, exceeds the optimum by at most
-    2^-16 ||O||^2.  The GPU's O is bf16 (relative 2^-9, so ||dO||^2 <= 2^-18 ||O||^2,
-    and a least-squares solution moves the objective by at most ||dO||^2); the hi/lo
-    Gram and the fp32 Cholesky add far less.  Four times that bound."""
+    2^-16 ||O||^2.  The GPU keeps O and A_S in fp16 (relative 2^-12 each, so ||dO||^2 <=
+    2^-22 ||O||^2, and a least-squares solution moves the objective by at most ||dO||^2;
+    the rounding of A_S moves it by the same order), and the fp32 Cholesky adds far less:
+    the bound leaves a factor of 64."""
     L, Hkv, Hq, d, T, nq, k = shape
     lam_rel = 1e-3
     x = _inputs(L, Hkv, Hq, d, T, 0, nq, seed=T + k)
