@@ -139,9 +139,9 @@ def test_validation_codes_next_rows(capi):
     assert lib.kvs_value_refit(by(dm), fake, 10, fake, fake, 9000, fake, 8193, 1e-3, fake, fake,
                                1 << 30, None) == C.KVS_ERR_UNSUPPORTED
     need = lib.kvs_value_refit_workspace_size(by(dm), 10, 100)
-    # O bf16 [40][128], lse fp32 [40], A_S hi and lo bf16 [40][128], Gram fp32 [2][128][128],
+    # O fp16 [40][128], lse fp32 [40], A_S fp16 [40][128], Gram fp32 [2][128][128],
     # right-hand sides fp32 [2][128][128], each rounded up to 256 bytes
-    assert need == 10240 + 256 + 10240 + 10240 + 131072 + 131072
+    assert need == 10240 + 256 + 10240 + 131072 + 131072
     assert lib.kvs_value_refit(by(dm), fake, 10, fake, fake, 200, fake, 100, 1e-3, fake, fake,
                                need - 1, None) == C.KVS_ERR_CAPACITY
     assert lib.kvs_value_refit(by(dm), None, 0, None, None, 200, None, 100, 1e-3, None, None, 0,
