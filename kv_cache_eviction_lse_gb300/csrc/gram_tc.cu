@@ -240,11 +240,197 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ wide tiles (refit)
+//
+// C = X^T Y for single-part fp16 operands (the value refit's Gram matrix and right-hand
+// side): one CTA per 256 x WN output block (WN = 256, or 128 when N <= 128), its two
+// 128-row halves in two TMEM accumulators of WN columns.  Per 64-row k-block the CTA
+// loads X (64 x 256) and Y (64 x WN) and issues 2 x 4 MMAs of 128 x WN x 16, so a byte of
+// operand feeds twice the flops of a 128 x 128 tile: the refit's products stream their
+// operands from L2, and that is what bounds them.
+constexpr int WM = 256;                    // output rows per CTA (two MMA halves)
+constexpr int kWideThreads = 64 + 256;     // producer, MMA issuer, 8 epilogue warps
+constexpr int kWideStages = 3;             // 64 KB per stage (X and Y tiles)
+constexpr uint32_t kWideStage = 8 * kBox;  // X: 4 boxes, Y: up to 4 boxes
+constexpr uint32_t kWideSmem = OFF_RING + kWideStages * kWideStage + 1024;
+static_assert(kWideSmem <= 232448, "shared-memory plan exceeds the per-block limit");
+
+template <int WN>
+__global__ void __launch_bounds__(kWideThreads, 1)
+    gram_wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
+                     const GramArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  if (pad + OFF_RING + kWideStages * kWideStage > kWideSmem) {
+    if (threadIdx.x == 0) atomicCAS(&g_gram_error, 0, kErrSmemAlign);
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sb = raw + pad;
+  const uint32_t bar0 = sb + OFF_BAR;
+  auto bar_full = [&](int s) { return bar0 + 8u * s; };
+  auto bar_empty = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
+  const uint32_t bar_done = bar0 + 8u * (2 * kMaxStages);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  constexpr uint32_t kCols = 2 * WN;       // TMEM columns: two accumulators
+  constexpr uint32_t kY = 4 * kBox;        // Y tile offset within a stage
+  constexpr uint32_t kBytes = 4 * kBox + (WN / 64) * kBox;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int tm, tn;
+  if (a.upper) {  // the upper block triangle of WM x WN blocks (WN == WM here)
+    int t = blockIdx.x, row = 0;
+    const int nt = (a.M + WM - 1) / WM;
+    while (t >= nt - row) {
+      t -= nt - row;
+      ++row;
+    }
+    tm = row;
+    tn = row + t;
+  } else {
+    const int ntn = (a.N + WN - 1) / WN;
+    tm = blockIdx.x / ntn;
+    tn = blockIdx.x % ntn;
+  }
+  const int b = blockIdx.y;
+  const int nkb = (a.rows + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kWideStages; ++s) {
+      tc::mbar_init(bar_full(s), 1);
+      tc::mbar_init(bar_empty(s), 1);
+    }
+    tc::mbar_init(bar_done, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(sb + OFF_MISC, kCols);
+    tc::tmem_relinquish();
+  }
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = misc[0];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int kb = 0;
+      bool ok = true;
+      for (; kb < nkb; ++kb) {
+        const int s = kb % kWideStages;
+        if (!tc::mbar_wait(bar_empty(s), ((kb / kWideStages) & 1) ^ 1u)) {
+          ok = false;
+          break;
+        }
+        const uint32_t st = sb + OFF_RING + s * kWideStage;
+        tc::mbar_expect_tx(bar_full(s), kBytes);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)  // X: columns tm*256 .. +255, four 64-column boxes
+          tc::tma_load_3d(st + c * kBox, &tm_x, bar_full(s), tm * WM + 64 * c, kb * BK, b);
+#pragma unroll
+        for (int c = 0; c < WN / 64; ++c)
+          tc::tma_load_3d(st + kY + c * kBox, &tm_y, bar_full(s), tn * WN + 64 * c, kb * BK, b);
+      }
+      if (!ok) {
+        atomicCAS(&g_gram_error, 0, kErrWaitTimeout);
+        for (int j = max(0, kb - kWideStages); j < kb; ++j)
+          tc::mbar_wait(bar_full(j % kWideStages), (j / kWideStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // A and B MN-major, fp16 (format fields 0)
+      constexpr uint32_t idesc =
+          (tc::idesc_bf16_bmn(128, WN) | (1u << 15)) & ~((1u << 7) | (1u << 10));
+      int kb = 0;
+      bool ok = true;
+      for (; kb < nkb; ++kb) {
+        const int s = kb % kWideStages;
+        if (!tc::mbar_wait(bar_full(s), (kb / kWideStages) & 1)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t st = sb + OFF_RING + s * kWideStage;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          const uint32_t o = 2048u * k;  // 16 rows of 128 bytes
+          const uint64_t yd = tc::sdesc_sw128_mn(st + kY + o, kBox);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+            tc::mma_bf16(tmem + (uint32_t)(hh * WN), tc::sdesc_sw128_mn(st + 2 * hh * kBox + o, kBox),
+                         yd, idesc, (kb | k) != 0 ? 1u : 0u);
+        }
+        tc::commit(bar_empty(s));
+      }
+      if (!ok) atomicCAS(&g_gram_error, 0, kErrWaitTimeout);
+      tc::commit(bar_done);
+      tc::mbar_wait(bar_done, 0);
+    }
+    __syncwarp();
+  } else {
+    // epilogue: warp w reads TMEM lanes 32 (w % 4) .. of accumulator hh = (w - 2) / 4
+    const int eq = warp & 3, hh = (warp - 2) >> 2;
+    const int m = tm * WM + hh * 128 + eq * 32 + lane;
+    const bool ok = tc::mbar_wait(bar_done, 0);
+    if (!ok) atomicCAS(&g_gram_error, 0, kErrWaitTimeout);
+    tc::fence_after_sync();
+    float* crow = a.c + ((size_t)b * a.M + m) * a.ldc + tn * WN;
+    const int nmax = min(WN, a.N - tn * WN);
+    const uint32_t t0 = tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(hh * WN);
+#pragma unroll
+    for (int cb = 0; cb < WN / 32; ++cb) {
+      uint32_t v[32];
+      tc::tmem_ld32(t0 + 32u * cb, v);
+      tc::tmem_ld_wait();
+      if (ok && m < a.M) {
+        if (32 * cb + 32 <= nmax) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 4)
+            *reinterpret_cast<float4*>(crow + 32 * cb + c) =
+                make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]),
+                            __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+        } else {
+          for (int c = 0; c < 32 && 32 * cb + c < nmax; ++c) crow[32 * cb + c] = __uint_as_float(v[c]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kCols);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_gram(const GramArgs& a, cudaStream_t s) {
   if (a.M <= 0 || a.N <= 0 || a.batch <= 0) return cudaSuccess;
   const bool diag = a.pair != nullptr;
+  if (a.f16 && !diag && !a.x_lo && !a.y_lo) {  // the refit's single-part fp16 products
+    if (a.upper && a.M != a.N) return cudaErrorInvalidValue;
+    if (a.ldx % 8 || a.ldy % 8 || a.ldc % 4) return cudaErrorInvalidValue;
+    CUtensorMap x, y;
+    cudaError_t e = tma_map_bf16_3d(&x, a.x_hi, a.ldx, a.rows, a.batch, BK);
+    if (e == cudaSuccess) e = tma_map_bf16_3d(&y, a.y_hi, a.ldy, a.rows, a.batch, BK);
+    if (e != cudaSuccess) return e;
+    const int tmn = (a.M + WM - 1) / WM;
+    count_launches(1);
+    if (a.N > 128 || a.upper) {
+      auto kern = gram_wide_kernel<256>;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWideSmem);
+      if (e != cudaSuccess) return e;
+      const int tiles = a.upper ? tmn * (tmn + 1) / 2 : tmn * ((a.N + 255) / 256);
+      kern<<<dim3(tiles, a.batch), kWideThreads, kWideSmem, s>>>(x, y, a);
+    } else {
+      auto kern = gram_wide_kernel<128>;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWideSmem);
+      if (e != cudaSuccess) return e;
+      kern<<<dim3(tmn, a.batch), kWideThreads, kWideSmem, s>>>(x, y, a);
+    }
+    return cudaGetLastError();
+  }
   if ((a.upper || diag) && a.M != a.N) return cudaErrorInvalidValue;
   if (diag && (a.pair_d <= 0 || BT % a.pair_d || a.M % a.pair_d || a.pair_d % 8))
     return cudaErrorInvalidValue;
