@@ -197,23 +197,25 @@ def test_c4_full_corners(mods):
             _check_pages(pg, l, hk, x["k"][l, hk].cpu(), x["v"][l, hk].cpu(), m[l, hk].cpu().numpy())
 
 
-def test_c5_full_layer0(mods):
+def test_c5_full_first_and_last_layer(mods):
     pipeline, W = mods
     wl = W.WORKLOADS["c5"]
     x = W.generate(wl, device="cuda")
     p = pipeline.make_pipeline(wl, x)
     p.step()
     torch.cuda.synchronize()
-    z = O.linear_surrogate(f64(x["h"][0:1]), f64(x["W"][0:1]), x["b"][0:1].double().cpu().numpy())
-    zg = p.score[0:1].cpu().numpy()
-    assert_close_abs(zg, z, LOG_SCORE_ATOL, "c5 surrogate")
-    m_ref, _ = O.prune_threshold(z, wl.tau, wl.w)
-    mg = p.mask[0:1].cpu().numpy()
-    assert_masks_match_near(mg, m_ref, z, np.full(z.shape[:-1], wl.tau), MASK_BAND, "c5 mask",
-                            log_domain=True)
-    assert np.array_equal(p.keep[0:1].cpu().numpy(), mg.sum(-1))
-    for h in range(wl.H_kv):
-        _check_pages(p.pages, 0, h, x["k"][0, h].cpu(), x["v"][0, h].cpu(), mg[0, h])
+    for l in (0, wl.L - 1):
+        sl = slice(l, l + 1)
+        z = O.linear_surrogate(f64(x["h"][sl]), f64(x["W"][sl]), x["b"][sl].double().cpu().numpy())
+        zg = p.score[sl].cpu().numpy()
+        assert_close_abs(zg, z, LOG_SCORE_ATOL, f"c5 surrogate (layer {l})")
+        m_ref, _ = O.prune_threshold(z, wl.tau, wl.w)
+        mg = p.mask[sl].cpu().numpy()
+        assert_masks_match_near(mg, m_ref, z, np.full(z.shape[:-1], wl.tau), MASK_BAND,
+                                f"c5 mask (layer {l})", log_domain=True)
+        assert np.array_equal(p.keep[sl].cpu().numpy(), mg.sum(-1))
+        for h in range(wl.H_kv):
+            _check_pages(p.pages, l, h, x["k"][l, h].cpu(), x["v"][l, h].cpu(), mg[0, h])
     # the page plan covers every layer: offsets are the prefix sum of ceil(keep/16)
     sl = p.pages.seq_lens.cpu().numpy().ravel()
     first = p.pages.block_table[:, :, 0].cpu().numpy().ravel()
@@ -222,7 +224,10 @@ def test_c5_full_layer0(mods):
     assert int(p.pages.needed.item()) == int(npg.sum())
 
 
-def test_c6_full_layer0_sampled(mods):
+def test_c6_full_sampled(mods):
+    """c6: the MLP surrogate of layers 0 and 35 on their first and last 4096 tokens
+    against the oracle; each layer's whole mask against the threshold rule applied to the
+    kernel's own scores; pages bit-exact."""
     pipeline, W = mods
     wl = W.WORKLOADS["c6"]
     x = W.generate(wl, device="cuda")
@@ -230,22 +235,25 @@ def test_c6_full_layer0_sampled(mods):
     p.step()
     torch.cuda.synchronize()
     rows = np.r_[0:4096, wl.T - 4096:wl.T]
-    z = O.mlp_surrogate(f64(x["h"][0:1, rows]), f64(x["W1"][0:1]), x["b1"][0:1].double().cpu().numpy(),
-                        f64(x["W2"][0:1]), x["b2"][0:1].double().cpu().numpy())
-    zg = p.score[0:1].cpu().numpy()
-    assert_close_abs(zg[..., rows], z, LOG_SCORE_ATOL, "c6 MLP surrogate (layer 0, sampled tokens)")
-    mg = p.mask[0:1].cpu().numpy()
-    # the threshold rule applied to the kernel's own fp32 scores, over the whole layer
-    m_same, _ = O.prune_threshold(zg.astype(np.float64), np.float32(wl.tau), wl.w)
-    assert np.array_equal(mg, m_same)
-    # and the oracle's decision on the sampled tokens, except next to tau
-    m_ref, _ = O.prune_threshold(z, wl.tau, 0)
-    m_ref[..., rows >= wl.T - wl.w] = 1
-    assert_masks_match_near(mg[..., rows], m_ref, z, np.full(z.shape[:-1], wl.tau), MASK_BAND,
-                            "c6 mask (sampled tokens)", log_domain=True)
-    assert np.array_equal(p.keep[0:1].cpu().numpy(), mg.sum(-1))
-    for h in range(wl.H_kv):
-        _check_pages(p.pages, 0, h, x["k"][0, h].cpu(), x["v"][0, h].cpu(), mg[0, h])
+    for l in (0, wl.L - 1):
+        sl = slice(l, l + 1)
+        z = O.mlp_surrogate(f64(x["h"][sl, rows]), f64(x["W1"][sl]), x["b1"][sl].double().cpu().numpy(),
+                            f64(x["W2"][sl]), x["b2"][sl].double().cpu().numpy())
+        zg = p.score[sl].cpu().numpy()
+        assert_close_abs(zg[..., rows], z, LOG_SCORE_ATOL,
+                         f"c6 MLP surrogate (layer {l}, sampled tokens)")
+        mg = p.mask[sl].cpu().numpy()
+        # the threshold rule applied to the kernel's own fp32 scores, over the whole layer
+        m_same, _ = O.prune_threshold(zg.astype(np.float64), np.float32(wl.tau), wl.w)
+        assert np.array_equal(mg, m_same)
+        # and the oracle's decision on the sampled tokens, except next to tau
+        m_ref, _ = O.prune_threshold(z, wl.tau, 0)
+        m_ref[..., rows >= wl.T - wl.w] = 1
+        assert_masks_match_near(mg[..., rows], m_ref, z, np.full(z.shape[:-1], wl.tau), MASK_BAND,
+                                f"c6 mask (layer {l}, sampled tokens)", log_domain=True)
+        assert np.array_equal(p.keep[sl].cpu().numpy(), mg.sum(-1))
+        for h in range(wl.H_kv):
+            _check_pages(p.pages, l, h, x["k"][l, h].cpu(), x["v"][l, h].cpu(), mg[0, h])
 
 
 def test_c4_attention_forward_sampled_rows(mods):
