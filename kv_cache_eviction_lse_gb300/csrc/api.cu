@@ -483,16 +483,11 @@ kvs_status kvs_value_refit(const kvs_dims* dims, const kvs_bf16* q, int32_t n_q,
   r.rows = a_s; r.rows_ld = pl.k_ld;
   if (e == cudaSuccess) e = kvs::launch_lse(r, s);
   if (e == cudaSuccess) e = kvs::launch_softmax_rows(r, s);
-  // 3. normal equations: Gram (upper block triangle) and right-hand side
-  kvs::GramArgs gg;
-  const auto* a16 = reinterpret_cast<const kvs::bf16_t*>(a_s);  // 16-bit words (fp16)
-  gg.x_hi = a16; gg.y_hi = a16; gg.c = gm; gg.f16 = 1;
-  gg.batch = L * Hkv; gg.rows = pl.rows; gg.M = gg.N = pl.k_ld;
-  gg.ldx = gg.ldy = gg.ldc = pl.k_ld; gg.upper = 1;
-  if (e == cudaSuccess) e = kvs::launch_gram(gg, s);
-  kvs::GramArgs rr = gg;
-  rr.y_hi = o_ws; rr.y_lo = nullptr; rr.c = rm; rr.N = d; rr.ldy = d; rr.ldc = d; rr.upper = 0;
-  if (e == cudaSuccess) e = kvs::launch_gram(rr, s);
+  // 3. normal equations: Gram (upper block triangle) and right-hand side, one launch
+  kvs::RefitProdArgs rp;
+  rp.a_s = a_s; rp.o = reinterpret_cast<const uint16_t*>(o_ws); rp.g = gm; rp.r = rm;
+  rp.batch = L * Hkv; rp.rows = pl.rows; rp.k_ld = pl.k_ld; rp.d = d;
+  if (e == cudaSuccess) e = kvs::launch_refit_products(rp, s);
   // 4. ridge solve per (layer, KV head)
   kvs::CholArgs c;
   c.g = gm; c.r = rm; c.x = v_fit; c.batch = L * Hkv; c.M = pl.k_ld; c.ldg = pl.k_ld;

@@ -551,14 +551,17 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
       const size_t rows_base = ((size_t)(l * a.Hq + hq_a) * a.n_q + warp_row0) * a.rows_ld;
       if (MODE == kRows && ra < a.n_q) l2row = a.lse[(size_t)(l * a.Hq + hq_a) * a.n_q + ra] * kLog2e;
 
-      auto ln_vn = [&](int it) -> float {  // ln ||W_O v|| of this key for the head of tile it
-        if (!a.vnorm || ra >= a.T) return 0.f;
-        return logf(a.vnorm[(size_t)(l * a.Hq + hk * G + it / U.per_head) * a.T + ra]);
+      // ||W_O v|| of this key for the head of tile it (1 without value norms); the
+      // logarithm is taken only when the head's maximum is folded, tiles later, so the
+      // load's latency never delays the release of an accumulator
+      auto vn_of = [&](int it) -> float {
+        if (!a.vnorm || ra >= a.T) return 1.f;
+        return a.vnorm[(size_t)(l * a.Hq + hk * G + it / U.per_head) * a.T + ra];
       };
 
       float m = -1e30f, ssum = 0.f;                  // kLse
       float r = -CUDART_INF_F, tot = -CUDART_INF_F;  // kMax
-      float lv = 0.f;                                // kMax: ln vnorm of the current head
+      float vn = 1.f;                                // kMax: vnorm of the current head
       int cur_head = -1;                             // kMax: head of r (-1: none yet)
       float f = 0.f;                                 // kFuture
 
@@ -644,9 +647,9 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
             if (MODE == kMax) {  // a new query head: fold the previous head's maximum
               const int hd = it / U.per_head;
               if (hd != cur_head) {
-                if (cur_head >= 0) tot = fmaxf(tot, r * scale + lv);
+                if (cur_head >= 0) tot = fmaxf(tot, r * scale + logf(vn));
                 r = -CUDART_INF_F;
-                lv = ln_vn(it);
+                vn = vn_of(it);
                 cur_head = hd;
               }
             }
@@ -698,7 +701,7 @@ __global__ void __launch_bounds__(Cfg<D, MODE>::THREADS, 1)
       // results of this unit: combine the groups' partial results of each row (kQuad:
       // the per-head partial dot products).  All groups vote on failure here, so they
       // leave the unit loop together and never wait at a barrier another has abandoned.
-      if (MODE == kMax && cur_head >= 0) tot = fmaxf(tot, r * scale + lv);
+      if (MODE == kMax && cur_head >= 0) tot = fmaxf(tot, r * scale + logf(vn));
       float* xchg = xchg_all + (n & 1) * (NG - 1) * BM * 2;
       if (MODE != kQuad && MODE != kRows && h > 0 && !bad) {
         float* xg = xchg + (h - 1) * BM * 2;

@@ -1,8 +1,8 @@
 // Launchers of the value refit's linear algebra: the batched X^T Y products on the
 // tensor cores and the per-problem Cholesky solve of the ridge normal equations.
 // The refit's products run on fp16 operands (softmax weights in [0, 1] and the attention
-// output, 2^-12 relative each) with fp32 accumulation; the value-norm Gram of o_proj
-// runs on bf16 with its result split into bf16 hi/lo pairs.
+// output, 2^-12 relative each) with fp32 accumulation (launch_refit_products); the
+// value-norm Gram of o_proj runs on bf16 with its result split into bf16 hi/lo pairs.
 #pragma once
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -19,7 +19,6 @@ struct GramArgs {
   float* c = nullptr;            // [batch][M][ldc]
   int batch = 0, rows = 0, M = 0, N = 0, ldx = 0, ldy = 0, ldc = 0;
   int upper = 0;                 // Y == X: write only the upper block triangle (M == N)
-  int f16 = 0;                   // operands are fp16 (else bf16); parts and layouts as above
   // Y == X, diagonal d x d blocks only (the Gram matrix of each d-column slice of X):
   // written as bf16 pairs pair[batch][M / d][2][d][d] (hi rows, then lo = bf16(G - hi))
   // instead of into c
@@ -28,6 +27,17 @@ struct GramArgs {
 };
 
 cudaError_t launch_gram(const GramArgs& a, cudaStream_t s);
+
+// The value refit's normal equations in one launch, fp16 operands, fp32 results:
+//   g[b] = A_S[b]^T A_S[b] (upper block triangle, k_ld x k_ld)   r[b] = A_S[b]^T O[b] (k_ld x d)
+struct RefitProdArgs {
+  const uint16_t* a_s = nullptr;  // [batch][rows][k_ld] fp16 softmax rows, zero past k
+  const uint16_t* o = nullptr;    // [batch][rows][d] fp16 attention outputs
+  float* g = nullptr;             // [batch][k_ld][k_ld]
+  float* r = nullptr;             // [batch][k_ld][d]
+  int batch = 0, rows = 0, k_ld = 0, d = 0;
+};
+cudaError_t launch_refit_products(const RefitProdArgs& a, cudaStream_t s);
 cudaError_t gram_device_error(int* code, bool clear, cudaStream_t s);
 
 struct CholArgs {

@@ -145,9 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // A and B MN-major; the A and B format fields (bits 7-9, 10-12) say bf16 (1) or fp16 (0)
-      const uint32_t idesc = (tc::idesc_bf16_bmn(BT, BT) | (1u << 15)) &
-                             (a.f16 ? ~((1u << 7) | (1u << 10)) : ~0u);
+      constexpr uint32_t idesc = tc::idesc_bf16_bmn(BT, BT) | (1u << 15);  // A and B MN-major
       int kb = 0;
       bool ok = true;
       for (; kb < nkb; ++kb) {
@@ -240,25 +238,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ------------------------------------------------------------------ wide tiles (refit)
+// ------------------------------------------------------------------ refit products
 //
-// C = X^T Y for single-part fp16 operands (the value refit's Gram matrix and right-hand
-// side): one CTA per 256 x WN output block (WN = 256, or 128 when N <= 128), its two
-// 128-row halves in two TMEM accumulators of WN columns.  Per 64-row k-block the CTA
-// loads X (64 x 256) and Y (64 x WN) and issues 2 x 4 MMAs of 128 x WN x 16, so a byte of
-// operand feeds twice the flops of a 128 x 128 tile: the refit's products stream their
-// operands from L2, and that is what bounds them.
+// The value refit's normal equations in one launch, on single-part fp16 operands:
+//   G = A_S^T A_S  (upper block triangle of 256 x 256 blocks)   and   R = A_S^T O
+// One CTA per 256 x WN output block (WN = 256 for G, 128 for R, so R's blocks carry no
+// empty columns), its two 128-row halves in two TMEM accumulators of WN columns.  Per
+// 64-row k-block the CTA loads 64 x 256 of A_S and 64 x WN of A_S or O and issues 2 x 4
+// MMAs of 128 x WN x 16: a byte of operand feeds twice the flops of a 128 x 128 tile
+// (these products stream their operands from L2, and that is what bounds them), and the
+// G and R blocks share one wave of CTAs.
 constexpr int WM = 256;                    // output rows per CTA (two MMA halves)
 constexpr int kWideThreads = 64 + 256;     // producer, MMA issuer, 8 epilogue warps
 constexpr int kWideStages = 3;             // 64 KB per stage (X and Y tiles)
 constexpr uint32_t kWideStage = 8 * kBox;  // X: 4 boxes, Y: up to 4 boxes
 constexpr uint32_t kWideSmem = OFF_RING + kWideStages * kWideStage + 1024;
+constexpr uint32_t kWideCols = 512;        // TMEM: two accumulators of up to 256 columns
 static_assert(kWideSmem <= 232448, "shared-memory plan exceeds the per-block limit");
 
-template <int WN>
 __global__ void __launch_bounds__(kWideThreads, 1)
-    gram_wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
-                     const GramArgs a) {
+    refit_products_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_o,
+                          const RefitProdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -273,26 +273,25 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   auto bar_empty = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
   const uint32_t bar_done = bar0 + 8u * (2 * kMaxStages);
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
-  constexpr uint32_t kCols = 2 * WN;       // TMEM columns: two accumulators
-  constexpr uint32_t kY = 4 * kBox;        // Y tile offset within a stage
-  constexpr uint32_t kBytes = 4 * kBox + (WN / 64) * kBox;
+  constexpr uint32_t kY = 4 * kBox;  // Y tile offset within a stage
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int tm, tn;
-  if (a.upper) {  // the upper block triangle of WM x WN blocks (WN == WM here)
+  // blocks [0, n_up): G's upper block triangle; the next nt blocks: R's row blocks
+  const int nt = (a.k_ld + WM - 1) / WM, n_up = nt * (nt + 1) / 2;
+  const bool rhs = (int)blockIdx.x >= n_up;
+  int tm, tn = 0;
+  if (rhs) {
+    tm = (int)blockIdx.x - n_up;
+  } else {
     int t = blockIdx.x, row = 0;
-    const int nt = (a.M + WM - 1) / WM;
     while (t >= nt - row) {
       t -= nt - row;
       ++row;
     }
     tm = row;
     tn = row + t;
-  } else {
-    const int ntn = (a.N + WN - 1) / WN;
-    tm = blockIdx.x / ntn;
-    tn = blockIdx.x % ntn;
   }
+  const int wn = rhs ? 128 : 256;
   const int b = blockIdx.y;
   const int nkb = (a.rows + BK - 1) / BK;
 
@@ -305,7 +304,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     tc::fence_mbar_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(sb + OFF_MISC, kCols);
+    tc::tmem_alloc(sb + OFF_MISC, kWideCols);
     tc::tmem_relinquish();
   }
   __syncthreads();
@@ -314,6 +313,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
+      const uint32_t bytes = 4 * kBox + (uint32_t)(wn / 64) * kBox;
+      const CUtensorMap* ym = rhs ? &tm_o : &tm_a;
       int kb = 0;
       bool ok = true;
       for (; kb < nkb; ++kb) {
@@ -323,13 +324,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           break;
         }
         const uint32_t st = sb + OFF_RING + s * kWideStage;
-        tc::mbar_expect_tx(bar_full(s), kBytes);
+        tc::mbar_expect_tx(bar_full(s), bytes);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)  // X: columns tm*256 .. +255, four 64-column boxes
-          tc::tma_load_3d(st + c * kBox, &tm_x, bar_full(s), tm * WM + 64 * c, kb * BK, b);
-#pragma unroll
-        for (int c = 0; c < WN / 64; ++c)
-          tc::tma_load_3d(st + kY + c * kBox, &tm_y, bar_full(s), tn * WN + 64 * c, kb * BK, b);
+        for (int c = 0; c < 4; ++c)  // X: A_S columns tm*256 .. +255, four 64-column boxes
+          tc::tma_load_3d(st + c * kBox, &tm_a, bar_full(s), tm * WM + 64 * c, kb * BK, b);
+        for (int c = 0; c < wn / 64; ++c)
+          tc::tma_load_3d(st + kY + c * kBox, ym, bar_full(s), tn * wn + 64 * c, kb * BK, b);
       }
       if (!ok) {
         atomicCAS(&g_gram_error, 0, kErrWaitTimeout);
@@ -339,9 +339,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // A and B MN-major, fp16 (format fields 0)
-      constexpr uint32_t idesc =
-          (tc::idesc_bf16_bmn(128, WN) | (1u << 15)) & ~((1u << 7) | (1u << 10));
+      // A and B MN-major, fp16 (format fields 0), N = wn
+      const uint32_t idesc =
+          (tc::idesc_bf16_bmn(128, wn) | (1u << 15)) & ~((1u << 7) | (1u << 10));
       int kb = 0;
       bool ok = true;
       for (; kb < nkb; ++kb) {
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           const uint64_t yd = tc::sdesc_sw128_mn(st + kY + o, kBox);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh)
-            tc::mma_bf16(tmem + (uint32_t)(hh * WN), tc::sdesc_sw128_mn(st + 2 * hh * kBox + o, kBox),
+            tc::mma_bf16(tmem + (uint32_t)(hh * wn), tc::sdesc_sw128_mn(st + 2 * hh * kBox + o, kBox),
                          yd, idesc, (kb | k) != 0 ? 1u : 0u);
         }
         tc::commit(bar_empty(s));
@@ -375,15 +375,16 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const bool ok = tc::mbar_wait(bar_done, 0);
     if (!ok) atomicCAS(&g_gram_error, 0, kErrWaitTimeout);
     tc::fence_after_sync();
-    float* crow = a.c + ((size_t)b * a.M + m) * a.ldc + tn * WN;
-    const int nmax = min(WN, a.N - tn * WN);
-    const uint32_t t0 = tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(hh * WN);
-#pragma unroll
-    for (int cb = 0; cb < WN / 32; ++cb) {
+    const int N = rhs ? a.d : a.k_ld, ldc = rhs ? a.d : a.k_ld;
+    float* crow = (rhs ? a.r : a.g) + ((size_t)b * a.k_ld + m) * ldc + tn * wn;
+    const int nmax = min(wn, N - tn * wn);
+    const uint32_t t0 = tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(hh * wn);
+#pragma unroll 1
+    for (int cb = 0; cb < wn / 32; ++cb) {
       uint32_t v[32];
       tc::tmem_ld32(t0 + 32u * cb, v);
       tc::tmem_ld_wait();
-      if (ok && m < a.M) {
+      if (ok && m < a.k_ld) {
         if (32 * cb + 32 <= nmax) {
 #pragma unroll
           for (int c = 0; c < 32; c += 4)
@@ -399,7 +400,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, kCols);
+    tc::tmem_dealloc(tmem, kWideCols);
   }
 }
 
@@ -408,29 +409,6 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 cudaError_t launch_gram(const GramArgs& a, cudaStream_t s) {
   if (a.M <= 0 || a.N <= 0 || a.batch <= 0) return cudaSuccess;
   const bool diag = a.pair != nullptr;
-  if (a.f16 && !diag && !a.x_lo && !a.y_lo) {  // the refit's single-part fp16 products
-    if (a.upper && a.M != a.N) return cudaErrorInvalidValue;
-    if (a.ldx % 8 || a.ldy % 8 || a.ldc % 4) return cudaErrorInvalidValue;
-    CUtensorMap x, y;
-    cudaError_t e = tma_map_bf16_3d(&x, a.x_hi, a.ldx, a.rows, a.batch, BK);
-    if (e == cudaSuccess) e = tma_map_bf16_3d(&y, a.y_hi, a.ldy, a.rows, a.batch, BK);
-    if (e != cudaSuccess) return e;
-    const int tmn = (a.M + WM - 1) / WM;
-    count_launches(1);
-    if (a.N > 128 || a.upper) {
-      auto kern = gram_wide_kernel<256>;
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWideSmem);
-      if (e != cudaSuccess) return e;
-      const int tiles = a.upper ? tmn * (tmn + 1) / 2 : tmn * ((a.N + 255) / 256);
-      kern<<<dim3(tiles, a.batch), kWideThreads, kWideSmem, s>>>(x, y, a);
-    } else {
-      auto kern = gram_wide_kernel<128>;
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWideSmem);
-      if (e != cudaSuccess) return e;
-      kern<<<dim3(tmn, a.batch), kWideThreads, kWideSmem, s>>>(x, y, a);
-    }
-    return cudaGetLastError();
-  }
   if ((a.upper || diag) && a.M != a.N) return cudaErrorInvalidValue;
   if (diag && (a.pair_d <= 0 || BT % a.pair_d || a.M % a.pair_d || a.pair_d % 8))
     return cudaErrorInvalidValue;
@@ -451,6 +429,23 @@ cudaError_t launch_gram(const GramArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   count_launches(1);
   gram_tc_kernel<<<dim3(tiles, a.batch), kThreads, smem, s>>>(xh, xl, yh, yl, a, ring);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_refit_products(const RefitProdArgs& a, cudaStream_t s) {
+  if (a.batch <= 0 || a.k_ld <= 0 || a.rows <= 0) return cudaSuccess;
+  if (a.k_ld % 64 || a.d % 8 || a.d > 128) return cudaErrorInvalidValue;
+  CUtensorMap ma, mo;
+  cudaError_t e = tma_map_bf16_3d(&ma, a.a_s, a.k_ld, a.rows, a.batch, BK);
+  if (e == cudaSuccess) e = tma_map_bf16_3d(&mo, a.o, a.d, a.rows, a.batch, BK);
+  if (e != cudaSuccess) return e;
+  const int nt = (a.k_ld + WM - 1) / WM;
+  e = cudaFuncSetAttribute(refit_products_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kWideSmem);
+  if (e != cudaSuccess) return e;
+  count_launches(1);
+  refit_products_kernel<<<dim3(nt * (nt + 1) / 2 + nt, a.batch), kWideThreads, kWideSmem, s>>>(
+      ma, mo, a);
   return cudaGetLastError();
 }
 

@@ -58,7 +58,7 @@ class PagePool:
         self.v_pages = _empty((self.capacity, page_size, d), torch.bfloat16, device)
         self.block_table = _empty((n, L, H, self.max_pages), torch.int32, device)
         self.seq_lens = _empty((n, L, H), torch.int32, device)
-        self.needed = _empty((4,), torch.int32, device)
+        self.needed = _empty((1,), torch.int32, device)
 
     def view(self, b):
         return types.SimpleNamespace(page_size=self.page_size, max_pages=self.max_pages,
