@@ -11,19 +11,13 @@
 
 namespace kvs {
 
+// The value norms' Gram pairs: the diagonal d x d blocks of X^T X for X = o_proj.weight,
+// the Gram matrix of each d-column slice (one head), written as bf16 pairs
+// pair[batch][M / d][2][d][d] (hi rows, then lo = bf16(G - hi)).
 struct GramArgs {
-  const bf16_t* x_hi = nullptr;  // [batch][rows][ldx], columns >= M are zero
-  const bf16_t* x_lo = nullptr;  // nullable: X taken as one bf16 part
-  const bf16_t* y_hi = nullptr;  // [batch][rows][ldy]
-  const bf16_t* y_lo = nullptr;  // nullable: Y taken as one bf16 part
-  float* c = nullptr;            // [batch][M][ldc]
-  int batch = 0, rows = 0, M = 0, N = 0, ldx = 0, ldy = 0, ldc = 0;
-  int upper = 0;                 // Y == X: write only the upper block triangle (M == N)
-  // Y == X, diagonal d x d blocks only (the Gram matrix of each d-column slice of X):
-  // written as bf16 pairs pair[batch][M / d][2][d][d] (hi rows, then lo = bf16(G - hi))
-  // instead of into c
+  const bf16_t* x = nullptr;  // [batch][rows][ldx]
   bf16_t* pair = nullptr;
-  int pair_d = 0;
+  int batch = 0, rows = 0, M = 0, ldx = 0, pair_d = 0;
 };
 
 cudaError_t launch_gram(const GramArgs& a, cudaStream_t s);

@@ -1,18 +1,12 @@
-// Batched C = X^T Y on the tensor cores (tcgen05 + TMEM + TMA), fp32 accumulation, bf16 or
-// fp16 operands, each optionally split into hi + lo parts: for the normal equations of
-// the value refit X = the fp16 softmax rows A_S of the kept keys ([rows][M]), Y = A_S
-// itself (Gram matrix, upper block triangle only) or the fp16 attention output O
-// ([rows][N]); for the value norms the diagonal d x d blocks of o_proj^T o_proj (bf16).
-//
-//   C[b][m][n] = sum_r X[b][r][m] Y[b][r][n]
-//             ~= sum_r Xhi Yhi + Xhi Ylo + Xlo Yhi   (Y split)    or   Xhi Y + Xlo Y
+// Products X^T Y on the tensor cores (tcgen05 + TMEM + TMA), fp32 accumulation:
+//   gram_tc_kernel         the value norms' Gram pairs: the diagonal d x d blocks of
+//                          o_proj^T o_proj (bf16 operands), written as bf16 hi/lo pairs
+//   refit_products_kernel  the value refit's normal equations A_S^T A_S and A_S^T O
+//                          (fp16 operands), below
 //
 // Both operands are read MN-major straight from their row-major [rows][cols] storage:
 // a TMA box of 64 rows x 64 columns is one 128-byte-swizzled MN-major atom column, so
 // a 128-column tile is two boxes (leading byte offset 8 KB) and each MMA takes 16 rows.
-// One CTA per 128 x 128 output tile; warp 0 streams 64-row k-blocks through a ring of 3
-// to 12 stages (as many as the operand tiles a product needs allow), warp 1 issues the
-// MMAs into one TMEM accumulator, warps 2-5 write the tile.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -30,12 +24,12 @@ constexpr int BT = 128;                 // output tile edge
 constexpr int BK = 64;                  // rows per k-block
 constexpr uint32_t kBox = 64 * 128;     // 64 rows x 64 bf16 = 8 KB
 constexpr uint32_t kOp = 2 * kBox;      // one 128-column operand tile of a k-block
-constexpr uint32_t kRing = 3 * 4 * kOp;  // operand ring of the refit products: 192 KB
 // The value-norm Gram streams one operand (16 KB per k-block) straight from HBM; a
 // 4-stage ring lets three CTAs share an SM, so all (layer, head) tiles of a call run at
 // once and the heads of a layer walk the rows of o_proj.weight together.
-constexpr uint32_t kRingDiag = 4 * kOp;
-constexpr int kMaxStages = 12;          // stages of (X hi, [X lo], [Y hi], [Y lo]) tiles
+constexpr int kStages = 4;
+constexpr uint32_t kRingDiag = kStages * kOp;
+constexpr int kMaxStages = 12;          // barrier slots (the refit products use 3)
 constexpr int kThreads = 64 + 128;
 constexpr uint32_t kTmemCols = 128;
 constexpr uint32_t OFF_BAR = 0;  // barriers and the TMEM address first, the ring after
@@ -43,20 +37,20 @@ constexpr uint32_t NBAR = 2 * kMaxStages + 1;  // full[S], empty[S], done
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr uint32_t OFF_RING = 1024;
 static_assert(OFF_MISC + 16 <= OFF_RING, "barrier block");
-static_assert(kRing % (4 * kOp) == 0 && kRing / kOp <= 3 * 4, "operand ring");
-__host__ __device__ constexpr uint32_t smem_bytes(uint32_t ring) { return OFF_RING + ring + 1024; }
-static_assert(smem_bytes(kRing) <= 232448, "shared-memory plan exceeds the per-block limit");
+constexpr uint32_t kDiagSmem = OFF_RING + kRingDiag + 1024;
 constexpr int kErrWaitTimeout = 1;
 constexpr int kErrSmemAlign = 3;
 
+// One CTA per 128 x 128 diagonal tile of X^T X (X = o_proj.weight [D_h][H_q d], tile tm
+// covers the 128 / d heads whose slices it holds): warp 0 streams 64-row k-blocks through
+// the ring, warp 1 issues the MMAs (X^T against itself) into one TMEM accumulator, warps
+// 2-5 write each head's d x d block as bf16 hi and lo parts.
 __global__ void __launch_bounds__(kThreads, 1)
-    gram_tc_kernel(const __grid_constant__ CUtensorMap tm_xhi, const __grid_constant__ CUtensorMap tm_xlo,
-                   const __grid_constant__ CUtensorMap tm_yhi, const __grid_constant__ CUtensorMap tm_ylo,
-                   const GramArgs a, const uint32_t ring) {
+    gram_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const GramArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-  if (pad + OFF_RING + ring > smem_bytes(ring)) {
+  if (pad + OFF_RING + kRingDiag > kDiagSmem) {
     if (threadIdx.x == 0) atomicCAS(&g_gram_error, 0, kErrSmemAlign);
     return;
   }
@@ -69,35 +63,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // output tile: the upper block triangle when Y is X (symmetric result)
-  const bool diag = a.pair != nullptr;  // Y == X, diagonal tiles, bf16 pairs out
-  int tm, tn;
-  if (diag) {
-    tm = tn = blockIdx.x;
-  } else if (a.upper) {
-    int t = blockIdx.x, row = 0, nt = (a.M + BT - 1) / BT;
-    while (t >= nt - row) {
-      t -= nt - row;
-      ++row;
-    }
-    tm = row;
-    tn = row + t;
-  } else {
-    tm = blockIdx.x / ((a.N + BT - 1) / BT);
-    tn = blockIdx.x % ((a.N + BT - 1) / BT);
-  }
-  const int b = blockIdx.y;
+  const int tm = blockIdx.x, b = blockIdx.y;
   const int nkb = (a.rows + BK - 1) / BK;
-  const bool y_split = a.y_lo != nullptr, x_split = a.x_lo != nullptr;
-  // a stage holds only the operand tiles this product needs, so fewer operands mean a
-  // deeper ring (3 stages for the split Gram, up to 12 for the value-norm Gram)
-  const int nop = 1 + (x_split ? 1 : 0) + (diag ? 0 : 1) + (y_split ? 1 : 0);
-  const uint32_t stage_bytes = nop * kOp;
-  const int kStages = min(kMaxStages, (int)(ring / stage_bytes));
-  const uint32_t o_xlo = kOp, o_yhi = (1 + (x_split ? 1 : 0)) * kOp, o_ylo = o_yhi + kOp;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kMaxStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(bar_full(s), 1);
       tc::mbar_init(bar_empty(s), 1);
     }
@@ -122,20 +92,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const uint32_t st = sb + OFF_RING + s * stage_bytes;
-        tc::mbar_expect_tx(bar_full(s), stage_bytes);
-        for (int c = 0; c < 2; ++c) {  // two 64-column boxes per operand tile
-          tc::tma_load_3d(st + c * kBox, &tm_xhi, bar_full(s), tm * BT + 64 * c, kb * BK, b);
-          if (x_split)
-            tc::tma_load_3d(st + o_xlo + c * kBox, &tm_xlo, bar_full(s), tm * BT + 64 * c,
-                            kb * BK, b);
-          if (!diag)
-            tc::tma_load_3d(st + o_yhi + c * kBox, &tm_yhi, bar_full(s), tn * BT + 64 * c,
-                            kb * BK, b);
-          if (y_split)
-            tc::tma_load_3d(st + o_ylo + c * kBox, &tm_ylo, bar_full(s), tn * BT + 64 * c,
-                            kb * BK, b);
-        }
+        const uint32_t st = sb + OFF_RING + s * kOp;
+        tc::mbar_expect_tx(bar_full(s), kOp);
+        for (int c = 0; c < 2; ++c)  // two 64-column boxes
+          tc::tma_load_3d(st + c * kBox, &tm_x, bar_full(s), tm * BT + 64 * c, kb * BK, b);
       }
       if (!ok) {
         atomicCAS(&g_gram_error, 0, kErrWaitTimeout);
@@ -155,15 +115,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc::fence_after_sync();
-        const uint32_t st = sb + OFF_RING + s * stage_bytes;
+        const uint32_t st = sb + OFF_RING + s * kOp;
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k) {
-          const uint32_t o = 2048u * k;  // 16 rows of 128 bytes
-          const uint64_t xh = tc::sdesc_sw128_mn(st + o, kBox), xl = tc::sdesc_sw128_mn(st + o_xlo + o, kBox);
-          const uint64_t yh = diag ? xh : tc::sdesc_sw128_mn(st + o_yhi + o, kBox);
-          tc::mma_bf16(tmem, xh, yh, idesc, (kb | k) != 0 ? 1u : 0u);
-          if (x_split) tc::mma_bf16(tmem, xl, yh, idesc, 1u);
-          if (y_split) tc::mma_bf16(tmem, xh, tc::sdesc_sw128_mn(st + o_ylo + o, kBox), idesc, 1u);
+          const uint64_t xd = tc::sdesc_sw128_mn(st + 2048u * k, kBox);  // 16 rows of 128 B
+          tc::mma_bf16(tmem, xd, xd, idesc, (kb | k) != 0 ? 1u : 0u);
         }
         tc::commit(bar_empty(s));
       }
@@ -173,62 +129,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // epilogue: warp w reads TMEM lanes 32 (w % 4) ..; row m of the tile per thread
+    // epilogue: warp w reads TMEM lanes 32 (w % 4) ..; row ml of the tile per thread
+    // belongs to slice (head) r = ml / d; write that slice's row of its d x d Gram block
+    // as bf16 hi and lo parts
     const int eq = warp & 3;
-    const int m = tm * BT + eq * 32 + lane;
     const bool ok = tc::mbar_wait(bar_done, 0);
     if (!ok) atomicCAS(&g_gram_error, 0, kErrWaitTimeout);
     tc::fence_after_sync();
-    if (diag) {
-      // row m of the tile belongs to slice (head) r = m_local / d; write that slice's row
-      // of its d x d Gram block as bf16 hi and lo parts
-      const int dd = a.pair_d, ml = eq * 32 + lane, r = ml / dd, i = ml % dd;
-      const int head = (tm * BT) / dd + r, nheads = a.M / dd;
-      bf16_t* gh = a.pair + (((size_t)b * nheads + head) * 2 * dd + i) * dd;
-#pragma unroll
-      for (int cb = 0; cb < BT / 32; ++cb) {
-        uint32_t v[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(eq * 32) << 16) + 32u * cb, v);
-        tc::tmem_ld_wait();
-        const int c0 = 32 * cb - r * dd;  // column within the slice
-        if (ok && head < nheads && c0 >= 0 && c0 < dd) {
-#pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float x0 = __uint_as_float(v[c + 2 * e]), x1 = __uint_as_float(v[c + 2 * e + 1]);
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
-              hi[e] = *reinterpret_cast<uint32_t*>(&h2);
-              __nv_bfloat162 l2 = __floats2bfloat162_rn(x0 - __low2float(h2), x1 - __high2float(h2));
-              lo[e] = *reinterpret_cast<uint32_t*>(&l2);
-            }
-            *reinterpret_cast<uint4*>(gh + c0 + c) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(gh + (size_t)dd * dd + c0 + c) =
-                make_uint4(lo[0], lo[1], lo[2], lo[3]);
-          }
-        }
-      }
-    } else {
-    float* crow = a.c + ((size_t)b * a.M + m) * a.ldc + tn * BT;
-    const int nmax = min(BT, a.N - tn * BT);
+    const int dd = a.pair_d, ml = eq * 32 + lane, r = ml / dd, i = ml % dd;
+    const int head = (tm * BT) / dd + r, nheads = a.M / dd;
+    bf16_t* gh = a.pair + (((size_t)b * nheads + head) * 2 * dd + i) * dd;
 #pragma unroll
     for (int cb = 0; cb < BT / 32; ++cb) {
       uint32_t v[32];
       tc::tmem_ld32(tmem + ((uint32_t)(eq * 32) << 16) + 32u * cb, v);
       tc::tmem_ld_wait();
-      if (ok && m < a.M) {
-        if (32 * cb + 32 <= nmax) {
+      const int c0 = 32 * cb - r * dd;  // column within the slice
+      if (ok && head < nheads && c0 >= 0 && c0 < dd) {
 #pragma unroll
-          for (int c = 0; c < 32; c += 4)
-            *reinterpret_cast<float4*>(crow + 32 * cb + c) =
-                make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]),
-                            __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
-        } else {
-          for (int c = 0; c < 32 && 32 * cb + c < nmax; ++c) crow[32 * cb + c] = __uint_as_float(v[c]);
+        for (int c = 0; c < 32; c += 8) {
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float x0 = __uint_as_float(v[c + 2 * e]), x1 = __uint_as_float(v[c + 2 * e + 1]);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+            hi[e] = *reinterpret_cast<uint32_t*>(&h2);
+            __nv_bfloat162 l2 = __floats2bfloat162_rn(x0 - __low2float(h2), x1 - __high2float(h2));
+            lo[e] = *reinterpret_cast<uint32_t*>(&l2);
+          }
+          *reinterpret_cast<uint4*>(gh + c0 + c) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(gh + (size_t)dd * dd + c0 + c) =
+              make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
-    }
     }
   }
   __syncthreads();
@@ -407,28 +340,18 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 }  // namespace
 
 cudaError_t launch_gram(const GramArgs& a, cudaStream_t s) {
-  if (a.M <= 0 || a.N <= 0 || a.batch <= 0) return cudaSuccess;
-  const bool diag = a.pair != nullptr;
-  if ((a.upper || diag) && a.M != a.N) return cudaErrorInvalidValue;
-  if (diag && (a.pair_d <= 0 || BT % a.pair_d || a.M % a.pair_d || a.pair_d % 8))
+  if (a.M <= 0 || a.batch <= 0) return cudaSuccess;
+  if (!a.x || !a.pair || a.pair_d <= 0 || BT % a.pair_d || a.M % a.pair_d || a.pair_d % 8 ||
+      a.ldx % 8)
     return cudaErrorInvalidValue;
-  if (a.ldx % 8 || a.ldy % 8 || (!diag && a.ldc % 4)) return cudaErrorInvalidValue;
-  CUtensorMap xh, xl, yh, yl;
-  cudaError_t e = tma_map_bf16_3d(&xh, a.x_hi, a.ldx, a.rows, a.batch, BK);
-  if (e == cudaSuccess)
-    e = tma_map_bf16_3d(&xl, a.x_lo ? a.x_lo : a.x_hi, a.ldx, a.rows, a.batch, BK);
-  if (e == cudaSuccess) e = tma_map_bf16_3d(&yh, a.y_hi, a.ldy, a.rows, a.batch, BK);
-  if (e == cudaSuccess)
-    e = tma_map_bf16_3d(&yl, a.y_lo ? a.y_lo : a.y_hi, a.ldy, a.rows, a.batch, BK);
+  CUtensorMap x;
+  cudaError_t e = tma_map_bf16_3d(&x, a.x, a.ldx, a.rows, a.batch, BK);
   if (e != cudaSuccess) return e;
-  const int tmn = (a.M + BT - 1) / BT, tnn = (a.N + BT - 1) / BT;
-  const int tiles = diag ? tmn : a.upper ? tmn * (tmn + 1) / 2 : tmn * tnn;
-  const uint32_t ring = diag ? kRingDiag : kRing, smem = smem_bytes(ring);
   e = cudaFuncSetAttribute(gram_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem_bytes(kRing));
+                           (int)kDiagSmem);
   if (e != cudaSuccess) return e;
   count_launches(1);
-  gram_tc_kernel<<<dim3(tiles, a.batch), kThreads, smem, s>>>(xh, xl, yh, yl, a, ring);
+  gram_tc_kernel<<<dim3((a.M + BT - 1) / BT, a.batch), kThreads, kDiagSmem, s>>>(x, a);
   return cudaGetLastError();
 }
 

@@ -34,8 +34,8 @@ cudaError_t launch_vnorm(const bf16_t* v, int L, int Hq, int Hkv, int d, int T, 
   // G_h = W_h^T W_h for every head: the diagonal d x d blocks of W_O^T W_O on tcgen05,
   // written as bf16 hi/lo pairs
   GramArgs g;
-  g.x_hi = w_o; g.y_hi = w_o; g.pair = G; g.pair_d = d;
-  g.batch = L; g.rows = Dh; g.M = g.N = Hq * d; g.ldx = g.ldy = Hq * d;
+  g.x = w_o; g.pair = G; g.pair_d = d;
+  g.batch = L; g.rows = Dh; g.M = Hq * d; g.ldx = Hq * d;
   cudaError_t e = launch_gram(g, s);
   if (e != cudaSuccess) return e;
   AttnArgs a;  // quadratic form on the tensor cores (tcgen05), see attn_tc.cu
