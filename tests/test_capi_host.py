@@ -34,6 +34,44 @@ def test_every_declared_symbol_is_exported(capi):
     assert set(syms) == set(capi.EXPORTED)
 
 
+def test_validation_of_multi_budget_and_quantile_calls(capi):
+    """kvs_prune_topk_multi, kvs_prune_quantile and kvs_compact_paged_multi reject bad
+    arguments before anything is enqueued, and their empty calls succeed."""
+    C = capi
+    lib = C._lib
+    by = ctypes.byref
+    dm = C.dims(2, 4, 2, 128, 0)
+    fake = 1 << 20
+    ks = (ctypes.c_int32 * 9)(*([5] * 9))
+    # top-k of several budgets: count outside 1..8, a negative budget, null k, misaligned
+    assert lib.kvs_prune_topk_multi(by(dm), fake, 10, 0, ks, 0, fake, fake, None) == C.KVS_ERR_UNSUPPORTED
+    assert lib.kvs_prune_topk_multi(by(dm), fake, 10, 9, ks, 0, fake, fake, None) == C.KVS_ERR_UNSUPPORTED
+    neg = (ctypes.c_int32 * 2)(3, -1)
+    assert lib.kvs_prune_topk_multi(by(dm), fake, 10, 2, neg, 0, fake, fake, None) == C.KVS_ERR_ARG
+    assert lib.kvs_prune_topk_multi(by(dm), fake, 10, 2, None, 0, fake, fake, None) == C.KVS_ERR_ARG
+    assert lib.kvs_prune_topk_multi(by(dm), fake, 10, 2, ks, -1, fake, fake, None) == C.KVS_ERR_ARG
+    assert lib.kvs_prune_topk_multi(by(dm), fake + 4, 10, 2, ks, 0, fake, fake, None) == C.KVS_ERR_ALIGN
+    assert lib.kvs_prune_topk_multi(by(dm), fake, 10, 2, ks, 0, None, fake, None) == C.KVS_ERR_ARG
+    # quantile threshold: q outside [0, 1] (NaN included), null tau, negative window
+    f = ctypes.c_float
+    for q in (-0.5, 1.5, float("nan")):
+        assert lib.kvs_prune_quantile(by(dm), fake, 10, f(q), 0, fake, fake, fake, None) == C.KVS_ERR_ARG
+    assert lib.kvs_prune_quantile(by(dm), fake, 10, f(0.25), 0, None, fake, fake, None) == C.KVS_ERR_ARG
+    assert lib.kvs_prune_quantile(by(dm), fake, 10, f(0.25), -3, fake, fake, fake, None) == C.KVS_ERR_ARG
+    # compaction of several masks: no mask, workspace of one mask only, bad page size
+    need1 = lib.kvs_compact_workspace_size(by(dm), 100)
+    need3 = lib.kvs_compact_multi_workspace_size(by(dm), 100, 3)
+    assert need3 > need1 and lib.kvs_compact_multi_workspace_size(by(dm), 100, 0) == 0
+    args = lambda n, ws: (by(dm), fake, fake, 100, n, fake, 16, fake, fake, 1000, fake, 7, fake,
+                          fake, fake, ws, None)
+    assert lib.kvs_compact_paged_multi(*args(0, need3)) == C.KVS_ERR_ARG
+    assert lib.kvs_compact_paged_multi(*args(3, need1)) == C.KVS_ERR_CAPACITY
+    assert "workspace" in C.kvs_last_error()
+    st = lib.kvs_compact_paged_multi(by(dm), fake, fake, 100, 3, fake, 5000, fake, fake, 1000,
+                                     fake, 7, fake, fake, fake, need3, None)
+    assert st == C.KVS_ERR_UNSUPPORTED
+
+
 def test_version_string(capi):
     assert "sm_103a" in capi.kvs_version()
 
