@@ -4,18 +4,22 @@
 // and two blocked triangular solves U^T Y = R, U X = Y.  Every factorisation step is one
 // launch over all problems, so the trailing updates (the bulk of the work) spread over
 // the whole GPU instead of one CTA per problem:
-//   per 64-row panel p:  factor the diagonal block (one CTA per problem), solve the row
-//                        panel U_pp^T X = [G[p][p+64:] | R[p]] (CTAs over 64-column
+//   per 64-row panel p:  factor the diagonal block and invert it, W = U_pp^-T (one CTA
+//                        per problem; the identity rides along the elimination), form
+//                        the row panel X = W [G[p][p+64:] | R[p]] (CTAs over 64-column
 //                        blocks), update the trailing upper triangle G -= X^T X and the
 //                        trailing rows of R (CTAs over 64 x 64 tiles)
 // R rides along as extra columns of the factorised matrix, so the forward solve U^T Y = R
 // is done when the factorisation is.  The backward solve U X = Y then runs as one launch:
 // the column blocks of right-hand sides are independent, so one CTA per (problem, column
-// block) takes the whole sweep, each diagonal block's triangular solve followed by the
-// update of every block row above it.
-// G arrives as its upper block triangle (the Gram kernel writes only those tiles); the
-// lower triangle is never read.  Rows/columns k .. M-1 (padding of the kept-key
-// dimension) are decoupled: their diagonal becomes 1 and their right-hand side 0.
+// block) takes the whole sweep, each diagonal block's product X[p] = W^T Y[p] followed by
+// the update of every block row above it.  Only the diagonal blocks' factorisations are
+// serial chains (64 pivots each); the triangular solves are products with the inverted
+// diagonal blocks.
+// G arrives as its upper block triangle (the Gram kernel writes only those tiles); its
+// lower triangle is never read, and the factorisation keeps each W in the strictly lower
+// part of its diagonal block.  Rows/columns k .. M-1 (padding of the kept-key dimension)
+// are decoupled: their diagonal becomes 1 and their right-hand side 0.
 #include <math.h>
 
 #include <algorithm>
@@ -83,128 +87,126 @@ __device__ __forceinline__ void shift_axpy(float (&x)[NB], const float* wrow, fl
 }
 
 // Pivots r0 .. r0+15 of the diagonal block (see potrf_kernel); W registers are live.
+// One barrier per pivot: the owners of the block's columns c >= r publish their raw
+// row-r entries into raw[r & 1] (two buffers, so a pivot's writes never meet the
+// previous pivot's reads), and every thread derives the pivot's inverse square root
+// from raw[r & 1][0] itself.  With d = A'[r][r], U[r][c] = A'[r][c] / sqrt(d), and the
+// rank-1 update of column c is x[i] -= A'[r][r+i] * (A'[r][c] / d).
 template <int W>
-__device__ __forceinline__ void potrf_steps(float (&x)[NB], int r0, int c, float* G, int ldg,
-                                            float* prow, float* pinv) {
+__device__ __forceinline__ void potrf_steps(float (&x)[NB], int r0, int c, bool carried,
+                                            float* D, int ldg, float (*raw)[NB]) {
 #pragma unroll 1
   for (int r = r0; r < r0 + 16; ++r) {
-    if (c == r) {
-      const float v = x[0];
-      if (!(v > 0.f)) atomicCAS(&g_chol_error, 0, kErrNotSpd);
-      const float piv = sqrtf(fmaxf(v, 1e-30f));
-      G[(size_t)r * ldg + r] = piv;
-      *pinv = 1.f / piv;
-    }
+    float* row = raw[r & 1];
+    if (!carried && c >= r) row[c - r] = x[0];
     __syncthreads();
-    float xr = 0.f;
-    if (c > r) {
-      xr = x[0] * *pinv;
-      G[(size_t)r * ldg + c] = xr;
-      prow[c - r] = xr;
+    const float dv = fmaxf(row[0], 1e-30f);
+    const float pinv = rsqrtf(dv);  // 1 / U[r][r]
+    const float xr = x[0] * pinv;  // U[r][c] (block columns) or W[r][c] (carried identity)
+    float t = 0.f;
+    if (!carried) {
+      if (c == r) {
+        if (!(row[0] > 0.f)) atomicCAS(&g_chol_error, 0, kErrNotSpd);
+        D[(size_t)r * ldg + r] = dv * pinv;
+      } else if (c > r) {
+        D[(size_t)r * ldg + c] = xr;
+        t = xr * pinv;
+      }
+    } else {
+      if (r > c) D[(size_t)r * ldg + c] = xr;  // W strictly below the diagonal
+      t = xr * pinv;
     }
-    __syncthreads();
-    // columns c > r: rows r+1 .. c; past c the registers hold nothing that is stored
-    shift_axpy<W>(x, prow, xr);
-    __syncthreads();  // prow is rewritten by the next pivot
-    if (c > r) prow[c - r] = 0.f;
+    // columns c > r: rows r+1 .. c; past c (and past the block) the registers hold
+    // nothing that is stored
+    shift_axpy<W>(x, row, t);
   }
 }
 
-// Cholesky of the diagonal block at p (upper, in place), one CTA of 64 threads per
-// problem: thread c keeps column c of the block in registers; per pivot r the owner of
-// column r takes the square root, every later column scales its row-r entry, stores it
-// and publishes it, and each column applies the rank-1 update to its own entries.
-__global__ void __launch_bounds__(NB) potrf_kernel(const CholArgs a, int p) {
-  float* G = prob(a.g, (size_t)a.M * a.ldg) + (size_t)p * a.ldg + p;
-  const int c = threadIdx.x;
-  __shared__ __align__(16) float prow[NB];  // prow[i] = U[r][r + i] (i >= 1), 0 past the block
-  __shared__ float pinv;
+// Cholesky of the diagonal block at p (upper, in place) and W = U_pp^-T, one CTA of 128
+// threads per problem.  Threads 0..63 keep column c of the block in registers; threads
+// 64..127 keep column c of the identity, which rides along as right-hand sides, so the
+// forward elimination that factors the block turns it into U_pp^-T.  Per pivot r the
+// block's columns store U[r][c] and the identity's store W[r][c] (r > c) into the
+// block's lower triangle, which nothing else reads; W's diagonal is 1 / U[r][r].
+__global__ void __launch_bounds__(2 * NB) potrf_kernel(const CholArgs a, int p) {
+  float* D = prob(a.g, (size_t)a.M * a.ldg) + (size_t)p * a.ldg + p;
+  const bool carried = threadIdx.x >= NB;
+  const int c = threadIdx.x & (NB - 1);
+  __shared__ __align__(16) float raw[2][NB];
   float x[NB];
 #pragma unroll
-  for (int i = 0; i < NB; ++i) x[i] = i <= c ? G[(size_t)i * a.ldg + c] : 0.f;
-  prow[c] = 0.f;
-  potrf_steps<64>(x, 0, c, G, a.ldg, prow, &pinv);
-  potrf_steps<48>(x, 16, c, G, a.ldg, prow, &pinv);
-  potrf_steps<32>(x, 32, c, G, a.ldg, prow, &pinv);
-  potrf_steps<16>(x, 48, c, G, a.ldg, prow, &pinv);
+  for (int i = 0; i < NB; ++i)
+    x[i] = carried ? (i == c ? 1.f : 0.f) : (i <= c ? D[(size_t)i * a.ldg + c] : 0.f);
+  raw[0][c] = 0.f;
+  raw[1][c] = 0.f;
+  __syncthreads();
+  potrf_steps<64>(x, 0, c, carried, D, a.ldg, raw);
+  potrf_steps<48>(x, 16, c, carried, D, a.ldg, raw);
+  potrf_steps<32>(x, 32, c, carried, D, a.ldg, raw);
+  potrf_steps<16>(x, 48, c, carried, D, a.ldg, raw);
 }
 
-// Triangular solve of 64 rows in registers against the staged diagonal block (rows of w
-// pre-shifted as above, dinv = 1 / diag), one column per thread; row r of the solution
-// is written to out[r * ld] as soon as it is final.  Forward: U^T y = x with x[i] = row i
-// initially; backward: U y = x with x[i] = row 63 - i initially.
-template <bool BACKWARD, int W>
-__device__ __forceinline__ void tri_steps(float (&x)[NB], const float (*w)[kLd],
-                                          const float* dinv, float* out, size_t ld, int k0) {
-#pragma unroll 1
-  for (int k = k0; k < k0 + 16; ++k) {
-    const int r = BACKWARD ? NB - 1 - k : k;
-    const float xr = x[0] * dinv[r];
-    out[(size_t)r * ld] = xr;
-    shift_axpy<W>(x, w[r], xr);
-  }
-}
-
-template <bool BACKWARD>
-__device__ __forceinline__ void tri_solve_col(float (&x)[NB], const float (*w)[kLd],
-                                              const float* dinv, float* out, size_t ld) {
-  tri_steps<BACKWARD, 64>(x, w, dinv, out, ld, 0);
-  tri_steps<BACKWARD, 48>(x, w, dinv, out, ld, 16);
-  tri_steps<BACKWARD, 32>(x, w, dinv, out, ld, 32);
-  tri_steps<BACKWARD, 16>(x, w, dinv, out, ld, 48);
-}
-
-// Stages the diagonal block at p pre-shifted for a forward solve (w[r][i] = U[r][r+i]) or
-// a backward one (w[r][i] = U[r-i][r]), zero past the block, and 1 / diag, with NT
-// threads in one pass: each thread issues all its (coalesced) loads before it stores, and
-// the lower-triangle positions it visits map one to one onto the zero slots (forward:
-// (r, c < r) -> w[r][63 - c]; backward: (r > c, c) -> w[c][r]).
-template <int NT, bool BACKWARD>
-__device__ __forceinline__ void load_diag_block(const float* G, int ldg, int p,
-                                                float (*w)[kLd], float* dinv) {
+// W = U_pp^-T of the diagonal block at p, staged in shared memory by NT threads: with
+// TRANSPOSE, w[j][i] = W[i][j] (the columns of W as rows), else w[j][i] = W[j][i].  W's
+// strictly lower part is read from the block's lower triangle, its diagonal is
+// 1 / U[i][i], and its upper part is 0.  Each thread issues all its loads (coalesced
+// along rows of W) before it stores, so their latencies overlap.
+template <int NT, bool TRANSPOSE>
+__device__ __forceinline__ void load_winv(const float* G, int ldg, int p, float (*w)[kLd]) {
   constexpr int PER = NB * NB / NT;
+  const float* D = G + (size_t)p * ldg + p;
   float v[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) {
-    const int idx = (int)threadIdx.x + e * NT, r = idx / NB, c = idx % NB;
-    v[e] = c >= r ? G[(size_t)(p + r) * ldg + p + c] : 0.f;
+    const int idx = (int)threadIdx.x + e * NT, i = idx / NB, j = idx % NB;  // W[i][j]
+    v[e] = i >= j ? D[(size_t)i * ldg + j] : 0.f;
   }
 #pragma unroll
   for (int e = 0; e < PER; ++e) {
-    const int idx = (int)threadIdx.x + e * NT, r = idx / NB, c = idx % NB;
-    if (BACKWARD) {
-      if (c >= r)
-        w[c][c - r] = v[e];
-      else
-        w[c][r] = 0.f;
-    } else {
-      if (c >= r)
-        w[r][c - r] = v[e];
-      else
-        w[r][NB - 1 - c] = 0.f;
-    }
+    const int idx = (int)threadIdx.x + e * NT, i = idx / NB, j = idx % NB;
+    const float wv = i == j ? 1.f / v[e] : v[e];
+    if (TRANSPOSE)
+      w[j][i] = wv;
+    else
+      w[i][j] = wv;
   }
-  __syncthreads();
-  if (threadIdx.x < NB) dinv[threadIdx.x] = 1.f / w[threadIdx.x][0];
-  __syncthreads();
 }
 
-// Row panel: X = U_pp^-T B for the 64 columns of block blockIdx.x of [G[p][p+64:] | R[p]]
-// (the first `rest` blocks are G's, the next d / 64 are R's); one thread per column
-__global__ void __launch_bounds__(NB) trsm_row_kernel(const CholArgs a, int p, int rest) {
+// Row panel: X = W B for the 64 columns of block blockIdx.x of [G[p][p+64:] | R[p]] (the
+// first `rest` blocks are G's, the next d / 64 are R's), W = U_pp^-T from the diagonal
+// block; 256 threads, 4 x 4 results each, written over B.
+__global__ void __launch_bounds__(256) panel_kernel(const CholArgs a, int p, int rest) {
   float* G = prob(a.g, (size_t)a.M * a.ldg);
   float* R = prob(a.r, (size_t)a.M * a.d);
   const bool in_r = (int)blockIdx.x >= rest;
-  float* col = in_r ? R + (size_t)p * a.d + (blockIdx.x - rest) * NB + threadIdx.x
-                    : G + (size_t)p * a.ldg + p + NB + blockIdx.x * NB + threadIdx.x;
+  float* blk = in_r ? R + (size_t)p * a.d + (blockIdx.x - rest) * NB
+                    : G + (size_t)p * a.ldg + p + NB + blockIdx.x * NB;
   const size_t ld = in_r ? (size_t)a.d : (size_t)a.ldg;
-  __shared__ __align__(16) float w[NB][kLd];
-  __shared__ float dinv[NB];
-  load_diag_block<NB, false>(G, a.ldg, p, w, dinv);
-  float x[NB];
+  __shared__ __align__(16) float wt[NB][kLd];  // wt[j][i] = W[i][j]
+  __shared__ __align__(16) float bs[NB][kLd];  // bs[j][c] = B[j][c]
+  load_winv<256, true>(G, a.ldg, p, wt);
+  for (int idx = threadIdx.x; idx < NB * NB / 4; idx += 256) {
+    const int r = idx / (NB / 4), c = (idx % (NB / 4)) * 4;
+    *reinterpret_cast<float4*>(&bs[r][c]) =
+        *reinterpret_cast<const float4*>(blk + (size_t)r * ld + c);
+  }
+  __syncthreads();
+  const int tr = (threadIdx.x / 16) * 4, tc = (threadIdx.x % 16) * 4;
+  float acc[4][4] = {};
+#pragma unroll 8
+  for (int j = 0; j < NB; ++j) {  // X[i][c] = sum_j W[i][j] B[j][c]
+    const float4 a4 = *reinterpret_cast<const float4*>(&wt[j][tr]);
+    const float4 b4 = *reinterpret_cast<const float4*>(&bs[j][tc]);
+    const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-  for (int r = 0; r < NB; ++r) x[r] = col[(size_t)r * ld];
-  tri_solve_col<false>(x, w, dinv, col, ld);
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    *reinterpret_cast<float4*>(blk + (size_t)(tr + u) * ld + tc) =
+        make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
 }
 
 // Trailing update after panel p, 256 threads, 4 x 4 each.  Blocks below nt (nt + 1) / 2:
@@ -274,44 +276,61 @@ __global__ void __launch_bounds__(256) syrk_kernel(const CholArgs a, int p) {
 
 // Backward solve U X = Y of one problem and one block of CB right-hand-side columns (Y
 // is in R: the forward solve rode along with the factorisation); the column blocks are
-// independent, so each CTA runs the whole chain with no other launch (narrow blocks give
-// more CTAs, whose latency chains overlap).  Per 64-row block p, descending: the diagonal
-// solve in registers (threads 0..CB-1, one column each) into the stage ys, then every
-// block row q above it is updated, R[q] -= U[q][p] X[p] (64 x 64 x CB; a thread owns
-// CB/16 rows x 4 columns).  The next block row's U block is loaded into registers while
-// the current one is multiplied, and a thread's R tile is read before the products so
-// that its loads overlap them.  X rows below k go to the output.
+// independent, so each CTA runs the whole sweep with no other launch.  Per 64-row block
+// p, descending: X[p] = U_pp^-1 Y[p] = W^T Y[p] with the factorisation's W = U_pp^-T
+// (64 x 64 x CB), then every block row q above it is updated, R[q] -= U[q][p] X[p]
+// (64 x 64 x CB); a thread owns CB/16 rows x 4 columns of both products.  The next block
+// row's U block is loaded into registers while the current one is multiplied, and a
+// thread's R tile is read before the products so that its loads overlap them.  X rows
+// below k go to the output.
 template <int CB>
 __global__ void __launch_bounds__(256, CB == 64 ? 1 : 2) solve_kernel(const CholArgs a) {
   constexpr int CG = CB / 4;      // groups of 4 columns
-  constexpr int RPT = CB / 16;    // rows per thread in the updates
-  constexpr int LDY = CB + 4;     // ys row stride (16-byte aligned rows)
+  constexpr int RPT = CB / 16;    // rows per thread in the products
+  constexpr int LDY = CB + 4;     // row stride of yin / ys (16-byte aligned rows)
   constexpr int UPT = NB * NB / 256;  // U block elements per thread
   static_assert(RPT >= 1 && (256 / CG) * RPT == NB, "column block of 16, 32 or 64");
   const float* G = prob(a.g, (size_t)a.M * a.ldg);
   float* R = prob(a.r, (size_t)a.M * a.d);
   float* X = prob(a.x, (size_t)a.k * a.d);
   const int c0 = blockIdx.x * CB, tid = threadIdx.x, nb = a.M / NB;
-  __shared__ __align__(16) float w[NB][kLd];  // diagonal block, pre-shifted
-  __shared__ float dinv[NB];
-  __shared__ __align__(16) float ys[NB][LDY];  // solved rows of block p
-  __shared__ __align__(16) float us[NB][kLd];  // us[r][i] = U[q+i][p+r]
+  __shared__ __align__(16) float yin[NB][LDY];  // right-hand sides of block p
+  __shared__ __align__(16) float ys[NB][LDY];   // solved rows of block p
+  __shared__ __align__(16) float us[NB][kLd];   // W of block p, then us[r][i] = U[q+i][p+r]
   const int tq = (tid / CG) * RPT, tc = (tid % CG) * 4;
   for (int p = (nb - 1) * NB; p >= 0; p -= NB) {
-    // the previous block's reads of w, ys and us are done and its updates of R visible
+    // the previous block's reads of ys and us are done and its updates of R visible
     __syncthreads();
-    float x[NB];
-    if (tid < CB) {  // the block's right-hand sides, in flight while w is staged
+    load_winv<256, false>(G, a.ldg, p, us);  // us[j][i] = W[j][i]
+    for (int idx = tid; idx < NB * CG; idx += 256) {
+      const int r = idx / CG, c = (idx % CG) * 4;
+      *reinterpret_cast<float4*>(&yin[r][c]) =
+          *reinterpret_cast<const float4*>(R + (size_t)(p + r) * a.d + c0 + c);
+    }
+    __syncthreads();
+    {  // X[p][i][c] = sum_j W[j][i] Y[p][j][c]
+      float acc[RPT][4] = {};
+#pragma unroll 8
+      for (int j = 0; j < NB; ++j) {
+        const float4 b4 = *reinterpret_cast<const float4*>(&yin[j][tc]);
+        const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+        float av[RPT];
 #pragma unroll
-      for (int i = 0; i < NB; ++i) x[i] = R[(size_t)(p + NB - 1 - i) * a.d + c0 + tid];
+        for (int u = 0; u < RPT; ++u) av[u] = us[j][tq + u];
+#pragma unroll
+        for (int u = 0; u < RPT; ++u)
+#pragma unroll
+          for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
+      }
+#pragma unroll
+      for (int u = 0; u < RPT; ++u) {
+        const float4 x4 = make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+        *reinterpret_cast<float4*>(&ys[tq + u][tc]) = x4;
+        if (p + tq + u < a.k)
+          *reinterpret_cast<float4*>(X + (size_t)(p + tq + u) * a.d + c0 + tc) = x4;
+      }
     }
-    load_diag_block<256, true>(G, a.ldg, p, w, dinv);
-    if (tid < CB) tri_solve_col<true>(x, w, dinv, &ys[0][tid], LDY);
-    __syncthreads();
-    for (int idx = tid; idx < NB * CB; idx += 256) {
-      const int r = idx / CB, c = idx % CB;
-      if (p + r < a.k) X[(size_t)(p + r) * a.d + c0 + c] = ys[r][c];
-    }
+    __syncthreads();  // ys is complete and us free for the U blocks
     // U[q+i][p+j] of block row q (consecutive threads read consecutive addresses)
     float ureg[UPT];
     auto load_u = [&](int q) {
@@ -373,8 +392,8 @@ cudaError_t launch_chol_solve(const CholArgs& a, cudaStream_t s) {
   ++launches;
   for (int b = 0; b < nb; ++b) {  // G + lam I = U^T U, and Y = U^-T R alongside
     const int p = b * NB, rest = nb - b - 1;
-    potrf_kernel<<<dim3(1, B), NB, 0, s>>>(a, p);
-    trsm_row_kernel<<<dim3(rest + dcb, B), NB, 0, s>>>(a, p, rest);
+    potrf_kernel<<<dim3(1, B), 2 * NB, 0, s>>>(a, p);
+    panel_kernel<<<dim3(rest + dcb, B), 256, 0, s>>>(a, p, rest);
     launches += 2;
     if (rest > 0) {
       syrk_kernel<<<dim3(rest * (rest + 1) / 2 + rest * dcb, B), 256, 0, s>>>(a, p);
