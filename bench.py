@@ -54,6 +54,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "context KV tokens scored+pruned/s per layer (all heads); % of tensor/HBM roofline"
 UNIT = "tokens/s/layer"
+# a contraction timed over at least this much back-to-back replay runs under the power cap
+LONG_RUN_MS = 1000.0
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -385,8 +387,15 @@ def run_gpu(args, rank, world, local):
         if amount is not None:
             if unit == "flop":
                 ach = amount / (t / 1e3) / 1e12
+                # a contraction whose timed replays run back to back for a second or more
+                # is held to the power-capped (sustained) tensor peak, a shorter one to
+                # the burst peak; both fractions are reported
+                sustained = reps * t >= LONG_RUN_MS
+                pk = tc_sus if sustained else tc_peak
                 k.update(bound="tensor", achieved=round(ach, 2), unit="TFLOP/s",
-                         peak=tc_peak, frac=round(ach / tc_peak, 4),
+                         peak=pk, frac=round(ach / pk, 4),
+                         peak_kind="sustained" if sustained else "burst",
+                         frac_burst=round(ach / tc_peak, 4),
                          frac_sustained=round(ach / tc_sus, 4))
             else:
                 ach = amount / (t / 1e3) / 1e9
@@ -401,10 +410,20 @@ def run_gpu(args, rank, world, local):
     dk = kernels[dom]
     roofline = {"kernel": dom, "bound": dk.get("bound"), "achieved": dk.get("achieved"),
                 "peak": dk.get("peak"), "unit": dk.get("unit"), "frac": dk.get("frac"),
-                "peak_source": f"{src} (MEASURED_PEAKS.json burst)" if src == "measured" else
-                "fallback", "traffic": None}
+                "traffic": None}
     if dk.get("bound") == "tensor":
-        roofline.update(peak_sustained=tc_sus, frac_sustained=dk.get("frac_sustained"))
+        kind = dk["peak_kind"]
+        key = "bf16_tflops_sustained" if kind == "sustained" else "bf16_tflops"
+        roofline["peak_source"] = (
+            f"{src} (MEASURED_PEAKS.json {key}: the stage's {reps} timed replays ran "
+            f"{reps * stage_ms[dom] / 1e3:.2f} s back to back"
+            + (", so the power-capped peak applies)" if kind == "sustained" else ")")
+            if src == "measured" else "fallback")
+        roofline.update(peak_burst=tc_peak, frac_burst=dk.get("frac_burst"),
+                        peak_sustained=tc_sus, frac_sustained=dk.get("frac_sustained"))
+    else:
+        roofline["peak_source"] = (f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
+                                   else "fallback")
     roofline["traffic"] = read_traffic(wl.name, dom)
 
     # ---------------------------------------------------------------- end to end

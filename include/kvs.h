@@ -294,6 +294,9 @@ kvs_status kvs_prune_mask(const kvs_dims* dims, const float* score, int32_t T, i
  *   keep t of head h  <=>  score[l][h][t] >= tau[l]  or  t >= T - w
  *   score [L][H_kv][T] fp32;  tau [L] fp32 output (device);  mask [L][H_kv][T] uint8
  *   output;  keep [L][H_kv] int32 output.  0 <= q <= 1, else KVS_ERR_ARG.
+ * Every byte of mask and keep is written; until the masks are, the call keeps its
+ * selection state in them (layers of at least 65536 non-window scores, with rows of at
+ * least 4096, select over many blocks per layer), so neither may alias score or tau.
  * ------------------------------------------------------------------------------- */
 kvs_status kvs_prune_quantile(const kvs_dims* dims, const float* score, int32_t T, float q,
                               int32_t w, float* tau, uint8_t* mask, int32_t* keep, void* stream);

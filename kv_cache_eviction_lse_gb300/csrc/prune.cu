@@ -10,7 +10,11 @@
 // the k-th key is found by an exact 4-pass radix select on order-preserving 32-bit
 // keys (shared-memory histograms), then ties at the k-th key go to the lowest
 // positions via a block-wide ordered scan.  Deterministic, no sorting.  One launch
-// selects any number (up to kMaxTopkBudgets) of budgets over the same scores.
+// selects any number (up to kMaxTopkBudgets) of budgets over the same scores.  The
+// quantile's select runs the same radix passes over a whole layer, spread over many
+// blocks per layer for long rows (one launch per digit).
+#include <algorithm>
+
 #include "common.cuh"
 #include "prune.cuh"
 
@@ -189,6 +193,122 @@ __global__ void __launch_bounds__(kPruneThreads) quantile_kernel(const float* __
   if (threadIdx.x == 0) tau[l] = key_value(s_prefix);
 }
 
+// The same selection spread over many blocks per layer, one launch per 8-bit digit:
+// block (h, b) of layer l histograms its part of row h (keys that match the digits
+// already chosen) and stores the histogram; the block that finishes last (an atomic
+// ticket, so nobody waits) adds the layer's histograms, picks the digit and the rank
+// left inside it, and after the last digit writes tau[l].  The layer's mask rows, which
+// the threshold pass rewrites afterwards, hold this state (16-byte aligned at the start
+// of the layer's H_kv T mask bytes): the chosen prefix and remaining rank, then one
+// 256-bin histogram per block.  keep[l H_kv] (zeroed before the first digit) counts the
+// tickets and is zeroed again after the last.
+constexpr int kQThreads = 256;
+constexpr long long kQuantileMultiMin = 65536;  // fewer values: one block per layer
+constexpr int kQuantilePerBlock = 4096;         // values per block (at least)
+constexpr int kQuantileMaxSplit = 8;            // blocks per row (at most)
+
+struct QuantileState {
+  uint32_t prefix;
+  uint32_t pad;
+  long long rem;
+};
+
+__device__ __forceinline__ QuantileState* quantile_state(uint8_t* mask, int l, size_t slice) {
+  uintptr_t p = reinterpret_cast<uintptr_t>(mask + (size_t)l * slice);
+  p = (p + 15u) & ~(uintptr_t)15u;
+  return reinterpret_cast<QuantileState*>(p);
+}
+
+__global__ void __launch_bounds__(kQThreads) quantile_digit_kernel(
+    const float* __restrict__ score, int Hkv, int T, int w, float q, int split, int pass,
+    float* __restrict__ tau, uint8_t* __restrict__ mask, int* __restrict__ keep) {
+  __shared__ unsigned hist[256];
+  __shared__ int s_last;
+  const int l = blockIdx.y, blk = blockIdx.x, nblk = Hkv * split;
+  const int h = blk / split, b = blk % split;
+  const int n = T - min(max(w, 0), T);
+  QuantileState* st = quantile_state(mask, l, (size_t)Hkv * T);
+  unsigned* partial = reinterpret_cast<unsigned*>(st + 1);
+  const int shift = 24 - 8 * pass;
+  const uint32_t hi_mask = pass == 0 ? 0u : 0xffffffffu << (32 - 8 * pass);
+  const uint32_t prefix = pass == 0 ? 0u : st->prefix;  // chosen by the previous launch
+  const int tid = threadIdx.x;
+  hist[tid] = 0u;
+  __syncthreads();
+  const int chunk = (n + split - 1) / split;
+  const int t0 = b * chunk, t1 = min(n, t0 + chunk);
+  const float* s = score + ((size_t)l * Hkv + h) * T;
+  constexpr int kBatch = 8;  // loads in flight per thread before the histogram updates
+  for (int tb = t0 + tid; tb < t1; tb += kBatch * kQThreads) {
+    float x[kBatch];
+#pragma unroll
+    for (int e = 0; e < kBatch; ++e) {
+      const int t = tb + e * kQThreads;
+      x[e] = t < t1 ? __ldg(s + t) : 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < kBatch; ++e) {
+      const uint32_t u = order_key(x[e]);
+      if (tb + e * kQThreads < t1 && (u & hi_mask) == prefix)
+        atomicAdd(&hist[(u >> shift) & 255u], 1u);
+    }
+  }
+  __syncthreads();
+  partial[(size_t)blk * 256 + tid] = hist[tid];
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&keep[(size_t)l * Hkv], 1) == (pass + 1) * nblk - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  unsigned acc[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // eight loads in flight
+  int i = 0;
+  for (; i + 8 <= nblk; i += 8) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] += __ldcg(&partial[(size_t)(i + e) * 256 + tid]);
+  }
+  for (; i < nblk; ++i) acc[0] += __ldcg(&partial[(size_t)i * 256 + tid]);
+  hist[tid] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+  __syncthreads();
+  if (tid < 32) {
+    // lane l owns digits 8l .. 8l+7; find the digit at which the count of keys from the
+    // bottom passes the remaining rank
+    const int lane = tid;
+    long long c[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      c[i] = hist[8 * lane + i];
+      sum += c[i];
+    }
+    long long incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const long long N = (long long)Hkv * n;
+    const long long r = pass == 0 ? (long long)floor((double)q * (double)(N - 1)) : st->rem;
+    const unsigned hit = __ballot_sync(0xffffffffu, incl > r);
+    const int src = __ffs(hit) - 1;  // first lane whose range passes rank r
+    if (lane == src) {
+      long long cum = incl - sum;
+      int i = 0;
+      for (; i < 7; ++i) {
+        if (cum + c[i] > r) break;
+        cum += c[i];
+      }
+      const uint32_t pre = prefix | ((uint32_t)(8 * lane + i) << shift);
+      if (pass == 3) {
+        tau[l] = key_value(pre);
+        keep[(size_t)l * Hkv] = 0;
+      } else {
+        st->prefix = pre;
+        st->rem = r - cum;
+      }
+    }
+  }
+}
+
 // One block per (row, budget): grid (rows, n_budgets).  Rows of up to kStageMaxT scores
 // are staged once in shared memory as order keys (the radix passes then read shared
 // memory); longer rows are read from global memory in every pass.  The last radix pass
@@ -361,8 +481,18 @@ cudaError_t launch_prune_quantile(const float* score, int L, int Hkv, int T, flo
   if (L == 0) return cudaSuccess;
   cudaError_t e = cudaMemsetAsync(keep, 0, sizeof(int) * (size_t)L * Hkv, s);
   if (e != cudaSuccess) return e;
-  count_launches(1);
-  quantile_kernel<<<L, kPruneThreads, 0, s>>>(score, Hkv, T, w, q, tau);
+  const int n = T - std::min(std::max(w, 0), T);
+  const long long N = (long long)Hkv * n;
+  if (N >= kQuantileMultiMin && n >= kQuantilePerBlock) {  // state fits in a quarter of the mask
+    const int split = std::max(1, std::min(kQuantileMaxSplit, n / kQuantilePerBlock));
+    count_launches(4);
+    for (int pass = 0; pass < 4; ++pass)
+      quantile_digit_kernel<<<dim3(Hkv * split, L), kQThreads, 0, s>>>(score, Hkv, T, w, q,
+                                                                       split, pass, tau, mask, keep);
+  } else {
+    count_launches(1);
+    quantile_kernel<<<L, kPruneThreads, 0, s>>>(score, Hkv, T, w, q, tau);
+  }
   if (T == 0) return cudaGetLastError();
   const int per_block = kThrThreads * kThrPer;
   count_launches(1);

@@ -387,11 +387,14 @@ def test_compact_exact(C, T, page, d):
 
 
 @pytest.mark.parametrize("L,H,T,w", [(1, 1, 1, 0), (2, 3, 300, 16), (3, 8, 2048, 128),
-                                     (2, 2, 5000, 5000), (1, 4, 20001, 7)])
+                                     (2, 2, 5000, 5000), (1, 4, 20001, 7), (2, 8, 9000, 128),
+                                     (1, 3, 70001, 0), (2, 20, 4200, 100)])
 @pytest.mark.parametrize("levels,nan_frac", [(None, 0.0), (3, 0.0), (4, 0.05)])
 def test_prune_quantile_exact(C, L, H, T, w, levels, nan_frac):
     """The per-layer tau is exactly the oracle's order statistic of the same fp32 scores
-    (NaN lowest) and the masks and counts are the threshold rule with it."""
+    (NaN lowest) and the masks and counts are the threshold rule with it.  Layers of at
+    least 65536 non-window scores in rows of at least 4096 (the last three shapes, and
+    20001 x 4) take the many-blocks-per-layer select."""
     s = _scores_with_ties((L, H, T), L * T + H, levels, nan_frac)
     s[-1] += 3.0  # the last layer's scores sit higher: its own tau
     for q in (0.25, 0.0, 1.0, 0.5):
