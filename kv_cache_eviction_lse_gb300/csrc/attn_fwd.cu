@@ -8,19 +8,24 @@
 // 1. Key Terms], so that pruning pays only for pass 2 when the attention runs anyway.
 //
 // One CTA per 128 queries of one head; keys in tiles of 128 (online softmax):
-//   warp 0      TMA: the Q tile once, then K and V tiles through two 2-stage rings
-//   warp 1      owns TMEM (three S/P buffers: 3 x 128 columns; O: d columns) and issues
-//               S(j) = Q K(j)^T, then O += P(j-1) V(j-1) with P read from TMEM as the A
-//               operand and V as an MN-major operand straight from its TMA box
-//   warps 2-9   softmax, two threads per query row (one per 64-key half): read S with
-//               tcgen05.ld, agree on the row max through shared memory, p = 2^(x - m)
-//               with one ex2 each, store P as bf16 over the S columns just read
-//               (tcgen05.st), and rescale O in TMEM when the running max grows by more
-//               than 2^8 (otherwise the stale max is kept: p <= 256 stays exact enough
-//               in bf16 and the final normalisation uses the same max)
-// P never leaves TMEM, so the softmax of tile j only waits for O += P(j-1) V(j-1) when
-// it has to rescale O; an S/P buffer is released by the MMA that consumed its P, and with
-// three buffers S(j) waits for P V(j-3), which the tensor pipe finished long before.
+//   warp 0      TMA: K and V tiles through two 2-stage rings
+//   warp 1      owns TMEM (two S buffers: 2 x 128 columns; P: 64; Q: d/2; O: d) and
+//               issues S(j) = Q K(j)^T with Q read from TMEM as the A operand, then
+//               O += P(j-1) V(j-1) with P read from TMEM as the A operand and V as an
+//               MN-major operand straight from its TMA box: shared memory feeds only
+//               the B operand of either product (half of what a shared-memory A would
+//               add to the QK^T product, whose N = 128 tile would otherwise need the
+//               whole shared-memory bandwidth)
+//   warps 2-9   first copy the CTA's query rows into TMEM (two threads per row, 16-byte
+//               loads, tcgen05.st), then the softmax, two threads per query row (one per
+//               64-key half): read S with tcgen05.ld and release its buffer at once, agree
+//               on the row max through shared memory, p = 2^(x - m) with one ex2 each,
+//               store P as bf16 pairs into the P columns (tcgen05.st) once the previous
+//               P V product has read them, and rescale O in TMEM when the running max
+//               grows by more than 2^8 (otherwise the stale max is kept: p <= 256 stays
+//               exact enough in bf16 and the final normalisation uses the same max)
+// S(j + 1) only waits for the softmax to have read S(j - 1), so the tensor pipe runs
+// S(j + 1) while the softmax of tile j works; P V(j) waits for P(j).
 // The epilogue divides O by the row sum, writes it as bf16 and writes the LSE.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -45,7 +50,7 @@ constexpr int kSoftThreads = NQ * 128;
 constexpr int kThreads = 64 + kSoftThreads;
 constexpr uint32_t kBox = 128 * 128;  // 128 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr uint32_t kTmemCols = 512;
-constexpr int NSB = 3;  // S/P buffers in TMEM (O takes the columns after them)
+constexpr int NSB = 2;  // S buffers in TMEM
 constexpr uint32_t kMaxSmem = 232448;
 constexpr int kErrWaitTimeout = 1;
 constexpr int kErrSmemAlign = 3;
@@ -54,17 +59,21 @@ constexpr float kRescale = 8.f;  // log2 growth of the row max that forces a res
 template <int D>
 struct FCfg {
   static constexpr int KH = D / 64;
-  static constexpr uint32_t TILE = KH * kBox;  // one K or V tile, or the Q tile
-  static constexpr uint32_t OFF_K = TILE;       // Q at 0
+  static constexpr uint32_t TILE = KH * kBox;  // one K or V tile
+  static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + 2 * TILE;
   // separate K and V rings: K(j) is released as soon as S(j) = Q K(j)^T is done, so the
   // load of K(j+2) overlaps the softmax and P V of tile j; V(j) is held until P V(j)
   static constexpr uint32_t OFF_XM = OFF_V + 2 * TILE;     // row max exchange [2][NQ][BM]
   static constexpr uint32_t OFF_XL = OFF_XM + 2 * NQ * BM * 4;  // row sum exchange [NQ][BM]
   static constexpr uint32_t OFF_BAR = OFF_XL + NQ * BM * 4;
-  // q, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[3], s_empty[3], p[2], o[2], done
-  static constexpr uint32_t NBAR = 20;
-  static_assert(NSB * BN + D <= (int)kTmemCols, "TMEM plan");
+  // q, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p[2], o[2], done
+  static constexpr uint32_t NBAR = 18;
+  // TMEM columns: S buffers, then P (bf16 pairs of one tile), Q (bf16 pairs), O
+  static constexpr uint32_t COL_P = NSB * BN;
+  static constexpr uint32_t COL_Q = COL_P + BN / 2;
+  static constexpr uint32_t COL_O = COL_Q + D / 2;
+  static_assert(COL_O + D <= kTmemCols, "TMEM plan");
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t USED = OFF_MISC + 16;
   static constexpr uint32_t SMEM = (USED + 1024 <= kMaxSmem) ? USED + 1024 : kMaxSmem;
@@ -91,7 +100,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kt,
                     const __grid_constant__ CUtensorMap tm_vt, const FwdArgs a) {
   using C = FCfg<D>;
@@ -104,24 +113,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   uint8_t* smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
-  const uint32_t sQ = sb, sK = sb + C::OFF_K, sV = sb + C::OFF_V;
+  const uint32_t sK = sb + C::OFF_K, sV = sb + C::OFF_V;
   float* xm = reinterpret_cast<float*>(smem + C::OFF_XM);
   float* xl = reinterpret_cast<float*>(smem + C::OFF_XL);
   const uint32_t bar0 = sb + C::OFF_BAR;
-  const uint32_t bar_q = bar0;
+  const uint32_t bar_q = bar0;  // the query rows are in TMEM (softmax threads arrive)
   auto bar_kfull = [&](int s) { return bar0 + 8u * (1 + s); };
   auto bar_kempty = [&](int s) { return bar0 + 8u * (3 + s); };
   auto bar_vfull = [&](int s) { return bar0 + 8u * (5 + s); };
   auto bar_vempty = [&](int s) { return bar0 + 8u * (7 + s); };
-  auto bar_sfull = [&](int s) { return bar0 + 8u * (9 + s); };    // S buffer s = j % NSB
-  auto bar_sempty = [&](int s) { return bar0 + 8u * (12 + s); };
-  // P(i) is ready on p[i & 1] and O += P(i) V(i) completes on o[i & 1]: with the softmax
-  // free to run a tile ahead of the MMAs (and to skip its waits for O), alternating
-  // barriers keep every parity wait unambiguous: P(i+2) needs S(i+2), issued only after
-  // the wait for P(i), and S(i+1) implies that P V(i-1) is done
-  auto bar_p = [&](int i) { return bar0 + 8u * (15 + (i & 1)); };
-  auto bar_o = [&](int i) { return bar0 + 8u * (17 + (i & 1)); };
-  const uint32_t bar_done = bar0 + 8u * 19;
+  auto bar_sfull = [&](int s) { return bar0 + 8u * (9 + s); };    // S buffer s = j & 1
+  auto bar_sempty = [&](int s) { return bar0 + 8u * (11 + s); };  // the softmax read it
+  // P(i) is ready on p[i & 1] and O += P(i) V(i) completes on o[i & 1]: the softmax waits
+  // for P V(i - 1) before it writes P(i), so neither barrier can run two phases ahead of
+  // a waiter and every parity wait is unambiguous
+  auto bar_p = [&](int i) { return bar0 + 8u * (13 + (i & 1)); };
+  auto bar_o = [&](int i) { return bar0 + 8u * (15 + (i & 1)); };
+  const uint32_t bar_done = bar0 + 8u * 17;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
 
@@ -138,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = n_ctx + (min(a.n_tail, max(0, kv_end - a.T)) + BN - 1) / BN;
 
   if (threadIdx.x == 0) {
-    tc::mbar_init(bar_q, 1);
+    tc::mbar_init(bar_q, kSoftThreads);
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(bar_kfull(s), 1);
       tc::mbar_init(bar_kempty(s), 1);
@@ -146,10 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(bar_vempty(s), 1);
       tc::mbar_init(bar_o(s), 1);
       tc::mbar_init(bar_p(s), kSoftThreads);
-    }
-    for (int s = 0; s < NSB; ++s) {
       tc::mbar_init(bar_sfull(s), 1);
-      tc::mbar_init(bar_sempty(s), 1);  // released by the MMA that read P from it
+      tc::mbar_init(bar_sempty(s), kSoftThreads);
     }
     tc::mbar_init(bar_done, 1);
     misc[1] = 0u;
@@ -160,22 +166,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    tc::tma_prefetch_desc(&tm_q);
     tc::tma_prefetch_desc(&tm_k);
     tc::tma_prefetch_desc(&tm_v);
   }
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = misc[0];
-  const uint32_t t_o = tmem + NSB * BN;  // O accumulator columns [384, 384 + D)
+  const uint32_t t_p = tmem + C::COL_P;  // P of the current tile: BN / 2 columns
+  const uint32_t t_q = tmem + C::COL_Q;  // the query rows: D / 2 columns
+  const uint32_t t_o = tmem + C::COL_O;  // O accumulator: D columns
 
   if (warp == 0) {
     // ============================================================ TMA producer
     if (lane == 0) {
-      tc::mbar_expect_tx(bar_q, C::TILE);
-#pragma unroll
-      for (int kh = 0; kh < C::KH; ++kh)
-        tc::tma_load_3d(sQ + kh * kBox, &tm_q, bar_q, kh * 64, row0, l * a.Hq + hq);
       // loads in the order the MMAs use them: K(0), K(1), V(0), K(2), V(1), ...
       const int head = l * a.Hkv + hk;
       auto load = [&](bool is_v, int j) -> bool {
@@ -207,7 +210,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         fail(abort_flag, kErrWaitTimeout);
         // let the copies already in flight land before the CTA exits
-        tc::mbar_wait(bar_q, 0);
         for (int i = max(0, nk - 2); i < nk; ++i) tc::mbar_wait(bar_kfull(i & 1), (i >> 1) & 1);
         for (int i = max(0, nv - 2); i < nv; ++i) tc::mbar_wait(bar_vfull(i & 1), (i >> 1) & 1);
       }
@@ -217,27 +219,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16(BM, BN);
       constexpr uint32_t idesc_o = tc::idesc_bf16_bmn(BM, D);
-      bool ok = tc::mbar_wait(bar_q, 0);
+      bool ok = tc::mbar_wait(bar_q, 0) && !*abort_flag;
+      tc::fence_after_sync();
       int issued = 0;  // MMA groups issued (for the final drain)
       for (int j = 0; ok && j <= ntiles; ++j) {
-        if (j < ntiles) {  // S(j) = Q K(j)^T into S/P buffer j % NSB
-          const int s = j & 1, sb3 = j % NSB;
+        if (j < ntiles) {  // S(j) = Q K(j)^T into S buffer j & 1 (Q from TMEM)
+          const int s = j & 1;
           const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-          if (!tc::mbar_wait(bar_kfull(s), ph) ||
-              !tc::mbar_wait(bar_sempty(sb3), ((uint32_t)(j / NSB) & 1u) ^ 1u) || *abort_flag) {
+          if (!tc::mbar_wait(bar_kfull(s), ph) || !tc::mbar_wait(bar_sempty(s), ph ^ 1u) ||
+              *abort_flag) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          const uint32_t d_s = tmem + (uint32_t)(sb3 * BN);
+          const uint32_t d_s = tmem + (uint32_t)(s * BN);
           const uint32_t k_s = sK + s * C::TILE;
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t o = (uint32_t)(k >> 2) * kBox + (uint32_t)(k & 3) * 32u;
-            tc::mma_bf16(d_s, tc::sdesc_sw128(sQ + o), tc::sdesc_sw128(k_s + o), idesc_s,
-                         k > 0 ? 1u : 0u);
+            tc::mma_bf16_ts(d_s, t_q + 8u * k, tc::sdesc_sw128(k_s + o), idesc_s, k > 0 ? 1u : 0u);
           }
-          tc::commit(bar_sfull(sb3));
+          tc::commit(bar_sfull(s));
           tc::commit(bar_kempty(s));
           ++issued;
         }
@@ -250,14 +252,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::fence_after_sync();
           const uint32_t v_s = sV + s * C::TILE;
-          const uint32_t p_t = tmem + (uint32_t)((jj % NSB) * BN);  // P(jj): 64 columns, bf16 pairs
 #pragma unroll
           for (int k = 0; k < BN / 16; ++k)
-            tc::mma_bf16_ts(t_o, p_t + 8u * k, tc::sdesc_sw128_mn(v_s + 2048u * k, kBox), idesc_o,
+            tc::mma_bf16_ts(t_o, t_p + 8u * k, tc::sdesc_sw128_mn(v_s + 2048u * k, kBox), idesc_o,
                             (jj > 0 || k > 0) ? 1u : 0u);
           tc::commit(bar_vempty(s));
           tc::commit(bar_o(jj));
-          tc::commit(bar_sempty(jj % NSB));  // the S/P buffer is free for S(jj + NSB)
           ++issued;
         }
       }
@@ -278,11 +278,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qr = row0 + row;          // query index
     const uint32_t lane_off = (uint32_t)(eq * 32) << 16;
     const float sc2 = rsqrtf((float)D) * kLog2e;
+    {  // this thread's half of its query row into TMEM (zeros past the last query)
+      constexpr int QW = D / 4;  // 32-bit words (bf16 pairs) per half row
+      uint32_t qv[QW];
+      if (qr < a.n_q) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.q + ((size_t)(l * a.Hq + hq) * a.n_q + qr) * D + h * (D / 2));
+#pragma unroll
+        for (int c = 0; c < QW / 4; ++c) {
+          const uint4 x = __ldg(src + c);
+          qv[4 * c] = x.x;
+          qv[4 * c + 1] = x.y;
+          qv[4 * c + 2] = x.z;
+          qv[4 * c + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < QW; ++c) qv[c] = 0u;
+      }
+      if constexpr (QW == 32)
+        tc::tmem_st32(t_q + lane_off + (uint32_t)(h * QW), qv);
+      else
+        tc::tmem_st16(t_q + lane_off + (uint32_t)(h * QW), qv);
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      tc::mbar_arrive(bar_q);
+    }
     float m_used = -1e30f, lsum = 0.f;
     bool failed = false, wait_failed = false;
     for (int j = 0; j < ntiles; ++j) {
-      const int s = j & 1, sb3 = j % NSB;  // max-exchange buffer, S/P buffer
-      bool ok = tc::mbar_wait(bar_sfull(sb3), (uint32_t)(j / NSB) & 1u) && !*abort_flag;
+      const int s = j & 1;  // max-exchange buffer and S buffer
+      bool ok = tc::mbar_wait(bar_sfull(s), (uint32_t)(j >> 1) & 1u) && !*abort_flag;
       if (tc::bar_or(2, kSoftThreads, !ok || wait_failed)) {
         failed = true;
         break;
@@ -291,8 +317,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t v[KC];
 #pragma unroll
       for (int c = 0; c < KC; c += 32)
-        tc::tmem_ld32(tmem + lane_off + (uint32_t)(sb3 * BN + h * KC + c), v + c);
+        tc::tmem_ld32(tmem + lane_off + (uint32_t)(s * BN + h * KC + c), v + c);
       tc::tmem_ld_wait();
+      tc::fence_before_sync();
+      tc::mbar_arrive(bar_sempty(s));  // S(j + 2) may overwrite the buffer now
 
       const bool ctx = j < n_ctx;
       const int kb = (ctx ? j * BN : a.T + (j - n_ctx) * BN) + h * KC;
@@ -302,16 +330,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < KC; ++c)
           if (kb + c >= lim || kb + c > off + qr) v[c] = __float_as_uint(-CUDART_INF_F);
       }
-      float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+      float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
 #pragma unroll
-      for (int c = 0; c < KC; c += 2) {
-        mx0 = fmaxf(mx0, __uint_as_float(v[c]));
-        mx1 = fmaxf(mx1, __uint_as_float(v[c + 1]));
+      for (int c = 0; c < KC; c += 8) {
+        mx0 = tc::max3(mx0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+        mx1 = tc::max3(mx1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+        mx2 = tc::max3(mx2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+        mx3 = tc::max3(mx3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
       }
-      const float mine = fmaxf(mx0, mx1) * sc2;
+      const float mine = tc::max3(mx0, mx1, fmaxf(mx2, mx3)) * sc2;
       float* xmj = xm + s * NQ * BM;
       xmj[h * BM + row] = mine;
-      named_sync(1, kSoftThreads);
+      // the NQ threads of a row are the warps eq + 2 + 4g: one named barrier per lane
+      // quarter (ids 3..6) pairs them without holding up the other quarters
+      named_sync(3 + eq, 32 * NQ);
       float mt = mine;
 #pragma unroll
       for (int g = 1; g < NQ; ++g) mt = fmaxf(mt, xmj[((h + g) % NQ) * BM + row]);
@@ -322,25 +354,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = mt;
         lsum *= factor;
       }
+      // p = 2^(x sc2 - m) with packed fp32 pairs (FFMA2 / FADD2): half the FMA-pipe
+      // instructions of scalar code, one MUFU ex2 per key
       uint32_t pk[KC / 2];
-      float ps0 = 0.f, ps1 = 0.f;
+      const float2 k2 = make_float2(sc2, sc2), nm = make_float2(-m_used, -m_used);
+      float2 a0 = make_float2(0.f, 0.f), a1 = a0;
 #pragma unroll
-      for (int c = 0; c < KC; c += 2) {
-        const float p0 = fast_exp2(fmaf(__uint_as_float(v[c]), sc2, -m_used));
-        const float p1 = fast_exp2(fmaf(__uint_as_float(v[c + 1]), sc2, -m_used));
-        ps0 += p0;
-        ps1 += p1;
+      for (int c = 0; c < KC; c += 4) {
+        const float2 y0 = __ffma2_rn(tc::f2(v[c], v[c + 1]), k2, nm);
+        const float2 y1 = __ffma2_rn(tc::f2(v[c + 2], v[c + 3]), k2, nm);
+        const float p0 = fast_exp2(y0.x), p1 = fast_exp2(y0.y);
+        const float p2 = fast_exp2(y1.x), p3 = fast_exp2(y1.y);
+        a0 = __fadd2_rn(a0, make_float2(p0, p1));
+        a1 = __fadd2_rn(a1, make_float2(p2, p3));
         pk[c / 2] = pack_bf16(p0, p1);
+        pk[c / 2 + 1] = pack_bf16(p2, p3);
       }
-      lsum += ps0 + ps1;
+      a0 = __fadd2_rn(a0, a1);
+      lsum += a0.x + a0.y;
 
-      // O is rescaled only when this row's max grew past the threshold, and only then
-      // does the softmax wait for O += P(j-1) V(j-1)
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
+      // P V(j - 1) has read P(j - 1) (and finished O) before P(j) is written; O is
+      // rescaled only when this row's max grew past the threshold
+      const bool any_need = __any_sync(0xffffffffu, need);
+      if (j > 0) {
         ok = tc::mbar_wait(bar_o(j - 1), (uint32_t)((j - 1) >> 1) & 1u) && !*abort_flag;
-        if (!ok) wait_failed = true;  // reported at the next vote
+        ok = __all_sync(0xffffffffu, ok);  // the TMEM accesses below are warp-wide
+        if (!ok) wait_failed = true;       // reported at the next vote
         tc::fence_after_sync();
-        if (ok) {
+        if (ok && any_need) {
           const uint32_t to = t_o + lane_off + (uint32_t)(h * OC);
           if constexpr (OC >= 32) {
 #pragma unroll
@@ -361,12 +402,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_st_wait();
         }
       }
-      // P of this thread's keys h*KC .. h*KC+KC-1 as bf16 pairs into columns h*KC/2 .. of
-      // the S buffer: both threads of the row read their S before the max exchange above
+      if (wait_failed) continue;  // the P columns may still be in use: leave them alone
+      // P of this thread's keys h*KC .. h*KC+KC-1 as bf16 pairs into P columns h*KC/2 ..
       if constexpr (KC == 64)
-        tc::tmem_st32(tmem + lane_off + (uint32_t)(sb3 * BN + h * (KC / 2)), pk);
+        tc::tmem_st32(t_p + lane_off + (uint32_t)(h * (KC / 2)), pk);
       else
-        tc::tmem_st16(tmem + lane_off + (uint32_t)(sb3 * BN + h * (KC / 2)), pk);
+        tc::tmem_st16(t_p + lane_off + (uint32_t)(h * (KC / 2)), pk);
       tc::tmem_st_wait();
       tc::fence_before_sync();
       tc::mbar_arrive(bar_p(j));
@@ -426,11 +467,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
   using C = FCfg<D>;
-  CUtensorMap tq, tk, tv, tkt, tvt;
-  cudaError_t e = tma_map_bf16_3d(&tq, a.q, D, a.n_q, a.L * a.Hq, BM);
-  if (e == cudaSuccess)
-    e = a.T > 0 ? tma_map_bf16_3d(&tk, a.k_ctx, D, a.T, a.L * a.Hkv, BN)
-                : tma_map_bf16_3d(&tk, a.q, D, 1, 1, BN);
+  CUtensorMap tk, tv, tkt, tvt;
+  cudaError_t e = a.T > 0 ? tma_map_bf16_3d(&tk, a.k_ctx, D, a.T, a.L * a.Hkv, BN)
+                          : tma_map_bf16_3d(&tk, a.q, D, 1, 1, BN);
   if (e == cudaSuccess)
     e = a.T > 0 ? tma_map_bf16_3d(&tv, a.v_ctx, D, a.T, a.L * a.Hkv, BN)
                 : tma_map_bf16_3d(&tv, a.q, D, 1, 1, BN);
@@ -446,7 +485,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   count_launches(1);
-  kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tkt, tvt, a);
+  kern<<<grid, kThreads, C::SMEM, s>>>(tk, tv, tkt, tvt, a);
   return cudaGetLastError();
 }
 

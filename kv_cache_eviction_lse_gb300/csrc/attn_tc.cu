@@ -129,15 +129,8 @@ __device__ __forceinline__ void fail(volatile uint32_t* abort_flag, int code) {
   atomicCAS(&g_attn_error, 0, code);
 }
 
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
-__device__ __forceinline__ float2 f2(uint32_t a, uint32_t b) {
-  return make_float2(__uint_as_float(a), __uint_as_float(b));
-}
+using tc::f2;
+using tc::max3;
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -270,5 +270,17 @@ __device__ __forceinline__ bool bar_or(int id, int nthreads, bool pred) {
   return r != 0;
 }
 
+// Maximum of three floats in one instruction (three-input max.f32).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Two raw 32-bit accumulator words as a float2 (the operand of the packed fp32 ops).
+__device__ __forceinline__ float2 f2(uint32_t a, uint32_t b) {
+  return make_float2(__uint_as_float(a), __uint_as_float(b));
+}
+
 }  // namespace tc
 }  // namespace kvs
