@@ -272,18 +272,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ============================================================ softmax + epilogue
     constexpr int OC = D / NQ;          // O columns of this thread in the rescale / epilogue
-    const int h = (warp - 2) >> 2;      // 32-key quarter of each tile (and D/4 of O)
+    const int h = (warp - 2) >> 2;      // key part of each tile (and D / NQ of O)
     const int eq = warp & 3;            // TMEM lane quarter
     const int row = eq * 32 + lane;     // query row within the tile
     const int qr = row0 + row;          // query index
     const uint32_t lane_off = (uint32_t)(eq * 32) << 16;
     const float sc2 = rsqrtf((float)D) * kLog2e;
-    {  // this thread's half of its query row into TMEM (zeros past the last query)
-      constexpr int QW = D / 4;  // 32-bit words (bf16 pairs) per half row
+    {  // this thread's part of its query row into TMEM (zeros past the last query)
+      constexpr int QW = D / (2 * NQ);  // 32-bit words (bf16 pairs) per thread
       uint32_t qv[QW];
       if (qr < a.n_q) {
         const uint4* src = reinterpret_cast<const uint4*>(
-            a.q + ((size_t)(l * a.Hq + hq) * a.n_q + qr) * D + h * (D / 2));
+            a.q + ((size_t)(l * a.Hq + hq) * a.n_q + qr) * D + h * (D / NQ));
 #pragma unroll
         for (int c = 0; c < QW / 4; ++c) {
           const uint4 x = __ldg(src + c);
@@ -298,8 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if constexpr (QW == 32)
         tc::tmem_st32(t_q + lane_off + (uint32_t)(h * QW), qv);
-      else
+      else if constexpr (QW == 16)
         tc::tmem_st16(t_q + lane_off + (uint32_t)(h * QW), qv);
+      else
+        tc::tmem_st8(t_q + lane_off + (uint32_t)(h * QW), qv);
       tc::tmem_st_wait();
       tc::fence_before_sync();
       tc::mbar_arrive(bar_q);
