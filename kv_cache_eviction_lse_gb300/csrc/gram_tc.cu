@@ -227,6 +227,15 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   const int wn = rhs ? 128 : 256;
   const int b = blockIdx.y;
   const int nkb = (a.rows + BK - 1) / BK;
+  // Only the block's rows and columns inside k_ld (d for R) are computed: a second
+  // 128-row half made only of padding is skipped, N follows the valid columns (rounded
+  // up to the MMA's multiple of 16), and the second half of a diagonal block of G, whose
+  // first 128 columns lie below the diagonal (never read), covers only the rest.
+  const int m_valid = min(WM, a.k_ld - tm * WM);
+  const int n_valid = min(wn, (rhs ? a.d : a.k_ld) - tn * wn);
+  const int n_mma = (n_valid + 15) & ~15;
+  const bool half1 = m_valid > 128;
+  const bool diag = !rhs && tm == tn;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWideStages; ++s) {
@@ -246,7 +255,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      const uint32_t bytes = 4 * kBox + (uint32_t)(wn / 64) * kBox;
+      // boxes loaded; a diagonal block of G multiplies A_S's column block by itself, so
+      // its Y operand is the X tile
+      const int nxb = (m_valid + 63) / 64, nyb = diag ? 0 : (n_valid + 63) / 64;
+      const uint32_t bytes = (uint32_t)(nxb + nyb) * kBox;
       const CUtensorMap* ym = rhs ? &tm_o : &tm_a;
       int kb = 0;
       bool ok = true;
@@ -258,10 +270,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         }
         const uint32_t st = sb + OFF_RING + s * kWideStage;
         tc::mbar_expect_tx(bar_full(s), bytes);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)  // X: A_S columns tm*256 .. +255, four 64-column boxes
+        for (int c = 0; c < nxb; ++c)  // X: A_S columns tm*256 .., 64-column boxes
           tc::tma_load_3d(st + c * kBox, &tm_a, bar_full(s), tm * WM + 64 * c, kb * BK, b);
-        for (int c = 0; c < wn / 64; ++c)
+        for (int c = 0; c < nyb; ++c)
           tc::tma_load_3d(st + kY + c * kBox, ym, bar_full(s), tn * wn + 64 * c, kb * BK, b);
       }
       if (!ok) {
@@ -272,9 +283,17 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // A and B MN-major, fp16 (format fields 0), N = wn
-      const uint32_t idesc =
-          (tc::idesc_bf16_bmn(128, wn) | (1u << 15)) & ~((1u << 7) | (1u << 10));
+      // A and B MN-major, fp16 (format fields 0); N = n_mma, or the columns from 128 on
+      // for the second half of a diagonal block.  The boxes a trimmed MMA reads past the
+      // loaded ones hold stale data that reaches only discarded rows and columns.
+      auto idesc_n = [](int n) {
+        return (tc::idesc_bf16_bmn(128, n) | (1u << 15)) & ~((1u << 7) | (1u << 10));
+      };
+      const uint32_t idesc0 = idesc_n(n_mma);
+      const int n1 = diag ? n_mma - 128 : n_mma;  // > 0 whenever half1
+      const uint32_t idesc1 = idesc_n(n1 > 0 ? n1 : 16);
+      const uint32_t c1 = diag ? 128u : 0u;       // first column of the second half
+      const uint32_t y_off = diag ? 0u : kY;       // the Y tile within a stage
       int kb = 0;
       bool ok = true;
       for (; kb < nkb; ++kb) {
@@ -288,11 +307,13 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k) {
           const uint32_t o = 2048u * k;  // 16 rows of 128 bytes
-          const uint64_t yd = tc::sdesc_sw128_mn(st + kY + o, kBox);
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh)
-            tc::mma_bf16(tmem + (uint32_t)(hh * wn), tc::sdesc_sw128_mn(st + 2 * hh * kBox + o, kBox),
-                         yd, idesc, (kb | k) != 0 ? 1u : 0u);
+          const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+          tc::mma_bf16(tmem, tc::sdesc_sw128_mn(st + o, kBox),
+                       tc::sdesc_sw128_mn(st + y_off + o, kBox), idesc0, acc);
+          if (half1)
+            tc::mma_bf16(tmem + (uint32_t)wn + c1, tc::sdesc_sw128_mn(st + 2 * kBox + o, kBox),
+                         tc::sdesc_sw128_mn(st + y_off + (c1 / 64) * kBox + o, kBox), idesc1,
+                         acc);
         }
         tc::commit(bar_empty(s));
       }
@@ -312,8 +333,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     float* crow = (rhs ? a.r : a.g) + ((size_t)b * a.k_ld + m) * ldc + tn * wn;
     const int nmax = min(wn, N - tn * wn);
     const uint32_t t0 = tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(hh * wn);
+    // the columns this half computed: none for a skipped half, from 128 on for the
+    // second half of a diagonal block
+    const int cb0 = hh == 1 ? (half1 ? (diag ? 4 : 0) : wn / 32) : 0;
 #pragma unroll 1
-    for (int cb = 0; cb < wn / 32; ++cb) {
+    for (int cb = cb0; cb < (nmax + 31) / 32; ++cb) {
       uint32_t v[32];
       tc::tmem_ld32(t0 + 32u * cb, v);
       tc::tmem_ld_wait();
