@@ -7,7 +7,8 @@
 // together with LSE_j, the normaliser the transposed scoring pass reuses [KVpop review,
 // 1. Key Terms], so that pruning pays only for pass 2 when the attention runs anyway.
 //
-// One CTA per 128 queries of one head; keys in tiles of 128 (online softmax):
+// A persistent grid (one CTA per SM) works through units of 128 queries of one head;
+// keys in tiles of 128 (online softmax):
 //   warp 0      TMA: K and V tiles through two 2-stage rings
 //   warp 1      owns TMEM (two S buffers: 2 x 128 columns; P: 64; Q: d/2; O: d) and
 //               issues S(j) = Q K(j)^T with Q read from TMEM as the A operand, then
@@ -25,8 +26,12 @@
 //               grows by more than 2^8 (otherwise the stale max is kept: p <= 256 stays
 //               exact enough in bf16 and the final normalisation uses the same max)
 // S(j + 1) only waits for the softmax to have read S(j - 1), so the tensor pipe runs
-// S(j + 1) while the softmax of tile j works; P V(j) waits for P(j).
+// S(j + 1) while the softmax of tile j works; P V(j) waits for P(j).  TMEM, barriers and
+// rings carry over between units: the next unit's K/V tiles load during this unit's last
+// ones, and its query rows are read into registers before this unit's O is finished.
 // The epilogue divides O by the row sum, writes it as bf16 and writes the LSE.
+#include <algorithm>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -98,6 +103,29 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
+// One unit of the persistent grid: 128 queries of one (layer, query head).  A CTA's
+// units visit one residue class of query tiles modulo dg = gcd(grid, tiles per head);
+// a causal unit's cost grows with its query tile, so odd groups of dg tiles are taken in
+// reverse order, giving every residue class the same mean cost.
+struct FwdUnit {
+  int l, hq, hk, row0, n_ctx, ntiles;
+};
+
+__device__ __forceinline__ FwdUnit fwd_unit(const FwdArgs& a, int u, int nqt, int dg, int G,
+                                            int off) {
+  FwdUnit f;
+  const int r = u % nqt, k = r / dg, sr = r - k * dg;
+  f.row0 = (k * dg + ((k & 1) ? dg - 1 - sr : sr)) * BM;
+  f.hq = (u / nqt) % a.Hq;
+  f.l = u / (nqt * a.Hq);
+  f.hk = f.hq / G;
+  // key tiles the unit sees: context tiles, then tail tiles
+  const int kv_end = off + min(f.row0 + BM, a.n_q);  // keys [0, kv_end) are visible to some query
+  f.n_ctx = (min(a.T, kv_end) + BN - 1) / BN;
+  f.ntiles = f.n_ctx + (min(a.n_tail, max(0, kv_end - a.T)) + BN - 1) / BN;
+  return f;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -134,16 +162,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* abort_flag = misc + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int l = blockIdx.z, hq = blockIdx.y;
   const int G = a.Hq / a.Hkv;
-  const int hk = hq / G;
   const int n_k = a.T + a.n_tail;
   const int off = a.causal ? n_k - a.n_q : n_k;  // non-causal: every key is visible
-  const int row0 = blockIdx.x * BM;
-  // key tiles this query tile sees: context tiles, then tail tiles
-  const int kv_end = off + min(row0 + BM, a.n_q);  // keys [0, kv_end) are visible to some query
-  const int n_ctx = (min(a.T, kv_end) + BN - 1) / BN;
-  const int ntiles = n_ctx + (min(a.n_tail, max(0, kv_end - a.T)) + BN - 1) / BN;
+  // Persistent grid: this CTA takes units blockIdx.x, blockIdx.x + gridDim.x, ... of all
+  // (layer, query head, 128-query tile), query tile fastest.  TMEM, the barriers and the
+  // K/V rings carry over from unit to unit (their phases follow global tile counters).
+  const int nqt = (a.n_q + BM - 1) / BM;
+  const int total = nqt * a.Hq * a.L;
+  const int nunits = (int)blockIdx.x < total ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+  int dg = (int)gridDim.x;  // gcd(grid, nqt)
+  for (int x = nqt; x > 0;) {
+    const int t = dg % x;
+    dg = x;
+    x = t;
+  }
+  auto unit = [&](int n) {
+    return fwd_unit(a, (int)blockIdx.x + n * (int)gridDim.x, nqt, dg, G, off);
+  };
 
   if (threadIdx.x == 0) {
     tc::mbar_init(bar_q, kSoftThreads);
@@ -179,39 +215,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ============================================================ TMA producer
     if (lane == 0) {
-      // loads in the order the MMAs use them: K(0), K(1), V(0), K(2), V(1), ...
-      const int head = l * a.Hkv + hk;
-      auto load = [&](bool is_v, int j) -> bool {
-        const int s = j & 1;
-        const uint32_t empty = is_v ? bar_vempty(s) : bar_kempty(s);
-        if (!tc::mbar_wait(empty, ((j >> 1) & 1) ^ 1u) || *abort_flag) return false;
-        const bool ctx = j < n_ctx;
-        const CUtensorMap* m = is_v ? (ctx ? &tm_v : &tm_vt) : (ctx ? &tm_k : &tm_kt);
-        const int row = ctx ? j * BN : (j - n_ctx) * BN;
-        const uint32_t full = is_v ? bar_vfull(s) : bar_kfull(s);
-        const uint32_t dst = (is_v ? sV : sK) + s * C::TILE;
-        tc::mbar_expect_tx(full, C::TILE);
-#pragma unroll
-        for (int kh = 0; kh < C::KH; ++kh) tc::tma_load_3d(dst + kh * kBox, m, full, kh * 64, row, head);
-        return true;
-      };
-      int nk = 0, nv = 0;  // loads issued
+      // per unit, loads in the order the MMAs use them: K(0), K(1), V(0), K(2), V(1), ...;
+      // the next unit's first tiles load while this unit's last ones are consumed
+      int gk = 0, gv = 0;  // K and V tiles issued (all units)
       bool ok = true;
-      for (int t = 0; ok && t <= ntiles; ++t) {
-        if (t < ntiles) {
-          ok = load(false, t);
-          if (ok) ++nk;
-        }
-        if (ok && t >= 1) {
-          ok = load(true, t - 1);
-          if (ok) ++nv;
+      for (int n = 0; n < nunits && ok; ++n) {
+        const FwdUnit U = unit(n);
+        const int head = U.l * a.Hkv + U.hk;
+        auto load = [&](bool is_v, int j, int g) -> bool {  // tile j of the unit, g-th overall
+          const int s = g & 1;
+          const uint32_t empty = is_v ? bar_vempty(s) : bar_kempty(s);
+          if (!tc::mbar_wait(empty, ((g >> 1) & 1) ^ 1u) || *abort_flag) return false;
+          const bool ctx = j < U.n_ctx;
+          const CUtensorMap* m = is_v ? (ctx ? &tm_v : &tm_vt) : (ctx ? &tm_k : &tm_kt);
+          const int row = ctx ? j * BN : (j - U.n_ctx) * BN;
+          const uint32_t full = is_v ? bar_vfull(s) : bar_kfull(s);
+          const uint32_t dst = (is_v ? sV : sK) + s * C::TILE;
+          tc::mbar_expect_tx(full, C::TILE);
+#pragma unroll
+          for (int kh = 0; kh < C::KH; ++kh) tc::tma_load_3d(dst + kh * kBox, m, full, kh * 64, row, head);
+          return true;
+        };
+        for (int t = 0; ok && t <= U.ntiles; ++t) {
+          if (t < U.ntiles) {
+            ok = load(false, t, gk);
+            if (ok) ++gk;
+          }
+          if (ok && t >= 1) {
+            ok = load(true, t - 1, gv);
+            if (ok) ++gv;
+          }
         }
       }
       if (!ok) {
         fail(abort_flag, kErrWaitTimeout);
         // let the copies already in flight land before the CTA exits
-        for (int i = max(0, nk - 2); i < nk; ++i) tc::mbar_wait(bar_kfull(i & 1), (i >> 1) & 1);
-        for (int i = max(0, nv - 2); i < nv; ++i) tc::mbar_wait(bar_vfull(i & 1), (i >> 1) & 1);
+        for (int i = max(0, gk - 2); i < gk; ++i) tc::mbar_wait(bar_kfull(i & 1), (i >> 1) & 1);
+        for (int i = max(0, gv - 2); i < gv; ++i) tc::mbar_wait(bar_vfull(i & 1), (i >> 1) & 1);
       }
     }
   } else if (warp == 1) {
@@ -219,46 +259,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16(BM, BN);
       constexpr uint32_t idesc_o = tc::idesc_bf16_bmn(BM, D);
-      bool ok = tc::mbar_wait(bar_q, 0) && !*abort_flag;
-      tc::fence_after_sync();
-      int issued = 0;  // MMA groups issued (for the final drain)
-      for (int j = 0; ok && j <= ntiles; ++j) {
-        if (j < ntiles) {  // S(j) = Q K(j)^T into S buffer j & 1 (Q from TMEM)
-          const int s = j & 1;
-          const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-          if (!tc::mbar_wait(bar_kfull(s), ph) || !tc::mbar_wait(bar_sempty(s), ph ^ 1u) ||
-              *abort_flag) {
-            ok = false;
-            break;
-          }
-          tc::fence_after_sync();
-          const uint32_t d_s = tmem + (uint32_t)(s * BN);
-          const uint32_t k_s = sK + s * C::TILE;
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t o = (uint32_t)(k >> 2) * kBox + (uint32_t)(k & 3) * 32u;
-            tc::mma_bf16_ts(d_s, t_q + 8u * k, tc::sdesc_sw128(k_s + o), idesc_s, k > 0 ? 1u : 0u);
-          }
-          tc::commit(bar_sfull(s));
-          tc::commit(bar_kempty(s));
-          ++issued;
+      int gs = 0, gp = 0;  // S and P V products issued (all units)
+      int issued = 0;      // MMA groups issued (for the final drain)
+      bool ok = true;
+      for (int n = 0; n < nunits && ok; ++n) {
+        const int ntiles = unit(n).ntiles;
+        // the unit's query rows are in TMEM, and the softmax threads have read the
+        // previous unit's O (they arrive after both), so P V(0) may overwrite it
+        if (!tc::mbar_wait(bar_q, (uint32_t)n & 1u) || *abort_flag) {
+          ok = false;
+          break;
         }
-        if (j >= 1) {  // O += P(j-1) V(j-1)
-          const int jj = j - 1, s = jj & 1;
-          if (!tc::mbar_wait(bar_p(jj), (uint32_t)(jj >> 1) & 1u) ||
-              !tc::mbar_wait(bar_vfull(s), (uint32_t)(jj >> 1) & 1u) || *abort_flag) {
-            ok = false;
-            break;
-          }
-          tc::fence_after_sync();
-          const uint32_t v_s = sV + s * C::TILE;
+        tc::fence_after_sync();
+        for (int j = 0; ok && j <= ntiles; ++j) {
+          if (j < ntiles) {  // S = Q K^T into S buffer gs & 1 (Q from TMEM)
+            const int s = gs & 1;
+            const uint32_t ph = (uint32_t)(gs >> 1) & 1u;
+            if (!tc::mbar_wait(bar_kfull(s), ph) || !tc::mbar_wait(bar_sempty(s), ph ^ 1u) ||
+                *abort_flag) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+            const uint32_t d_s = tmem + (uint32_t)(s * BN);
+            const uint32_t k_s = sK + s * C::TILE;
 #pragma unroll
-          for (int k = 0; k < BN / 16; ++k)
-            tc::mma_bf16_ts(t_o, t_p + 8u * k, tc::sdesc_sw128_mn(v_s + 2048u * k, kBox), idesc_o,
-                            (jj > 0 || k > 0) ? 1u : 0u);
-          tc::commit(bar_vempty(s));
-          tc::commit(bar_o(jj));
-          ++issued;
+            for (int k = 0; k < D / 16; ++k) {
+              const uint32_t o = (uint32_t)(k >> 2) * kBox + (uint32_t)(k & 3) * 32u;
+              tc::mma_bf16_ts(d_s, t_q + 8u * k, tc::sdesc_sw128(k_s + o), idesc_s, k > 0 ? 1u : 0u);
+            }
+            tc::commit(bar_sfull(s));
+            tc::commit(bar_kempty(s));
+            ++gs;
+            ++issued;
+          }
+          if (j >= 1) {  // O += P V of the unit's tile j - 1
+            const int s = gp & 1;
+            if (!tc::mbar_wait(bar_p(gp), (uint32_t)(gp >> 1) & 1u) ||
+                !tc::mbar_wait(bar_vfull(s), (uint32_t)(gp >> 1) & 1u) || *abort_flag) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+            const uint32_t v_s = sV + s * C::TILE;
+#pragma unroll
+            for (int k = 0; k < BN / 16; ++k)
+              tc::mma_bf16_ts(t_o, t_p + 8u * k, tc::sdesc_sw128_mn(v_s + 2048u * k, kBox), idesc_o,
+                              (j > 1 || k > 0) ? 1u : 0u);
+            tc::commit(bar_vempty(s));
+            tc::commit(bar_o(gp));
+            ++gp;
+            ++issued;
+          }
         }
       }
       if (!ok) fail(abort_flag, kErrWaitTimeout);
@@ -272,18 +324,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ============================================================ softmax + epilogue
     constexpr int OC = D / NQ;          // O columns of this thread in the rescale / epilogue
+    constexpr int QW = D / (2 * NQ);    // 32-bit words (bf16 pairs) of the query row per thread
     const int h = (warp - 2) >> 2;      // key part of each tile (and D / NQ of O)
     const int eq = warp & 3;            // TMEM lane quarter
     const int row = eq * 32 + lane;     // query row within the tile
-    const int qr = row0 + row;          // query index
     const uint32_t lane_off = (uint32_t)(eq * 32) << 16;
     const float sc2 = rsqrtf((float)D) * kLog2e;
-    {  // this thread's part of its query row into TMEM (zeros past the last query)
-      constexpr int QW = D / (2 * NQ);  // 32-bit words (bf16 pairs) per thread
-      uint32_t qv[QW];
+    // this thread's part of a unit's query row (zeros past the last query)
+    uint32_t qv[QW];
+    auto load_q = [&](const FwdUnit& U) {
+      const int qr = U.row0 + row;
       if (qr < a.n_q) {
         const uint4* src = reinterpret_cast<const uint4*>(
-            a.q + ((size_t)(l * a.Hq + hq) * a.n_q + qr) * D + h * (D / NQ));
+            a.q + ((size_t)(U.l * a.Hq + U.hq) * a.n_q + qr) * D + h * (D / NQ));
 #pragma unroll
         for (int c = 0; c < QW / 4; ++c) {
           const uint4 x = __ldg(src + c);
@@ -296,6 +349,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < QW; ++c) qv[c] = 0u;
       }
+    };
+    if (nunits > 0) load_q(unit(0));
+    int gs = 0;  // tiles processed (all units): S buffer, exchange buffer, P and O barriers
+    bool failed = false, wait_failed = false;
+    for (int n = 0; n < nunits && !failed; ++n) {
+      const FwdUnit U = unit(n);
+      const int qr = U.row0 + row;  // query index
+      // the unit's query rows into TMEM: the previous unit's S products are complete (its
+      // last P V was waited for below) and its O is in registers
       if constexpr (QW == 32)
         tc::tmem_st32(t_q + lane_off + (uint32_t)(h * QW), qv);
       else if constexpr (QW == 16)
@@ -305,156 +367,158 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tmem_st_wait();
       tc::fence_before_sync();
       tc::mbar_arrive(bar_q);
-    }
-    float m_used = -1e30f, lsum = 0.f;
-    bool failed = false, wait_failed = false;
-    for (int j = 0; j < ntiles; ++j) {
-      const int s = j & 1;  // max-exchange buffer and S buffer
-      bool ok = tc::mbar_wait(bar_sfull(s), (uint32_t)(j >> 1) & 1u) && !*abort_flag;
-      if (tc::bar_or(2, kSoftThreads, !ok || wait_failed)) {
-        failed = true;
-        break;
-      }
-      tc::fence_after_sync();
-      uint32_t v[KC];
-#pragma unroll
-      for (int c = 0; c < KC; c += 32)
-        tc::tmem_ld32(tmem + lane_off + (uint32_t)(s * BN + h * KC + c), v + c);
-      tc::tmem_ld_wait();
-      tc::fence_before_sync();
-      tc::mbar_arrive(bar_sempty(s));  // S(j + 2) may overwrite the buffer now
-
-      const bool ctx = j < n_ctx;
-      const int kb = (ctx ? j * BN : a.T + (j - n_ctx) * BN) + h * KC;
-      const int lim = ctx ? a.T : n_k;
-      if (kb + KC > lim || kb + KC - 1 > off + qr) {
-#pragma unroll
-        for (int c = 0; c < KC; ++c)
-          if (kb + c >= lim || kb + c > off + qr) v[c] = __float_as_uint(-CUDART_INF_F);
-      }
-      float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
-#pragma unroll
-      for (int c = 0; c < KC; c += 8) {
-        mx0 = tc::max3(mx0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
-        mx1 = tc::max3(mx1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
-        mx2 = tc::max3(mx2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
-        mx3 = tc::max3(mx3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
-      }
-      const float mine = tc::max3(mx0, mx1, fmaxf(mx2, mx3)) * sc2;
-      float* xmj = xm + s * NQ * BM;
-      xmj[h * BM + row] = mine;
-      // the NQ threads of a row are the warps eq + 2 + 4g: one named barrier per lane
-      // quarter (ids 3..6) pairs them without holding up the other quarters
-      named_sync(3 + eq, 32 * NQ);
-      float mt = mine;
-#pragma unroll
-      for (int g = 1; g < NQ; ++g) mt = fmaxf(mt, xmj[((h + g) % NQ) * BM + row]);
-      const bool need = mt > m_used + kRescale;
-      float factor = 1.f;
-      if (need) {
-        factor = fast_exp2(m_used - mt);
-        m_used = mt;
-        lsum *= factor;
-      }
-      // p = 2^(x sc2 - m) with packed fp32 pairs (FFMA2 / FADD2): half the FMA-pipe
-      // instructions of scalar code, one MUFU ex2 per key
-      uint32_t pk[KC / 2];
-      const float2 k2 = make_float2(sc2, sc2), nm = make_float2(-m_used, -m_used);
-      float2 a0 = make_float2(0.f, 0.f), a1 = a0;
-#pragma unroll
-      for (int c = 0; c < KC; c += 4) {
-        const float2 y0 = __ffma2_rn(tc::f2(v[c], v[c + 1]), k2, nm);
-        const float2 y1 = __ffma2_rn(tc::f2(v[c + 2], v[c + 3]), k2, nm);
-        const float p0 = fast_exp2(y0.x), p1 = fast_exp2(y0.y);
-        const float p2 = fast_exp2(y1.x), p3 = fast_exp2(y1.y);
-        a0 = __fadd2_rn(a0, make_float2(p0, p1));
-        a1 = __fadd2_rn(a1, make_float2(p2, p3));
-        pk[c / 2] = pack_bf16(p0, p1);
-        pk[c / 2 + 1] = pack_bf16(p2, p3);
-      }
-      a0 = __fadd2_rn(a0, a1);
-      lsum += a0.x + a0.y;
-
-      // P V(j - 1) has read P(j - 1) (and finished O) before P(j) is written; O is
-      // rescaled only when this row's max grew past the threshold
-      const bool any_need = __any_sync(0xffffffffu, need);
-      if (j > 0) {
-        ok = tc::mbar_wait(bar_o(j - 1), (uint32_t)((j - 1) >> 1) & 1u) && !*abort_flag;
-        ok = __all_sync(0xffffffffu, ok);  // the TMEM accesses below are warp-wide
-        if (!ok) wait_failed = true;       // reported at the next vote
+      float m_used = -1e30f, lsum = 0.f;
+      for (int j = 0; j < U.ntiles; ++j, ++gs) {
+        const int s = gs & 1;  // max-exchange buffer and S buffer
+        bool ok = tc::mbar_wait(bar_sfull(s), (uint32_t)(gs >> 1) & 1u) && !*abort_flag;
+        if (tc::bar_or(2, kSoftThreads, !ok || wait_failed)) {
+          failed = true;
+          break;
+        }
         tc::fence_after_sync();
-        if (ok && any_need) {
-          const uint32_t to = t_o + lane_off + (uint32_t)(h * OC);
-          if constexpr (OC >= 32) {
+        uint32_t v[KC];
 #pragma unroll
-            for (int cb = 0; cb < OC; cb += 32) {
-              tc::tmem_ld32(to + cb, v);
+        for (int c = 0; c < KC; c += 32)
+          tc::tmem_ld32(tmem + lane_off + (uint32_t)(s * BN + h * KC + c), v + c);
+        tc::tmem_ld_wait();
+        tc::fence_before_sync();
+        tc::mbar_arrive(bar_sempty(s));  // the next S into this buffer may start now
+
+        const bool ctx = j < U.n_ctx;
+        const int kb = (ctx ? j * BN : a.T + (j - U.n_ctx) * BN) + h * KC;
+        const int lim = ctx ? a.T : n_k;
+        if (kb + KC > lim || kb + KC - 1 > off + qr) {
+#pragma unroll
+          for (int c = 0; c < KC; ++c)
+            if (kb + c >= lim || kb + c > off + qr) v[c] = __float_as_uint(-CUDART_INF_F);
+        }
+        float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
+#pragma unroll
+        for (int c = 0; c < KC; c += 8) {
+          mx0 = tc::max3(mx0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+          mx1 = tc::max3(mx1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+          mx2 = tc::max3(mx2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+          mx3 = tc::max3(mx3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
+        }
+        const float mine = tc::max3(mx0, mx1, fmaxf(mx2, mx3)) * sc2;
+        float* xmj = xm + s * NQ * BM;
+        xmj[h * BM + row] = mine;
+        // the NQ threads of a row are the warps eq + 2 + 4g: one named barrier per lane
+        // quarter (ids 3..6) pairs them without holding up the other quarters
+        named_sync(3 + eq, 32 * NQ);
+        float mt = mine;
+#pragma unroll
+        for (int g = 1; g < NQ; ++g) mt = fmaxf(mt, xmj[((h + g) % NQ) * BM + row]);
+        const bool need = mt > m_used + kRescale;
+        float factor = 1.f;
+        if (need) {
+          factor = fast_exp2(m_used - mt);
+          m_used = mt;
+          lsum *= factor;
+        }
+        // p = 2^(x sc2 - m) with packed fp32 pairs (FFMA2 / FADD2): half the FMA-pipe
+        // instructions of scalar code, one MUFU ex2 per key
+        uint32_t pk[KC / 2];
+        const float2 k2 = make_float2(sc2, sc2), nm = make_float2(-m_used, -m_used);
+        float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+#pragma unroll
+        for (int c = 0; c < KC; c += 4) {
+          const float2 y0 = __ffma2_rn(tc::f2(v[c], v[c + 1]), k2, nm);
+          const float2 y1 = __ffma2_rn(tc::f2(v[c + 2], v[c + 3]), k2, nm);
+          const float p0 = fast_exp2(y0.x), p1 = fast_exp2(y0.y);
+          const float p2 = fast_exp2(y1.x), p3 = fast_exp2(y1.y);
+          a0 = __fadd2_rn(a0, make_float2(p0, p1));
+          a1 = __fadd2_rn(a1, make_float2(p2, p3));
+          pk[c / 2] = pack_bf16(p0, p1);
+          pk[c / 2 + 1] = pack_bf16(p2, p3);
+        }
+        a0 = __fadd2_rn(a0, a1);
+        lsum += a0.x + a0.y;
+
+        // P V of the previous tile has read its P (and finished O) before P is written;
+        // O is rescaled only when this row's max grew past the threshold.  The unit's
+        // first tile needs no wait: the previous unit's last P V was waited for below.
+        const bool any_need = __any_sync(0xffffffffu, need);
+        if (j > 0) {
+          ok = tc::mbar_wait(bar_o(gs - 1), (uint32_t)((gs - 1) >> 1) & 1u) && !*abort_flag;
+          ok = __all_sync(0xffffffffu, ok);  // the TMEM accesses below are warp-wide
+          if (!ok) wait_failed = true;       // reported at the next vote
+          tc::fence_after_sync();
+          if (ok && any_need) {
+            const uint32_t to = t_o + lane_off + (uint32_t)(h * OC);
+            if constexpr (OC >= 32) {
+#pragma unroll
+              for (int cb = 0; cb < OC; cb += 32) {
+                tc::tmem_ld32(to + cb, v);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * factor);
+                tc::tmem_st32(to + cb, v);
+              }
+            } else {
+              tc::tmem_ld16(to, v);
               tc::tmem_ld_wait();
 #pragma unroll
-              for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * factor);
-              tc::tmem_st32(to + cb, v);
+              for (int c = 0; c < 16; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * factor);
+              tc::tmem_st16(to, v);
             }
-          } else {
-            tc::tmem_ld16(to, v);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 16; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * factor);
-            tc::tmem_st16(to, v);
+            tc::tmem_st_wait();
           }
-          tc::tmem_st_wait();
         }
+        if (wait_failed) continue;  // the P columns may still be in use: leave them alone
+        // P of this thread's keys h*KC .. h*KC+KC-1 as bf16 pairs into P columns h*KC/2 ..
+        if constexpr (KC == 64)
+          tc::tmem_st32(t_p + lane_off + (uint32_t)(h * (KC / 2)), pk);
+        else
+          tc::tmem_st16(t_p + lane_off + (uint32_t)(h * (KC / 2)), pk);
+        tc::tmem_st_wait();
+        tc::fence_before_sync();
+        tc::mbar_arrive(bar_p(gs));
       }
-      if (wait_failed) continue;  // the P columns may still be in use: leave them alone
-      // P of this thread's keys h*KC .. h*KC+KC-1 as bf16 pairs into P columns h*KC/2 ..
-      if constexpr (KC == 64)
-        tc::tmem_st32(t_p + lane_off + (uint32_t)(h * (KC / 2)), pk);
-      else
-        tc::tmem_st16(t_p + lane_off + (uint32_t)(h * (KC / 2)), pk);
-      tc::tmem_st_wait();
-      tc::fence_before_sync();
-      tc::mbar_arrive(bar_p(j));
-    }
-    if (!failed && ntiles > 0) {
-      // the last two P V products (on o[0] and o[1]) complete O
-      bool ok = ntiles < 2 || tc::mbar_wait(bar_o(ntiles - 2), (uint32_t)((ntiles - 2) >> 1) & 1u);
-      ok = ok && tc::mbar_wait(bar_o(ntiles - 1), (uint32_t)((ntiles - 1) >> 1) & 1u) &&
-           !*abort_flag;
+      if (failed) break;
+      // the next unit's query rows load while this unit's O is finished and written
+      if (n + 1 < nunits) load_q(unit(n + 1));
+      // the last two P V products of the unit (on o[0] and o[1]) complete O
+      bool ok = U.ntiles < 2 || tc::mbar_wait(bar_o(gs - 2), (uint32_t)((gs - 2) >> 1) & 1u);
+      ok = ok && tc::mbar_wait(bar_o(gs - 1), (uint32_t)((gs - 1) >> 1) & 1u) && !*abort_flag;
       failed = tc::bar_or(2, kSoftThreads, !ok || wait_failed);
-      if (!failed) {
-        tc::fence_after_sync();
-        xl[h * BM + row] = lsum;
-        named_sync(1, kSoftThreads);
-        float ltot = lsum;
+      if (failed) break;
+      tc::fence_after_sync();
+      xl[h * BM + row] = lsum;
+      named_sync(1, kSoftThreads);
+      float ltot = lsum;
 #pragma unroll
-        for (int g = 1; g < NQ; ++g) ltot += xl[((h + g) % NQ) * BM + row];
-        const float inv = 1.f / ltot;
-        uint32_t v[OC];
-        uint32_t ob[OC / 2];
-        if constexpr (OC >= 32) {
+      for (int g = 1; g < NQ; ++g) ltot += xl[((h + g) % NQ) * BM + row];
+      const float inv = 1.f / ltot;
+      uint32_t v[OC];
+      uint32_t ob[OC / 2];
+      if constexpr (OC >= 32) {
 #pragma unroll
-          for (int cb = 0; cb < OC; cb += 32) tc::tmem_ld32(t_o + lane_off + (uint32_t)(h * OC + cb), v + cb);
-        } else {
-          tc::tmem_ld16(t_o + lane_off + (uint32_t)(h * OC), v);
-        }
-        tc::tmem_ld_wait();
-        if (a.o_f16) {
-#pragma unroll
-          for (int c = 0; c < OC; c += 2)
-            ob[c / 2] = pack_f16(__uint_as_float(v[c]) * inv, __uint_as_float(v[c + 1]) * inv);
-        } else {
-#pragma unroll
-          for (int c = 0; c < OC; c += 2)
-            ob[c / 2] = pack_bf16(__uint_as_float(v[c]) * inv, __uint_as_float(v[c + 1]) * inv);
-        }
-        if (qr < a.n_q) {
-          uint4* dst = reinterpret_cast<uint4*>(
-              a.o + ((size_t)(l * a.Hq + hq) * a.n_q + qr) * D + h * OC);
-#pragma unroll
-          for (int c = 0; c < OC / 8; ++c)
-            dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
-          if (h == 0) a.lse[(size_t)(l * a.Hq + hq) * a.n_q + qr] = (m_used + fast_log2(ltot)) * kLn2;
-        }
+        for (int cb = 0; cb < OC; cb += 32) tc::tmem_ld32(t_o + lane_off + (uint32_t)(h * OC + cb), v + cb);
+      } else {
+        tc::tmem_ld16(t_o + lane_off + (uint32_t)(h * OC), v);
       }
+      tc::tmem_ld_wait();
+      if (a.o_f16) {
+#pragma unroll
+        for (int c = 0; c < OC; c += 2)
+          ob[c / 2] = pack_f16(__uint_as_float(v[c]) * inv, __uint_as_float(v[c + 1]) * inv);
+      } else {
+#pragma unroll
+        for (int c = 0; c < OC; c += 2)
+          ob[c / 2] = pack_bf16(__uint_as_float(v[c]) * inv, __uint_as_float(v[c + 1]) * inv);
+      }
+      if (qr < a.n_q) {
+        uint4* dst = reinterpret_cast<uint4*>(
+            a.o + ((size_t)(U.l * a.Hq + U.hq) * a.n_q + qr) * D + h * OC);
+#pragma unroll
+        for (int c = 0; c < OC / 8; ++c)
+          dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+        if (h == 0)
+          a.lse[(size_t)(U.l * a.Hq + U.hq) * a.n_q + qr] = (m_used + fast_log2(ltot)) * kLn2;
+      }
+      // xl is rewritten at the next unit's end only after the rows' pair barriers of its
+      // tiles, which every partner reaches after reading xl here
     }
     if (failed) atomicCAS(&g_fwd_error, 0, (int)kErrWaitTimeout);
   }
@@ -482,7 +546,17 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
     e = a.n_tail > 0 ? tma_map_bf16_3d(&tvt, a.v_tail, D, a.n_tail, a.L * a.Hkv, BN)
                      : tma_map_bf16_3d(&tvt, a.q, D, 1, 1, BN);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.n_q + BM - 1) / BM, a.Hq, a.L);
+  static int nsm[64] = {0};
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!nsm[dev]) {
+    e = cudaDeviceGetAttribute(&nsm[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  const long long units = (long long)((a.n_q + BM - 1) / BM) * a.Hq * a.L;
+  dim3 grid((unsigned)std::min<long long>(units, std::max(1, nsm[dev])));  // one CTA per SM
   auto kern = attn_fwd_kernel<D>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
