@@ -61,6 +61,10 @@ FWD_SHAPES = [
     (1, 1, 4, 128, 0, 97, 97),       # no context keys
     (3, 1, 2, 128, 333, 5, 1),       # one query
     (1, 2, 4, 128, 700, 20, 400),    # several key tiles per query tile, two query tiles
+    # more 128-query units than SMs: the persistent grid's CTAs carry TMEM, rings and
+    # barrier phases from one unit to the next (causal units of different lengths)
+    (2, 4, 32, 64, 300, 40, 300),
+    (1, 8, 64, 128, 260, 200, 450),
 ]
 
 
